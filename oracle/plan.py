@@ -1,0 +1,257 @@
+"""Oracle planner: block summaries, tile classes, PTRR order, per-step lists, needed index.
+
+Sources (MARBLE post):
+  * section 03 "Block classification": per 128-token block, the min and max of every
+    metadata track plus a small bitmap of the segments the block holds; a block pair is
+    *full* if every pair is provably legal, *empty* if every pair is provably illegal,
+    *partial* otherwise.  One test per block pair.
+  * section 03 "PTRR": sort query blocks by cost, deal them to ranks in rounds of R with
+    every other round reversed, keep each rank's blocks in sequence order.
+  * section 03 "Chunked ring attention": PTRR's rule applied to contiguous chunks.
+  * section 03 "Block classification" (ring steps): at step s, rank r pairs its queries
+    with the key/value shard of rank (r - s) mod R.
+  * section 04 "Sparse all-to-all": each rank needs exactly the key/value blocks its
+    queries can see (local blocks included; one pass over local + fetched keys).
+  * section 04 "Layout transforms": tokens are permuted once, carrying their metadata
+    and original position.
+
+The exact summary test is not printed on the page; the reading used here (and by the
+CUDA planner, written separately) is:
+
+  per block X: Slo/Shi (sample), Plo/Phi (pos), Nlo/Nhi (noise), over tokens with seg >= 0
+  Glo/Ghi, hasseg (any seg >= 0), allseg (all seg >= 0), Gbits = OR of 1 << (seg mod 64).
+
+  For q block A and k block B:
+    samp_all   = Slo_A == Shi_A == Slo_B == Shi_B
+    samp_none  = Shi_A < Slo_B  or  Shi_B < Slo_A
+    caus_all   = Plo_A - Phi_B >= 0  and  Phi_A - Plo_B < W
+    caus_none  = Phi_A - Plo_B < 0   or   Plo_A - Phi_B >= W
+    span_all   = allseg_A and allseg_B and Glo_A == Ghi_A == Glo_B == Ghi_B
+    span_none  = not hasseg_A or not hasseg_B or (Gbits_A & Gbits_B) == 0
+                 or Ghi_A < Glo_B or Ghi_B < Glo_A
+    noise_all  = Nhi_B < 0  or  Nlo_A == Nhi_A == Nlo_B == Nhi_B >= 0
+    noise_none = Nlo_B >= 0 and (Nhi_A < Nlo_B or Nhi_B < Nlo_A)
+
+    empty = samp_none or noise_none or (caus_none and span_none)
+    full  = samp_all and noise_all and (caus_all or span_all)      (when not empty)
+    partial otherwise.
+
+The oracle evaluates the rule on all nb x nb block pairs (no candidate band).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, List
+
+import numpy as np
+
+from .mask import tracks_with_pos
+
+BLOCK = 128
+EMPTY, FULL, PARTIAL = 0, 1, 2
+NO_SEG_LO = 2**31 - 1
+NO_SEG_HI = -1
+
+
+def block_summaries(tr) -> Dict[str, np.ndarray]:
+    sample, seg, noise, pos = tracks_with_pos(tr)
+    n = len(sample)
+    if n % BLOCK:
+        raise ValueError("n must be a multiple of 128")
+    nb = n // BLOCK
+    S = sample.reshape(nb, BLOCK)
+    P = pos.reshape(nb, BLOCK)
+    N = noise.reshape(nb, BLOCK)
+    G = seg.reshape(nb, BLOCK)
+    has = G >= 0
+    glo = np.where(has, G, NO_SEG_LO).min(1)
+    ghi = np.where(has, G, NO_SEG_HI).max(1)
+    bits = np.zeros(nb, np.uint64)
+    for b in range(nb):
+        for g in np.unique(G[b][has[b]]):
+            bits[b] |= np.uint64(1) << np.uint64(int(g) & 63)
+    return {
+        "slo": S.min(1), "shi": S.max(1),
+        "plo": P.min(1), "phi": P.max(1),
+        "nlo": N.min(1), "nhi": N.max(1),
+        "glo": glo, "ghi": ghi,
+        "hasseg": has.any(1), "allseg": has.all(1),
+        "gbits": bits,
+    }
+
+
+def classify(summ, W, rows=None) -> np.ndarray:
+    """Tile class matrix [len(rows), nb] (0 empty, 1 full, 2 partial) by the rule above."""
+    nb = len(summ["slo"])
+    rows = np.arange(nb) if rows is None else np.asarray(rows)
+    A = {k: v[rows][:, None] for k, v in summ.items()}
+    B = {k: v[None, :] for k, v in summ.items()}
+    W = np.int64(W)
+
+    samp_all = (A["slo"] == A["shi"]) & (A["shi"] == B["slo"]) & (B["slo"] == B["shi"])
+    samp_none = (A["shi"] < B["slo"]) | (B["shi"] < A["slo"])
+    caus_all = (A["plo"] - B["phi"] >= 0) & (A["phi"] - B["plo"] < W)
+    caus_none = (A["phi"] - B["plo"] < 0) | (A["plo"] - B["phi"] >= W)
+    span_all = (A["allseg"] & B["allseg"] & (A["glo"] == A["ghi"]) & (A["ghi"] == B["glo"])
+                & (B["glo"] == B["ghi"]))
+    span_none = ((~A["hasseg"]) | (~B["hasseg"]) | ((A["gbits"] & B["gbits"]) == 0)
+                 | (A["ghi"] < B["glo"]) | (B["ghi"] < A["glo"]))
+    noise_all = (B["nhi"] < 0) | ((A["nlo"] == A["nhi"]) & (A["nhi"] == B["nlo"])
+                                  & (B["nlo"] == B["nhi"]) & (B["nhi"] >= 0))
+    noise_none = (B["nlo"] >= 0) & ((A["nhi"] < B["nlo"]) | (B["nhi"] < A["nlo"]))
+
+    empty = samp_none | noise_none | (caus_none & span_none)
+    full = samp_all & noise_all & (caus_all | span_all) & ~empty
+    out = np.full(empty.shape, PARTIAL, np.int8)
+    out[empty] = EMPTY
+    out[full] = FULL
+    return out
+
+
+def tile_csr(summ, W, row_chunk: int = 512):
+    """Global tile map in original block coordinates as CSR (row_ptr int64, col int32,
+    tag uint8 with 1 = full, 2 = partial; empty tiles are not stored)."""
+    nb = len(summ["slo"])
+    ptr = np.zeros(nb + 1, np.int64)
+    cols: List[np.ndarray] = []
+    tags: List[np.ndarray] = []
+    for a in range(0, nb, row_chunk):
+        rows = np.arange(a, min(nb, a + row_chunk))
+        c = classify(summ, W, rows)
+        for i, r in enumerate(rows):
+            nz = np.flatnonzero(c[i])
+            cols.append(nz.astype(np.int32))
+            tags.append(c[i][nz].astype(np.uint8))
+            ptr[r + 1] = len(nz)
+    ptr = np.cumsum(ptr)
+    col = np.concatenate(cols) if cols else np.zeros(0, np.int32)
+    tag = np.concatenate(tags) if tags else np.zeros(0, np.uint8)
+    return ptr, col, tag
+
+
+# --------------------------------------------------------------------------------------
+# token order
+# --------------------------------------------------------------------------------------
+def ptrr_assign(cost, P):
+    """PTRR over units with the given costs.
+
+    Sort by (cost descending, unit index ascending); the t-th round of P units goes to
+    ranks 0..P-1 when t is even and P-1..0 when t is odd; each rank then keeps its units
+    in ascending index order.  Returns the list of units of each rank."""
+    cost = np.asarray(cost)
+    U = len(cost)
+    if U % P:
+        raise ValueError("number of units must be divisible by P")
+    order = sorted(range(U), key=lambda u: (-int(cost[u]), u))
+    rank = np.empty(U, np.int64)
+    for p, u in enumerate(order):
+        t, i = divmod(p, P)
+        rank[u] = i if t % 2 == 0 else P - 1 - i
+    return [[u for u in range(U) if rank[u] == r] for r in range(P)]
+
+
+@dataclasses.dataclass
+class Plan:
+    nb: int
+    P: int
+    W: int
+    row_ptr: np.ndarray      # global tile CSR, original block coordinates
+    col: np.ndarray
+    tag: np.ndarray
+    cost: np.ndarray         # per original q block: number of non-empty tiles
+    block_perm: np.ndarray   # new block -> original block
+    inv_block_perm: np.ndarray
+    perm: np.ndarray         # new token -> original token
+    tracks_perm: Dict[str, np.ndarray]  # sample, seg, noise, pos in new order
+    step_ptr: np.ndarray     # [nb*P + 1]; entries of (new q block nq, kv shard j) at nq*P + j
+    step_col: np.ndarray     # new kv block
+    step_tag: np.ndarray
+    colT_ptr: np.ndarray     # [nb*P + 1]; entries of (new kv block nk, q shard r) at nk*P + r
+    colT_row: np.ndarray     # new q block
+    colT_tag: np.ndarray
+    needed_ptr: np.ndarray   # [P + 1]
+    needed: np.ndarray       # sorted unique new kv blocks per q shard
+
+
+def make_plan(tr, W, P, order="contiguous", chunk_tokens=0) -> Plan:
+    summ = block_summaries(tr)
+    nb = len(summ["slo"])
+    if nb % P:
+        raise ValueError("number of blocks must be divisible by P")
+    row_ptr, col, tag = tile_csr(summ, W)
+    cost = np.diff(row_ptr)
+
+    if order == "contiguous":
+        per = nb // P
+        units_of_rank = [list(range(r * per, (r + 1) * per)) for r in range(P)]
+        unit_blocks = 1
+    elif order == "ptrr_block":
+        units_of_rank = ptrr_assign(cost, P)
+        unit_blocks = 1
+    elif order == "ptrr_chunk":
+        if chunk_tokens <= 0 or chunk_tokens % BLOCK or (nb * BLOCK) % chunk_tokens:
+            raise ValueError("bad chunk size")
+        unit_blocks = chunk_tokens // BLOCK
+        ccost = cost.reshape(-1, unit_blocks).sum(1)
+        units_of_rank = ptrr_assign(ccost, P)
+    else:
+        raise ValueError(order)
+
+    block_perm = np.array([u * unit_blocks + i for r in range(P) for u in units_of_rank[r]
+                           for i in range(unit_blocks)], np.int64)
+    inv = np.empty(nb, np.int64)
+    inv[block_perm] = np.arange(nb)
+    tok = np.arange(nb * BLOCK)
+    perm = block_perm[tok // BLOCK] * BLOCK + tok % BLOCK
+    sample, seg, noise, pos = tracks_with_pos(tr)
+    tracks_perm = {"sample": sample[perm], "seg": seg[perm], "noise": noise[perm],
+                   "pos": pos[perm]}
+
+    bps = nb // P
+    # every non-empty tile as (new q block nq, new kv block nk, tag)
+    qb_of = np.repeat(np.arange(nb), np.diff(row_ptr))
+    nq = inv[qb_of]
+    nk = inv[col.astype(np.int64)]
+
+    def grouped(major, minor, shard_of_minor):
+        """Lists keyed by (major, shard of minor), each ascending in minor, as CSR over
+        major * P + shard."""
+        key = major * P + shard_of_minor
+        o = np.lexsort((minor, key))
+        ptr = np.zeros(nb * P + 1, np.int64)
+        ptr[1:] = np.cumsum(np.bincount(key, minlength=nb * P))
+        return ptr, minor[o].astype(np.int32), tag[o].astype(np.uint8)
+
+    # forward / dQ: per (q block, kv shard j) the kv blocks of step j
+    step_ptr, step_col, step_tag = grouped(nq, nk, nk // bps)
+    # dK / dV: per (kv block, q shard r) the q blocks
+    colT_ptr, colT_row, colT_tag = grouped(nk, nq, nq // bps)
+
+    # needed kv blocks of each q shard: sorted unique over all its rows' tiles
+    pairs = np.unique((nq // bps) * nb + nk)
+    needed = (pairs % nb).astype(np.int32)
+    needed_ptr = np.zeros(P + 1, np.int64)
+    needed_ptr[1:] = np.cumsum(np.bincount(pairs // nb, minlength=P))
+
+    return Plan(nb, P, W, row_ptr, col, tag, cost, block_perm, inv, perm, tracks_perm,
+                step_ptr, step_col, step_tag, colT_ptr, colT_row, colT_tag,
+                needed_ptr, needed)
+
+
+def shard_work(plan: Plan) -> np.ndarray:
+    """W[r, j] = non-empty tiles between q shard r and kv shard j (tile units)."""
+    P, nb = plan.P, plan.nb
+    Wm = np.zeros((P, P), np.int64)
+    bps = nb // P
+    for nq in range(nb):
+        for j in range(P):
+            Wm[nq // bps, j] += plan.step_ptr[nq * P + j + 1] - plan.step_ptr[nq * P + j]
+    return Wm
+
+
+def step_cost(plan: Plan) -> int:
+    """sum over steps s of max over ranks r of W[r, (r - s) mod P] (chunk-layout cost C
+    of the chunked-ring section without the per-range overhead term), in tiles."""
+    Wm = shard_work(plan)
+    P = plan.P
+    return int(sum(max(Wm[r, (r - s) % P] for r in range(P)) for s in range(P)))

@@ -1,0 +1,449 @@
+"""Pins for the CPU oracle: values the pages print, closed forms, invariants, brute force.
+
+None of these tests needs a GPU.  Each one is chosen so that a plausible mistake in the
+oracle (a dropped term, a wrong sign or index, a transposed operand) fails it.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import workloads as wl
+from oracle import attention, counts, mask, plan, ring
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+INF = wl.WINDOW_INF
+
+
+def _golden_kv(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = line.split(None, 1)
+            out[k] = v
+    return out
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(x) for x in line.split()])
+    return rows
+
+
+def _rand_qkv(rng, n, hq, hkv, d):
+    return (rng.standard_normal((n, hq, d)), rng.standard_normal((n, hkv, d)),
+            rng.standard_normal((n, hkv, d)))
+
+
+# --------------------------------------------------------------------------------------
+# ring / online recurrence
+# --------------------------------------------------------------------------------------
+def test_worked_example_ring_equals_full_attention_f32():
+    g = _golden_kv("ring_worked_example.txt")
+    Q, K, V = ring.worked_example_inputs()
+    assert Q.shape == (int(g["tokens"]), int(g["head_dim"]))
+    P = int(g["devices"])
+    O, _ = ring.ring_forward(Q[:, None, :], K[:, None, :], V[:, None, :], None, P=P,
+                             dtype=np.float32)
+    ref = ring.dense_unmasked_f32(Q, K, V)
+    diff = float(np.abs(O[:, 0, :] - ref).max())
+    page = float(g["max_difference"])
+    # same arithmetic in float32: the page's figure is one or two ulp-scale roundings
+    assert diff <= 1e-6
+    assert abs(diff - page) <= 1e-6
+    assert np.allclose(O[:, 0, :], ref, atol=float(g["allclose_atol"])) == (g["allclose"] == "True")
+    # the fp64 ring agrees with fp64 dense to rounding
+    O64, _ = ring.ring_forward(Q[:, None, :], K[:, None, :], V[:, None, :], None, P=P)
+    ref64, _ = attention.forward(Q[:, None, :], K[:, None, :], V[:, None, :],
+                                 np.ones((16, 16), bool))
+    assert np.abs(O64 - ref64).max() < 1e-13
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16])
+def test_ring_fp64_equals_dense_any_P_and_step_order(P):
+    rng = np.random.default_rng(7)
+    n = 256
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, INF)
+    q, k, v = _rand_qkv(rng, n, 4, 2, 16)
+    O, L = attention.forward(q, k, v, M)
+    Or, Lr = ring.ring_forward(q, k, v, M, P=P)
+    assert np.abs(Or - O).max() < 1e-12
+    fin = np.isfinite(L)
+    assert (np.isfinite(Lr) == fin).all()
+    assert np.abs(Lr[fin] - L[fin]).max() < 1e-12
+    order = [list(rng.permutation(P)) for _ in range(P)]
+    Or2, Lr2 = ring.ring_forward(q, k, v, M, P=P, step_order=order)
+    assert np.abs(Or2 - O).max() < 1e-12
+    assert np.abs(Lr2[fin] - L[fin]).max() < 1e-12
+
+
+def test_ring_with_window_mask_and_plan_order():
+    rng = np.random.default_rng(3)
+    n = 1024
+    tr = wl.random_pack(rng, n)
+    W = 200
+    pl = plan.make_plan(tr, W, 4, "ptrr_block")
+    trp = pl.tracks_perm
+    Mp = mask.dense_mask(trp, W)
+    q, k, v = _rand_qkv(rng, n, 2, 2, 8)
+    Or, Lr = ring.ring_forward(q[pl.perm], k[pl.perm], v[pl.perm], Mp, P=4)
+    O, L = attention.forward(q, k, v, mask.dense_mask(tr, W))
+    assert np.abs(Or - O[pl.perm]).max() < 1e-12
+    fin = np.isfinite(L[:, pl.perm])
+    assert np.abs(Lr[fin] - L[:, pl.perm][fin]).max() < 1e-12
+
+
+def test_fully_masked_rows_give_zero_output_and_neg_inf_lse():
+    # W = 0 and causal tokens: the causal test 0 <= dp < 0 never holds, so a causal
+    # token sees nothing; a bidirectional span still sees its own span.
+    samples = [[wl.Span("causal", 5), wl.Span("full", 4)], [wl.Span("causal", 3)]]
+    tr = wl.tracks_from_samples(samples)
+    n = 12
+    M = mask.dense_mask(tr, 0)
+    assert not M[:5].any() and not M[9:].any() and M[5:9, 5:9].all()
+    rng = np.random.default_rng(0)
+    q, k, v = _rand_qkv(rng, n, 2, 1, 4)
+    O, L = attention.forward(q, k, v, M)
+    assert (O[:5] == 0).all() and (O[9:] == 0).all()
+    assert np.isneginf(L[:, :5]).all() and np.isneginf(L[:, 9:]).all()
+    Or, Lr = ring.ring_forward(q[:12], k[:12], v[:12], M, P=4)
+    assert (Or[:5] == 0).all() and np.isneginf(Lr[:, 9:]).all()
+    # the live rows equal attention restricted to the bidirectional span
+    O2, _ = attention.forward(q[5:9], k[5:9], v[5:9], np.ones((4, 4), bool))
+    assert np.abs(O[5:9] - O2).max() < 1e-13
+    # and their gradients vanish where no key is legal
+    do = rng.standard_normal(q.shape)
+    dq, dk, dv, _, _ = attention.backward(q, k, v, do, M)
+    assert (dq[:5] == 0).all() and (dk[:5] == 0).all() and (dv[9:] == 0).all()
+
+
+def test_uniform_scores_closed_form():
+    # K = 0 makes every legal score 0: softmax is uniform over the legal keys, so
+    # O_q = mean of V over them and LSE_q = ln(number of legal keys).
+    rng = np.random.default_rng(1)
+    n = 300
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, 37)
+    q, _, v = _rand_qkv(rng, n, 2, 2, 8)
+    k = np.zeros_like(v)
+    O, L = attention.forward(q, k, v, M)
+    cnt = M.sum(1)
+    for h in range(2):
+        want = (M.astype(float) @ v[:, h, :]) / np.maximum(cnt, 1)[:, None]
+        assert np.abs(O[:, h, :] - want).max() < 1e-12
+        assert np.abs(L[h][cnt > 0] - np.log(cnt[cnt > 0])).max() < 1e-12
+
+
+def test_single_legal_key_closed_form():
+    # W = 1 on causal tokens: each query sees only itself -> O_q = V_q, LSE = q.k_q/sqrt(d)
+    n, d = 64, 8
+    tr = wl.tracks_from_samples([[wl.Span("causal", n)]])
+    M = mask.dense_mask(tr, 1)
+    assert (M == np.eye(n, dtype=bool)).all()
+    rng = np.random.default_rng(2)
+    q, k, v = _rand_qkv(rng, n, 4, 2, d)
+    O, L = attention.forward(q, k, v, M)
+    for h in range(4):
+        kh = h // 2
+        assert np.abs(O[:, h, :] - v[:, kh, :]).max() < 1e-13
+        s = (q[:, h, :] * k[:, kh, :]).sum(1) / math.sqrt(d)
+        assert np.abs(L[h] - s).max() < 1e-13
+
+
+def test_gqa_head_grouping():
+    # q heads 2 and 3 must read kv head 1; zero its keys -> those heads become uniform.
+    rng = np.random.default_rng(5)
+    n = 40
+    M = np.tril(np.ones((n, n), bool))
+    q, k, v = _rand_qkv(rng, n, 4, 2, 8)
+    k[:, 1, :] = 0
+    O, L = attention.forward(q, k, v, M)
+    cnt = np.arange(1, n + 1)
+    for h in (2, 3):
+        assert np.abs(L[h] - np.log(cnt)).max() < 1e-12
+        assert np.abs(O[:, h, :] - np.cumsum(v[:, 1, :], 0) / cnt[:, None]).max() < 1e-12
+    for h in (0, 1):
+        assert np.abs(L[h] - np.log(cnt)).max() > 1e-3
+
+
+def test_backward_matches_finite_differences():
+    rng = np.random.default_rng(11)
+    samples = [[wl.Span("causal", 6), wl.Span("full", 5), wl.Span("noise", 3),
+                wl.Span("causal", 4)], [wl.Span("group", 3, 0), wl.Span("causal", 2),
+                                        wl.Span("group", 3, 0)]]
+    tr = wl.tracks_from_samples(samples)
+    n = 26
+    M = mask.dense_mask(tr, 5)
+    q, k, v = _rand_qkv(rng, n, 2, 1, 4)
+    do = rng.standard_normal(q.shape)
+
+    def loss(q_, k_, v_):
+        O, _ = attention.forward(q_, k_, v_, M)
+        return float((O * do).sum())
+
+    dq, dk, dv, _, _ = attention.backward(q, k, v, do, M)
+    eps = 1e-6
+    for X, G in ((q, dq), (k, dk), (v, dv)):
+        for idx in [tuple(rng.integers(0, s) for s in X.shape) for _ in range(25)]:
+            Xp = X.copy()
+            Xm = X.copy()
+            Xp[idx] += eps
+            Xm[idx] -= eps
+            args_p = [Xp if Y is X else Y for Y in (q, k, v)]
+            args_m = [Xm if Y is X else Y for Y in (q, k, v)]
+            num = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+            assert abs(num - G[idx]) < 1e-7 * max(1.0, abs(num)), (idx, num, G[idx])
+
+
+def test_permuting_tokens_with_their_tracks_permutes_the_output():
+    rng = np.random.default_rng(4)
+    n = 200
+    tr = wl.random_pack(rng, n)
+    perm = rng.permutation(n)
+    trp = {k: np.asarray(v)[perm] for k, v in tr.items()}
+    trp["pos"] = perm
+    q, k, v = _rand_qkv(rng, n, 2, 1, 8)
+    O, L = attention.forward(q, k, v, mask.dense_mask(tr, 50))
+    Op, Lp = attention.forward(q[perm], k[perm], v[perm], mask.dense_mask(trp, 50))
+    assert np.abs(Op - O[perm]).max() < 1e-12
+
+
+# --------------------------------------------------------------------------------------
+# mask semantics
+# --------------------------------------------------------------------------------------
+def _span_semantics(samples, W):
+    """Legality from the mode table of the MARBLE post (section 01) and its prose, per
+    pair, written without the four-track predicate: within a span by its mode; a later
+    span reads an earlier one unless the earlier one is a noise span; spans of one group
+    read each other in both directions; the window limits causal distance only; no
+    pair crosses samples."""
+    spans = []  # (sample, index in sample, start, end, mode, group)
+    t = 0
+    for si, s in enumerate(samples):
+        for ji, sp in enumerate(s):
+            spans.append((si, ji, t, t + sp.length, sp.mode, sp.group))
+            t += sp.length
+    n = t
+    owner = np.empty(n, np.int64)
+    for i, (_, _, a, b, _, _) in enumerate(spans):
+        owner[a:b] = i
+    out = np.zeros((n, n), bool)
+    for qi in range(n):
+        A = spans[owner[qi]]
+        for ki in range(n):
+            B = spans[owner[ki]]
+            if A[0] != B[0]:
+                continue
+            dp = qi - ki
+            if owner[qi] == owner[ki]:
+                ok = (0 <= dp < W) if A[4] == "causal" else True
+            elif A[4] == "group" and B[4] == "group" and A[5] == B[5]:
+                ok = True
+            elif B[3] <= A[2]:  # key span lies before the query span
+                ok = B[4] != "noise" and dp < W
+            else:
+                ok = False
+            out[qi, ki] = ok
+    return out
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mask_equals_span_semantics_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    samples = wl.random_samples(rng, 160)
+    tr = wl.tracks_from_samples(samples)
+    for W in (INF, 1, 7, 40):
+        assert (mask.dense_mask(tr, W) == _span_semantics(samples, W)).all()
+
+
+def test_mask_hand_derived_cases():
+    S = wl.Span
+    samples = [[S("causal", 4), S("noise", 3), S("causal", 2)],            # 0..8
+               [S("group", 2, 0), S("causal", 2), S("group", 2, 0)],       # 9..14
+               [S("full", 3), S("causal", 2)]]                             # 15..19
+    tr = wl.tracks_from_samples(samples)
+    M = mask.dense_mask(tr, INF)
+    assert M[5, 0] and M[5, 6] and M[4, 6]          # noise span: sees prompt and itself
+    assert not M[7, 4] and not M[8, 6]               # later text cannot see the noise span
+    assert M[7, 3] and not M[3, 7]                   # causal text
+    assert M[9, 13] and M[13, 9]                     # group: earlier frame sees later frame
+    assert not M[9, 11] and M[13, 11]                # ... but not the text between them
+    assert M[15, 17] and M[17, 15] and M[18, 17] and not M[17, 18]
+    assert not M[9, 8] and not M[15, 14] and not M[0, 19]   # never across samples
+    Mw = mask.dense_mask(tr, 2)
+    assert Mw[3, 2] and Mw[3, 3] and not Mw[3, 1]    # last W tokens, the query included
+    assert Mw[15, 17] and Mw[9, 13]                  # spans are not cut by the window
+
+
+# --------------------------------------------------------------------------------------
+# legal-pair counts (Libra Eq. 2, Eq. 6)
+# --------------------------------------------------------------------------------------
+def test_legal_pairs_closed_forms():
+    lens = [300, 17, 1024, 5, 256]
+    causal = wl.tracks_from_samples([[wl.Span("causal", L)] for L in lens])
+    bidi = wl.tracks_from_samples([[wl.Span("full", L)] for L in lens])
+    want_c = sum(L * (L + 1) // 2 for L in lens)
+    want_b = sum(L * L for L in lens)
+    assert counts.by_brute_force(causal, INF) == want_c
+    assert counts.by_key_classes(causal, INF) == want_c
+    assert counts.by_brute_force(bidi, INF) == want_b
+    assert counts.by_key_classes(bidi, INF) == want_b
+    # Libra Eq. 6 per block of query rows
+    rows = mask.dense_mask(causal, INF).sum(1)
+    n = len(rows)
+    per_block = rows[: n // 128 * 128].reshape(-1, 128).sum(1)
+    assert (counts.causal_block_rows(lens)[: n // 128] == per_block).all()
+
+
+def test_legal_pairs_config1_and_config3():
+    tr1 = wl.config_tracks(1)
+    want1 = 768 * 769 // 2 + 1024 ** 2 + 256 * 257 // 2
+    assert want1 == 1376768
+    assert counts.by_brute_force(tr1, INF) == want1
+    assert counts.by_key_classes(tr1, INF) == want1
+    tr3 = wl.config_tracks(3)
+    N, W = 262144, 4096
+    want3 = W * (W + 1) // 2 + (N - W) * W
+    assert want3 == 1065355264
+    assert counts.by_key_classes(tr3, W) == want3
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_legal_pair_counters_agree(seed):
+    rng = np.random.default_rng(seed)
+    tr = wl.random_pack(rng, 700)
+    for W in (INF, 1, 33):
+        assert counts.by_key_classes(tr, W) == counts.by_brute_force(tr, W)
+        assert (counts.per_row_by_key_classes(tr, W) == mask.dense_mask(tr, W).sum(1)).all()
+
+
+# --------------------------------------------------------------------------------------
+# tile map
+# --------------------------------------------------------------------------------------
+def test_tile_map_config1_exact():
+    tr = wl.config_tracks(1)
+    T = plan.classify(plan.block_summaries(tr), INF)
+    assert (T == plan.FULL).sum() == 80
+    assert (T == plan.PARTIAL).sum() == 8
+    assert (T == plan.EMPTY).sum() == 168
+    # sample A = blocks 0..5 (causal): partial diagonal, full below
+    for a in range(6):
+        assert T[a, a] == plan.PARTIAL
+        assert all(T[a, b] == plan.FULL for b in range(a))
+        assert all(T[a, b] == plan.EMPTY for b in range(a + 1, 16))
+    assert (T[6:14, 6:14] == plan.FULL).all()
+    assert T[14, 14] == T[15, 15] == plan.PARTIAL and T[15, 14] == plan.FULL
+
+
+def test_tile_map_config3_structure():
+    tr = wl.config_tracks(3)
+    summ = plan.block_summaries(tr)
+    rows = np.array([0, 1, 31, 32, 33, 500, 2047])
+    T = plan.classify(summ, 4096, rows)
+    for i, b in enumerate(rows):
+        full = set(np.flatnonzero(T[i] == plan.FULL))
+        part = set(np.flatnonzero(T[i] == plan.PARTIAL))
+        assert full == set(range(max(0, b - 31), b))
+        assert part == ({b, b - 32} if b >= 32 else {b})
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_tile_map_is_sound_by_brute_force(seed):
+    rng = np.random.default_rng(50 + seed)
+    n = 128 * 12
+    tr = wl.random_pack(rng, n, max_samples=3)
+    for W in (INF, 100, 300):
+        T = plan.classify(plan.block_summaries(tr), W)
+        M = mask.dense_mask(tr, W)
+        for a in range(12):
+            for b in range(12):
+                blk = M[a * 128:(a + 1) * 128, b * 128:(b + 1) * 128]
+                if T[a, b] == plan.FULL:
+                    assert blk.all()
+                elif T[a, b] == plan.EMPTY:
+                    assert not blk.any()
+
+
+# --------------------------------------------------------------------------------------
+# order, step lists, needed index
+# --------------------------------------------------------------------------------------
+def test_ptrr_reproduces_zigzag():
+    tr = wl.tracks_from_samples([[wl.Span("causal", 8 * 128)]])
+    pl = plan.make_plan(tr, INF, 4, "ptrr_block")
+    gold = _golden_rows("zigzag_p4.txt")
+    for dev, a, b, work in gold:
+        blocks = sorted(pl.block_perm[dev * 2:(dev + 1) * 2].tolist())
+        assert blocks == sorted([a, b])
+        assert int(pl.cost[blocks].sum()) == work
+
+
+def test_contiguous_causal_imbalance():
+    tr = wl.tracks_from_samples([[wl.Span("causal", 4 * 128)]])
+    pl = plan.make_plan(tr, INF, 4, "contiguous")
+    Wm = plan.shard_work(pl)
+    for dev, blocks in _golden_rows("causal_contiguous_p4.txt"):
+        assert Wm[dev].sum() == blocks
+        assert (Wm[dev, : dev + 1] == 1).all() and (Wm[dev, dev + 1:] == 0).all()
+
+
+def test_ptrr_chunk_units_and_tie_break():
+    # equal costs: ties are broken by ascending unit index
+    assert plan.ptrr_assign([5, 5, 5, 5], 2) == [[0, 3], [1, 2]]
+    assert plan.ptrr_assign([1, 2, 3, 4, 5, 6], 3) == [[0, 5], [1, 4], [2, 3]]
+    tr = wl.tracks_from_samples([[wl.Span("causal", 16 * 128)]])
+    pl = plan.make_plan(tr, INF, 2, "ptrr_chunk", chunk_tokens=512)
+    # 4 chunks of 4 blocks, causal costs grow with the chunk index: ranks {3,0}, {2,1}
+    assert pl.block_perm.tolist() == [0, 1, 2, 3, 12, 13, 14, 15, 4, 5, 6, 7, 8, 9, 10, 11]
+
+
+def test_needed_index_config3():
+    tr = wl.config_tracks(3)
+    pl = plan.make_plan(tr, 4096, 16, "contiguous")
+    sizes = np.diff(pl.needed_ptr)
+    assert sizes[0] == 128 and (sizes[1:] == 160).all()
+    r = 5
+    assert pl.needed[pl.needed_ptr[r]:pl.needed_ptr[r + 1]].tolist() == list(
+        range(128 * r - 32, 128 * r + 128))
+
+
+@pytest.mark.parametrize("order", ["contiguous", "ptrr_block", "ptrr_chunk"])
+def test_step_lists_partition_the_tile_map(order):
+    rng = np.random.default_rng(9)
+    n = 128 * 32
+    tr = wl.random_pack(rng, n, max_samples=4)
+    P = 4
+    pl = plan.make_plan(tr, 700, P, order, chunk_tokens=512)
+    nb = pl.nb
+    T = plan.classify(plan.block_summaries(tr), 700)
+    bps = nb // P
+    seen = np.zeros((nb, nb), np.int8)
+    for nq in range(nb):
+        for j in range(P):
+            a, b = pl.step_ptr[nq * P + j], pl.step_ptr[nq * P + j + 1]
+            cols = pl.step_col[a:b]
+            assert (np.diff(cols) > 0).all() and ((cols // bps) == j).all()
+            seen[nq, cols] = pl.step_tag[a:b]
+    assert (seen == T[np.ix_(pl.block_perm, pl.block_perm)]).all()
+    seenT = np.zeros((nb, nb), np.int8)
+    for nk in range(nb):
+        for r in range(P):
+            a, b = pl.colT_ptr[nk * P + r], pl.colT_ptr[nk * P + r + 1]
+            rows = pl.colT_row[a:b]
+            assert (np.diff(rows) > 0).all() and ((rows // bps) == r).all()
+            seenT[rows, nk] = pl.colT_tag[a:b]
+    assert (seenT == seen).all()
+    for r in range(P):
+        want = np.flatnonzero(seen[r * bps:(r + 1) * bps].any(0))
+        assert pl.needed[pl.needed_ptr[r]:pl.needed_ptr[r + 1]].tolist() == want.tolist()
+    # permuted tracks carry the original positions
+    assert (pl.tracks_perm["pos"] == pl.perm).all()
+    assert (pl.tracks_perm["sample"] == tr["sample"][pl.perm]).all()
