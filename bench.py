@@ -1,0 +1,409 @@
+"""Benchmark: attention fwd+bwd effective TFLOP/s on legal-pair (unmasked) FLOPs.
+
+Workload (default): the packed multimodal 64K pack -- N = 65536 tokens, 16 q / 16 kv heads,
+d = 128, bf16 Q/K/V/dO ~ N(0, 1) (seed 0), lognormal 60/30/10 text/image/generated sample
+mix, P = 8 virtual shards in PTRR order.  One step = every forward ring step (P^2 calls,
+r-major), the finalize, the backward preprocessing and every backward ring step (P^2
+calls), all through the C ABI on one GPU.  The plan is built once per pack (it is reused by
+every layer, forward and backward) and is timed separately.
+
+Effective FLOPs per step = 14 * d * legal_pairs * Hq (forward 4 d, backward 10 d per legal
+pair); legal_pairs comes from the library's own counter (marble_plan_stats).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl marble|reference]
+For N > 1 (torchrun) every rank runs an independent replica (the path has no exchange
+step on one GPU); rank 0 prints the line with the max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attn fwd+bwd effective TFLOP/s (unmasked FLOPs) and % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", 0)) or None, \
+            float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    backend = os.environ.get("MARBLE_BENCH_BACKEND", "nccl")
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", "0")), dist
+
+
+def max_over_ranks(x: float, dist) -> float:
+    """Max of a per-rank scalar over all ranks (identity without a process group)."""
+    if dist is None:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                for nm, val in zip(names, r[5:9]):
+                    if val.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample of the same workload)
+# --------------------------------------------------------------------------------------
+def oracle_sample_rate(cfg, tr, budget_s: float, seed: int = 0):
+    """Time the fp64 oracle's dense forward+backward on whole samples of the pack (all q
+    heads) until ``budget_s`` seconds are spent; return effective TFLOP/s on legal pairs."""
+    import numpy as np
+    import torch
+
+    from oracle import attention, counts, mask
+
+    st = np.asarray(tr["sample"])
+    ids = np.unique(st)
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(ids)
+    g = torch.Generator().manual_seed(seed)
+    pairs = 0
+    tokens = 0
+    nsamp = 0
+    elapsed = 0.0
+    for sid in order:
+        idx = np.flatnonzero(st == sid)
+        L = len(idx)
+        if L > 4096:
+            continue
+        sub = {k: np.asarray(v)[idx] for k, v in tr.items()}
+        sub["pos"] = idx
+        q = torch.randn((L, cfg.hq, cfg.d), generator=g).to(torch.bfloat16)
+        k = torch.randn((L, cfg.hkv, cfg.d), generator=g).to(torch.bfloat16)
+        v = torch.randn((L, cfg.hkv, cfg.d), generator=g).to(torch.bfloat16)
+        do = torch.randn((L, cfg.hq, cfg.d), generator=g).to(torch.bfloat16)
+        t0 = time.perf_counter()
+        attention.backward(q, k, v, do, mask.dense_mask(sub, cfg.window))
+        elapsed += time.perf_counter() - t0
+        pairs += counts.by_key_classes(sub, cfg.window)
+        tokens += L
+        nsamp += 1
+        if elapsed >= budget_s:
+            break
+    flops = 14.0 * cfg.d * pairs * cfg.hq
+    return flops / elapsed / 1e12, elapsed, nsamp, tokens
+
+
+def run_reference(args, rank, world, dist):
+    """The oracle as it stands, timed on the host cores (rank 0 only)."""
+    import workloads as wl
+    cfg = wl.CONFIGS[args.config]
+    if rank != 0:
+        return
+    tr = wl.config_tracks(args.config)
+    for _ in range(args.warmup):
+        oracle_sample_rate(cfg, tr, args.ref_budget)
+    rates, times = [], []
+    desc = None
+    for i in range(args.steps):
+        r, el, ns, tok = oracle_sample_rate(cfg, tr, args.ref_budget, seed=i)
+        rates.append(r)
+        times.append(el)
+        desc = (f"{ns} whole samples ({tok} tokens) of the {cfg.name} pack, all {cfg.hq} q "
+                f"heads, fp64 dense forward+backward, ~{args.ref_budget:.0f} s per step")
+    value = statistics.mean(rates)
+    cores = os.cpu_count()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": cfg.name, "n_tokens": cfg.n, "heads": f"{cfg.hq}/{cfg.hkv}",
+                   "d": cfg.d, "shards": cfg.shards, "order": cfg.order},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------
+# the CUDA path
+# --------------------------------------------------------------------------------------
+def run_marble(args, rank, world, local, dist):
+    import numpy as np
+    import torch
+
+    import context_attention_metadata_gb300 as M
+    import workloads as wl
+    from context_attention_metadata_gb300 import _build
+
+    torch.cuda.set_device(local)
+    _build.build()
+    cfg = wl.CONFIGS[args.config]
+    n, hq, hkv, d, P = cfg.n, cfg.hq, cfg.hkv, cfg.d, cfg.shards
+    needed = cfg.needed
+    tr = wl.config_tracks(args.config)
+    trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    stream = torch.cuda.current_stream()
+
+    # plan: built once per pack, timed on its own (best of 3)
+    plan_ms = []
+    pl = None
+    for _ in range(3):
+        if pl is not None:
+            pl.close()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens)
+        torch.cuda.synchronize()
+        plan_ms.append(1e3 * (time.perf_counter() - t0))
+    stats = pl.stats()
+    pairs = stats["legal_pairs"]
+    flops_fwd = 4.0 * d * pairs * hq
+    flops_bwd = 10.0 * d * pairs * hq
+    flops = flops_fwd + flops_bwd
+
+    q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda", seed=0)
+    qp, kp, vp, dop = (pl.permute(t) for t in (q, k, v, do))
+    st = M.State(n, hq, d)
+    o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dq = torch.empty((n, hq, d), dtype=torch.float32, device="cuda")
+    dk = torch.empty((n, hkv, d), dtype=torch.float32, device="cuda")
+    dv = torch.empty((n, hkv, d), dtype=torch.float32, device="cuda")
+    sched = M.ring_schedule(P, needed)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(marks=None):
+        if marks:
+            marks[0].record(stream)
+        for r, j, first in sched:
+            M.attn_step(pl, qp, kp, vp, r, j, st, first=first)
+        if marks:
+            marks[1].record(stream)
+        M.attn_finalize(pl, st, o, lse)
+        M.attn_bwd_prep(pl, o, dop, delta)
+        dq.zero_()
+        dk.zero_()
+        dv.zero_()
+        if marks:
+            marks[2].record(stream)
+        for r, j, _ in sched:
+            M.attn_bwd(pl, qp, kp, vp, dop, lse, delta, r, j, dq, dk, dv)
+        if marks:
+            marks[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    pl.check()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter()
+        for i in range(args.steps):
+            step(marks[i])
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    pl.check()
+    step_ms = [m[0].elapsed_time(m[3]) for m in marks]
+    fwd_ms = [m[0].elapsed_time(m[1]) for m in marks]
+    bwd_ms = [m[2].elapsed_time(m[3]) for m in marks]
+    mid_ms = [m[1].elapsed_time(m[2]) for m in marks]
+    dev_s = max_over_ranks(sum(step_ms) / 1e3, dist)
+    value = world * flops * args.steps / dev_s / 1e12
+    ms_per_step = 1e3 * dev_s / args.steps
+
+    peak, peak_sus, hbm, peak_kind = _peaks()
+    fwd_launches, bwd_launches = len(sched), 2 * len(sched)
+    mf, mb = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
+    # dominant phase: report its own kernel's algorithmic FLOPs per launch / launch time
+    if mb >= mf:
+        dom = {"kernel": "k_bwd_dq + k_bwd_dkdv (one marble_attn_bwd call)",
+               "flops_per_launch": flops_bwd / len(sched), "ms_per_launch": mb / len(sched)}
+    else:
+        dom = {"kernel": "k_attn_fwd (one marble_attn_step call)",
+               "flops_per_launch": flops_fwd / len(sched), "ms_per_launch": mf / len(sched)}
+    ach = dom["flops_per_launch"] / (dom["ms_per_launch"] / 1e3) / 1e12
+    roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "traffic": None, "kernel": dom["kernel"],
+            "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)"}
+
+    # end to end through the public API: H2D of the step's inputs from pinned memory,
+    # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results
+    e2e = None
+    if args.e2e_steps > 0:
+        hq_pin = [t.cpu().pin_memory() for t in (q, k, v, do)]
+        htr = [t.cpu().pin_memory() for t in trk]
+        out_pin = [torch.empty((n, hq, d), dtype=torch.bfloat16).pin_memory()] + \
+                  [torch.empty(s, dtype=torch.bfloat16).pin_memory()
+                   for s in ((n, hq, d), (n, hkv, d), (n, hkv, d))]
+        dq_b = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+        dk_b = torch.empty((n, hkv, d), dtype=torch.bfloat16, device="cuda")
+        dv_b = torch.empty((n, hkv, d), dtype=torch.bfloat16, device="cuda")
+        dev_in = [torch.empty_like(t, device="cuda") for t in hq_pin]
+        dev_tr = [torch.empty_like(t, device="cuda") for t in htr]
+
+        def e2e_step():
+            for dst, src in zip(dev_in + dev_tr, hq_pin + htr):
+                dst.copy_(src, non_blocking=True)
+            p2 = M.Plan(dev_tr[0], dev_tr[1], dev_tr[2], cfg.window, P, cfg.order,
+                        cfg.chunk_tokens)
+            q2, k2, v2, do2 = (p2.permute(t) for t in dev_in)
+            M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
+            dq.zero_()
+            dk.zero_()
+            dv.zero_()
+            M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
+            o_u = p2.permute(o, inverse=True)
+            for g_, b_ in ((dq, dq_b), (dk, dk_b), (dv, dv_b)):
+                M.cast_bf16(p2.permute(g_, inverse=True), b_)
+            for dst, src in zip(out_pin, (o_u, dq_b, dk_b, dv_b)):
+                dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+            p2.close()
+
+        e2e_step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dist)
+        h2d = sum(t.numel() * t.element_size() for t in hq_pin + htr)
+        d2h = sum(t.numel() * t.element_size() for t in out_pin)
+        e2e = {"value": world * flops / e2e_s / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
+               "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H"}
+
+    cpu = None
+    if rank == 0 and args.cpu_budget > 0:
+        r, el, ns, tok = oracle_sample_rate(cfg, tr, args.cpu_budget)
+        cpu = {"value": r, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{ns} whole samples ({tok} tokens) of the pack, all {hq} q heads, "
+                         f"fp64 dense fwd+bwd, {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": cfg.name, "n_tokens": n, "heads": f"{hq}/{hkv}", "d": d,
+                       "shards": P, "order": cfg.order, "window": cfg.window,
+                       "schedule": "needed-blocks" if needed else "ring r-major P^2 steps",
+                       "l2": "inputs larger than L2 (Q/K/V/dO 256 MiB each; state 512 MiB)",
+                       "legal_pairs_per_head": pairs, "flops_per_step": flops,
+                       "parallelism": f"replicas x{world}"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "pct_of_sustained_peak": (100.0 * value / world / peak_sus) if peak_sus else None,
+            "phases_ms": {"fwd_steps": mf, "finalize+prep+zero": statistics.mean(mid_ms),
+                          "bwd_steps": mb},
+            "fwd_tflops": flops_fwd / (mf / 1e3) / 1e12,
+            "bwd_tflops": flops_bwd / (mb / 1e3) / 1e12,
+            "plan_ms": min(plan_ms), "plan_stats": stats,
+            "wall_s_timed_region": t_wall,
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps * (fwd_launches + 2 + bwd_launches),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="marble", choices=["marble", "reference"])
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle time for cpu_baseline (0 disables)")
+    ap.add_argument("--ref-budget", type=float, default=5.0,
+                    help="seconds of oracle time per reference-arm step")
+    args = ap.parse_args()
+    rank, world, local, dist = _dist()
+    if args.impl == "reference":
+        run_reference(args, rank, world, dist)
+    else:
+        run_marble(args, rank, world, local, dist)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

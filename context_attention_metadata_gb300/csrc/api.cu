@@ -1,0 +1,377 @@
+// C ABI of libmarble: argument validation, plan lifetime, statistics and exports, and
+// the launches of the planner, attention and helper kernels.  Declarations and the
+// contract of every call are in include/marble.h.
+#include <climits>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace marble {
+
+static thread_local std::string g_last_error;
+static uint64_t g_wait_limit_ns = 0;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+marble_status_t fail(marble_status_t st, const std::string& msg) {
+  g_last_error = msg;
+  return st;
+}
+
+marble_status_t cuda_fail(cudaError_t e, const char* what) {
+  g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+  return MARBLE_ERR_CUDA;
+}
+
+uint64_t wait_limit_ns() {
+  if (g_wait_limit_ns == 0) {
+    const char* env = std::getenv("MARBLE_WAIT_LIMIT_MS");
+    uint64_t ms = env ? std::strtoull(env, nullptr, 10) : 0;
+    g_wait_limit_ns = ms ? ms * 1000000ull : 2000000000ull;
+  }
+  return g_wait_limit_ns;
+}
+
+// true for device or managed memory of the current context
+static bool is_device_ptr(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static marble_status_t check_tensor(const void* p, const char* name) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, std::string(name) + " is null");
+  if (!aligned16(p)) return fail(MARBLE_ERR_INVALID_ARG, std::string(name) + " is not 16-byte aligned");
+  if (!is_device_ptr(p)) return fail(MARBLE_ERR_INVALID_ARG, std::string(name) + " is not device memory");
+  return MARBLE_OK;
+}
+
+static marble_status_t check_qkv(const marble_plan_t* p, const marble_qkv_t* qkv) {
+  if (!qkv) return fail(MARBLE_ERR_INVALID_ARG, "qkv is null");
+  if (qkv->d != 64 && qkv->d != 128)
+    return fail(MARBLE_ERR_INVALID_ARG, "head dim d must be 64 or 128");
+  if (qkv->hq < 1 || qkv->hkv < 1 || qkv->hq % qkv->hkv)
+    return fail(MARBLE_ERR_INVALID_ARG, "hq must be a positive multiple of hkv");
+  if ((int64_t)p->bps * qkv->hq > INT_MAX)
+    return fail(MARBLE_ERR_UNSUPPORTED, "too many (block, head) work units per shard");
+  if (!(qkv->scale >= 0.f) || std::isinf(qkv->scale))
+    return fail(MARBLE_ERR_INVALID_ARG, "scale must be finite and >= 0 (0 = 1/sqrt(d))");
+  marble_status_t st;
+  if ((st = check_tensor(qkv->q, "q")) != MARBLE_OK) return st;
+  if ((st = check_tensor(qkv->k, "k")) != MARBLE_OK) return st;
+  if ((st = check_tensor(qkv->v, "v")) != MARBLE_OK) return st;
+  return MARBLE_OK;
+}
+
+static marble_status_t check_shards(const marble_plan_t* p, int q_shard, int kv_shard) {
+  if (q_shard < 0 || q_shard >= p->P)
+    return fail(MARBLE_ERR_INVALID_ARG, "q_shard out of range");
+  if (kv_shard != MARBLE_KV_NEEDED && (kv_shard < 0 || kv_shard >= p->P))
+    return fail(MARBLE_ERR_INVALID_ARG, "kv_shard out of range");
+  return MARBLE_OK;
+}
+
+}  // namespace marble
+
+using namespace marble;
+
+#define MARBLE_API extern "C" __attribute__((visibility("default")))
+
+MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_stream_t stream,
+                                       marble_plan_t** out) {
+  if (!d || !out) return fail(MARBLE_ERR_INVALID_ARG, "desc and out must be non-null");
+  *out = nullptr;
+  if (d->n_tokens <= 0 || d->n_tokens % MARBLE_BLOCK || d->n_tokens >= (int64_t)INT_MAX)
+    return fail(MARBLE_ERR_INVALID_ARG, "n_tokens must be a positive multiple of 128 below 2^31");
+  if (d->window < 0) return fail(MARBLE_ERR_INVALID_ARG, "window must be >= 0");
+  if (d->num_shards < 1 || d->num_shards > 256)
+    return fail(MARBLE_ERR_INVALID_ARG, "num_shards must be in [1, 256]");
+  const int64_t nb = d->n_tokens / MARBLE_BLOCK;
+  if (nb % d->num_shards)
+    return fail(MARBLE_ERR_INVALID_ARG, "number of 128-token blocks must be divisible by num_shards");
+  if (d->order < MARBLE_ORDER_CONTIGUOUS || d->order > MARBLE_ORDER_PTRR_CHUNK)
+    return fail(MARBLE_ERR_INVALID_ARG, "unknown order");
+  if (d->order == MARBLE_ORDER_PTRR_CHUNK) {
+    if (d->chunk_tokens <= 0 || d->chunk_tokens % MARBLE_BLOCK || d->n_tokens % d->chunk_tokens ||
+        (d->n_tokens / d->chunk_tokens) % d->num_shards)
+      return fail(MARBLE_ERR_INVALID_ARG,
+                  "chunk_tokens must be a multiple of 128 dividing n_tokens into a multiple of "
+                  "num_shards chunks");
+  }
+  if (!is_device_ptr(d->sample_id) || !is_device_ptr(d->seg_id) || !is_device_ptr(d->noise_id))
+    return fail(MARBLE_ERR_INVALID_ARG, "track arrays must be device memory");
+  marble_plan_t* p = new (std::nothrow) marble_plan_t();
+  if (!p) return fail(MARBLE_ERR_OOM, "host allocation failed");
+  cudaGetDevice(&p->device);
+  p->n = d->n_tokens;
+  p->nb = nb;
+  p->P = d->num_shards;
+  p->W = d->window;
+  p->order = d->order;
+  p->chunk_tokens = d->chunk_tokens;
+  p->bps = nb / d->num_shards;
+  marble_status_t st = build_plan(d, (cudaStream_t)stream, p);
+  if (st != MARBLE_OK) {
+    std::string msg = g_last_error;
+    marble_plan_destroy(p);
+    g_last_error = msg;
+    return st;
+  }
+  *out = p;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
+  if (!p) return MARBLE_OK;
+  cudaDeviceSynchronize();
+  for (void* q : p->owned) cudaFree(q);
+  delete p;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stream_t stream,
+                                             marble_plan_stats_t* out) {
+  if (!p || !out) return fail(MARBLE_ERR_INVALID_ARG, "plan and out must be non-null");
+  cudaStream_t s = (cudaStream_t)stream;
+  memset(out, 0, sizeof(*out));
+  out->n_tokens = p->n;
+  out->n_blocks = p->nb;
+  out->num_shards = p->P;
+  out->nnz = p->nnz;
+  marble_status_t st = plan_legal_pairs(p, s, &out->legal_pairs, &out->n_full, &out->n_partial);
+  if (st != MARBLE_OK) return st;
+  const int64_t np = p->nb * p->P + 1;
+  std::vector<int64_t> ptr(np);
+  std::vector<int64_t> nptr(p->P + 1);
+  std::vector<int32_t> needed(p->needed_total);
+  cudaError_t e = cudaMemcpyAsync(ptr.data(), p->step_ptr, np * 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(nptr.data(), p->needed_ptr, (p->P + 1) * 8, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess && p->needed_total)
+    e = cudaMemcpyAsync(needed.data(), p->needed, p->needed_total * 4, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_plan_stats copies");
+  const int P = p->P;
+  std::vector<int64_t> W((size_t)P * P, 0);
+  for (int64_t nq = 0; nq < p->nb; ++nq)
+    for (int j = 0; j < P; ++j)
+      W[(nq / p->bps) * P + j] += ptr[nq * P + j + 1] - ptr[nq * P + j];
+  int64_t mx = 0, sum = 0, sc = 0;
+  for (int r = 0; r < P; ++r) {
+    int64_t c = 0;
+    for (int j = 0; j < P; ++j) c += W[r * P + j];
+    mx = c > mx ? c : mx;
+    sum += c;
+  }
+  for (int s2 = 0; s2 < P; ++s2) {
+    int64_t best = 0;
+    for (int r = 0; r < P; ++r) {
+      const int64_t v = W[r * P + ((r - s2) % P + P) % P];
+      best = v > best ? v : best;
+    }
+    sc += best;
+  }
+  out->shard_cost_max = mx;
+  out->shard_cost_sum = sum;
+  out->step_cost = sc;
+  out->needed_total = p->needed_total;
+  int64_t remote = 0;
+  for (int r = 0; r < P; ++r)
+    for (int64_t x = nptr[r]; x < nptr[r + 1]; ++x)
+      remote += (needed[x] / p->bps) != r;
+  out->needed_remote = remote;
+  return MARBLE_OK;
+}
+
+static bool field_info(const marble_plan_t* p, int32_t field, const void** src, size_t* bytes) {
+  const int64_t n = p->n, nb = p->nb, P = p->P;
+  switch (field) {
+    case MARBLE_FIELD_PERM: *src = p->perm; *bytes = n * 4; return true;
+    case MARBLE_FIELD_BLOCK_PERM: *src = p->block_perm; *bytes = nb * 4; return true;
+    case MARBLE_FIELD_TRACKS_PERM: *src = p->tracks; *bytes = 4 * n * 4; return true;
+    case MARBLE_FIELD_TILE_ROWPTR: *src = p->row_ptr; *bytes = (nb + 1) * 8; return true;
+    case MARBLE_FIELD_TILE_COL: *src = p->col; *bytes = p->nnz * 4; return true;
+    case MARBLE_FIELD_TILE_TAG: *src = p->tag; *bytes = p->nnz; return true;
+    case MARBLE_FIELD_STEP_PTR: *src = p->step_ptr; *bytes = (nb * P + 1) * 8; return true;
+    case MARBLE_FIELD_STEP_COL: *src = p->step_col; *bytes = p->nnz * 4; return true;
+    case MARBLE_FIELD_STEP_TAG: *src = p->step_tag; *bytes = p->nnz; return true;
+    case MARBLE_FIELD_COLT_PTR: *src = p->colT_ptr; *bytes = (nb * P + 1) * 8; return true;
+    case MARBLE_FIELD_COLT_ROW: *src = p->colT_row; *bytes = p->nnz * 4; return true;
+    case MARBLE_FIELD_COLT_TAG: *src = p->colT_tag; *bytes = p->nnz; return true;
+    case MARBLE_FIELD_NEEDED_PTR: *src = p->needed_ptr; *bytes = (P + 1) * 8; return true;
+    case MARBLE_FIELD_NEEDED: *src = p->needed; *bytes = p->needed_total * 4; return true;
+    default: return false;
+  }
+}
+
+MARBLE_API marble_status_t marble_plan_field_bytes(const marble_plan_t* p, int32_t field,
+                                                   size_t* bytes) {
+  const void* src = nullptr;
+  if (!p || !bytes) return fail(MARBLE_ERR_INVALID_ARG, "plan and bytes must be non-null");
+  if (!field_info(p, field, &src, bytes)) return fail(MARBLE_ERR_INVALID_ARG, "unknown field");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_plan_export(const marble_plan_t* p, int32_t field, void* dst,
+                                              size_t bytes, marble_stream_t stream) {
+  const void* src = nullptr;
+  size_t want = 0;
+  if (!p || (!dst && bytes)) return fail(MARBLE_ERR_INVALID_ARG, "plan and dst must be non-null");
+  if (!field_info(p, field, &src, &want)) return fail(MARBLE_ERR_INVALID_ARG, "unknown field");
+  if (bytes != want) return fail(MARBLE_ERR_INVALID_ARG, "bytes does not match the field size");
+  if (!bytes) return MARBLE_OK;
+  cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_plan_export");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_permute(const marble_plan_t* p, const void* src, void* dst,
+                                          int64_t row_bytes, int32_t inverse,
+                                          marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  if (row_bytes <= 0 || row_bytes % 4)
+    return fail(MARBLE_ERR_INVALID_ARG, "row_bytes must be a positive multiple of 4");
+  marble_status_t st;
+  if ((st = check_tensor(src, "src")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dst, "dst")) != MARBLE_OK) return st;
+  const char* a = static_cast<const char*>(src);
+  const char* b = static_cast<const char*>(dst);
+  const int64_t bytes = p->n * row_bytes;
+  if (a < b + bytes && b < a + bytes) return fail(MARBLE_ERR_INVALID_ARG, "src and dst overlap");
+  cudaError_t e = launch_permute(p, src, dst, row_bytes, inverse ? 1 : 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_permute launch");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                            int32_t q_shard, int32_t kv_shard,
+                                            const marble_state_t* state, uint32_t flags,
+                                            marble_stream_t stream) {
+  if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_shards(p, q_shard, kv_shard)) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
+  if (flags & ~MARBLE_STEP_FIRST) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+  return run_attn_fwd(p, qkv, q_shard, kv_shard, state, flags, (cudaStream_t)stream);
+}
+
+MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
+                                                const marble_state_t* state, int32_t hq,
+                                                int32_t d, void* o_bf16, float* lse,
+                                                marble_stream_t stream) {
+  if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
+  if (d != 64 && d != 128) return fail(MARBLE_ERR_INVALID_ARG, "d must be 64 or 128");
+  if (hq < 1) return fail(MARBLE_ERR_INVALID_ARG, "hq must be >= 1");
+  marble_status_t st;
+  if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
+  if ((st = check_tensor(o_bf16, "o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(lse, "lse")) != MARBLE_OK) return st;
+  cudaError_t e = launch_finalize(p, state->o_acc, state->m, state->l, hq, d, o_bf16, lse,
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_attn_finalize launch");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_attn_bwd_prep(const marble_plan_t* p, const void* o,
+                                                const void* d_o, int32_t hq, int32_t d,
+                                                float* delta, marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  if (d != 64 && d != 128) return fail(MARBLE_ERR_INVALID_ARG, "d must be 64 or 128");
+  if (hq < 1) return fail(MARBLE_ERR_INVALID_ARG, "hq must be >= 1");
+  marble_status_t st;
+  if ((st = check_tensor(o, "o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(d_o, "d_o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(delta, "delta")) != MARBLE_OK) return st;
+  cudaError_t e = launch_bwd_prep(p, o, d_o, hq, d, delta, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_attn_bwd_prep launch");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                           const void* d_o, const float* lse,
+                                           const float* delta, int32_t q_shard,
+                                           int32_t kv_shard, float* dq_acc, float* dk_acc,
+                                           float* dv_acc, uint32_t flags,
+                                           marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_shards(p, q_shard, kv_shard)) != MARBLE_OK) return st;
+  if ((st = check_tensor(d_o, "d_o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(lse, "lse")) != MARBLE_OK) return st;
+  if ((st = check_tensor(delta, "delta")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dq_acc, "dq_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
+  if (flags != 0) return fail(MARBLE_ERR_INVALID_ARG, "flags must be 0");
+  return run_attn_bwd(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq_acc, dk_acc, dv_acc,
+                      (cudaStream_t)stream);
+}
+
+MARBLE_API marble_status_t marble_cast_bf16(const float* src, void* dst, int64_t n,
+                                            marble_stream_t stream) {
+  if (n < 0 || n % 4) return fail(MARBLE_ERR_INVALID_ARG, "n must be a non-negative multiple of 4");
+  if (n == 0) return MARBLE_OK;
+  marble_status_t st;
+  if ((st = check_tensor(src, "src")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dst, "dst")) != MARBLE_OK) return st;
+  cudaError_t e = launch_cast_bf16(src, dst, n, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_cast_bf16 launch");
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_check(const marble_plan_t* p, marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "asynchronous CUDA error");
+  unsigned h = 0;
+  e = cudaMemcpy(&h, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "reading the plan's error word");
+  if (h) {
+    e = cudaMemset(p->err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the plan's error word");
+    if (h & kErrTimeout)
+      return fail(MARBLE_ERR_TIMEOUT, "a bounded in-kernel wait ran out (error word " +
+                                          std::to_string(h) + ")");
+    return fail(MARBLE_ERR_CUDA, "device error word " + std::to_string(h));
+  }
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) return fail(MARBLE_ERR_INVALID_ARG, "limit must be > 0");
+  g_wait_limit_ns = ns;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_debug_wait_timeout(const marble_plan_t* p, uint64_t limit_ns,
+                                                     marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(MARBLE_ERR_INVALID_ARG, "limit_ns must be in (0, 10 s]");
+  cudaError_t e = launch_debug_wait(p->err, limit_ns, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_debug_wait_timeout launch");
+  return MARBLE_OK;
+}
+
+MARBLE_API const char* marble_last_error(void) { return g_last_error.c_str(); }
+
+MARBLE_API const char* marble_version(void) { return "marble-gb300 0.1 (sm_103a)"; }

@@ -1,0 +1,597 @@
+// Backward ring step: fp32 dQ / dK / dV accumulation for the tiles between one q shard
+// and one kv shard (or every needed kv block), against the FINAL LSE.
+//
+// MARBLE post, s03 "Exact ring attention accumulation": each step runs the attention
+// backward against the final LSE, starting from an fp32 dQ accumulator carried across
+// steps, while each kv shard's fp32 dK/dV accumulator travels with the shard; s03 closing
+// rule: gradients summed across calls are summed in fp32.
+//
+// Per tile (S = Q K^T * scale, P = exp(S - LSE), dP = dO V^T, dS = P * (dP - delta)):
+//   dV += P^T dO,  dK += scale * dS^T Q,  dQ += scale * dS K.
+// Two kernels, so that every accumulator has exactly one owner per launch and no atomics
+// are needed (a fused kernel would scatter one fp32 dQ tile per (q, kv) tile):
+//   k_bwd_dq    Q-stationary, one CTA per (q block, q head): S and dP in TMEM, dS (bf16)
+//               back into TMEM over S, dQ += dS K with K read MN-major from the K tile
+//               already staged for S; at the end dq_acc += scale * dQ.
+//   k_bwd_dkdv  KV-stationary, one CTA per (kv block, kv head), looping over the q heads of
+//               its group and the q blocks listed for it: S^T = K Q^T and dP^T = V dO^T in
+//               TMEM, P^T and dS^T (bf16) back into TMEM, dV += P^T dO and dK += dS^T Q with
+//               dO and Q read MN-major; at the end dv_acc += dV, dk_acc += scale * dK.
+// Both: warp 0 TMA producer (two stages), warp 1 TMEM allocation + MMA issue, warps 2..5
+// one thread per TMEM lane for the elementwise stage.  Masks only on partial tiles.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tma_host.h"
+
+namespace marble {
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdParams {
+  CUtensorMap q_map, k_map, v_map, do_map;
+  const int64_t* step_ptr;   // row lists (dQ kernel)
+  const int32_t* step_col;
+  const uint8_t* step_tag;
+  const int64_t* colT_ptr;   // column lists (dK/dV kernel)
+  const int32_t* colT_row;
+  const uint8_t* colT_tag;
+  const int64_t* needed_ptr;
+  const int32_t* needed;
+  const int32_t* tracks;     // [4][n] plan order
+  const float* lse;          // [hq][n] natural log
+  const float* delta;        // [hq][n]
+  float* dq;
+  float* dk;
+  float* dv;
+  unsigned* err;
+  unsigned long long wait_ns;
+  long long n;
+  int P, bps, q_shard, kv_shard;
+  int hq, hkv, group;
+  int W;
+  float scale, sl2;
+};
+
+// ======================================================================================
+// dQ (Q-stationary)
+// ======================================================================================
+enum { Q_QFULL, Q_KVFULL0, Q_KVFULL1, Q_KVEMPTY0, Q_KVEMPTY1, Q_SFULL, Q_PFULL, Q_DQDONE,
+       Q_DRAIN, Q_TRK0, Q_TRK1, Q_NUM };
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
+  constexpr int kTile = 128 * D * 2;
+  constexpr int kAtoms = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + kTile;
+  uint8_t* sK0 = smem + 2 * kTile;  // stage s: K at 2+2s, V at 3+2s
+  int32_t* ktr = reinterpret_cast<int32_t*>(smem + 6 * kTile);  // [2][4][128]
+  __shared__ __align__(8) uint64_t bar[Q_NUM];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x / p.bps, i = blockIdx.x % p.bps;
+  const long long n = p.n;
+  const int64_t nq = (int64_t)p.q_shard * p.bps + i;
+  int64_t e0, e1;
+  if (p.kv_shard >= 0) {
+    e0 = p.step_ptr[nq * p.P + p.kv_shard];
+    e1 = p.step_ptr[nq * p.P + p.kv_shard + 1];
+  } else {
+    e0 = p.step_ptr[nq * p.P];
+    e1 = p.step_ptr[nq * p.P + p.P];
+  }
+  const int T = (int)(e1 - e0);
+  if (T == 0) return;
+
+  WaitCtx w{p.wait_ns, p.err, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int b = 0; b < Q_NUM; ++b)
+      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1) ? 128 : 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tS = tmem_base;         // S fp32 [0,128); dS bf16 in [0,64)
+  const uint32_t tP = tmem_base + 128;   // dP fp32 [128,256)
+  const uint32_t tQ = tmem_base + 256;   // dQ fp32 [256, 256+D)
+  const int kvh = h / p.group;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&p.q_map);
+      tma_prefetch_desc(&p.k_map);
+      tma_prefetch_desc(&p.v_map);
+      tma_prefetch_desc(&p.do_map);
+      mbar_arrive_expect_tx(&bar[Q_QFULL], 2 * kTile);
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
+        tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
+      }
+    }
+    int fills[2] = {0, 0};
+    for (int j = 0; j < T; ++j) {
+      const int s = j & 1;
+      if (j >= 2 && !warp_wait(&bar[Q_KVEMPTY0 + s], ((j >> 1) - 1) & 1, w)) break;
+      const int nk = p.step_col[e0 + j];
+      if (lane == 0) {
+        uint8_t* sK = sK0 + s * 2 * kTile;
+        uint8_t* sV = sK + kTile;
+        mbar_arrive_expect_tx(&bar[Q_KVFULL0 + s], 2 * kTile);
+        for (int a = 0; a < kAtoms; ++a) {
+          tma_load_3d(sK + a * 16384, &p.k_map, &bar[Q_KVFULL0 + s], a * 64, nk * 128, kvh);
+          tma_load_3d(sV + a * 16384, &p.v_map, &bar[Q_KVFULL0 + s], a * 64, nk * 128, kvh);
+        }
+      }
+      ++fills[s];
+    }
+    if (lane == 0) {
+      drain_wait(&bar[Q_QFULL], 0, p.wait_ns, p.err);
+      for (int s = 0; s < 2; ++s)
+        if (fills[s]) drain_wait(&bar[Q_KVFULL0 + s], (fills[s] - 1) & 1, p.wait_ns, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
+      bool ok = mbar_wait(&bar[Q_QFULL], 0, w);
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(&bar[Q_KVFULL0 + s], (j >> 1) & 1, w)) break;
+        if (j > 0 && !mbar_wait(&bar[Q_DQDONE], (j - 1) & 1, w)) break;
+        tc_fence_after();
+        const uint32_t aK = smem_u32(sK0 + s * 2 * kTile), aV = aK + kTile;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024), kIdS,
+                 k > 0);
+        }
+        mma_commit(&bar[Q_SFULL]);
+        if (!mbar_wait(&bar[Q_PFULL], j & 1, w)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tQ, tS + k * 8, sdesc_sw128(aK + k * 2048, 16384, 1024), kIdQ,
+                 (j > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar[Q_DQDONE]);
+        mma_commit(&bar[Q_KVEMPTY0 + s]);
+      }
+      mma_commit(&bar[Q_DRAIN]);
+      drain_wait(&bar[Q_DRAIN], 0, p.wait_ns, p.err);
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+    const int64_t tq = nq * 128 + row;
+    const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
+              pq = p.tracks[3 * n + tq];
+    float lse2 = p.lse[(int64_t)h * n + tq] * kLog2e;
+    if (lse2 == -INFINITY) lse2 = INFINITY;  // a row with no legal key: every P is 0
+    const float dlt = p.delta[(int64_t)h * n + tq];
+    const float sl2 = p.sl2;
+    bool ok = true;
+    int n_partial = 0;
+    for (int j = 0; j < T; ++j) {
+      const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
+      uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};
+      if (partial) {
+        const int b = n_partial & 1;
+        const uint32_t par = (n_partial >> 1) & 1;
+        ++n_partial;
+        int32_t* kt = ktr + b * 512;
+        const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
+        kt[row] = p.tracks[t];
+        kt[128 + row] = p.tracks[n + t];
+        kt[256 + row] = p.tracks[2 * n + t];
+        kt[384 + row] = p.tracks[3 * n + t];
+        mbar_arrive(&bar[Q_TRK0 + b]);
+        if (!mbar_wait(&bar[Q_TRK0 + b], par, w)) { ok = false; break; }
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t bits = 0;
+#pragma unroll
+          for (int t2 = 0; t2 < 32; ++t2) {
+            const int kc = c * 32 + t2;
+            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc], kt[384 + kc],
+                                p.W) ? 1u : 0u) << t2;
+          }
+          lm[c] = bits;
+        }
+      }
+      if (!mbar_wait(&bar[Q_SFULL], j & 1, w)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vs[32], vp[32];
+        tmem_ld32(tS + lb + c * 32, vs);
+        tmem_ld32(tP + lb + c * 32, vp);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const bool l0 = (lm[c] >> t) & 1u, l1 = (lm[c] >> (t + 1)) & 1u;
+          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[t]) * sl2 - lse2) : 0.f;
+          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[t + 1]) * sl2 - lse2) : 0.f;
+          const float d0 = p0 * (__uint_as_float(vp[t]) - dlt);
+          const float d1 = p1 * (__uint_as_float(vp[t + 1]) - dlt);
+          pk[t >> 1] = pack_bf16(d0, d1);
+        }
+        tmem_st16(tS + lb + c * 16, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[Q_PFULL]);
+    }
+    if (ok && !mbar_wait(&bar[Q_DQDONE], (T - 1) & 1, w)) ok = false;
+    tc_fence_after();
+    if (ok) {
+      float* dst = p.dq + (tq * p.hq + h) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tQ + lb + c * 32, v);
+        tmem_ld_wait();
+        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          float4 a = d4[t];
+          a.x += p.scale * __uint_as_float(v[4 * t]);
+          a.y += p.scale * __uint_as_float(v[4 * t + 1]);
+          a.z += p.scale * __uint_as_float(v[4 * t + 2]);
+          a.w += p.scale * __uint_as_float(v[4 * t + 3]);
+          d4[t] = a;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ======================================================================================
+// dK / dV (KV-stationary)
+// ======================================================================================
+enum { K_KVFULL, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL, K_PFULL, K_MMA2, K_DRAIN,
+       K_TRK0, K_TRK1, K_NUM };
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant__ BwdParams p) {
+  constexpr int kTile = 128 * D * 2;
+  constexpr int kAtoms = D / 64;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sK = smem;
+  uint8_t* sV = smem + kTile;
+  uint8_t* sQ0 = smem + 2 * kTile;  // stage s: Q at 2+2s, dO at 3+2s
+  float* stg = reinterpret_cast<float*>(smem + 6 * kTile);  // [2][ lse2[128] | delta[128] ]
+  int32_t* qtr = reinterpret_cast<int32_t*>(smem + 6 * kTile + 2048);  // [2][4][128]
+  __shared__ __align__(8) uint64_t bar[K_NUM];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long n = p.n;
+  int64_t nk;
+  int kh;
+  if (p.kv_shard >= 0) {
+    kh = blockIdx.x / p.bps;
+    nk = (int64_t)p.kv_shard * p.bps + blockIdx.x % p.bps;
+  } else {
+    const int64_t cnt = p.needed_ptr[p.q_shard + 1] - p.needed_ptr[p.q_shard];
+    kh = (int)(blockIdx.x / cnt);
+    nk = p.needed[p.needed_ptr[p.q_shard] + blockIdx.x % cnt];
+  }
+  const int64_t c0 = p.colT_ptr[nk * p.P + p.q_shard];
+  const int L = (int)(p.colT_ptr[nk * p.P + p.q_shard + 1] - c0);
+  const int T = L * p.group;  // items: (q head of the group, listed q block)
+  if (T == 0) return;
+
+  WaitCtx w{p.wait_ns, p.err, &abort_flag};
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int b = 0; b < K_NUM; ++b)
+      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1) ? 128 : 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tS = tmem_base;          // S^T fp32 [0,128); P^T bf16 in [0,64)
+  const uint32_t tP = tmem_base + 128;    // dP^T fp32 [128,256); dS^T bf16 in [128,192)
+  const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
+  const uint32_t tdK = tmem_base + 384;   // dK fp32 [384, 384+D)
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&p.q_map);
+      tma_prefetch_desc(&p.k_map);
+      tma_prefetch_desc(&p.v_map);
+      tma_prefetch_desc(&p.do_map);
+      mbar_arrive_expect_tx(&bar[K_KVFULL], 2 * kTile);
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_3d(sK + a * 16384, &p.k_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
+        tma_load_3d(sV + a * 16384, &p.v_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
+      }
+    }
+    int fills[2] = {0, 0};
+    for (int it = 0; it < T; ++it) {
+      const int s = it & 1;
+      if (it >= 2 && !warp_wait(&bar[K_QEMPTY0 + s], ((it >> 1) - 1) & 1, w)) break;
+      const int h = kh * p.group + it / L;
+      const int nqb = p.colT_row[c0 + it % L];
+      if (lane == 0) {
+        uint8_t* sQ = sQ0 + s * 2 * kTile;
+        uint8_t* sDO = sQ + kTile;
+        mbar_arrive_expect_tx(&bar[K_QFULL0 + s], 2 * kTile);
+        for (int a = 0; a < kAtoms; ++a) {
+          tma_load_3d(sQ + a * 16384, &p.q_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
+          tma_load_3d(sDO + a * 16384, &p.do_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
+        }
+      }
+      ++fills[s];
+    }
+    if (lane == 0) {
+      drain_wait(&bar[K_KVFULL], 0, p.wait_ns, p.err);
+      for (int s = 0; s < 2; ++s)
+        if (fills[s]) drain_wait(&bar[K_QFULL0 + s], (fills[s] - 1) & 1, p.wait_ns, p.err);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
+      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
+      bool ok = mbar_wait(&bar[K_KVFULL], 0, w);
+      for (int it = 0; ok && it < T; ++it) {
+        const int s = it & 1;
+        if (!mbar_wait(&bar[K_QFULL0 + s], (it >> 1) & 1, w)) break;
+        if (it > 0 && !mbar_wait(&bar[K_MMA2], (it - 1) & 1, w)) break;
+        tc_fence_after();
+        const uint32_t aQ = smem_u32(sQ0 + s * 2 * kTile), aDO = aQ + kTile;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024), kIdS, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO + off, 16, 1024), kIdS,
+                 k > 0);
+        }
+        mma_commit(&bar[K_SFULL]);
+        if (!mbar_wait(&bar[K_PFULL], it & 1, w)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tdV, tS + k * 8, sdesc_sw128(aDO + k * 2048, 16384, 1024), kIdAcc,
+                 (it > 0 || k > 0) ? 1u : 0u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ts(tdK, tP + k * 8, sdesc_sw128(aQ + k * 2048, 16384, 1024), kIdAcc,
+                 (it > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&bar[K_MMA2]);
+        mma_commit(&bar[K_QEMPTY0 + s]);
+      }
+      mma_commit(&bar[K_DRAIN]);
+      drain_wait(&bar[K_DRAIN], 0, p.wait_ns, p.err);
+    }
+    __syncwarp();
+  } else {
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;  // kv row of the tile
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
+    const int64_t tk = nk * 128 + row;
+    const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
+              pk = p.tracks[3 * n + tk];
+    const float sl2 = p.sl2;
+    bool ok = true;
+    for (int it = 0; it < T; ++it) {
+      const int h = kh * p.group + it / L;
+      const int64_t e = c0 + it % L;
+      const int64_t qrow = (int64_t)p.colT_row[e] * 128 + row;
+      const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
+      // stage this item's per-query LSE (base 2), delta and, on partial tiles, tracks
+      const int b = it & 1;
+      float* lse2s = stg + b * 256;
+      float* dls = lse2s + 128;
+      int32_t* qt = qtr + b * 512;
+      float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
+      lse2s[row] = (l2 == -INFINITY) ? INFINITY : l2;
+      dls[row] = p.delta[(int64_t)h * n + qrow];
+      if (partial) {
+        qt[row] = p.tracks[qrow];
+        qt[128 + row] = p.tracks[n + qrow];
+        qt[256 + row] = p.tracks[2 * n + qrow];
+        qt[384 + row] = p.tracks[3 * n + qrow];
+      }
+      mbar_arrive(&bar[K_TRK0 + b]);
+      if (!mbar_wait(&bar[K_TRK0 + b], (it >> 1) & 1, w)) { ok = false; break; }
+      uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};
+      if (partial) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t bits = 0;
+#pragma unroll
+          for (int t2 = 0; t2 < 32; ++t2) {
+            const int q = c * 32 + t2;
+            bits |= (mask_legal(qt[q], qt[128 + q], qt[256 + q], qt[384 + q], sk, gk, zk, pk,
+                                p.W) ? 1u : 0u) << t2;
+          }
+          lm[c] = bits;
+        }
+      }
+      if (!mbar_wait(&bar[K_SFULL], it & 1, w)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t vs[32], vp[32];
+        tmem_ld32(tS + lb + c * 32, vs);
+        tmem_ld32(tP + lb + c * 32, vp);
+        tmem_ld_wait();
+        uint32_t pk16[16], dk16[16];
+#pragma unroll
+        for (int t = 0; t < 32; t += 2) {
+          const int q0 = c * 32 + t;
+          const bool l0 = (lm[c] >> t) & 1u, l1 = (lm[c] >> (t + 1)) & 1u;
+          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[t]) * sl2 - lse2s[q0]) : 0.f;
+          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
+          const float d0 = p0 * (__uint_as_float(vp[t]) - dls[q0]);
+          const float d1 = p1 * (__uint_as_float(vp[t + 1]) - dls[q0 + 1]);
+          pk16[t >> 1] = pack_bf16(p0, p1);
+          dk16[t >> 1] = pack_bf16(d0, d1);
+        }
+        tmem_st16(tS + lb + c * 16, pk16);
+        tmem_st16(tP + lb + c * 16, dk16);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bar[K_PFULL]);
+    }
+    if (ok && !mbar_wait(&bar[K_MMA2], (T - 1) & 1, w)) ok = false;
+    tc_fence_after();
+    if (ok) {
+      float* dvr = p.dv + (tk * p.hkv + kh) * D;
+      float* dkr = p.dk + (tk * p.hkv + kh) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32], kk[32];
+        tmem_ld32(tdV + lb + c * 32, v);
+        tmem_ld32(tdK + lb + c * 32, kk);
+        tmem_ld_wait();
+        float4* v4 = reinterpret_cast<float4*>(dvr + c * 32);
+        float4* k4 = reinterpret_cast<float4*>(dkr + c * 32);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          float4 a = v4[t], bb = k4[t];
+          a.x += __uint_as_float(v[4 * t]);
+          a.y += __uint_as_float(v[4 * t + 1]);
+          a.z += __uint_as_float(v[4 * t + 2]);
+          a.w += __uint_as_float(v[4 * t + 3]);
+          bb.x += p.scale * __uint_as_float(kk[4 * t]);
+          bb.y += p.scale * __uint_as_float(kk[4 * t + 1]);
+          bb.z += p.scale * __uint_as_float(kk[4 * t + 2]);
+          bb.w += p.scale * __uint_as_float(kk[4 * t + 3]);
+          v4[t] = a;
+          k4[t] = bb;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+template <int D>
+marble_status_t launch(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
+                       const float* lse, const float* delta, int q_shard, int kv_shard,
+                       float* dq, float* dk, float* dv, cudaStream_t s) {
+  BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  const int64_t n = pl->n;
+  const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_rows_map(&prm.q_map, qkv->q, bf, 2, n, qkv->hq, D, 64, 128, sw) ||
+      !make_rows_map(&prm.k_map, qkv->k, bf, 2, n, qkv->hkv, D, 64, 128, sw) ||
+      !make_rows_map(&prm.v_map, qkv->v, bf, 2, n, qkv->hkv, D, 64, 128, sw) ||
+      !make_rows_map(&prm.do_map, d_o, bf, 2, n, qkv->hq, D, 64, 128, sw))
+    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for Q/K/V/dO");
+  prm.step_ptr = pl->step_ptr;
+  prm.step_col = pl->step_col;
+  prm.step_tag = pl->step_tag;
+  prm.colT_ptr = pl->colT_ptr;
+  prm.colT_row = pl->colT_row;
+  prm.colT_tag = pl->colT_tag;
+  prm.needed_ptr = pl->needed_ptr;
+  prm.needed = pl->needed;
+  prm.tracks = pl->tracks;
+  prm.lse = lse;
+  prm.delta = delta;
+  prm.dq = dq;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.err = pl->err;
+  prm.wait_ns = wait_limit_ns();
+  prm.n = n;
+  prm.P = pl->P;
+  prm.bps = (int)pl->bps;
+  prm.q_shard = q_shard;
+  prm.kv_shard = kv_shard;
+  prm.hq = qkv->hq;
+  prm.hkv = qkv->hkv;
+  prm.group = qkv->hq / qkv->hkv;
+  prm.W = pl->W;
+  prm.scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
+  prm.sl2 = prm.scale * kLog2e;
+  // one CTA per SM: each CTA owns all 512 TMEM columns
+  size_t smem = 6 * (128 * D * 2) + 8192 + 1024;
+  if (smem < 120 * 1024) smem = 120 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
+  k_bwd_dq<D><<<(unsigned)(pl->bps * qkv->hq), kThreads, smem, s>>>(prm);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_bwd_dq");
+  int64_t units;
+  if (kv_shard >= 0) {
+    units = pl->bps * qkv->hkv;
+  } else {
+    units = (pl->h_needed_ptr[q_shard + 1] - pl->h_needed_ptr[q_shard]) * qkv->hkv;
+  }
+  if (units > 0) {
+    k_bwd_dkdv<D><<<(unsigned)units, kThreads, smem, s>>>(prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch k_bwd_dkdv");
+  }
+  return MARBLE_OK;
+}
+
+}  // namespace
+
+marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
+                             const float* lse, const float* delta, int q_shard, int kv_shard,
+                             float* dq, float* dk, float* dv, cudaStream_t s) {
+  if (qkv->d == 128) return launch<128>(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq, dk, dv, s);
+  if (qkv->d == 64) return launch<64>(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq, dk, dv, s);
+  return fail(MARBLE_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+}
+
+}  // namespace marble

@@ -1,0 +1,89 @@
+// Internal declarations shared by the translation units of libmarble (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/marble.h"
+
+namespace marble {
+
+// Per-block summary of the metadata tracks (MARBLE s03 "Block classification"): min and
+// max of each track plus a 64-bit bitmap of the segment ids the block holds.
+struct Summary {
+  int slo, shi;    // sample id
+  int nlo, nhi;    // noise id
+  int glo, ghi;    // segment id over tokens with seg >= 0 (INT_MAX / -1 when none)
+  int plo, phi;    // original position
+  unsigned long long gbits;  // OR of 1 << (seg mod 64) over tokens with seg >= 0
+  int flags;       // bit 0: some token has seg >= 0; bit 1: every token has seg >= 0
+  int pad;
+};
+
+}  // namespace marble
+
+struct marble_plan {
+  int device = 0;
+  int64_t n = 0, nb = 0;
+  int P = 1, W = 0, order = 0, chunk_tokens = 0;
+  int64_t bps = 0;           // blocks per shard
+  int64_t nnz = 0, needed_total = 0;
+  // device arrays (owned)
+  marble::Summary* summ = nullptr;   // [nb], original block order
+  int32_t* band = nullptr;           // [2*nb] candidate kv range per block (lo, hi incl.)
+  int64_t* row_ptr = nullptr;        // [nb+1] tile map, original coordinates
+  int32_t* col = nullptr;            // [nnz]
+  uint8_t* tag = nullptr;            // [nnz]
+  int32_t* block_perm = nullptr;     // [nb] new -> original
+  int32_t* inv_block_perm = nullptr; // [nb] original -> new
+  int32_t* perm = nullptr;           // [n] new token -> original token
+  int32_t* tracks = nullptr;         // [4*n] sample, seg, noise, pos (new order)
+  int64_t* step_ptr = nullptr;       // [nb*P+1]
+  int32_t* step_col = nullptr;       // [nnz]
+  uint8_t* step_tag = nullptr;       // [nnz]
+  int64_t* colT_ptr = nullptr;       // [nb*P+1]
+  int32_t* colT_row = nullptr;       // [nnz]
+  uint8_t* colT_tag = nullptr;       // [nnz]
+  int64_t* needed_ptr = nullptr;     // [P+1]
+  int32_t* needed = nullptr;         // [needed_total]
+  unsigned* err = nullptr;           // device error word
+  unsigned long long* counters = nullptr;  // [8] device scratch for statistics
+  std::vector<int64_t> h_needed_ptr;      // host copy of needed_ptr
+  std::vector<void*> owned;
+};
+
+namespace marble {
+
+// error reporting (api.cu)
+void set_error(const std::string& msg);
+marble_status_t fail(marble_status_t st, const std::string& msg);
+marble_status_t cuda_fail(cudaError_t e, const char* what);
+uint64_t wait_limit_ns();
+
+// planner (plan.cu)
+marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_plan_t* p);
+marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t* pairs,
+                                 int64_t* n_full, int64_t* n_partial);
+
+// elementwise kernels (misc.cu)
+cudaError_t launch_permute(const marble_plan_t* p, const void* src, void* dst, int64_t row_bytes,
+                           int inverse, cudaStream_t s);
+cudaError_t launch_cast_bf16(const float* src, void* dst, int64_t n, cudaStream_t s);
+cudaError_t launch_finalize(const marble_plan_t* p, const float* o_acc, const float* m,
+                            const float* l, int hq, int d, void* o, float* lse, cudaStream_t s);
+cudaError_t launch_bwd_prep(const marble_plan_t* p, const void* o, const void* d_o, int hq, int d,
+                            float* delta, cudaStream_t s);
+cudaError_t launch_debug_wait(unsigned* err, uint64_t limit_ns, cudaStream_t s);
+
+// attention (attn_fwd.cu, attn_bwd.cu)
+marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int q_shard,
+                             int kv_shard, const marble_state_t* st, uint32_t flags,
+                             cudaStream_t s);
+marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
+                             const float* lse, const float* delta, int q_shard, int kv_shard,
+                             float* dq, float* dk, float* dv, cudaStream_t s);
+
+}  // namespace marble

@@ -1,0 +1,651 @@
+// Mask-metadata -> tile map planner, token order and per-step tile lists, all on device.
+//
+// MARBLE post, s03 "Block classification": per 128-token block, cheap summaries (min/max
+// of every track and a small segment bitmap) let one test per block pair decide whether
+// the pair is full (provably all legal), empty (provably none legal) or partial.  s03
+// "PTRR": sort query blocks by cost, deal them to ranks in rounds of R with every other
+// round reversed, keep each rank's blocks in sequence order.  s03 "Chunked ring
+// attention": PTRR's rule over contiguous chunks.  s04 "Sparse all-to-all": the key/value
+// blocks each rank's queries need.  s04 "Layout transforms": tokens are permuted once and
+// carry their metadata and original position.
+//
+// The candidate band: sample ids are non-decreasing along the pack, so every block
+// outside [first block whose max sample >= this block's min sample, last block whose min
+// sample <= this block's max sample] has a disjoint sample range and is empty by the
+// sample test; classification only visits the band.
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace marble {
+namespace {
+
+constexpr int kWarpsPerCta = 8;
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// ------------------------------------------------------------------------------------
+// a1 + a2: validation and block summaries (one warp per block, 4 tokens per lane)
+// ------------------------------------------------------------------------------------
+__global__ void k_summaries(const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
+                            const int32_t* __restrict__ noise, int64_t nb,
+                            Summary* __restrict__ out, unsigned* err) {
+  const int lane = threadIdx.x & 31;
+  const int64_t b = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (b >= nb) return;
+  const int64_t t0 = b * kBlock + lane * 4;
+  int slo = INT_MAX, shi = INT_MIN, nlo = INT_MAX, nhi = INT_MIN, glo = INT_MAX, ghi = -1;
+  unsigned blo = 0, bhi = 0;
+  bool any_seg = false, all_seg = true, bad = false;
+  int prev = t0 > 0 ? sample[t0 - 1] : INT_MIN;
+  for (int i = 0; i < 4; ++i) {
+    const int s = sample[t0 + i], g = seg[t0 + i], z = noise[t0 + i];
+    bad |= (s < 0) | (g < -1) | (z < -1) | (s < prev);
+    prev = s;
+    slo = min(slo, s); shi = max(shi, s);
+    nlo = min(nlo, z); nhi = max(nhi, z);
+    if (g >= 0) {
+      any_seg = true;
+      glo = min(glo, g); ghi = max(ghi, g);
+      const int bit = g & 63;
+      if (bit < 32) blo |= 1u << bit; else bhi |= 1u << (bit - 32);
+    } else {
+      all_seg = false;
+    }
+  }
+  const unsigned full = 0xffffffffu;
+  slo = __reduce_min_sync(full, slo); shi = __reduce_max_sync(full, shi);
+  nlo = __reduce_min_sync(full, nlo); nhi = __reduce_max_sync(full, nhi);
+  glo = __reduce_min_sync(full, glo); ghi = __reduce_max_sync(full, ghi);
+  blo = __reduce_or_sync(full, blo); bhi = __reduce_or_sync(full, bhi);
+  const bool has = __any_sync(full, any_seg);
+  const bool all = __all_sync(full, all_seg);
+  if (__any_sync(full, bad) && lane == 0) atomicOr(err, kErrBadTracks);
+  if (lane == 0) {
+    Summary r;
+    r.slo = slo; r.shi = shi; r.nlo = nlo; r.nhi = nhi; r.glo = glo; r.ghi = ghi;
+    r.plo = (int)(b * kBlock); r.phi = (int)(b * kBlock + kBlock - 1);
+    r.gbits = ((unsigned long long)bhi << 32) | blo;
+    r.flags = (has ? 1 : 0) | (all ? 2 : 0);
+    r.pad = 0;
+    out[b] = r;
+  }
+}
+
+// candidate band [lo, hi] of every block by binary search over the non-decreasing
+// per-block sample bounds
+__global__ void k_band(const Summary* __restrict__ s, int64_t nb, int32_t* __restrict__ band) {
+  const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (a >= nb) return;
+  const int slo = s[a].slo, shi = s[a].shi;
+  int64_t lo = 0, hi = a;  // first b with s[b].shi >= slo (b <= a holds)
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (s[mid].shi >= slo) hi = mid; else lo = mid + 1;
+  }
+  band[2 * a] = (int32_t)lo;
+  lo = a; hi = nb;  // first b with s[b].slo > shi
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (s[mid].slo > shi) hi = mid; else lo = mid + 1;
+  }
+  band[2 * a + 1] = (int32_t)(lo - 1);
+}
+
+// a3: the summary rule (full = 1, partial = 2, empty = 0) for q block A, k block B
+__device__ __forceinline__ int classify(const Summary& A, const Summary& B, int W) {
+  const bool samp_all = A.slo == A.shi && A.shi == B.slo && B.slo == B.shi;
+  const bool samp_none = A.shi < B.slo || B.shi < A.slo;
+  const bool caus_all = (A.plo - B.phi >= 0) && (A.phi - B.plo < W);
+  const bool caus_none = (A.phi - B.plo < 0) || (A.plo - B.phi >= W);
+  const bool hasA = A.flags & 1, hasB = B.flags & 1;
+  const bool allA = A.flags & 2, allB = B.flags & 2;
+  const bool span_all = allA && allB && A.glo == A.ghi && A.ghi == B.glo && B.glo == B.ghi;
+  const bool span_none =
+      !hasA || !hasB || (A.gbits & B.gbits) == 0ull || A.ghi < B.glo || B.ghi < A.glo;
+  const bool noise_all =
+      B.nhi < 0 || (A.nlo == A.nhi && A.nhi == B.nlo && B.nlo == B.nhi && B.nhi >= 0);
+  const bool noise_none = B.nlo >= 0 && (A.nhi < B.nlo || B.nhi < A.nlo);
+  if (samp_none || noise_none || (caus_none && span_none)) return 0;
+  if (samp_all && noise_all && (caus_all || span_all)) return MARBLE_TILE_FULL;
+  return MARBLE_TILE_PARTIAL;
+}
+
+// one warp per q block: count non-empty tiles of the row
+__global__ void k_tiles_count(const Summary* __restrict__ s, const int32_t* __restrict__ band,
+                              int64_t nb, int W, int32_t* __restrict__ cnt) {
+  const int lane = threadIdx.x & 31;
+  const int64_t a = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (a >= nb) return;
+  const Summary A = s[a];
+  const int lo = band[2 * a], hi = band[2 * a + 1];
+  int c = 0;
+  for (int b0 = lo; b0 <= hi; b0 += 32) {
+    const int b = b0 + lane;
+    const int t = b <= hi ? classify(A, s[b], W) : 0;
+    c += __popc(__ballot_sync(0xffffffffu, t != 0));
+  }
+  if (lane == 0) cnt[a] = c;
+}
+
+// one warp per q block: write the row's tiles in ascending kv block order
+__global__ void k_tiles_write(const Summary* __restrict__ s, const int32_t* __restrict__ band,
+                              const int64_t* __restrict__ row_ptr, int64_t nb, int W,
+                              int32_t* __restrict__ col, uint8_t* __restrict__ tag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t a = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (a >= nb) return;
+  const Summary A = s[a];
+  const int lo = band[2 * a], hi = band[2 * a + 1];
+  int64_t out = row_ptr[a];
+  for (int b0 = lo; b0 <= hi; b0 += 32) {
+    const int b = b0 + lane;
+    const int t = b <= hi ? classify(A, s[b], W) : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, t != 0);
+    if (t) {
+      const int64_t o = out + __popc(m & lanemask_lt());
+      col[o] = b;
+      tag[o] = (uint8_t)t;
+    }
+    out += __popc(m);
+  }
+}
+
+// exclusive scan of n counters into out[0..n] (out[n] = total); one CTA, each thread owns
+// a contiguous chunk
+template <typename T>
+__global__ void k_scan(const T* __restrict__ in, int64_t n, int64_t* __restrict__ out) {
+  __shared__ int64_t ws[32];
+  const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31, wid = tid >> 5;
+  const int64_t per = (n + nt - 1) / nt;
+  const int64_t a = min(n, (int64_t)tid * per), b = min(n, a + per);
+  int64_t sum = 0;
+  for (int64_t i = a; i < b; ++i) sum += (int64_t)in[i];
+  int64_t x = sum;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) ws[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int64_t y = lane < (nt >> 5) ? ws[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
+    }
+    ws[lane] = y;
+  }
+  __syncthreads();
+  int64_t run = (wid ? ws[wid - 1] : 0) + x - sum;
+  for (int64_t i = a; i < b; ++i) {
+    out[i] = run;
+    run += (int64_t)in[i];
+  }
+  if (tid == nt - 1) out[n] = run;
+}
+
+// ------------------------------------------------------------------------------------
+// a4: order
+// ------------------------------------------------------------------------------------
+__global__ void k_unit_cost(const int32_t* __restrict__ cnt, int ub, int64_t units,
+                            int32_t* __restrict__ ucost) {
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  int c = 0;
+  for (int i = 0; i < ub; ++i) c += cnt[u * ub + i];
+  ucost[u] = c;
+}
+
+// PTRR rank of every unit: its position in the (cost desc, index asc) order decides the
+// round t and slot i; even rounds deal slots to ranks 0..P-1, odd rounds to P-1..0.
+__global__ void k_ptrr_rank(const int32_t* __restrict__ ucost, int64_t U, int P,
+                            int32_t* __restrict__ rank_of) {
+  __shared__ int32_t tile[1024];
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int cu = u < U ? ucost[u] : 0;
+  int64_t pos = 0;
+  for (int64_t v0 = 0; v0 < U; v0 += 1024) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+      tile[i] = (v0 + i < U) ? ucost[v0 + i] : INT_MIN;
+    __syncthreads();
+    const int lim = (int)min((int64_t)1024, U - v0);
+    for (int i = 0; i < lim; ++i) {
+      const int cv = tile[i];
+      pos += (cv > cu) || (cv == cu && v0 + i < u);
+    }
+  }
+  if (u < U) {
+    const int64_t t = pos / P, i = pos % P;
+    rank_of[u] = (int32_t)((t & 1) ? (P - 1 - i) : i);
+  }
+}
+
+// slot of every unit inside its rank: ascending unit index
+__global__ void k_ptrr_place(const int32_t* __restrict__ rank_of, int64_t U, int P,
+                             int32_t* __restrict__ unit_new) {
+  __shared__ int32_t tile[1024];
+  const int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int ru = u < U ? rank_of[u] : -1;
+  int64_t idx = 0;
+  const int64_t last = min(U, ((int64_t)blockIdx.x + 1) * blockDim.x);
+  for (int64_t v0 = 0; v0 < last; v0 += 1024) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < 1024; i += blockDim.x)
+      tile[i] = (v0 + i < U) ? rank_of[v0 + i] : -2;
+    __syncthreads();
+    const int lim = (int)min((int64_t)1024, U - v0);
+    for (int i = 0; i < lim; ++i) idx += (v0 + i < u) && (tile[i] == ru);
+  }
+  if (u < U) unit_new[u] = (int32_t)((int64_t)ru * (U / P) + idx);
+}
+
+__global__ void k_block_perm(const int32_t* __restrict__ unit_new, int ub, int64_t nb,
+                             int32_t* __restrict__ block_perm, int32_t* __restrict__ inv) {
+  const int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= nb) return;
+  const int64_t nbk = unit_new ? (int64_t)unit_new[b / ub] * ub + (b % ub) : b;
+  block_perm[nbk] = (int32_t)b;
+  inv[b] = (int32_t)nbk;
+}
+
+__global__ void k_perm_tracks(const int32_t* __restrict__ block_perm,
+                              const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
+                              const int32_t* __restrict__ noise, int64_t n,
+                              int32_t* __restrict__ perm, int32_t* __restrict__ tracks) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const int64_t o = (int64_t)block_perm[t >> 7] * kBlock + (t & (kBlock - 1));
+  perm[t] = (int32_t)o;
+  tracks[t] = sample[o];
+  tracks[n + t] = seg[o];
+  tracks[2 * n + t] = noise[o];
+  tracks[3 * n + t] = (int32_t)o;
+}
+
+// ------------------------------------------------------------------------------------
+// a5: per-step lists
+// ------------------------------------------------------------------------------------
+// rows: new q block nq (forward / dQ lists keyed (nq, kv shard j))
+__global__ void k_step_count(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                             const int32_t* __restrict__ block_perm,
+                             const int32_t* __restrict__ inv, int64_t nb, int P, int64_t bps,
+                             int32_t* __restrict__ cnt) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nq = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (nq >= nb) return;
+  const int64_t qb = block_perm[nq];
+  const int64_t a = row_ptr[qb], e = row_ptr[qb + 1];
+  for (int64_t i0 = a; i0 < e; i0 += 32) {
+    const int64_t i = i0 + lane;
+    const bool ok = i < e;
+    const unsigned act = __ballot_sync(0xffffffffu, ok);
+    if (ok) {
+      const int j = (int)(inv[col[i]] / bps);
+      const unsigned peers = __match_any_sync(act, j);
+      if ((peers & lanemask_lt()) == 0) atomicAdd(&cnt[nq * P + j], __popc(peers));
+    }
+  }
+}
+
+__global__ void k_step_write(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                             const uint8_t* __restrict__ tag,
+                             const int32_t* __restrict__ block_perm,
+                             const int32_t* __restrict__ inv, int64_t nb, int P, int64_t bps,
+                             const int64_t* __restrict__ step_ptr, int32_t* __restrict__ out_col,
+                             uint8_t* __restrict__ out_tag) {
+  extern __shared__ int64_t offs_all[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int64_t* offs = offs_all + (int64_t)w * P;
+  const int64_t nq = (int64_t)blockIdx.x * kWarpsPerCta + w;
+  if (nq >= nb) return;
+  for (int j = lane; j < P; j += 32) offs[j] = step_ptr[nq * P + j];
+  __syncwarp();
+  const int64_t qb = block_perm[nq];
+  const int64_t a = row_ptr[qb], e = row_ptr[qb + 1];
+  for (int64_t i0 = a; i0 < e; i0 += 32) {
+    const int64_t i = i0 + lane;
+    const bool ok = i < e;
+    const unsigned act = __ballot_sync(0xffffffffu, ok);
+    int j = 0;
+    unsigned peers = 0;
+    int64_t o = 0;
+    if (ok) {
+      const int nk = inv[col[i]];
+      j = (int)(nk / bps);
+      peers = __match_any_sync(act, j);
+      o = offs[j] + __popc(peers & lanemask_lt());
+      out_col[o] = nk;
+      out_tag[o] = tag[i];
+    }
+    __syncwarp();
+    if (ok && (peers & lanemask_lt()) == 0) offs[j] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// columns: original kv block B (dK/dV lists keyed (nk, q shard r)), visiting the band of
+// q blocks in ascending original order and classifying (A, B) directly
+template <bool kWrite>
+__global__ void k_colT(const Summary* __restrict__ s, const int32_t* __restrict__ band,
+                       const int32_t* __restrict__ inv, int64_t nb, int W, int P, int64_t bps,
+                       int32_t* __restrict__ cnt, const int64_t* __restrict__ colT_ptr,
+                       int32_t* __restrict__ out_row, uint8_t* __restrict__ out_tag) {
+  extern __shared__ int64_t offs_all[];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t b = (int64_t)blockIdx.x * kWarpsPerCta + w;
+  if (b >= nb) return;
+  const int64_t nk = inv[b];
+  int64_t* offs = offs_all + (int64_t)w * P;
+  if (kWrite) {
+    for (int r = lane; r < P; r += 32) offs[r] = colT_ptr[nk * P + r];
+    __syncwarp();
+  }
+  const Summary B = s[b];
+  const int lo = band[2 * b], hi = band[2 * b + 1];  // the band is symmetric
+  for (int a0 = lo; a0 <= hi; a0 += 32) {
+    const int a = a0 + lane;
+    const int t = a <= hi ? classify(s[a], B, W) : 0;
+    const unsigned act = __ballot_sync(0xffffffffu, t != 0);
+    int r = 0;
+    unsigned peers = 0;
+    if (t) {
+      const int nq = inv[a];
+      r = (int)(nq / bps);
+      peers = __match_any_sync(act, r);
+      if (kWrite) {
+        const int64_t o = offs[r] + __popc(peers & lanemask_lt());
+        out_row[o] = nq;
+        out_tag[o] = (uint8_t)t;
+      } else if ((peers & lanemask_lt()) == 0) {
+        atomicAdd(&cnt[nk * P + r], __popc(peers));
+      }
+    }
+    if (kWrite) {
+      __syncwarp();
+      if (t && (peers & lanemask_lt()) == 0) offs[r] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// needed kv blocks of q shard r = kv blocks with a non-empty (kv block, r) list
+template <bool kWrite>
+__global__ void k_needed(const int64_t* __restrict__ colT_ptr, int64_t nb, int P,
+                         int32_t* __restrict__ count, const int64_t* __restrict__ needed_ptr,
+                         int32_t* __restrict__ needed) {
+  __shared__ int ws[32];
+  __shared__ int64_t carry;
+  const int r = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) carry = kWrite ? needed_ptr[r] : 0;
+  __syncthreads();
+  for (int64_t k0 = 0; k0 < nb; k0 += blockDim.x) {
+    const int64_t k = k0 + tid;
+    const int f = (k < nb) && (colT_ptr[k * P + r + 1] > colT_ptr[k * P + r]);
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) ws[wid] = __popc(m);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) {
+      if (i < wid) before += ws[i];
+      total += ws[i];
+    }
+    if (kWrite && f) needed[carry + before + __popc(m & lanemask_lt())] = (int32_t)k;
+    __syncthreads();
+    if (tid == 0) carry += total;
+    __syncthreads();
+  }
+  if (!kWrite && tid == 0) count[r] = (int32_t)carry;
+}
+
+// ------------------------------------------------------------------------------------
+// statistics: legal pairs (full tiles 128*128, partial tiles evaluated pair by pair)
+// ------------------------------------------------------------------------------------
+__global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                              const uint8_t* __restrict__ tag, const int32_t* __restrict__ inv,
+                              const int32_t* __restrict__ tracks, int64_t n, int64_t nb, int W,
+                              unsigned long long* __restrict__ acc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  const int32_t* smp = tracks;
+  const int32_t* sg = tracks + n;
+  const int32_t* nz = tracks + 2 * n;
+  const int32_t* ps = tracks + 3 * n;
+  unsigned long long legal = 0, nfull = 0, npart = 0;
+  for (int64_t qb = warp0; qb < nb; qb += nwarps) {
+    const int64_t qn = (int64_t)inv[qb] * kBlock;
+    for (int64_t e = row_ptr[qb]; e < row_ptr[qb + 1]; ++e) {
+      if (tag[e] == MARBLE_TILE_FULL) {
+        if (lane == 0) { legal += kBlock * kBlock; ++nfull; }
+        continue;
+      }
+      if (lane == 0) ++npart;
+      const int64_t kn = (int64_t)inv[col[e]] * kBlock;
+      for (int qi = lane; qi < kBlock; qi += 32) {
+        const int64_t q = qn + qi;
+        const int sq = smp[q], gq = sg[q], zq = nz[q], pq = ps[q];
+        int c = 0;
+        for (int ki = 0; ki < kBlock; ++ki) {
+          const int64_t k = kn + ki;
+          const int dp = pq - ps[k];
+          const bool causal = dp >= 0 && dp < W;
+          const bool span = gq >= 0 && sg[k] == gq;
+          const bool keep = nz[k] < 0 || nz[k] == zq;
+          c += (causal || span) && keep && smp[k] == sq;
+        }
+        legal += c;
+      }
+    }
+  }
+  for (int o = 16; o; o >>= 1) {
+    legal += __shfl_xor_sync(0xffffffffu, legal, o);
+  }
+  if (lane == 0) {
+    atomicAdd(&acc[0], legal);
+    atomicAdd(&acc[1], nfull);
+    atomicAdd(&acc[2], npart);
+  }
+}
+
+inline unsigned grid_for(int64_t items, int per_cta) {
+  return (unsigned)((items + per_cta - 1) / per_cta);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------------------------
+// host driver
+// ------------------------------------------------------------------------------------
+#define MARBLE_CK(call)                                   \
+  do {                                                    \
+    cudaError_t e_ = (call);                              \
+    if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+  } while (0)
+
+template <typename T>
+static marble_status_t dalloc(marble_plan_t* p, T** ptr, size_t count) {
+  void* q = nullptr;
+  const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
+  cudaError_t e = cudaMalloc(&q, bytes);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return fail(MARBLE_ERR_OOM, "cudaMalloc of plan workspace failed (" +
+                                    std::to_string(bytes) + " bytes)");
+  }
+  p->owned.push_back(q);
+  *ptr = static_cast<T*>(q);
+  return MARBLE_OK;
+}
+
+#define MARBLE_TRY(x)                     \
+  do {                                    \
+    marble_status_t st_ = (x);            \
+    if (st_ != MARBLE_OK) return st_;     \
+  } while (0)
+
+marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_plan_t* p) {
+  const int64_t n = p->n, nb = p->nb;
+  const int P = p->P, W = p->W;
+  const int64_t bps = p->bps;
+  const int threads = 256;
+  const int warp_ctas = (int)grid_for(nb, kWarpsPerCta);
+
+  MARBLE_TRY(dalloc(p, &p->err, 4));
+  MARBLE_TRY(dalloc(p, &p->counters, 8));
+  MARBLE_TRY(dalloc(p, &p->summ, nb));
+  MARBLE_TRY(dalloc(p, &p->band, 2 * nb));
+  MARBLE_TRY(dalloc(p, &p->row_ptr, nb + 1));
+  MARBLE_TRY(dalloc(p, &p->block_perm, nb));
+  MARBLE_TRY(dalloc(p, &p->inv_block_perm, nb));
+  MARBLE_TRY(dalloc(p, &p->perm, n));
+  MARBLE_TRY(dalloc(p, &p->tracks, 4 * n));
+  MARBLE_TRY(dalloc(p, &p->step_ptr, nb * P + 1));
+  MARBLE_TRY(dalloc(p, &p->colT_ptr, nb * P + 1));
+  MARBLE_TRY(dalloc(p, &p->needed_ptr, P + 1));
+  // scratch: counters of the two-pass compactions and the order builder
+  int32_t *cnt = nullptr, *cnt2 = nullptr, *cntT = nullptr, *ucost = nullptr,
+          *rank_of = nullptr, *unit_new = nullptr, *ncount = nullptr;
+  std::vector<void*> scratch;
+  auto salloc = [&](int32_t** ptr, size_t count) -> marble_status_t {
+    void* q = nullptr;
+    cudaError_t e = cudaMalloc(&q, (count ? count : 1) * sizeof(int32_t));
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(MARBLE_ERR_OOM, "cudaMalloc of planner scratch failed");
+    }
+    scratch.push_back(q);
+    *ptr = static_cast<int32_t*>(q);
+    return MARBLE_OK;
+  };
+  struct Freer {
+    std::vector<void*>* v;
+    ~Freer() {
+      for (void* q : *v) cudaFree(q);
+    }
+  } freer{&scratch};
+  const int ub = (p->order == MARBLE_ORDER_PTRR_CHUNK) ? p->chunk_tokens / kBlock : 1;
+  const int64_t units = nb / ub;
+  MARBLE_TRY(salloc(&cnt, nb));
+  MARBLE_TRY(salloc(&cnt2, nb * P));
+  MARBLE_TRY(salloc(&cntT, nb * P));
+  MARBLE_TRY(salloc(&ucost, units));
+  MARBLE_TRY(salloc(&rank_of, units));
+  MARBLE_TRY(salloc(&unit_new, units));
+  MARBLE_TRY(salloc(&ncount, P));
+
+  MARBLE_CK(cudaMemsetAsync(p->err, 0, 4 * sizeof(unsigned), s));
+  MARBLE_CK(cudaMemsetAsync(p->counters, 0, 8 * sizeof(unsigned long long), s));
+  MARBLE_CK(cudaMemsetAsync(cnt2, 0, nb * P * sizeof(int32_t), s));
+  MARBLE_CK(cudaMemsetAsync(cntT, 0, nb * P * sizeof(int32_t), s));
+
+  // a1 + a2
+  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(d->sample_id, d->seg_id, d->noise_id, nb,
+                                                      p->summ, p->err);
+  MARBLE_CK(cudaGetLastError());
+  unsigned herr = 0;
+  MARBLE_CK(cudaMemcpyAsync(&herr, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaStreamSynchronize(s));
+  if (herr & kErrBadTracks)
+    return fail(MARBLE_ERR_INVALID_ARG,
+                "metadata check failed: sample ids must be >= 0 and non-decreasing, seg and "
+                "noise ids >= -1");
+
+  // a3
+  k_band<<<grid_for(nb, threads), threads, 0, s>>>(p->summ, nb, p->band);
+  k_tiles_count<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->summ, p->band, nb, W, cnt);
+  k_scan<int32_t><<<1, 1024, 0, s>>>(cnt, nb, p->row_ptr);
+  MARBLE_CK(cudaGetLastError());
+  int64_t nnz = 0;
+  MARBLE_CK(cudaMemcpyAsync(&nnz, p->row_ptr + nb, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaStreamSynchronize(s));
+  p->nnz = nnz;
+  MARBLE_TRY(dalloc(p, &p->col, nnz));
+  MARBLE_TRY(dalloc(p, &p->tag, nnz));
+  MARBLE_TRY(dalloc(p, &p->step_col, nnz));
+  MARBLE_TRY(dalloc(p, &p->step_tag, nnz));
+  MARBLE_TRY(dalloc(p, &p->colT_row, nnz));
+  MARBLE_TRY(dalloc(p, &p->colT_tag, nnz));
+  k_tiles_write<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->summ, p->band, p->row_ptr, nb, W,
+                                                        p->col, p->tag);
+  MARBLE_CK(cudaGetLastError());
+
+  // a4
+  if (p->order == MARBLE_ORDER_CONTIGUOUS) {
+    k_block_perm<<<grid_for(nb, threads), threads, 0, s>>>(nullptr, 1, nb, p->block_perm,
+                                                            p->inv_block_perm);
+  } else {
+    k_unit_cost<<<grid_for(units, threads), threads, 0, s>>>(cnt, ub, units, ucost);
+    k_ptrr_rank<<<grid_for(units, threads), threads, 0, s>>>(ucost, units, P, rank_of);
+    k_ptrr_place<<<grid_for(units, threads), threads, 0, s>>>(rank_of, units, P, unit_new);
+    k_block_perm<<<grid_for(nb, threads), threads, 0, s>>>(unit_new, ub, nb, p->block_perm,
+                                                            p->inv_block_perm);
+  }
+  k_perm_tracks<<<grid_for(n, threads), threads, 0, s>>>(p->block_perm, d->sample_id, d->seg_id,
+                                                          d->noise_id, n, p->perm, p->tracks);
+  MARBLE_CK(cudaGetLastError());
+
+  // a5: forward lists
+  const size_t offs_smem = (size_t)kWarpsPerCta * P * sizeof(int64_t);
+  k_step_count<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->row_ptr, p->col, p->block_perm,
+                                                       p->inv_block_perm, nb, P, bps, cnt2);
+  k_scan<int32_t><<<1, 1024, 0, s>>>(cnt2, nb * P, p->step_ptr);
+  k_step_write<<<warp_ctas, 32 * kWarpsPerCta, offs_smem, s>>>(
+      p->row_ptr, p->col, p->tag, p->block_perm, p->inv_block_perm, nb, P, bps, p->step_ptr,
+      p->step_col, p->step_tag);
+  MARBLE_CK(cudaGetLastError());
+  // column lists
+  k_colT<false><<<warp_ctas, 32 * kWarpsPerCta, offs_smem, s>>>(
+      p->summ, p->band, p->inv_block_perm, nb, W, P, bps, cntT, nullptr, nullptr, nullptr);
+  k_scan<int32_t><<<1, 1024, 0, s>>>(cntT, nb * P, p->colT_ptr);
+  k_colT<true><<<warp_ctas, 32 * kWarpsPerCta, offs_smem, s>>>(
+      p->summ, p->band, p->inv_block_perm, nb, W, P, bps, nullptr, p->colT_ptr, p->colT_row,
+      p->colT_tag);
+  MARBLE_CK(cudaGetLastError());
+  // needed index
+  k_needed<false><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, ncount, nullptr, nullptr);
+  k_scan<int32_t><<<1, 1024, 0, s>>>(ncount, P, p->needed_ptr);
+  MARBLE_CK(cudaGetLastError());
+  int64_t ntot = 0;
+  MARBLE_CK(cudaMemcpyAsync(&ntot, p->needed_ptr + P, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaStreamSynchronize(s));
+  p->needed_total = ntot;
+  p->h_needed_ptr.resize(P + 1);
+  MARBLE_CK(cudaMemcpyAsync(p->h_needed_ptr.data(), p->needed_ptr, (P + 1) * sizeof(int64_t),
+                            cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaStreamSynchronize(s));
+  MARBLE_TRY(dalloc(p, &p->needed, ntot));
+  k_needed<true><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, nullptr, p->needed_ptr, p->needed);
+  MARBLE_CK(cudaGetLastError());
+  MARBLE_CK(cudaStreamSynchronize(s));
+  return MARBLE_OK;
+}
+
+marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t* pairs,
+                                 int64_t* n_full, int64_t* n_partial) {
+  MARBLE_CK(cudaMemsetAsync(p->counters, 0, 3 * sizeof(unsigned long long), s));
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const unsigned ctas = (unsigned)std::min<int64_t>(grid_for(p->nb, kWarpsPerCta), 8 * sms);
+  k_legal_pairs<<<ctas, 32 * kWarpsPerCta, 0, s>>>(p->row_ptr, p->col, p->tag,
+                                                   p->inv_block_perm, p->tracks, p->n, p->nb,
+                                                   p->W, p->counters);
+  MARBLE_CK(cudaGetLastError());
+  unsigned long long h[3] = {0, 0, 0};
+  MARBLE_CK(cudaMemcpyAsync(h, p->counters, sizeof(h), cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaStreamSynchronize(s));
+  *pairs = (int64_t)h[0];
+  *n_full = (int64_t)h[1];
+  *n_partial = (int64_t)h[2];
+  return MARBLE_OK;
+}
+
+}  // namespace marble

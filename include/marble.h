@@ -1,0 +1,299 @@
+/*
+ * marble.h -- C ABI of a single-GPU (GB300, sm_103a) library for exact, mask-aware
+ * blockwise attention over packed multimodal sequences, carrying the online-softmax
+ * state (O, m, l) in fp32 across a sequence of key/value shards ("ring steps" run
+ * back to back on one GPU).
+ *
+ * Sources for the operations (cited by page title and section):
+ *   [MARBLE]  "MARBLE: exact sequence parallelism for packed multimodal masks"
+ *             (Luma AI): s01 "Packed multimodal masks" (four per-token tracks and the
+ *             mask_mod predicate), s03 "Block classification", "PTRR: balancing ring
+ *             attention steps", "Exact ring attention accumulation", s04 "Sparse
+ *             all-to-all and strategy selection", "Layout transforms", "Planning cost".
+ *   [RING]    "RingAttention and Context Parallelism: Mathematical Foundations ..."
+ *             (llms.blog): "The Online Softmax Formulation", "Execution Algorithm".
+ *   [LIBRA]   "Libra: Taming Attention Workload Skew ..." (arXiv 2607.23250):
+ *             s2.2 Eq. 1 (CoreAttn = softmax(QK^T/sqrt(d_h) + M) V).
+ *
+ * Conventions for every call
+ *   - Pointers named "device" must be CUDA device pointers (or managed memory) on the
+ *     device that was current when the plan was created; "host" pointers are ordinary
+ *     host memory.  Export/copy calls accept either (the copy direction is inferred).
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream) unless
+ *     stated otherwise.  Arguments are validated before anything is launched; an invalid
+ *     argument returns MARBLE_ERR_INVALID_ARG and launches nothing.
+ *   - The caller owns every tensor it passes.  A plan owns only its own device
+ *     workspace, allocated by marble_plan and freed by marble_plan_destroy.  No other
+ *     call allocates memory.
+ *   - No C++ exception crosses this boundary.  marble_last_error() returns a
+ *     thread-local, human-readable message for the last failing call on this thread.
+ *   - Every wait inside a kernel is bounded in time; a wait that runs out sets an error
+ *     word owned by the plan and the kernel returns.  marble_check() reports it as
+ *     MARBLE_ERR_TIMEOUT.  Asynchronous CUDA faults surface as MARBLE_ERR_CUDA.
+ *
+ * Token order and layouts
+ *   - The plan's tracks are given in ORIGINAL order; the original position of a token
+ *     is its index (pos = index).  marble_plan computes a token permutation (`perm`,
+ *     new index -> original index).  All attention tensors below are in the plan's NEW
+ *     order: the caller gathers Q/K/V (and dO) with marble_permute first and scatters
+ *     results back with marble_permute(..., inverse = 1).
+ *   - Virtual shard r holds new tokens [r*N/P, (r+1)*N/P), i.e. new blocks
+ *     [r*nb/P, (r+1)*nb/P) with nb = N/128.
+ *   - Q, O, dO: bf16 [N, Hq, d]; K, V: bf16 [N, Hkv, d]; token-major, contiguous.
+ *     O_acc, dQ_acc: fp32 [N, Hq, d]; dK_acc, dV_acc: fp32 [N, Hkv, d].
+ *     m, l, LSE, delta: fp32 [Hq, N].
+ *     All base pointers must be 16-byte aligned.
+ *   - Grouped-query attention: q head h reads kv head h / (Hq / Hkv).
+ *   - Supported head dims: d = 64 and d = 128.  Hq must be a multiple of Hkv.
+ */
+#ifndef MARBLE_H_
+#define MARBLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st *marble_stream_t;
+
+typedef enum {
+  MARBLE_OK = 0,
+  MARBLE_ERR_INVALID_ARG = 1, /* bad pointer, size, layout or metadata */
+  MARBLE_ERR_UNSUPPORTED = 2, /* valid request outside what this build implements */
+  MARBLE_ERR_CUDA = 3,        /* a CUDA runtime/driver call or a kernel failed */
+  MARBLE_ERR_OOM = 4,         /* plan workspace allocation failed */
+  MARBLE_ERR_TIMEOUT = 5      /* a bounded in-kernel wait ran out (see marble_check) */
+} marble_status_t;
+
+#define MARBLE_BLOCK 128               /* tokens per block (MARBLE s03) */
+#define MARBLE_WINDOW_INF 2147483647   /* W for globally causal layers */
+#define MARBLE_TILE_FULL 1             /* every pair provably legal: no mask evaluated */
+#define MARBLE_TILE_PARTIAL 2          /* mixed: the mask predicate runs per pair */
+#define MARBLE_KV_NEEDED (-1)          /* kv_shard value: every needed KV block at once */
+#define MARBLE_STEP_FIRST 1u           /* flags bit: this is the first step of the rows */
+
+typedef enum {
+  MARBLE_ORDER_CONTIGUOUS = 0, /* identity order: shard r = contiguous token range */
+  MARBLE_ORDER_PTRR_BLOCK = 1, /* PTRR over 128-token blocks (MARBLE s03 "PTRR") */
+  MARBLE_ORDER_PTRR_CHUNK = 2  /* PTRR over contiguous chunks of chunk_tokens tokens
+                                  (MARBLE s03 "Chunked ring attention") */
+} marble_order_t;
+
+/*
+ * Plan descriptor.  MARBLE s01: four integers per token encode the packed mask -- a
+ * sample id, a segment id shared by the tokens of one bidirectional span (or of all
+ * spans of one image group), a noise-group id for generated spans, and the original
+ * position (here: the index).  The predicate is
+ *   allowed(q, k) = (0 <= pos[q]-pos[k] < W  or  seg[q] == seg[k] >= 0)
+ *                   and (noise[k] < 0 or noise[q] == noise[k]) and sample[q] == sample[k].
+ * Requirements (checked; MARBLE_ERR_INVALID_ARG otherwise):
+ *   n_tokens > 0, a multiple of 128, < 2^31;
+ *   sample_id non-decreasing along the pack and >= 0 (each sample one contiguous run);
+ *   seg_id >= -1, noise_id >= -1 (-1 = none);
+ *   window >= 0 (MARBLE_WINDOW_INF for global layers);
+ *   1 <= num_shards <= 256 and nb % num_shards == 0;
+ *   PTRR_CHUNK: chunk_tokens a positive multiple of 128 dividing n_tokens, and the
+ *   number of chunks divisible by num_shards.
+ * The three track arrays are device int32[n_tokens]; they are read during marble_plan
+ * only (the plan keeps its own permuted copy).
+ */
+typedef struct {
+  int64_t n_tokens;
+  const int32_t *sample_id;
+  const int32_t *seg_id;
+  const int32_t *noise_id;
+  int32_t window;
+  int32_t num_shards;
+  int32_t order;        /* marble_order_t */
+  int32_t chunk_tokens; /* PTRR_CHUNK only */
+} marble_plan_desc_t;
+
+typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
+
+/*
+ * Build a plan on the current device (MARBLE s03 "Block classification", "PTRR";
+ * s04 "Sparse all-to-all", "Layout transforms"; s04 "Planning cost": a plan depends only
+ * on the metadata and is reused by every layer, forward and backward).
+ * Steps, all in CUDA kernels: validate the tracks; per-block summaries (min/max of each
+ * track plus a 64-bit segment bitmap); classify every block pair of the candidate band
+ * as full / partial / empty from the summaries alone; per-row cost = non-empty tiles;
+ * token order (contiguous or PTRR); permuted tracks; per (q block, kv shard) tile lists
+ * for the forward and dQ, per (kv block, q shard) lists for dK/dV, and the needed-KV
+ * block index of every q shard.
+ * Synchronises `stream` a few times (to size its arrays).  On success *out owns device
+ * memory until marble_plan_destroy.  Errors: INVALID_ARG (descriptor or metadata),
+ * UNSUPPORTED, OOM, CUDA.
+ */
+marble_status_t marble_plan(const marble_plan_desc_t *desc, marble_stream_t stream,
+                            marble_plan_t **out);
+
+/* Frees the plan (synchronises the device first).  NULL is accepted. */
+marble_status_t marble_plan_destroy(marble_plan_t *plan);
+
+typedef struct {
+  int64_t n_tokens, n_blocks, num_shards;
+  int64_t nnz;          /* non-empty tiles */
+  int64_t n_full, n_partial;
+  int64_t legal_pairs;  /* legal (q, k) pairs of the mask, per head */
+  int64_t shard_cost_max, shard_cost_sum; /* non-empty tiles per q shard: max, sum */
+  int64_t step_cost;    /* sum_s max_r W[r, (r-s) mod P], W in tiles (MARBLE s03,
+                           chunk-layout cost C without the per-range term) */
+  int64_t needed_total; /* sum over q shards of needed kv blocks */
+  int64_t needed_remote;/* ... of which lie outside the q shard's own kv shard */
+} marble_plan_stats_t;
+
+/* Plan statistics; counts legal pairs with a kernel over the partial tiles (full tiles
+ * contribute 128*128 each).  Synchronises `stream`. */
+marble_status_t marble_plan_stats(const marble_plan_t *plan, marble_stream_t stream,
+                                  marble_plan_stats_t *out);
+
+typedef enum {
+  MARBLE_FIELD_PERM = 0,         /* int32[N]   new token -> original token */
+  MARBLE_FIELD_BLOCK_PERM = 1,   /* int32[nb]  new block -> original block */
+  MARBLE_FIELD_TRACKS_PERM = 2,  /* int32[4][N] sample, seg, noise, pos in new order */
+  MARBLE_FIELD_TILE_ROWPTR = 3,  /* int64[nb+1] tile map CSR, ORIGINAL block coords */
+  MARBLE_FIELD_TILE_COL = 4,     /* int32[nnz]  original kv block, ascending per row */
+  MARBLE_FIELD_TILE_TAG = 5,     /* uint8[nnz]  MARBLE_TILE_FULL / MARBLE_TILE_PARTIAL */
+  MARBLE_FIELD_STEP_PTR = 6,     /* int64[nb*P+1] list of (new q block i, kv shard j)
+                                    at [ptr[i*P+j], ptr[i*P+j+1]) */
+  MARBLE_FIELD_STEP_COL = 7,     /* int32[nnz] new kv block, ascending per list */
+  MARBLE_FIELD_STEP_TAG = 8,     /* uint8[nnz] */
+  MARBLE_FIELD_COLT_PTR = 9,     /* int64[nb*P+1] list of (new kv block k, q shard r)
+                                    at [ptr[k*P+r], ptr[k*P+r+1]) */
+  MARBLE_FIELD_COLT_ROW = 10,    /* int32[nnz] new q block, ascending per list */
+  MARBLE_FIELD_COLT_TAG = 11,    /* uint8[nnz] */
+  MARBLE_FIELD_NEEDED_PTR = 12,  /* int64[P+1] */
+  MARBLE_FIELD_NEEDED = 13       /* int32[needed_total] sorted unique new kv blocks that
+                                    q shard r's rows need (local blocks included) */
+} marble_field_t;
+
+/* Size in bytes of an exported field (host call, no synchronisation). */
+marble_status_t marble_plan_field_bytes(const marble_plan_t *plan, int32_t field,
+                                        size_t *bytes);
+
+/* Copy a plan field to `dst` (host or device), asynchronously on `stream`.  `bytes`
+ * must equal marble_plan_field_bytes(). */
+marble_status_t marble_plan_export(const marble_plan_t *plan, int32_t field, void *dst,
+                                   size_t bytes, marble_stream_t stream);
+
+/*
+ * Gather (inverse = 0: dst[i] = src[perm[i]]) or scatter (inverse = 1:
+ * dst[perm[i]] = src[i]) rows of `row_bytes` bytes per token between original and plan
+ * order (MARBLE s04 "Layout transforms").  src and dst are device pointers of
+ * N * row_bytes bytes that must not overlap; row_bytes must be a positive multiple of 4
+ * and both pointers 16-byte aligned.
+ */
+marble_status_t marble_permute(const marble_plan_t *plan, const void *src, void *dst,
+                               int64_t row_bytes, int32_t inverse, marble_stream_t stream);
+
+/* Queries, keys and values in plan order (layouts above). scale <= 0 selects 1/sqrt(d)
+ * (LIBRA Eq. 1). */
+typedef struct {
+  const void *q; /* device bf16 [N, hq, d] */
+  const void *k; /* device bf16 [N, hkv, d] */
+  const void *v; /* device bf16 [N, hkv, d] */
+  int32_t hq, hkv, d;
+  float scale;
+} marble_qkv_t;
+
+/* Online-softmax state of every (token, q head), caller-owned, plan order.
+ * o_acc: unnormalised fp32 accumulator [N, hq, d]; m: running row maximum of the
+ * scaled scores, kept in base-2 units (score * scale * log2(e)); l: running row sum of
+ * exp2(score*scale*log2(e) - m).  (O_acc, m, l) always satisfy O_acc = sum_k 2^(s_k - m) v_k
+ * and l = sum_k 2^(s_k - m) over the keys seen so far. */
+typedef struct {
+  float *o_acc; /* device fp32 [N, hq, d] */
+  float *m;     /* device fp32 [hq, N] */
+  float *l;     /* device fp32 [hq, N] */
+} marble_state_t;
+
+/*
+ * One ring step of the forward (MARBLE s03 "Exact ring attention accumulation";
+ * RING "The Online Softmax Formulation"): for every row of q shard `q_shard` and every
+ * q head, process the tiles the plan lists between the row's block and kv shard
+ * `kv_shard` (or, with kv_shard == MARBLE_KV_NEEDED, every tile of the row: one pass
+ * over the local and needed remote blocks, MARBLE s04) and update (O_acc, m, l) in
+ * fp32.  Full tiles skip the mask; partial tiles evaluate the predicate per pair; empty
+ * tiles are never loaded.
+ * flags & MARBLE_STEP_FIRST: the state of this shard's rows is uninitialised; every row
+ * of the shard starts from (O = 0, m = -inf, l = 0), including rows with no tile in this
+ * step (which are written as such).  Otherwise the stored state is resumed.
+ * The ring pairing of MARBLE s03 is kv_shard = (q_shard - s) mod P at step s; any order
+ * of the P kv shards gives the same result up to fp32 rounding.
+ * Errors: INVALID_ARG (shard out of range, null/misaligned pointer, d not 64/128,
+ * hq % hkv != 0), CUDA.
+ */
+marble_status_t marble_attn_step(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                 int32_t q_shard, int32_t kv_shard,
+                                 const marble_state_t *state, uint32_t flags,
+                                 marble_stream_t stream);
+
+/*
+ * Normalise once at the end (MARBLE s03: "only the last call normalizes the output,
+ * writes the LSE and casts to bf16"):  O = O_acc / l as bf16 [N, hq, d] and
+ * LSE = ln(sum_k exp(s_k)) = (m + log2 l) * ln 2 as fp32 [hq, N].  A row with l = 0 (no
+ * legal key) gives O = 0 and LSE = -inf.  Covers all N tokens.
+ */
+marble_status_t marble_attn_finalize(const marble_plan_t *plan, const marble_state_t *state,
+                                     int32_t hq, int32_t d, void *o_bf16, float *lse,
+                                     marble_stream_t stream);
+
+/* Backward preprocessing: delta = rowsum(dO * O) as fp32 [hq, N] from bf16 O and dO
+ * (the O emitted by marble_attn_finalize). */
+marble_status_t marble_attn_bwd_prep(const marble_plan_t *plan, const void *o,
+                                     const void *d_o, int32_t hq, int32_t d, float *delta,
+                                     marble_stream_t stream);
+
+/*
+ * One ring step of the backward (MARBLE s03: each step runs the attention backward
+ * against the FINAL LSE; the fp32 dQ accumulator is carried across steps and each kv
+ * shard's fp32 dK/dV accumulators travel with the shard; s03 closing rule: gradients
+ * summed across calls are summed in fp32).  For the tiles between q shard `q_shard` and
+ * kv shard `kv_shard` (or every tile of the q shard's rows with MARBLE_KV_NEEDED):
+ *   P = exp(S*scale - LSE), dV += P^T dO, dP = dO V^T, dS = P * (dP - delta),
+ *   dK += scale * dS^T Q, dQ += scale * dS K,
+ * accumulated in place into dq_acc [N, hq, d], dk_acc / dv_acc [N, hkv, d] (fp32).
+ * The accumulators must be zeroed by the caller before the first step.
+ * flags: reserved, pass 0.
+ */
+marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                const void *d_o, const float *lse, const float *delta,
+                                int32_t q_shard, int32_t kv_shard, float *dq_acc,
+                                float *dk_acc, float *dv_acc, uint32_t flags,
+                                marble_stream_t stream);
+
+/* Cast fp32 -> bf16 (round to nearest even) for n elements, e.g. gradient accumulators;
+ * n must be a multiple of 4 and both pointers 16-byte aligned. */
+marble_status_t marble_cast_bf16(const float *src, void *dst, int64_t n,
+                                 marble_stream_t stream);
+
+/*
+ * Synchronise `stream` and report the plan's device error word: MARBLE_ERR_TIMEOUT if a
+ * bounded in-kernel wait ran out since the last check (the word is then cleared),
+ * MARBLE_ERR_CUDA on an asynchronous CUDA error, MARBLE_OK otherwise.
+ */
+marble_status_t marble_check(const marble_plan_t *plan, marble_stream_t stream);
+
+/* Upper bound, in nanoseconds, on every in-kernel wait of later launches in this
+ * process (default 2e9 ns; also read once from env MARBLE_WAIT_LIMIT_MS). */
+marble_status_t marble_set_wait_limit_ns(uint64_t ns);
+
+/* Test hook: launch one CTA that waits, with the normal bounded wait, on a barrier that
+ * nothing completes; it gives up after `limit_ns` and sets the plan's error word, so a
+ * following marble_check returns MARBLE_ERR_TIMEOUT.  Nothing faults or hangs. */
+marble_status_t marble_debug_wait_timeout(const marble_plan_t *plan, uint64_t limit_ns,
+                                          marble_stream_t stream);
+
+/* Thread-local message describing the last error on this thread ("" if none). */
+const char *marble_last_error(void);
+
+/* Library version string. */
+const char *marble_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MARBLE_H_ */

@@ -104,24 +104,26 @@ def rows_forward(q, k, v, tr, W, rows, heads=None, scale=None):
     # group rows by sample run
     keys = st[rows]
     for a in np.unique(keys):
-        sel = np.flatnonzero(keys == a)
-        b = int(en[rows[sel[0]]])
+        sel_all = np.flatnonzero(keys == a)
+        b = int(en[rows[sel_all[0]]])
         kk = np.arange(int(a), b)
-        m = allowed(tr, W, rows[sel][:, None], kk[None, :])
-        qs = _f64(q[rows[sel]])
         ks = _f64(k[int(a):b])
         vs = _f64(v[int(a):b])
-        for hi, h in enumerate(heads):
-            kh = h // g
-            S = (qs[:, h, :] @ ks[:, kh, :].T) * scale
-            S = np.where(m, S, -np.inf)
-            mx = S.max(axis=1)
-            has = np.isfinite(mx)
-            E = np.exp(S - np.where(has, mx, 0)[:, None])
-            l = E.sum(axis=1)
-            O[sel, hi, :] = np.where(has[:, None],
-                                     (E @ vs[:, kh, :]) / np.where(has, l, 1)[:, None], 0)
-            LSE[hi, sel] = np.where(has, mx + np.log(np.where(has, l, 1)), -np.inf)
+        for c0 in range(0, len(sel_all), 512):
+            sel = sel_all[c0:c0 + 512]
+            m = allowed(tr, W, rows[sel][:, None], kk[None, :])
+            qs = _f64(q[rows[sel]])
+            for hi, h in enumerate(heads):
+                kh = h // g
+                S = (qs[:, h, :] @ ks[:, kh, :].T) * scale
+                S = np.where(m, S, -np.inf)
+                mx = S.max(axis=1)
+                has = np.isfinite(mx)
+                E = np.exp(S - np.where(has, mx, 0)[:, None])
+                l = E.sum(axis=1)
+                O[sel, hi, :] = np.where(has[:, None],
+                                         (E @ vs[:, kh, :]) / np.where(has, l, 1)[:, None], 0)
+                LSE[hi, sel] = np.where(has, mx + np.log(np.where(has, l, 1)), -np.inf)
     return O, LSE
 
 

@@ -1,0 +1,86 @@
+"""Helpers shared by the GPU tests: run the CUDA path through the Python binding of the
+C ABI and bring results back to original token order for comparison with the oracle."""
+import numpy as np
+import torch
+
+import context_attention_metadata_gb300 as M
+import workloads as wl
+
+TOL_O_MAX = 2e-2
+TOL_O_MEAN = 2e-3
+TOL_LSE = 1e-3
+TOL_GRAD_REL = 1e-2
+
+
+def device_tracks(tr):
+    return [torch.as_tensor(np.asarray(tr[k], np.int32)).cuda() for k in ("sample", "seg", "noise")]
+
+
+def make_plan(tr, W, P, order="contiguous", chunk_tokens=0):
+    s, g, z = device_tracks(tr)
+    return M.Plan(s, g, z, W, P, order, chunk_tokens)
+
+
+def plan_for(cfg, tr):
+    return make_plan(tr, cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens)
+
+
+def run_forward(pl, q, k, v, needed=False, schedule=None):
+    """q/k/v in ORIGINAL order on the GPU.  Returns (O, LSE, state) with O [N, hq, d]
+    and LSE [hq, N] in original order and the raw state in plan order."""
+    n, hq, d = q.shape
+    qp, kp, vp = pl.permute(q), pl.permute(k), pl.permute(v)
+    st = M.State(n, hq, d)
+    o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    if schedule is None:
+        M.forward(pl, qp, kp, vp, st, o, lse, needed=needed)
+    else:
+        for r, j, first in schedule:
+            M.attn_step(pl, qp, kp, vp, r, j, st, first=first)
+        M.attn_finalize(pl, st, o, lse)
+    pl.check()
+    perm = pl.export("perm").long()
+    O = pl.permute(o, inverse=True)
+    LSE = torch.empty_like(lse)
+    LSE[:, perm] = lse
+    return O, LSE, st
+
+
+def run_backward(pl, q, k, v, do, needed=False):
+    """Full forward + backward through the C ABI; gradients in original order (fp32)."""
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    qp, kp, vp, dop = pl.permute(q), pl.permute(k), pl.permute(v), pl.permute(do)
+    st = M.State(n, hq, d)
+    o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    M.forward(pl, qp, kp, vp, st, o, lse, needed=needed)
+    delta = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    dq = torch.zeros((n, hq, d), dtype=torch.float32, device="cuda")
+    dk = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    dv = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=needed)
+    pl.check()
+    return (pl.permute(dq, inverse=True), pl.permute(dk, inverse=True),
+            pl.permute(dv, inverse=True))
+
+
+def check_o_lse(O, LSE, O_ref, LSE_ref):
+    O = O.float().cpu().numpy()
+    LSE = LSE.cpu().numpy()
+    err = np.abs(O - O_ref)
+    assert err.max() <= TOL_O_MAX, f"O max abs err {err.max()}"
+    assert err.mean() <= TOL_O_MEAN, f"O mean abs err {err.mean()}"
+    fin = np.isfinite(LSE_ref)
+    assert (np.isfinite(LSE) == fin).all(), "LSE -inf pattern differs"
+    if fin.any():
+        e = np.abs(LSE[fin] - LSE_ref[fin]).max()
+        assert e <= TOL_LSE, f"LSE abs err {e}"
+    return float(err.max()), float(err.mean())
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))

@@ -447,3 +447,30 @@ def test_step_lists_partition_the_tile_map(order):
     # permuted tracks carry the original positions
     assert (pl.tracks_perm["pos"] == pl.perm).all()
     assert (pl.tracks_perm["sample"] == tr["sample"][pl.perm]).all()
+
+
+# --------------------------------------------------------------------------------------
+# sampled-row / sampled-column oracle paths agree with the dense oracle
+# --------------------------------------------------------------------------------------
+def test_sampled_rows_and_columns_equal_dense():
+    rng = np.random.default_rng(21)
+    n = 900
+    tr = wl.random_pack(rng, n, max_samples=4)
+    W = 120
+    M = mask.dense_mask(tr, W)
+    q, k, v = _rand_qkv(rng, n, 4, 2, 8)
+    do = rng.standard_normal(q.shape)
+    dq, dk, dv, O, L = attention.backward(q, k, v, do, M)
+    rows = np.sort(rng.choice(n, 200, replace=False))
+    O2, L2 = attention.rows_forward(q, k, v, tr, W, rows)
+    assert np.abs(O2 - O[rows]).max() < 1e-12
+    fin = np.isfinite(L[:, rows])
+    assert (np.isfinite(L2) == fin).all() and np.abs(L2[fin] - L[:, rows][fin]).max() < 1e-12
+    dq2 = attention.rows_dq(q, k, v, do, tr, W, rows)
+    assert np.abs(dq2 - dq[rows]).max() < 1e-10
+    cols = np.sort(rng.choice(n, 60, replace=False))
+    dk2, dv2 = attention.cols_backward(q, k, v, do, tr, W, cols)
+    assert np.abs(dk2 - dk[cols]).max() < 1e-10
+    assert np.abs(dv2 - dv[cols]).max() < 1e-10
+    dk3, dv3 = attention.cols_backward(q, k, v, do, tr, W, cols, kv_heads=[1])
+    assert np.abs(dk3[:, 0] - dk[cols, 1]).max() < 1e-10

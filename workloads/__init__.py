@@ -223,7 +223,7 @@ def mini_config(cid: int, n: int = 16384, hq: Optional[int] = None,
     window = c.window if c.window == WINDOW_INF else min(c.window, n // 8)
     chunk = 0
     if c.order == "ptrr_chunk":
-        chunk = max(BLOCK, n // (4 * c.shards)) // BLOCK * BLOCK
+        chunk = max(BLOCK, n // (2 * c.shards)) // BLOCK * BLOCK
     return dataclasses.replace(c, name=c.name + f"_mini{n}", n=n, hq=hq, hkv=hkv,
                                window=window, chunk_tokens=chunk)
 
