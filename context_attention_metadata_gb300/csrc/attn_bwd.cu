@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         kt[256 + row] = p.tracks[2 * n + t];
         kt[384 + row] = p.tracks[3 * n + t];
         mbar_arrive(&bar[Q_TRK0 + b]);
-        if (!mbar_wait(&bar[Q_TRK0 + b], par, w)) { ok = false; break; }
+        if (!wait_all(&bar[Q_TRK0 + b], par, w)) { ok = false; break; }
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t bits = 0;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
           lm[c] = bits;
         }
       }
-      if (!mbar_wait(&bar[Q_SFULL], j & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[Q_SFULL], j & 1, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -245,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bar[Q_PFULL]);
     }
-    if (ok && !mbar_wait(&bar[Q_DQDONE], (T - 1) & 1, w)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !wait_all(&bar[Q_DQDONE], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
     if (ok) {
       float* dst = p.dq + (tq * p.hq + h) * D;
@@ -437,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         qt[384 + row] = p.tracks[3 * n + qrow];
       }
       mbar_arrive(&bar[K_TRK0 + b]);
-      if (!mbar_wait(&bar[K_TRK0 + b], (it >> 1) & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[K_TRK0 + b], (it >> 1) & 1, w)) { ok = false; break; }
       uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};
       if (partial) {
 #pragma unroll 1
@@ -452,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
           lm[c] = bits;
         }
       }
-      if (!mbar_wait(&bar[K_SFULL], it & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[K_SFULL], it & 1, w)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
@@ -479,7 +480,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bar[K_PFULL]);
     }
-    if (ok && !mbar_wait(&bar[K_MMA2], (T - 1) & 1, w)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !wait_all(&bar[K_MMA2], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
     if (ok) {
       float* dvr = p.dv + (tk * p.hkv + kh) * D;

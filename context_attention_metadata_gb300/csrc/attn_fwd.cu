@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
         kt[256 + row] = p.tracks[2 * n + t];
         kt[384 + row] = p.tracks[3 * n + t];
         mbar_arrive(&bar[B_TRK0 + b]);
-        if (!mbar_wait(&bar[B_TRK0 + b], par, w)) { ok = false; break; }
+        if (!wait_all(&bar[B_TRK0 + b], par, w)) { ok = false; break; }
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t bits = 0;
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
           lm[c] = bits;
         }
       }
-      if (!mbar_wait(&bar[B_SFULL], j & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[B_SFULL], j & 1, w)) { ok = false; break; }
       tc_fence_after();
       // pass 1: row maximum of the scaled, masked scores
       float mx = -INFINITY;
@@ -266,24 +266,28 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
       // exact power of two, and bf16 rounding of P does not depend on which keys a step
       // happened to see first
       const float m_new = ceilf(mx);
-      if (m_new > m_run + kRescaleThreshold) {
-        if (m_run != -INFINITY) {
-          // rescale what the earlier tiles of this call accumulated (j >= 1 here)
-          const float alpha = ldexpf(1.f, (int)(m_run - m_new));
-          l_run *= alpha;
-          if (!mbar_wait(&bar[B_OFULL], (j - 1) & 1, w)) { ok = false; break; }
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t v[32];
-            tmem_ld32(tO + lb + c * 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-            tmem_st32(tO + lb + c * 32, v);
-          }
-        }
+      const bool grow = m_new > m_run + kRescaleThreshold;
+      const bool need = grow && (m_run != -INFINITY);  // earlier tiles of this call to rescale
+      const float alpha = need ? ldexpf(1.f, (int)(m_run - m_new)) : 1.f;
+      if (grow) {
+        l_run *= alpha;
         m_run = m_new;
+      }
+      // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
+      // must (alpha = 1 on the others).  A row that needs it has a finite max from an
+      // earlier tile, so j >= 1 and PV_{j-1} is the accumulation to wait for.
+      if (__any_sync(0xffffffffu, need)) {
+        if (!wait_all(&bar[B_OFULL], (j - 1) & 1, w)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + lb + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+          tmem_st32(tO + lb + c * 32, v);
+        }
       }
       // pass 2: P = exp2(s - m_run) as bf16 into TMEM over the consumed S columns
       const float base = (m_run == -INFINITY) ? 0.f : m_run;
@@ -311,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
       mbar_arrive(&bar[B_PFULL]);
     }
     // epilogue: merge this call's (O, m, l) with the stored state (or start it)
-    if (ok && !mbar_wait(&bar[B_OFULL], (T - 1) & 1, w)) ok = false;
+    ok = __all_sync(0xffffffffu, ok);
+    if (ok && !wait_all(&bar[B_OFULL], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
     if (ok) {
       const int64_t gi = (int64_t)h * n + tq;

@@ -120,6 +120,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// bounded wait whose result is the same on every lane of the warp (each lane polls and
+// acquires; if any lane gave up, all report failure).  Used by warps whose next step is a
+// warp-collective tcgen05 instruction, so that a timeout never splits the warp.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, const WaitCtx& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // the packed-mask predicate of MARBLE s01 for one (query, key) pair of tracks
 __device__ __forceinline__ bool mask_legal(int sq, int gq, int zq, int pq, int sk, int gk, int zk,
                                            int pk, int W) {

@@ -75,25 +75,26 @@ def test_full_configs_backward_sampled(cid):
     q, k, v, do = wl.make_qkvdo(cfg.n, cfg.hq, cfg.hkv, cfg.d, device="cuda")
     pl = plan_for(cfg, tr)
     dq, dk, dv = run_backward(pl, q, k, v, do, needed=cfg.needed)
+    for g in (dq, dk, dv):
+        assert torch.isfinite(g).all()
+    qc, kc, vc, dc = (t.cpu() for t in (q, k, v, do))
     rng = np.random.default_rng(10 + cid)
-    big = cid >= 4
-    rows = np.sort(rng.choice(cfg.n, 64 if big else 256, replace=False))
+    st = np.asarray(tr["sample"])
+    lengths = np.bincount(st)
+    # rows and key columns from samples small enough for the fp64 oracle to finish quickly
+    small = np.flatnonzero(lengths[st] <= 8192)
+    pool = small if len(small) >= 64 else np.arange(cfg.n)
+    rows = np.sort(rng.choice(pool, 48, replace=False))
     heads = np.array([0, cfg.hq - 1])
-    ref = attention.rows_dq(q, k, v, do, tr, cfg.window, rows, heads=heads)
+    ref = attention.rows_dq(qc, kc, vc, dc, tr, cfg.window, rows, heads=heads)
     got = dq[torch.as_tensor(rows).cuda()][:, torch.as_tensor(heads).cuda()].cpu().double().numpy()
     assert rel_fro(got, ref) <= TOL_GRAD_REL
-    # key columns whose visible-query sets stay small enough for the oracle
-    if big:
-        st = np.asarray(tr["sample"])
-        lengths = np.bincount(st)
-        ok = np.flatnonzero(lengths[st] <= 20000)
-        cols = np.sort(rng.choice(ok, 16, replace=False))
-    else:
-        cols = np.sort(rng.choice(cfg.n, 48, replace=False))
+    # eight consecutive key columns (their visible-query sets overlap)
+    c0 = int(rng.choice(pool))
+    c0 = min(c0, cfg.n - 8)
+    cols = np.arange(c0, c0 + 8)
     kvh = np.array([0])
-    rk, rv = attention.cols_backward(q, k, v, do, tr, cfg.window, cols, kv_heads=kvh)
+    rk, rv = attention.cols_backward(qc, kc, vc, dc, tr, cfg.window, cols, kv_heads=kvh)
     c_t = torch.as_tensor(cols).cuda()
-    gk = dk[c_t][:, :1].cpu().double().numpy()
-    gv = dv[c_t][:, :1].cpu().double().numpy()
-    assert rel_fro(gk, rk) <= TOL_GRAD_REL
-    assert rel_fro(gv, rv) <= TOL_GRAD_REL
+    assert rel_fro(dk[c_t][:, :1].cpu().double().numpy(), rk) <= TOL_GRAD_REL
+    assert rel_fro(dv[c_t][:, :1].cpu().double().numpy(), rv) <= TOL_GRAD_REL
