@@ -89,6 +89,10 @@ _SIGS = {
     "marble_check": ([ctypes.c_void_p, ctypes.c_void_p]),
     "marble_set_wait_limit_ns": ([ctypes.c_uint64]),
     "marble_debug_wait_timeout": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
+    "marble_tile_map_static": ([ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                ctypes.c_void_p]),
     "marble_last_error": ([]),
     "marble_version": ([]),
 }
@@ -292,6 +296,23 @@ def set_wait_limit_ns(ns: int):
 
 def debug_wait_timeout(plan: Plan, limit_ns: int, stream=None):
     _call("marble_debug_wait_timeout", plan.handle, int(limit_ns), _stream(stream))
+
+
+TILE_MAP_STATIC_MAX_TOKENS = 2097152
+
+
+def tile_map_static(sample, seg, noise, window: int, row_ptr, col, tag, stream=None):
+    """Global tile map into caller-provided CUDA tensors without any allocation by the
+    library (marble_tile_map_static): row_ptr int64[nb+1], col int32[cap], tag uint8[cap]."""
+    import torch
+    n = int(sample.shape[0])
+    for t, nm in ((sample, "sample"), (seg, "seg"), (noise, "noise")):
+        _need(t, torch.int32, nm, (n,))
+    _need(row_ptr, torch.int64, "row_ptr", (n // BLOCK + 1,))
+    _need(col, torch.int32, "col")
+    _need(tag, torch.uint8, "tag", (col.numel(),))
+    _call("marble_tile_map_static", n, _ptr(sample), _ptr(seg), _ptr(noise), int(window),
+          _ptr(row_ptr), _ptr(col), _ptr(tag), col.numel(), _stream(stream))
 
 
 def ring_schedule(num_shards: int, needed: bool = False):

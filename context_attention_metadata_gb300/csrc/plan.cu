@@ -14,6 +14,8 @@
 // sample <= this block's max sample] has a disjoint sample range and is empty by the
 // sample test; classification only visits the band.
 #include <climits>
+#include <mutex>
+#include <string>
 
 #include "common.cuh"
 #include "internal.h"
@@ -649,3 +651,126 @@ marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t
 }
 
 }  // namespace marble
+
+// ======================================================================================
+// Tile map into caller buffers, without allocating
+// ======================================================================================
+// Some callers cannot call cudaMalloc: a planner that runs for every packed batch on a
+// data-loader stream while the previous training step is still running must not pay the
+// device-wide synchronisation cudaMalloc may imply, and a process whose device memory is
+// owned by another allocator (a framework's caching allocator that has reserved the pool,
+// or a fixed per-process budget) cannot obtain memory outside it.  For them,
+// marble_tile_map_static builds the global tile map with the same kernels as marble_plan,
+// keeping its intermediate scratch (per-block summaries, candidate bands, per-row counts
+// and a validation word) in the file-scope array below instead of allocated memory.  The
+// array is part of the module image: every GPU that loads the library holds it until the
+// process exits.
+namespace marble {
+namespace {
+
+constexpr int64_t kStaticMaxBlocks = MARBLE_TILE_MAP_STATIC_MAX_TOKENS / kBlock;
+constexpr size_t kStaticSummaryBytes = kStaticMaxBlocks * sizeof(Summary);
+constexpr size_t kStaticBandBytes = kStaticMaxBlocks * 2 * sizeof(int32_t);
+constexpr size_t kStaticCountBytes = kStaticMaxBlocks * sizeof(int32_t);
+constexpr size_t kStaticScratchBytes =
+    kStaticSummaryBytes + kStaticBandBytes + kStaticCountBytes + 256;
+
+// In host code this name is only a host-side stand-in for the device array: its address
+// must be obtained with cudaGetSymbolAddress on each device (see static_scratch()).
+static __device__ __align__(256) unsigned char g_tile_map_scratch[kStaticScratchBytes];
+
+// writes the tiles of each row whose CSR index is below `capacity`
+__global__ void k_tiles_write_capped(const Summary* __restrict__ s,
+                                     const int32_t* __restrict__ band,
+                                     const int64_t* __restrict__ row_ptr, int64_t nb, int W,
+                                     int64_t capacity, int32_t* __restrict__ col,
+                                     uint8_t* __restrict__ tag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t a = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (a >= nb) return;
+  const Summary A = s[a];
+  const int lo = band[2 * a], hi = band[2 * a + 1];
+  int64_t out = row_ptr[a];
+  for (int b0 = lo; b0 <= hi; b0 += 32) {
+    const int b = b0 + lane;
+    const int t = b <= hi ? classify(A, s[b], W) : 0;
+    const unsigned m = __ballot_sync(0xffffffffu, t != 0);
+    if (t) {
+      const int64_t o = out + __popc(m & lanemask_lt());
+      if (o < capacity) {
+        col[o] = b;
+        tag[o] = (uint8_t)t;
+      }
+    }
+    out += __popc(m);
+  }
+}
+
+// metadata that failed validation is reported in the output itself: row_ptr[0] = -1
+__global__ void k_flag_invalid(const unsigned* __restrict__ err, int64_t* __restrict__ row_ptr) {
+  if (threadIdx.x == 0 && (*err & kErrBadTracks)) row_ptr[0] = -1;
+}
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[64] = {};
+
+// Device address of the scratch array on the current device, looked up once per device.
+marble_status_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(MARBLE_ERR_UNSUPPORTED, "device ordinal >= 64");
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_tile_map_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(tile-map scratch)");
+    g_scratch_addr[dev] = ptr;
+  }
+  *out = g_scratch_addr[dev];
+  return MARBLE_OK;
+}
+
+}  // namespace
+}  // namespace marble
+
+extern "C" __attribute__((visibility("default"))) marble_status_t marble_tile_map_static(
+    int64_t n_tokens, const int32_t* sample_id, const int32_t* seg_id, const int32_t* noise_id,
+    int32_t window, int64_t* row_ptr, int32_t* col, uint8_t* tag, int64_t capacity,
+    marble_stream_t stream) {
+  using namespace marble;
+  if (n_tokens <= 0 || n_tokens % kBlock)
+    return fail(MARBLE_ERR_INVALID_ARG, "n_tokens must be a positive multiple of 128");
+  if (n_tokens > MARBLE_TILE_MAP_STATIC_MAX_TOKENS)
+    return fail(MARBLE_ERR_INVALID_ARG,
+                "n_tokens exceeds MARBLE_TILE_MAP_STATIC_MAX_TOKENS (" +
+                    std::to_string((long long)MARBLE_TILE_MAP_STATIC_MAX_TOKENS) +
+                    "), the size of the static scratch; use marble_plan instead");
+  if (window < 0) return fail(MARBLE_ERR_INVALID_ARG, "window must be >= 0");
+  if (capacity < 0) return fail(MARBLE_ERR_INVALID_ARG, "capacity must be >= 0");
+  if (!sample_id || !seg_id || !noise_id || !row_ptr || (capacity > 0 && (!col || !tag)))
+    return fail(MARBLE_ERR_INVALID_ARG, "null pointer");
+  void* base = nullptr;
+  marble_status_t st = static_scratch(&base);
+  if (st != MARBLE_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int64_t nb = n_tokens / kBlock;
+  unsigned char* scratch = static_cast<unsigned char*>(base);
+  Summary* summ = reinterpret_cast<Summary*>(scratch);
+  int32_t* band = reinterpret_cast<int32_t*>(scratch + kStaticSummaryBytes);
+  int32_t* cnt = reinterpret_cast<int32_t*>(scratch + kStaticSummaryBytes + kStaticBandBytes);
+  unsigned* err = reinterpret_cast<unsigned*>(scratch + kStaticSummaryBytes + kStaticBandBytes +
+                                              kStaticCountBytes);
+  const int warp_ctas = (int)grid_for(nb, kWarpsPerCta);
+  // the validation word accumulates with atomicOr: it must start at zero on every call
+  MARBLE_CK(cudaMemsetAsync(err, 0, sizeof(unsigned), s));
+  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(sample_id, seg_id, noise_id, nb, summ, err);
+  k_band<<<grid_for(nb, 256), 256, 0, s>>>(summ, nb, band);
+  k_tiles_count<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(summ, band, nb, window, cnt);
+  k_scan<int32_t><<<1, 1024, 0, s>>>(cnt, nb, row_ptr);
+  k_tiles_write_capped<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(summ, band, row_ptr, nb, window,
+                                                               capacity, col, tag);
+  k_flag_invalid<<<1, 32, 0, s>>>(err, row_ptr);
+  MARBLE_CK(cudaGetLastError());
+  return MARBLE_OK;
+}

@@ -287,6 +287,41 @@ marble_status_t marble_set_wait_limit_ns(uint64_t ns);
 marble_status_t marble_debug_wait_timeout(const marble_plan_t *plan, uint64_t limit_ns,
                                           marble_stream_t stream);
 
+/*
+ * Tile map without allocation.  The paper has no counterpart for this call: it is a
+ * library convenience for callers that cannot call cudaMalloc.  Typical cases:
+ *   - a planner that runs for every packed batch on a side stream while the previous
+ *     training step still runs, and cannot afford the device-wide synchronisation that
+ *     cudaMalloc may imply;
+ *   - a process whose device memory is owned by another allocator (a framework caching
+ *     allocator that has reserved the pool) or is capped by a fixed budget.
+ * It computes the same global tile map as marble_plan (MARBLE_FIELD_TILE_ROWPTR / _COL /
+ * _TAG: per-row CSR in original block coordinates, kv blocks ascending, tags FULL /
+ * PARTIAL) into caller buffers, and allocates nothing.  Its intermediate scratch
+ * (per-block summaries, candidate bands, per-row counts, a validation word; about 64 bytes
+ * per 128-token block) lives in a fixed array inside the library, sized for at most
+ * MARBLE_TILE_MAP_STATIC_MAX_TOKENS tokens; every GPU that loads the library holds that
+ * array (about 1 MiB) until the process exits.
+ *   n_tokens  multiple of 128, at most MARBLE_TILE_MAP_STATIC_MAX_TOKENS (larger packs are
+ *             rejected with MARBLE_ERR_INVALID_ARG: use marble_plan);
+ *   sample_id, seg_id, noise_id, window: as in marble_plan_desc_t (device int32[n_tokens]);
+ *   row_ptr   device int64[n_tokens/128 + 1], written completely; row_ptr[nb] = number of
+ *             non-empty tiles.  If the metadata fails validation, row_ptr[0] is set to -1;
+ *   col, tag  device int32[capacity], uint8[capacity]; entries at CSR index >= capacity are
+ *             not written (compare row_ptr[nb] with capacity to detect a short buffer).
+ * Asynchronous on `stream`; host-side argument errors return before any launch.  The first
+ * call on a device looks up the device address of the scratch array on that device (a
+ * host-side step, done once per device, with that device current); make that first call
+ * before any stream capture.  All calls on a device share the one scratch array, so calls
+ * whose executions overlap on the GPU (different streams, or several host threads) race;
+ * serialise them, e.g. on one stream.
+ */
+#define MARBLE_TILE_MAP_STATIC_MAX_TOKENS 2097152
+marble_status_t marble_tile_map_static(int64_t n_tokens, const int32_t *sample_id,
+                                       const int32_t *seg_id, const int32_t *noise_id,
+                                       int32_t window, int64_t *row_ptr, int32_t *col,
+                                       uint8_t *tag, int64_t capacity, marble_stream_t stream);
+
 /* Thread-local message describing the last error on this thread ("" if none). */
 const char *marble_last_error(void);
 
