@@ -243,8 +243,7 @@ def run_marble(args, rank, world, local, dist):
     def step(marks=None):
         if marks:
             marks[0].record(stream)
-        for r, j, first in sched:
-            M.attn_step(pl, qp, kp, vp, r, j, st, first=first)
+        M.attn_steps(pl, qp, kp, vp, sched, st)
         if marks:
             marks[1].record(stream)
         M.attn_finalize(pl, st, o, lse)
@@ -254,8 +253,7 @@ def run_marble(args, rank, world, local, dist):
         dv.zero_()
         if marks:
             marks[2].record(stream)
-        for r, j, _ in sched:
-            M.attn_bwd(pl, qp, kp, vp, dop, lse, delta, r, j, dq, dk, dv)
+        M.attn_bwd_steps(pl, qp, kp, vp, dop, lse, delta, sched, dq, dk, dv)
         if marks:
             marks[3].record(stream)
 
@@ -289,10 +287,10 @@ def run_marble(args, rank, world, local, dist):
     mf, mb = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
     # dominant phase: report its own kernel's algorithmic FLOPs per launch / launch time
     if mb >= mf:
-        dom = {"kernel": "k_bwd_dq + k_bwd_dkdv (one marble_attn_bwd call)",
+        dom = {"kernel": "k_bwd_dq + k_bwd_dkdv (one backward ring step)",
                "flops_per_launch": flops_bwd / len(sched), "ms_per_launch": mb / len(sched)}
     else:
-        dom = {"kernel": "k_attn_fwd (one marble_attn_step call)",
+        dom = {"kernel": "k_attn_fwd (one forward ring step)",
                "flops_per_launch": flops_fwd / len(sched), "ms_per_launch": mf / len(sched)}
     ach = dom["flops_per_launch"] / (dom["ms_per_launch"] / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",

@@ -85,6 +85,15 @@ _SIGS = {
     "marble_attn_bwd": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_void_p, ctypes.c_void_p,
                          ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint32, ctypes.c_void_p]),
+    "marble_attn_steps": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_int32,
+                           ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                           ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(_State),
+                           ctypes.c_void_p]),
+    "marble_attn_bwd_steps": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                               ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p]),
     "marble_cast_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "marble_check": ([ctypes.c_void_p, ctypes.c_void_p]),
     "marble_set_wait_limit_ns": ([ctypes.c_uint64]),
@@ -324,11 +333,41 @@ def ring_schedule(num_shards: int, needed: bool = False):
     return [(r, (r - s) % P, s == 0) for r in range(P) for s in range(P)]
 
 
+def attn_steps(plan: Plan, q, k, v, schedule, state: State, scale: float = 0.0, stream=None):
+    """A list of forward ring steps [(q_shard, kv_shard, first), ...] in one C call."""
+    c = _qkv(plan, q, k, v, scale)
+    st = state._c()
+    n = len(schedule)
+    qs = (ctypes.c_int32 * n)(*[int(r) for r, _, _ in schedule])
+    ks = (ctypes.c_int32 * n)(*[int(j) for _, j, _ in schedule])
+    fl = (ctypes.c_uint32 * n)(*[STEP_FIRST if f else 0 for _, _, f in schedule])
+    _call("marble_attn_steps", plan.handle, ctypes.byref(c), n, qs, ks, fl, ctypes.byref(st),
+          _stream(stream))
+
+
+def attn_bwd_steps(plan: Plan, q, k, v, do, lse, delta, schedule, dq_acc, dk_acc, dv_acc,
+                   scale: float = 0.0, stream=None):
+    """A list of backward ring steps [(q_shard, kv_shard, _), ...] in one C call."""
+    import torch
+    c = _qkv(plan, q, k, v, scale)
+    _need(do, torch.bfloat16, "do", q.shape)
+    _need(lse, torch.float32, "lse", (q.shape[1], plan.n))
+    _need(delta, torch.float32, "delta", (q.shape[1], plan.n))
+    _need(dq_acc, torch.float32, "dq_acc", q.shape)
+    _need(dk_acc, torch.float32, "dk_acc", k.shape)
+    _need(dv_acc, torch.float32, "dv_acc", k.shape)
+    n = len(schedule)
+    qs = (ctypes.c_int32 * n)(*[int(r) for r, _, _ in schedule])
+    ks = (ctypes.c_int32 * n)(*[int(j) for _, j, _ in schedule])
+    _call("marble_attn_bwd_steps", plan.handle, ctypes.byref(c), _ptr(do), _ptr(lse),
+          _ptr(delta), n, qs, ks, _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), _stream(stream))
+
+
 def forward(plan: Plan, q, k, v, state: State, o, lse, needed: bool = False, scale: float = 0.0,
             stream=None):
     """All forward ring steps (r-major, keeping shard r's state hot in L2) + finalize."""
-    for r, j, first in ring_schedule(plan.num_shards, needed):
-        attn_step(plan, q, k, v, r, j, state, first=first, scale=scale, stream=stream)
+    attn_steps(plan, q, k, v, ring_schedule(plan.num_shards, needed), state, scale=scale,
+               stream=stream)
     attn_finalize(plan, state, o, lse, stream=stream)
 
 
@@ -336,9 +375,8 @@ def backward(plan: Plan, q, k, v, o, do, lse, delta, dq_acc, dk_acc, dv_acc,
              needed: bool = False, scale: float = 0.0, stream=None):
     """bwd preprocessing + all backward ring steps (accumulators must be zeroed)."""
     attn_bwd_prep(plan, o, do, delta, stream=stream)
-    for r, j, _ in ring_schedule(plan.num_shards, needed):
-        attn_bwd(plan, q, k, v, do, lse, delta, r, j, dq_acc, dk_acc, dv_acc, scale=scale,
-                 stream=stream)
+    attn_bwd_steps(plan, q, k, v, do, lse, delta, ring_schedule(plan.num_shards, needed),
+                   dq_acc, dk_acc, dv_acc, scale=scale, stream=stream)
 
 
 def version() -> str:

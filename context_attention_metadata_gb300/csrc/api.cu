@@ -5,7 +5,9 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
+#include <set>
 #include <string>
 #include <vector>
 
@@ -36,6 +38,15 @@ uint64_t wait_limit_ns() {
     g_wait_limit_ns = ms ? ms * 1000000ull : 2000000000ull;
   }
   return g_wait_limit_ns;
+}
+
+bool once_per_device(int key) {
+  static std::mutex mu;
+  static std::set<std::pair<int, int>> seen;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  return seen.insert({key, dev}).second;
 }
 
 // true for device or managed memory of the current context
@@ -268,7 +279,60 @@ MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
   if (flags & ~MARBLE_STEP_FIRST) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
-  return run_attn_fwd(p, qkv, q_shard, kv_shard, state, flags, (cudaStream_t)stream);
+  return run_attn_fwd(p, qkv, 1, &q_shard, &kv_shard, &flags, state, (cudaStream_t)stream);
+}
+
+static marble_status_t check_step_list(const marble_plan_t* p, int32_t n_steps,
+                                       const int32_t* q_shards, const int32_t* kv_shards) {
+  if (n_steps < 0) return fail(MARBLE_ERR_INVALID_ARG, "n_steps must be >= 0");
+  if (n_steps > 0 && (!q_shards || !kv_shards))
+    return fail(MARBLE_ERR_INVALID_ARG, "step arrays must be non-null");
+  for (int32_t i = 0; i < n_steps; ++i) {
+    marble_status_t st = check_shards(p, q_shards[i], kv_shards[i]);
+    if (st != MARBLE_OK) return st;
+  }
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_attn_steps(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                             int32_t n_steps, const int32_t* q_shards,
+                                             const int32_t* kv_shards, const uint32_t* flags,
+                                             const marble_state_t* state,
+                                             marble_stream_t stream) {
+  if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_step_list(p, n_steps, q_shards, kv_shards)) != MARBLE_OK) return st;
+  if (n_steps > 0 && !flags) return fail(MARBLE_ERR_INVALID_ARG, "flags must be non-null");
+  for (int32_t i = 0; i < n_steps; ++i)
+    if (flags[i] & ~MARBLE_STEP_FIRST) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+  if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
+  if (n_steps == 0) return MARBLE_OK;
+  return run_attn_fwd(p, qkv, n_steps, q_shards, kv_shards, flags, state, (cudaStream_t)stream);
+}
+
+MARBLE_API marble_status_t marble_attn_bwd_steps(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                                 const void* d_o, const float* lse,
+                                                 const float* delta, int32_t n_steps,
+                                                 const int32_t* q_shards,
+                                                 const int32_t* kv_shards, float* dq_acc,
+                                                 float* dk_acc, float* dv_acc,
+                                                 marble_stream_t stream) {
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_step_list(p, n_steps, q_shards, kv_shards)) != MARBLE_OK) return st;
+  if ((st = check_tensor(d_o, "d_o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(lse, "lse")) != MARBLE_OK) return st;
+  if ((st = check_tensor(delta, "delta")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dq_acc, "dq_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
+  if (n_steps == 0) return MARBLE_OK;
+  return run_attn_bwd(p, qkv, d_o, lse, delta, n_steps, q_shards, kv_shards, dq_acc, dk_acc,
+                      dv_acc, (cudaStream_t)stream);
 }
 
 MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
@@ -322,7 +386,7 @@ MARBLE_API marble_status_t marble_attn_bwd(const marble_plan_t* p, const marble_
   if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
   if (flags != 0) return fail(MARBLE_ERR_INVALID_ARG, "flags must be 0");
-  return run_attn_bwd(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq_acc, dk_acc, dv_acc,
+  return run_attn_bwd(p, qkv, d_o, lse, delta, 1, &q_shard, &kv_shard, dq_acc, dk_acc, dv_acc,
                       (cudaStream_t)stream);
 }
 

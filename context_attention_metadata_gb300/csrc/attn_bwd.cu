@@ -12,11 +12,12 @@
 // are needed (a fused kernel would scatter one fp32 dQ tile per (q, kv) tile):
 //   k_bwd_dq    Q-stationary, one CTA per (q block, q head): S and dP in TMEM, dS (bf16)
 //               back into TMEM over S, dQ += dS K with K read MN-major from the K tile
-//               already staged for S; at the end dq_acc += scale * dQ.
+//               already staged for S; at the end dq_acc += scale * dQ by a TMA reduce-add.
 //   k_bwd_dkdv  KV-stationary, one CTA per (kv block, kv head), looping over the q heads of
 //               its group and the q blocks listed for it: S^T = K Q^T and dP^T = V dO^T in
 //               TMEM, P^T and dS^T (bf16) back into TMEM, dV += P^T dO and dK += dS^T Q with
-//               dO and Q read MN-major; at the end dv_acc += dV, dk_acc += scale * dK.
+//               dO and Q read MN-major; at the end dv_acc += dV, dk_acc += scale * dK by TMA
+//               reduce-adds.
 // Both: warp 0 TMA producer (two stages), warp 1 TMEM allocation + MMA issue, warps 2..5
 // one thread per TMEM lane for the elementwise stage.  Masks only on partial tiles.
 #include <math.h>
@@ -33,6 +34,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;
+  CUtensorMap dq_map, dk_map, dv_map;  // fp32 accumulators, box 32 x 128 x 1, 128-byte swizzle
   const int64_t* step_ptr;   // row lists (dQ kernel)
   const int32_t* step_col;
   const uint8_t* step_tag;
@@ -60,7 +62,7 @@ struct BwdParams {
 // dQ (Q-stationary)
 // ======================================================================================
 enum { Q_QFULL, Q_KVFULL0, Q_KVFULL1, Q_KVEMPTY0, Q_KVEMPTY1, Q_SFULL, Q_PFULL, Q_DQDONE,
-       Q_DRAIN, Q_TRK0, Q_TRK1, Q_NUM };
+       Q_DRAIN, Q_TRK0, Q_TRK1, Q_EPI, Q_NUM };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int b = 0; b < Q_NUM; ++b)
-      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1) ? 128 : 1);
+      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1 || b == Q_EPI) ? 128 : 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -245,27 +247,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       tc_fence_before();
       mbar_arrive(&bar[Q_PFULL]);
     }
+    // epilogue: dq_acc += scale * dQ as a TMA fp32 reduce-add of a tile staged in the Q/dO
+    // slots (all MMAs are done), D/32 boxes of 128 x 32 fp32: no load of dq_acc
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !wait_all(&bar[Q_DQDONE], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
+    uint8_t* stg = smem;
     if (ok) {
-      float* dst = p.dq + (tq * p.hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tQ + lb + c * 32, v);
+        uint32_t x[32];
+        tmem_ld32(tQ + lb + c * 32, x);
         tmem_ld_wait();
-        float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+        float v[32];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          float4 a = d4[t];
-          a.x += p.scale * __uint_as_float(v[4 * t]);
-          a.y += p.scale * __uint_as_float(v[4 * t + 1]);
-          a.z += p.scale * __uint_as_float(v[4 * t + 2]);
-          a.w += p.scale * __uint_as_float(v[4 * t + 3]);
-          d4[t] = a;
-        }
+        for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(x[t]);
+        stage_row32(stg + c * 16384, row, v);
       }
+      fence_proxy_async_smem();
+    }
+    mbar_arrive(&bar[Q_EPI]);
+    if (row == 0 && ok && mbar_wait(&bar[Q_EPI], 0, w)) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c)
+        tma_reduce_add_3d(&p.dq_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
+      bulk_commit();
+      bulk_wait_all();
     }
   }
   tc_fence_before();
@@ -280,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
 // dK / dV (KV-stationary)
 // ======================================================================================
 enum { K_KVFULL, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL, K_PFULL, K_MMA2, K_DRAIN,
-       K_TRK0, K_TRK1, K_NUM };
+       K_TRK0, K_TRK1, K_EPI, K_NUM };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant__ BwdParams p) {
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int b = 0; b < K_NUM; ++b)
-      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1) ? 128 : 1);
+      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1 || b == K_EPI) ? 128 : 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -480,35 +487,39 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bar[K_PFULL]);
     }
+    // epilogue: dv_acc += dV and dk_acc += scale * dK as TMA fp32 reduce-adds of tiles staged
+    // in the K/V and first Q/dO slots (all MMAs are done): no load of the accumulators
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !wait_all(&bar[K_MMA2], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
+    uint8_t* stv = smem;
+    uint8_t* stk = smem + (D / 32) * 16384;
     if (ok) {
-      float* dvr = p.dv + (tk * p.hkv + kh) * D;
-      float* dkr = p.dk + (tk * p.hkv + kh) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32], kk[32];
-        tmem_ld32(tdV + lb + c * 32, v);
-        tmem_ld32(tdK + lb + c * 32, kk);
+        uint32_t xv[32], xk[32];
+        tmem_ld32(tdV + lb + c * 32, xv);
+        tmem_ld32(tdK + lb + c * 32, xk);
         tmem_ld_wait();
-        float4* v4 = reinterpret_cast<float4*>(dvr + c * 32);
-        float4* k4 = reinterpret_cast<float4*>(dkr + c * 32);
+        float v[32];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          float4 a = v4[t], bb = k4[t];
-          a.x += __uint_as_float(v[4 * t]);
-          a.y += __uint_as_float(v[4 * t + 1]);
-          a.z += __uint_as_float(v[4 * t + 2]);
-          a.w += __uint_as_float(v[4 * t + 3]);
-          bb.x += p.scale * __uint_as_float(kk[4 * t]);
-          bb.y += p.scale * __uint_as_float(kk[4 * t + 1]);
-          bb.z += p.scale * __uint_as_float(kk[4 * t + 2]);
-          bb.w += p.scale * __uint_as_float(kk[4 * t + 3]);
-          v4[t] = a;
-          k4[t] = bb;
-        }
+        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(xv[t]);
+        stage_row32(stv + c * 16384, row, v);
+#pragma unroll
+        for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(xk[t]);
+        stage_row32(stk + c * 16384, row, v);
       }
+      fence_proxy_async_smem();
+    }
+    mbar_arrive(&bar[K_EPI]);
+    if (row == 0 && ok && mbar_wait(&bar[K_EPI], 0, w)) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        tma_reduce_add_3d(&p.dv_map, stv + c * 16384, c * 32, (int)(nk * 128), kh);
+        tma_reduce_add_3d(&p.dk_map, stk + c * 16384, c * 32, (int)(nk * 128), kh);
+      }
+      bulk_commit();
+      bulk_wait_all();
     }
   }
   tc_fence_before();
@@ -520,9 +531,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
 }
 
 template <int D>
-marble_status_t launch(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
-                       const float* lse, const float* delta, int q_shard, int kv_shard,
-                       float* dq, float* dk, float* dv, cudaStream_t s) {
+size_t bwd_smem() {
+  // one CTA per SM: each CTA owns all 512 TMEM columns
+  size_t smem = 6 * (128 * D * 2) + 8192 + 1024;
+  return smem < 120 * 1024 ? 120 * 1024 : smem;
+}
+
+template <int D>
+marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
+                             const float* lse, const float* delta, int n_steps,
+                             const int* q_shards, const int* kv_shards, float* dq, float* dk,
+                             float* dv, cudaStream_t s) {
   BwdParams prm;
   memset(&prm, 0, sizeof(prm));
   const int64_t n = pl->n;
@@ -531,8 +550,14 @@ marble_status_t launch(const marble_plan_t* pl, const marble_qkv_t* qkv, const v
   if (!make_rows_map(&prm.q_map, qkv->q, bf, 2, n, qkv->hq, D, 64, 128, sw) ||
       !make_rows_map(&prm.k_map, qkv->k, bf, 2, n, qkv->hkv, D, 64, 128, sw) ||
       !make_rows_map(&prm.v_map, qkv->v, bf, 2, n, qkv->hkv, D, 64, 128, sw) ||
-      !make_rows_map(&prm.do_map, d_o, bf, 2, n, qkv->hq, D, 64, 128, sw))
-    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for Q/K/V/dO");
+      !make_rows_map(&prm.do_map, d_o, bf, 2, n, qkv->hq, D, 64, 128, sw) ||
+      !make_rows_map(&prm.dq_map, dq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, qkv->hq, D, 32, 128,
+                     sw) ||
+      !make_rows_map(&prm.dk_map, dk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, qkv->hkv, D, 32, 128,
+                     sw) ||
+      !make_rows_map(&prm.dv_map, dv, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, qkv->hkv, D, 32, 128,
+                     sw))
+    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for Q/K/V/dO/accumulators");
   prm.step_ptr = pl->step_ptr;
   prm.step_col = pl->step_col;
   prm.step_tag = pl->step_tag;
@@ -552,47 +577,47 @@ marble_status_t launch(const marble_plan_t* pl, const marble_qkv_t* qkv, const v
   prm.n = n;
   prm.P = pl->P;
   prm.bps = (int)pl->bps;
-  prm.q_shard = q_shard;
-  prm.kv_shard = kv_shard;
   prm.hq = qkv->hq;
   prm.hkv = qkv->hkv;
   prm.group = qkv->hq / qkv->hkv;
   prm.W = pl->W;
   prm.scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
   prm.sl2 = prm.scale * kLog2e;
-  // one CTA per SM: each CTA owns all 512 TMEM columns
-  size_t smem = 6 * (128 * D * 2) + 8192 + 1024;
-  if (smem < 120 * 1024) smem = 120 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
-  k_bwd_dq<D><<<(unsigned)(pl->bps * qkv->hq), kThreads, smem, s>>>(prm);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "launch k_bwd_dq");
-  int64_t units;
-  if (kv_shard >= 0) {
-    units = pl->bps * qkv->hkv;
-  } else {
-    units = (pl->h_needed_ptr[q_shard + 1] - pl->h_needed_ptr[q_shard]) * qkv->hkv;
+  const size_t smem = bwd_smem<D>();
+  if (once_per_device(D == 128 ? 3 : 4)) {
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
   }
-  if (units > 0) {
-    k_bwd_dkdv<D><<<(unsigned)units, kThreads, smem, s>>>(prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "launch k_bwd_dkdv");
+  for (int i = 0; i < n_steps; ++i) {
+    prm.q_shard = q_shards[i];
+    prm.kv_shard = kv_shards[i];
+    k_bwd_dq<D><<<(unsigned)(pl->bps * qkv->hq), kThreads, smem, s>>>(prm);
+    int64_t units;
+    if (prm.kv_shard >= 0)
+      units = pl->bps * qkv->hkv;
+    else
+      units = (pl->h_needed_ptr[prm.q_shard + 1] - pl->h_needed_ptr[prm.q_shard]) * qkv->hkv;
+    if (units > 0) k_bwd_dkdv<D><<<(unsigned)units, kThreads, smem, s>>>(prm);
   }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");
   return MARBLE_OK;
 }
 
 }  // namespace
 
 marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
-                             const float* lse, const float* delta, int q_shard, int kv_shard,
-                             float* dq, float* dk, float* dv, cudaStream_t s) {
-  if (qkv->d == 128) return launch<128>(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq, dk, dv, s);
-  if (qkv->d == 64) return launch<64>(p, qkv, d_o, lse, delta, q_shard, kv_shard, dq, dk, dv, s);
+                             const float* lse, const float* delta, int n_steps,
+                             const int* q_shards, const int* kv_shards, float* dq, float* dk,
+                             float* dv, cudaStream_t s) {
+  if (qkv->d == 128)
+    return launch_steps<128>(p, qkv, d_o, lse, delta, n_steps, q_shards, kv_shards, dq, dk, dv, s);
+  if (qkv->d == 64)
+    return launch_steps<64>(p, qkv, d_o, lse, delta, n_steps, q_shards, kv_shards, dq, dk, dv, s);
   return fail(MARBLE_ERR_UNSUPPORTED, "head dim must be 64 or 128");
 }
 

@@ -36,11 +36,12 @@ constexpr float kRescaleThreshold = 8.0f;  // base-2 units: rescale O when max g
 
 enum {
   B_QFULL, B_KFULL, B_VFULL, B_KEMPTY, B_VEMPTY, B_SFULL, B_PFULL, B_OFULL, B_DRAIN,
-  B_TRK0, B_TRK1, B_NUM
+  B_TRK0, B_TRK1, B_EPI0, B_EPI1, B_NUM
 };
 
 struct FwdParams {
   CUtensorMap q_map, k_map, v_map;
+  CUtensorMap o_map;  // fp32 O_acc, box 32 x 128 x 1, 128-byte swizzle
   const int64_t* step_ptr;
   const int32_t* step_col;
   const uint8_t* step_tag;
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
   __shared__ __align__(8) uint64_t bar[B_NUM];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ int epi_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x / p.bps, i = blockIdx.x % p.bps;
@@ -115,6 +117,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
     mbar_init(&bar[B_DRAIN], 1);
     mbar_init(&bar[B_TRK0], 128);
     mbar_init(&bar[B_TRK1], 128);
+    mbar_init(&bar[B_EPI0], 128);
+    mbar_init(&bar[B_EPI1], 128);
+    epi_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -314,45 +319,78 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bar[B_PFULL]);
     }
-    // epilogue: merge this call's (O, m, l) with the stored state (or start it)
+    // epilogue: merge this call's (O, m, l) into the stored state through a staged tile.
+    //   FIRST             the tile is stored (TMA store);
+    //   otherwise         the stored max is kept unless some row's max grew past it by more
+    //                     than the lazy threshold, so the update is a pure addition of
+    //                     O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
+    //   some row grew     exact merge with the stored tile (loaded by the row threads),
+    //                     then a TMA store.
+    // Q and K slots (all MMAs are done) hold the staging tile: D/32 boxes of 128 x 32 fp32.
     ok = __all_sync(0xffffffffu, ok);
     if (ok && !wait_all(&bar[B_OFULL], (T - 1) & 1, w)) ok = false;
     tc_fence_after();
+    const int64_t gi = (int64_t)h * n + tq;
+    float m_old = -INFINITY, l_old = 0.f;
+    if (!p.first) {
+      m_old = p.m[gi];
+      l_old = p.l[gi];
+    }
+    const bool grows = !p.first && m_old != -INFINITY && m_run > m_old + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_flag, 1);
+    mbar_arrive(&bar[B_EPI0]);
+    if (ok && !wait_all(&bar[B_EPI0], 0, w)) ok = false;
+    const int mode = p.first ? 0 : (epi_flag ? 2 : 1);
+    uint8_t* stg = smem;
     if (ok) {
-      const int64_t gi = (int64_t)h * n + tq;
-      float* orow = p.o_acc + (tq * p.hq + h) * D;
       float a_new = 1.f, a_old = 0.f, m_out = m_run, l_out = l_run;
-      if (!p.first) {
-        const float m_old = p.m[gi], l_old = p.l[gi];
+      if (mode == 1) {
+        m_out = (m_old == -INFINITY) ? m_run : m_old;
+        a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
+        l_out = l_old + l_run * a_new;
+      } else if (mode == 2) {
         m_out = fmaxf(m_old, m_run);  // both integral: the factors are exact powers of two
         a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
         a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
         l_out = l_old * a_old + l_run * a_new;
       }
+      const float* orow = p.o_acc + (tq * p.hq + h) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tO + lb + c * 32, v);
+        uint32_t x[32];
+        tmem_ld32(tO + lb + c * 32, x);
         tmem_ld_wait();
-        float4* dst = reinterpret_cast<float4*>(orow + c * 32);
+        float v[32];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          float4 o = make_float4(__uint_as_float(v[4 * t]) * a_new,
-                                 __uint_as_float(v[4 * t + 1]) * a_new,
-                                 __uint_as_float(v[4 * t + 2]) * a_new,
-                                 __uint_as_float(v[4 * t + 3]) * a_new);
-          if (!p.first) {
-            const float4 old = dst[t];
-            o.x += old.x * a_old;
-            o.y += old.y * a_old;
-            o.z += old.z * a_old;
-            o.w += old.w * a_old;
+        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(x[t]) * a_new;
+        if (mode == 2) {
+          const float4* src = reinterpret_cast<const float4*>(orow + c * 32);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const float4 o = src[t];
+            v[4 * t] += o.x * a_old;
+            v[4 * t + 1] += o.y * a_old;
+            v[4 * t + 2] += o.z * a_old;
+            v[4 * t + 3] += o.w * a_old;
           }
-          dst[t] = o;
         }
+        stage_row32(stg + c * 16384, row, v);
       }
+      fence_proxy_async_smem();
       p.m[gi] = m_out;
       p.l[gi] = l_out;
+    }
+    mbar_arrive(&bar[B_EPI1]);
+    if (row == 0 && ok && mbar_wait(&bar[B_EPI1], 0, w)) {
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        if (mode == 1)
+          tma_reduce_add_3d(&p.o_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
+        else
+          tma_store_3d(&p.o_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
+      }
+      bulk_commit();
+      bulk_wait_all();
     }
   }
 
@@ -365,58 +403,80 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
 }
 
 template <int D>
-marble_status_t launch(const marble_plan_t* pl, const marble_qkv_t* qkv, int q_shard, int kv_shard,
-                       const marble_state_t* st, uint32_t flags, cudaStream_t s) {
-  FwdParams prm;
-  memset(&prm, 0, sizeof(prm));
-  const int64_t n = pl->n;
-  if (!make_rows_map(&prm.q_map, qkv->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hq, D, 64,
-                     128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_rows_map(&prm.k_map, qkv->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hkv, D, 64,
-                     128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_rows_map(&prm.v_map, qkv->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hkv, D, 64,
-                     128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for Q/K/V");
-  prm.step_ptr = pl->step_ptr;
-  prm.step_col = pl->step_col;
-  prm.step_tag = pl->step_tag;
-  prm.tracks = pl->tracks;
-  prm.o_acc = st->o_acc;
-  prm.m = st->m;
-  prm.l = st->l;
-  prm.err = pl->err;
-  prm.wait_ns = wait_limit_ns();
-  prm.n = n;
-  prm.P = pl->P;
-  prm.bps = (int)pl->bps;
-  prm.q_shard = q_shard;
-  prm.kv_shard = kv_shard;
-  prm.hq = qkv->hq;
-  prm.group = qkv->hq / qkv->hkv;
-  prm.W = pl->W;
-  prm.first = (flags & MARBLE_STEP_FIRST) ? 1 : 0;
-  const float scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
-  prm.scale_log2 = scale * 1.4426950408889634f;
+size_t fwd_smem() {
   // at least ~100 KB so that exactly two CTAs share an SM (two 256-column TMEM halves)
   size_t smem = 3 * (128 * D * 2) + 4096 + 1024;
-  if (smem < 100 * 1024) smem = 100 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_attn_fwd)");
+  return smem < 100 * 1024 ? 100 * 1024 : smem;
+}
+
+// everything but the shard pair and the FIRST flag: encoded once per call
+template <int D>
+marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
+                        const marble_state_t* st, FwdParams* prm) {
+  memset(prm, 0, sizeof(*prm));
+  const int64_t n = pl->n;
+  if (!make_rows_map(&prm->q_map, qkv->q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hq, D, 64,
+                     128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_rows_map(&prm->k_map, qkv->k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hkv, D, 64,
+                     128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_rows_map(&prm->v_map, qkv->v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, n, qkv->hkv, D, 64,
+                     128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_rows_map(&prm->o_map, st->o_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, n, qkv->hq, D, 32,
+                     128, CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for Q/K/V/O_acc");
+  prm->step_ptr = pl->step_ptr;
+  prm->step_col = pl->step_col;
+  prm->step_tag = pl->step_tag;
+  prm->tracks = pl->tracks;
+  prm->o_acc = st->o_acc;
+  prm->m = st->m;
+  prm->l = st->l;
+  prm->err = pl->err;
+  prm->wait_ns = wait_limit_ns();
+  prm->n = n;
+  prm->P = pl->P;
+  prm->bps = (int)pl->bps;
+  prm->hq = qkv->hq;
+  prm->group = qkv->hq / qkv->hkv;
+  prm->W = pl->W;
+  const float scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
+  prm->scale_log2 = scale * 1.4426950408889634f;
+  if (once_per_device(D == 128 ? 1 : 2)) {
+    cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)fwd_smem<D>());
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_attn_fwd)");
+  }
+  return MARBLE_OK;
+}
+
+template <int D>
+marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, int n_steps,
+                             const int* q_shards, const int* kv_shards, const uint32_t* flags,
+                             const marble_state_t* st, cudaStream_t s) {
+  FwdParams base;
+  marble_status_t rc = prepare<D>(pl, qkv, st, &base);
+  if (rc != MARBLE_OK) return rc;
   const unsigned grid = (unsigned)(pl->bps * qkv->hq);
-  k_attn_fwd<D><<<grid, kThreads, smem, s>>>(prm);
-  e = cudaGetLastError();
+  for (int i = 0; i < n_steps; ++i) {
+    FwdParams prm = base;
+    prm.q_shard = q_shards[i];
+    prm.kv_shard = kv_shards[i];
+    prm.first = (flags[i] & MARBLE_STEP_FIRST) ? 1 : 0;
+    k_attn_fwd<D><<<grid, kThreads, fwd_smem<D>(), s>>>(prm);
+  }
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch k_attn_fwd");
   return MARBLE_OK;
 }
 
 }  // namespace
 
-marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int q_shard,
-                             int kv_shard, const marble_state_t* st, uint32_t flags,
-                             cudaStream_t s) {
-  if (qkv->d == 128) return launch<128>(p, qkv, q_shard, kv_shard, st, flags, s);
-  if (qkv->d == 64) return launch<64>(p, qkv, q_shard, kv_shard, st, flags, s);
+marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int n_steps,
+                             const int* q_shards, const int* kv_shards, const uint32_t* flags,
+                             const marble_state_t* st, cudaStream_t s) {
+  if (qkv->d == 128) return launch_steps<128>(p, qkv, n_steps, q_shards, kv_shards, flags, st, s);
+  if (qkv->d == 64) return launch_steps<64>(p, qkv, n_steps, q_shards, kv_shards, flags, st, s);
   return fail(MARBLE_ERR_UNSUPPORTED, "head dim must be 64 or 128");
 }
 

@@ -151,6 +151,48 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* map, uint64_t
       : "memory");
 }
 
+// shared -> global tile store / element-wise fp32 add-reduce through a tensor map, tracked
+// by the issuing thread's bulk async-group
+__device__ __forceinline__ void tma_store_3d(const void* map, const void* src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d(const void* map, const void* src, int c0, int c1,
+                                                  int c2) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+      " [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+      "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// wait until every committed bulk copy of this thread has completed (writes performed)
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// wait until every committed bulk copy of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Row `row` of a [128 rows x 32 fp32] staging box in the 128-byte-swizzled layout a TMA
+// store/reduce with 128-byte swizzle reads: 16-byte chunk i of the row goes to chunk
+// i ^ (row mod 8), so the 8 rows of an atom hit distinct banks.
+__device__ __forceinline__ void stage_row32(uint8_t* box, int row, const float (&v)[32]) {
+  uint8_t* r = box + row * 128;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    float4 x = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    *reinterpret_cast<float4*>(r + ((i ^ (row & 7)) << 4)) = x;
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // tcgen05
 // ------------------------------------------------------------------------------------

@@ -78,12 +78,16 @@ cudaError_t launch_bwd_prep(const marble_plan_t* p, const void* o, const void* d
                             float* delta, cudaStream_t s);
 cudaError_t launch_debug_wait(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 
-// attention (attn_fwd.cu, attn_bwd.cu)
-marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int q_shard,
-                             int kv_shard, const marble_state_t* st, uint32_t flags,
-                             cudaStream_t s);
+// attention (attn_fwd.cu, attn_bwd.cu): a list of ring steps launched back to back on `s`
+marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int n_steps,
+                             const int* q_shards, const int* kv_shards, const uint32_t* flags,
+                             const marble_state_t* st, cudaStream_t s);
 marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
-                             const float* lse, const float* delta, int q_shard, int kv_shard,
-                             float* dq, float* dk, float* dv, cudaStream_t s);
+                             const float* lse, const float* delta, int n_steps,
+                             const int* q_shards, const int* kv_shards, float* dq, float* dk,
+                             float* dv, cudaStream_t s);
+
+// true the first time it is called for (key, current device); used for per-device set-up
+bool once_per_device(int key);
 
 }  // namespace marble

@@ -232,6 +232,19 @@ marble_status_t marble_attn_step(const marble_plan_t *plan, const marble_qkv_t *
                                  marble_stream_t stream);
 
 /*
+ * A list of forward ring steps in one call: step i is exactly
+ * marble_attn_step(plan, qkv, q_shards[i], kv_shards[i], state, flags[i], stream), launched
+ * in list order on `stream` (each step is still its own kernel launch and the state passes
+ * through HBM between steps).  The host arrays q_shards, kv_shards, flags hold n_steps
+ * entries and are read before the call returns.  Saves per-call validation and tensor-map
+ * set-up when a whole ring schedule is issued at once.
+ */
+marble_status_t marble_attn_steps(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                  int32_t n_steps, const int32_t *q_shards,
+                                  const int32_t *kv_shards, const uint32_t *flags,
+                                  const marble_state_t *state, marble_stream_t stream);
+
+/*
  * Normalise once at the end (MARBLE s03: "only the last call normalizes the output,
  * writes the LSE and casts to bf16"):  O = O_acc / l as bf16 [N, hq, d] and
  * LSE = ln(sum_k exp(s_k)) = (m + log2 l) * ln 2 as fp32 [hq, N].  A row with l = 0 (no
@@ -264,6 +277,14 @@ marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *q
                                 int32_t q_shard, int32_t kv_shard, float *dq_acc,
                                 float *dk_acc, float *dv_acc, uint32_t flags,
                                 marble_stream_t stream);
+
+/* A list of backward ring steps in one call: step i is marble_attn_bwd(..., q_shards[i],
+ * kv_shards[i], ..., flags = 0), in list order on `stream`; host arrays of n_steps entries. */
+marble_status_t marble_attn_bwd_steps(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                      const void *d_o, const float *lse, const float *delta,
+                                      int32_t n_steps, const int32_t *q_shards,
+                                      const int32_t *kv_shards, float *dq_acc, float *dk_acc,
+                                      float *dv_acc, marble_stream_t stream);
 
 /* Cast fp32 -> bf16 (round to nearest even) for n elements, e.g. gradient accumulators;
  * n must be a multiple of 4 and both pointers 16-byte aligned. */
