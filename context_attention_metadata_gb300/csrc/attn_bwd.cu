@@ -29,8 +29,9 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;  // producer, MMA, 8 elementwise warps (2 per lane quarter)
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPrefetchTiles = 64;  // L2 prefetch depth per unit
 
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int b = 0; b < Q_NUM; ++b)
-      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1 || b == Q_EPI) ? 128 : 1);
+      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1 || b == Q_EPI) ? 256 : 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -107,7 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = tmem_base;         // S fp32 [0,128); dS bf16 in [0,64)
+  // S fp32 [0,128); dS bf16 packed over it: q/kv columns [64h, 64h + 64) of half h go to
+  // TMEM columns [64h, 64h + 32), inside the fp32 columns that same half has read
+  const uint32_t tS = tmem_base;
   const uint32_t tP = tmem_base + 128;   // dP fp32 [128,256)
   const uint32_t tQ = tmem_base + 256;   // dQ fp32 [256, 256+D)
   const int kvh = h / p.group;
@@ -122,6 +125,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       for (int a = 0; a < kAtoms; ++a) {
         tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
         tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
+      }
+    }
+    // pull the unit's K/V tiles toward L2 ahead of their loads
+    for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
+      const int nk = p.step_col[e0 + j];
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
+        tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
       }
     }
     int fills[2] = {0, 0};
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tQ, tS + k * 8, sdesc_sw128(aK + k * 2048, 16384, 1024), kIdQ,
+          mma_ts(tQ, tS + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aK + k * 2048, 16384, 1024), kIdQ,
                  (j > 0 || k > 0) ? 1u : 0u);
         mma_commit(&bar[Q_DQDONE]);
         mma_commit(&bar[Q_KVEMPTY0 + s]);
@@ -184,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     }
     __syncwarp();
   } else {
+    // two warps per TMEM lane quarter: `half` selects columns [64 half, 64 half + 64)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const int64_t tq = nq * 128 + row;
@@ -198,21 +211,25 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     int n_partial = 0;
     for (int j = 0; j < T; ++j) {
       const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
-      uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};
+      uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
       if (partial) {
         const int b = n_partial & 1;
         const uint32_t par = (n_partial >> 1) & 1;
         ++n_partial;
         int32_t* kt = ktr + b * 512;
         const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
-        kt[row] = p.tracks[t];
-        kt[128 + row] = p.tracks[n + t];
-        kt[256 + row] = p.tracks[2 * n + t];
-        kt[384 + row] = p.tracks[3 * n + t];
+        if (half == 0) {
+          kt[row] = p.tracks[t];
+          kt[128 + row] = p.tracks[n + t];
+        } else {
+          kt[256 + row] = p.tracks[2 * n + t];
+          kt[384 + row] = p.tracks[3 * n + t];
+        }
         mbar_arrive(&bar[Q_TRK0 + b]);
         if (!wait_all(&bar[Q_TRK0 + b], par, w)) { ok = false; break; }
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
           uint32_t bits = 0;
 #pragma unroll
           for (int t2 = 0; t2 < 32; ++t2) {
@@ -220,28 +237,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
             bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc], kt[384 + kc],
                                 p.W) ? 1u : 0u) << t2;
           }
-          lm[c] = bits;
+          lm[cc] = bits;
         }
       }
       if (!wait_all(&bar[Q_SFULL], j & 1, w)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t vs[32], vp[32];
-        tmem_ld32(tS + lb + c * 32, vs);
-        tmem_ld32(tP + lb + c * 32, vp);
-        tmem_ld_wait();
+      uint32_t vs[2][32], vp[2][32];
+      tmem_ld32(tS + lb + (2 * half) * 32, vs[0]);
+      tmem_ld32(tS + lb + (2 * half + 1) * 32, vs[1]);
+      tmem_ld32(tP + lb + (2 * half) * 32, vp[0]);
+      tmem_ld32(tP + lb + (2 * half + 1) * 32, vp[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const bool l0 = (lm[c] >> t) & 1u, l1 = (lm[c] >> (t + 1)) & 1u;
-          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[t]) * sl2 - lse2) : 0.f;
-          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[t + 1]) * sl2 - lse2) : 0.f;
-          const float d0 = p0 * (__uint_as_float(vp[t]) - dlt);
-          const float d1 = p1 * (__uint_as_float(vp[t + 1]) - dlt);
+          const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
+          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2) : 0.f;
+          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2) : 0.f;
+          const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dlt);
+          const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dlt);
           pk[t >> 1] = pack_bf16(d0, d1);
         }
-        tmem_st16(tS + lb + c * 16, pk);
+        tmem_st16(tS + lb + half * 64 + cc * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -255,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     uint8_t* stg = smem;
     if (ok) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t x[32];
         tmem_ld32(tQ + lb + c * 32, x);
         tmem_ld_wait();
@@ -267,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       fence_proxy_async_smem();
     }
     mbar_arrive(&bar[Q_EPI]);
-    if (row == 0 && ok && mbar_wait(&bar[Q_EPI], 0, w)) {
+    if (row == 0 && half == 0 && ok && mbar_wait(&bar[Q_EPI], 0, w)) {
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c)
         tma_reduce_add_3d(&p.dq_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int b = 0; b < K_NUM; ++b)
-      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1 || b == K_EPI) ? 128 : 1);
+      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1 || b == K_EPI) ? 256 : 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -335,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = tmem_base;          // S^T fp32 [0,128); P^T bf16 in [0,64)
-  const uint32_t tP = tmem_base + 128;    // dP^T fp32 [128,256); dS^T bf16 in [128,192)
+  // S^T fp32 [0,128) and dP^T fp32 [128,256); P^T / dS^T bf16 packed over them: q columns
+  // [64h, 64h + 64) of half h go to columns [64h, 64h + 32) of the same region
+  const uint32_t tS = tmem_base;
+  const uint32_t tP = tmem_base + 128;
   const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
   const uint32_t tdK = tmem_base + 384;   // dK fp32 [384, 384+D)
 
@@ -350,6 +371,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       for (int a = 0; a < kAtoms; ++a) {
         tma_load_3d(sK + a * 16384, &p.k_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
         tma_load_3d(sV + a * 16384, &p.v_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
+      }
+    }
+    // pull the items' Q/dO tiles toward L2 ahead of their loads
+    for (int it = lane; it < T && it < kPrefetchTiles; it += 32) {
+      const int h = kh * p.group + it / L;
+      const int nqb = p.colT_row[c0 + it % L];
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_prefetch_l2_3d(&p.q_map, a * 64, nqb * 128, h);
+        tma_prefetch_l2_3d(&p.do_map, a * 64, nqb * 128, h);
       }
     }
     int fills[2] = {0, 0};
@@ -403,11 +433,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tdV, tS + k * 8, sdesc_sw128(aDO + k * 2048, 16384, 1024), kIdAcc,
+          mma_ts(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aDO + k * 2048, 16384, 1024), kIdAcc,
                  (it > 0 || k > 0) ? 1u : 0u);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-          mma_ts(tdK, tP + k * 8, sdesc_sw128(aQ + k * 2048, 16384, 1024), kIdAcc,
+          mma_ts(tdK, tP + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aQ + k * 2048, 16384, 1024), kIdAcc,
                  (it > 0 || k > 0) ? 1u : 0u);
         mma_commit(&bar[K_MMA2]);
         mma_commit(&bar[K_QEMPTY0 + s]);
@@ -417,7 +447,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     }
     __syncwarp();
   } else {
+    // two warps per TMEM lane quarter: `half` selects q columns [64 half, 64 half + 64)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;  // kv row of the tile
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const int64_t tk = nk * 128 + row;
@@ -435,10 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       float* lse2s = stg + b * 256;
       float* dls = lse2s + 128;
       int32_t* qt = qtr + b * 512;
-      float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
-      lse2s[row] = (l2 == -INFINITY) ? INFINITY : l2;
-      dls[row] = p.delta[(int64_t)h * n + qrow];
-      if (partial) {
+      if (half == 0) {
+        const float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
+        lse2s[row] = (l2 == -INFINITY) ? INFINITY : l2;
+        dls[row] = p.delta[(int64_t)h * n + qrow];
+      } else if (partial) {
         qt[row] = p.tracks[qrow];
         qt[128 + row] = p.tracks[n + qrow];
         qt[256 + row] = p.tracks[2 * n + qrow];
@@ -446,10 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       }
       mbar_arrive(&bar[K_TRK0 + b]);
       if (!wait_all(&bar[K_TRK0 + b], (it >> 1) & 1, w)) { ok = false; break; }
-      uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};
+      uint32_t lm[2] = {~0u, ~0u};
       if (partial) {
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
           uint32_t bits = 0;
 #pragma unroll
           for (int t2 = 0; t2 < 32; ++t2) {
@@ -457,31 +491,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             bits |= (mask_legal(qt[q], qt[128 + q], qt[256 + q], qt[384 + q], sk, gk, zk, pk,
                                 p.W) ? 1u : 0u) << t2;
           }
-          lm[c] = bits;
+          lm[cc] = bits;
         }
       }
       if (!wait_all(&bar[K_SFULL], it & 1, w)) { ok = false; break; }
       tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t vs[32], vp[32];
-        tmem_ld32(tS + lb + c * 32, vs);
-        tmem_ld32(tP + lb + c * 32, vp);
-        tmem_ld_wait();
+      uint32_t vs[2][32], vp[2][32];
+      tmem_ld32(tS + lb + (2 * half) * 32, vs[0]);
+      tmem_ld32(tS + lb + (2 * half + 1) * 32, vs[1]);
+      tmem_ld32(tP + lb + (2 * half) * 32, vp[0]);
+      tmem_ld32(tP + lb + (2 * half + 1) * 32, vp[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * half + cc;
         uint32_t pk16[16], dk16[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
           const int q0 = c * 32 + t;
-          const bool l0 = (lm[c] >> t) & 1u, l1 = (lm[c] >> (t + 1)) & 1u;
-          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[t]) * sl2 - lse2s[q0]) : 0.f;
-          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
-          const float d0 = p0 * (__uint_as_float(vp[t]) - dls[q0]);
-          const float d1 = p1 * (__uint_as_float(vp[t + 1]) - dls[q0 + 1]);
+          const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
+          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2s[q0]) : 0.f;
+          const float p1 =
+              l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
+          const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dls[q0]);
+          const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dls[q0 + 1]);
           pk16[t >> 1] = pack_bf16(p0, p1);
           dk16[t >> 1] = pack_bf16(d0, d1);
         }
-        tmem_st16(tS + lb + c * 16, pk16);
-        tmem_st16(tP + lb + c * 16, dk16);
+        tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
+        tmem_st16(tP + lb + half * 64 + cc * 16, dk16);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -496,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     uint8_t* stk = smem + (D / 32) * 16384;
     if (ok) {
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t xv[32], xk[32];
         tmem_ld32(tdV + lb + c * 32, xv);
         tmem_ld32(tdK + lb + c * 32, xk);
@@ -512,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       fence_proxy_async_smem();
     }
     mbar_arrive(&bar[K_EPI]);
-    if (row == 0 && ok && mbar_wait(&bar[K_EPI], 0, w)) {
+    if (row == 0 && half == 0 && ok && mbar_wait(&bar[K_EPI], 0, w)) {
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         tma_reduce_add_3d(&p.dv_map, stv + c * 16384, c * 32, (int)(nk * 128), kh);

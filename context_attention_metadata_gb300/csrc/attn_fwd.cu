@@ -32,7 +32,8 @@ namespace marble {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr float kRescaleThreshold = 8.0f;  // base-2 units: rescale O when max grows > 2^8
+constexpr float kRescaleThreshold = 8.0f;
+constexpr int kPrefetchTiles = 64;  // L2 prefetch depth per unit  // base-2 units: rescale O when max grows > 2^8
 
 enum {
   B_QFULL, B_KFULL, B_VFULL, B_KEMPTY, B_VEMPTY, B_SFULL, B_PFULL, B_OFULL, B_DRAIN,
@@ -142,6 +143,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant_
       mbar_arrive_expect_tx(&bar[B_QFULL], kTile);
       for (int a = 0; a < kAtoms; ++a)
         tma_load_3d(sQ + a * 16384, &p.q_map, &bar[B_QFULL], a * 64, (int)(nq * 128), h);
+    }
+    // pull the unit's K/V tiles toward L2 ahead of their loads (single smem slots)
+    for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
+      const int nk = p.step_col[e0 + j];
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
+        tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
+      }
     }
     int kfill = 0, vfill = 0;
     for (int j = 0; j < T; ++j) {
