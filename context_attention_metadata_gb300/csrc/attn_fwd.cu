@@ -7,21 +7,26 @@
 // the last call normalises.  RingAttention tutorial, "The Online Softmax Formulation":
 // the recurrence m_new = max(m, rowmax S), rescale by exp(m - m_new), add exp(S - m_new).
 //
-// Kernel structure (sm_103a): one CTA per (q block, q head) work unit, two CTAs per SM.
-//   warp 0      TMA producer: Q tile once, then K_j and V_j of every listed tile (single
-//               slot each; K_j+1 streams in while tile j's softmax and PV run).
-//   warp 1      allocates 256 TMEM columns; lane 0 issues tcgen05.mma:
-//                 S = Q K_j^T  (SS, 128x128, fp32 in TMEM columns [0,128))
-//                 O += P_j V_j (TS: P as bf16 in TMEM columns [0,64) over S; V MN-major)
-//   warps 2..5  one thread per query row (TMEM lane): row max, exp2, row sum, bf16 P
-//               back into TMEM, lazy O rescale, and the final merge with the stored state;
-//               on partial tiles they first stage the keys' metadata tracks in shared
-//               memory and evaluate the mask once per pair into a 128-bit row mask.
-// Full tiles skip the mask; partial tiles evaluate the packed-mask predicate per pair;
-// empty tiles are never listed, so never loaded.  Scores are kept in base-2 units
-// (s * scale * log2 e); the stored m is in the same units and always an integer, so that
-// every rescale (lazy, by at least 2^8, within a call; and the merge with the stored
-// state) multiplies by an exact power of two.
+// Kernel structure (sm_103a): a persistent CTA per SM walks its (q block, q head) work
+// units round-robin; every role advances the same cursor over (unit, tile), so each
+// mbarrier phase is a function of those counters.
+//   warp 0      TMA producer: Q of each unit (one slot, refilled once the unit's last S
+//               has read it), K_j and V_j through two-slot rings, and L2 prefetches of a
+//               unit's K/V tiles when the unit starts.
+//   warp 1      allocates all 512 TMEM columns: S double buffer [0,128) and [128,256),
+//               O double buffer [256,384) and [384,512) (units alternate); lane 0 issues
+//               tcgen05.mma -- S = Q K^T two tiles ahead of the softmax, O += P V with P as
+//               bf16 in TMEM over its S buffer and V read MN-major; it polls its inputs and
+//               issues whichever of the next PV and the next S is ready.
+//   warps 2..9  softmax: two warps per TMEM lane quarter, each owning 64 of a row's 128
+//               columns; the row max is exchanged through shared memory.  Row max, exp2,
+//               row sum, bf16 P back into TMEM, lazy O rescale, and the per-unit merge of
+//               (O, m, l) into the stored state through a staged TMA store / reduce-add.
+//               On partial tiles they stage the keys' tracks and evaluate the mask once
+//               per pair; full tiles skip it; empty tiles are never listed, so never loaded.
+// Scores are kept in base-2 units (s * scale * log2 e); the stored m is in the same units
+// and always an integer, so that every rescale (lazy, when the max grows past 2^8, within
+// a call; and the merge with the stored state) multiplies by an exact power of two.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,13 +36,26 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr float kRescaleThreshold = 8.0f;
-constexpr int kPrefetchTiles = 64;  // L2 prefetch depth per unit  // base-2 units: rescale O when max grows > 2^8
+constexpr int kThreads = 320;              // producer, MMA, 8 softmax warps
+constexpr int kSoftmax = 256;              // softmax threads
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units: rescale O when max grows > 2^8
+constexpr int kPrefetchTiles = 64;         // L2 prefetch depth per unit
 
 enum {
-  B_QFULL, B_KFULL, B_VFULL, B_KEMPTY, B_VEMPTY, B_SFULL, B_PFULL, B_OFULL, B_DRAIN,
-  B_TRK0, B_TRK1, B_EPI0, B_EPI1, B_NUM
+  B_QFULL, B_QEMPTY,                 // Q slot: TMA fill / last S of the unit done
+  B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,  // K ring (slot = tile & 1): fill / S done
+  B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,  // V ring: fill / PV done
+  B_SFULL0, B_SFULL1,                // S buffer (tile & 1) computed
+  B_PFULL0, B_PFULL1,                // P written over S buffer (256 softmax arrivals)
+  B_PVDONE,                          // one phase per tile: its PV has completed
+  B_PCONS0, B_PCONS1,                // S buffer (tile & 1): its P consumed by the PV
+  B_OFREE0, B_OFREE1,                // O buffer (unit & 1) read out by the epilogue
+  B_MX0, B_MX1,                      // per-row max exchanged between the two halves
+  B_TRK0, B_TRK1,                    // key tracks of a partial tile staged
+  B_EPI,                             // per unit: l and the merge mode exchanged
+  B_STG0, B_STG1,                    // per unit: staging rows of half 0 / half 1 written
+  B_STGMID, B_STGFREE,               // per unit: half 0's / half 1's TMA has read staging
+  B_DRAIN, B_NUM
 };
 
 struct FwdParams {
@@ -55,367 +73,543 @@ struct FwdParams {
   long long n;
   int P, bps, q_shard, kv_shard;
   int hq, group;
+  int units;  // bps * hq
   int W;
   int first;
   float scale_log2;
 };
 
+// list range of work unit u = h * bps + i (q block i of the shard, q head h)
+__device__ __forceinline__ int unit_tiles(const FwdParams& p, int u, int64_t* e0) {
+  const int i = u % p.bps;
+  const int64_t nq = (int64_t)p.q_shard * p.bps + i;
+  int64_t a, b;
+  if (p.kv_shard >= 0) {
+    a = p.step_ptr[nq * p.P + p.kv_shard];
+    b = p.step_ptr[nq * p.P + p.kv_shard + 1];
+  } else {
+    a = p.step_ptr[nq * p.P];
+    b = p.step_ptr[nq * p.P + p.P];
+  }
+  *e0 = a;
+  return (int)(b - a);
+}
+
+// Position in this CTA's stream of work: units blockIdx.x, blockIdx.x + gridDim.x, ... with
+// at least one tile; tiles in list order.  g counts tiles, uc counts non-empty units.
+struct Cursor {
+  int unit, T, j, g, uc;
+  int64_t e0;
+  bool valid;
+  __device__ __forceinline__ int h(const FwdParams& p) const { return unit / p.bps; }
+  __device__ __forceinline__ int64_t nq(const FwdParams& p) const {
+    return (int64_t)p.q_shard * p.bps + unit % p.bps;
+  }
+};
+
+__device__ __forceinline__ void seek_unit(const FwdParams& p, Cursor& c, int u) {
+  for (; u < p.units; u += gridDim.x) {
+    int64_t e0;
+    const int T = unit_tiles(p, u, &e0);
+    if (T > 0) {
+      c.unit = u;
+      c.T = T;
+      c.e0 = e0;
+      c.j = 0;
+      c.valid = true;
+      return;
+    }
+  }
+  c.valid = false;
+}
+
+__device__ __forceinline__ void cursor_begin(const FwdParams& p, Cursor& c) {
+  c.g = 0;
+  c.uc = 0;
+  seek_unit(p, c, blockIdx.x);
+}
+
+__device__ __forceinline__ void cursor_next(const FwdParams& p, Cursor& c) {
+  ++c.g;
+  if (++c.j == c.T) {
+    ++c.uc;
+    seek_unit(p, c, c.unit + gridDim.x);
+  }
+}
+
+// two-slot rings indexed by the tile counter g: slot g & 1, phase parity (g >> 1) & 1
+__device__ __forceinline__ uint32_t ring_slot(int g) { return (uint32_t)(g & 1); }
+__device__ __forceinline__ uint32_t ring_parity(int g) { return (uint32_t)((g >> 1) & 1); }
+
+// shared memory: Q | K ring (2) | V ring (2) | staging (2 boxes of 128 x 32 fp32) | key tracks
+// [2][4][128] int32 | row-max exchange [2][2][128] f32 | row-sum exchange [2][128] f32
 template <int D>
-__global__ void __launch_bounds__(kThreads, 2) k_attn_fwd(const __grid_constant__ FwdParams p) {
-  constexpr int kTile = 128 * D * 2;  // bytes of one bf16 128 x D tile
-  constexpr int kAtoms = D / 64;      // 128-byte swizzle atoms along d
+struct Smem {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kQ = 0;
+  static constexpr int kK = kTile;
+  static constexpr int kV = 3 * kTile;
+  static constexpr int kStg = 5 * kTile;
+  static constexpr int kTrk = kStg + 2 * 16384;
+  static constexpr int kMx = kTrk + 2 * 512 * 4;
+  static constexpr int kLs = kMx + 2 * 2 * 128 * 4;
+  static constexpr int kEnd = kLs + 2 * 128 * 4;
+  static constexpr size_t bytes() { return (size_t)kEnd + 1024; }  // + alignment slack
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant__ FwdParams p) {
+  using L = Smem<D>;
+  constexpr int kTile = L::kTile;
+  constexpr int kAtoms = D / 64;  // 128-byte swizzle atoms along d
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;
-  uint8_t* sK = smem + kTile;
-  uint8_t* sV = smem + 2 * kTile;
-  int32_t* ktr = reinterpret_cast<int32_t*>(smem + 3 * kTile);  // [2][4][128]
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sK = smem + L::kK;  // slot s at sK + s * kTile
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sStg = smem + L::kStg;
+  int32_t* ktr = reinterpret_cast<int32_t*>(smem + L::kTrk);
+  float* mxs = reinterpret_cast<float*>(smem + L::kMx);
+  float* lss = reinterpret_cast<float*>(smem + L::kLs);
   __shared__ __align__(8) uint64_t bar[B_NUM];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ int epi_flag;
+  __shared__ int epi_mode[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x / p.bps, i = blockIdx.x % p.bps;
   const long long n = p.n;
-  const int64_t nq = (int64_t)p.q_shard * p.bps + i;
-  int64_t e0, e1;
-  if (p.kv_shard >= 0) {
-    e0 = p.step_ptr[nq * p.P + p.kv_shard];
-    e1 = p.step_ptr[nq * p.P + p.kv_shard + 1];
-  } else {
-    e0 = p.step_ptr[nq * p.P];
-    e1 = p.step_ptr[nq * p.P + p.P];
-  }
-  const int T = (int)(e1 - e0);
-
-  if (T == 0) {
-    if (!p.first) return;
-    // rows with no tile on their first step start from (O = 0, m = -inf, l = 0)
-    for (int r = threadIdx.x; r < 128; r += kThreads) {
-      p.m[(int64_t)h * n + nq * 128 + r] = -INFINITY;
-      p.l[(int64_t)h * n + nq * 128 + r] = 0.f;
-    }
-    for (int idx = threadIdx.x; idx < 128 * (D / 4); idx += kThreads) {
-      const int r = idx / (D / 4), c = idx % (D / 4);
-      float4* o = reinterpret_cast<float4*>(p.o_acc + ((nq * 128 + r) * p.hq + h) * D) + c;
-      *o = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    return;
-  }
-
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(&bar[B_QFULL], 1);
-    mbar_init(&bar[B_KFULL], 1);
-    mbar_init(&bar[B_VFULL], 1);
-    mbar_init(&bar[B_KEMPTY], 1);
-    mbar_init(&bar[B_VEMPTY], 1);
-    mbar_init(&bar[B_SFULL], 1);
-    mbar_init(&bar[B_PFULL], 128);
-    mbar_init(&bar[B_OFULL], 1);
-    mbar_init(&bar[B_DRAIN], 1);
-    mbar_init(&bar[B_TRK0], 128);
-    mbar_init(&bar[B_TRK1], 128);
-    mbar_init(&bar[B_EPI0], 128);
-    mbar_init(&bar[B_EPI1], 128);
-    epi_flag = 0;
+    epi_mode[0] = epi_mode[1] = 0;
+    for (int b = 0; b < B_NUM; ++b) {
+      const bool softmax_wide = b == B_PFULL0 || b == B_PFULL1 || b == B_OFREE0 ||
+                                b == B_OFREE1 || b == B_MX0 || b == B_MX1 || b == B_TRK0 ||
+                                b == B_TRK1 || b == B_EPI;
+      const bool half_wide = b == B_STG0 || b == B_STG1;
+      mbar_init(&bar[b], softmax_wide ? kSoftmax : (half_wide ? kSoftmax / 2 : 1));
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, 256);
+    tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tS = tmem_base;        // S (fp32, 128 cols); P (bf16) in cols [0, 64)
-  const uint32_t tO = tmem_base + 128;  // O (fp32, D cols)
-  const int kvh = h / p.group;
+  const uint32_t tS = tmem_base;        // S buffers at +0 and +128
+  const uint32_t tO = tmem_base + 256;  // O buffers at +0 and +128
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.q_map);
       tma_prefetch_desc(&p.k_map);
       tma_prefetch_desc(&p.v_map);
-      mbar_arrive_expect_tx(&bar[B_QFULL], kTile);
-      for (int a = 0; a < kAtoms; ++a)
-        tma_load_3d(sQ + a * 16384, &p.q_map, &bar[B_QFULL], a * 64, (int)(nq * 128), h);
+      tma_prefetch_desc(&p.o_map);
     }
-    // pull the unit's K/V tiles toward L2 ahead of their loads (single smem slots)
-    for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
-      const int nk = p.step_col[e0 + j];
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
-        tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
+    Cursor c;
+    cursor_begin(p, c);
+    int q_fills = 0, k_fills = 0, v_fills = 0;  // fills issued (k/v fill t is tile t)
+    while (c.valid) {
+      const int h = c.h(p);
+      const int kvh = h / p.group;
+      if (c.j == 0) {
+        // Q of a new unit once the previous unit's last S has read the slot
+        if (c.uc > 0 && !warp_wait(&bar[B_QEMPTY], (c.uc - 1) & 1, w)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[B_QFULL], kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(sQ + a * 16384, &p.q_map, &bar[B_QFULL], a * 64, (int)(c.nq(p) * 128), h);
+        }
+        ++q_fills;
+        // pull the unit's K/V tiles toward L2 ahead of their loads
+        for (int j = lane; j < c.T && j < kPrefetchTiles; j += 32) {
+          const int nk = p.step_col[c.e0 + j];
+          for (int a = 0; a < kAtoms; ++a) {
+            tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
+            tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
+          }
+        }
       }
-    }
-    int kfill = 0, vfill = 0;
-    for (int j = 0; j < T; ++j) {
-      const int nk = p.step_col[e0 + j];
-      if (j > 0 && !warp_wait(&bar[B_KEMPTY], (j - 1) & 1, w)) break;
+      const int nk = p.step_col[c.e0 + c.j];
+      const uint32_t s = ring_slot(c.g);
+      if (c.g >= 2 && !warp_wait(&bar[B_KEMPTY0 + s], ring_parity(c.g - 2), w)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar[B_KFULL], kTile);
+        mbar_arrive_expect_tx(&bar[B_KFULL0 + s], kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sK + a * 16384, &p.k_map, &bar[B_KFULL], a * 64, nk * 128, kvh);
+          tma_load_3d(sK + s * kTile + a * 16384, &p.k_map, &bar[B_KFULL0 + s], a * 64, nk * 128,
+                      kvh);
       }
-      ++kfill;
-      if (j > 0 && !warp_wait(&bar[B_VEMPTY], (j - 1) & 1, w)) break;
+      ++k_fills;
+      if (c.g >= 2 && !warp_wait(&bar[B_VEMPTY0 + s], ring_parity(c.g - 2), w)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar[B_VFULL], kTile);
+        mbar_arrive_expect_tx(&bar[B_VFULL0 + s], kTile);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sV + a * 16384, &p.v_map, &bar[B_VFULL], a * 64, nk * 128, kvh);
+          tma_load_3d(sV + s * kTile + a * 16384, &p.v_map, &bar[B_VFULL0 + s], a * 64, nk * 128,
+                      kvh);
       }
-      ++vfill;
+      ++v_fills;
+      cursor_next(p, c);
     }
-    // never leave the CTA with a copy still landing in its shared memory
+    // never leave the CTA with a copy still landing in its shared memory: the fills of a
+    // slot complete in order, so waiting for the latest fill of each slot suffices
     if (lane == 0) {
-      drain_wait(&bar[B_QFULL], 0, p.wait_ns, p.err);
-      if (kfill) drain_wait(&bar[B_KFULL], (kfill - 1) & 1, p.wait_ns, p.err);
-      if (vfill) drain_wait(&bar[B_VFULL], (vfill - 1) & 1, p.wait_ns, p.err);
+      if (q_fills) drain_wait(&bar[B_QFULL], (q_fills - 1) & 1, p.wait_ns, p.err);
+      for (int t = k_fills - 1; t >= 0 && t >= k_fills - 2; --t)
+        drain_wait(&bar[B_KFULL0 + ring_slot(t)], ring_parity(t), p.wait_ns, p.err);
+      for (int t = v_fills - 1; t >= 0 && t >= v_fills - 2; --t)
+        drain_wait(&bar[B_VFULL0 + ring_slot(t)], ring_parity(t), p.wait_ns, p.err);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  }
+  else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(&bar[B_QFULL], 0, w);
-      for (int j = 0; ok && j < T; ++j) {
-        if (!mbar_wait(&bar[B_KFULL], j & 1, w)) break;
-        // S/P columns are free once the previous PV has consumed P
-        if (j > 0 && !mbar_wait(&bar[B_OFULL], (j - 1) & 1, w)) break;
-        tc_fence_after();
+      const uint32_t aQ = smem_u32(sQ), aK0 = smem_u32(sK), aV0 = smem_u32(sV);
+      // Event loop: issue whichever of the next PV (priority: it feeds the softmax and the
+      // epilogue) and the next S (at most two tiles ahead of the next PV) has its inputs
+      // ready, polling with non-blocking tests; a wait for S's inputs never delays a PV.
+      Cursor cs, cp;
+      cursor_begin(p, cs);
+      cursor_begin(p, cp);
+      uint64_t t_last = globaltimer_ns();
+      uint32_t idle = 0;
+      while (cp.valid || cs.valid) {
+        bool progressed = false;
+        if (cp.valid) {
+          const int g = cp.g;
+          const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g), ob = (uint32_t)(cp.uc & 1);
+          // the first PV of a unit overwrites its O buffer: the unit two back must be read out
+          const bool ready =
+              mbar_test(&bar[B_PFULL0 + b], (g >> 1) & 1) &&
+              mbar_test(&bar[B_VFULL0 + s], ring_parity(g)) &&
+              (cp.j != 0 || cp.uc < 2 || mbar_test(&bar[B_OFREE0 + ob], ((cp.uc >> 1) - 1) & 1));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t aV = aV0 + s * kTile;
+            // P of half h sits in columns [64 h, 64 h + 32) of the S buffer
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS,
-                 k > 0);
+            for (int k = 0; k < 8; ++k)
+              mma_ts(tO + ob * 128, tS + b * 128 + (k >> 2) * 64 + (k & 3) * 8,
+                     sdesc_sw128(aV + k * 2048, 16384, 1024), kIdO, (cp.j > 0 || k > 0) ? 1u : 0u);
+            mma_commit(&bar[B_PVDONE]);
+            mma_commit(&bar[B_PCONS0 + b]);
+            mma_commit(&bar[B_VEMPTY0 + s]);
+            cursor_next(p, cp);
+            progressed = true;
+          }
         }
-        mma_commit(&bar[B_SFULL]);
-        mma_commit(&bar[B_KEMPTY]);
-        if (!mbar_wait(&bar[B_PFULL], j & 1, w)) break;
-        if (!mbar_wait(&bar[B_VFULL], j & 1, w)) break;
-        tc_fence_after();
+        if (cs.valid && (!cp.valid || cs.g < cp.g + 2)) {
+          const int g = cs.g;
+          const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g);
+          const bool ready = (cs.j != 0 || mbar_test(&bar[B_QFULL], cs.uc & 1)) &&
+                             mbar_test(&bar[B_KFULL0 + s], ring_parity(g)) &&
+                             (g < 2 || mbar_test(&bar[B_PCONS0 + b], ((g - 2) >> 1) & 1));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t aK = aK0 + s * kTile;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tO, tS + k * 8, sdesc_sw128(aV + k * 2048, 16384, 1024), kIdO,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar[B_OFULL]);
-        mma_commit(&bar[B_VEMPTY]);
+            for (int k = 0; k < D / 16; ++k) {
+              const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+              mma_ss(tS + b * 128, sdesc_sw128(aQ + off, 16, 1024),
+                     sdesc_sw128(aK + off, 16, 1024), kIdS, k > 0);
+            }
+            mma_commit(&bar[B_SFULL0 + b]);
+            mma_commit(&bar[B_KEMPTY0 + s]);
+            if (cs.j == cs.T - 1) mma_commit(&bar[B_QEMPTY]);  // the unit's last read of Q
+            cursor_next(p, cs);
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+          idle = 0;
+        } else {
+          __nanosleep(32);
+          if ((++idle & 63) == 0) {
+            if (*w.abort) break;
+            if (globaltimer_ns() - t_last > p.wait_ns) {
+              atomicOr(p.err, kErrTimeout);
+              *w.abort = 1;
+              break;
+            }
+          }
+        }
       }
       // every MMA issued by this thread has completed before TMEM is released
       mma_commit(&bar[B_DRAIN]);
       drain_wait(&bar[B_DRAIN], 0, p.wait_ns, p.err);
     }
     __syncwarp();
-  } else {
-    // ---------------------------------------------------------------- softmax warps
+  }
+  else {
+    // ------------------------------------------------------------------ softmax warps
+    // two warps per TMEM lane quarter: `half` owns S columns [64 half, 64 half + 64) and O
+    // columns [D/2 half, D/2 half + D/2) of its row
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    const int64_t tq = nq * 128 + row;
-    const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
-              pq = p.tracks[3 * n + tq];
     const float sl2 = p.scale_log2;
-    const int W = p.W;
-    float m_run = -INFINITY, l_run = 0.f;
+    if (p.first) {
+      // rows of units without a tile in this step start from (O = 0, m = -inf, l = 0)
+      for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+        int64_t e0;
+        if (unit_tiles(p, u, &e0) != 0) continue;
+        const int h = u / p.bps;
+        const int64_t tq = ((int64_t)p.q_shard * p.bps + u % p.bps) * 128 + row;
+        if (half == 0) {
+          p.m[(int64_t)h * n + tq] = -INFINITY;
+          p.l[(int64_t)h * n + tq] = 0.f;
+        }
+        float4* o = reinterpret_cast<float4*>(p.o_acc + (tq * p.hq + h) * D + half * (D / 2));
+#pragma unroll
+        for (int t = 0; t < D / 8; ++t) o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    Cursor c;
+    cursor_begin(p, c);
     bool ok = true;
     int n_partial = 0;
-    for (int j = 0; j < T; ++j) {
-      const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
-      uint32_t lm[4] = {~0u, ~0u, ~0u, ~0u};  // legal-key bits of this row in tile j
+    float m_run = -INFINITY, l_h = 0.f;
+    int sq = 0, gq = -1, zq = -1, pq = 0;
+    while (ok && c.valid) {
+      const int g = c.g;
+      const uint32_t b = (uint32_t)(g & 1);
+      const int h = c.h(p);
+      const int64_t tq = c.nq(p) * 128 + row;
+      if (c.j == 0) {
+        sq = p.tracks[tq];
+        gq = p.tracks[n + tq];
+        zq = p.tracks[2 * n + tq];
+        pq = p.tracks[3 * n + tq];
+        m_run = -INFINITY;
+        l_h = 0.f;
+      }
+      const bool partial = p.step_tag[c.e0 + c.j] == MARBLE_TILE_PARTIAL;
+      uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
       if (partial) {
-        // stage the 128 keys' tracks in one of two buffers; all 128 rows arrive before
-        // any reads, so a buffer is rewritten only after every row left its last use
-        const int b = n_partial & 1;
+        // stage the 128 keys' tracks in one of two buffers (the two halves load two tracks
+        // each); every softmax thread arrives before any reads, so a buffer is rewritten
+        // only after every thread left its previous use
+        const int bb = n_partial & 1;
         const uint32_t par = (n_partial >> 1) & 1;
         ++n_partial;
-        int32_t* kt = ktr + b * 512;
-        const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
-        kt[row] = p.tracks[t];
-        kt[128 + row] = p.tracks[n + t];
-        kt[256 + row] = p.tracks[2 * n + t];
-        kt[384 + row] = p.tracks[3 * n + t];
-        mbar_arrive(&bar[B_TRK0 + b]);
-        if (!wait_all(&bar[B_TRK0 + b], par, w)) { ok = false; break; }
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        int32_t* kt = ktr + bb * 512;
+        const int64_t t = (int64_t)p.step_col[c.e0 + c.j] * 128 + row;
+        if (half == 0) {
+          kt[row] = p.tracks[t];
+          kt[128 + row] = p.tracks[n + t];
+        } else {
+          kt[256 + row] = p.tracks[2 * n + t];
+          kt[384 + row] = p.tracks[3 * n + t];
+        }
+        mbar_arrive(&bar[B_TRK0 + bb]);
+        if (!wait_all(&bar[B_TRK0 + bb], par, w)) { ok = false; break; }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int kc0 = (2 * half + cc) * 32;
           uint32_t bits = 0;
 #pragma unroll
           for (int t2 = 0; t2 < 32; ++t2) {
-            const int kc = c * 32 + t2;
-            const int dp = pq - kt[384 + kc];
-            const bool legal = ((dp >= 0 && dp < W) || (gq >= 0 && gq == kt[128 + kc])) &&
-                               (kt[256 + kc] < 0 || kt[256 + kc] == zq) && (kt[kc] == sq);
-            bits |= (legal ? 1u : 0u) << t2;
+            const int kc = kc0 + t2;
+            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc], kt[384 + kc],
+                                p.W) ? 1u : 0u) << t2;
           }
-          lm[c] = bits;
+          lm[cc] = bits;
         }
       }
-      if (!wait_all(&bar[B_SFULL], j & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[B_SFULL0 + b], (g >> 1) & 1, w)) { ok = false; break; }
       tc_fence_after();
-      // pass 1: row maximum of the scaled, masked scores
+      const uint32_t sb = tS + b * 128;
+      uint32_t v[2][32];
+      tmem_ld32(sb + lb + (2 * half) * 32, v[0]);
+      tmem_ld32(sb + lb + (2 * half + 1) * 32, v[1]);
+      tmem_ld_wait();
+      // scaled, masked scores (kept in v) and this half's row maximum
       float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lb + c * 32, v);
-        tmem_ld_wait();
-        if (partial) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const float s = ((lm[c] >> t) & 1u) ? __uint_as_float(v[t]) * sl2 : -INFINITY;
-            mx = fmaxf(mx, s);
-          }
-        } else {
+      for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(v[t]) * sl2);
+        for (int t = 0; t < 32; ++t) {
+          const float s = ((lm[cc] >> t) & 1u) ? __uint_as_float(v[cc][t]) * sl2 : -INFINITY;
+          v[cc][t] = __float_as_uint(s);
+          mx = fmaxf(mx, s);
         }
       }
+      float* mxb = mxs + b * 256;
+      mxb[half * 128 + row] = mx;
+      mbar_arrive(&bar[B_MX0 + b]);
+      if (!wait_all(&bar[B_MX0 + b], (g >> 1) & 1, w)) { ok = false; break; }
+      mx = fmaxf(mx, mxb[(1 - half) * 128 + row]);
       // the running max is kept integral (base 2): every rescale factor below is then an
       // exact power of two, and bf16 rounding of P does not depend on which keys a step
       // happened to see first
       const float m_new = ceilf(mx);
       const bool grow = m_new > m_run + kRescaleThreshold;
-      const bool need = grow && (m_run != -INFINITY);  // earlier tiles of this call to rescale
+      const bool need = grow && (m_run != -INFINITY);  // earlier tiles of this unit to rescale
       const float alpha = need ? ldexpf(1.f, (int)(m_run - m_new)) : 1.f;
       if (grow) {
-        l_run *= alpha;
+        l_h *= alpha;
         m_run = m_new;
       }
       // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
       // must (alpha = 1 on the others).  A row that needs it has a finite max from an
-      // earlier tile, so j >= 1 and PV_{j-1} is the accumulation to wait for.
+      // earlier tile of this unit, so PV(g-1) is the accumulation to wait for.
       if (__any_sync(0xffffffffu, need)) {
-        if (!wait_all(&bar[B_OFULL], (j - 1) & 1, w)) { ok = false; break; }
+        if (!wait_all(&bar[B_PVDONE], (g - 1) & 1, w)) { ok = false; break; }
         tc_fence_after();
+        const uint32_t ob = tO + (uint32_t)(c.uc & 1) * 128;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + lb + c * 32, v);
+        for (int cc = 0; cc < D / 64; ++cc) {
+          const uint32_t col = half * (D / 2) + cc * 32;
+          uint32_t x[32];
+          tmem_ld32(ob + lb + col, x);
           tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-          tmem_st32(tO + lb + c * 32, v);
+          for (int t = 0; t < 32; ++t) x[t] = __float_as_uint(__uint_as_float(x[t]) * alpha);
+          tmem_st32(ob + lb + col, x);
         }
       }
-      // pass 2: P = exp2(s - m_run) as bf16 into TMEM over the consumed S columns
+      // P = exp2(s - m_run) as bf16, packed into columns [64 half, 64 half + 32) of the S
+      // buffer: inside the fp32 columns this warp has just read
       const float base = (m_run == -INFINITY) ? 0.f : m_run;
       float rs = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + lb + c * 32, v);
-        tmem_ld_wait();
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t pk[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          float s0 = __uint_as_float(v[t]) * sl2, s1 = __uint_as_float(v[t + 1]) * sl2;
-          if (!((lm[c] >> t) & 1u)) s0 = -INFINITY;
-          if (!((lm[c] >> (t + 1)) & 1u)) s1 = -INFINITY;
-          const float p0 = fast_exp2(s0 - base), p1 = fast_exp2(s1 - base);
+          const float p0 = fast_exp2(__uint_as_float(v[cc][t]) - base);
+          const float p1 = fast_exp2(__uint_as_float(v[cc][t + 1]) - base);
           rs += p0 + p1;
           pk[t >> 1] = pack_bf16(p0, p1);
         }
-        tmem_st16(tS + lb + c * 16, pk);
+        tmem_st16(sb + lb + half * 64 + cc * 16, pk);
       }
       tmem_st_wait();
-      l_run += rs;
+      l_h += rs;
       tc_fence_before();
-      mbar_arrive(&bar[B_PFULL]);
-    }
-    // epilogue: merge this call's (O, m, l) into the stored state through a staged tile.
-    //   FIRST             the tile is stored (TMA store);
-    //   otherwise         the stored max is kept unless some row's max grew past it by more
-    //                     than the lazy threshold, so the update is a pure addition of
-    //                     O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
-    //   some row grew     exact merge with the stored tile (loaded by the row threads),
-    //                     then a TMA store.
-    // Q and K slots (all MMAs are done) hold the staging tile: D/32 boxes of 128 x 32 fp32.
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok && !wait_all(&bar[B_OFULL], (T - 1) & 1, w)) ok = false;
-    tc_fence_after();
-    const int64_t gi = (int64_t)h * n + tq;
-    float m_old = -INFINITY, l_old = 0.f;
-    if (!p.first) {
-      m_old = p.m[gi];
-      l_old = p.l[gi];
-    }
-    const bool grows = !p.first && m_old != -INFINITY && m_run > m_old + kRescaleThreshold;
-    if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_flag, 1);
-    mbar_arrive(&bar[B_EPI0]);
-    if (ok && !wait_all(&bar[B_EPI0], 0, w)) ok = false;
-    const int mode = p.first ? 0 : (epi_flag ? 2 : 1);
-    uint8_t* stg = smem;
-    if (ok) {
-      float a_new = 1.f, a_old = 0.f, m_out = m_run, l_out = l_run;
-      if (mode == 1) {
-        m_out = (m_old == -INFINITY) ? m_run : m_old;
-        a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
-        l_out = l_old + l_run * a_new;
-      } else if (mode == 2) {
-        m_out = fmaxf(m_old, m_run);  // both integral: the factors are exact powers of two
-        a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
-        a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
-        l_out = l_old * a_old + l_run * a_new;
-      }
-      const float* orow = p.o_acc + (tq * p.hq + h) * D;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t x[32];
-        tmem_ld32(tO + lb + c * 32, x);
-        tmem_ld_wait();
-        float v[32];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(x[t]) * a_new;
-        if (mode == 2) {
-          const float4* src = reinterpret_cast<const float4*>(orow + c * 32);
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const float4 o = src[t];
-            v[4 * t] += o.x * a_old;
-            v[4 * t + 1] += o.y * a_old;
-            v[4 * t + 2] += o.z * a_old;
-            v[4 * t + 3] += o.w * a_old;
-          }
+      mbar_arrive(&bar[B_PFULL0 + b]);
+      if (c.j == c.T - 1) {
+        // ---------------------------------------------------------------- unit epilogue
+        // Merge this call's (O, m, l) into the stored state through a staged tile:
+        //   FIRST         the tile is stored (TMA store);
+        //   otherwise     the stored max is kept unless some row's max grew past it by more
+        //                 than the lazy threshold, so the update is a pure addition of
+        //                 O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
+        //   some row grew exact merge with the stored tile (loaded by the row threads),
+        //                 then a TMA store.
+        // The 32 KB staging buffer holds one half's boxes at a time: half 0 stages and its
+        // TMA reads, then half 1 (the next unit's half 0 waits for half 1's TMA).
+        const int uc = c.uc;
+        // PV(g-2) is done (S(g) needed its P consumed), but PV(g-1) may not be: wait for
+        // PV(g-1) then PV(g), so that no parity wait runs two phases ahead of the barrier
+        if (g >= 1 && !wait_all(&bar[B_PVDONE], (g - 1) & 1, w)) { ok = false; break; }
+        if (!wait_all(&bar[B_PVDONE], g & 1, w)) { ok = false; break; }
+        tc_fence_after();
+        const int64_t gi = (int64_t)h * n + tq;
+        float m_old = -INFINITY, l_old = 0.f;
+        if (!p.first) {
+          m_old = p.m[gi];
+          l_old = p.l[gi];
         }
-        stage_row32(stg + c * 16384, row, v);
-      }
-      fence_proxy_async_smem();
-      p.m[gi] = m_out;
-      p.l[gi] = l_out;
-    }
-    mbar_arrive(&bar[B_EPI1]);
-    if (row == 0 && ok && mbar_wait(&bar[B_EPI1], 0, w)) {
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        if (mode == 1)
-          tma_reduce_add_3d(&p.o_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
+        const bool grows = !p.first && m_old != -INFINITY && m_run > m_old + kRescaleThreshold;
+        lss[half * 128 + row] = l_h;
+        if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_mode[uc & 1], 1);
+        mbar_arrive(&bar[B_EPI]);
+        if (!wait_all(&bar[B_EPI], uc & 1, w)) { ok = false; break; }
+        const float l_run = lss[row] + lss[128 + row];
+        const int mode = p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
+        if (row == 0 && half == 0) epi_mode[(uc + 1) & 1] = 0;  // every thread has read it
+        float a_new = 1.f, a_old = 0.f, m_out = m_run, l_out = l_run;
+        if (mode == 1) {
+          m_out = (m_old == -INFINITY) ? m_run : m_old;
+          a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
+          l_out = l_old + l_run * a_new;
+        } else if (mode == 2) {
+          m_out = fmaxf(m_old, m_run);  // both integral: the factors are exact powers of two
+          a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
+          a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
+          l_out = l_old * a_old + l_run * a_new;
+        }
+        // this half's O columns out of TMEM; then the O buffer can take unit uc + 2
+        const uint32_t ob = tO + (uint32_t)(uc & 1) * 128;
+        float ov[D / 64][32];
+#pragma unroll
+        for (int cc = 0; cc < D / 64; ++cc) {
+          uint32_t x[32];
+          tmem_ld32(ob + lb + half * (D / 2) + cc * 32, x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) ov[cc][t] = __uint_as_float(x[t]) * a_new;
+        }
+        tc_fence_before();
+        mbar_arrive(&bar[B_OFREE0 + (uc & 1)]);
+        if (mode == 2) {
+          const float4* src =
+              reinterpret_cast<const float4*>(p.o_acc + (tq * p.hq + h) * D + half * (D / 2));
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc)
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 o = src[cc * 8 + t];
+              ov[cc][4 * t] += o.x * a_old;
+              ov[cc][4 * t + 1] += o.y * a_old;
+              ov[cc][4 * t + 2] += o.z * a_old;
+              ov[cc][4 * t + 3] += o.w * a_old;
+            }
+        }
+        if (half == 0) {
+          p.m[gi] = m_out;
+          p.l[gi] = l_out;
+        }
+        // staging round of this half
+        bool stg_ok;
+        if (half == 0)
+          stg_ok = uc == 0 || wait_all(&bar[B_STGFREE], (uc - 1) & 1, w);
         else
-          tma_store_3d(&p.o_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
+          stg_ok = wait_all(&bar[B_STGMID], uc & 1, w);
+        if (stg_ok) {
+#pragma unroll
+          for (int cc = 0; cc < D / 64; ++cc) stage_row32(sStg + cc * 16384, row, ov[cc]);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(&bar[B_STG0 + half]);
+        if (row == 0) {
+          if (stg_ok && mbar_wait(&bar[B_STG0 + half], uc & 1, w)) {
+            const int y = (int)(c.nq(p) * 128);
+#pragma unroll
+            for (int cc = 0; cc < D / 64; ++cc) {
+              const int x0 = (half * (D / 64) + cc) * 32;
+              if (mode == 1)
+                tma_reduce_add_3d(&p.o_map, sStg + cc * 16384, x0, y, h);
+              else
+                tma_store_3d(&p.o_map, sStg + cc * 16384, x0, y, h);
+            }
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar[half == 0 ? B_STGMID : B_STGFREE]);
+        }
+        if (!stg_ok) { ok = false; break; }
       }
-      bulk_commit();
-      bulk_wait_all();
+      cursor_next(p, c);
     }
+    // the global writes of every TMA store / reduce this thread issued have completed
+    if (row == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 256);
+    tmem_dealloc(tmem_base, 512);
   }
-}
-
-template <int D>
-size_t fwd_smem() {
-  // at least ~100 KB so that exactly two CTAs share an SM (two 256-column TMEM halves)
-  size_t smem = 3 * (128 * D * 2) + 4096 + 1024;
-  return smem < 100 * 1024 ? 100 * 1024 : smem;
 }
 
 // everything but the shard pair and the FIRST flag: encoded once per call
@@ -447,13 +641,14 @@ marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
   prm->bps = (int)pl->bps;
   prm->hq = qkv->hq;
   prm->group = qkv->hq / qkv->hkv;
+  prm->units = (int)(pl->bps * qkv->hq);
   prm->W = pl->W;
   const float scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
   prm->scale_log2 = scale * 1.4426950408889634f;
   if (once_per_device(D == 128 ? 1 : 2)) {
     cudaError_t e = cudaFuncSetAttribute(k_attn_fwd<D>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)fwd_smem<D>());
+                                         (int)Smem<D>::bytes());
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(k_attn_fwd)");
   }
   return MARBLE_OK;
@@ -466,13 +661,17 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   FwdParams base;
   marble_status_t rc = prepare<D>(pl, qkv, st, &base);
   if (rc != MARBLE_OK) return rc;
-  const unsigned grid = (unsigned)(pl->bps * qkv->hq);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // persistent: one CTA per SM (each takes all 512 TMEM columns), at most one per unit
+  const unsigned grid = (unsigned)(base.units < sms ? base.units : sms);
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
     prm.first = (flags[i] & MARBLE_STEP_FIRST) ? 1 : 0;
-    k_attn_fwd<D><<<grid, kThreads, fwd_smem<D>(), s>>>(prm);
+    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), s>>>(prm);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch k_attn_fwd");
