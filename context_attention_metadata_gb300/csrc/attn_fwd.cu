@@ -7,23 +7,28 @@
 // the last call normalises.  RingAttention tutorial, "The Online Softmax Formulation":
 // the recurrence m_new = max(m, rowmax S), rescale by exp(m - m_new), add exp(S - m_new).
 //
-// Kernel structure (sm_103a): a persistent CTA per SM walks its (q block, q head) work
-// units round-robin; every role advances the same cursor over (unit, tile), so each
-// mbarrier phase is a function of those counters.
-//   warp 0      TMA producer: Q of each unit (one slot, refilled once the unit's last S
-//               has read it), K_j and V_j through two-slot rings, and L2 prefetches of a
-//               unit's K/V tiles when the unit starts.
+// Kernel structure (sm_103a): one persistent CTA per SM takes work units (q block, q head)
+// from a shared ticket counter, in the plan's order for the step (longest tile list first),
+// and runs them through a pipeline of warp roles that meet at mbarriers:
+//   warp 14     scheduler: draws a ticket, turns it into a unit and its tile-list range and
+//               posts it in a 4-entry queue in shared memory; every other role reads the
+//               queue in order, and the epilogue frees an entry once all roles are past it.
+//   warp 0      TMA producer: Q of each unit into one of two slots, K_j and V_j through
+//               two-slot rings, and L2 prefetches of a unit's K/V tiles when it starts.
 //   warp 1      allocates all 512 TMEM columns: S double buffer [0,128) and [128,256),
 //               O double buffer [256,384) and [384,512) (units alternate); lane 0 issues
-//               tcgen05.mma -- S = Q K^T two tiles ahead of the softmax, O += P V with P as
-//               bf16 in TMEM over its S buffer and V read MN-major; it polls its inputs and
-//               issues whichever of the next PV and the next S is ready.
+//               tcgen05.mma -- S = Q K^T up to two tiles ahead of the softmax, O += P V with P
+//               as bf16 in TMEM over its S buffer and V read MN-major -- polling its inputs
+//               and issuing whichever of the next PV and the next S is ready.
 //   warps 2..9  softmax: two warps per TMEM lane quarter, each owning 64 of a row's 128
 //               columns; the row max is exchanged through shared memory.  Row max, exp2,
-//               row sum, bf16 P back into TMEM, lazy O rescale, and the per-unit merge of
-//               (O, m, l) into the stored state through a staged TMA store / reduce-add.
-//               On partial tiles they stage the keys' tracks and evaluate the mask once
-//               per pair; full tiles skip it; empty tiles are never listed, so never loaded.
+//               row sum, bf16 P back into TMEM, lazy O rescale; at a unit's end they hand
+//               the row's (m, l) to the epilogue and go on with the next unit at once.  On
+//               partial tiles they stage the keys' tracks and evaluate the mask once per
+//               pair; full tiles skip it; empty tiles are never listed, so never loaded.
+//   warps 10..13 epilogue, one thread per row: merge the unit's (O, m, l) into the stored
+//               state through a staged TMA store / reduce-add, while the softmax warps and
+//               the tensor core work on the next unit in the other O buffer.
 // Scores are kept in base-2 units (s * scale * log2 e); the stored m is in the same units
 // and always an integer, so that every rescale (lazy, when the max grows past 2^8, within
 // a call; and the merge with the stored state) multiplies by an exact power of two.
@@ -36,27 +41,47 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 320;              // producer, MMA, 8 softmax warps
-constexpr int kSoftmax = 256;              // softmax threads
+constexpr int kThreads = 480;              // 15 warps, roles above
+constexpr int kSoftmax = 256;              // softmax threads (warps 2..9)
+constexpr int kEpi = 128;                  // epilogue threads (warps 10..13)
+constexpr int kWarpEpi0 = 10;
+constexpr int kWarpSched = 14;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units: rescale O when max grows > 2^8
 constexpr int kPrefetchTiles = 64;         // L2 prefetch depth per unit
+constexpr int kQueue = 4;                  // work-queue entries
 
 enum {
-  B_QFULL, B_QEMPTY,                 // Q slot: TMA fill / last S of the unit done
+  B_QFULL0, B_QFULL1, B_QEMPTY0, B_QEMPTY1,  // Q slots (unit & 1): fill / last S of the unit
   B_KFULL0, B_KFULL1, B_KEMPTY0, B_KEMPTY1,  // K ring (slot = tile & 1): fill / S done
   B_VFULL0, B_VFULL1, B_VEMPTY0, B_VEMPTY1,  // V ring: fill / PV done
   B_SFULL0, B_SFULL1,                // S buffer (tile & 1) computed
   B_PFULL0, B_PFULL1,                // P written over S buffer (256 softmax arrivals)
   B_PVDONE,                          // one phase per tile: its PV has completed
   B_PCONS0, B_PCONS1,                // S buffer (tile & 1): its P consumed by the PV
-  B_OFREE0, B_OFREE1,                // O buffer (unit & 1) read out by the epilogue
+  B_OFULL0, B_OFULL1,                // O buffer (unit & 1): the unit's last PV completed
+  B_OFREE0, B_OFREE1,                // O buffer read out by the epilogue (128 arrivals)
   B_MX0, B_MX1,                      // per-row max exchanged between the two halves
   B_TRK0, B_TRK1,                    // key tracks of a partial tile staged
-  B_EPI,                             // per unit: l and the merge mode exchanged
-  B_STG0, B_STG1,                    // per unit: staging rows of half 0 / half 1 written
-  B_STGMID, B_STGFREE,               // per unit: half 0's / half 1's TMA has read staging
-  B_DRAIN, B_NUM
+  B_EPIRDY0, B_EPIRDY1,              // (m, l) of the unit handed over (256 arrivals)
+  B_HFREE0, B_HFREE1,                // hand-over slot read by the epilogue (128 arrivals)
+  B_EVOTE,                           // per unit: epilogue's merge-mode vote (128 arrivals)
+  B_STG,                             // per staging round: rows written (128 arrivals)
+  B_STGFREE,                         // per staging round: the TMA has read the staging box
+  B_UFULL0,                          // queue entry posted (kQueue barriers)
+  B_UEMPTY0 = B_UFULL0 + kQueue,     // queue entry released (kQueue barriers)
+  B_DRAIN = B_UEMPTY0 + kQueue,
+  B_NUM
 };
+
+__host__ __device__ constexpr int arrivals(int b) {
+  return (b == B_PFULL0 || b == B_PFULL1 || b == B_MX0 || b == B_MX1 || b == B_TRK0 ||
+          b == B_TRK1 || b == B_EPIRDY0 || b == B_EPIRDY1)
+             ? kSoftmax
+             : ((b == B_OFREE0 || b == B_OFREE1 || b == B_HFREE0 || b == B_HFREE1 ||
+                 b == B_EVOTE || b == B_STG)
+                    ? kEpi
+                    : 1);
+}
 
 struct FwdParams {
   CUtensorMap q_map, k_map, v_map;
@@ -65,6 +90,8 @@ struct FwdParams {
   const int32_t* step_col;
   const uint8_t* step_tag;
   const int32_t* tracks;  // [4][n] sample, seg, noise, pos in plan order
+  const int32_t* order;   // work order of this step: q blocks of the shard, longest first
+  unsigned* sched;        // ticket counter pair of this launch
   float* o_acc;
   float* m;
   float* l;
@@ -74,6 +101,7 @@ struct FwdParams {
   int P, bps, q_shard, kv_shard;
   int hq, group;
   int units;  // bps * hq
+  int nwork;  // units with at least one tile: nonempty blocks of the order x hq
   int W;
   int first;
   float scale_log2;
@@ -95,67 +123,35 @@ __device__ __forceinline__ int unit_tiles(const FwdParams& p, int u, int64_t* e0
   return (int)(b - a);
 }
 
-// Position in this CTA's stream of work: units blockIdx.x, blockIdx.x + gridDim.x, ... with
-// at least one tile; tiles in list order.  g counts tiles, uc counts non-empty units.
-struct Cursor {
-  int unit, T, j, g, uc;
-  int64_t e0;
-  bool valid;
-  __device__ __forceinline__ int h(const FwdParams& p) const { return unit / p.bps; }
-  __device__ __forceinline__ int64_t nq(const FwdParams& p) const {
-    return (int64_t)p.q_shard * p.bps + unit % p.bps;
-  }
+// the work queue in shared memory: entry uc of this CTA sits in slot uc % kQueue
+struct Queue {
+  int unit[kQueue];  // -1: no more work
+  int T[kQueue];
+  long long e0[kQueue];
 };
-
-__device__ __forceinline__ void seek_unit(const FwdParams& p, Cursor& c, int u) {
-  for (; u < p.units; u += gridDim.x) {
-    int64_t e0;
-    const int T = unit_tiles(p, u, &e0);
-    if (T > 0) {
-      c.unit = u;
-      c.T = T;
-      c.e0 = e0;
-      c.j = 0;
-      c.valid = true;
-      return;
-    }
-  }
-  c.valid = false;
-}
-
-__device__ __forceinline__ void cursor_begin(const FwdParams& p, Cursor& c) {
-  c.g = 0;
-  c.uc = 0;
-  seek_unit(p, c, blockIdx.x);
-}
-
-__device__ __forceinline__ void cursor_next(const FwdParams& p, Cursor& c) {
-  ++c.g;
-  if (++c.j == c.T) {
-    ++c.uc;
-    seek_unit(p, c, c.unit + gridDim.x);
-  }
-}
 
 // two-slot rings indexed by the tile counter g: slot g & 1, phase parity (g >> 1) & 1
 __device__ __forceinline__ uint32_t ring_slot(int g) { return (uint32_t)(g & 1); }
 __device__ __forceinline__ uint32_t ring_parity(int g) { return (uint32_t)((g >> 1) & 1); }
 
-// shared memory: Q | K ring (2) | V ring (2) | staging (2 boxes of 128 x 32 fp32) | key tracks
-// [2][4][128] int32 | row-max exchange [2][2][128] f32 | row-sum exchange [2][128] f32
+// shared memory: Q (2) | K ring (2) | V ring (2) | staging (one 128 x 32 fp32 box) | key
+// tracks [2][4][128] int32 | row-max exchange [2][2][128] f32 | hand-over m [2][128] and
+// l [2][2][128] f32
 template <int D>
 struct Smem {
   static constexpr int kTile = 128 * D * 2;
   static constexpr int kQ = 0;
-  static constexpr int kK = kTile;
-  static constexpr int kV = 3 * kTile;
-  static constexpr int kStg = 5 * kTile;
-  static constexpr int kTrk = kStg + 2 * 16384;
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = 4 * kTile;
+  static constexpr int kStg = 6 * kTile;
+  static constexpr int kTrk = kStg + 16384;
   static constexpr int kMx = kTrk + 2 * 512 * 4;
-  static constexpr int kLs = kMx + 2 * 2 * 128 * 4;
-  static constexpr int kEnd = kLs + 2 * 128 * 4;
+  static constexpr int kHm = kMx + 2 * 2 * 128 * 4;
+  static constexpr int kHl = kHm + 2 * 128 * 4;
+  static constexpr int kEnd = kHl + 2 * 2 * 128 * 4;
   static constexpr size_t bytes() { return (size_t)kEnd + 1024; }  // + alignment slack
 };
+static_assert(Smem<128>::bytes() <= 232448, "shared memory budget");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant__ FwdParams p) {
@@ -164,14 +160,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
   constexpr int kAtoms = D / 64;  // 128-byte swizzle atoms along d
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem + L::kQ;
-  uint8_t* sK = smem + L::kK;  // slot s at sK + s * kTile
+  uint8_t* sQ = smem + L::kQ;  // slot b at sQ + b * kTile
+  uint8_t* sK = smem + L::kK;
   uint8_t* sV = smem + L::kV;
   uint8_t* sStg = smem + L::kStg;
   int32_t* ktr = reinterpret_cast<int32_t*>(smem + L::kTrk);
   float* mxs = reinterpret_cast<float*>(smem + L::kMx);
-  float* lss = reinterpret_cast<float*>(smem + L::kLs);
+  float* hm = reinterpret_cast<float*>(smem + L::kHm);
+  float* hl = reinterpret_cast<float*>(smem + L::kHl);
   __shared__ __align__(8) uint64_t bar[B_NUM];
+  __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int epi_mode[2];
@@ -182,13 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
   if (threadIdx.x == 0) {
     abort_flag = 0;
     epi_mode[0] = epi_mode[1] = 0;
-    for (int b = 0; b < B_NUM; ++b) {
-      const bool softmax_wide = b == B_PFULL0 || b == B_PFULL1 || b == B_OFREE0 ||
-                                b == B_OFREE1 || b == B_MX0 || b == B_MX1 || b == B_TRK0 ||
-                                b == B_TRK1 || b == B_EPI;
-      const bool half_wide = b == B_STG0 || b == B_STG1;
-      mbar_init(&bar[b], softmax_wide ? kSoftmax : (half_wide ? kSoftmax / 2 : 1));
-    }
+    for (int b = 0; b < B_NUM; ++b) mbar_init(&bar[b], arrivals(b));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -201,7 +193,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
   const uint32_t tS = tmem_base;        // S buffers at +0 and +128
   const uint32_t tO = tmem_base + 256;  // O buffers at +0 and +128
 
-  if (warp == 0) {
+  if (warp == kWarpSched) {
+    // ------------------------------------------------------------------ scheduler
+    if (lane == 0) {
+      for (int uc = 0;; ++uc) {
+        const int slot = uc % kQueue;
+        if (uc >= kQueue && !mbar_wait(&bar[B_UEMPTY0 + slot], ((uc / kQueue) - 1) & 1, w)) break;
+        int unit = -1, T = 0;
+        int64_t e0 = 0;
+        const unsigned t = atomicAdd(p.sched, 1u);
+        if (t < (unsigned)p.nwork) {
+          unit = (int)(t % (unsigned)p.hq) * p.bps + p.order[t / (unsigned)p.hq];
+          T = unit_tiles(p, unit, &e0);
+        }
+        queue.unit[slot] = unit;
+        queue.T[slot] = T;
+        queue.e0[slot] = e0;
+        mbar_arrive(&bar[B_UFULL0 + slot]);
+        if (unit < 0) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.q_map);
@@ -209,78 +222,106 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
       tma_prefetch_desc(&p.v_map);
       tma_prefetch_desc(&p.o_map);
     }
-    Cursor c;
-    cursor_begin(p, c);
-    int q_fills = 0, k_fills = 0, v_fills = 0;  // fills issued (k/v fill t is tile t)
-    while (c.valid) {
-      const int h = c.h(p);
+    int uc = 0, g = 0;          // units reached, tiles reached
+    int q_fills = 0, k_fills = 0, v_fills = 0;  // copies issued (fill t of K/V is tile t)
+    bool ok = true;
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[B_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int unit = queue.unit[slot];
+      if (unit < 0) break;
+      const int T = queue.T[slot];
+      const int64_t e0 = queue.e0[slot];
+      const int h = unit / p.bps;
       const int kvh = h / p.group;
-      if (c.j == 0) {
-        // Q of a new unit once the previous unit's last S has read the slot
-        if (c.uc > 0 && !warp_wait(&bar[B_QEMPTY], (c.uc - 1) & 1, w)) break;
+      const int64_t nq = (int64_t)p.q_shard * p.bps + unit % p.bps;
+      // Q of the unit once the unit two back has finished reading the slot
+      const int qb = uc & 1;
+      if (uc >= 2 && !wait_all(&bar[B_QEMPTY0 + qb], ((uc >> 1) - 1) & 1, w)) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar[B_QFULL0 + qb], kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(sQ + qb * kTile + a * 16384, &p.q_map, &bar[B_QFULL0 + qb], a * 64,
+                      (int)(nq * 128), h);
+      }
+      ++q_fills;
+      // pull the unit's K/V tiles toward L2 ahead of their loads
+      for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
+        const int nk = p.step_col[e0 + j];
+        for (int a = 0; a < kAtoms; ++a) {
+          tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
+          tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
+        }
+      }
+      for (int j = 0; j < T; ++j, ++g) {
+        const int nk = p.step_col[e0 + j];
+        const uint32_t s = ring_slot(g);
+        if (g >= 2 && !wait_all(&bar[B_KEMPTY0 + s], ring_parity(g - 2), w)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar[B_QFULL], kTile);
+          mbar_arrive_expect_tx(&bar[B_KFULL0 + s], kTile);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_3d(sQ + a * 16384, &p.q_map, &bar[B_QFULL], a * 64, (int)(c.nq(p) * 128), h);
+            tma_load_3d(sK + s * kTile + a * 16384, &p.k_map, &bar[B_KFULL0 + s], a * 64,
+                        nk * 128, kvh);
         }
-        ++q_fills;
-        // pull the unit's K/V tiles toward L2 ahead of their loads
-        for (int j = lane; j < c.T && j < kPrefetchTiles; j += 32) {
-          const int nk = p.step_col[c.e0 + j];
-          for (int a = 0; a < kAtoms; ++a) {
-            tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
-            tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
-          }
+        ++k_fills;
+        if (g >= 2 && !wait_all(&bar[B_VEMPTY0 + s], ring_parity(g - 2), w)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[B_VFULL0 + s], kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(sV + s * kTile + a * 16384, &p.v_map, &bar[B_VFULL0 + s], a * 64,
+                        nk * 128, kvh);
         }
+        ++v_fills;
       }
-      const int nk = p.step_col[c.e0 + c.j];
-      const uint32_t s = ring_slot(c.g);
-      if (c.g >= 2 && !warp_wait(&bar[B_KEMPTY0 + s], ring_parity(c.g - 2), w)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar[B_KFULL0 + s], kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sK + s * kTile + a * 16384, &p.k_map, &bar[B_KFULL0 + s], a * 64, nk * 128,
-                      kvh);
-      }
-      ++k_fills;
-      if (c.g >= 2 && !warp_wait(&bar[B_VEMPTY0 + s], ring_parity(c.g - 2), w)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar[B_VFULL0 + s], kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sV + s * kTile + a * 16384, &p.v_map, &bar[B_VFULL0 + s], a * 64, nk * 128,
-                      kvh);
-      }
-      ++v_fills;
-      cursor_next(p, c);
+      ++uc;
     }
     // never leave the CTA with a copy still landing in its shared memory: the fills of a
-    // slot complete in order, so waiting for the latest fill of each slot suffices
+    // slot complete in order, so waiting for the latest fill of each slot suffices (Q fill
+    // f went to slot f & 1, K and V fill t to ring slot t & 1)
     if (lane == 0) {
-      if (q_fills) drain_wait(&bar[B_QFULL], (q_fills - 1) & 1, p.wait_ns, p.err);
+      for (int f = q_fills - 1; f >= 0 && f >= q_fills - 2; --f)
+        drain_wait(&bar[B_QFULL0 + (f & 1)], (f >> 1) & 1, p.wait_ns, p.err);
       for (int t = k_fills - 1; t >= 0 && t >= k_fills - 2; --t)
         drain_wait(&bar[B_KFULL0 + ring_slot(t)], ring_parity(t), p.wait_ns, p.err);
       for (int t = v_fills - 1; t >= 0 && t >= v_fills - 2; --t)
         drain_wait(&bar[B_VFULL0 + ring_slot(t)], ring_parity(t), p.wait_ns, p.err);
     }
     __syncwarp();
-  }
-  else if (warp == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdO = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aK0 = smem_u32(sK), aV0 = smem_u32(sV);
-      // Event loop: issue whichever of the next PV (priority: it feeds the softmax and the
-      // epilogue) and the next S (at most two tiles ahead of the next PV) has its inputs
-      // ready, polling with non-blocking tests; a wait for S's inputs never delays a PV.
-      Cursor cs, cp;
-      cursor_begin(p, cs);
-      cursor_begin(p, cp);
-      uint64_t t_last = globaltimer_ns();
+      const uint32_t aQ0 = smem_u32(sQ), aK0 = smem_u32(sK), aV0 = smem_u32(sV);
+      // Event loop over two cursors into the work queue: issue whichever of the next PV
+      // (priority: it feeds the softmax and the epilogue) and the next S (at most two tiles
+      // ahead of the next PV) has its inputs ready, polling with non-blocking tests.
+      struct Cur {
+        int uc, j, g, T, state;  // state: 0 waiting for queue entry uc, 1 in a unit, 2 done
+      };
+      Cur cs{0, 0, 0, 0, 0}, cp{0, 0, 0, 0, 0};
+      auto fetch = [&](Cur& c) {
+        if (c.state != 0) return;
+        const int slot = c.uc % kQueue;
+        if (!mbar_test(&bar[B_UFULL0 + slot], (c.uc / kQueue) & 1)) return;
+        c.state = queue.unit[slot] < 0 ? 2 : 1;
+        c.T = queue.T[slot];
+        c.j = 0;
+      };
+      auto advance = [](Cur& c) {
+        ++c.g;
+        if (++c.j == c.T) {
+          ++c.uc;
+          c.state = 0;
+        }
+      };
+      uint64_t t_idle = 0;
       uint32_t idle = 0;
-      while (cp.valid || cs.valid) {
+      while (cs.state != 2 || cp.state != 2) {
+        fetch(cs);
+        fetch(cp);
         bool progressed = false;
-        if (cp.valid) {
+        if (cp.state == 1) {
           const int g = cp.g;
           const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g), ob = (uint32_t)(cp.uc & 1);
           // the first PV of a unit overwrites its O buffer: the unit two back must be read out
@@ -299,19 +340,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
             mma_commit(&bar[B_PVDONE]);
             mma_commit(&bar[B_PCONS0 + b]);
             mma_commit(&bar[B_VEMPTY0 + s]);
-            cursor_next(p, cp);
+            if (cp.j == cp.T - 1) mma_commit(&bar[B_OFULL0 + ob]);
+            advance(cp);
             progressed = true;
           }
         }
-        if (cs.valid && (!cp.valid || cs.g < cp.g + 2)) {
+        if (cs.state == 1 && cs.g < cp.g + 2) {
           const int g = cs.g;
-          const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g);
-          const bool ready = (cs.j != 0 || mbar_test(&bar[B_QFULL], cs.uc & 1)) &&
+          const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g), qb = (uint32_t)(cs.uc & 1);
+          const bool ready = (cs.j != 0 || mbar_test(&bar[B_QFULL0 + qb], (cs.uc >> 1) & 1)) &&
                              mbar_test(&bar[B_KFULL0 + s], ring_parity(g)) &&
                              (g < 2 || mbar_test(&bar[B_PCONS0 + b], ((g - 2) >> 1) & 1));
           if (ready) {
             tc_fence_after();
-            const uint32_t aK = aK0 + s * kTile;
+            const uint32_t aQ = aQ0 + qb * kTile, aK = aK0 + s * kTile;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
               const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -320,19 +362,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
             }
             mma_commit(&bar[B_SFULL0 + b]);
             mma_commit(&bar[B_KEMPTY0 + s]);
-            if (cs.j == cs.T - 1) mma_commit(&bar[B_QEMPTY]);  // the unit's last read of Q
-            cursor_next(p, cs);
+            if (cs.j == cs.T - 1) mma_commit(&bar[B_QEMPTY0 + qb]);  // the unit's last read of Q
+            advance(cs);
             progressed = true;
           }
         }
         if (progressed) {
-          t_last = globaltimer_ns();
           idle = 0;
         } else {
+          // the clock is read only while idle, so that it never delays an issue
           __nanosleep(32);
           if ((++idle & 63) == 0) {
             if (*w.abort) break;
-            if (globaltimer_ns() - t_last > p.wait_ns) {
+            const uint64_t now = globaltimer_ns();
+            if (idle == 64) {
+              t_idle = now;
+            } else if (now - t_idle > p.wait_ns) {
               atomicOr(p.err, kErrTimeout);
               *w.abort = 1;
               break;
@@ -346,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
     }
     __syncwarp();
   }
-  else {
+  else if (warp < kWarpEpi0) {
     // ------------------------------------------------------------------ softmax warps
     // two warps per TMEM lane quarter: `half` owns S columns [64 half, 64 half + 64) and O
     // columns [D/2 half, D/2 half + D/2) of its row
@@ -355,6 +400,143 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
+    int uc = 0, g = 0, n_partial = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[B_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int unit = queue.unit[slot];
+      if (unit < 0) break;
+      const int T = queue.T[slot];
+      const int64_t e0 = queue.e0[slot];
+      const int64_t tq = ((int64_t)p.q_shard * p.bps + unit % p.bps) * 128 + row;
+      const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
+                pq = p.tracks[3 * n + tq];
+      const uint32_t ob = tO + (uint32_t)(uc & 1) * 128;
+      float m_run = -INFINITY, l_h = 0.f;
+      for (int j = 0; j < T; ++j, ++g) {
+        const uint32_t b = (uint32_t)(g & 1);
+        const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
+        uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
+        if (partial) {
+          // stage the 128 keys' tracks in one of two buffers (the two halves load two tracks
+          // each); every softmax thread arrives before any reads, so a buffer is rewritten
+          // only after every thread left its previous use
+          const int bb = n_partial & 1;
+          const uint32_t par = (n_partial >> 1) & 1;
+          ++n_partial;
+          int32_t* kt = ktr + bb * 512;
+          const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
+          if (half == 0) {
+            kt[row] = p.tracks[t];
+            kt[128 + row] = p.tracks[n + t];
+          } else {
+            kt[256 + row] = p.tracks[2 * n + t];
+            kt[384 + row] = p.tracks[3 * n + t];
+          }
+          mbar_arrive(&bar[B_TRK0 + bb]);
+          if (!wait_all(&bar[B_TRK0 + bb], par, w)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int kc0 = (2 * half + cc) * 32;
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t2 = 0; t2 < 32; ++t2) {
+              const int kc = kc0 + t2;
+              bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc],
+                                  kt[384 + kc], p.W) ? 1u : 0u) << t2;
+            }
+            lm[cc] = bits;
+          }
+        }
+        if (!wait_all(&bar[B_SFULL0 + b], (g >> 1) & 1, w)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t sb = tS + b * 128;
+        uint32_t v[2][32];
+        tmem_ld32(sb + lb + (2 * half) * 32, v[0]);
+        tmem_ld32(sb + lb + (2 * half + 1) * 32, v[1]);
+        tmem_ld_wait();
+        // scaled, masked scores (kept in v) and this half's row maximum
+        float mx = -INFINITY;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) {
+            const float s = ((lm[cc] >> t) & 1u) ? __uint_as_float(v[cc][t]) * sl2 : -INFINITY;
+            v[cc][t] = __float_as_uint(s);
+            mx = fmaxf(mx, s);
+          }
+        }
+        float* mxb = mxs + b * 256;
+        mxb[half * 128 + row] = mx;
+        mbar_arrive(&bar[B_MX0 + b]);
+        if (!wait_all(&bar[B_MX0 + b], (g >> 1) & 1, w)) { ok = false; break; }
+        mx = fmaxf(mx, mxb[(1 - half) * 128 + row]);
+        // the running max is kept integral (base 2): every rescale factor below is then an
+        // exact power of two, and bf16 rounding of P does not depend on which keys a step
+        // happened to see first
+        const float m_new = ceilf(mx);
+        const bool grow = m_new > m_run + kRescaleThreshold;
+        const bool need = grow && (m_run != -INFINITY);  // earlier tiles of this unit to rescale
+        const float alpha = need ? ldexpf(1.f, (int)(m_run - m_new)) : 1.f;
+        if (grow) {
+          l_h *= alpha;
+          m_run = m_new;
+        }
+        // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
+        // must (alpha = 1 on the others).  A row that needs it has a finite max from an
+        // earlier tile of this unit, so PV(g-1) is the accumulation to wait for.
+        if (__any_sync(0xffffffffu, need)) {
+          if (!wait_all(&bar[B_PVDONE], (g - 1) & 1, w)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int cc = 0; cc < D / 64; ++cc) {
+            const uint32_t col = half * (D / 2) + cc * 32;
+            uint32_t x[32];
+            tmem_ld32(ob + lb + col, x);
+            tmem_ld_wait();
+#pragma unroll
+            for (int t = 0; t < 32; ++t) x[t] = __float_as_uint(__uint_as_float(x[t]) * alpha);
+            tmem_st32(ob + lb + col, x);
+          }
+        }
+        // P = exp2(s - m_run) as bf16, packed into columns [64 half, 64 half + 32) of the S
+        // buffer: inside the fp32 columns this warp has just read
+        const float base = (m_run == -INFINITY) ? 0.f : m_run;
+        float rs = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int t = 0; t < 32; t += 2) {
+            const float p0 = fast_exp2(__uint_as_float(v[cc][t]) - base);
+            const float p1 = fast_exp2(__uint_as_float(v[cc][t + 1]) - base);
+            rs += p0 + p1;
+            pk[t >> 1] = pack_bf16(p0, p1);
+          }
+          tmem_st16(sb + lb + half * 64 + cc * 16, pk);
+        }
+        tmem_st_wait();
+        l_h += rs;
+        tc_fence_before();
+        mbar_arrive(&bar[B_PFULL0 + b]);
+      }
+      if (!ok) break;
+      // hand the unit's (m, l) to the epilogue once it has read the slot's previous use
+      const int ub = uc & 1;
+      if (uc >= 2 && !wait_all(&bar[B_HFREE0 + ub], ((uc >> 1) - 1) & 1, w)) break;
+      if (half == 0) hm[ub * 128 + row] = m_run;
+      hl[(ub * 2 + half) * 128 + row] = l_h;
+      mbar_arrive(&bar[B_EPIRDY0 + ub]);
+      ++uc;
+    }
+  }
+  else {
+    // ------------------------------------------------------------------ epilogue warps
+    // one thread per row (warp w owns TMEM lane quarter w & 3)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;
+    const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     if (p.first) {
       // rows of units without a tile in this step start from (O = 0, m = -inf, l = 0)
       for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
@@ -362,243 +544,112 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         if (unit_tiles(p, u, &e0) != 0) continue;
         const int h = u / p.bps;
         const int64_t tq = ((int64_t)p.q_shard * p.bps + u % p.bps) * 128 + row;
-        if (half == 0) {
-          p.m[(int64_t)h * n + tq] = -INFINITY;
-          p.l[(int64_t)h * n + tq] = 0.f;
-        }
-        float4* o = reinterpret_cast<float4*>(p.o_acc + (tq * p.hq + h) * D + half * (D / 2));
-#pragma unroll
-        for (int t = 0; t < D / 8; ++t) o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.m[(int64_t)h * n + tq] = -INFINITY;
+        p.l[(int64_t)h * n + tq] = 0.f;
+        float4* o = reinterpret_cast<float4*>(p.o_acc + (tq * p.hq + h) * D);
+#pragma unroll 8
+        for (int t = 0; t < D / 4; ++t) o[t] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    Cursor c;
-    cursor_begin(p, c);
+    // Merge each unit's (O, m, l) into the stored state through one staged fp32 box of 32
+    // columns at a time:
+    //   FIRST         the tile is stored (TMA store);
+    //   otherwise     the stored max is kept unless some row's max grew past it by more
+    //                 than the lazy threshold, so the update is a pure addition of
+    //                 O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
+    //   some row grew exact merge with the stored tile (loaded by the row threads), then a
+    //                 TMA store.
+    int uc = 0, k = 0;  // units merged, staging rounds
     bool ok = true;
-    int n_partial = 0;
-    float m_run = -INFINITY, l_h = 0.f;
-    int sq = 0, gq = -1, zq = -1, pq = 0;
-    while (ok && c.valid) {
-      const int g = c.g;
-      const uint32_t b = (uint32_t)(g & 1);
-      const int h = c.h(p);
-      const int64_t tq = c.nq(p) * 128 + row;
-      if (c.j == 0) {
-        sq = p.tracks[tq];
-        gq = p.tracks[n + tq];
-        zq = p.tracks[2 * n + tq];
-        pq = p.tracks[3 * n + tq];
-        m_run = -INFINITY;
-        l_h = 0.f;
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[B_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int unit = queue.unit[slot];
+      if (unit < 0) break;
+      const int h = unit / p.bps;
+      const int64_t q0 = ((int64_t)p.q_shard * p.bps + unit % p.bps) * 128;
+      const int64_t tq = q0 + row;
+      const int64_t gi = (int64_t)h * n + tq;
+      float m_old = -INFINITY, l_old = 0.f;
+      if (!p.first) {
+        m_old = p.m[gi];
+        l_old = p.l[gi];
       }
-      const bool partial = p.step_tag[c.e0 + c.j] == MARBLE_TILE_PARTIAL;
-      uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
-      if (partial) {
-        // stage the 128 keys' tracks in one of two buffers (the two halves load two tracks
-        // each); every softmax thread arrives before any reads, so a buffer is rewritten
-        // only after every thread left its previous use
-        const int bb = n_partial & 1;
-        const uint32_t par = (n_partial >> 1) & 1;
-        ++n_partial;
-        int32_t* kt = ktr + bb * 512;
-        const int64_t t = (int64_t)p.step_col[c.e0 + c.j] * 128 + row;
-        if (half == 0) {
-          kt[row] = p.tracks[t];
-          kt[128 + row] = p.tracks[n + t];
-        } else {
-          kt[256 + row] = p.tracks[2 * n + t];
-          kt[384 + row] = p.tracks[3 * n + t];
-        }
-        mbar_arrive(&bar[B_TRK0 + bb]);
-        if (!wait_all(&bar[B_TRK0 + bb], par, w)) { ok = false; break; }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int kc0 = (2 * half + cc) * 32;
-          uint32_t bits = 0;
-#pragma unroll
-          for (int t2 = 0; t2 < 32; ++t2) {
-            const int kc = kc0 + t2;
-            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc], kt[384 + kc],
-                                p.W) ? 1u : 0u) << t2;
-          }
-          lm[cc] = bits;
-        }
-      }
-      if (!wait_all(&bar[B_SFULL0 + b], (g >> 1) & 1, w)) { ok = false; break; }
+      const int ub = uc & 1;
+      if (!wait_all(&bar[B_EPIRDY0 + ub], (uc >> 1) & 1, w)) break;
+      const float m_run = hm[ub * 128 + row];
+      const float l_run = hl[ub * 256 + row] + hl[ub * 256 + 128 + row];
+      mbar_arrive(&bar[B_HFREE0 + ub]);
+      // the merge mode is one per unit: the four warps vote
+      const bool grows = !p.first && m_old != -INFINITY && m_run > m_old + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_mode[uc & 1], 1);
+      mbar_arrive(&bar[B_EVOTE]);
+      if (!wait_all(&bar[B_EVOTE], uc & 1, w)) break;
+      const int mode = p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
+      // every epilogue thread has read the other flag (before this vote), and none can vote
+      // on the next unit before row 0 has passed its first staging round of this one
+      if (row == 0) epi_mode[(uc + 1) & 1] = 0;
+      if (!wait_all(&bar[B_OFULL0 + ub], (uc >> 1) & 1, w)) break;
       tc_fence_after();
-      const uint32_t sb = tS + b * 128;
-      uint32_t v[2][32];
-      tmem_ld32(sb + lb + (2 * half) * 32, v[0]);
-      tmem_ld32(sb + lb + (2 * half + 1) * 32, v[1]);
-      tmem_ld_wait();
-      // scaled, masked scores (kept in v) and this half's row maximum
-      float mx = -INFINITY;
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const float s = ((lm[cc] >> t) & 1u) ? __uint_as_float(v[cc][t]) * sl2 : -INFINITY;
-          v[cc][t] = __float_as_uint(s);
-          mx = fmaxf(mx, s);
-        }
+      // every role is past queue entry uc: the producer and the S cursor before the last S,
+      // the PV cursor before the last PV, the softmax before the hand-over, and this group
+      // before the vote
+      if (row == 0) mbar_arrive(&bar[B_UEMPTY0 + slot]);
+      float a_new = 1.f, a_old = 0.f, m_out = m_run, l_out = l_run;
+      if (mode == 1) {
+        m_out = (m_old == -INFINITY) ? m_run : m_old;
+        a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
+        l_out = l_old + l_run * a_new;
+      } else if (mode == 2) {
+        m_out = fmaxf(m_old, m_run);  // both integral: the factors are exact powers of two
+        a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
+        a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
+        l_out = l_old * a_old + l_run * a_new;
       }
-      float* mxb = mxs + b * 256;
-      mxb[half * 128 + row] = mx;
-      mbar_arrive(&bar[B_MX0 + b]);
-      if (!wait_all(&bar[B_MX0 + b], (g >> 1) & 1, w)) { ok = false; break; }
-      mx = fmaxf(mx, mxb[(1 - half) * 128 + row]);
-      // the running max is kept integral (base 2): every rescale factor below is then an
-      // exact power of two, and bf16 rounding of P does not depend on which keys a step
-      // happened to see first
-      const float m_new = ceilf(mx);
-      const bool grow = m_new > m_run + kRescaleThreshold;
-      const bool need = grow && (m_run != -INFINITY);  // earlier tiles of this unit to rescale
-      const float alpha = need ? ldexpf(1.f, (int)(m_run - m_new)) : 1.f;
-      if (grow) {
-        l_h *= alpha;
-        m_run = m_new;
-      }
-      // tcgen05.ld/st are warp-collective: the whole warp rescales when any of its rows
-      // must (alpha = 1 on the others).  A row that needs it has a finite max from an
-      // earlier tile of this unit, so PV(g-1) is the accumulation to wait for.
-      if (__any_sync(0xffffffffu, need)) {
-        if (!wait_all(&bar[B_PVDONE], (g - 1) & 1, w)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t ob = tO + (uint32_t)(c.uc & 1) * 128;
+      p.m[gi] = m_out;
+      p.l[gi] = l_out;
+      const uint32_t ob = tO + (uint32_t)ub * 128;
+      const float4* src = reinterpret_cast<const float4*>(p.o_acc + (tq * p.hq + h) * D);
 #pragma unroll 1
-        for (int cc = 0; cc < D / 64; ++cc) {
-          const uint32_t col = half * (D / 2) + cc * 32;
-          uint32_t x[32];
-          tmem_ld32(ob + lb + col, x);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) x[t] = __float_as_uint(__uint_as_float(x[t]) * alpha);
-          tmem_st32(ob + lb + col, x);
+      for (int r = 0; r < D / 32; ++r, ++k) {
+        if (k > 0 && !wait_all(&bar[B_STGFREE], (k - 1) & 1, w)) { ok = false; break; }
+        uint32_t x[32];
+        tmem_ld32(ob + lb + r * 32, x);
+        tmem_ld_wait();
+        if (r == D / 32 - 1) {
+          // the O buffer can take unit uc + 2
+          tc_fence_before();
+          mbar_arrive(&bar[B_OFREE0 + ub]);
         }
-      }
-      // P = exp2(s - m_run) as bf16, packed into columns [64 half, 64 half + 32) of the S
-      // buffer: inside the fp32 columns this warp has just read
-      const float base = (m_run == -INFINITY) ? 0.f : m_run;
-      float rs = 0.f;
+        float vals[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const float p0 = fast_exp2(__uint_as_float(v[cc][t]) - base);
-          const float p1 = fast_exp2(__uint_as_float(v[cc][t + 1]) - base);
-          rs += p0 + p1;
-          pk[t >> 1] = pack_bf16(p0, p1);
-        }
-        tmem_st16(sb + lb + half * 64 + cc * 16, pk);
-      }
-      tmem_st_wait();
-      l_h += rs;
-      tc_fence_before();
-      mbar_arrive(&bar[B_PFULL0 + b]);
-      if (c.j == c.T - 1) {
-        // ---------------------------------------------------------------- unit epilogue
-        // Merge this call's (O, m, l) into the stored state through a staged tile:
-        //   FIRST         the tile is stored (TMA store);
-        //   otherwise     the stored max is kept unless some row's max grew past it by more
-        //                 than the lazy threshold, so the update is a pure addition of
-        //                 O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
-        //   some row grew exact merge with the stored tile (loaded by the row threads),
-        //                 then a TMA store.
-        // The 32 KB staging buffer holds one half's boxes at a time: half 0 stages and its
-        // TMA reads, then half 1 (the next unit's half 0 waits for half 1's TMA).
-        const int uc = c.uc;
-        // PV(g-2) is done (S(g) needed its P consumed), but PV(g-1) may not be: wait for
-        // PV(g-1) then PV(g), so that no parity wait runs two phases ahead of the barrier
-        if (g >= 1 && !wait_all(&bar[B_PVDONE], (g - 1) & 1, w)) { ok = false; break; }
-        if (!wait_all(&bar[B_PVDONE], g & 1, w)) { ok = false; break; }
-        tc_fence_after();
-        const int64_t gi = (int64_t)h * n + tq;
-        float m_old = -INFINITY, l_old = 0.f;
-        if (!p.first) {
-          m_old = p.m[gi];
-          l_old = p.l[gi];
-        }
-        const bool grows = !p.first && m_old != -INFINITY && m_run > m_old + kRescaleThreshold;
-        lss[half * 128 + row] = l_h;
-        if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_mode[uc & 1], 1);
-        mbar_arrive(&bar[B_EPI]);
-        if (!wait_all(&bar[B_EPI], uc & 1, w)) { ok = false; break; }
-        const float l_run = lss[row] + lss[128 + row];
-        const int mode = p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
-        if (row == 0 && half == 0) epi_mode[(uc + 1) & 1] = 0;  // every thread has read it
-        float a_new = 1.f, a_old = 0.f, m_out = m_run, l_out = l_run;
-        if (mode == 1) {
-          m_out = (m_old == -INFINITY) ? m_run : m_old;
-          a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
-          l_out = l_old + l_run * a_new;
-        } else if (mode == 2) {
-          m_out = fmaxf(m_old, m_run);  // both integral: the factors are exact powers of two
-          a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
-          a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
-          l_out = l_old * a_old + l_run * a_new;
-        }
-        // this half's O columns out of TMEM; then the O buffer can take unit uc + 2
-        const uint32_t ob = tO + (uint32_t)(uc & 1) * 128;
-        float ov[D / 64][32];
-#pragma unroll
-        for (int cc = 0; cc < D / 64; ++cc) {
-          uint32_t x[32];
-          tmem_ld32(ob + lb + half * (D / 2) + cc * 32, x);
-          tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) ov[cc][t] = __uint_as_float(x[t]) * a_new;
-        }
-        tc_fence_before();
-        mbar_arrive(&bar[B_OFREE0 + (uc & 1)]);
+        for (int t = 0; t < 32; ++t) vals[t] = __uint_as_float(x[t]) * a_new;
         if (mode == 2) {
-          const float4* src =
-              reinterpret_cast<const float4*>(p.o_acc + (tq * p.hq + h) * D + half * (D / 2));
 #pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc)
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              const float4 o = src[cc * 8 + t];
-              ov[cc][4 * t] += o.x * a_old;
-              ov[cc][4 * t + 1] += o.y * a_old;
-              ov[cc][4 * t + 2] += o.z * a_old;
-              ov[cc][4 * t + 3] += o.w * a_old;
-            }
+          for (int t = 0; t < 8; ++t) {
+            const float4 o = src[r * 8 + t];
+            vals[4 * t] += o.x * a_old;
+            vals[4 * t + 1] += o.y * a_old;
+            vals[4 * t + 2] += o.z * a_old;
+            vals[4 * t + 3] += o.w * a_old;
+          }
         }
-        if (half == 0) {
-          p.m[gi] = m_out;
-          p.l[gi] = l_out;
-        }
-        // staging round of this half
-        bool stg_ok;
-        if (half == 0)
-          stg_ok = uc == 0 || wait_all(&bar[B_STGFREE], (uc - 1) & 1, w);
-        else
-          stg_ok = wait_all(&bar[B_STGMID], uc & 1, w);
-        if (stg_ok) {
-#pragma unroll
-          for (int cc = 0; cc < D / 64; ++cc) stage_row32(sStg + cc * 16384, row, ov[cc]);
-          fence_proxy_async_smem();
-        }
-        mbar_arrive(&bar[B_STG0 + half]);
+        stage_row32(sStg, row, vals);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[B_STG]);
         if (row == 0) {
-          if (stg_ok && mbar_wait(&bar[B_STG0 + half], uc & 1, w)) {
-            const int y = (int)(c.nq(p) * 128);
-#pragma unroll
-            for (int cc = 0; cc < D / 64; ++cc) {
-              const int x0 = (half * (D / 64) + cc) * 32;
-              if (mode == 1)
-                tma_reduce_add_3d(&p.o_map, sStg + cc * 16384, x0, y, h);
-              else
-                tma_store_3d(&p.o_map, sStg + cc * 16384, x0, y, h);
-            }
+          if (mbar_wait(&bar[B_STG], k & 1, w)) {
+            if (mode == 1)
+              tma_reduce_add_3d(&p.o_map, sStg, r * 32, (int)q0, h);
+            else
+              tma_store_3d(&p.o_map, sStg, r * 32, (int)q0, h);
             bulk_commit();
             bulk_wait_read_all();
           }
-          mbar_arrive(&bar[half == 0 ? B_STGMID : B_STGFREE]);
+          mbar_arrive(&bar[B_STGFREE]);
         }
-        if (!stg_ok) { ok = false; break; }
       }
-      cursor_next(p, c);
+      ++uc;
     }
     // the global writes of every TMA store / reduce this thread issued have completed
     if (row == 0) bulk_wait_all();
@@ -610,9 +661,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (threadIdx.x == 0) {
+    // every CTA of the launch has drawn its last ticket once it gets here: the last one to
+    // arrive puts the counter pair back to zero for a later launch
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
 }
 
-// everything but the shard pair and the FIRST flag: encoded once per call
+// everything but the shard pair, the FIRST flag and the work list: encoded once per call
 template <int D>
 marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
                         const marble_state_t* st, FwdParams* prm) {
@@ -664,13 +724,20 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // persistent: one CTA per SM (each takes all 512 TMEM columns), at most one per unit
-  const unsigned grid = (unsigned)(base.units < sms ? base.units : sms);
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
     prm.first = (flags[i] & MARBLE_STEP_FIRST) ? 1 : 0;
+    const int64_t seg = (int64_t)prm.q_shard * (pl->P + 1) + (prm.kv_shard >= 0 ? prm.kv_shard : pl->P);
+    prm.order = pl->fwd_order + seg * pl->bps;
+    prm.nwork = pl->h_fwd_nwork[seg] * qkv->hq;
+    if (prm.nwork == 0 && !prm.first) continue;  // nothing to add to the state
+    prm.sched = sched_slot(pl);
+    // persistent: one CTA per SM (each takes all 512 TMEM columns); the FIRST call also
+    // initialises the units without tiles, spread over the whole grid
+    const int want = prm.first ? base.units : prm.nwork;
+    const unsigned grid = (unsigned)(want < sms ? want : sms);
     k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), s>>>(prm);
   }
   cudaError_t e = cudaGetLastError();

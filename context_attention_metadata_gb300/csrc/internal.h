@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <string>
 #include <vector>
 
@@ -49,6 +50,18 @@ struct marble_plan {
   uint8_t* colT_tag = nullptr;       // [nnz]
   int64_t* needed_ptr = nullptr;     // [P+1]
   int32_t* needed = nullptr;         // [needed_total]
+  // work lists of the persistent kernels: for shard s and option k (k < P: kv shard k of
+  // the forward / q shard k of the key-side backward; k == P: every shard), the blocks of
+  // shard s with a non-empty list, longest list first
+  int32_t* fwd_order = nullptr;      // [P*(P+1)*bps] over step_ptr (q blocks)
+  int32_t* fwd_nwork = nullptr;      // [P*(P+1)]
+  int32_t* bwd_order = nullptr;      // [P*(P+1)*bps] over colT_ptr (kv blocks)
+  int32_t* bwd_nwork = nullptr;      // [P*(P+1)]
+  std::vector<int32_t> h_fwd_nwork, h_bwd_nwork;
+  // ticket counters of the persistent kernels: launch i uses pair (i mod kSchedSlots); the
+  // last CTA of a launch puts its pair back to zero
+  unsigned* sched = nullptr;         // [2*kSchedSlots]
+  mutable std::atomic<unsigned> sched_next{0};
   unsigned* err = nullptr;           // device error word
   unsigned long long* counters = nullptr;  // [8] device scratch for statistics
   std::vector<int64_t> h_needed_ptr;      // host copy of needed_ptr
@@ -56,6 +69,14 @@ struct marble_plan {
 };
 
 namespace marble {
+
+constexpr int kSchedSlots = 256;
+
+// a ticket-counter pair of `p` for one persistent-kernel launch
+inline unsigned* sched_slot(const marble_plan_t* p) {
+  const unsigned i = p->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
+  return p->sched + 2 * i;
+}
 
 // error reporting (api.cu)
 void set_error(const std::string& msg);

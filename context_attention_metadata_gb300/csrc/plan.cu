@@ -487,6 +487,53 @@ static marble_status_t dalloc(marble_plan_t* p, T** ptr, size_t count) {
   return MARBLE_OK;
 }
 
+// Work order of the persistent attention kernels (one CTA of 1024 threads per segment):
+// segment (s, k) lists the blocks i of shard s whose list for option k is non-empty --
+// option k < P counts the entries of column k of row s*bps+i of `ptr`, option P the whole
+// row -- sorted by that count, longest first (counts above 1023 share a bucket).  Equal
+// counts come out in no fixed order: each unit's result does not depend on where or when
+// it runs.
+__global__ void __launch_bounds__(1024) k_work_order(const int64_t* __restrict__ ptr, int P,
+                                                     int64_t bps, int32_t* __restrict__ order,
+                                                     int32_t* __restrict__ nwork) {
+  __shared__ int hist[1024];
+  __shared__ int scan[1024];
+  const int seg = blockIdx.x;
+  const int s = seg / (P + 1), k = seg % (P + 1);
+  const int c_lo = k < P ? k : 0, c_hi = k < P ? k + 1 : P;
+  hist[threadIdx.x] = 0;
+  __syncthreads();
+  for (int64_t i = threadIdx.x; i < bps; i += blockDim.x) {
+    const int64_t r = (int64_t)s * bps + i;
+    const int64_t c = ptr[r * P + c_hi] - ptr[r * P + c_lo];
+    if (c > 0) atomicAdd(&hist[c < 1023 ? c : 1023], 1);
+  }
+  __syncthreads();
+  // inclusive scan of the histogram read from the top bucket down (Hillis-Steele)
+  const int t = threadIdx.x;
+  scan[t] = hist[1023 - t];
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {
+    const int v = t >= off ? scan[t - off] : 0;
+    __syncthreads();
+    scan[t] += v;
+    __syncthreads();
+  }
+  // first output position of bucket b = entries in buckets above b
+  const int b = 1023 - t;
+  const int start = scan[t] - hist[b];
+  __syncthreads();
+  hist[b] = start;  // reused as the bucket cursors
+  if (t == 1023) nwork[seg] = scan[1023];
+  __syncthreads();
+  int32_t* out = order + (int64_t)seg * bps;
+  for (int64_t i = threadIdx.x; i < bps; i += blockDim.x) {
+    const int64_t r = (int64_t)s * bps + i;
+    const int64_t c = ptr[r * P + c_hi] - ptr[r * P + c_lo];
+    if (c > 0) out[atomicAdd(&hist[c < 1023 ? c : 1023], 1)] = (int32_t)i;
+  }
+}
+
 #define MARBLE_TRY(x)                     \
   do {                                    \
     marble_status_t st_ = (x);            \
@@ -512,6 +559,11 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->step_ptr, nb * P + 1));
   MARBLE_TRY(dalloc(p, &p->colT_ptr, nb * P + 1));
   MARBLE_TRY(dalloc(p, &p->needed_ptr, P + 1));
+  MARBLE_TRY(dalloc(p, &p->fwd_order, (size_t)P * (P + 1) * bps));
+  MARBLE_TRY(dalloc(p, &p->fwd_nwork, (size_t)P * (P + 1)));
+  MARBLE_TRY(dalloc(p, &p->bwd_order, (size_t)P * (P + 1) * bps));
+  MARBLE_TRY(dalloc(p, &p->bwd_nwork, (size_t)P * (P + 1)));
+  MARBLE_TRY(dalloc(p, &p->sched, 2 * kSchedSlots));
   // scratch: counters of the two-pass compactions and the order builder
   int32_t *cnt = nullptr, *cnt2 = nullptr, *cntT = nullptr, *ucost = nullptr,
           *rank_of = nullptr, *unit_new = nullptr, *ncount = nullptr;
@@ -545,6 +597,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
 
   MARBLE_CK(cudaMemsetAsync(p->err, 0, 4 * sizeof(unsigned), s));
   MARBLE_CK(cudaMemsetAsync(p->counters, 0, 8 * sizeof(unsigned long long), s));
+  MARBLE_CK(cudaMemsetAsync(p->sched, 0, 2 * kSchedSlots * sizeof(unsigned), s));
   MARBLE_CK(cudaMemsetAsync(cnt2, 0, nb * P * sizeof(int32_t), s));
   MARBLE_CK(cudaMemsetAsync(cntT, 0, nb * P * sizeof(int32_t), s));
 
@@ -626,6 +679,16 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->needed, ntot));
   k_needed<true><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, nullptr, p->needed_ptr, p->needed);
   MARBLE_CK(cudaGetLastError());
+  // work order of the persistent kernels
+  k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->fwd_order, p->fwd_nwork);
+  k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->colT_ptr, P, bps, p->bwd_order, p->bwd_nwork);
+  MARBLE_CK(cudaGetLastError());
+  p->h_fwd_nwork.resize((size_t)P * (P + 1));
+  p->h_bwd_nwork.resize((size_t)P * (P + 1));
+  MARBLE_CK(cudaMemcpyAsync(p->h_fwd_nwork.data(), p->fwd_nwork, P * (P + 1) * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaMemcpyAsync(p->h_bwd_nwork.data(), p->bwd_nwork, P * (P + 1) * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, s));
   MARBLE_CK(cudaStreamSynchronize(s));
   return MARBLE_OK;
 }
