@@ -18,8 +18,10 @@
 //               TMEM, P^T and dS^T (bf16) back into TMEM, dV += P^T dO and dK += dS^T Q with
 //               dO and Q read MN-major; at the end dv_acc += dV, dk_acc += scale * dK by TMA
 //               reduce-adds.
-// Both: warp 0 TMA producer (two stages), warp 1 TMEM allocation + MMA issue, warps 2..5
-// one thread per TMEM lane for the elementwise stage.  Masks only on partial tiles.
+// Both: warp 0 TMA producer (two stages), warp 1 TMEM allocation + MMA issue, warps 2..9
+// elementwise, four warps (one thread per TMEM lane) for each 64-column half of a tile; the
+// halves run as two chains offset in time so that the tensor core works on one half while
+// the other half's elementwise stage runs.  Masks only on partial tiles.
 #include <math.h>
 
 #include "common.cuh"
@@ -62,8 +64,16 @@ struct BwdParams {
 // ======================================================================================
 // dQ (Q-stationary)
 // ======================================================================================
-enum { Q_QFULL, Q_KVFULL0, Q_KVFULL1, Q_KVEMPTY0, Q_KVEMPTY1, Q_SFULL, Q_PFULL, Q_DQDONE,
-       Q_DRAIN, Q_TRK0, Q_TRK1, Q_EPI, Q_NUM };
+// The tile's 128 kv columns are worked as two halves (h = 0, 1) that run as two chains
+// offset in time: while the elementwise warps of one half compute dS, the tensor core runs
+// the other half's MMAs.  Per tile j and half h:
+//   S_h = Q K_h^T and dP_h = dO V_h^T (N = 64)  ->  elementwise: dS_h (bf16) over S_h
+//   ->  dQ += dS_h K_h (K = 64).
+// S alternates between two TMEM buffers by tile, so S_h(j+1) never overwrites the dS_h(j)
+// that dQ_h(j) reads; dP has one buffer, rewritten once the elementwise has loaded it.
+enum { Q_QFULL, Q_KVFULL0, Q_KVFULL1, Q_KVEMPTY0, Q_KVEMPTY1, Q_SFULL0, Q_SFULL1, Q_PFULL0,
+       Q_PFULL1, Q_DQDONE0, Q_DQDONE1, Q_DRAIN, Q_TRK00, Q_TRK01, Q_TRK10, Q_TRK11, Q_EPI,
+       Q_NUM };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
@@ -74,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + kTile;
   uint8_t* sK0 = smem + 2 * kTile;  // stage s: K at 2+2s, V at 3+2s
-  int32_t* ktr = reinterpret_cast<int32_t*>(smem + 6 * kTile);  // [2][4][128]
+  int32_t* ktr = reinterpret_cast<int32_t*>(smem + 6 * kTile);  // [half][buffer][4][64]
   __shared__ __align__(8) uint64_t bar[Q_NUM];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -97,8 +107,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int b = 0; b < Q_NUM; ++b)
-      mbar_init(&bar[b], (b == Q_PFULL || b == Q_TRK0 || b == Q_TRK1 || b == Q_EPI) ? 256 : 1);
+    for (int b = 0; b < Q_NUM; ++b) {
+      const int cnt = (b == Q_EPI) ? 256
+                      : (b == Q_PFULL0 || b == Q_PFULL1 || b == Q_TRK00 || b == Q_TRK01 ||
+                         b == Q_TRK10 || b == Q_TRK11)
+                          ? 128
+                          : 1;
+      mbar_init(&bar[b], cnt);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -108,11 +124,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // S fp32 [0,128); dS bf16 packed over it: q/kv columns [64h, 64h + 64) of half h go to
-  // TMEM columns [64h, 64h + 32), inside the fp32 columns that same half has read
-  const uint32_t tS = tmem_base;
-  const uint32_t tP = tmem_base + 128;   // dP fp32 [128,256)
-  const uint32_t tQ = tmem_base + 256;   // dQ fp32 [256, 256+D)
+  // S buffers fp32 at [0,128) (even tiles) and [384,512) (odd tiles); dS_h bf16 is packed into
+  // columns [64h, 64h + 32) of its S buffer, inside the fp32 columns half h has read.
+  // dP fp32 [128,256); dQ fp32 [256, 256+D).
+  const uint32_t tS0 = tmem_base, tS1 = tmem_base + 384;
+  const uint32_t tP = tmem_base + 128;
+  const uint32_t tQ = tmem_base + 256;
   const int kvh = h / p.group;
 
   if (warp == 0) {
@@ -125,14 +142,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       for (int a = 0; a < kAtoms; ++a) {
         tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
         tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
-      }
-    }
-    // pull the unit's K/V tiles toward L2 ahead of their loads
-    for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
-      const int nk = p.step_col[e0 + j];
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
-        tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
       }
     }
     int fills[2] = {0, 0};
@@ -150,6 +159,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         }
       }
       ++fills[s];
+      if (j == 1) {
+        // pull the later K/V tiles toward L2 once the first two loads are queued
+        for (int jj = 2 + lane; jj < T && jj < kPrefetchTiles; jj += 32) {
+          const int nkk = p.step_col[e0 + jj];
+          for (int a = 0; a < kAtoms; ++a) {
+            tma_prefetch_l2_3d(&p.k_map, a * 64, nkk * 128, kvh);
+            tma_prefetch_l2_3d(&p.v_map, a * 64, nkk * 128, kvh);
+          }
+        }
+      }
     }
     if (lane == 0) {
       drain_wait(&bar[Q_QFULL], 0, p.wait_ns, p.err);
@@ -159,46 +178,64 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
       const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      bool ok = mbar_wait(&bar[Q_QFULL], 0, w);
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(&bar[Q_KVFULL0 + s], (j >> 1) & 1, w)) break;
-        if (j > 0 && !mbar_wait(&bar[Q_DQDONE], (j - 1) & 1, w)) break;
-        tc_fence_after();
-        const uint32_t aK = smem_u32(sK0 + s * 2 * kTile), aV = aK + kTile;
+      // S_hh(jj) and dP_hh(jj): kv rows [64 hh, 64 hh + 64) of stage jj & 1
+      auto issue_s = [&](int jj, int hh) {
+        const uint32_t aK = smem_u32(sK0 + (jj & 1) * 2 * kTile) + hh * 8192, aV = aK + kTile;
+        const uint32_t ts = ((jj & 1) ? tS1 : tS0) + hh * 64;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tS, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS, k > 0);
-        }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024), kIdS,
+          mma_ss(ts, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS,
                  k > 0);
         }
-        mma_commit(&bar[Q_SFULL]);
-        if (!mbar_wait(&bar[Q_PFULL], j & 1, w)) break;
-        tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tQ, tS + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aK + k * 2048, 16384, 1024), kIdQ,
-                 (j > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar[Q_DQDONE]);
-        mma_commit(&bar[Q_KVEMPTY0 + s]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tP + hh * 64, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024),
+                 kIdS, k > 0);
+        }
+        mma_commit(&bar[Q_SFULL0 + hh]);
+      };
+      bool ok = mbar_wait(&bar[Q_QFULL], 0, w) && mbar_wait(&bar[Q_KVFULL0], 0, w);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j & 1;
+        const bool nxt = j + 1 < T;
+        if (nxt && !mbar_wait(&bar[Q_KVFULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, w)) break;
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&bar[Q_PFULL0 + hh], j & 1, w)) { ok = false; break; }
+          // S_hh(j+1) goes to the buffer dQ_hh(j-1) read: wait for it before dQ_hh(j) is
+          // issued, so that the wait is on the phase just before the one in flight
+          if (nxt && j >= 1 && !mbar_wait(&bar[Q_DQDONE0 + hh], (j - 1) & 1, w)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t aK = smem_u32(sK0 + s * 2 * kTile);
+          const uint32_t ts = (s ? tS1 : tS0) + hh * 64;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tQ, ts + kk * 8, sdesc_sw128(aK + (4 * hh + kk) * 2048, 16384, 1024), kIdQ,
+                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar[Q_DQDONE0 + hh]);
+          if (hh == 1) mma_commit(&bar[Q_KVEMPTY0 + s]);
+          if (nxt) issue_s(j + 1, hh);
+        }
       }
       mma_commit(&bar[Q_DRAIN]);
       drain_wait(&bar[Q_DRAIN], 0, p.wait_ns, p.err);
     }
     __syncwarp();
   } else {
-    // two warps per TMEM lane quarter: `half` selects columns [64 half, 64 half + 64)
+    // four warps per half: `half` owns kv columns [64 half, 64 half + 64), one row a thread
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
+    const int hr = row & 63;  // this thread's share of the half's key tracks
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const int64_t tq = nq * 128 + row;
     const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
@@ -213,40 +250,37 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
       uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
       if (partial) {
+        // the half's 64 keys' tracks, two per thread, in one of two buffers
         const int b = n_partial & 1;
         const uint32_t par = (n_partial >> 1) & 1;
         ++n_partial;
-        int32_t* kt = ktr + b * 512;
-        const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
-        if (half == 0) {
-          kt[row] = p.tracks[t];
-          kt[128 + row] = p.tracks[n + t];
-        } else {
-          kt[256 + row] = p.tracks[2 * n + t];
-          kt[384 + row] = p.tracks[3 * n + t];
-        }
-        mbar_arrive(&bar[Q_TRK0 + b]);
-        if (!wait_all(&bar[Q_TRK0 + b], par, w)) { ok = false; break; }
+        int32_t* kt = ktr + (half * 2 + b) * 256;
+        const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + half * 64 + hr;
+        const int tr0 = (row >> 6) * 2;  // tracks tr0, tr0 + 1
+        kt[tr0 * 64 + hr] = p.tracks[tr0 * n + t];
+        kt[(tr0 + 1) * 64 + hr] = p.tracks[(tr0 + 1) * n + t];
+        mbar_arrive(&bar[Q_TRK00 + half * 2 + b]);
+        if (!wait_all(&bar[Q_TRK00 + half * 2 + b], par, w)) { ok = false; break; }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
           uint32_t bits = 0;
 #pragma unroll
           for (int t2 = 0; t2 < 32; ++t2) {
-            const int kc = c * 32 + t2;
-            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc], kt[384 + kc],
+            const int kc = cc * 32 + t2;
+            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[64 + kc], kt[128 + kc], kt[192 + kc],
                                 p.W) ? 1u : 0u) << t2;
           }
           lm[cc] = bits;
         }
       }
-      if (!wait_all(&bar[Q_SFULL], j & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[Q_SFULL0 + half], j & 1, w)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t ts = ((j & 1) ? tS1 : tS0) + half * 64;
       uint32_t vs[2][32], vp[2][32];
-      tmem_ld32(tS + lb + (2 * half) * 32, vs[0]);
-      tmem_ld32(tS + lb + (2 * half + 1) * 32, vs[1]);
-      tmem_ld32(tP + lb + (2 * half) * 32, vp[0]);
-      tmem_ld32(tP + lb + (2 * half + 1) * 32, vp[1]);
+      tmem_ld32(ts + lb, vs[0]);
+      tmem_ld32(ts + lb + 32, vs[1]);
+      tmem_ld32(tP + lb + half * 64, vp[0]);
+      tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
       tmem_ld_wait();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -260,16 +294,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
           const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dlt);
           pk[t >> 1] = pack_bf16(d0, d1);
         }
-        tmem_st16(tS + lb + half * 64 + cc * 16, pk);
+        tmem_st16(ts + lb + cc * 16, pk);
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[Q_PFULL]);
+      mbar_arrive(&bar[Q_PFULL0 + half]);
     }
     // epilogue: dq_acc += scale * dQ as a TMA fp32 reduce-add of a tile staged in the Q/dO
-    // slots (all MMAs are done), D/32 boxes of 128 x 32 fp32: no load of dq_acc
+    // slots (all MMAs are done), D/32 boxes of 128 x 32 fp32: no load of dq_acc.  The MMA
+    // thread's final commit has one phase, so it is safe to wait on from either half (a
+    // per-tile barrier could be two phases behind while the other half is still working).
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && !wait_all(&bar[Q_DQDONE], (T - 1) & 1, w)) ok = false;
+    if (ok && !wait_all(&bar[Q_DRAIN], 0, w)) ok = false;
     tc_fence_after();
     uint8_t* stg = smem;
     if (ok) {
@@ -305,8 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
 // ======================================================================================
 // dK / dV (KV-stationary)
 // ======================================================================================
-enum { K_KVFULL, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL, K_PFULL, K_MMA2, K_DRAIN,
-       K_TRK0, K_TRK1, K_EPI, K_NUM };
+// As in the dQ kernel, the item's 128 q columns are worked as two halves that run as two
+// chains offset in time.  Per item j and half h:
+//   S^T_h = K Q_h^T and dP^T_h = V dO_h^T (N = 64)  ->  elementwise: P^T_h and dS^T_h (bf16)
+//   over them  ->  dV += P^T_h dO_h and dK += dS^T_h Q_h (K = 64).
+// With dV and dK resident, TMEM holds one S^T / dP^T buffer: S^T_h(j+1) is issued once the
+// MMAs of half h of item j have completed, while the other half's elementwise runs.
+enum { K_KVFULL, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL0, K_SFULL1, K_PFULL0,
+       K_PFULL1, K_CONS0, K_CONS1, K_DRAIN, K_TRK00, K_TRK01, K_TRK10, K_TRK11, K_EPI, K_NUM };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant__ BwdParams p) {
@@ -317,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   uint8_t* sK = smem;
   uint8_t* sV = smem + kTile;
   uint8_t* sQ0 = smem + 2 * kTile;  // stage s: Q at 2+2s, dO at 3+2s
-  float* stg = reinterpret_cast<float*>(smem + 6 * kTile);  // [2][ lse2[128] | delta[128] ]
-  int32_t* qtr = reinterpret_cast<int32_t*>(smem + 6 * kTile + 2048);  // [2][4][128]
+  // per half and buffer: lse2[64] | delta[64] | tracks [4][64]
+  float* stg = reinterpret_cast<float*>(smem + 6 * kTile);
   __shared__ __align__(8) uint64_t bar[K_NUM];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -343,8 +385,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int b = 0; b < K_NUM; ++b)
-      mbar_init(&bar[b], (b == K_PFULL || b == K_TRK0 || b == K_TRK1 || b == K_EPI) ? 256 : 1);
+    for (int b = 0; b < K_NUM; ++b) {
+      const int cnt = (b == K_EPI) ? 256
+                      : (b == K_PFULL0 || b == K_PFULL1 || b == K_TRK00 || b == K_TRK01 ||
+                         b == K_TRK10 || b == K_TRK11)
+                          ? 128
+                          : 1;
+      mbar_init(&bar[b], cnt);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -354,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // S^T fp32 [0,128) and dP^T fp32 [128,256); P^T / dS^T bf16 packed over them: q columns
-  // [64h, 64h + 64) of half h go to columns [64h, 64h + 32) of the same region
+  // S^T fp32 [0,128) and dP^T fp32 [128,256), half h in columns [64h, 64h + 64) of each;
+  // P^T_h / dS^T_h bf16 packed into columns [64h, 64h + 32) of the same region
   const uint32_t tS = tmem_base;
   const uint32_t tP = tmem_base + 128;
   const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
@@ -371,15 +419,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       for (int a = 0; a < kAtoms; ++a) {
         tma_load_3d(sK + a * 16384, &p.k_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
         tma_load_3d(sV + a * 16384, &p.v_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
-      }
-    }
-    // pull the items' Q/dO tiles toward L2 ahead of their loads
-    for (int it = lane; it < T && it < kPrefetchTiles; it += 32) {
-      const int h = kh * p.group + it / L;
-      const int nqb = p.colT_row[c0 + it % L];
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_prefetch_l2_3d(&p.q_map, a * 64, nqb * 128, h);
-        tma_prefetch_l2_3d(&p.do_map, a * 64, nqb * 128, h);
       }
     }
     int fills[2] = {0, 0};
@@ -398,6 +437,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         }
       }
       ++fills[s];
+      if (it == 1) {
+        // pull the later items' Q/dO tiles toward L2 once the first two loads are queued
+        for (int i2 = 2 + lane; i2 < T && i2 < kPrefetchTiles; i2 += 32) {
+          const int h2 = kh * p.group + i2 / L;
+          const int nq2 = p.colT_row[c0 + i2 % L];
+          for (int a = 0; a < kAtoms; ++a) {
+            tma_prefetch_l2_3d(&p.q_map, a * 64, nq2 * 128, h2);
+            tma_prefetch_l2_3d(&p.do_map, a * 64, nq2 * 128, h2);
+          }
+        }
+      }
     }
     if (lane == 0) {
       drain_wait(&bar[K_KVFULL], 0, p.wait_ns, p.err);
@@ -407,50 +457,70 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      bool ok = mbar_wait(&bar[K_KVFULL], 0, w);
+      // S^T_hh(it) and dP^T_hh(it): q rows [64 hh, 64 hh + 64) of stage it & 1
+      auto issue_s = [&](int it, int hh) {
+        const uint32_t aQ = smem_u32(sQ0 + (it & 1) * 2 * kTile) + hh * 8192, aDO = aQ + kTile;
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tS + hh * 64, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024),
+                 kIdS, k > 0);
+        }
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
+          mma_ss(tP + hh * 64, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO + off, 16, 1024),
+                 kIdS, k > 0);
+        }
+        mma_commit(&bar[K_SFULL0 + hh]);
+      };
+      bool ok = mbar_wait(&bar[K_KVFULL], 0, w) && mbar_wait(&bar[K_QFULL0], 0, w);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(0, 1);
+      }
       for (int it = 0; ok && it < T; ++it) {
         const int s = it & 1;
-        if (!mbar_wait(&bar[K_QFULL0 + s], (it >> 1) & 1, w)) break;
-        if (it > 0 && !mbar_wait(&bar[K_MMA2], (it - 1) & 1, w)) break;
-        tc_fence_after();
+        const bool nxt = it + 1 < T;
+        if (nxt && !mbar_wait(&bar[K_QFULL0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, w)) break;
         const uint32_t aQ = smem_u32(sQ0 + s * 2 * kTile), aDO = aQ + kTile;
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&bar[K_PFULL0 + hh], it & 1, w)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tS, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024), kIdS, k > 0);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tdV, tS + hh * 64 + kk * 8,
+                   sdesc_sw128(aDO + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
+                   (it > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tdK, tP + hh * 64 + kk * 8,
+                   sdesc_sw128(aQ + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
+                   (it > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar[K_CONS0 + hh]);
+          if (hh == 1) mma_commit(&bar[K_QEMPTY0 + s]);
+          if (nxt) {
+            // half hh of the S^T / dP^T buffer is free once these MMAs have read P^T / dS^T
+            if (!mbar_wait(&bar[K_CONS0 + hh], it & 1, w)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(it + 1, hh);
+          }
         }
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tP, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO + off, 16, 1024), kIdS,
-                 k > 0);
-        }
-        mma_commit(&bar[K_SFULL]);
-        if (!mbar_wait(&bar[K_PFULL], it & 1, w)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tdV, tS + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aDO + k * 2048, 16384, 1024), kIdAcc,
-                 (it > 0 || k > 0) ? 1u : 0u);
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mma_ts(tdK, tP + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aQ + k * 2048, 16384, 1024), kIdAcc,
-                 (it > 0 || k > 0) ? 1u : 0u);
-        mma_commit(&bar[K_MMA2]);
-        mma_commit(&bar[K_QEMPTY0 + s]);
       }
       mma_commit(&bar[K_DRAIN]);
       drain_wait(&bar[K_DRAIN], 0, p.wait_ns, p.err);
     }
     __syncwarp();
   } else {
-    // two warps per TMEM lane quarter: `half` selects q columns [64 half, 64 half + 64)
+    // four warps per half: `half` owns q columns [64 half, 64 half + 64), one kv row a thread
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;  // kv row of the tile
+    const int hr = row & 63;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const int64_t tk = nk * 128 + row;
     const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
@@ -460,55 +530,54 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     for (int it = 0; it < T; ++it) {
       const int h = kh * p.group + it / L;
       const int64_t e = c0 + it % L;
-      const int64_t qrow = (int64_t)p.colT_row[e] * 128 + row;
+      const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
       const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
-      // stage this item's per-query LSE (base 2), delta and, on partial tiles, tracks
+      // stage this half's per-query LSE (base 2), delta and, on partial tiles, tracks: the
+      // first 64 threads of the half the two floats, the other 64 the four tracks
       const int b = it & 1;
-      float* lse2s = stg + b * 256;
-      float* dls = lse2s + 128;
-      int32_t* qt = qtr + b * 512;
-      if (half == 0) {
+      float* lse2s = stg + (half * 2 + b) * 384;
+      float* dls = lse2s + 64;
+      int32_t* qt = reinterpret_cast<int32_t*>(lse2s + 128);
+      if ((row >> 6) == 0) {
         const float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
-        lse2s[row] = (l2 == -INFINITY) ? INFINITY : l2;
-        dls[row] = p.delta[(int64_t)h * n + qrow];
+        lse2s[hr] = (l2 == -INFINITY) ? INFINITY : l2;
+        dls[hr] = p.delta[(int64_t)h * n + qrow];
       } else if (partial) {
-        qt[row] = p.tracks[qrow];
-        qt[128 + row] = p.tracks[n + qrow];
-        qt[256 + row] = p.tracks[2 * n + qrow];
-        qt[384 + row] = p.tracks[3 * n + qrow];
+        qt[hr] = p.tracks[qrow];
+        qt[64 + hr] = p.tracks[n + qrow];
+        qt[128 + hr] = p.tracks[2 * n + qrow];
+        qt[192 + hr] = p.tracks[3 * n + qrow];
       }
-      mbar_arrive(&bar[K_TRK0 + b]);
-      if (!wait_all(&bar[K_TRK0 + b], (it >> 1) & 1, w)) { ok = false; break; }
+      mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
+      if (!wait_all(&bar[K_TRK00 + half * 2 + b], (it >> 1) & 1, w)) { ok = false; break; }
       uint32_t lm[2] = {~0u, ~0u};
       if (partial) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
           uint32_t bits = 0;
 #pragma unroll
           for (int t2 = 0; t2 < 32; ++t2) {
-            const int q = c * 32 + t2;
-            bits |= (mask_legal(qt[q], qt[128 + q], qt[256 + q], qt[384 + q], sk, gk, zk, pk,
+            const int q = cc * 32 + t2;
+            bits |= (mask_legal(qt[q], qt[64 + q], qt[128 + q], qt[192 + q], sk, gk, zk, pk,
                                 p.W) ? 1u : 0u) << t2;
           }
           lm[cc] = bits;
         }
       }
-      if (!wait_all(&bar[K_SFULL], it & 1, w)) { ok = false; break; }
+      if (!wait_all(&bar[K_SFULL0 + half], it & 1, w)) { ok = false; break; }
       tc_fence_after();
       uint32_t vs[2][32], vp[2][32];
-      tmem_ld32(tS + lb + (2 * half) * 32, vs[0]);
-      tmem_ld32(tS + lb + (2 * half + 1) * 32, vs[1]);
-      tmem_ld32(tP + lb + (2 * half) * 32, vp[0]);
-      tmem_ld32(tP + lb + (2 * half + 1) * 32, vp[1]);
+      tmem_ld32(tS + lb + half * 64, vs[0]);
+      tmem_ld32(tS + lb + half * 64 + 32, vs[1]);
+      tmem_ld32(tP + lb + half * 64, vp[0]);
+      tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
       tmem_ld_wait();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * half + cc;
         uint32_t pk16[16], dk16[16];
 #pragma unroll
         for (int t = 0; t < 32; t += 2) {
-          const int q0 = c * 32 + t;
+          const int q0 = cc * 32 + t;
           const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
           const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2s[q0]) : 0.f;
           const float p1 =
@@ -523,12 +592,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bar[K_PFULL]);
+      mbar_arrive(&bar[K_PFULL0 + half]);
     }
     // epilogue: dv_acc += dV and dk_acc += scale * dK as TMA fp32 reduce-adds of tiles staged
-    // in the K/V and first Q/dO slots (all MMAs are done): no load of the accumulators
+    // in the K/V and first Q/dO slots (all MMAs are done): no load of the accumulators.  The
+    // MMA thread's final commit has one phase, so it is safe to wait on from either half.
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && !wait_all(&bar[K_MMA2], (T - 1) & 1, w)) ok = false;
+    if (ok && !wait_all(&bar[K_DRAIN], 0, w)) ok = false;
     tc_fence_after();
     uint8_t* stv = smem;
     uint8_t* stk = smem + (D / 32) * 16384;
@@ -571,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
 template <int D>
 size_t bwd_smem() {
   // one CTA per SM: each CTA owns all 512 TMEM columns
-  size_t smem = 6 * (128 * D * 2) + 8192 + 1024;
+  size_t smem = 6 * (128 * D * 2) + 2 * 2 * 384 * 4 + 1024;
   return smem < 120 * 1024 ? 120 * 1024 : smem;
 }
 

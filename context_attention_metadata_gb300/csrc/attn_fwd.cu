@@ -14,7 +14,7 @@
 //               posts it in a 4-entry queue in shared memory; every other role reads the
 //               queue in order, and the epilogue frees an entry once all roles are past it.
 //   warp 0      TMA producer: Q of each unit into one of two slots, K_j and V_j through
-//               two-slot rings, and L2 prefetches of a unit's K/V tiles when it starts.
+//               two-slot rings.
 //   warp 1      allocates all 512 TMEM columns: S double buffer [0,128) and [128,256),
 //               O double buffer [256,384) and [384,512) (units alternate); lane 0 issues
 //               tcgen05.mma -- S = Q K^T up to two tiles ahead of the softmax, O += P V with P
@@ -47,7 +47,6 @@ constexpr int kEpi = 128;                  // epilogue threads (warps 10..13)
 constexpr int kWarpEpi0 = 10;
 constexpr int kWarpSched = 14;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units: rescale O when max grows > 2^8
-constexpr int kPrefetchTiles = 64;         // L2 prefetch depth per unit
 constexpr int kQueue = 4;                  // work-queue entries
 
 enum {
@@ -201,6 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         if (uc >= kQueue && !mbar_wait(&bar[B_UEMPTY0 + slot], ((uc / kQueue) - 1) & 1, w)) break;
         int unit = -1, T = 0;
         int64_t e0 = 0;
+        // longest lists first, the q heads of a block one after the other
         const unsigned t = atomicAdd(p.sched, 1u);
         if (t < (unsigned)p.nwork) {
           unit = (int)(t % (unsigned)p.hq) * p.bps + p.order[t / (unsigned)p.hq];
@@ -245,14 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
                       (int)(nq * 128), h);
       }
       ++q_fills;
-      // pull the unit's K/V tiles toward L2 ahead of their loads
-      for (int j = lane; j < T && j < kPrefetchTiles; j += 32) {
-        const int nk = p.step_col[e0 + j];
-        for (int a = 0; a < kAtoms; ++a) {
-          tma_prefetch_l2_3d(&p.k_map, a * 64, nk * 128, kvh);
-          tma_prefetch_l2_3d(&p.v_map, a * 64, nk * 128, kvh);
-        }
-      }
       for (int j = 0; j < T; ++j, ++g) {
         const int nk = p.step_col[e0 + j];
         const uint32_t s = ring_slot(g);
