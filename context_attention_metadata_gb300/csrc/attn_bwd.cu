@@ -8,20 +8,28 @@
 //
 // Per tile (S = Q K^T * scale, P = exp(S - LSE), dP = dO V^T, dS = P * (dP - delta)):
 //   dV += P^T dO,  dK += scale * dS^T Q,  dQ += scale * dS K.
-// Two kernels, so that every accumulator has exactly one owner per launch and no atomics
-// are needed (a fused kernel would scatter one fp32 dQ tile per (q, kv) tile):
-//   k_bwd_dq    Q-stationary, one CTA per (q block, q head): S and dP in TMEM, dS (bf16)
-//               back into TMEM over S, dQ += dS K with K read MN-major from the K tile
-//               already staged for S; at the end dq_acc += scale * dQ by a TMA reduce-add.
-//   k_bwd_dkdv  KV-stationary, one CTA per (kv block, kv head), looping over the q heads of
-//               its group and the q blocks listed for it: S^T = K Q^T and dP^T = V dO^T in
+// Two kernels, so that every accumulator tile has one owner per launch and the kernels never
+// add partial tiles of the same accumulator concurrently:
+//   k_bwd_dq    Q-stationary units (q block, q head): S and dP in TMEM, dS (bf16) back into
+//               TMEM over S, dQ += dS K with K read MN-major from the K tile staged for S.
+//   k_bwd_dkdv  KV-stationary units (kv block, kv head), looping over the q heads of the
+//               group and the q blocks listed for the block: S^T = K Q^T and dP^T = V dO^T in
 //               TMEM, P^T and dS^T (bf16) back into TMEM, dV += P^T dO and dK += dS^T Q with
-//               dO and Q read MN-major; at the end dv_acc += dV, dk_acc += scale * dK by TMA
-//               reduce-adds.
-// Both: warp 0 TMA producer (two stages), warp 1 TMEM allocation + MMA issue, warps 2..9
-// elementwise, four warps (one thread per TMEM lane) for each 64-column half of a tile; the
-// halves run as two chains offset in time so that the tensor core works on one half while
-// the other half's elementwise stage runs.  Masks only on partial tiles.
+//               dO and Q read MN-major.
+// Both are persistent (one CTA per SM) and take their units from a ticket counter in the
+// plan's order (longest list first), through a 4-entry queue in shared memory:
+//   warp 10     scheduler: ticket -> unit -> queue
+//   warp 0      TMA producer: the unit's stationary tiles into one slot (refilled once the
+//               unit's last score MMAs have read it), the streamed tiles through two stages
+//   warp 1      TMEM allocation and MMA issue
+//   warps 2..9  elementwise, four warps (one thread per TMEM lane) for each 64-column half
+//               of a tile; the halves run as two chains offset in time, so that the tensor
+//               core works on one half while the other half's elementwise stage runs.  At a
+//               unit's end the same warps read the fp32 accumulator out of TMEM (releasing it
+//               for the next unit, whose first MMAs are already under way), stage it in a
+//               shared-memory slot the unit no longer needs and add it to the global
+//               accumulator with TMA fp32 reduce-adds (no load of the accumulator).
+// Masks only on partial tiles.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,9 +39,10 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 320;  // producer, MMA, 8 elementwise warps (2 per lane quarter)
+constexpr int kThreads = 352;  // producer, MMA, 8 elementwise warps, scheduler
+constexpr int kWarpSched = 10;
+constexpr int kQueue = 4;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kPrefetchTiles = 64;  // L2 prefetch depth per unit
 
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;
@@ -46,6 +55,8 @@ struct BwdParams {
   const uint8_t* colT_tag;
   const int64_t* needed_ptr;
   const int32_t* needed;
+  const int32_t* order;      // work order of the launch (blocks of one shard, longest first)
+  unsigned* sched;           // ticket counter pair of the launch
   const int32_t* tracks;     // [4][n] plan order
   const float* lse;          // [hq][n] natural log
   const float* delta;        // [hq][n]
@@ -57,64 +68,166 @@ struct BwdParams {
   long long n;
   int P, bps, q_shard, kv_shard;
   int hq, hkv, group;
+  int nwork;                 // units with a non-empty list
   int W;
   float scale, sl2;
 };
 
+// queue entry: head, block (plan order), list start and length
+struct Queue {
+  int head[kQueue];  // -1: no more work
+  int blk[kQueue];
+  int T[kQueue];
+  long long e0[kQueue];
+};
+
+// ticket -> unit of the dQ kernel: q head h (innermost), q block of the order
+__device__ __forceinline__ void dq_unit(const BwdParams& p, unsigned t, int* h, int* blk,
+                                        int64_t* e0, int* T) {
+  *h = (int)(t % (unsigned)p.hq);
+  const int64_t nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
+  int64_t a, b;
+  if (p.kv_shard >= 0) {
+    a = p.step_ptr[nq * p.P + p.kv_shard];
+    b = p.step_ptr[nq * p.P + p.kv_shard + 1];
+  } else {
+    a = p.step_ptr[nq * p.P];
+    b = p.step_ptr[nq * p.P + p.P];
+  }
+  *blk = (int)nq;
+  *e0 = a;
+  *T = (int)(b - a);
+}
+
+// ticket -> unit of the dK/dV kernel: kv head (innermost), kv block of the order (or of the
+// needed list); T = number of listed q blocks (items = T x group)
+__device__ __forceinline__ void dkdv_unit(const BwdParams& p, unsigned t, int* kh, int* blk,
+                                          int64_t* c0, int* T) {
+  *kh = (int)(t % (unsigned)p.hkv);
+  const unsigned i = t / (unsigned)p.hkv;
+  int64_t nk;
+  if (p.kv_shard >= 0)
+    nk = (int64_t)p.kv_shard * p.bps + p.order[i];
+  else
+    nk = p.needed[p.needed_ptr[p.q_shard] + i];
+  *blk = (int)nk;
+  *c0 = p.colT_ptr[nk * p.P + p.q_shard];
+  *T = (int)(p.colT_ptr[nk * p.P + p.q_shard + 1] - *c0);
+}
+
+// scheduler loop (one lane): post units until the tickets run out, then a terminator.  An
+// entry is rewritten only once every role has released it.
+template <bool kDQ>
+__device__ void schedule(const BwdParams& p, Queue& queue, uint64_t* ufull, uint64_t* uempty,
+                         const WaitCtx& w) {
+  for (int uc = 0;; ++uc) {
+    const int slot = uc % kQueue;
+    if (uc >= kQueue && !mbar_wait(&uempty[slot], ((uc / kQueue) - 1) & 1, w)) return;
+    int hd = -1, blk = 0, T = 0;
+    int64_t e0 = 0;
+    while (true) {  // units with an empty list (possible only in the needed-block mode) are skipped
+      const unsigned t = atomicAdd(p.sched, 1u);
+      if (t >= (unsigned)p.nwork) {
+        hd = -1;
+        break;
+      }
+      if (kDQ)
+        dq_unit(p, t, &hd, &blk, &e0, &T);
+      else
+        dkdv_unit(p, t, &hd, &blk, &e0, &T);
+      if (T > 0) break;
+    }
+    queue.head[slot] = hd;
+    queue.blk[slot] = blk;
+    queue.T[slot] = T;
+    queue.e0[slot] = e0;
+    mbar_arrive(&ufull[slot]);
+    if (hd < 0) return;
+  }
+}
+
+// the last CTA of a launch to finish puts the ticket counter pair back to zero
+__device__ __forceinline__ void release_tickets(const BwdParams& p) {
+  __threadfence();
+  if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+    atomicExch(p.sched, 0u);
+    atomicExch(p.sched + 1, 0u);
+  }
+}
+
 // ======================================================================================
 // dQ (Q-stationary)
 // ======================================================================================
-// The tile's 128 kv columns are worked as two halves (h = 0, 1) that run as two chains
-// offset in time: while the elementwise warps of one half compute dS, the tensor core runs
-// the other half's MMAs.  Per tile j and half h:
-//   S_h = Q K_h^T and dP_h = dO V_h^T (N = 64)  ->  elementwise: dS_h (bf16) over S_h
-//   ->  dQ += dS_h K_h (K = 64).
-// S alternates between two TMEM buffers by tile, so S_h(j+1) never overwrites the dS_h(j)
-// that dQ_h(j) reads; dP has one buffer, rewritten once the elementwise has loaded it.
-enum { Q_QFULL, Q_KVFULL0, Q_KVFULL1, Q_KVEMPTY0, Q_KVEMPTY1, Q_SFULL0, Q_SFULL1, Q_PFULL0,
-       Q_PFULL1, Q_DQDONE0, Q_DQDONE1, Q_DRAIN, Q_TRK00, Q_TRK01, Q_TRK10, Q_TRK11, Q_EPI,
-       Q_NUM };
+// Tile g counts the tiles of all units of the CTA.  Per tile:
+//   S = Q K^T and dP = dO V^T (N = 128)  ->  elementwise, half h (kv columns [64h, 64h+64)):
+//   dS_h (bf16) over S_h  ->  dQ += dS_h K_h (K = 64).
+// S alternates between two TMEM buffers by tile and is issued for tile g+1 as soon as the dQ
+// MMAs of tile g-1 are done; dP has one buffer, rewritten once both halves have loaded it.
+// So S(g+1) and dP(g+1) run during the elementwise stage of tile g, and the elementwise warps
+// can finish tile g+1 before the MMA thread has seen tile g finished: the "dS written" barrier
+// of each half is therefore doubled by tile parity, so that no wait aliases a phase two ahead.  K streams through three
+// stages (S(g+1) is issued while K(g) still feeds dQ(g)), V through one (only dP reads it).
+// The epilogue stages the fp32 dQ tile in shared memory (in the K stage of the unit's last
+// tile when d = 128, which the epilogue hands back to the producer) and adds it to dq_acc
+// with TMA reduce-adds.
+enum {
+  Q_QFULL, Q_QEMPTY, Q_KFULL0, Q_KFULL1, Q_KFULL2, Q_KEMPTY0, Q_KEMPTY1, Q_KEMPTY2, Q_VFULL,
+  Q_VEMPTY, Q_SFULL0, Q_SFULL1, Q_DPFULL, Q_DPFREE, Q_PFULL00, Q_PFULL01, Q_PFULL10, Q_PFULL11,
+  Q_DQDONE, Q_ACCFULL,
+  Q_ACCFREE, Q_STG0, Q_STG1, Q_STGR0, Q_STGR1, Q_TRK00, Q_TRK01, Q_TRK10, Q_TRK11, Q_UFULL0,
+  Q_UEMPTY0 = Q_UFULL0 + kQueue, Q_DRAIN = Q_UEMPTY0 + kQueue, Q_NUM
+};
+
+__host__ __device__ constexpr int dq_arrivals(int b) {
+  return (b == Q_ACCFREE || b == Q_DPFREE || (b >= Q_UEMPTY0 && b < Q_UEMPTY0 + kQueue))
+             ? 256
+             : (((b >= Q_PFULL00 && b <= Q_PFULL11) || b == Q_STG0 || b == Q_STG1 ||
+                 (b >= Q_TRK00 && b <= Q_TRK11))
+                    ? 128
+                    : 1);
+}
+
+// shared memory of the dQ kernel: Q | dO | K stages (3) | V | key tracks [2][2][4][64] |
+// (d = 64 only) a staging area of two fp32 boxes
+template <int D>
+struct DqSmem {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr bool kStageInK = D == 128;  // two 16 KB boxes fit in one K stage
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = 5 * kTile;
+  static constexpr int kTrk = 6 * kTile;
+  static constexpr int kStg = kTrk + 4096;
+  static constexpr int kEnd = kStg + (kStageInK ? 0 : 32768);
+  static constexpr size_t bytes() { return (size_t)kEnd + 1024; }
+};
+static_assert(DqSmem<128>::bytes() <= 232448 - 1024, "shared memory budget");
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
-  constexpr int kTile = 128 * D * 2;
+  using L = DqSmem<D>;
+  constexpr int kTile = L::kTile;
   constexpr int kAtoms = D / 64;
+  constexpr int kRounds = D / 64;  // epilogue rounds: one 32-column box per half per round
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + kTile;
-  uint8_t* sK0 = smem + 2 * kTile;  // stage s: K at 2+2s, V at 3+2s
-  int32_t* ktr = reinterpret_cast<int32_t*>(smem + 6 * kTile);  // [half][buffer][4][64]
+  uint8_t* sK0 = smem + L::kK;  // stage s at sK0 + s * kTile
+  uint8_t* sV = smem + L::kV;
+  int32_t* ktr = reinterpret_cast<int32_t*>(smem + L::kTrk);  // [half][buffer][4][64]
   __shared__ __align__(8) uint64_t bar[Q_NUM];
+  __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ int epi_count;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.x / p.bps, i = blockIdx.x % p.bps;
   const long long n = p.n;
-  const int64_t nq = (int64_t)p.q_shard * p.bps + i;
-  int64_t e0, e1;
-  if (p.kv_shard >= 0) {
-    e0 = p.step_ptr[nq * p.P + p.kv_shard];
-    e1 = p.step_ptr[nq * p.P + p.kv_shard + 1];
-  } else {
-    e0 = p.step_ptr[nq * p.P];
-    e1 = p.step_ptr[nq * p.P + p.P];
-  }
-  const int T = (int)(e1 - e0);
-  if (T == 0) return;
-
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int b = 0; b < Q_NUM; ++b) {
-      const int cnt = (b == Q_EPI) ? 256
-                      : (b == Q_PFULL0 || b == Q_PFULL1 || b == Q_TRK00 || b == Q_TRK01 ||
-                         b == Q_TRK10 || b == Q_TRK11)
-                          ? 128
-                          : 1;
-      mbar_init(&bar[b], cnt);
-    }
+    epi_count = 0;
+    for (int b = 0; b < Q_NUM; ++b) mbar_init(&bar[b], dq_arrivals(b));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -130,100 +243,166 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   const uint32_t tS0 = tmem_base, tS1 = tmem_base + 384;
   const uint32_t tP = tmem_base + 128;
   const uint32_t tQ = tmem_base + 256;
-  const int kvh = h / p.group;
 
-  if (warp == 0) {
+  if (warp == kWarpSched) {
+    if (lane == 0) schedule<true>(p, queue, &bar[Q_UFULL0], &bar[Q_UEMPTY0], w);
+    __syncwarp();
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.q_map);
       tma_prefetch_desc(&p.k_map);
       tma_prefetch_desc(&p.v_map);
       tma_prefetch_desc(&p.do_map);
-      mbar_arrive_expect_tx(&bar[Q_QFULL], 2 * kTile);
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
-        tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
-      }
     }
-    int fills[2] = {0, 0};
-    for (int j = 0; j < T; ++j) {
-      const int s = j & 1;
-      if (j >= 2 && !warp_wait(&bar[Q_KVEMPTY0 + s], ((j >> 1) - 1) & 1, w)) break;
-      const int nk = p.step_col[e0 + j];
+    int uc = 0, g = 0, q_fills = 0, k_fills[3] = {0, 0, 0}, v_fills = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[Q_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int h = queue.head[slot];
+      if (h < 0) break;
+      const int64_t nq = queue.blk[slot];
+      const int T = queue.T[slot];
+      const int64_t e0 = queue.e0[slot];
+      const int kvh = h / p.group;
+      // Q and dO of the unit once the previous unit's last S / dP have read the slot
+      if (uc >= 1 && !wait_all(&bar[Q_QEMPTY], (uc - 1) & 1, w)) break;
       if (lane == 0) {
-        uint8_t* sK = sK0 + s * 2 * kTile;
-        uint8_t* sV = sK + kTile;
-        mbar_arrive_expect_tx(&bar[Q_KVFULL0 + s], 2 * kTile);
+        mbar_arrive_expect_tx(&bar[Q_QFULL], 2 * kTile);
         for (int a = 0; a < kAtoms; ++a) {
-          tma_load_3d(sK + a * 16384, &p.k_map, &bar[Q_KVFULL0 + s], a * 64, nk * 128, kvh);
-          tma_load_3d(sV + a * 16384, &p.v_map, &bar[Q_KVFULL0 + s], a * 64, nk * 128, kvh);
+          tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
+          tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
         }
       }
-      ++fills[s];
-      if (j == 1) {
-        // pull the later K/V tiles toward L2 once the first two loads are queued
-        for (int jj = 2 + lane; jj < T && jj < kPrefetchTiles; jj += 32) {
-          const int nkk = p.step_col[e0 + jj];
-          for (int a = 0; a < kAtoms; ++a) {
-            tma_prefetch_l2_3d(&p.k_map, a * 64, nkk * 128, kvh);
-            tma_prefetch_l2_3d(&p.v_map, a * 64, nkk * 128, kvh);
-          }
+      ++q_fills;
+      for (int j = 0; j < T; ++j, ++g) {
+        const int s = g % 3;
+        const int nk = p.step_col[e0 + j];
+        if (g >= 3 && !wait_all(&bar[Q_KEMPTY0 + s], ((g / 3) - 1) & 1, w)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[Q_KFULL0 + s], kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(sK0 + s * kTile + a * 16384, &p.k_map, &bar[Q_KFULL0 + s], a * 64,
+                        nk * 128, kvh);
         }
+        ++k_fills[s];
+        if (g >= 1 && !wait_all(&bar[Q_VEMPTY], (g - 1) & 1, w)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar[Q_VFULL], kTile);
+          for (int a = 0; a < kAtoms; ++a)
+            tma_load_3d(sV + a * 16384, &p.v_map, &bar[Q_VFULL], a * 64, nk * 128, kvh);
+        }
+        ++v_fills;
       }
+      ++uc;
     }
+    // no copy may still be landing in shared memory when the CTA exits: the fills of a slot
+    // complete in order, so waiting for the latest fill of each slot suffices
     if (lane == 0) {
-      drain_wait(&bar[Q_QFULL], 0, p.wait_ns, p.err);
-      for (int s = 0; s < 2; ++s)
-        if (fills[s]) drain_wait(&bar[Q_KVFULL0 + s], (fills[s] - 1) & 1, p.wait_ns, p.err);
+      if (q_fills) drain_wait(&bar[Q_QFULL], (q_fills - 1) & 1, p.wait_ns, p.err);
+      for (int s = 0; s < 3; ++s)
+        if (k_fills[s]) drain_wait(&bar[Q_KFULL0 + s], (k_fills[s] - 1) & 1, p.wait_ns, p.err);
+      if (v_fills) drain_wait(&bar[Q_VFULL], (v_fills - 1) & 1, p.wait_ns, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      // S_hh(jj) and dP_hh(jj): kv rows [64 hh, 64 hh + 64) of stage jj & 1
-      auto issue_s = [&](int jj, int hh) {
-        const uint32_t aK = smem_u32(sK0 + (jj & 1) * 2 * kTile) + hh * 8192, aV = aK + kTile;
-        const uint32_t ts = ((jj & 1) ? tS1 : tS0) + hh * 64;
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aV = smem_u32(sV);
+      auto issue_s = [&](int gg) {  // S(gg) into S buffer gg & 1
+        const uint32_t aK = smem_u32(sK0 + (gg % 3) * kTile);
+        const uint32_t ts = (gg & 1) ? tS1 : tS0;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
           mma_ss(ts, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS,
                  k > 0);
         }
+        mma_commit(&bar[Q_SFULL0 + (gg & 1)]);
+      };
+      auto issue_dp = [&]() {  // dP of the tile whose V is staged
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tP + hh * 64, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024),
-                 kIdS, k > 0);
+          mma_ss(tP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024), kIdS,
+                 k > 0);
         }
-        mma_commit(&bar[Q_SFULL0 + hh]);
+        mma_commit(&bar[Q_DPFULL]);
+        mma_commit(&bar[Q_VEMPTY]);
       };
-      bool ok = mbar_wait(&bar[Q_QFULL], 0, w) && mbar_wait(&bar[Q_KVFULL0], 0, w);
+      int uc = 0, j = 0, g = 0, T = 0;
+      bool ok = mbar_wait(&bar[Q_UFULL0], 0, w) && queue.head[0] >= 0;
+      if (ok) {
+        T = queue.T[0];
+        ok = mbar_wait(&bar[Q_QFULL], 0, w) && mbar_wait(&bar[Q_KFULL0], 0, w) &&
+             mbar_wait(&bar[Q_VFULL], 0, w);
+      }
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_s(0);
+        issue_dp();
+        if (T == 1) mma_commit(&bar[Q_QEMPTY]);  // the unit's last read of Q and dO
       }
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j & 1;
-        const bool nxt = j + 1 < T;
-        if (nxt && !mbar_wait(&bar[Q_KVFULL0 + ((j + 1) & 1)], ((j + 1) >> 1) & 1, w)) break;
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&bar[Q_PFULL0 + hh], j & 1, w)) { ok = false; break; }
-          // S_hh(j+1) goes to the buffer dQ_hh(j-1) read: wait for it before dQ_hh(j) is
-          // issued, so that the wait is on the phase just before the one in flight
-          if (nxt && j >= 1 && !mbar_wait(&bar[Q_DQDONE0 + hh], (j - 1) & 1, w)) { ok = false; break; }
+      while (ok) {
+        // the tile after g: the next of this unit, or the first of the next unit
+        bool nxt = true, newu = false;
+        int Tn = T;
+        if (j + 1 == T) {
+          const int slot = (uc + 1) % kQueue;
+          if (!mbar_wait(&bar[Q_UFULL0 + slot], ((uc + 1) / kQueue) & 1, w)) break;
+          if (queue.head[slot] < 0) {
+            nxt = false;
+          } else {
+            newu = true;
+            Tn = queue.T[slot];
+          }
+        }
+        const bool last_next = newu ? Tn == 1 : j + 2 == T;  // tile g+1 ends its unit
+        if (nxt) {
+          // S(g+1): its K, its Q (a new unit's), and its S buffer, which dQ(g-1) read
+          if (!mbar_wait(&bar[Q_KFULL0 + (g + 1) % 3], ((g + 1) / 3) & 1, w)) break;
+          if (newu && !mbar_wait(&bar[Q_QFULL], (uc + 1) & 1, w)) break;
+          if (g >= 1 && !mbar_wait(&bar[Q_DQDONE], (g - 1) & 1, w)) break;
           tc_fence_after();
-          const uint32_t aK = smem_u32(sK0 + s * 2 * kTile);
-          const uint32_t ts = (s ? tS1 : tS0) + hh * 64;
+          issue_s(g + 1);
+          // dP(g+1) once both halves have loaded dP(g) and V(g+1) has landed
+          if (!mbar_wait(&bar[Q_DPFREE], g & 1, w) || !mbar_wait(&bar[Q_VFULL], (g + 1) & 1, w)) break;
+          tc_fence_after();
+          issue_dp();
+          if (last_next) mma_commit(&bar[Q_QEMPTY]);
+        }
+        const uint32_t aK = smem_u32(sK0 + (g % 3) * kTile);
+        const uint32_t tsb = (g & 1) ? tS1 : tS0;
+        for (int hh = 0; hh < 2; ++hh) {
+          if (!mbar_wait(&bar[Q_PFULL00 + 2 * hh + (g & 1)], (g >> 1) & 1, w)) { ok = false; break; }
+          // the unit's first dQ MMA overwrites the accumulator: the previous unit's must be out
+          if (j == 0 && hh == 0 && uc >= 1 && !mbar_wait(&bar[Q_ACCFREE], (uc - 1) & 1, w)) { ok = false; break; }
+          tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tQ, ts + kk * 8, sdesc_sw128(aK + (4 * hh + kk) * 2048, 16384, 1024), kIdQ,
-                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar[Q_DQDONE0 + hh]);
-          if (hh == 1) mma_commit(&bar[Q_KVEMPTY0 + s]);
-          if (nxt) issue_s(j + 1, hh);
+            mma_ts(tQ, tsb + hh * 64 + kk * 8, sdesc_sw128(aK + (4 * hh + kk) * 2048, 16384, 1024),
+                   kIdQ, (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+        }
+        if (!ok) break;
+        mma_commit(&bar[Q_DQDONE]);
+        if (j == T - 1) {
+          mma_commit(&bar[Q_ACCFULL]);
+          // with d = 128 the epilogue stages in this K stage and hands it back itself
+          if (!L::kStageInK) mma_commit(&bar[Q_KEMPTY0 + g % 3]);
+        } else {
+          mma_commit(&bar[Q_KEMPTY0 + g % 3]);
+        }
+        if (!nxt) break;
+        ++g;
+        if (newu) {
+          ++uc;
+          j = 0;
+          T = Tn;
+        } else {
+          ++j;
         }
       }
       mma_commit(&bar[Q_DRAIN]);
@@ -231,104 +410,134 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     }
     __syncwarp();
   } else {
+    // ------------------------------------------------------------------ elementwise
     // four warps per half: `half` owns kv columns [64 half, 64 half + 64), one row a thread
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const int hr = row & 63;  // this thread's share of the half's key tracks
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    const int64_t tq = nq * 128 + row;
-    const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
-              pq = p.tracks[3 * n + tq];
-    float lse2 = p.lse[(int64_t)h * n + tq] * kLog2e;
-    if (lse2 == -INFINITY) lse2 = INFINITY;  // a row with no legal key: every P is 0
-    const float dlt = p.delta[(int64_t)h * n + tq];
     const float sl2 = p.sl2;
+    int uc = 0, g = 0, n_partial = 0, rc = 0;  // rc: this half's epilogue rounds
     bool ok = true;
-    int n_partial = 0;
-    for (int j = 0; j < T; ++j) {
-      const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
-      uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
-      if (partial) {
-        // the half's 64 keys' tracks, two per thread, in one of two buffers
-        const int b = n_partial & 1;
-        const uint32_t par = (n_partial >> 1) & 1;
-        ++n_partial;
-        int32_t* kt = ktr + (half * 2 + b) * 256;
-        const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + half * 64 + hr;
-        const int tr0 = (row >> 6) * 2;  // tracks tr0, tr0 + 1
-        kt[tr0 * 64 + hr] = p.tracks[tr0 * n + t];
-        kt[(tr0 + 1) * 64 + hr] = p.tracks[(tr0 + 1) * n + t];
-        mbar_arrive(&bar[Q_TRK00 + half * 2 + b]);
-        if (!wait_all(&bar[Q_TRK00 + half * 2 + b], par, w)) { ok = false; break; }
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[Q_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int h = queue.head[slot];
+      if (h < 0) break;
+      const int64_t nq = queue.blk[slot];
+      const int T = queue.T[slot];
+      const int64_t e0 = queue.e0[slot];
+      const int64_t tq = nq * 128 + row;
+      const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
+                pq = p.tracks[3 * n + tq];
+      float lse2 = p.lse[(int64_t)h * n + tq] * kLog2e;
+      if (lse2 == -INFINITY) lse2 = INFINITY;  // a row with no legal key: every P is 0
+      const float dlt = p.delta[(int64_t)h * n + tq];
+      for (int j = 0; j < T; ++j, ++g) {
+        const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
+        uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
+        if (partial) {
+          // the half's 64 keys' tracks, two per thread, in one of two buffers
+          const int b = n_partial & 1;
+          const uint32_t par = (n_partial >> 1) & 1;
+          ++n_partial;
+          int32_t* kt = ktr + (half * 2 + b) * 256;
+          const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + half * 64 + hr;
+          const int tr0 = (row >> 6) * 2;  // tracks tr0, tr0 + 1
+          kt[tr0 * 64 + hr] = p.tracks[tr0 * n + t];
+          kt[(tr0 + 1) * 64 + hr] = p.tracks[(tr0 + 1) * n + t];
+          mbar_arrive(&bar[Q_TRK00 + half * 2 + b]);
+          if (!wait_all(&bar[Q_TRK00 + half * 2 + b], par, w)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t2 = 0; t2 < 32; ++t2) {
+              const int kc = cc * 32 + t2;
+              bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[64 + kc], kt[128 + kc],
+                                  kt[192 + kc], p.W) ? 1u : 0u) << t2;
+            }
+            lm[cc] = bits;
+          }
+        }
+        // S(g) has one barrier per buffer, so a wait never runs two phases behind S(g+1)
+        if (!wait_all(&bar[Q_SFULL0 + (g & 1)], (g >> 1) & 1, w)) { ok = false; break; }
+        if (!wait_all(&bar[Q_DPFULL], g & 1, w)) { ok = false; break; }
+        // S of the unit's first tile is issued: every role has read the queue entry
+        if (j == 0) mbar_arrive(&bar[Q_UEMPTY0 + slot]);
+        tc_fence_after();
+        const uint32_t ts = ((g & 1) ? tS1 : tS0) + half * 64;
+        uint32_t vs[2][32], vp[2][32];
+        tmem_ld32(ts + lb, vs[0]);
+        tmem_ld32(ts + lb + 32, vs[1]);
+        tmem_ld32(tP + lb + half * 64, vp[0]);
+        tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[Q_DPFREE]);  // dP(g+1) may now overwrite dP(g)
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t bits = 0;
+          uint32_t pk[16];
 #pragma unroll
-          for (int t2 = 0; t2 < 32; ++t2) {
-            const int kc = cc * 32 + t2;
-            bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[64 + kc], kt[128 + kc], kt[192 + kc],
-                                p.W) ? 1u : 0u) << t2;
+          for (int t = 0; t < 32; t += 2) {
+            const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
+            const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2) : 0.f;
+            const float p1 = l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2) : 0.f;
+            const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dlt);
+            const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dlt);
+            pk[t >> 1] = pack_bf16(d0, d1);
           }
-          lm[cc] = bits;
+          tmem_st16(ts + lb + cc * 16, pk);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[Q_PFULL00 + 2 * half + (g & 1)]);
       }
-      if (!wait_all(&bar[Q_SFULL0 + half], j & 1, w)) { ok = false; break; }
+      if (!ok) break;
+      // ---- the unit's dQ: dq_acc += scale * dQ through staged boxes and TMA reduce-adds.
+      // Every thread waits on each unit's phase in order, so no wait runs two phases ahead.
+      if (!wait_all(&bar[Q_ACCFULL], uc & 1, w)) break;
       tc_fence_after();
-      const uint32_t ts = ((j & 1) ? tS1 : tS0) + half * 64;
-      uint32_t vs[2][32], vp[2][32];
-      tmem_ld32(ts + lb, vs[0]);
-      tmem_ld32(ts + lb + 32, vs[1]);
-      tmem_ld32(tP + lb + half * 64, vp[0]);
-      tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
-          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2) : 0.f;
-          const float p1 = l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2) : 0.f;
-          const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dlt);
-          const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dlt);
-          pk[t >> 1] = pack_bf16(d0, d1);
-        }
-        tmem_st16(ts + lb + cc * 16, pk);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[Q_PFULL0 + half]);
-    }
-    // epilogue: dq_acc += scale * dQ as a TMA fp32 reduce-add of a tile staged in the Q/dO
-    // slots (all MMAs are done), D/32 boxes of 128 x 32 fp32: no load of dq_acc.  The MMA
-    // thread's final commit has one phase, so it is safe to wait on from either half (a
-    // per-tile barrier could be two phases behind while the other half is still working).
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok && !wait_all(&bar[Q_DRAIN], 0, w)) ok = false;
-    tc_fence_after();
-    uint8_t* stg = smem;
-    if (ok) {
+      uint8_t* box = (L::kStageInK ? sK0 + ((g - 1) % 3) * kTile : smem + L::kStg) + half * 16384;
 #pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
+      for (int r = 0; r < kRounds; ++r, ++rc) {
+        const int c = half * kRounds + r;  // 32-column chunk of dQ
         uint32_t x[32];
         tmem_ld32(tQ + lb + c * 32, x);
         tmem_ld_wait();
+        if (r == kRounds - 1) {
+          tc_fence_before();
+          mbar_arrive(&bar[Q_ACCFREE]);  // the next unit's dQ MMAs may overwrite TMEM
+        }
+        // the box is free once this half's previous round has been read by its TMA
+        if (rc > 0 && !wait_all(&bar[Q_STGR0 + half], (rc - 1) & 1, w)) { ok = false; break; }
         float v[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(x[t]);
-        stage_row32(stg + c * 16384, row, v);
+        fence_proxy_async_smem();
+        stage_row32(box, row, v);
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[Q_STG0 + half]);
+        if (row == 0) {
+          if (mbar_wait(&bar[Q_STG0 + half], rc & 1, w)) {
+            tma_reduce_add_3d(&p.dq_map, box, c * 32, (int)(nq * 128), h);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar[Q_STGR0 + half]);
+          // with d = 128 the boxes sit in the last tile's K stage: the second half to finish
+          // hands it back to the producer
+          if (L::kStageInK && r == kRounds - 1 && atomicAdd(&epi_count, 1) == 1) {
+            epi_count = 0;
+            mbar_arrive(&bar[Q_KEMPTY0 + (g - 1) % 3]);
+          }
+        }
       }
-      fence_proxy_async_smem();
+      ++uc;
     }
-    mbar_arrive(&bar[Q_EPI]);
-    if (row == 0 && half == 0 && ok && mbar_wait(&bar[Q_EPI], 0, w)) {
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c)
-        tma_reduce_add_3d(&p.dq_map, stg + c * 16384, c * 32, (int)(nq * 128), h);
-      bulk_commit();
-      bulk_wait_all();
-    }
+    // the global writes of every TMA reduce this thread issued have completed
+    if (row == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -336,19 +545,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (threadIdx.x == 0) release_tickets(p);
 }
 
 // ======================================================================================
 // dK / dV (KV-stationary)
 // ======================================================================================
-// As in the dQ kernel, the item's 128 q columns are worked as two halves that run as two
-// chains offset in time.  Per item j and half h:
+// Item g (counted over all units of the CTA) and half h (q columns [64h, 64h + 64)):
 //   S^T_h = K Q_h^T and dP^T_h = V dO_h^T (N = 64)  ->  elementwise: P^T_h and dS^T_h (bf16)
 //   over them  ->  dV += P^T_h dO_h and dK += dS^T_h Q_h (K = 64).
-// With dV and dK resident, TMEM holds one S^T / dP^T buffer: S^T_h(j+1) is issued once the
-// MMAs of half h of item j have completed, while the other half's elementwise runs.
-enum { K_KVFULL, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL0, K_SFULL1, K_PFULL0,
-       K_PFULL1, K_CONS0, K_CONS1, K_DRAIN, K_TRK00, K_TRK01, K_TRK10, K_TRK11, K_EPI, K_NUM };
+// With dV and dK resident, TMEM holds one S^T / dP^T buffer: S^T_h(g+1) is issued once the
+// MMAs of half h of item g have completed, while the other half's elementwise runs.
+// The epilogue stages dV, then dK, in the Q/dO stage of the unit's last item (free once the
+// unit's last MMAs are done; the epilogue hands it back to the producer) and adds them to
+// dv_acc / dk_acc with TMA reduce-adds.
+enum {
+  K_KVFULL, K_KVEMPTY, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL0, K_SFULL1, K_PFULL0,
+  K_PFULL1, K_CONS0, K_CONS1, K_ACCFULL, K_ACCFREE, K_STG0, K_STG1, K_STGR0, K_STGR1, K_TRK00,
+  K_TRK01, K_TRK10, K_TRK11, K_UFULL0, K_UEMPTY0 = K_UFULL0 + kQueue,
+  K_DRAIN = K_UEMPTY0 + kQueue, K_NUM
+};
+
+__host__ __device__ constexpr int dkdv_arrivals(int b) {
+  return (b == K_ACCFREE || (b >= K_UEMPTY0 && b < K_UEMPTY0 + kQueue))
+             ? 256
+             : ((b == K_PFULL0 || b == K_PFULL1 || b == K_STG0 || b == K_STG1 ||
+                 (b >= K_TRK00 && b <= K_TRK11))
+                    ? 128
+                    : 1);
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant__ BwdParams p) {
@@ -362,37 +587,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   // per half and buffer: lse2[64] | delta[64] | tracks [4][64]
   float* stg = reinterpret_cast<float*>(smem + 6 * kTile);
   __shared__ __align__(8) uint64_t bar[K_NUM];
+  __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ int epi_count;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long n = p.n;
-  int64_t nk;
-  int kh;
-  if (p.kv_shard >= 0) {
-    kh = blockIdx.x / p.bps;
-    nk = (int64_t)p.kv_shard * p.bps + blockIdx.x % p.bps;
-  } else {
-    const int64_t cnt = p.needed_ptr[p.q_shard + 1] - p.needed_ptr[p.q_shard];
-    kh = (int)(blockIdx.x / cnt);
-    nk = p.needed[p.needed_ptr[p.q_shard] + blockIdx.x % cnt];
-  }
-  const int64_t c0 = p.colT_ptr[nk * p.P + p.q_shard];
-  const int L = (int)(p.colT_ptr[nk * p.P + p.q_shard + 1] - c0);
-  const int T = L * p.group;  // items: (q head of the group, listed q block)
-  if (T == 0) return;
-
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int b = 0; b < K_NUM; ++b) {
-      const int cnt = (b == K_EPI) ? 256
-                      : (b == K_PFULL0 || b == K_PFULL1 || b == K_TRK00 || b == K_TRK01 ||
-                         b == K_TRK10 || b == K_TRK11)
-                          ? 128
-                          : 1;
-      mbar_init(&bar[b], cnt);
-    }
+    epi_count = 0;
+    for (int b = 0; b < K_NUM; ++b) mbar_init(&bar[b], dkdv_arrivals(b));
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -409,60 +615,72 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
   const uint32_t tdK = tmem_base + 384;   // dK fp32 [384, 384+D)
 
-  if (warp == 0) {
+  if (warp == kWarpSched) {
+    if (lane == 0) schedule<false>(p, queue, &bar[K_UFULL0], &bar[K_UEMPTY0], w);
+    __syncwarp();
+  } else if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&p.q_map);
       tma_prefetch_desc(&p.k_map);
       tma_prefetch_desc(&p.v_map);
       tma_prefetch_desc(&p.do_map);
-      mbar_arrive_expect_tx(&bar[K_KVFULL], 2 * kTile);
-      for (int a = 0; a < kAtoms; ++a) {
-        tma_load_3d(sK + a * 16384, &p.k_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
-        tma_load_3d(sV + a * 16384, &p.v_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
-      }
     }
-    int fills[2] = {0, 0};
-    for (int it = 0; it < T; ++it) {
-      const int s = it & 1;
-      if (it >= 2 && !warp_wait(&bar[K_QEMPTY0 + s], ((it >> 1) - 1) & 1, w)) break;
-      const int h = kh * p.group + it / L;
-      const int nqb = p.colT_row[c0 + it % L];
+    int uc = 0, g = 0, kv_fills = 0, q_fills[2] = {0, 0};
+    bool ok = true;
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[K_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int kh = queue.head[slot];
+      if (kh < 0) break;
+      const int64_t nk = queue.blk[slot];
+      const int L = queue.T[slot];
+      const int64_t c0 = queue.e0[slot];
+      const int items = L * p.group;
+      // K and V of the unit once the previous unit's last S^T / dP^T have read the slot
+      if (uc >= 1 && !wait_all(&bar[K_KVEMPTY], (uc - 1) & 1, w)) break;
       if (lane == 0) {
-        uint8_t* sQ = sQ0 + s * 2 * kTile;
-        uint8_t* sDO = sQ + kTile;
-        mbar_arrive_expect_tx(&bar[K_QFULL0 + s], 2 * kTile);
+        mbar_arrive_expect_tx(&bar[K_KVFULL], 2 * kTile);
         for (int a = 0; a < kAtoms; ++a) {
-          tma_load_3d(sQ + a * 16384, &p.q_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
-          tma_load_3d(sDO + a * 16384, &p.do_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
+          tma_load_3d(sK + a * 16384, &p.k_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
+          tma_load_3d(sV + a * 16384, &p.v_map, &bar[K_KVFULL], a * 64, (int)(nk * 128), kh);
         }
       }
-      ++fills[s];
-      if (it == 1) {
-        // pull the later items' Q/dO tiles toward L2 once the first two loads are queued
-        for (int i2 = 2 + lane; i2 < T && i2 < kPrefetchTiles; i2 += 32) {
-          const int h2 = kh * p.group + i2 / L;
-          const int nq2 = p.colT_row[c0 + i2 % L];
+      ++kv_fills;
+      for (int it = 0; it < items; ++it) {
+        const int s = g & 1;
+        if (g >= 2 && !wait_all(&bar[K_QEMPTY0 + s], ((g >> 1) - 1) & 1, w)) { ok = false; break; }
+        const int h = kh * p.group + it / L;
+        const int nqb = p.colT_row[c0 + it % L];
+        if (lane == 0) {
+          uint8_t* sQ = sQ0 + s * 2 * kTile;
+          uint8_t* sDO = sQ + kTile;
+          mbar_arrive_expect_tx(&bar[K_QFULL0 + s], 2 * kTile);
           for (int a = 0; a < kAtoms; ++a) {
-            tma_prefetch_l2_3d(&p.q_map, a * 64, nq2 * 128, h2);
-            tma_prefetch_l2_3d(&p.do_map, a * 64, nq2 * 128, h2);
+            tma_load_3d(sQ + a * 16384, &p.q_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
+            tma_load_3d(sDO + a * 16384, &p.do_map, &bar[K_QFULL0 + s], a * 64, nqb * 128, h);
           }
         }
+        ++q_fills[s];
+        ++g;
       }
+      ++uc;
     }
     if (lane == 0) {
-      drain_wait(&bar[K_KVFULL], 0, p.wait_ns, p.err);
+      if (kv_fills) drain_wait(&bar[K_KVFULL], (kv_fills - 1) & 1, p.wait_ns, p.err);
       for (int s = 0; s < 2; ++s)
-        if (fills[s]) drain_wait(&bar[K_QFULL0 + s], (fills[s] - 1) & 1, p.wait_ns, p.err);
+        if (q_fills[s]) drain_wait(&bar[K_QFULL0 + s], (q_fills[s] - 1) & 1, p.wait_ns, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      // S^T_hh(it) and dP^T_hh(it): q rows [64 hh, 64 hh + 64) of stage it & 1
-      auto issue_s = [&](int it, int hh) {
-        const uint32_t aQ = smem_u32(sQ0 + (it & 1) * 2 * kTile) + hh * 8192, aDO = aQ + kTile;
+      // S^T_hh(gg) and dP^T_hh(gg): q rows [64 hh, 64 hh + 64) of stage gg & 1
+      auto issue_s = [&](int gg, int hh) {
+        const uint32_t aQ = smem_u32(sQ0 + (gg & 1) * 2 * kTile) + hh * 8192, aDO = aQ + kTile;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -477,38 +695,76 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         }
         mma_commit(&bar[K_SFULL0 + hh]);
       };
-      bool ok = mbar_wait(&bar[K_KVFULL], 0, w) && mbar_wait(&bar[K_QFULL0], 0, w);
+      int uc = 0, j = 0, g = 0, items = 0;
+      bool ok = mbar_wait(&bar[K_UFULL0], 0, w) && queue.head[0] >= 0;
+      if (ok) {
+        items = queue.T[0] * p.group;
+        ok = mbar_wait(&bar[K_KVFULL], 0, w) && mbar_wait(&bar[K_QFULL0], 0, w);
+      }
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         issue_s(0, 1);
+        if (items == 1) mma_commit(&bar[K_KVEMPTY]);  // the unit's last read of K and V
       }
-      for (int it = 0; ok && it < T; ++it) {
-        const int s = it & 1;
-        const bool nxt = it + 1 < T;
-        if (nxt && !mbar_wait(&bar[K_QFULL0 + ((it + 1) & 1)], ((it + 1) >> 1) & 1, w)) break;
-        const uint32_t aQ = smem_u32(sQ0 + s * 2 * kTile), aDO = aQ + kTile;
+      while (ok) {
+        // the item after g: the next of this unit, or the first of the next unit
+        bool nxt = true, newu = false;
+        int itn = items;
+        if (j + 1 == items) {
+          const int slot = (uc + 1) % kQueue;
+          if (!mbar_wait(&bar[K_UFULL0 + slot], ((uc + 1) / kQueue) & 1, w)) break;
+          if (queue.head[slot] < 0) {
+            nxt = false;
+          } else {
+            newu = true;
+            itn = queue.T[slot] * p.group;
+          }
+        }
+        if (nxt) {
+          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) break;
+          if (newu && !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w)) break;
+        }
+        const uint32_t aQ = smem_u32(sQ0 + (g & 1) * 2 * kTile), aDO = aQ + kTile;
         for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&bar[K_PFULL0 + hh], it & 1, w)) { ok = false; break; }
+          if (!mbar_wait(&bar[K_PFULL0 + hh], g & 1, w)) { ok = false; break; }
+          // the unit's first accumulation overwrites dV / dK: the previous unit's must be out
+          if (j == 0 && hh == 0 && uc >= 1 && !mbar_wait(&bar[K_ACCFREE], (uc - 1) & 1, w)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tdV, tS + hh * 64 + kk * 8,
                    sdesc_sw128(aDO + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
-                   (it > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ts(tdK, tP + hh * 64 + kk * 8,
                    sdesc_sw128(aQ + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
-                   (it > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&bar[K_CONS0 + hh]);
-          if (hh == 1) mma_commit(&bar[K_QEMPTY0 + s]);
+          if (hh == 1) {
+            // the unit's last Q/dO stage is handed back by the epilogue, which stages in it
+            if (j == items - 1)
+              mma_commit(&bar[K_ACCFULL]);
+            else
+              mma_commit(&bar[K_QEMPTY0 + (g & 1)]);
+          }
           if (nxt) {
             // half hh of the S^T / dP^T buffer is free once these MMAs have read P^T / dS^T
-            if (!mbar_wait(&bar[K_CONS0 + hh], it & 1, w)) { ok = false; break; }
+            if (!mbar_wait(&bar[K_CONS0 + hh], g & 1, w)) { ok = false; break; }
             tc_fence_after();
-            issue_s(it + 1, hh);
+            issue_s(g + 1, hh);
+            if (hh == 1 && (newu ? itn == 1 : j + 2 == items)) mma_commit(&bar[K_KVEMPTY]);
           }
+        }
+        if (!ok || !nxt) break;
+        ++g;
+        if (newu) {
+          ++uc;
+          j = 0;
+          items = itn;
+        } else {
+          ++j;
         }
       }
       mma_commit(&bar[K_DRAIN]);
@@ -516,119 +772,151 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     }
     __syncwarp();
   } else {
+    // ------------------------------------------------------------------ elementwise
     // four warps per half: `half` owns q columns [64 half, 64 half + 64), one kv row a thread
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;  // kv row of the tile
     const int hr = row & 63;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    const int64_t tk = nk * 128 + row;
-    const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
-              pk = p.tracks[3 * n + tk];
     const float sl2 = p.sl2;
+    int uc = 0, g = 0, rc = 0;  // rc: this half's epilogue rounds
     bool ok = true;
-    for (int it = 0; it < T; ++it) {
-      const int h = kh * p.group + it / L;
-      const int64_t e = c0 + it % L;
-      const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
-      const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
-      // stage this half's per-query LSE (base 2), delta and, on partial tiles, tracks: the
-      // first 64 threads of the half the two floats, the other 64 the four tracks
-      const int b = it & 1;
-      float* lse2s = stg + (half * 2 + b) * 384;
-      float* dls = lse2s + 64;
-      int32_t* qt = reinterpret_cast<int32_t*>(lse2s + 128);
-      if ((row >> 6) == 0) {
-        const float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
-        lse2s[hr] = (l2 == -INFINITY) ? INFINITY : l2;
-        dls[hr] = p.delta[(int64_t)h * n + qrow];
-      } else if (partial) {
-        qt[hr] = p.tracks[qrow];
-        qt[64 + hr] = p.tracks[n + qrow];
-        qt[128 + hr] = p.tracks[2 * n + qrow];
-        qt[192 + hr] = p.tracks[3 * n + qrow];
-      }
-      mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
-      if (!wait_all(&bar[K_TRK00 + half * 2 + b], (it >> 1) & 1, w)) { ok = false; break; }
-      uint32_t lm[2] = {~0u, ~0u};
-      if (partial) {
+    while (ok) {
+      const int slot = uc % kQueue;
+      if (!wait_all(&bar[K_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      const int kh = queue.head[slot];
+      if (kh < 0) break;
+      const int64_t nk = queue.blk[slot];
+      const int L = queue.T[slot];
+      const int64_t c0 = queue.e0[slot];
+      const int items = L * p.group;
+      const int64_t tk = nk * 128 + row;
+      const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
+                pk = p.tracks[3 * n + tk];
+      for (int it = 0; it < items; ++it, ++g) {
+        const int h = kh * p.group + it / L;
+        const int64_t e = c0 + it % L;
+        const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
+        const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
+        // stage this half's per-query LSE (base 2), delta and, on partial tiles, tracks: the
+        // threads of rows [0, 64) the two floats, those of rows [64, 128) the four tracks
+        const int b = g & 1;
+        float* lse2s = stg + (half * 2 + b) * 384;
+        float* dls = lse2s + 64;
+        int32_t* qt = reinterpret_cast<int32_t*>(lse2s + 128);
+        if ((row >> 6) == 0) {
+          const float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
+          lse2s[hr] = (l2 == -INFINITY) ? INFINITY : l2;
+          dls[hr] = p.delta[(int64_t)h * n + qrow];
+        } else if (partial) {
+          qt[hr] = p.tracks[qrow];
+          qt[64 + hr] = p.tracks[n + qrow];
+          qt[128 + hr] = p.tracks[2 * n + qrow];
+          qt[192 + hr] = p.tracks[3 * n + qrow];
+        }
+        mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
+        if (!wait_all(&bar[K_TRK00 + half * 2 + b], (g >> 1) & 1, w)) { ok = false; break; }
+        uint32_t lm[2] = {~0u, ~0u};
+        if (partial) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t2 = 0; t2 < 32; ++t2) {
+              const int q = cc * 32 + t2;
+              bits |= (mask_legal(qt[q], qt[64 + q], qt[128 + q], qt[192 + q], sk, gk, zk, pk,
+                                  p.W) ? 1u : 0u) << t2;
+            }
+            lm[cc] = bits;
+          }
+        }
+        if (!wait_all(&bar[K_SFULL0 + half], g & 1, w)) { ok = false; break; }
+        // S^T of the unit's first item is issued: every role has read the queue entry
+        if (it == 0) mbar_arrive(&bar[K_UEMPTY0 + slot]);
+        tc_fence_after();
+        uint32_t vs[2][32], vp[2][32];
+        tmem_ld32(tS + lb + half * 64, vs[0]);
+        tmem_ld32(tS + lb + half * 64 + 32, vs[1]);
+        tmem_ld32(tP + lb + half * 64, vp[0]);
+        tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
+        tmem_ld_wait();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
-          uint32_t bits = 0;
+          uint32_t pk16[16], dk16[16];
 #pragma unroll
-          for (int t2 = 0; t2 < 32; ++t2) {
-            const int q = cc * 32 + t2;
-            bits |= (mask_legal(qt[q], qt[64 + q], qt[128 + q], qt[192 + q], sk, gk, zk, pk,
-                                p.W) ? 1u : 0u) << t2;
+          for (int t = 0; t < 32; t += 2) {
+            const int q0 = cc * 32 + t;
+            const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
+            const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2s[q0]) : 0.f;
+            const float p1 =
+                l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
+            const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dls[q0]);
+            const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dls[q0 + 1]);
+            pk16[t >> 1] = pack_bf16(p0, p1);
+            dk16[t >> 1] = pack_bf16(d0, d1);
           }
-          lm[cc] = bits;
+          tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
+          tmem_st16(tP + lb + half * 64 + cc * 16, dk16);
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[K_PFULL0 + half]);
       }
-      if (!wait_all(&bar[K_SFULL0 + half], it & 1, w)) { ok = false; break; }
+      if (!ok) break;
+      // ---- the unit's dV and dK (dv_acc += dV, dk_acc += scale * dK): round 0 stages this
+      // half's dV columns, round 1 its dK columns, as 128 x 32 fp32 boxes in the Q/dO stage of
+      // the unit's last item, each added by a TMA reduce-add.  Every thread waits on each
+      // unit's phase in order, so no wait runs two phases ahead.
+      if (!wait_all(&bar[K_ACCFULL], uc & 1, w)) break;
       tc_fence_after();
-      uint32_t vs[2][32], vp[2][32];
-      tmem_ld32(tS + lb + half * 64, vs[0]);
-      tmem_ld32(tS + lb + half * 64 + 32, vs[1]);
-      tmem_ld32(tP + lb + half * 64, vp[0]);
-      tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t pk16[16], dk16[16];
-#pragma unroll
-        for (int t = 0; t < 32; t += 2) {
-          const int q0 = cc * 32 + t;
-          const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
-          const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2s[q0]) : 0.f;
-          const float p1 =
-              l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
-          const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dls[q0]);
-          const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dls[q0 + 1]);
-          pk16[t >> 1] = pack_bf16(p0, p1);
-          dk16[t >> 1] = pack_bf16(d0, d1);
-        }
-        tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
-        tmem_st16(tP + lb + half * 64 + cc * 16, dk16);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bar[K_PFULL0 + half]);
-    }
-    // epilogue: dv_acc += dV and dk_acc += scale * dK as TMA fp32 reduce-adds of tiles staged
-    // in the K/V and first Q/dO slots (all MMAs are done): no load of the accumulators.  The
-    // MMA thread's final commit has one phase, so it is safe to wait on from either half.
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok && !wait_all(&bar[K_DRAIN], 0, w)) ok = false;
-    tc_fence_after();
-    uint8_t* stv = smem;
-    uint8_t* stk = smem + (D / 32) * 16384;
-    if (ok) {
+      constexpr int kB = D / 64;  // boxes per half and round
+      uint8_t* boxes = sQ0 + ((g - 1) & 1) * 2 * kTile + half * kB * 16384;
 #pragma unroll 1
-      for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
-        uint32_t xv[32], xk[32];
-        tmem_ld32(tdV + lb + c * 32, xv);
-        tmem_ld32(tdK + lb + c * 32, xk);
+      for (int r = 0; r < 2; ++r, ++rc) {
+        const uint32_t tacc = r == 0 ? tdV : tdK;
+        const float sc = r == 0 ? 1.f : p.scale;
+        uint32_t x[kB][32];
+#pragma unroll
+        for (int cb = 0; cb < kB; ++cb) tmem_ld32(tacc + lb + (half * kB + cb) * 32, x[cb]);
         tmem_ld_wait();
-        float v[32];
+        if (r == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar[K_ACCFREE]);  // the next unit's dV / dK MMAs may overwrite TMEM
+        }
+        // the boxes are free once this half's previous round has been read by its TMA
+        if (rc > 0 && !wait_all(&bar[K_STGR0 + half], (rc - 1) & 1, w)) { ok = false; break; }
+        fence_proxy_async_smem();
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = __uint_as_float(xv[t]);
-        stage_row32(stv + c * 16384, row, v);
+        for (int cb = 0; cb < kB; ++cb) {
+          float v[32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(xk[t]);
-        stage_row32(stk + c * 16384, row, v);
+          for (int t = 0; t < 32; ++t) v[t] = sc * __uint_as_float(x[cb][t]);
+          stage_row32(boxes + cb * 16384, row, v);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[K_STG0 + half]);
+        if (row == 0) {
+          if (mbar_wait(&bar[K_STG0 + half], rc & 1, w)) {
+#pragma unroll
+            for (int cb = 0; cb < kB; ++cb)
+              tma_reduce_add_3d(r == 0 ? (const void*)&p.dv_map : (const void*)&p.dk_map,
+                                boxes + cb * 16384, (half * kB + cb) * 32, (int)(nk * 128), kh);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar[K_STGR0 + half]);
+          // the second half to finish hands the Q/dO stage back to the producer
+          if (r == 1 && atomicAdd(&epi_count, 1) == 1) {
+            epi_count = 0;
+            mbar_arrive(&bar[K_QEMPTY0 + ((g - 1) & 1)]);
+          }
+        }
       }
-      fence_proxy_async_smem();
+      ++uc;
     }
-    mbar_arrive(&bar[K_EPI]);
-    if (row == 0 && half == 0 && ok && mbar_wait(&bar[K_EPI], 0, w)) {
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        tma_reduce_add_3d(&p.dv_map, stv + c * 16384, c * 32, (int)(nk * 128), kh);
-        tma_reduce_add_3d(&p.dk_map, stk + c * 16384, c * 32, (int)(nk * 128), kh);
-      }
-      bulk_commit();
-      bulk_wait_all();
-    }
+    // the global writes of every TMA reduce this thread issued have completed
+    if (row == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -636,13 +924,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+  if (threadIdx.x == 0) release_tickets(p);
 }
 
 template <int D>
-size_t bwd_smem() {
-  // one CTA per SM: each CTA owns all 512 TMEM columns
-  size_t smem = 6 * (128 * D * 2) + 2 * 2 * 384 * 4 + 1024;
-  return smem < 120 * 1024 ? 120 * 1024 : smem;
+size_t dkdv_smem() {
+  // K, V, two Q/dO stages (6 tiles) + per-half staging of LSE, delta and tracks
+  return 6 * (128 * D * 2) + 2 * 2 * 384 * 4 + 1024;
 }
 
 template <int D>
@@ -691,25 +979,51 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   prm.W = pl->W;
   prm.scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
   prm.sl2 = prm.scale * kLog2e;
-  const size_t smem = bwd_smem<D>();
+  const size_t smem_q = DqSmem<D>::bytes(), smem_k = dkdv_smem<D>();
   if (once_per_device(D == 128 ? 3 : 4)) {
     cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem);
+                               (int)smem_k);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
   }
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int P = pl->P;
   for (int i = 0; i < n_steps; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
-    k_bwd_dq<D><<<(unsigned)(pl->bps * qkv->hq), kThreads, smem, s>>>(prm);
-    int64_t units;
-    if (prm.kv_shard >= 0)
-      units = pl->bps * qkv->hkv;
-    else
-      units = (pl->h_needed_ptr[prm.q_shard + 1] - pl->h_needed_ptr[prm.q_shard]) * qkv->hkv;
-    if (units > 0) k_bwd_dkdv<D><<<(unsigned)units, kThreads, smem, s>>>(prm);
+    // dQ: the q blocks of the q shard with tiles in this step, longest list first
+    {
+      BwdParams pq = prm;
+      const int64_t seg = (int64_t)pq.q_shard * (P + 1) + (pq.kv_shard >= 0 ? pq.kv_shard : P);
+      pq.order = pl->fwd_order + seg * pl->bps;
+      pq.nwork = pl->h_fwd_nwork[seg] * qkv->hq;
+      if (pq.nwork > 0) {
+        pq.sched = sched_slot(pl);
+        k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kThreads, smem_q, s>>>(pq);
+      }
+    }
+    // dK/dV: the kv blocks of the kv shard listed for the q shard (longest list first), or
+    // the q shard's needed kv blocks
+    {
+      BwdParams pk = prm;
+      if (pk.kv_shard >= 0) {
+        const int64_t seg = (int64_t)pk.kv_shard * (P + 1) + pk.q_shard;
+        pk.order = pl->bwd_order + seg * pl->bps;
+        pk.nwork = pl->h_bwd_nwork[seg] * qkv->hkv;
+      } else {
+        pk.order = nullptr;
+        pk.nwork = (int)(pl->h_needed_ptr[pk.q_shard + 1] - pl->h_needed_ptr[pk.q_shard]) *
+                   qkv->hkv;
+      }
+      if (pk.nwork > 0) {
+        pk.sched = sched_slot(pl);
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s>>>(pk);
+      }
+    }
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");
