@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <map>
 #include <set>
 #include <string>
 #include <vector>
@@ -47,6 +48,36 @@ bool once_per_device(int key) {
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
   return seen.insert({key, dev}).second;
+}
+
+// Fork / join of a per-device side stream: work queued on the side stream between fork()
+// and join() runs after everything queued on `s` before fork(), and everything queued on `s`
+// after join() runs after it.
+cudaStream_t side_stream() {
+  static std::mutex mu;
+  static std::map<int, cudaStream_t> streams;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = streams.find(dev);
+  if (it != streams.end()) return it->second;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  streams[dev] = st;
+  return st;
+}
+
+cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
+  cudaEvent_t e;
+  cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+  if (r != cudaSuccess) return r;
+  r = cudaEventRecord(e, from);
+  if (r == cudaSuccess) r = cudaStreamWaitEvent(to, e, 0);
+  cudaEventDestroy(e);  // released once the recorded work completes
+  return r;
 }
 
 // true for device or managed memory of the current context

@@ -160,43 +160,44 @@ __device__ __forceinline__ void release_tickets(const BwdParams& p) {
 // ======================================================================================
 // Tile g counts the tiles of all units of the CTA.  Per tile:
 //   S = Q K^T and dP = dO V^T (N = 128)  ->  elementwise, half h (kv columns [64h, 64h+64)):
-//   dS_h (bf16) over S_h  ->  dQ += dS_h K_h (K = 64).
+//   dS_h (bf16) over S_h  ->  dQ += dS K (dS read from the halves' packed columns).
 // S alternates between two TMEM buffers by tile and is issued for tile g+1 as soon as the dQ
 // MMAs of tile g-1 are done; dP has one buffer, rewritten once both halves have loaded it.
 // So S(g+1) and dP(g+1) run during the elementwise stage of tile g, and the elementwise warps
 // can finish tile g+1 before the MMA thread has seen tile g finished: the "dS written" barrier
 // of each half is therefore doubled by tile parity, so that no wait aliases a phase two ahead.  K streams through three
-// stages (S(g+1) is issued while K(g) still feeds dQ(g)), V through one (only dP reads it).
-// The epilogue stages the fp32 dQ tile in shared memory (in the K stage of the unit's last
-// tile when d = 128, which the epilogue hands back to the producer) and adds it to dq_acc
-// with TMA reduce-adds.
+// stages (S(g+1) is issued while K(g) still feeds dQ(g)), V through two (only dP reads it).
+// The epilogue stages the fp32 dQ tile in shared memory in one round (in the K and V stages
+// of the unit's last tile when d = 128, which the epilogue then hands back to the producer)
+// and adds it to dq_acc with TMA reduce-adds.  At a unit's last tile the MMA thread issues
+// the last dQ MMA before the next unit's score MMAs, which wait for that unit's Q and dO.
 enum {
-  Q_QFULL, Q_QEMPTY, Q_KFULL0, Q_KFULL1, Q_KFULL2, Q_KEMPTY0, Q_KEMPTY1, Q_KEMPTY2, Q_VFULL,
-  Q_VEMPTY, Q_SFULL0, Q_SFULL1, Q_DPFULL, Q_DPFREE, Q_PFULL00, Q_PFULL01, Q_PFULL10, Q_PFULL11,
+  Q_QFULL, Q_QEMPTY, Q_KFULL0, Q_KFULL1, Q_KFULL2, Q_KEMPTY0, Q_KEMPTY1, Q_KEMPTY2, Q_VFULL0,
+  Q_VFULL1, Q_VEMPTY0, Q_VEMPTY1, Q_SFULL0, Q_SFULL1, Q_DPFULL, Q_DPFREE, Q_PFULL00, Q_PFULL01,
+  Q_PFULL10, Q_PFULL11,
   Q_DQDONE, Q_ACCFULL,
-  Q_ACCFREE, Q_STG0, Q_STG1, Q_STGR0, Q_STGR1, Q_TRK00, Q_TRK01, Q_TRK10, Q_TRK11, Q_UFULL0,
+  Q_ACCFREE, Q_STG0, Q_STG1, Q_UFULL0,
   Q_UEMPTY0 = Q_UFULL0 + kQueue, Q_DRAIN = Q_UEMPTY0 + kQueue, Q_NUM
 };
 
 __host__ __device__ constexpr int dq_arrivals(int b) {
   return (b == Q_ACCFREE || b == Q_DPFREE || (b >= Q_UEMPTY0 && b < Q_UEMPTY0 + kQueue))
              ? 256
-             : (((b >= Q_PFULL00 && b <= Q_PFULL11) || b == Q_STG0 || b == Q_STG1 ||
-                 (b >= Q_TRK00 && b <= Q_TRK11))
-                    ? 128
-                    : 1);
+             : (((b >= Q_PFULL00 && b <= Q_PFULL11) || b == Q_STG0 || b == Q_STG1) ? 128 : 1);
 }
 
-// shared memory of the dQ kernel: Q | dO | K stages (3) | V | key tracks [2][2][4][64] |
-// (d = 64 only) a staging area of two fp32 boxes
+// shared memory of the dQ kernel: Q | dO | K stages (3) | V stages (2) | (d = 64 only) a
+// staging area of two fp32 boxes.  With d = 128 this is 224 KB, so the keys' tracks of a
+// partial tile are read from global memory rather than staged.
 template <int D>
 struct DqSmem {
   static constexpr int kTile = 128 * D * 2;
-  static constexpr bool kStageInK = D == 128;  // two 16 KB boxes fit in one K stage
+  // d = 128: half 0 stages its two 16 KB boxes in the last tile's K stage, half 1 in its V
+  // stage; d = 64: a dedicated area of two boxes
+  static constexpr bool kStageInK = D == 128;
   static constexpr int kK = 2 * kTile;
   static constexpr int kV = 5 * kTile;
-  static constexpr int kTrk = 6 * kTile;
-  static constexpr int kStg = kTrk + 4096;
+  static constexpr int kStg = 7 * kTile;
   static constexpr int kEnd = kStg + (kStageInK ? 0 : 32768);
   static constexpr size_t bytes() { return (size_t)kEnd + 1024; }
 };
@@ -207,14 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
   using L = DqSmem<D>;
   constexpr int kTile = L::kTile;
   constexpr int kAtoms = D / 64;
-  constexpr int kRounds = D / 64;  // epilogue rounds: one 32-column box per half per round
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + kTile;
   uint8_t* sK0 = smem + L::kK;  // stage s at sK0 + s * kTile
-  uint8_t* sV = smem + L::kV;
-  int32_t* ktr = reinterpret_cast<int32_t*>(smem + L::kTrk);  // [half][buffer][4][64]
+  uint8_t* sV0 = smem + L::kV;  // stage s at sV0 + s * kTile
   __shared__ __align__(8) uint64_t bar[Q_NUM];
   __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
@@ -255,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       tma_prefetch_desc(&p.v_map);
       tma_prefetch_desc(&p.do_map);
     }
-    int uc = 0, g = 0, q_fills = 0, k_fills[3] = {0, 0, 0}, v_fills = 0;
+    int uc = 0, g = 0, q_fills = 0, k_fills[3] = {0, 0, 0}, v_fills[2] = {0, 0};
     bool ok = true;
     while (ok) {
       const int slot = uc % kQueue;
@@ -287,13 +286,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
                         nk * 128, kvh);
         }
         ++k_fills[s];
-        if (g >= 1 && !wait_all(&bar[Q_VEMPTY], (g - 1) & 1, w)) { ok = false; break; }
+        const int sv = g & 1;
+        if (g >= 2 && !wait_all(&bar[Q_VEMPTY0 + sv], ((g >> 1) - 1) & 1, w)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar[Q_VFULL], kTile);
+          mbar_arrive_expect_tx(&bar[Q_VFULL0 + sv], kTile);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_3d(sV + a * 16384, &p.v_map, &bar[Q_VFULL], a * 64, nk * 128, kvh);
+            tma_load_3d(sV0 + sv * kTile + a * 16384, &p.v_map, &bar[Q_VFULL0 + sv], a * 64,
+                        nk * 128, kvh);
         }
-        ++v_fills;
+        ++v_fills[sv];
       }
       ++uc;
     }
@@ -303,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
       if (q_fills) drain_wait(&bar[Q_QFULL], (q_fills - 1) & 1, p.wait_ns, p.err);
       for (int s = 0; s < 3; ++s)
         if (k_fills[s]) drain_wait(&bar[Q_KFULL0 + s], (k_fills[s] - 1) & 1, p.wait_ns, p.err);
-      if (v_fills) drain_wait(&bar[Q_VFULL], (v_fills - 1) & 1, p.wait_ns, p.err);
+      for (int s = 0; s < 2; ++s)
+        if (v_fills[s]) drain_wait(&bar[Q_VFULL0 + s], (v_fills[s] - 1) & 1, p.wait_ns, p.err);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -311,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO), aV = smem_u32(sV);
+      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
       auto issue_s = [&](int gg) {  // S(gg) into S buffer gg & 1
         const uint32_t aK = smem_u32(sK0 + (gg % 3) * kTile);
         const uint32_t ts = (gg & 1) ? tS1 : tS0;
@@ -323,7 +325,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         }
         mma_commit(&bar[Q_SFULL0 + (gg & 1)]);
       };
-      auto issue_dp = [&]() {  // dP of the tile whose V is staged
+      auto issue_dp = [&](int gg, bool last) {  // dP(gg), V from stage gg & 1
+        const uint32_t aV = smem_u32(sV0 + (gg & 1) * kTile);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
@@ -331,19 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
                  k > 0);
         }
         mma_commit(&bar[Q_DPFULL]);
-        mma_commit(&bar[Q_VEMPTY]);
+        // with d = 128 the epilogue stages in a unit's last V stage and hands it back itself
+        if (!(L::kStageInK && last)) mma_commit(&bar[Q_VEMPTY0 + (gg & 1)]);
       };
       int uc = 0, j = 0, g = 0, T = 0;
       bool ok = mbar_wait(&bar[Q_UFULL0], 0, w) && queue.head[0] >= 0;
       if (ok) {
         T = queue.T[0];
         ok = mbar_wait(&bar[Q_QFULL], 0, w) && mbar_wait(&bar[Q_KFULL0], 0, w) &&
-             mbar_wait(&bar[Q_VFULL], 0, w);
+             mbar_wait(&bar[Q_VFULL0], 0, w);
       }
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        issue_dp();
+        issue_dp(0, T == 1);
         if (T == 1) mma_commit(&bar[Q_QEMPTY]);  // the unit's last read of Q and dO
       }
       while (ok) {
@@ -361,40 +365,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
           }
         }
         const bool last_next = newu ? Tn == 1 : j + 2 == T;  // tile g+1 ends its unit
-        if (nxt) {
-          // S(g+1): its K, its Q (a new unit's), and its S buffer, which dQ(g-1) read
-          if (!mbar_wait(&bar[Q_KFULL0 + (g + 1) % 3], ((g + 1) / 3) & 1, w)) break;
-          if (newu && !mbar_wait(&bar[Q_QFULL], (uc + 1) & 1, w)) break;
-          if (g >= 1 && !mbar_wait(&bar[Q_DQDONE], (g - 1) & 1, w)) break;
+        // S(g+1) and dP(g+1): dP first, as it waits only for both halves to have loaded dP(g)
+        // (at the start of their elementwise stage) and for V(g+1); then S once K(g+1) has
+        // landed (its S buffer held the dS(g-1) that dQ(g-1) read, and MMAs issued by one
+        // thread execute in issue order)
+        auto lookahead = [&]() -> bool {
+          if (newu && !mbar_wait(&bar[Q_QFULL], (uc + 1) & 1, w)) return false;
+          if (!mbar_wait(&bar[Q_DPFREE], g & 1, w) ||
+              !mbar_wait(&bar[Q_VFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w))
+            return false;
+          tc_fence_after();
+          issue_dp(g + 1, last_next);
+          if (!mbar_wait(&bar[Q_KFULL0 + (g + 1) % 3], ((g + 1) / 3) & 1, w)) return false;
           tc_fence_after();
           issue_s(g + 1);
-          // dP(g+1) once both halves have loaded dP(g) and V(g+1) has landed
-          if (!mbar_wait(&bar[Q_DPFREE], g & 1, w) || !mbar_wait(&bar[Q_VFULL], (g + 1) & 1, w)) break;
-          tc_fence_after();
-          issue_dp();
           if (last_next) mma_commit(&bar[Q_QEMPTY]);
-        }
-        const uint32_t aK = smem_u32(sK0 + (g % 3) * kTile);
-        const uint32_t tsb = (g & 1) ? tS1 : tS0;
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&bar[Q_PFULL00 + 2 * hh + (g & 1)], (g >> 1) & 1, w)) { ok = false; break; }
-          // the unit's first dQ MMA overwrites the accumulator: the previous unit's must be out
-          if (j == 0 && hh == 0 && uc >= 1 && !mbar_wait(&bar[Q_ACCFREE], (uc - 1) & 1, w)) { ok = false; break; }
-          tc_fence_after();
+          return true;
+        };
+        const bool unit_end = j == T - 1;
+        if (nxt && !unit_end && !lookahead()) break;
+        // dQ(g) once both halves have written dS(g); the unit's first dQ MMA overwrites the
+        // accumulator, so the previous unit's must be out
+        if (!mbar_wait(&bar[Q_PFULL00 + (g & 1)], (g >> 1) & 1, w) ||
+            !mbar_wait(&bar[Q_PFULL10 + (g & 1)], (g >> 1) & 1, w) ||
+            (j == 0 && uc >= 1 && !mbar_wait(&bar[Q_ACCFREE], (uc - 1) & 1, w)))
+          break;
+        tc_fence_after();
+        {
+          const uint32_t aK = smem_u32(sK0 + (g % 3) * kTile);
+          const uint32_t tsb = (g & 1) ? tS1 : tS0;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tQ, tsb + hh * 64 + kk * 8, sdesc_sw128(aK + (4 * hh + kk) * 2048, 16384, 1024),
-                   kIdQ, (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
+          for (int k = 0; k < 8; ++k)
+            mma_ts(tQ, tsb + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aK + k * 2048, 16384, 1024),
+                   kIdQ, (j > 0 || k > 0) ? 1u : 0u);
         }
-        if (!ok) break;
         mma_commit(&bar[Q_DQDONE]);
-        if (j == T - 1) {
+        if (unit_end) {
           mma_commit(&bar[Q_ACCFULL]);
           // with d = 128 the epilogue stages in this K stage and hands it back itself
           if (!L::kStageInK) mma_commit(&bar[Q_KEMPTY0 + g % 3]);
         } else {
           mma_commit(&bar[Q_KEMPTY0 + g % 3]);
         }
+        // the next unit's first score MMAs only once the unit's accumulator is complete
+        if (nxt && unit_end && !lookahead()) break;
         if (!nxt) break;
         ++g;
         if (newu) {
@@ -415,10 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
-    const int hr = row & 63;  // this thread's share of the half's key tracks
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.sl2;
-    int uc = 0, g = 0, n_partial = 0, rc = 0;  // rc: this half's epilogue rounds
+    int uc = 0, g = 0;
     bool ok = true;
     while (ok) {
       const int slot = uc % kQueue;
@@ -438,25 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
         uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
         if (partial) {
-          // the half's 64 keys' tracks, two per thread, in one of two buffers
-          const int b = n_partial & 1;
-          const uint32_t par = (n_partial >> 1) & 1;
-          ++n_partial;
-          int32_t* kt = ktr + (half * 2 + b) * 256;
-          const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + half * 64 + hr;
-          const int tr0 = (row >> 6) * 2;  // tracks tr0, tr0 + 1
-          kt[tr0 * 64 + hr] = p.tracks[tr0 * n + t];
-          kt[(tr0 + 1) * 64 + hr] = p.tracks[(tr0 + 1) * n + t];
-          mbar_arrive(&bar[Q_TRK00 + half * 2 + b]);
-          if (!wait_all(&bar[Q_TRK00 + half * 2 + b], par, w)) { ok = false; break; }
+          // the half's 64 keys' tracks, read straight from global memory: every lane reads the
+          // same addresses (broadcast), four keys per load
+          const int32_t* kt = p.tracks + (int64_t)p.step_col[e0 + j] * 128 + half * 64;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t bits = 0;
 #pragma unroll
-            for (int t2 = 0; t2 < 32; ++t2) {
+            for (int t2 = 0; t2 < 32; t2 += 4) {
               const int kc = cc * 32 + t2;
-              bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[64 + kc], kt[128 + kc],
-                                  kt[192 + kc], p.W) ? 1u : 0u) << t2;
+              const int4 s4 = __ldg(reinterpret_cast<const int4*>(kt + kc));
+              const int4 g4 = __ldg(reinterpret_cast<const int4*>(kt + n + kc));
+              const int4 z4 = __ldg(reinterpret_cast<const int4*>(kt + 2 * n + kc));
+              const int4 p4 = __ldg(reinterpret_cast<const int4*>(kt + 3 * n + kc));
+              bits |= (mask_legal(sq, gq, zq, pq, s4.x, g4.x, z4.x, p4.x, p.W) ? 1u : 0u) << t2;
+              bits |= (mask_legal(sq, gq, zq, pq, s4.y, g4.y, z4.y, p4.y, p.W) ? 1u : 0u) << (t2 + 1);
+              bits |= (mask_legal(sq, gq, zq, pq, s4.z, g4.z, z4.z, p4.z, p.W) ? 1u : 0u) << (t2 + 2);
+              bits |= (mask_legal(sq, gq, zq, pq, s4.w, g4.w, z4.w, p4.w, p.W) ? 1u : 0u) << (t2 + 3);
             }
             lm[cc] = bits;
           }
@@ -495,42 +506,48 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
         mbar_arrive(&bar[Q_PFULL00 + 2 * half + (g & 1)]);
       }
       if (!ok) break;
-      // ---- the unit's dQ: dq_acc += scale * dQ through staged boxes and TMA reduce-adds.
-      // Every thread waits on each unit's phase in order, so no wait runs two phases ahead.
+      // ---- the unit's dQ: dq_acc += scale * dQ through staged boxes and TMA reduce-adds, in
+      // one round (this half's D/64 boxes of 32 columns).  Every thread waits on each unit's
+      // phase in order, so no wait runs two phases ahead.
       if (!wait_all(&bar[Q_ACCFULL], uc & 1, w)) break;
       tc_fence_after();
-      uint8_t* box = (L::kStageInK ? sK0 + ((g - 1) % 3) * kTile : smem + L::kStg) + half * 16384;
-#pragma unroll 1
-      for (int r = 0; r < kRounds; ++r, ++rc) {
-        const int c = half * kRounds + r;  // 32-column chunk of dQ
-        uint32_t x[32];
-        tmem_ld32(tQ + lb + c * 32, x);
-        tmem_ld_wait();
-        if (r == kRounds - 1) {
-          tc_fence_before();
-          mbar_arrive(&bar[Q_ACCFREE]);  // the next unit's dQ MMAs may overwrite TMEM
-        }
-        // the box is free once this half's previous round has been read by its TMA
-        if (rc > 0 && !wait_all(&bar[Q_STGR0 + half], (rc - 1) & 1, w)) { ok = false; break; }
-        float v[32];
+      const int gl = g - 1;  // the unit's last tile
+      uint8_t* box = L::kStageInK
+                         ? (half == 0 ? sK0 + (gl % 3) * kTile : sV0 + (gl & 1) * kTile)
+                         : smem + L::kStg + half * 16384;
+      {
+        constexpr int kB = D / 64;
+        uint32_t x[kB][32];
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(x[t]);
+        for (int cb = 0; cb < kB; ++cb) tmem_ld32(tQ + lb + (half * kB + cb) * 32, x[cb]);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bar[Q_ACCFREE]);  // the next unit's dQ MMAs may overwrite TMEM
         fence_proxy_async_smem();
-        stage_row32(box, row, v);
+#pragma unroll
+        for (int cb = 0; cb < kB; ++cb) {
+          float v[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(x[cb][t]);
+          stage_row32(box + cb * 16384, row, v);
+        }
         fence_proxy_async_smem();
         mbar_arrive(&bar[Q_STG0 + half]);
+        // one thread per half issues the reduce-adds and waits until they have read the boxes
+        // (the rest of its warp waits for it before the next warp-wide step); with d = 128 the
+        // second half to finish hands the K and V stages back to the producer
         if (row == 0) {
-          if (mbar_wait(&bar[Q_STG0 + half], rc & 1, w)) {
-            tma_reduce_add_3d(&p.dq_map, box, c * 32, (int)(nq * 128), h);
+          if (mbar_wait(&bar[Q_STG0 + half], uc & 1, w)) {
+#pragma unroll
+            for (int cb = 0; cb < kB; ++cb)
+              tma_reduce_add_3d(&p.dq_map, box + cb * 16384, (half * kB + cb) * 32, (int)(nq * 128), h);
             bulk_commit();
             bulk_wait_read_all();
           }
-          mbar_arrive(&bar[Q_STGR0 + half]);
-          // with d = 128 the boxes sit in the last tile's K stage: the second half to finish
-          // hands it back to the producer
-          if (L::kStageInK && r == kRounds - 1 && atomicAdd(&epi_count, 1) == 1) {
+          if (L::kStageInK && atomicAdd(&epi_count, 1) == 1) {
             epi_count = 0;
-            mbar_arrive(&bar[Q_KEMPTY0 + (g - 1) % 3]);
+            mbar_arrive(&bar[Q_KEMPTY0 + gl % 3]);
+            mbar_arrive(&bar[Q_VEMPTY0 + (gl & 1)]);
           }
         }
       }
@@ -721,10 +738,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             itn = queue.T[slot] * p.group;
           }
         }
-        if (nxt) {
-          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) break;
-          if (newu && !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w)) break;
-        }
         const uint32_t aQ = smem_u32(sQ0 + (g & 1) * 2 * kTile), aDO = aQ + kTile;
         for (int hh = 0; hh < 2; ++hh) {
           if (!mbar_wait(&bar[K_PFULL0 + hh], g & 1, w)) { ok = false; break; }
@@ -749,13 +762,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             else
               mma_commit(&bar[K_QEMPTY0 + (g & 1)]);
           }
-          if (nxt) {
-            // half hh of the S^T / dP^T buffer is free once these MMAs have read P^T / dS^T
-            if (!mbar_wait(&bar[K_CONS0 + hh], g & 1, w)) { ok = false; break; }
+          if (nxt && !newu) {
+            // the next item's Q / dO are needed from here on only
+            if (hh == 0 && !mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) {
+              ok = false;
+              break;
+            }
+            // S^T_hh(g+1) / dP^T_hh(g+1) overwrite the P^T / dS^T these MMAs read: MMAs issued
+            // by one thread execute in issue order, so no wait is needed in between
             tc_fence_after();
             issue_s(g + 1, hh);
-            if (hh == 1 && (newu ? itn == 1 : j + 2 == items)) mma_commit(&bar[K_KVEMPTY]);
+            if (hh == 1 && j + 2 == items) mma_commit(&bar[K_KVEMPTY]);
           }
+        }
+        // the next unit's first score MMAs once this unit's accumulators are complete: they
+        // wait for the new unit's K / V and first Q / dO
+        if (ok && nxt && newu) {
+          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w) ||
+              !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w))
+            break;
+          tc_fence_after();
+          issue_s(g + 1, 0);
+          issue_s(g + 1, 1);
+          if (itn == 1) mma_commit(&bar[K_KVEMPTY]);
         }
         if (!ok || !nxt) break;
         ++g;
@@ -992,6 +1021,14 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int P = pl->P;
+  // The dQ launches (one accumulator) stay in order on `s`; the dK/dV launches (the other
+  // accumulators) run in order on a side stream, so that the two kernels' tails overlap.
+  cudaStream_t s2 = side_stream();
+  if (!s2) s2 = s;
+  if (s2 != s) {
+    cudaError_t e = stream_fork(s, s2);
+    if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+  }
   for (int i = 0; i < n_steps; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
@@ -1021,9 +1058,13 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       }
       if (pk.nwork > 0) {
         pk.sched = sched_slot(pl);
-        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s>>>(pk);
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s2>>>(pk);
       }
     }
+  }
+  if (s2 != s) {
+    cudaError_t e = stream_fork(s2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "join of the backward streams");
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");

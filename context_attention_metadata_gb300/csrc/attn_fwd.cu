@@ -716,6 +716,15 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // Steps of different q shards touch disjoint rows of the state: those of odd q shards run on
+  // a side stream, so that consecutive launches' tails overlap.  Steps of one q shard stay in
+  // order on one stream.
+  cudaStream_t s2 = n_steps > 1 ? side_stream() : nullptr;
+  if (!s2) s2 = s;
+  if (s2 != s) {
+    cudaError_t e = stream_fork(s, s2);
+    if (e != cudaSuccess) return cuda_fail(e, "fork of the forward streams");
+  }
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;
     prm.q_shard = q_shards[i];
@@ -730,7 +739,11 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     // initialises the units without tiles, spread over the whole grid
     const int want = prm.first ? base.units : prm.nwork;
     const unsigned grid = (unsigned)(want < sms ? want : sms);
-    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), s>>>(prm);
+    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), (prm.q_shard & 1) ? s2 : s>>>(prm);
+  }
+  if (s2 != s) {
+    cudaError_t e = stream_fork(s2, s);
+    if (e != cudaSuccess) return cuda_fail(e, "join of the forward streams");
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch k_attn_fwd");

@@ -111,4 +111,9 @@ marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, co
 // true the first time it is called for (key, current device); used for per-device set-up
 bool once_per_device(int key);
 
+// a second stream of the current device (nullptr if it cannot be created), and an ordering
+// edge from everything queued on `from` so far to everything queued on `to` afterwards
+cudaStream_t side_stream();
+cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);
+
 }  // namespace marble
