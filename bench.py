@@ -25,6 +25,11 @@ import sys
 import threading
 import time
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel on
+# the 64K packed workload, from one ncu capture of the kernels as they are now (the capture's
+# command is recorded beside its summary); None where the kernel changed since its capture
+KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 304.7e6, "k_bwd_dq": 199.4e6, "k_attn_fwd": 148.2e6}
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -264,6 +269,8 @@ def run_marble(args, rank, world, local, dist):
     if dist is not None:
         dist.barrier()
     marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    M.timing_read()  # drop anything recorded before the timed region
+    M.timing_enable(True)
     with ClockSampler(torch.cuda.current_device()) as clk:
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
@@ -271,6 +278,8 @@ def run_marble(args, rank, world, local, dist):
             step(marks[i])
         torch.cuda.synchronize()
         t_wall = time.perf_counter() - t_wall
+    M.timing_enable(False)
+    ktime = M.timing_read()  # per-kernel device time, CUDA events on each kernel's stream
     if dist is not None:
         dist.barrier()
     pl.check()
@@ -283,19 +292,28 @@ def run_marble(args, rank, world, local, dist):
     ms_per_step = 1e3 * dev_s / args.steps
 
     peak, peak_sus, hbm, peak_kind = _peaks()
-    fwd_launches, bwd_launches = len(sched), 2 * len(sched)
     mf, mb = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    # dominant phase: report its own kernel's algorithmic FLOPs per launch / launch time
-    if mb >= mf:
-        dom = {"kernel": "k_bwd_dq + k_bwd_dkdv (one backward ring step)",
-               "flops_per_launch": flops_bwd / len(sched), "ms_per_launch": mb / len(sched)}
-    else:
-        dom = {"kernel": "k_attn_fwd (one forward ring step)",
-               "flops_per_launch": flops_fwd / len(sched), "ms_per_launch": mf / len(sched)}
-    ach = dom["flops_per_launch"] / (dom["ms_per_launch"] / 1e3) / 1e12
+    # roofline of the dominant kernel: its algorithmic FLOPs (forward: S and PV; dK/dV
+    # kernel: S, dP, dV, dK; dQ kernel: dQ -- its S and dP are recomputed, not algorithmic)
+    # over its own summed device time, per launch
+    kern = {
+        "k_attn_fwd": (flops_fwd, ktime["fwd_ms"], ktime["fwd_launches"]),
+        "k_bwd_dkdv": (0.8 * flops_bwd, ktime["dkdv_ms"], ktime["dkdv_launches"]),
+        "k_bwd_dq": (0.2 * flops_bwd, ktime["dq_ms"], ktime["dq_launches"]),
+    }
+    dom_name = max(kern, key=lambda k_: kern[k_][1])
+    f_step, k_ms, k_launches = kern[dom_name]
+    ms_per_launch = k_ms / max(k_launches, 1)
+    flops_per_launch = f_step * args.steps / max(k_launches, 1)
+    ach = flops_per_launch / (ms_per_launch / 1e3) / 1e12
     roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-            "frac": ach / peak, "traffic": None, "kernel": dom["kernel"],
-            "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)"}
+            "frac": ach / peak, "traffic": KERNEL_DRAM_BYTES_PER_LAUNCH.get(dom_name),
+            "kernel": dom_name, "launches": k_launches, "ms_per_launch": ms_per_launch,
+            "flops_per_launch": flops_per_launch,
+            "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
+            "kernel_ms": {k_: round(v_[1] / args.steps, 3) for k_, v_ in kern.items()},
+            "kernel_tflops": {k_: (v_[0] * args.steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
+                              for k_, v_ in kern.items()}}
 
     # end to end through the public API: H2D of the step's inputs from pinned memory,
     # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results
@@ -374,10 +392,43 @@ def run_marble(args, rank, world, local, dist):
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * (fwd_launches + 2 + bwd_launches),
+            # our kernels in the timed region: attention launches counted by the library,
+            # plus finalize and bwd_prep once per step
+            "gpu_launches": ktime["fwd_launches"] + ktime["dq_launches"] +
+                            ktime["dkdv_launches"] + 2 * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
+
+
+def run_profile_pass(args):
+    """Driver for ncu captures: plan + `--profile-pass` forward+backward passes of the
+    workload (optionally a smaller pack of the same recipe, `--tokens`), untimed, no JSON."""
+    import numpy as np
+    import torch
+    import context_attention_metadata_gb300 as M
+    import workloads as wl
+    cid = args.config
+    cfg = wl.CONFIGS[cid] if args.tokens <= 0 else wl.mini_config(cid, args.tokens, hq=wl.CONFIGS[cid].hq)
+    tr = wl.config_tracks(cid) if args.tokens <= 0 else wl.config_tracks(cid, cfg.n)
+    trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens)
+    n, hq, hkv, d = cfg.n, cfg.hq, cfg.hkv, cfg.d
+    q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda")
+    qp, kp, vp, dop = (pl.permute(t) for t in (q, k, v, do))
+    st = M.State(n, hq, d)
+    o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dq = torch.zeros((n, hq, d), dtype=torch.float32, device="cuda")
+    dk = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    dv = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    for _ in range(args.profile_pass):
+        M.forward(pl, qp, kp, vp, st, o, lse, needed=cfg.needed)
+        M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=cfg.needed)
+    pl.check()
+    torch.cuda.synchronize()
+    print(f"profile pass ok: {cfg.name} n={n} passes={args.profile_pass}", flush=True)
 
 
 def main():
@@ -392,7 +443,14 @@ def main():
                     help="seconds of oracle time for cpu_baseline (0 disables)")
     ap.add_argument("--ref-budget", type=float, default=5.0,
                     help="seconds of oracle time per reference-arm step")
+    ap.add_argument("--profile-pass", type=int, default=0,
+                    help="run this many untimed fwd+bwd passes for a profiler and exit")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="with --profile-pass: a smaller pack of the same recipe")
     args = ap.parse_args()
+    if args.profile_pass > 0:
+        run_profile_pass(args)
+        return
     rank, world, local, dist = _dist()
     if args.impl == "reference":
         run_reference(args, rank, world, dist)

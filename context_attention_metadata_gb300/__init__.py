@@ -98,6 +98,8 @@ _SIGS = {
     "marble_check": ([ctypes.c_void_p, ctypes.c_void_p]),
     "marble_set_wait_limit_ns": ([ctypes.c_uint64]),
     "marble_debug_wait_timeout": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
+    "marble_timing_enable": ([ctypes.c_int]),
+    "marble_timing_read": ([ctypes.c_void_p]),
     "marble_tile_map_static": ([ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
                                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
@@ -301,6 +303,19 @@ def cast_bf16(src, dst, stream=None):
 
 def set_wait_limit_ns(ns: int):
     _call("marble_set_wait_limit_ns", int(ns))
+
+
+def timing_enable(on: bool = True):
+    """Per-kernel device timing of later attention calls (CUDA events on each kernel's stream)."""
+    _call("marble_timing_enable", 1 if on else 0)
+
+
+def timing_read() -> dict:
+    """Summed device ms and launch counts per kernel since the previous read."""
+    buf = (ctypes.c_double * 6)()
+    _call("marble_timing_read", ctypes.cast(buf, ctypes.c_void_p))
+    return {"fwd_ms": buf[0], "fwd_launches": int(buf[1]), "dq_ms": buf[2],
+            "dq_launches": int(buf[3]), "dkdv_ms": buf[4], "dkdv_launches": int(buf[5])}
 
 
 def debug_wait_timeout(plan: Plan, limit_ns: int, stream=None):

@@ -70,6 +70,49 @@ cudaStream_t side_stream() {
   return st;
 }
 
+namespace {
+struct TimingSpan {
+  cudaEvent_t a = nullptr, b = nullptr;
+  int kind = 0, launches = 0;
+};
+std::mutex g_timing_mu;
+bool g_timing = false;
+std::vector<TimingSpan> g_spans;
+}  // namespace
+
+bool timing_on() {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  return g_timing;
+}
+
+int timing_begin(cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (!g_timing) return -1;
+  TimingSpan t;
+  if (cudaEventCreate(&t.a) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  cudaEventRecord(t.a, s);
+  g_spans.push_back(t);
+  return (int)g_spans.size() - 1;
+}
+
+void timing_end(int span, cudaStream_t s, int kind, int launches) {
+  if (span < 0) return;
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  if (span >= (int)g_spans.size()) return;
+  TimingSpan& t = g_spans[span];
+  if (cudaEventCreate(&t.b) != cudaSuccess) {
+    (void)cudaGetLastError();
+    t.b = nullptr;
+    return;
+  }
+  cudaEventRecord(t.b, s);
+  t.kind = kind;
+  t.launches = launches;
+}
+
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
   cudaEvent_t e;
   cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -454,6 +497,37 @@ MARBLE_API marble_status_t marble_check(const marble_plan_t* p, marble_stream_t 
 MARBLE_API marble_status_t marble_set_wait_limit_ns(uint64_t ns) {
   if (ns == 0) return fail(MARBLE_ERR_INVALID_ARG, "limit must be > 0");
   g_wait_limit_ns = ns;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_timing_enable(int on) {
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  g_timing = on != 0;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_timing_read(double* out) {
+  if (!out) return fail(MARBLE_ERR_INVALID_ARG, "out is null");
+  std::lock_guard<std::mutex> lock(g_timing_mu);
+  for (int i = 0; i < 6; ++i) out[i] = 0.0;
+  cudaError_t err = cudaSuccess;
+  for (TimingSpan& t : g_spans) {
+    if (t.b) {
+      float ms = 0.f;
+      cudaError_t e = cudaEventSynchronize(t.b);
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.a, t.b);
+      if (e == cudaSuccess && t.kind >= 0 && t.kind < 3) {
+        out[2 * t.kind] += ms;
+        out[2 * t.kind + 1] += t.launches;
+      } else if (e != cudaSuccess) {
+        err = e;
+      }
+      cudaEventDestroy(t.b);
+    }
+    if (t.a) cudaEventDestroy(t.a);
+  }
+  g_spans.clear();
+  if (err != cudaSuccess) return cuda_fail(err, "marble_timing_read");
   return MARBLE_OK;
 }
 

@@ -1029,6 +1029,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     cudaError_t e = stream_fork(s, s2);
     if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
   }
+  const int span_q = timing_begin(s), span_k = timing_begin(s2);
+  int launches_q = 0, launches_k = 0;
   for (int i = 0; i < n_steps; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
@@ -1041,6 +1043,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       if (pq.nwork > 0) {
         pq.sched = sched_slot(pl);
         k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kThreads, smem_q, s>>>(pq);
+        ++launches_q;
       }
     }
     // dK/dV: the kv blocks of the kv shard listed for the q shard (longest list first), or
@@ -1059,9 +1062,12 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       if (pk.nwork > 0) {
         pk.sched = sched_slot(pl);
         k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s2>>>(pk);
+        ++launches_k;
       }
     }
   }
+  timing_end(span_q, s, kTimeDq, launches_q);
+  timing_end(span_k, s2, kTimeDkdv, launches_k);
   if (s2 != s) {
     cudaError_t e = stream_fork(s2, s);
     if (e != cudaSuccess) return cuda_fail(e, "join of the backward streams");

@@ -725,6 +725,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     cudaError_t e = stream_fork(s, s2);
     if (e != cudaSuccess) return cuda_fail(e, "fork of the forward streams");
   }
+  const int span_s = timing_begin(s), span_s2 = s2 != s ? timing_begin(s2) : -1;
+  int launches_s = 0, launches_s2 = 0;
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;
     prm.q_shard = q_shards[i];
@@ -739,8 +741,12 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     // initialises the units without tiles, spread over the whole grid
     const int want = prm.first ? base.units : prm.nwork;
     const unsigned grid = (unsigned)(want < sms ? want : sms);
-    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), (prm.q_shard & 1) ? s2 : s>>>(prm);
+    const bool side = (prm.q_shard & 1) && s2 != s;
+    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), side ? s2 : s>>>(prm);
+    ++(side ? launches_s2 : launches_s);
   }
+  timing_end(span_s, s, kTimeFwd, launches_s);
+  timing_end(span_s2, s2, kTimeFwd, launches_s2);
   if (s2 != s) {
     cudaError_t e = stream_fork(s2, s);
     if (e != cudaSuccess) return cuda_fail(e, "join of the forward streams");

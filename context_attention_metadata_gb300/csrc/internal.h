@@ -116,4 +116,11 @@ bool once_per_device(int key);
 cudaStream_t side_stream();
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);
 
+// per-kernel timing (marble_timing_enable): kinds of kernels, and a span of launches of one
+// kind on one stream, opened before the first launch and closed after the last
+enum TimingKind { kTimeFwd = 0, kTimeDq = 1, kTimeDkdv = 2 };
+bool timing_on();
+int timing_begin(cudaStream_t s);  // -1 when timing is off
+void timing_end(int span, cudaStream_t s, int kind, int launches);
+
 }  // namespace marble

@@ -302,6 +302,19 @@ marble_status_t marble_check(const marble_plan_t *plan, marble_stream_t stream);
  * process (default 2e9 ns; also read once from env MARBLE_WAIT_LIMIT_MS). */
 marble_status_t marble_set_wait_limit_ns(uint64_t ns);
 
+/*
+ * Per-kernel device timing, a measurement hook (off by default).  While it is on, every
+ * marble_attn_step(s) / marble_attn_bwd(_steps) call records CUDA events, on the stream each
+ * kernel runs on, before its first and after its last launch of that kernel, and counts the
+ * launches.  marble_timing_read synchronises on those events, adds up their spans since the
+ * previous read and writes out[0..5] = forward ms, forward launches, dQ-kernel ms, dQ-kernel
+ * launches, dK/dV-kernel ms, dK/dV-kernel launches.  The launches of one kernel on one stream
+ * run back to back, so a span is the sum of their durations; different kernels may overlap
+ * in time (they run on two streams).  Returns MARBLE_ERR_INVALID_ARG if `out` is null.
+ */
+marble_status_t marble_timing_enable(int on);
+marble_status_t marble_timing_read(double *out);
+
 /* Test hook: launch one CTA that waits, with the normal bounded wait, on a barrier that
  * nothing completes; it gives up after `limit_ns` and sets the plan's error word, so a
  * following marble_check returns MARBLE_ERR_TIMEOUT.  Nothing faults or hangs. */
