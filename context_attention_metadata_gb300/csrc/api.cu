@@ -223,6 +223,7 @@ MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
   if (!p) return MARBLE_OK;
   cudaDeviceSynchronize();
   for (void* q : p->owned) cudaFree(q);
+  if (p->ds_scratch) cudaFree(p->ds_scratch);
   delete p;
   return MARBLE_OK;
 }

@@ -10,12 +10,13 @@
 //   dV += P^T dO,  dK += scale * dS^T Q,  dQ += scale * dS K.
 // Two kernels, so that every accumulator tile has one owner per launch and the kernels never
 // add partial tiles of the same accumulator concurrently:
-//   k_bwd_dq    Q-stationary units (q block, q head): S and dP in TMEM, dS (bf16) back into
-//               TMEM over S, dQ += dS K with K read MN-major from the K tile staged for S.
 //   k_bwd_dkdv  KV-stationary units (kv block, kv head), looping over the q heads of the
 //               group and the q blocks listed for the block: S^T = K Q^T and dP^T = V dO^T in
 //               TMEM, P^T and dS^T (bf16) back into TMEM, dV += P^T dO and dK += dS^T Q with
-//               dO and Q read MN-major.
+//               dO and Q read MN-major; it also stores each bf16 dS^T tile to a scratch slot
+//               numbered by the step's tile order.
+//   k_bwd_dq    Q-stationary units (q block, q head): dQ += dS K, a GEMM over the unit's
+//               dS^T tiles (read MN-major) and K tiles, after the step's dK/dV kernel.
 // Both are persistent (one CTA per SM) and take their units from a ticket counter in the
 // plan's order (longest list first), through a 4-entry queue in shared memory:
 //   warp 10     scheduler: ticket -> unit -> queue
@@ -47,6 +48,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;
   CUtensorMap dq_map, dk_map, dv_map;  // fp32 accumulators, box 32 x 128 x 1, 128-byte swizzle
+  CUtensorMap ds_map;  // bf16 dS^T scratch tiles [slot][128 kv rows][128 q cols], box 64 x 128
   const int64_t* step_ptr;   // row lists (dQ kernel)
   const int32_t* step_col;
   const uint8_t* step_tag;
@@ -56,6 +58,9 @@ struct BwdParams {
   const int64_t* needed_ptr;
   const int32_t* needed;
   const int32_t* order;      // work order of the launch (blocks of one shard, longest first)
+  const int32_t* step_off;   // [nb][P+1] tiles of the q shard's earlier q blocks in a step
+  const int32_t* colT_j;     // [nnz] index of a column-list entry in its q block's row list
+  long long ds_slot0;        // first scratch slot of this step's dS^T tiles
   unsigned* sched;           // ticket counter pair of the launch
   const int32_t* tracks;     // [4][n] plan order
   const float* lse;          // [hq][n] natural log
@@ -156,411 +161,207 @@ __device__ __forceinline__ void release_tickets(const BwdParams& p) {
 }
 
 // ======================================================================================
-// dQ (Q-stationary)
+// dQ (Q-stationary GEMM over the dS^T tiles the dK/dV kernel wrote)
 // ======================================================================================
-// Tile g counts the tiles of all units of the CTA.  Per tile:
-//   S = Q K^T and dP = dO V^T (N = 128)  ->  elementwise, half h (kv columns [64h, 64h+64)):
-//   dS_h (bf16) over S_h  ->  dQ += dS K (dS read from the halves' packed columns).
-// S alternates between two TMEM buffers by tile and is issued for tile g+1 as soon as the dQ
-// MMAs of tile g-1 are done; dP has one buffer, rewritten once both halves have loaded it.
-// So S(g+1) and dP(g+1) run during the elementwise stage of tile g, and the elementwise warps
-// can finish tile g+1 before the MMA thread has seen tile g finished: the "dS written" barrier
-// of each half is therefore doubled by tile parity, so that no wait aliases a phase two ahead.  K streams through three
-// stages (S(g+1) is issued while K(g) still feeds dQ(g)), V through two (only dP reads it).
-// The epilogue stages the fp32 dQ tile in shared memory in one round (in the K and V stages
-// of the unit's last tile when d = 128, which the epilogue then hands back to the producer)
-// and adds it to dq_acc with TMA reduce-adds.  At a unit's last tile the MMA thread issues
-// the last dQ MMA before the next unit's score MMAs, which wait for that unit's Q and dO.
+// For a unit (q block, q head): dQ += dS K over the unit's tiles, A = dS read MN-major from
+// the step's scratch tile [kv rows][q columns], B = K read MN-major; dq_acc += scale * dQ at
+// the unit's end.  The dS^T tile and the K tile of each tile stream through three stages.
+// The accumulator alternates between two TMEM buffers by unit, so that the epilogue warps
+// read one out (and add it to dq_acc through staged boxes and TMA reduce-adds) while the
+// tensor core accumulates the next unit in the other.
 enum {
-  Q_QFULL, Q_QEMPTY, Q_KFULL0, Q_KFULL1, Q_KFULL2, Q_KEMPTY0, Q_KEMPTY1, Q_KEMPTY2, Q_VFULL0,
-  Q_VFULL1, Q_VEMPTY0, Q_VEMPTY1, Q_SFULL0, Q_SFULL1, Q_DPFULL, Q_DPFREE, Q_PFULL00, Q_PFULL01,
-  Q_PFULL10, Q_PFULL11,
-  Q_DQDONE, Q_ACCFULL,
-  Q_ACCFREE, Q_STG0, Q_STG1, Q_UFULL0,
-  Q_UEMPTY0 = Q_UFULL0 + kQueue, Q_DRAIN = Q_UEMPTY0 + kQueue, Q_NUM
+  G_FULL0, G_FULL1, G_FULL2, G_EMPTY0, G_EMPTY1, G_EMPTY2, G_OFULL0, G_OFULL1, G_OFREE0,
+  G_OFREE1, G_STG, G_STGFREE, G_UFULL0, G_UEMPTY0 = G_UFULL0 + kQueue,
+  G_DRAIN = G_UEMPTY0 + kQueue, G_NUM
 };
+constexpr int kGThreads = 224;  // producer, MMA, 4 epilogue warps, scheduler
+constexpr int kGWarpSched = 6;
 
-__host__ __device__ constexpr int dq_arrivals(int b) {
-  return (b == Q_ACCFREE || b == Q_DPFREE || (b >= Q_UEMPTY0 && b < Q_UEMPTY0 + kQueue))
-             ? 256
-             : (((b >= Q_PFULL00 && b <= Q_PFULL11) || b == Q_STG0 || b == Q_STG1) ? 128 : 1);
+__host__ __device__ constexpr int dqg_arrivals(int b) {
+  return (b == G_OFREE0 || b == G_OFREE1 || b == G_STG ||
+          (b >= G_UEMPTY0 && b < G_UEMPTY0 + kQueue))
+             ? 128
+             : 1;
 }
 
-// shared memory of the dQ kernel: Q | dO | K stages (3) | V stages (2) | (d = 64 only) a
-// staging area of two fp32 boxes.  With d = 128 this is 224 KB, so the keys' tracks of a
-// partial tile are read from global memory rather than staged.
+// shared memory of the dQ GEMM: three stages of (dS^T tile, two 16 KB boxes | K tile), then
+// a staging area of two fp32 boxes
 template <int D>
 struct DqSmem {
   static constexpr int kTile = 128 * D * 2;
-  // d = 128: half 0 stages its two 16 KB boxes in the last tile's K stage, half 1 in its V
-  // stage; d = 64: a dedicated area of two boxes
-  static constexpr bool kStageInK = D == 128;
-  static constexpr int kK = 2 * kTile;
-  static constexpr int kV = 5 * kTile;
-  static constexpr int kStg = 7 * kTile;
-  static constexpr int kEnd = kStg + (kStageInK ? 0 : 32768);
+  static constexpr int kDs = 32768;
+  static constexpr int kStage = kDs + kTile;
+  static constexpr int kStg = 3 * kStage;
+  static constexpr int kEnd = kStg + 32768;
   static constexpr size_t bytes() { return (size_t)kEnd + 1024; }
 };
 static_assert(DqSmem<128>::bytes() <= 232448 - 1024, "shared memory budget");
 
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kGThreads, 1) k_bwd_dq(const __grid_constant__ BwdParams p) {
   using L = DqSmem<D>;
   constexpr int kTile = L::kTile;
   constexpr int kAtoms = D / 64;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  uint8_t* sQ = smem;
-  uint8_t* sDO = smem + kTile;
-  uint8_t* sK0 = smem + L::kK;  // stage s at sK0 + s * kTile
-  uint8_t* sV0 = smem + L::kV;  // stage s at sV0 + s * kTile
-  __shared__ __align__(8) uint64_t bar[Q_NUM];
+  uint8_t* sStg = smem + L::kStg;
+  __shared__ __align__(8) uint64_t bar[G_NUM];
   __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
-  __shared__ int epi_count;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long n = p.n;
   WaitCtx w{p.wait_ns, p.err, &abort_flag};
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    epi_count = 0;
-    for (int b = 0; b < Q_NUM; ++b) mbar_init(&bar[b], dq_arrivals(b));
+    for (int b = 0; b < G_NUM; ++b) mbar_init(&bar[b], dqg_arrivals(b));
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, 512);
+    tmem_alloc(&tmem_base, 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // S buffers fp32 at [0,128) (even tiles) and [384,512) (odd tiles); dS_h bf16 is packed into
-  // columns [64h, 64h + 32) of its S buffer, inside the fp32 columns half h has read.
-  // dP fp32 [128,256); dQ fp32 [256, 256+D).
-  const uint32_t tS0 = tmem_base, tS1 = tmem_base + 384;
-  const uint32_t tP = tmem_base + 128;
-  const uint32_t tQ = tmem_base + 256;
+  const uint32_t tQ = tmem_base;  // dQ buffers at +0 and +128
+  const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;  // the step's list option
 
-  if (warp == kWarpSched) {
-    if (lane == 0) schedule<true>(p, queue, &bar[Q_UFULL0], &bar[Q_UEMPTY0], w);
+  if (warp == kGWarpSched) {
+    if (lane == 0) schedule<true>(p, queue, &bar[G_UFULL0], &bar[G_UEMPTY0], w);
     __syncwarp();
   } else if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&p.q_map);
+      tma_prefetch_desc(&p.ds_map);
       tma_prefetch_desc(&p.k_map);
-      tma_prefetch_desc(&p.v_map);
-      tma_prefetch_desc(&p.do_map);
     }
-    int uc = 0, g = 0, q_fills = 0, k_fills[3] = {0, 0, 0}, v_fills[2] = {0, 0};
+    int uc = 0, g = 0, fills[3] = {0, 0, 0};
     bool ok = true;
     while (ok) {
       const int slot = uc % kQueue;
-      if (!wait_all(&bar[Q_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      if (!wait_all(&bar[G_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
       const int h = queue.head[slot];
       if (h < 0) break;
       const int64_t nq = queue.blk[slot];
       const int T = queue.T[slot];
       const int64_t e0 = queue.e0[slot];
       const int kvh = h / p.group;
-      // Q and dO of the unit once the previous unit's last S / dP have read the slot
-      if (uc >= 1 && !wait_all(&bar[Q_QEMPTY], (uc - 1) & 1, w)) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar[Q_QFULL], 2 * kTile);
-        for (int a = 0; a < kAtoms; ++a) {
-          tma_load_3d(sQ + a * 16384, &p.q_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
-          tma_load_3d(sDO + a * 16384, &p.do_map, &bar[Q_QFULL], a * 64, (int)(nq * 128), h);
-        }
-      }
-      ++q_fills;
+      const int64_t base = p.step_off[nq * (p.P + 1) + opt];
       for (int j = 0; j < T; ++j, ++g) {
         const int s = g % 3;
-        const int nk = p.step_col[e0 + j];
-        if (g >= 3 && !wait_all(&bar[Q_KEMPTY0 + s], ((g / 3) - 1) & 1, w)) { ok = false; break; }
+        if (g >= 3 && !wait_all(&bar[G_EMPTY0 + s], ((g / 3) - 1) & 1, w)) { ok = false; break; }
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar[Q_KFULL0 + s], kTile);
+          const int nk = p.step_col[e0 + j];
+          const int64_t sl = p.ds_slot0 + (base + j) * p.hq + h;
+          uint8_t* st = smem + s * L::kStage;
+          mbar_arrive_expect_tx(&bar[G_FULL0 + s], L::kDs + kTile);
+          tma_load_3d(st, &p.ds_map, &bar[G_FULL0 + s], 0, (int)(sl * 128), 0);
+          tma_load_3d(st + 16384, &p.ds_map, &bar[G_FULL0 + s], 64, (int)(sl * 128), 0);
           for (int a = 0; a < kAtoms; ++a)
-            tma_load_3d(sK0 + s * kTile + a * 16384, &p.k_map, &bar[Q_KFULL0 + s], a * 64,
-                        nk * 128, kvh);
+            tma_load_3d(st + L::kDs + a * 16384, &p.k_map, &bar[G_FULL0 + s], a * 64, nk * 128,
+                        kvh);
         }
-        ++k_fills[s];
-        const int sv = g & 1;
-        if (g >= 2 && !wait_all(&bar[Q_VEMPTY0 + sv], ((g >> 1) - 1) & 1, w)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bar[Q_VFULL0 + sv], kTile);
-          for (int a = 0; a < kAtoms; ++a)
-            tma_load_3d(sV0 + sv * kTile + a * 16384, &p.v_map, &bar[Q_VFULL0 + sv], a * 64,
-                        nk * 128, kvh);
-        }
-        ++v_fills[sv];
+        ++fills[s];
       }
       ++uc;
     }
-    // no copy may still be landing in shared memory when the CTA exits: the fills of a slot
-    // complete in order, so waiting for the latest fill of each slot suffices
-    if (lane == 0) {
-      if (q_fills) drain_wait(&bar[Q_QFULL], (q_fills - 1) & 1, p.wait_ns, p.err);
+    if (lane == 0)
       for (int s = 0; s < 3; ++s)
-        if (k_fills[s]) drain_wait(&bar[Q_KFULL0 + s], (k_fills[s] - 1) & 1, p.wait_ns, p.err);
-      for (int s = 0; s < 2; ++s)
-        if (v_fills[s]) drain_wait(&bar[Q_VFULL0 + s], (v_fills[s] - 1) & 1, p.wait_ns, p.err);
-    }
+        if (fills[s]) drain_wait(&bar[G_FULL0 + s], (fills[s] - 1) & 1, p.wait_ns, p.err);
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdQ = idesc_bf16(128, D, false, true);
-      const uint32_t aQ = smem_u32(sQ), aDO = smem_u32(sDO);
-      auto issue_s = [&](int gg) {  // S(gg) into S buffer gg & 1
-        const uint32_t aK = smem_u32(sK0 + (gg % 3) * kTile);
-        const uint32_t ts = (gg & 1) ? tS1 : tS0;
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(ts, sdesc_sw128(aQ + off, 16, 1024), sdesc_sw128(aK + off, 16, 1024), kIdS,
-                 k > 0);
-        }
-        mma_commit(&bar[Q_SFULL0 + (gg & 1)]);
-      };
-      auto issue_dp = [&](int gg, bool last) {  // dP(gg), V from stage gg & 1
-        const uint32_t aV = smem_u32(sV0 + (gg & 1) * kTile);
-#pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tP, sdesc_sw128(aDO + off, 16, 1024), sdesc_sw128(aV + off, 16, 1024), kIdS,
-                 k > 0);
-        }
-        mma_commit(&bar[Q_DPFULL]);
-        // with d = 128 the epilogue stages in a unit's last V stage and hands it back itself
-        if (!(L::kStageInK && last)) mma_commit(&bar[Q_VEMPTY0 + (gg & 1)]);
-      };
-      int uc = 0, j = 0, g = 0, T = 0;
-      bool ok = mbar_wait(&bar[Q_UFULL0], 0, w) && queue.head[0] >= 0;
-      if (ok) {
-        T = queue.T[0];
-        ok = mbar_wait(&bar[Q_QFULL], 0, w) && mbar_wait(&bar[Q_KFULL0], 0, w) &&
-             mbar_wait(&bar[Q_VFULL0], 0, w);
-      }
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0, T == 1);
-        if (T == 1) mma_commit(&bar[Q_QEMPTY]);  // the unit's last read of Q and dO
-      }
+      constexpr uint32_t kId = idesc_bf16(128, D, true, true);  // A and B both MN-major
+      int uc = 0, g = 0;
+      bool ok = true;
       while (ok) {
-        // the tile after g: the next of this unit, or the first of the next unit
-        bool nxt = true, newu = false;
-        int Tn = T;
-        if (j + 1 == T) {
-          const int slot = (uc + 1) % kQueue;
-          if (!mbar_wait(&bar[Q_UFULL0 + slot], ((uc + 1) / kQueue) & 1, w)) break;
-          if (queue.head[slot] < 0) {
-            nxt = false;
-          } else {
-            newu = true;
-            Tn = queue.T[slot];
-          }
-        }
-        const bool last_next = newu ? Tn == 1 : j + 2 == T;  // tile g+1 ends its unit
-        // S(g+1) and dP(g+1): dP first, as it waits only for both halves to have loaded dP(g)
-        // (at the start of their elementwise stage) and for V(g+1); then S once K(g+1) has
-        // landed (its S buffer held the dS(g-1) that dQ(g-1) read, and MMAs issued by one
-        // thread execute in issue order)
-        auto lookahead = [&]() -> bool {
-          if (newu && !mbar_wait(&bar[Q_QFULL], (uc + 1) & 1, w)) return false;
-          if (!mbar_wait(&bar[Q_DPFREE], g & 1, w) ||
-              !mbar_wait(&bar[Q_VFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w))
-            return false;
+        const int slot = uc % kQueue;
+        if (!mbar_wait(&bar[G_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+        if (queue.head[slot] < 0) break;
+        const int T = queue.T[slot];
+        const uint32_t ob = (uint32_t)(uc & 1);
+        for (int j = 0; j < T; ++j, ++g) {
+          const int s = g % 3;
+          if (!mbar_wait(&bar[G_FULL0 + s], (g / 3) & 1, w)) { ok = false; break; }
+          // the unit's first MMA overwrites its buffer: the unit two back must be read out
+          if (j == 0 && uc >= 2 && !mbar_wait(&bar[G_OFREE0 + ob], ((uc >> 1) - 1) & 1, w)) { ok = false; break; }
           tc_fence_after();
-          issue_dp(g + 1, last_next);
-          if (!mbar_wait(&bar[Q_KFULL0 + (g + 1) % 3], ((g + 1) / 3) & 1, w)) return false;
-          tc_fence_after();
-          issue_s(g + 1);
-          if (last_next) mma_commit(&bar[Q_QEMPTY]);
-          return true;
-        };
-        const bool unit_end = j == T - 1;
-        if (nxt && !unit_end && !lookahead()) break;
-        // dQ(g) once both halves have written dS(g); the unit's first dQ MMA overwrites the
-        // accumulator, so the previous unit's must be out
-        if (!mbar_wait(&bar[Q_PFULL00 + (g & 1)], (g >> 1) & 1, w) ||
-            !mbar_wait(&bar[Q_PFULL10 + (g & 1)], (g >> 1) & 1, w) ||
-            (j == 0 && uc >= 1 && !mbar_wait(&bar[Q_ACCFREE], (uc - 1) & 1, w)))
-          break;
-        tc_fence_after();
-        {
-          const uint32_t aK = smem_u32(sK0 + (g % 3) * kTile);
-          const uint32_t tsb = (g & 1) ? tS1 : tS0;
+          const uint32_t aS = smem_u32(smem + s * L::kStage), aK = aS + L::kDs;
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            mma_ts(tQ, tsb + (k >> 2) * 64 + (k & 3) * 8, sdesc_sw128(aK + k * 2048, 16384, 1024),
-                   kIdQ, (j > 0 || k > 0) ? 1u : 0u);
+            mma_ss(tQ + ob * 128, sdesc_sw128(aS + k * 2048, 16384, 1024),
+                   sdesc_sw128(aK + k * 2048, 16384, 1024), kId, (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(&bar[G_EMPTY0 + s]);
+          if (j == T - 1) mma_commit(&bar[G_OFULL0 + ob]);
         }
-        mma_commit(&bar[Q_DQDONE]);
-        if (unit_end) {
-          mma_commit(&bar[Q_ACCFULL]);
-          // with d = 128 the epilogue stages in this K stage and hands it back itself
-          if (!L::kStageInK) mma_commit(&bar[Q_KEMPTY0 + g % 3]);
-        } else {
-          mma_commit(&bar[Q_KEMPTY0 + g % 3]);
-        }
-        // the next unit's first score MMAs only once the unit's accumulator is complete
-        if (nxt && unit_end && !lookahead()) break;
-        if (!nxt) break;
-        ++g;
-        if (newu) {
-          ++uc;
-          j = 0;
-          T = Tn;
-        } else {
-          ++j;
-        }
+        ++uc;
       }
-      mma_commit(&bar[Q_DRAIN]);
-      drain_wait(&bar[Q_DRAIN], 0, p.wait_ns, p.err);
+      mma_commit(&bar[G_DRAIN]);
+      drain_wait(&bar[G_DRAIN], 0, p.wait_ns, p.err);
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------------ elementwise
-    // four warps per half: `half` owns kv columns [64 half, 64 half + 64), one row a thread
+    // ------------------------------------------------------------------ epilogue
+    // one thread per row (warp w owns TMEM lane quarter w & 3)
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
-    const float sl2 = p.sl2;
-    int uc = 0, g = 0;
+    int uc = 0, k = 0;  // units, staging rounds
     bool ok = true;
     while (ok) {
       const int slot = uc % kQueue;
-      if (!wait_all(&bar[Q_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
+      if (!wait_all(&bar[G_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
       const int h = queue.head[slot];
       if (h < 0) break;
       const int64_t nq = queue.blk[slot];
-      const int T = queue.T[slot];
-      const int64_t e0 = queue.e0[slot];
-      const int64_t tq = nq * 128 + row;
-      const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
-                pq = p.tracks[3 * n + tq];
-      float lse2 = p.lse[(int64_t)h * n + tq] * kLog2e;
-      if (lse2 == -INFINITY) lse2 = INFINITY;  // a row with no legal key: every P is 0
-      const float dlt = p.delta[(int64_t)h * n + tq];
-      for (int j = 0; j < T; ++j, ++g) {
-        const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
-        uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
-        if (partial) {
-          // the half's 64 keys' tracks, read straight from global memory: every lane reads the
-          // same addresses (broadcast), four keys per load
-          const int32_t* kt = p.tracks + (int64_t)p.step_col[e0 + j] * 128 + half * 64;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t bits = 0;
-#pragma unroll
-            for (int t2 = 0; t2 < 32; t2 += 4) {
-              const int kc = cc * 32 + t2;
-              const int4 s4 = __ldg(reinterpret_cast<const int4*>(kt + kc));
-              const int4 g4 = __ldg(reinterpret_cast<const int4*>(kt + n + kc));
-              const int4 z4 = __ldg(reinterpret_cast<const int4*>(kt + 2 * n + kc));
-              const int4 p4 = __ldg(reinterpret_cast<const int4*>(kt + 3 * n + kc));
-              bits |= (mask_legal(sq, gq, zq, pq, s4.x, g4.x, z4.x, p4.x, p.W) ? 1u : 0u) << t2;
-              bits |= (mask_legal(sq, gq, zq, pq, s4.y, g4.y, z4.y, p4.y, p.W) ? 1u : 0u) << (t2 + 1);
-              bits |= (mask_legal(sq, gq, zq, pq, s4.z, g4.z, z4.z, p4.z, p.W) ? 1u : 0u) << (t2 + 2);
-              bits |= (mask_legal(sq, gq, zq, pq, s4.w, g4.w, z4.w, p4.w, p.W) ? 1u : 0u) << (t2 + 3);
-            }
-            lm[cc] = bits;
-          }
-        }
-        // S(g) has one barrier per buffer, so a wait never runs two phases behind S(g+1)
-        if (!wait_all(&bar[Q_SFULL0 + (g & 1)], (g >> 1) & 1, w)) { ok = false; break; }
-        if (!wait_all(&bar[Q_DPFULL], g & 1, w)) { ok = false; break; }
-        // S of the unit's first tile is issued: every role has read the queue entry
-        if (j == 0) mbar_arrive(&bar[Q_UEMPTY0 + slot]);
-        tc_fence_after();
-        const uint32_t ts = ((g & 1) ? tS1 : tS0) + half * 64;
-        uint32_t vs[2][32], vp[2][32];
-        tmem_ld32(ts + lb, vs[0]);
-        tmem_ld32(ts + lb + 32, vs[1]);
-        tmem_ld32(tP + lb + half * 64, vp[0]);
-        tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[Q_DPFREE]);  // dP(g+1) may now overwrite dP(g)
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int t = 0; t < 32; t += 2) {
-            const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
-            const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2) : 0.f;
-            const float p1 = l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2) : 0.f;
-            const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dlt);
-            const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dlt);
-            pk[t >> 1] = pack_bf16(d0, d1);
-          }
-          tmem_st16(ts + lb + cc * 16, pk);
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[Q_PFULL00 + 2 * half + (g & 1)]);
-      }
-      if (!ok) break;
-      // ---- the unit's dQ: dq_acc += scale * dQ through staged boxes and TMA reduce-adds, in
-      // one round (this half's D/64 boxes of 32 columns).  Every thread waits on each unit's
-      // phase in order, so no wait runs two phases ahead.
-      if (!wait_all(&bar[Q_ACCFULL], uc & 1, w)) break;
+      const uint32_t ob = (uint32_t)(uc & 1);
+      if (!wait_all(&bar[G_OFULL0 + ob], (uc >> 1) & 1, w)) break;
       tc_fence_after();
-      const int gl = g - 1;  // the unit's last tile
-      uint8_t* box = L::kStageInK
-                         ? (half == 0 ? sK0 + (gl % 3) * kTile : sV0 + (gl & 1) * kTile)
-                         : smem + L::kStg + half * 16384;
-      {
-        constexpr int kB = D / 64;
-        uint32_t x[kB][32];
-#pragma unroll
-        for (int cb = 0; cb < kB; ++cb) tmem_ld32(tQ + lb + (half * kB + cb) * 32, x[cb]);
+      // the unit's last MMA is done: the producer and the MMA thread are past its entry
+      mbar_arrive(&bar[G_UEMPTY0 + slot]);
+      // dq_acc += scale * dQ, 64 columns (two staged 128 x 32 boxes) per round
+#pragma unroll 1
+      for (int r = 0; r < D / 64; ++r, ++k) {
+        uint32_t x[2][32];
+        tmem_ld32(tQ + ob * 128 + lb + (2 * r) * 32, x[0]);
+        tmem_ld32(tQ + ob * 128 + lb + (2 * r + 1) * 32, x[1]);
         tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&bar[Q_ACCFREE]);  // the next unit's dQ MMAs may overwrite TMEM
+        if (r == D / 64 - 1) {
+          tc_fence_before();
+          mbar_arrive(&bar[G_OFREE0 + ob]);  // the buffer can take unit uc + 2
+        }
+        if (k > 0 && !wait_all(&bar[G_STGFREE], (k - 1) & 1, w)) { ok = false; break; }
         fence_proxy_async_smem();
 #pragma unroll
-        for (int cb = 0; cb < kB; ++cb) {
+        for (int cb = 0; cb < 2; ++cb) {
           float v[32];
 #pragma unroll
           for (int t = 0; t < 32; ++t) v[t] = p.scale * __uint_as_float(x[cb][t]);
-          stage_row32(box + cb * 16384, row, v);
+          stage_row32(sStg + cb * 16384, row, v);
         }
         fence_proxy_async_smem();
-        mbar_arrive(&bar[Q_STG0 + half]);
-        // one thread per half issues the reduce-adds and waits until they have read the boxes
-        // (the rest of its warp waits for it before the next warp-wide step); with d = 128 the
-        // second half to finish hands the K and V stages back to the producer
+        mbar_arrive(&bar[G_STG]);
         if (row == 0) {
-          if (mbar_wait(&bar[Q_STG0 + half], uc & 1, w)) {
-#pragma unroll
-            for (int cb = 0; cb < kB; ++cb)
-              tma_reduce_add_3d(&p.dq_map, box + cb * 16384, (half * kB + cb) * 32, (int)(nq * 128), h);
+          if (mbar_wait(&bar[G_STG], k & 1, w)) {
+            for (int cb = 0; cb < 2; ++cb)
+              tma_reduce_add_3d(&p.dq_map, sStg + cb * 16384, (2 * r + cb) * 32, (int)(nq * 128), h);
             bulk_commit();
             bulk_wait_read_all();
           }
-          if (L::kStageInK && atomicAdd(&epi_count, 1) == 1) {
-            epi_count = 0;
-            mbar_arrive(&bar[Q_KEMPTY0 + gl % 3]);
-            mbar_arrive(&bar[Q_VEMPTY0 + (gl & 1)]);
-          }
+          mbar_arrive(&bar[G_STGFREE]);
         }
       }
       ++uc;
     }
-    // the global writes of every TMA reduce this thread issued have completed
     if (row == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
+    tmem_dealloc(tmem_base, 256);
   }
   if (threadIdx.x == 0) release_tickets(p);
 }
@@ -579,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dq(const __grid_constant__ 
 enum {
   K_KVFULL, K_KVEMPTY, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL0, K_SFULL1, K_PFULL0,
   K_PFULL1, K_CONS0, K_CONS1, K_ACCFULL, K_ACCFREE, K_STG0, K_STG1, K_STGR0, K_STGR1, K_TRK00,
-  K_TRK01, K_TRK10, K_TRK11, K_UFULL0, K_UEMPTY0 = K_UFULL0 + kQueue,
+  K_TRK01, K_TRK10, K_TRK11, K_DSSTG0, K_DSSTG1, K_DSFREE0, K_DSFREE1, K_UFULL0, K_UEMPTY0 = K_UFULL0 + kQueue,
   K_DRAIN = K_UEMPTY0 + kQueue, K_NUM
 };
 
@@ -587,7 +388,7 @@ __host__ __device__ constexpr int dkdv_arrivals(int b) {
   return (b == K_ACCFREE || (b >= K_UEMPTY0 && b < K_UEMPTY0 + kQueue))
              ? 256
              : ((b == K_PFULL0 || b == K_PFULL1 || b == K_STG0 || b == K_STG1 ||
-                 (b >= K_TRK00 && b <= K_TRK11))
+                 b == K_DSSTG0 || b == K_DSSTG1 || (b >= K_TRK00 && b <= K_TRK11))
                     ? 128
                     : 1);
 }
@@ -601,8 +402,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   uint8_t* sK = smem;
   uint8_t* sV = smem + kTile;
   uint8_t* sQ0 = smem + 2 * kTile;  // stage s: Q at 2+2s, dO at 3+2s
-  // per half and buffer: lse2[64] | delta[64] | tracks [4][64]
-  float* stg = reinterpret_cast<float*>(smem + 6 * kTile);
+  // one 16 KB box of bf16 dS^T (128 kv rows x 64 q columns) that the halves take turns in,
+  // then per half and buffer: lse2[64] | delta[64]
+  uint8_t* sDS = smem + 6 * kTile;
+  float* stg = reinterpret_cast<float*>(smem + 6 * kTile + 16384);
   __shared__ __align__(8) uint64_t bar[K_NUM];
   __shared__ Queue queue;
   __shared__ uint32_t tmem_base;
@@ -828,38 +631,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         const int64_t e = c0 + it % L;
         const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
         const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
-        // stage this half's per-query LSE (base 2), delta and, on partial tiles, tracks: the
-        // threads of rows [0, 64) the two floats, those of rows [64, 128) the four tracks
+        // stage this half's per-query LSE (base 2) and delta (threads of rows [0, 64))
         const int b = g & 1;
-        float* lse2s = stg + (half * 2 + b) * 384;
+        float* lse2s = stg + (half * 2 + b) * 128;
         float* dls = lse2s + 64;
-        int32_t* qt = reinterpret_cast<int32_t*>(lse2s + 128);
         if ((row >> 6) == 0) {
           const float l2 = p.lse[(int64_t)h * n + qrow] * kLog2e;
           lse2s[hr] = (l2 == -INFINITY) ? INFINITY : l2;
           dls[hr] = p.delta[(int64_t)h * n + qrow];
-        } else if (partial) {
-          qt[hr] = p.tracks[qrow];
-          qt[64 + hr] = p.tracks[n + qrow];
-          qt[128 + hr] = p.tracks[2 * n + qrow];
-          qt[192 + hr] = p.tracks[3 * n + qrow];
         }
         mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
-        if (!wait_all(&bar[K_TRK00 + half * 2 + b], (g >> 1) & 1, w)) { ok = false; break; }
         uint32_t lm[2] = {~0u, ~0u};
         if (partial) {
+          // the half's 64 queries' tracks, read straight from global memory (the same
+          // addresses for every lane: broadcast loads), four queries per load
+          const int32_t* qt = p.tracks + (int64_t)p.colT_row[e] * 128 + half * 64;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t bits = 0;
 #pragma unroll
-            for (int t2 = 0; t2 < 32; ++t2) {
+            for (int t2 = 0; t2 < 32; t2 += 4) {
               const int q = cc * 32 + t2;
-              bits |= (mask_legal(qt[q], qt[64 + q], qt[128 + q], qt[192 + q], sk, gk, zk, pk,
-                                  p.W) ? 1u : 0u) << t2;
+              const int4 s4 = __ldg(reinterpret_cast<const int4*>(qt + q));
+              const int4 g4 = __ldg(reinterpret_cast<const int4*>(qt + n + q));
+              const int4 z4 = __ldg(reinterpret_cast<const int4*>(qt + 2 * n + q));
+              const int4 p4 = __ldg(reinterpret_cast<const int4*>(qt + 3 * n + q));
+              bits |= (mask_legal(s4.x, g4.x, z4.x, p4.x, sk, gk, zk, pk, p.W) ? 1u : 0u) << t2;
+              bits |= (mask_legal(s4.y, g4.y, z4.y, p4.y, sk, gk, zk, pk, p.W) ? 1u : 0u) << (t2 + 1);
+              bits |= (mask_legal(s4.z, g4.z, z4.z, p4.z, sk, gk, zk, pk, p.W) ? 1u : 0u) << (t2 + 2);
+              bits |= (mask_legal(s4.w, g4.w, z4.w, p4.w, sk, gk, zk, pk, p.W) ? 1u : 0u) << (t2 + 3);
             }
             lm[cc] = bits;
           }
         }
+        if (!wait_all(&bar[K_TRK00 + half * 2 + b], (g >> 1) & 1, w)) { ok = false; break; }
         if (!wait_all(&bar[K_SFULL0 + half], g & 1, w)) { ok = false; break; }
         // S^T of the unit's first item is issued: every role has read the queue entry
         if (it == 0) mbar_arrive(&bar[K_UEMPTY0 + slot]);
@@ -870,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tmem_ld32(tP + lb + half * 64, vp[0]);
         tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
         tmem_ld_wait();
+        uint32_t dsv[32];  // this row's bf16 dS^T pairs over the half's 64 q columns
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk16[16], dk16[16];
@@ -884,6 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dls[q0 + 1]);
             pk16[t >> 1] = pack_bf16(p0, p1);
             dk16[t >> 1] = pack_bf16(d0, d1);
+            dsv[cc * 16 + (t >> 1)] = dk16[t >> 1];
           }
           tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
           tmem_st16(tP + lb + half * 64 + cc * 16, dk16);
@@ -891,6 +698,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar[K_PFULL0 + half]);
+        // ---- this half's bf16 dS^T (its 64 q columns) to the step's scratch tile, for the
+        // dQ GEMM.  The halves take turns in one box (half 0 of item g, half 1 of item g, half
+        // 0 of item g+1, ...); DSFREE_h completes one phase per store of half h once its TMA
+        // has read the box.  Before its store of item g a half waits for its own store of item
+        // g-1 and for the other half's latest store (item g-1 for half 0, item g for half 1);
+        // each of these waits is on the current or the just-completed phase of its barrier.
+        if (g >= 1 && !wait_all(&bar[K_DSFREE0 + half], (uint32_t)((g - 1) & 1), w)) { ok = false; break; }
+        if (half == 0 ? (g >= 1 && !wait_all(&bar[K_DSFREE1], (uint32_t)((g - 1) & 1), w))
+                      : !wait_all(&bar[K_DSFREE0], (uint32_t)(g & 1), w)) {
+          ok = false;
+          break;
+        }
+        fence_proxy_async_smem();
+        {
+          uint8_t* r8 = sDS + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* src = dsv + 4 * c;
+            *reinterpret_cast<uint4*>(r8 + ((c ^ (row & 7)) << 4)) =
+                make_uint4(src[0], src[1], src[2], src[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bar[K_DSSTG0 + half]);
+        if (row == 0) {
+          if (mbar_wait(&bar[K_DSSTG0 + half], g & 1, w)) {
+            const int64_t nq = p.colT_row[e];
+            const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
+            int64_t jj = p.colT_j[e];
+            if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
+            const int64_t slot_ds =
+                p.ds_slot0 + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
+            tma_store_3d(&p.ds_map, sDS, half * 64, (int)(slot_ds * 128), 0);
+            bulk_commit();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(&bar[K_DSFREE0 + half]);
+        }
       }
       if (!ok) break;
       // ---- the unit's dV and dK (dv_acc += dV, dk_acc += scale * dK): round 0 stages this
@@ -958,8 +803,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
 
 template <int D>
 size_t dkdv_smem() {
-  // K, V, two Q/dO stages (6 tiles) + per-half staging of LSE, delta and tracks
-  return 6 * (128 * D * 2) + 2 * 2 * 384 * 4 + 1024;
+  // K, V, two Q/dO stages (6 tiles) + the dS^T box + per-half staging of LSE and delta
+  return 6 * (128 * D * 2) + 16384 + 2 * 2 * 128 * 4 + 1024;
 }
 
 template <int D>
@@ -1021,31 +866,59 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int P = pl->P;
-  // The dQ launches (one accumulator) stay in order on `s`; the dK/dV launches (the other
-  // accumulators) run in order on a side stream, so that the two kernels' tails overlap.
+  prm.step_off = pl->step_off;
+  prm.colT_j = pl->colT_j;
+  // scratch for the bf16 dS^T tiles of two steps: the dQ GEMM of step i reads one half while
+  // the dK/dV kernel of step i+1 writes the other
+  int64_t max_tiles = 0;  // the largest step of this call
+  for (int i = 0; i < n_steps; ++i) {
+    const int64_t t =
+        pl->h_step_tiles[(size_t)q_shards[i] * (P + 1) + (kv_shards[i] >= 0 ? kv_shards[i] : P)];
+    max_tiles = t > max_tiles ? t : max_tiles;
+  }
+  const int64_t buf_slots = max_tiles * qkv->hq;
+  {
+    std::lock_guard<std::mutex> lock(pl->scratch_mu);
+    const size_t need = (size_t)(2 * buf_slots) * 32768;
+    if (need > pl->ds_scratch_bytes) {
+      if (pl->ds_scratch) {
+        cudaDeviceSynchronize();
+        cudaFree(pl->ds_scratch);
+        pl->ds_scratch = nullptr;
+        pl->ds_scratch_bytes = 0;
+      }
+      void* q = nullptr;
+      if (cudaMalloc(&q, need) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(MARBLE_ERR_OOM, "cudaMalloc of the backward dS scratch failed (" +
+                                        std::to_string(need) + " bytes)");
+      }
+      pl->ds_scratch = q;
+      pl->ds_scratch_bytes = need;
+    }
+  }
+  if (buf_slots > 0 &&
+      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, 2 * buf_slots * 128, 1, 128, 64, 128, sw))
+    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
+  // Step i: the dK/dV kernel (side stream) writes the step's dS^T tiles into half i & 1 of the
+  // scratch, then the dQ GEMM (stream s) reads them; dK/dV of step i+2 waits until the dQ GEMM
+  // of step i has finished with that half.  dK/dV of step i+1 overlaps the dQ GEMM of step i.
   cudaStream_t s2 = side_stream();
   if (!s2) s2 = s;
   if (s2 != s) {
     cudaError_t e = stream_fork(s, s2);
     if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
   }
-  const int span_q = timing_begin(s), span_k = timing_begin(s2);
+  std::vector<cudaEvent_t> ev_k(n_steps, nullptr), ev_q(n_steps, nullptr);
+  auto make_event = [](cudaEvent_t* ev) {
+    return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+  };
   int launches_q = 0, launches_k = 0;
-  for (int i = 0; i < n_steps; ++i) {
+  cudaError_t err = cudaSuccess;
+  for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
-    // dQ: the q blocks of the q shard with tiles in this step, longest list first
-    {
-      BwdParams pq = prm;
-      const int64_t seg = (int64_t)pq.q_shard * (P + 1) + (pq.kv_shard >= 0 ? pq.kv_shard : P);
-      pq.order = pl->fwd_order + seg * pl->bps;
-      pq.nwork = pl->h_fwd_nwork[seg] * qkv->hq;
-      if (pq.nwork > 0) {
-        pq.sched = sched_slot(pl);
-        k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kThreads, smem_q, s>>>(pq);
-        ++launches_q;
-      }
-    }
+    prm.ds_slot0 = (long long)(i & 1) * buf_slots;
     // dK/dV: the kv blocks of the kv shard listed for the q shard (longest list first), or
     // the q shard's needed kv blocks
     {
@@ -1059,19 +932,47 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
         pk.nwork = (int)(pl->h_needed_ptr[pk.q_shard + 1] - pl->h_needed_ptr[pk.q_shard]) *
                    qkv->hkv;
       }
-      if (pk.nwork > 0) {
+      if (s2 != s && i >= 2) err = cudaStreamWaitEvent(s2, ev_q[i - 2], 0);
+      if (pk.nwork > 0 && err == cudaSuccess) {
         pk.sched = sched_slot(pl);
+        const int span = timing_begin(s2);
         k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s2>>>(pk);
+        timing_end(span, s2, kTimeDkdv, 1);
         ++launches_k;
+      }
+      if (s2 != s && err == cudaSuccess) {
+        err = make_event(&ev_k[i]);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_k[i], s2);
+        if (err == cudaSuccess) err = cudaStreamWaitEvent(s, ev_k[i], 0);
+      }
+    }
+    // dQ GEMM: the q blocks of the q shard with tiles in this step, longest list first
+    if (err == cudaSuccess) {
+      BwdParams pq = prm;
+      const int64_t seg = (int64_t)pq.q_shard * (P + 1) + (pq.kv_shard >= 0 ? pq.kv_shard : P);
+      pq.order = pl->fwd_order + seg * pl->bps;
+      pq.nwork = pl->h_fwd_nwork[seg] * qkv->hq;
+      if (pq.nwork > 0) {
+        pq.sched = sched_slot(pl);
+        const int span = timing_begin(s);
+        k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kGThreads, smem_q, s>>>(pq);
+        timing_end(span, s, kTimeDq, 1);
+        ++launches_q;
+      }
+      if (s2 != s) {
+        err = make_event(&ev_q[i]);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_q[i], s);
       }
     }
   }
-  timing_end(span_q, s, kTimeDq, launches_q);
-  timing_end(span_k, s2, kTimeDkdv, launches_k);
-  if (s2 != s) {
-    cudaError_t e = stream_fork(s2, s);
-    if (e != cudaSuccess) return cuda_fail(e, "join of the backward streams");
-  }
+  if (s2 != s && err == cudaSuccess) err = stream_fork(s2, s);
+  for (cudaEvent_t ev : ev_k)
+    if (ev) cudaEventDestroy(ev);
+  for (cudaEvent_t ev : ev_q)
+    if (ev) cudaEventDestroy(ev);
+  (void)launches_q;
+  (void)launches_k;
+  if (err != cudaSuccess) return cuda_fail(err, "ordering of the backward streams");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");
   return MARBLE_OK;

@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -58,6 +59,18 @@ struct marble_plan {
   int32_t* bwd_order = nullptr;      // [P*(P+1)*bps] over colT_ptr (kv blocks)
   int32_t* bwd_nwork = nullptr;      // [P*(P+1)]
   std::vector<int32_t> h_fwd_nwork, h_bwd_nwork;
+  // compact tile numbering of each step (the backward's dS tiles): step_off[nq*(P+1)+opt] is
+  // the number of tiles of the q blocks before nq in its q shard, for option opt (kv shard opt,
+  // or every kv shard when opt == P); colT_j[e] the index of column-list entry e's kv block in
+  // its q block's list for that kv shard
+  int32_t* step_off = nullptr;       // [nb*(P+1)]
+  int64_t* step_tiles = nullptr;     // [P*(P+1)] tiles per (q shard, option)
+  int32_t* colT_j = nullptr;         // [nnz]
+  std::vector<int64_t> h_step_tiles;
+  // backward scratch: bf16 dS^T tiles of two steps (allocated by the first backward call)
+  mutable std::mutex scratch_mu;
+  mutable void* ds_scratch = nullptr;
+  mutable size_t ds_scratch_bytes = 0;
   // ticket counters of the persistent kernels: launch i uses pair (i mod kSchedSlots); the
   // last CTA of a launch puts its pair back to zero
   unsigned* sched = nullptr;         // [2*kSchedSlots]

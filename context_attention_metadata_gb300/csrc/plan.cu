@@ -377,6 +377,71 @@ __global__ void k_colT(const Summary* __restrict__ s, const int32_t* __restrict_
   }
 }
 
+// Positions of the column-list entries in the row lists: for the entry of (kv block nk, q
+// shard r) that lists q block nq, the index of nk within nq's list for kv shard nk / bps.  Both
+// lists are sorted by original block index, so a binary search on it finds the entry.
+__global__ void k_colT_pos(const int64_t* __restrict__ colT_ptr, const int32_t* __restrict__ colT_row,
+                           const int64_t* __restrict__ step_ptr, const int32_t* __restrict__ step_col,
+                           const int32_t* __restrict__ block_perm, int64_t nb, int P, int64_t bps,
+                           int32_t* __restrict__ colT_j) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);  // nk * P + r
+  if (row >= nb * P) return;
+  const int64_t nk = row / P;
+  const int s = (int)(nk / bps);
+  const int32_t key = block_perm[nk];
+  for (int64_t e = colT_ptr[row] + lane; e < colT_ptr[row + 1]; e += 32) {
+    const int64_t nq = colT_row[e];
+    const int64_t base = step_ptr[nq * P + s];
+    int64_t lo = base, hi = step_ptr[nq * P + s + 1] - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (block_perm[step_col[mid]] < key)
+        lo = mid + 1;
+      else
+        hi = mid;
+    }
+    colT_j[e] = (int32_t)(lo - base);
+  }
+}
+
+// Compact numbering of one step's tiles (one CTA per (q shard r, option opt); option opt < P
+// is kv shard opt, option P every kv shard): step_off[nq * (P+1) + opt] = number of tiles of
+// the q blocks of shard r before nq; step_tiles[r * (P+1) + opt] = the step's total.
+__global__ void __launch_bounds__(1024) k_step_off(const int64_t* __restrict__ step_ptr, int P,
+                                                   int64_t bps, int32_t* __restrict__ step_off,
+                                                   int64_t* __restrict__ step_tiles) {
+  __shared__ int64_t sc[1024];
+  __shared__ int64_t carry;
+  const int seg = blockIdx.x;
+  const int r = seg / (P + 1), opt = seg % (P + 1);
+  const int c_lo = opt < P ? opt : 0, c_hi = opt < P ? opt + 1 : P;
+  const int t = threadIdx.x;
+  if (t == 0) carry = 0;
+  __syncthreads();
+  for (int64_t i0 = 0; i0 < bps; i0 += 1024) {
+    const int64_t i = i0 + t;
+    int64_t len = 0;
+    if (i < bps) {
+      const int64_t nq = (int64_t)r * bps + i;
+      len = step_ptr[nq * P + c_hi] - step_ptr[nq * P + c_lo];
+    }
+    sc[t] = len;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      const int64_t v = t >= off ? sc[t - off] : 0;
+      __syncthreads();
+      sc[t] += v;
+      __syncthreads();
+    }
+    if (i < bps) step_off[((int64_t)r * bps + i) * (P + 1) + opt] = (int32_t)(carry + sc[t] - len);
+    __syncthreads();
+    if (t == 1023) carry += sc[1023];
+    __syncthreads();
+  }
+  if (t == 0) step_tiles[seg] = carry;
+}
+
 // needed kv blocks of q shard r = kv blocks with a non-empty (kv block, r) list
 template <bool kWrite>
 __global__ void k_needed(const int64_t* __restrict__ colT_ptr, int64_t nb, int P,
@@ -564,6 +629,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->bwd_order, (size_t)P * (P + 1) * bps));
   MARBLE_TRY(dalloc(p, &p->bwd_nwork, (size_t)P * (P + 1)));
   MARBLE_TRY(dalloc(p, &p->sched, 2 * kSchedSlots));
+  MARBLE_TRY(dalloc(p, &p->step_off, (size_t)nb * (P + 1)));
+  MARBLE_TRY(dalloc(p, &p->step_tiles, (size_t)P * (P + 1)));
   // scratch: counters of the two-pass compactions and the order builder
   int32_t *cnt = nullptr, *cnt2 = nullptr, *cntT = nullptr, *ucost = nullptr,
           *rank_of = nullptr, *unit_new = nullptr, *ncount = nullptr;
@@ -628,6 +695,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->step_tag, nnz));
   MARBLE_TRY(dalloc(p, &p->colT_row, nnz));
   MARBLE_TRY(dalloc(p, &p->colT_tag, nnz));
+  MARBLE_TRY(dalloc(p, &p->colT_j, nnz));
   k_tiles_write<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->summ, p->band, p->row_ptr, nb, W,
                                                         p->col, p->tag);
   MARBLE_CK(cudaGetLastError());
@@ -679,6 +747,11 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->needed, ntot));
   k_needed<true><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, nullptr, p->needed_ptr, p->needed);
   MARBLE_CK(cudaGetLastError());
+  // positions of the column-list entries in the row lists, and each step's tile numbering
+  k_colT_pos<<<(unsigned)grid_for(nb * P, kWarpsPerCta), 32 * kWarpsPerCta, 0, s>>>(
+      p->colT_ptr, p->colT_row, p->step_ptr, p->step_col, p->block_perm, nb, P, bps, p->colT_j);
+  k_step_off<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->step_off, p->step_tiles);
+  MARBLE_CK(cudaGetLastError());
   // work order of the persistent kernels
   k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->fwd_order, p->fwd_nwork);
   k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->colT_ptr, P, bps, p->bwd_order, p->bwd_nwork);
@@ -688,6 +761,9 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_CK(cudaMemcpyAsync(p->h_fwd_nwork.data(), p->fwd_nwork, P * (P + 1) * sizeof(int32_t),
                             cudaMemcpyDeviceToHost, s));
   MARBLE_CK(cudaMemcpyAsync(p->h_bwd_nwork.data(), p->bwd_nwork, P * (P + 1) * sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, s));
+  p->h_step_tiles.resize((size_t)P * (P + 1));
+  MARBLE_CK(cudaMemcpyAsync(p->h_step_tiles.data(), p->step_tiles, P * (P + 1) * sizeof(int64_t),
                             cudaMemcpyDeviceToHost, s));
   MARBLE_CK(cudaStreamSynchronize(s));
   return MARBLE_OK;
