@@ -676,21 +676,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
         tmem_ld_wait();
         uint32_t dsv[32];  // this row's bf16 dS^T pairs over the half's 64 q columns
+        // P^T = exp2(s * scale * log2 e - lse2[q]), dS^T = P^T (dP^T - delta[q]); the per-query
+        // LSE and delta are read four at a time; full tiles skip the mask
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk16[16], dk16[16];
 #pragma unroll
-          for (int t = 0; t < 32; t += 2) {
+          for (int t = 0; t < 32; t += 4) {
             const int q0 = cc * 32 + t;
-            const bool l0 = (lm[cc] >> t) & 1u, l1 = (lm[cc] >> (t + 1)) & 1u;
-            const float p0 = l0 ? fast_exp2(__uint_as_float(vs[cc][t]) * sl2 - lse2s[q0]) : 0.f;
-            const float p1 =
-                l1 ? fast_exp2(__uint_as_float(vs[cc][t + 1]) * sl2 - lse2s[q0 + 1]) : 0.f;
-            const float d0 = p0 * (__uint_as_float(vp[cc][t]) - dls[q0]);
-            const float d1 = p1 * (__uint_as_float(vp[cc][t + 1]) - dls[q0 + 1]);
-            pk16[t >> 1] = pack_bf16(p0, p1);
-            dk16[t >> 1] = pack_bf16(d0, d1);
+            const float4 l4 = *reinterpret_cast<const float4*>(lse2s + q0);
+            const float4 d4 = *reinterpret_cast<const float4*>(dls + q0);
+            const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dv4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float e = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
+              pv[u] = (partial && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : e;
+              dv4[u] = pv[u] * (__uint_as_float(vp[cc][t + u]) - dq4[u]);
+            }
+            pk16[t >> 1] = pack_bf16(pv[0], pv[1]);
+            pk16[(t >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+            dk16[t >> 1] = pack_bf16(dv4[0], dv4[1]);
+            dk16[(t >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
             dsv[cc * 16 + (t >> 1)] = dk16[t >> 1];
+            dsv[cc * 16 + (t >> 1) + 1] = dk16[(t >> 1) + 1];
           }
           tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
           tmem_st16(tP + lb + half * 64 + cc * 16, dk16);

@@ -448,16 +448,26 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         tmem_ld32(sb + lb + (2 * half) * 32, v[0]);
         tmem_ld32(sb + lb + (2 * half + 1) * 32, v[1]);
         tmem_ld_wait();
-        // scaled, masked scores (kept in v) and this half's row maximum
+        // this half's row maximum of the scaled, masked scores; on a partial tile the scaled
+        // scores (-inf where masked) replace v, on a full tile v keeps the raw scores (scaling
+        // by a positive constant commutes with the maximum, and P takes one FMA below)
         float mx = -INFINITY;
+        if (partial) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
+          for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) {
-            const float s = ((lm[cc] >> t) & 1u) ? __uint_as_float(v[cc][t]) * sl2 : -INFINITY;
-            v[cc][t] = __float_as_uint(s);
-            mx = fmaxf(mx, s);
+            for (int t = 0; t < 32; ++t) {
+              const float s = ((lm[cc] >> t) & 1u) ? __uint_as_float(v[cc][t]) * sl2 : -INFINITY;
+              v[cc][t] = __float_as_uint(s);
+              mx = fmaxf(mx, s);
+            }
           }
+        } else {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+#pragma unroll
+            for (int t = 0; t < 32; ++t) mx = fmaxf(mx, __uint_as_float(v[cc][t]));
+          mx *= sl2;
         }
         float* mxb = mxs + b * 256;
         mxb[half * 128 + row] = mx;
@@ -495,14 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         // P = exp2(s - m_run) as bf16, packed into columns [64 half, 64 half + 32) of the S
         // buffer: inside the fp32 columns this warp has just read
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
+        // v holds scaled scores on a partial tile, raw ones on a full tile
+        const float vs = partial ? 1.f : sl2;
         float rs = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int t = 0; t < 32; t += 2) {
-            const float p0 = fast_exp2(__uint_as_float(v[cc][t]) - base);
-            const float p1 = fast_exp2(__uint_as_float(v[cc][t + 1]) - base);
+            const float p0 = fast_exp2(fmaf(__uint_as_float(v[cc][t]), vs, -base));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(v[cc][t + 1]), vs, -base));
             rs += p0 + p1;
             pk[t >> 1] = pack_bf16(p0, p1);
           }
