@@ -82,3 +82,66 @@ def worked_example_inputs():
     rng = np.random.default_rng(0)
     Q, K, V = (rng.normal(size=(16, 8)).astype(np.float32) for _ in range(3))
     return Q, K, V
+
+
+def round_bf16(x):
+    """Round to the nearest bfloat16 (ties to even), returned as float64: the value goes to
+    float32 first (a CUDA kernel holds it in fp32), then keeps the top 16 bits of its
+    encoding after round-to-nearest-even on the lower 16 (the bfloat16 format: 8 exponent
+    bits, 7 stored mantissa bits)."""
+    f = np.asarray(x, np.float64).astype(np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    finite = np.isfinite(f)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000).astype(np.uint32)
+    out = np.where(finite, r.view(np.float32), f)
+    return out.astype(np.float64)
+
+
+def ring_forward_bf16_merge(q, k, v, mask=None, P=4, step_order=None, scale=None,
+                            rounding=round_bf16):
+    """Standard ring attention, the baseline MARBLE post section 03 ("Exact ring attention
+    accumulation") measures against: every step runs one attention over the step's keys and
+    emits a normalised partial output rounded to bf16 plus its log-sum-exp; the running
+    output is merged with it by a log-sum-exp rescale and rounded to bf16 again.
+
+    Per row and head, with running (O, lse) starting at (0, -inf) and a step's legal scores s:
+      lse_s = max s + ln sum exp(s - max s),  O_s = round(sum softmax(s) V)
+      lse'  = ln(exp(lse) + exp(lse_s)),      O'  = round(O exp(lse - lse') + O_s exp(lse_s - lse'))
+    A step with no legal key for the row leaves it unchanged.  fp64 between roundings;
+    `rounding` is the rounding applied at both points (bf16 by default).  Returns (O, LSE)."""
+    q, k, v = (_f64(x) for x in (q, k, v))
+    n, hq, d = q.shape
+    if n % P:
+        raise ValueError("N must be divisible by P")
+    g = _group(hq, k.shape[1])
+    S_ = n // P
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if step_order is None:
+        step_order = [[(r - s) % P for s in range(P)] for r in range(P)]
+    O = np.zeros((n, hq, d))
+    lse = np.full((hq, n), -np.inf)
+    for r in range(P):
+        qs = slice(r * S_, (r + 1) * S_)
+        for j in step_order[r]:
+            ks = slice(j * S_, (j + 1) * S_)
+            blk = None if mask is None else mask[qs, ks]
+            for h in range(hq):
+                kh = h // g
+                s = (q[qs, h, :] @ k[ks, kh, :].T) * scale
+                if blk is not None:
+                    s = np.where(blk, s, -np.inf)
+                mx = s.max(axis=1)
+                live = np.isfinite(mx)
+                base = np.where(live, mx, 0.0)
+                e = np.exp(s - base[:, None])
+                l_s = e.sum(axis=1)
+                O_s = rounding((e @ v[ks, kh, :]) / np.where(live, l_s, 1.0)[:, None])
+                lse_s = np.where(live, base + np.log(np.where(live, l_s, 1.0)), -np.inf)
+                lse_old = lse[h, qs]
+                lse_new = np.logaddexp(lse_old, lse_s)
+                w_old = np.where(np.isfinite(lse_old), np.exp(lse_old - np.where(live | np.isfinite(lse_old), lse_new, 0.0)), 0.0)
+                w_new = np.where(live, np.exp(lse_s - np.where(live, lse_new, 0.0)), 0.0)
+                merged = rounding(O[qs, h, :] * w_old[:, None] + O_s * w_new[:, None])
+                O[qs, h, :] = np.where(live[:, None], merged, O[qs, h, :])
+                lse[h, qs] = np.where(live, lse_new, lse_old)
+    return O, lse

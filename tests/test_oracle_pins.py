@@ -474,3 +474,86 @@ def test_sampled_rows_and_columns_equal_dense():
     assert np.abs(dv2 - dv[cols]).max() < 1e-10
     dk3, dv3 = attention.cols_backward(q, k, v, do, tr, W, cols, kv_heads=[1])
     assert np.abs(dk3[:, 0] - dk[cols, 1]).max() < 1e-10
+
+
+def test_round_bf16_ties_and_library_conversion():
+    # bfloat16 keeps 7 stored mantissa bits: at 1 the spacing is 2^-7, so 1 + 2^-8 is a tie
+    # that goes to the even neighbour 1, and 1 + 3 * 2^-8 ties up to 1 + 2^-6
+    x = np.array([1 + 2.0**-8, 1 + 3 * 2.0**-8, -(1 + 2.0**-8), 1 + 2.0**-8 + 2.0**-20,
+                  0.0, -0.0, np.inf, -np.inf, 3.40e38])
+    r = ring.round_bf16(x)
+    assert r[0] == 1.0 and r[1] == 1 + 2.0**-6 and r[2] == -1.0 and r[3] == 1 + 2.0**-7
+    assert r[4] == 0.0 and np.signbit(r[5]) and r[6] == np.inf and r[7] == -np.inf
+    assert r[8] == np.inf  # past the midpoint between the largest finite bfloat16 (about 3.3895e38) and 2^128
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    y = rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000)
+    lib = torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ring.round_bf16(y), lib)
+
+
+def test_bf16_merge_without_rounding_is_exact_attention():
+    # with the identity in place of both roundings, the log-sum-exp merge of normalised
+    # partials is an exact identity: the result equals dense attention for any P and order
+    rng = np.random.default_rng(11)
+    n = 256
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, 96)
+    q, k, v = _rand_qkv(rng, n, 4, 2, 16)
+    O, L = attention.forward(q, k, v, M)
+    fin = np.isfinite(L)
+    for P in (1, 2, 8):
+        order = [list(rng.permutation(P)) for _ in range(P)]
+        Ob, Lb = ring.ring_forward_bf16_merge(q, k, v, M, P=P, step_order=order,
+                                              rounding=lambda x: x)
+        assert np.abs(Ob - O).max() < 1e-12
+        assert (np.isfinite(Lb) == fin).all()
+        assert np.abs(Lb[fin] - L[fin]).max() < 1e-12
+
+
+def test_bf16_merge_single_step_is_rounded_exact_output():
+    # P = 1: one partial (rounded once) merged into the empty state (weight 1, rounded again,
+    # which leaves a bf16 value unchanged)
+    rng = np.random.default_rng(12)
+    n = 128
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, INF)
+    q, k, v = _rand_qkv(rng, n, 2, 2, 16)
+    O, L = attention.forward(q, k, v, M)
+    Ob, Lb = ring.ring_forward_bf16_merge(q, k, v, M, P=1)
+    assert np.array_equal(Ob, ring.round_bf16(O))
+    fin = np.isfinite(L)
+    assert np.abs(Lb[fin] - L[fin]).max() < 1e-12
+
+
+def test_bf16_merge_two_steps_by_hand():
+    # one row, one head, two keys in two shards of one token each: the merge written out
+    q = np.array([[[0.3, -1.2]], [[0.0, 0.0]]])
+    k = np.array([[[1.1, 0.4]], [[-0.7, 2.0]]])
+    v = np.array([[[0.123456, -2.5]], [[1.75, 0.333333]]])
+    Ob, Lb = ring.ring_forward_bf16_merge(q, k, v, None, P=2, step_order=[[0, 1], [1, 0]],
+                                          scale=1.0)
+    s0 = 0.3 * 1.1 - 1.2 * 0.4
+    s1 = 0.3 * -0.7 - 1.2 * 2.0
+    lse = math.log(math.exp(s0) + math.exp(s1))
+    o0 = ring.round_bf16(v[0, 0])          # step 1: the partial is V of key 0, lse_1 = s0
+    o1 = ring.round_bf16(v[1, 0])          # step 2: V of key 1, lse_2 = s1
+    want = ring.round_bf16(o0 * math.exp(s0 - lse) + o1 * math.exp(s1 - lse))
+    assert np.array_equal(Ob[0, 0], want)
+    assert abs(Lb[0, 0] - lse) < 1e-14
+
+
+def test_bf16_merge_masked_rows_and_error_gap():
+    rng = np.random.default_rng(13)
+    n = 512
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, INF)
+    M[:3] = False  # rows with no legal key at all
+    q, k, v = _rand_qkv(rng, n, 2, 2, 32)
+    O, L = attention.forward(q, k, v, M)
+    Ob, Lb = ring.ring_forward_bf16_merge(q, k, v, M, P=8)
+    assert (Ob[:3] == 0).all() and np.isneginf(Lb[:, :3]).all()
+    # bf16 rounding after every step costs more than one rounding of the exact result
+    e_once = np.abs(ring.round_bf16(O) - O).mean()
+    e_merge = np.abs(Ob - O).mean()
+    assert e_merge > 1.2 * e_once
