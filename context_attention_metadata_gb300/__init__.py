@@ -25,6 +25,7 @@ WINDOW_INF = 2147483647
 TILE_FULL, TILE_PARTIAL = 1, 2
 KV_NEEDED = -1
 STEP_FIRST = 1
+STEP_BF16_MERGE = 2  # standard ring merge in bf16 (the comparison baseline)
 ORDERS = {"contiguous": 0, "ptrr_block": 1, "ptrr_chunk": 2}
 FIELDS = {
     "perm": (0, "int32"), "block_perm": (1, "int32"), "tracks_perm": (2, "int32"),
@@ -249,13 +250,18 @@ def _qkv(plan, q, k, v, scale):
     return _QKV(q.data_ptr(), k.data_ptr(), v.data_ptr(), hq, hkv, d, float(scale))
 
 
+def _flags(first: bool, bf16_merge: bool) -> int:
+    return (STEP_FIRST if first else 0) | (STEP_BF16_MERGE if bf16_merge else 0)
+
+
 def attn_step(plan: Plan, q, k, v, q_shard: int, kv_shard: int, state: State,
-              first: bool = False, scale: float = 0.0, stream=None):
-    """One forward ring step (marble_attn_step)."""
+              first: bool = False, scale: float = 0.0, stream=None, bf16_merge: bool = False):
+    """One forward ring step (marble_attn_step); ``bf16_merge`` selects the standard
+    bf16 per-step merge instead of the carried fp32 state."""
     c = _qkv(plan, q, k, v, scale)
     st = state._c()
     _call("marble_attn_step", plan.handle, ctypes.byref(c), int(q_shard), int(kv_shard),
-          ctypes.byref(st), STEP_FIRST if first else 0, _stream(stream))
+          ctypes.byref(st), _flags(first, bf16_merge), _stream(stream))
 
 
 def attn_finalize(plan: Plan, state: State, o, lse, stream=None):
@@ -348,14 +354,15 @@ def ring_schedule(num_shards: int, needed: bool = False):
     return [(r, (r - s) % P, s == 0) for r in range(P) for s in range(P)]
 
 
-def attn_steps(plan: Plan, q, k, v, schedule, state: State, scale: float = 0.0, stream=None):
+def attn_steps(plan: Plan, q, k, v, schedule, state: State, scale: float = 0.0, stream=None,
+               bf16_merge: bool = False):
     """A list of forward ring steps [(q_shard, kv_shard, first), ...] in one C call."""
     c = _qkv(plan, q, k, v, scale)
     st = state._c()
     n = len(schedule)
     qs = (ctypes.c_int32 * n)(*[int(r) for r, _, _ in schedule])
     ks = (ctypes.c_int32 * n)(*[int(j) for _, j, _ in schedule])
-    fl = (ctypes.c_uint32 * n)(*[STEP_FIRST if f else 0 for _, _, f in schedule])
+    fl = (ctypes.c_uint32 * n)(*[_flags(f, bf16_merge) for _, _, f in schedule])
     _call("marble_attn_steps", plan.handle, ctypes.byref(c), n, qs, ks, fl, ctypes.byref(st),
           _stream(stream))
 
@@ -379,10 +386,10 @@ def attn_bwd_steps(plan: Plan, q, k, v, do, lse, delta, schedule, dq_acc, dk_acc
 
 
 def forward(plan: Plan, q, k, v, state: State, o, lse, needed: bool = False, scale: float = 0.0,
-            stream=None):
+            stream=None, bf16_merge: bool = False):
     """All forward ring steps (r-major, keeping shard r's state hot in L2) + finalize."""
     attn_steps(plan, q, k, v, ring_schedule(plan.num_shards, needed), state, scale=scale,
-               stream=stream)
+               stream=stream, bf16_merge=bf16_merge)
     attn_finalize(plan, state, o, lse, stream=stream)
 
 

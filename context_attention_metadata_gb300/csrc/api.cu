@@ -353,7 +353,7 @@ MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble
   if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
-  if (flags & ~MARBLE_STEP_FIRST) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+  if (flags & ~(MARBLE_STEP_FIRST | MARBLE_STEP_BF16_MERGE)) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
   return run_attn_fwd(p, qkv, 1, &q_shard, &kv_shard, &flags, state, (cudaStream_t)stream);
 }
 
@@ -379,8 +379,12 @@ MARBLE_API marble_status_t marble_attn_steps(const marble_plan_t* p, const marbl
   if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
   if ((st = check_step_list(p, n_steps, q_shards, kv_shards)) != MARBLE_OK) return st;
   if (n_steps > 0 && !flags) return fail(MARBLE_ERR_INVALID_ARG, "flags must be non-null");
-  for (int32_t i = 0; i < n_steps; ++i)
-    if (flags[i] & ~MARBLE_STEP_FIRST) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+  for (int32_t i = 0; i < n_steps; ++i) {
+    if (flags[i] & ~(MARBLE_STEP_FIRST | MARBLE_STEP_BF16_MERGE))
+      return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+    if ((flags[i] ^ flags[0]) & MARBLE_STEP_BF16_MERGE)
+      return fail(MARBLE_ERR_INVALID_ARG, "MARBLE_STEP_BF16_MERGE differs between steps");
+  }
   if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;

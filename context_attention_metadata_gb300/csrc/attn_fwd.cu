@@ -103,6 +103,7 @@ struct FwdParams {
   int nwork;  // units with at least one tile: nonempty blocks of the order x hq
   int W;
   int first;
+  int bf16_merge;  // standard ring merge: bf16 partials and running output, running LSE
   float scale_log2;
 };
 
@@ -563,6 +564,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
     //                 O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
     //   some row grew exact merge with the stored tile (loaded by the row threads), then a
     //                 TMA store.
+    //   bf16 merge    the standard ring-attention merge kept for comparison: the call's
+    //                 output is normalised and rounded to bf16, merged with the stored
+    //                 (bf16-valued) output by the log-sum-exp weights and rounded to bf16
+    //                 again; m then holds the running base-2 LSE and l is 1 (0 for a row
+    //                 that has seen no legal key), which the finalize reads unchanged.
     int uc = 0, k = 0;  // units merged, staging rounds
     bool ok = true;
     while (ok) {
@@ -589,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
       if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_mode[uc & 1], 1);
       mbar_arrive(&bar[B_EVOTE]);
       if (!wait_all(&bar[B_EVOTE], uc & 1, w)) break;
-      const int mode = p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
+      const int mode = p.bf16_merge ? 3 : p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
       // every epilogue thread has read the other flag (before this vote), and none can vote
       // on the next unit before row 0 has passed its first staging round of this one
       if (row == 0) epi_mode[(uc + 1) & 1] = 0;
@@ -609,6 +615,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         a_old = (m_old == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_old - m_out, -1000.f));
         a_new = (m_run == -INFINITY) ? 0.f : ldexpf(1.f, (int)fmaxf(m_run - m_out, -1000.f));
         l_out = l_old * a_old + l_run * a_new;
+      } else if (mode == 3) {
+        // log-sum-exp merge in base 2: b = the call's LSE, m_old = the stored one
+        const float b = l_run > 0.f ? m_run + log2f(l_run) : -INFINITY;
+        const float hi = fmaxf(m_old, b), lo = fminf(m_old, b);
+        m_out = lo == -INFINITY ? hi : hi + log1pf(exp2f(lo - hi)) * 1.4426950408889634f;
+        a_old = m_old == -INFINITY ? 0.f : exp2f(m_old - m_out);
+        a_new = b == -INFINITY ? 0.f : exp2f(b - m_out);  // weight of the normalised partial
+        l_out = m_out == -INFINITY ? 0.f : 1.f;
       }
       p.m[gi] = m_out;
       p.l[gi] = l_out;
@@ -626,8 +640,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
           mbar_arrive(&bar[B_OFREE0 + ub]);
         }
         float vals[32];
+        if (mode == 3) {
+          // bf16(O_old * a_old + bf16(O_call / l_call) * a_new)
+          const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) vals[t] = __uint_as_float(x[t]) * a_new;
+          for (int t = 0; t < 32; ++t) vals[t] = bf16_round(__uint_as_float(x[t]) * inv_l) * a_new;
+          if (!p.first) {
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float4 o = src[r * 8 + t];
+              vals[4 * t] = fmaf(o.x, a_old, vals[4 * t]);
+              vals[4 * t + 1] = fmaf(o.y, a_old, vals[4 * t + 1]);
+              vals[4 * t + 2] = fmaf(o.z, a_old, vals[4 * t + 2]);
+              vals[4 * t + 3] = fmaf(o.w, a_old, vals[4 * t + 3]);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 32; ++t) vals[t] = bf16_round(vals[t]);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) vals[t] = __uint_as_float(x[t]) * a_new;
+        }
         if (mode == 2) {
 #pragma unroll
           for (int t = 0; t < 8; ++t) {
@@ -744,6 +777,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
     prm.first = (flags[i] & MARBLE_STEP_FIRST) ? 1 : 0;
+    prm.bf16_merge = (flags[i] & MARBLE_STEP_BF16_MERGE) ? 1 : 0;
     const int64_t seg = (int64_t)prm.q_shard * (pl->P + 1) + (prm.kv_shard >= 0 ? prm.kv_shard : pl->P);
     prm.order = pl->fwd_order + seg * pl->bps;
     prm.nwork = pl->h_fwd_nwork[seg] * qkv->hq;

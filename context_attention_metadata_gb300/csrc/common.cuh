@@ -362,6 +362,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// x rounded to the nearest bf16 (ties to even), as fp32
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);

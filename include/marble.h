@@ -74,6 +74,7 @@ typedef enum {
 #define MARBLE_TILE_PARTIAL 2          /* mixed: the mask predicate runs per pair */
 #define MARBLE_KV_NEEDED (-1)          /* kv_shard value: every needed KV block at once */
 #define MARBLE_STEP_FIRST 1u           /* flags bit: this is the first step of the rows */
+#define MARBLE_STEP_BF16_MERGE 2u      /* flags bit: standard ring merge in bf16 (baseline) */
 
 typedef enum {
   MARBLE_ORDER_CONTIGUOUS = 0, /* identity order: shard r = contiguous token range */
@@ -223,6 +224,13 @@ typedef struct {
  * step (which are written as such).  Otherwise the stored state is resumed.
  * The ring pairing of MARBLE s03 is kv_shard = (q_shard - s) mod P at step s; any order
  * of the P kv shards gives the same result up to fp32 rounding.
+ * flags & MARBLE_STEP_BF16_MERGE: instead of carrying the fp32 state, run the standard
+ * ring-attention merge that MARBLE s03 compares against: the step's output is normalised
+ * and rounded to bf16, then merged with the stored output by log-sum-exp weights and
+ * rounded to bf16 again.  O_acc then holds bf16-representable values, m the running
+ * log-sum-exp in base 2 (ln -> log2) and l = 1 (0 while a row has seen no legal key), so
+ * that marble_attn_finalize gives O and LSE unchanged.  Every step of a pass over the
+ * same rows must carry the same setting of this bit.
  * Errors: INVALID_ARG (shard out of range, null/misaligned pointer, d not 64/128,
  * hq % hkv != 0), CUDA.
  */

@@ -8,7 +8,7 @@ import torch
 import context_attention_metadata_gb300 as M
 import workloads as wl
 from marble_testlib import check_o_lse, make_plan, plan_for, rel_fro, run_forward
-from oracle import attention, mask
+from oracle import attention, mask, ring
 
 pytestmark = pytest.mark.gpu
 INF = wl.WINDOW_INF
@@ -156,3 +156,69 @@ def test_full_configs_forward_sampled(cid):
     Oref, Lref = attention.rows_forward(qc, kc, vc, tr, cfg.window, rows, heads=heads)
     hs = torch.as_tensor(heads).cuda()
     check_o_lse(O[rows_t][:, hs], L[hs][:, rows_t], Oref, Lref)
+
+
+def _bf16_merge_case(n=8192, hq=2, d=128, seed=21):
+    cfg = wl.mini_config(2, n, hq=hq)
+    tr = wl.config_tracks(2, n)
+    q, k, v = _qkv(n, cfg.hq, cfg.hkv, d, seed=seed)
+    return cfg, tr, q, k, v
+
+
+def test_bf16_merge_matches_its_oracle():
+    # the standard ring merge (bf16 partial per step, bf16 running output, log-sum-exp
+    # weights) in the same ring order and on the same plan-ordered shards as the oracle
+    cfg, tr, q, k, v = _bf16_merge_case()
+    pl = plan_for(cfg, tr)
+    O, L, st = run_forward(pl, q, k, v, bf16_merge=True)
+    perm = pl.export("perm").long().cpu().numpy()
+    Mp = mask.dense_mask(tr, cfg.window, rows=perm, cols=perm)  # plan order, original positions
+    Ob, Lb = ring.ring_forward_bf16_merge(q.cpu()[perm], k.cpu()[perm], v.cpu()[perm], Mp,
+                                          P=cfg.shards)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    check_o_lse(O, L, Ob[inv], Lb[:, inv])
+    # the stored running output is bf16-valued and l is 1 on live rows, 0 on dead ones
+    acc = st.o_acc.cpu()
+    assert torch.equal(acc, acc.to(torch.bfloat16).float())
+    lv = st.l.cpu().numpy()
+    assert set(np.unique(lv)) <= {0.0, 1.0}
+
+
+def test_bf16_merge_single_pass_is_rounded_exact():
+    # needed-block mode runs one call per q shard: one rounded partial, nothing to merge
+    cfg, tr, q, k, v = _bf16_merge_case(n=4096, seed=22)
+    pl = plan_for(cfg, tr)
+    O, L, _ = run_forward(pl, q, k, v, needed=True, bf16_merge=True)
+    Oref, Lref = _dense_ref(tr, cfg.window, q, k, v)
+    check_o_lse(O, L, ring.round_bf16(Oref), Lref)
+
+
+def test_bf16_merge_error_exceeds_carried_fp32():
+    # the accuracy gap the carried fp32 state removes: same inputs, same plan, P = 8
+    cfg, tr, q, k, v = _bf16_merge_case(seed=23)
+    pl = plan_for(cfg, tr)
+    Oref, _ = _dense_ref(tr, cfg.window, q, k, v)
+    O32, _, _ = run_forward(pl, q, k, v)
+    O16, _, _ = run_forward(pl, q, k, v, bf16_merge=True)
+    e32 = np.abs(O32.float().cpu().numpy() - Oref).mean()
+    e16 = np.abs(O16.float().cpu().numpy() - Oref).mean()
+    print(f"mean |O - O_exact|: carried fp32 {e32:.3e}, bf16 merge {e16:.3e}, "
+          f"ratio {e16 / e32:.3f}")
+    assert e16 > 1.05 * e32
+
+
+def test_bf16_merge_flag_is_uniform_per_call():
+    cfg, tr, q, k, v = _bf16_merge_case(n=2048, seed=24)
+    pl = plan_for(cfg, tr)
+    st = M.State(cfg.n, cfg.hq, cfg.d)
+    qp, kp, vp = pl.permute(q), pl.permute(k), pl.permute(v)
+    import ctypes
+    c = M._qkv(pl, qp, kp, vp, 0.0)
+    s = st._c()
+    qs = (ctypes.c_int32 * 2)(0, 0)
+    ks = (ctypes.c_int32 * 2)(0, 1)
+    fl = (ctypes.c_uint32 * 2)(M.STEP_FIRST | M.STEP_BF16_MERGE, 0)
+    rc = M.lib().marble_attn_steps(pl.handle, ctypes.byref(c), 2, qs, ks, fl,
+                                   ctypes.byref(s), None)
+    assert rc == 1  # MARBLE_ERR_INVALID_ARG, nothing launched
