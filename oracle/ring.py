@@ -145,3 +145,17 @@ def ring_forward_bf16_merge(q, k, v, mask=None, P=4, step_order=None, scale=None
                 O[qs, h, :] = np.where(live[:, None], merged, O[qs, h, :])
                 lse[h, qs] = np.where(live, lse_new, lse_old)
     return O, lse
+
+
+def round_f32(x):
+    """Round to the nearest float32 (ties to even), returned as float64."""
+    return np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+
+
+def ring_forward_fp32_merge(q, k, v, mask=None, P=4, step_order=None, scale=None):
+    """The same per-step merge with fp32 in place of bf16 at both rounding points: every
+    call's output is an fp32 partial with its LSE and the partials are merged in fp32, the
+    route to exactness the MARBLE post gives for Blackwell's split-KV partials (section 03,
+    "Exact ring attention accumulation"; section 06).  Returns (O, LSE)."""
+    return ring_forward_bf16_merge(q, k, v, mask, P=P, step_order=step_order, scale=scale,
+                                   rounding=round_f32)

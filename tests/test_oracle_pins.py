@@ -557,3 +557,21 @@ def test_bf16_merge_masked_rows_and_error_gap():
     e_once = np.abs(ring.round_bf16(O) - O).mean()
     e_merge = np.abs(Ob - O).mean()
     assert e_merge > 1.2 * e_once
+
+
+def test_fp32_merge_is_exact_to_fp32_rounding():
+    # fp32 partials merged in fp32: the error against fp64 attention is a few fp32 ulps of
+    # the output, far below one bf16 rounding, for any P and step order
+    rng = np.random.default_rng(14)
+    n = 512
+    tr = wl.random_pack(rng, n)
+    M = mask.dense_mask(tr, INF)
+    q, k, v = _rand_qkv(rng, n, 2, 2, 32)
+    O, L = attention.forward(q, k, v, M)
+    fin = np.isfinite(L)
+    for P in (1, 4, 16):
+        order = [list(rng.permutation(P)) for _ in range(P)]
+        Of, Lf = ring.ring_forward_fp32_merge(q, k, v, M, P=P, step_order=order)
+        assert np.abs(Of - O).max() < 8 * 2.0**-24 * max(1.0, np.abs(O).max())
+        assert np.abs(Lf[fin] - L[fin]).max() < 1e-12
+    assert ring.round_f32(1 + 2.0**-24) == 1.0 and ring.round_f32(1 + 3 * 2.0**-24) == 1 + 2.0**-22
