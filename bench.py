@@ -84,10 +84,15 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
+            # the timed region starts once the sampler is producing rows
+            t0 = time.perf_counter()
+            while not self.rows and time.perf_counter() - t0 < 5.0:
+                time.sleep(0.01)
+            self.rows.clear()
         except Exception:
             self.proc = None
         return self
@@ -362,6 +367,25 @@ def run_marble(args, rank, world, local, dist):
                "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
                "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H"}
 
+    # the forward with each merge of the ring steps: the carried fp32 state (the timed step
+    # above), the merge of fp32 partials and the standard merge of bf16 partials
+    merge_ms = {}
+    for merge in ("carried", "fp32", "bf16"):
+        M.attn_steps(pl, qp, kp, vp, sched, st, merge=merge)
+        M.attn_finalize(pl, st, o, lse)
+        evs = [(ev(), ev()) for _ in range(3)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            M.attn_steps(pl, qp, kp, vp, sched, st, merge=merge)
+            M.attn_finalize(pl, st, o, lse)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        merge_ms[merge] = statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+    pl.check()
+    merge_variants = {"unit": "ms per forward pass (all ring steps + finalize), mean of 3",
+                      **{k_: round(v_, 3) for k_, v_ in merge_ms.items()},
+                      "tflops": {k_: flops_fwd / (v_ / 1e3) / 1e12 for k_, v_ in merge_ms.items()}}
+
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
         r, el, ns, tok = oracle_sample_rate(cfg, tr, args.cpu_budget)
@@ -390,6 +414,7 @@ def run_marble(args, rank, world, local, dist):
             "plan_ms": min(plan_ms), "plan_stats": stats,
             "wall_s_timed_region": t_wall,
             "roofline": roof,
+            "fwd_merge_variants": merge_variants,
             "cpu_baseline": cpu,
             "e2e": e2e,
             # our kernels in the timed region: attention launches counted by the library,
@@ -434,7 +459,7 @@ def run_profile_pass(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="marble", choices=["marble", "reference"])
     ap.add_argument("--config", type=int, default=2)

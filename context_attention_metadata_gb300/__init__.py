@@ -26,6 +26,8 @@ TILE_FULL, TILE_PARTIAL = 1, 2
 KV_NEEDED = -1
 STEP_FIRST = 1
 STEP_BF16_MERGE = 2  # standard ring merge in bf16 (the comparison baseline)
+STEP_FP32_MERGE = 4  # merge of fp32 partials by their LSE
+_MERGE = {None: 0, "carried": 0, "bf16": STEP_BF16_MERGE, "fp32": STEP_FP32_MERGE}
 ORDERS = {"contiguous": 0, "ptrr_block": 1, "ptrr_chunk": 2}
 FIELDS = {
     "perm": (0, "int32"), "block_perm": (1, "int32"), "tracks_perm": (2, "int32"),
@@ -250,18 +252,21 @@ def _qkv(plan, q, k, v, scale):
     return _QKV(q.data_ptr(), k.data_ptr(), v.data_ptr(), hq, hkv, d, float(scale))
 
 
-def _flags(first: bool, bf16_merge: bool) -> int:
-    return (STEP_FIRST if first else 0) | (STEP_BF16_MERGE if bf16_merge else 0)
+def _flags(first: bool, merge) -> int:
+    if merge not in _MERGE:
+        raise ValueError(f"merge must be one of {sorted(k for k in _MERGE if k)}")
+    return (STEP_FIRST if first else 0) | _MERGE[merge]
 
 
 def attn_step(plan: Plan, q, k, v, q_shard: int, kv_shard: int, state: State,
-              first: bool = False, scale: float = 0.0, stream=None, bf16_merge: bool = False):
-    """One forward ring step (marble_attn_step); ``bf16_merge`` selects the standard
-    bf16 per-step merge instead of the carried fp32 state."""
+              first: bool = False, scale: float = 0.0, stream=None, merge: str = "carried"):
+    """One forward ring step (marble_attn_step).  ``merge``: "carried" (the fp32 state
+    carried across steps), "bf16" (the standard per-step merge of bf16 partials) or "fp32"
+    (the same merge of fp32 partials)."""
     c = _qkv(plan, q, k, v, scale)
     st = state._c()
     _call("marble_attn_step", plan.handle, ctypes.byref(c), int(q_shard), int(kv_shard),
-          ctypes.byref(st), _flags(first, bf16_merge), _stream(stream))
+          ctypes.byref(st), _flags(first, merge), _stream(stream))
 
 
 def attn_finalize(plan: Plan, state: State, o, lse, stream=None):
@@ -355,14 +360,14 @@ def ring_schedule(num_shards: int, needed: bool = False):
 
 
 def attn_steps(plan: Plan, q, k, v, schedule, state: State, scale: float = 0.0, stream=None,
-               bf16_merge: bool = False):
+               merge: str = "carried"):
     """A list of forward ring steps [(q_shard, kv_shard, first), ...] in one C call."""
     c = _qkv(plan, q, k, v, scale)
     st = state._c()
     n = len(schedule)
     qs = (ctypes.c_int32 * n)(*[int(r) for r, _, _ in schedule])
     ks = (ctypes.c_int32 * n)(*[int(j) for _, j, _ in schedule])
-    fl = (ctypes.c_uint32 * n)(*[_flags(f, bf16_merge) for _, _, f in schedule])
+    fl = (ctypes.c_uint32 * n)(*[_flags(f, merge) for _, _, f in schedule])
     _call("marble_attn_steps", plan.handle, ctypes.byref(c), n, qs, ks, fl, ctypes.byref(st),
           _stream(stream))
 
@@ -386,10 +391,10 @@ def attn_bwd_steps(plan: Plan, q, k, v, do, lse, delta, schedule, dq_acc, dk_acc
 
 
 def forward(plan: Plan, q, k, v, state: State, o, lse, needed: bool = False, scale: float = 0.0,
-            stream=None, bf16_merge: bool = False):
+            stream=None, merge: str = "carried"):
     """All forward ring steps (r-major, keeping shard r's state hot in L2) + finalize."""
     attn_steps(plan, q, k, v, ring_schedule(plan.num_shards, needed), state, scale=scale,
-               stream=stream, bf16_merge=bf16_merge)
+               stream=stream, merge=merge)
     attn_finalize(plan, state, o, lse, stream=stream)
 
 

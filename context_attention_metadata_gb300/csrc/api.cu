@@ -342,6 +342,13 @@ MARBLE_API marble_status_t marble_permute(const marble_plan_t* p, const void* sr
   return MARBLE_OK;
 }
 
+constexpr uint32_t kMergeBits = MARBLE_STEP_BF16_MERGE | MARBLE_STEP_FP32_MERGE;
+
+// known bits only, and at most one merge variant
+static bool step_flags_ok(uint32_t f) {
+  return !(f & ~(MARBLE_STEP_FIRST | kMergeBits)) && (f & kMergeBits) != kMergeBits;
+}
+
 MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble_qkv_t* qkv,
                                             int32_t q_shard, int32_t kv_shard,
                                             const marble_state_t* state, uint32_t flags,
@@ -353,7 +360,7 @@ MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble
   if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
-  if (flags & ~(MARBLE_STEP_FIRST | MARBLE_STEP_BF16_MERGE)) return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
+  if (!step_flags_ok(flags)) return fail(MARBLE_ERR_INVALID_ARG, "unknown or conflicting flags");
   return run_attn_fwd(p, qkv, 1, &q_shard, &kv_shard, &flags, state, (cudaStream_t)stream);
 }
 
@@ -380,10 +387,10 @@ MARBLE_API marble_status_t marble_attn_steps(const marble_plan_t* p, const marbl
   if ((st = check_step_list(p, n_steps, q_shards, kv_shards)) != MARBLE_OK) return st;
   if (n_steps > 0 && !flags) return fail(MARBLE_ERR_INVALID_ARG, "flags must be non-null");
   for (int32_t i = 0; i < n_steps; ++i) {
-    if (flags[i] & ~(MARBLE_STEP_FIRST | MARBLE_STEP_BF16_MERGE))
-      return fail(MARBLE_ERR_INVALID_ARG, "unknown flags");
-    if ((flags[i] ^ flags[0]) & MARBLE_STEP_BF16_MERGE)
-      return fail(MARBLE_ERR_INVALID_ARG, "MARBLE_STEP_BF16_MERGE differs between steps");
+    if (!step_flags_ok(flags[i]))
+      return fail(MARBLE_ERR_INVALID_ARG, "unknown or conflicting flags");
+    if ((flags[i] ^ flags[0]) & kMergeBits)
+      return fail(MARBLE_ERR_INVALID_ARG, "the merge flags differ between steps");
   }
   if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;

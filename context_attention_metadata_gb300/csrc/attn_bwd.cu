@@ -40,8 +40,9 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 352;  // producer, MMA, 8 elementwise warps, scheduler
+constexpr int kThreads = 384;  // producer, MMA, 8 elementwise warps, scheduler, dS store
 constexpr int kWarpSched = 10;
+constexpr int kWarpStore = 11;
 constexpr int kQueue = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -411,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
   __shared__ int epi_count;
+  __shared__ long long ds_mail[2];  // per half: scratch slot of the staged dS^T (-1: no more)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long n = p.n;
@@ -603,6 +605,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       drain_wait(&bar[K_DRAIN], 0, p.wait_ns, p.err);
     }
     __syncwarp();
+  } else if (warp == kWarpStore) {
+    // ------------------------------------------------------------------ dS^T store
+    // one thread writes the staged dS^T boxes to the scratch in the order the halves use the
+    // box (half 0 of item g, half 1 of item g, half 0 of item g + 1, ...), so that no
+    // elementwise warp waits for a TMA to read shared memory
+    if (lane == 0) {
+      bool more = true;
+      for (int g = 0; more; ++g) {
+        for (int half = 0; half < 2 && more; ++half) {
+          if (!mbar_wait(&bar[K_DSSTG0 + half], (uint32_t)(g & 1), w)) {
+            more = false;
+            break;
+          }
+          const long long slot_ds = ds_mail[half];
+          if (slot_ds < 0) {
+            more = false;
+            break;
+          }
+          tma_store_3d(&p.ds_map, sDS, half * 64, (int)(slot_ds * 128), 0);
+          bulk_commit();
+          bulk_wait_read_all();
+          mbar_arrive(&bar[K_DSFREE0 + half]);
+        }
+      }
+      // the global writes of every store this thread issued have completed
+      bulk_wait_all();
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ elementwise
     // four warps per half: `half` owns q columns [64 half, 64 half + 64), one kv row a thread
@@ -618,7 +648,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       const int slot = uc % kQueue;
       if (!wait_all(&bar[K_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
       const int kh = queue.head[slot];
-      if (kh < 0) break;
+      if (kh < 0) {
+        // no more work: half 0 posts the end of the dS^T stores once its last one is read
+        if (half == 0) {
+          if (row == 0) {
+            if (g >= 1) mbar_wait(&bar[K_DSFREE0], (uint32_t)((g - 1) & 1), w);
+            ds_mail[0] = -1;
+          }
+          mbar_arrive(&bar[K_DSSTG0]);
+        }
+        break;
+      }
       const int64_t nk = queue.blk[slot];
       const int L = queue.T[slot];
       const int64_t c0 = queue.e0[slot];
@@ -729,22 +769,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
                 make_uint4(src[0], src[1], src[2], src[3]);
           }
         }
+        if (row == 0) {
+          // the tile's scratch slot: the step's tiles in row-list order, q heads innermost
+          const int64_t nq = p.colT_row[e];
+          const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
+          int64_t jj = p.colT_j[e];
+          if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
+          ds_mail[half] = p.ds_slot0 + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
+        }
         fence_proxy_async_smem();
         mbar_arrive(&bar[K_DSSTG0 + half]);
-        if (row == 0) {
-          if (mbar_wait(&bar[K_DSSTG0 + half], g & 1, w)) {
-            const int64_t nq = p.colT_row[e];
-            const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
-            int64_t jj = p.colT_j[e];
-            if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
-            const int64_t slot_ds =
-                p.ds_slot0 + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
-            tma_store_3d(&p.ds_map, sDS, half * 64, (int)(slot_ds * 128), 0);
-            bulk_commit();
-            bulk_wait_read_all();
-          }
-          mbar_arrive(&bar[K_DSFREE0 + half]);
-        }
       }
       if (!ok) break;
       // ---- the unit's dV and dK (dv_acc += dV, dk_acc += scale * dK): round 0 stages this

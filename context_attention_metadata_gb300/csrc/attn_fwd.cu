@@ -103,7 +103,7 @@ struct FwdParams {
   int nwork;  // units with at least one tile: nonempty blocks of the order x hq
   int W;
   int first;
-  int bf16_merge;  // standard ring merge: bf16 partials and running output, running LSE
+  int lse_merge;   // 0 carried state; 1 merge of bf16 partials (standard ring); 2 of fp32 ones
   float scale_log2;
 };
 
@@ -564,11 +564,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
     //                 O_call * 2^(m_call - m_stored): a TMA fp32 reduce-add, no load;
     //   some row grew exact merge with the stored tile (loaded by the row threads), then a
     //                 TMA store.
-    //   bf16 merge    the standard ring-attention merge kept for comparison: the call's
-    //                 output is normalised and rounded to bf16, merged with the stored
-    //                 (bf16-valued) output by the log-sum-exp weights and rounded to bf16
-    //                 again; m then holds the running base-2 LSE and l is 1 (0 for a row
-    //                 that has seen no legal key), which the finalize reads unchanged.
+    //   LSE merge     the call's output is normalised into a partial, merged with the
+    //                 stored (normalised) output by log-sum-exp weights and stored; m then
+    //                 holds the running base-2 LSE and l is 1 (0 for a row that has seen no
+    //                 legal key), which the finalize reads unchanged.  Partial and merged
+    //                 output are rounded to bf16 (the standard ring merge, kept for
+    //                 comparison) or kept in fp32 (merging fp32 partials: exact to fp32).
     int uc = 0, k = 0;  // units merged, staging rounds
     bool ok = true;
     while (ok) {
@@ -595,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
       if (__any_sync(0xffffffffu, grows) && lane == 0) atomicOr(&epi_mode[uc & 1], 1);
       mbar_arrive(&bar[B_EVOTE]);
       if (!wait_all(&bar[B_EVOTE], uc & 1, w)) break;
-      const int mode = p.bf16_merge ? 3 : p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
+      const int mode = p.lse_merge ? 3 : p.first ? 0 : (epi_mode[uc & 1] ? 2 : 1);
       // every epilogue thread has read the other flag (before this vote), and none can vote
       // on the next unit before row 0 has passed its first staging round of this one
       if (row == 0) epi_mode[(uc + 1) & 1] = 0;
@@ -641,10 +642,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         }
         float vals[32];
         if (mode == 3) {
-          // bf16(O_old * a_old + bf16(O_call / l_call) * a_new)
+          // rnd(O_old * a_old + rnd(O_call / l_call) * a_new), rnd = bf16 rounding or none
           const float inv_l = l_run > 0.f ? 1.f / l_run : 0.f;
+          const bool rb = p.lse_merge == 1;
 #pragma unroll
-          for (int t = 0; t < 32; ++t) vals[t] = bf16_round(__uint_as_float(x[t]) * inv_l) * a_new;
+          for (int t = 0; t < 32; ++t) {
+            const float o = __uint_as_float(x[t]) * inv_l;
+            vals[t] = (rb ? bf16_round(o) : o) * a_new;
+          }
           if (!p.first) {
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
@@ -655,8 +660,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
               vals[4 * t + 3] = fmaf(o.w, a_old, vals[4 * t + 3]);
             }
           }
+          if (rb) {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) vals[t] = bf16_round(vals[t]);
+            for (int t = 0; t < 32; ++t) vals[t] = bf16_round(vals[t]);
+          }
         } else {
 #pragma unroll
           for (int t = 0; t < 32; ++t) vals[t] = __uint_as_float(x[t]) * a_new;
@@ -777,7 +784,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
     prm.first = (flags[i] & MARBLE_STEP_FIRST) ? 1 : 0;
-    prm.bf16_merge = (flags[i] & MARBLE_STEP_BF16_MERGE) ? 1 : 0;
+    prm.lse_merge = (flags[i] & MARBLE_STEP_BF16_MERGE) ? 1 : (flags[i] & MARBLE_STEP_FP32_MERGE) ? 2 : 0;
     const int64_t seg = (int64_t)prm.q_shard * (pl->P + 1) + (prm.kv_shard >= 0 ? prm.kv_shard : pl->P);
     prm.order = pl->fwd_order + seg * pl->bps;
     prm.nwork = pl->h_fwd_nwork[seg] * qkv->hq;

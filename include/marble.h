@@ -75,6 +75,7 @@ typedef enum {
 #define MARBLE_KV_NEEDED (-1)          /* kv_shard value: every needed KV block at once */
 #define MARBLE_STEP_FIRST 1u           /* flags bit: this is the first step of the rows */
 #define MARBLE_STEP_BF16_MERGE 2u      /* flags bit: standard ring merge in bf16 (baseline) */
+#define MARBLE_STEP_FP32_MERGE 4u      /* flags bit: merge of fp32 partials by their LSE */
 
 typedef enum {
   MARBLE_ORDER_CONTIGUOUS = 0, /* identity order: shard r = contiguous token range */
@@ -229,8 +230,13 @@ typedef struct {
  * and rounded to bf16, then merged with the stored output by log-sum-exp weights and
  * rounded to bf16 again.  O_acc then holds bf16-representable values, m the running
  * log-sum-exp in base 2 (ln -> log2) and l = 1 (0 while a row has seen no legal key), so
- * that marble_attn_finalize gives O and LSE unchanged.  Every step of a pass over the
- * same rows must carry the same setting of this bit.
+ * that marble_attn_finalize gives O and LSE unchanged.
+ * flags & MARBLE_STEP_FP32_MERGE: the same merge with no rounding: each step's output is an
+ * fp32 partial with its LSE and the partials are merged in fp32 (MARBLE s03 and s06: the
+ * route to exactness through fp32 split-KV partials).  O_acc holds the normalised fp32
+ * output, m and l as above.
+ * At most one of the two merge bits may be set, and every step of a pass over the same rows
+ * must carry the same merge bits.
  * Errors: INVALID_ARG (shard out of range, null/misaligned pointer, d not 64/128,
  * hq % hkv != 0), CUDA.
  */

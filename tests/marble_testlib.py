@@ -25,7 +25,7 @@ def plan_for(cfg, tr):
     return make_plan(tr, cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens)
 
 
-def run_forward(pl, q, k, v, needed=False, schedule=None, bf16_merge=False):
+def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried"):
     """q/k/v in ORIGINAL order on the GPU.  Returns (O, LSE, state) with O [N, hq, d]
     and LSE [hq, N] in original order and the raw state in plan order."""
     n, hq, d = q.shape
@@ -34,10 +34,10 @@ def run_forward(pl, q, k, v, needed=False, schedule=None, bf16_merge=False):
     o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
     if schedule is None:
-        M.forward(pl, qp, kp, vp, st, o, lse, needed=needed, bf16_merge=bf16_merge)
+        M.forward(pl, qp, kp, vp, st, o, lse, needed=needed, merge=merge)
     else:
         for r, j, first in schedule:
-            M.attn_step(pl, qp, kp, vp, r, j, st, first=first, bf16_merge=bf16_merge)
+            M.attn_step(pl, qp, kp, vp, r, j, st, first=first, merge=merge)
         M.attn_finalize(pl, st, o, lse)
     pl.check()
     perm = pl.export("perm").long()

@@ -75,10 +75,12 @@ def _canonical(st, n):
     return on, lse
 
 
-def test_state_is_invariant_to_P_and_step_order():
+@pytest.mark.parametrize("merge", ["carried", "fp32"])
+def test_state_is_invariant_to_P_and_step_order(merge):
     """MARBLE s03: the online kernel's results equal a single GPU's at every ring degree.
     The carried fp32 state (canonicalised as O_acc / l and m + log l) agrees across
-    P in {1, 2, 4, 8, 16} and under a shuffled step order to 1e-5 relative."""
+    P in {1, 2, 4, 8, 16} and under a shuffled step order to 1e-5 relative; so does the
+    state of the merge of fp32 partials (O_acc normalised, l = 1, m the base-2 LSE)."""
     cfg = wl.CONFIGS[1]
     tr = wl.config_tracks(1)
     q, k, v = _qkv(cfg.n, cfg.hq, cfg.hkv, cfg.d)
@@ -93,7 +95,7 @@ def test_state_is_invariant_to_P_and_step_order():
                 for r in range(P):
                     js = list(rng.permutation(P))
                     sched += [(r, int(j), s == 0) for s, j in enumerate(js)]
-            _, _, st = run_forward(pl, q, k, v, schedule=sched)
+            _, _, st = run_forward(pl, q, k, v, schedule=sched, merge=merge)
             on, lse = _canonical(st, cfg.n)  # contiguous order: plan order = original
             if ref is None:
                 ref = (on, lse)
@@ -170,7 +172,7 @@ def test_bf16_merge_matches_its_oracle():
     # weights) in the same ring order and on the same plan-ordered shards as the oracle
     cfg, tr, q, k, v = _bf16_merge_case()
     pl = plan_for(cfg, tr)
-    O, L, st = run_forward(pl, q, k, v, bf16_merge=True)
+    O, L, st = run_forward(pl, q, k, v, merge="bf16")
     perm = pl.export("perm").long().cpu().numpy()
     Mp = mask.dense_mask(tr, cfg.window, rows=perm, cols=perm)  # plan order, original positions
     Ob, Lb = ring.ring_forward_bf16_merge(q.cpu()[perm], k.cpu()[perm], v.cpu()[perm], Mp,
@@ -189,7 +191,7 @@ def test_bf16_merge_single_pass_is_rounded_exact():
     # needed-block mode runs one call per q shard: one rounded partial, nothing to merge
     cfg, tr, q, k, v = _bf16_merge_case(n=4096, seed=22)
     pl = plan_for(cfg, tr)
-    O, L, _ = run_forward(pl, q, k, v, needed=True, bf16_merge=True)
+    O, L, _ = run_forward(pl, q, k, v, needed=True, merge="bf16")
     Oref, Lref = _dense_ref(tr, cfg.window, q, k, v)
     check_o_lse(O, L, ring.round_bf16(Oref), Lref)
 
@@ -200,7 +202,7 @@ def test_bf16_merge_error_exceeds_carried_fp32():
     pl = plan_for(cfg, tr)
     Oref, _ = _dense_ref(tr, cfg.window, q, k, v)
     O32, _, _ = run_forward(pl, q, k, v)
-    O16, _, _ = run_forward(pl, q, k, v, bf16_merge=True)
+    O16, _, _ = run_forward(pl, q, k, v, merge="bf16")
     e32 = np.abs(O32.float().cpu().numpy() - Oref).mean()
     e16 = np.abs(O16.float().cpu().numpy() - Oref).mean()
     print(f"mean |O - O_exact|: carried fp32 {e32:.3e}, bf16 merge {e16:.3e}, "
@@ -222,3 +224,54 @@ def test_bf16_merge_flag_is_uniform_per_call():
     rc = M.lib().marble_attn_steps(pl.handle, ctypes.byref(c), 2, qs, ks, fl,
                                    ctypes.byref(s), None)
     assert rc == 1  # MARBLE_ERR_INVALID_ARG, nothing launched
+
+
+@pytest.mark.parametrize("cid", [2, 3, 5])
+def test_fp32_merge_matches_exact(cid):
+    # the merge of fp32 partials is exact to fp32: same bar as the carried state against the
+    # fp64 oracle, and within one bf16 step of the carried state's output
+    cfg = wl.mini_config(cid, 8192, hq=2)
+    tr = wl.config_tracks(cid, cfg.n)
+    q, k, v = _qkv(cfg.n, cfg.hq, cfg.hkv, cfg.d, seed=30 + cid)
+    pl = plan_for(cfg, tr)
+    O, L, _ = run_forward(pl, q, k, v, merge="fp32", needed=cfg.needed)
+    Oref, Lref = _dense_ref(tr, cfg.window, q, k, v)
+    check_o_lse(O, L, Oref, Lref)
+    Oc, Lc, _ = run_forward(pl, q, k, v, needed=cfg.needed)
+    assert ((O.float() - Oc.float()).abs() <= 2.0**-7 * Oc.float().abs().clamp(min=1)).all()
+    fin = torch.isfinite(Lc)
+    assert torch.equal(torch.isfinite(L), fin)
+    assert (L[fin] - Lc[fin]).abs().max() <= 1e-4
+
+
+def test_fp32_merge_error_matches_carried_and_beats_bf16():
+    cfg, tr, q, k, v = _bf16_merge_case(seed=25)
+    pl = plan_for(cfg, tr)
+    Oref, _ = _dense_ref(tr, cfg.window, q, k, v)
+    err = {}
+    for merge in ("carried", "fp32", "bf16"):
+        O, _, _ = run_forward(pl, q, k, v, merge=merge)
+        err[merge] = np.abs(O.float().cpu().numpy() - Oref).mean()
+    print("mean |O - O_exact|:", {k_: f"{v_:.3e}" for k_, v_ in err.items()})
+    assert abs(err["fp32"] / err["carried"] - 1) < 0.05
+    assert err["bf16"] > 1.05 * err["fp32"]
+
+
+def test_merge_flags_are_checked():
+    import ctypes
+    cfg, tr, q, k, v = _bf16_merge_case(n=2048, seed=26)
+    pl = plan_for(cfg, tr)
+    st = M.State(cfg.n, cfg.hq, cfg.d)
+    qp, kp, vp = pl.permute(q), pl.permute(k), pl.permute(v)
+    c = M._qkv(pl, qp, kp, vp, 0.0)
+    s_ = st._c()
+    both = M.STEP_FIRST | M.STEP_BF16_MERGE | M.STEP_FP32_MERGE
+    assert M.lib().marble_attn_step(pl.handle, ctypes.byref(c), 0, 0, ctypes.byref(s_),
+                                    both, None) == 1
+    qs = (ctypes.c_int32 * 2)(0, 0)
+    ks = (ctypes.c_int32 * 2)(0, 1)
+    fl = (ctypes.c_uint32 * 2)(M.STEP_FIRST | M.STEP_FP32_MERGE, M.STEP_BF16_MERGE)
+    assert M.lib().marble_attn_steps(pl.handle, ctypes.byref(c), 2, qs, ks, fl,
+                                     ctypes.byref(s_), None) == 1
+    with pytest.raises(ValueError):
+        M.attn_step(pl, qp, kp, vp, 0, 0, st, first=True, merge="fp16")
