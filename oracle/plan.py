@@ -7,7 +7,9 @@ Sources (MARBLE post):
     *partial* otherwise.  One test per block pair.
   * section 03 "PTRR": sort query blocks by cost, deal them to ranks in rounds of R with
     every other round reversed, keep each rank's blocks in sequence order.
-  * section 03 "Chunked ring attention": PTRR's rule applied to contiguous chunks.
+  * section 03 "Chunked ring attention": PTRR's rule applied to contiguous chunks, and the
+    layout search over the number of chunks per rank that minimises the layout cost
+    C = sum_s max_r W[r, (r - s) mod R] + tau * R * k (W in legal pairs).
   * section 03 "Block classification" (ring steps): at step s, rank r pairs its queries
     with the key/value shard of rank (r - s) mod R.
   * section 04 "Sparse all-to-all": each rank needs exactly the key/value blocks its
@@ -45,7 +47,7 @@ from typing import Dict, List
 
 import numpy as np
 
-from .mask import tracks_with_pos
+from .mask import dense_mask, tracks_with_pos
 
 BLOCK = 128
 EMPTY, FULL, PARTIAL = 0, 1, 2
@@ -173,7 +175,7 @@ class Plan:
     needed: np.ndarray       # sorted unique new kv blocks per q shard
 
 
-def make_plan(tr, W, P, order="contiguous", chunk_tokens=0) -> Plan:
+def make_plan(tr, W, P, order="contiguous", chunk_tokens=0, range_cost=0) -> Plan:
     summ = block_summaries(tr)
     nb = len(summ["slo"])
     if nb % P:
@@ -194,6 +196,10 @@ def make_plan(tr, W, P, order="contiguous", chunk_tokens=0) -> Plan:
         unit_blocks = chunk_tokens // BLOCK
         ccost = cost.reshape(-1, unit_blocks).sum(1)
         units_of_rank = ptrr_assign(ccost, P)
+    elif order == "chunk_search":
+        _, k, rank, _ = chunk_search(block_pair_counts(tr, W), P, range_cost)
+        unit_blocks = nb // (k * P)
+        units_of_rank = [[u for u in range(k * P) if rank[u] == r] for r in range(P)]
     else:
         raise ValueError(order)
 
@@ -255,3 +261,91 @@ def step_cost(plan: Plan) -> int:
     Wm = shard_work(plan)
     P = plan.P
     return int(sum(max(Wm[r, (r - s) % P] for r in range(P)) for s in range(P)))
+
+
+# --------------------------------------------------------------------------------------
+# chunk-layout search (chunked ring attention)
+# --------------------------------------------------------------------------------------
+CHUNKS_PER_RANK = (1, 2, 4, 8, 16, 32, 64)
+MAX_CHUNKS = 1024        # the search skips chunk counts above this many chunks in all
+MAX_SWAP_PASSES = 64     # greedy-swap passes per chunk count at most
+
+
+def block_pair_counts(tr, W) -> np.ndarray:
+    """[nb, nb] legal (q, k) pairs between every q block and kv block (original order):
+    128 * 128 on full tiles, counted from the explicit mask on partial ones."""
+    summ = block_summaries(tr)
+    nb = len(summ["slo"])
+    row_ptr, col, tag = tile_csr(summ, W)
+    out = np.zeros((nb, nb), np.int64)
+    for a in range(nb):
+        for e in range(row_ptr[a], row_ptr[a + 1]):
+            b = int(col[e])
+            if tag[e] == 1:
+                out[a, b] = BLOCK * BLOCK
+            else:
+                rows = np.arange(a * BLOCK, (a + 1) * BLOCK)
+                cols = np.arange(b * BLOCK, (b + 1) * BLOCK)
+                out[a, b] = int(dense_mask(tr, W, rows, cols).sum())
+    return out
+
+
+def layout_step_cost(Wc, rank, P) -> int:
+    """sum over steps s of max over ranks r of W[r, (r - s) mod P], where W[r, j] sums the
+    chunk-pair work Wc[a, b] over chunks a of rank r and b of rank j (MARBLE post,
+    section 03 "Chunked ring attention": the first term of the layout cost C)."""
+    rank = np.asarray(rank)
+    Wr = np.zeros((P, P), np.int64)
+    np.add.at(Wr, (rank[:, None], rank[None, :]), Wc)
+    return int(sum(max(Wr[r, (r - s) % P] for r in range(P)) for s in range(P)))
+
+
+def chunk_search(Wb, P, tau):
+    """The chunked ring's layout search (MARBLE post, section 03 "Chunked ring attention"):
+    for 1, 2, 4, ..., 64 chunks per rank (chunk counts that divide the blocks evenly and
+    stay within MAX_CHUNKS), deal the contiguous chunks to ranks with PTRR's rule once in
+    the order of their work (legal pairs of their queries) and once in sequence order,
+    start from the layout with the lower step cost (the work order on a tie), then swap
+    chunks between ranks whenever that strictly lowers the step cost: passes over the chunk
+    pairs (a, b), a < b, in ascending order, first improvement taken, until a pass makes no
+    swap (MAX_SWAP_PASSES at most).  The layout costs C = step cost + tau * P * k with k
+    chunks per rank; the lowest C wins (the fewer chunks on a tie).
+
+    Wb: [nb, nb] legal pairs between blocks.  Returns (C, k, rank of every chunk,
+    step cost)."""
+    nb = Wb.shape[0]
+    best = None
+    for k in CHUNKS_PER_RANK:
+        K = k * P
+        if K > nb or nb % K or K > MAX_CHUNKS:
+            continue
+        cs = nb // K
+        Wc = Wb.reshape(K, cs, K, cs).sum(axis=(1, 3))
+        starts = []
+        for costs in (Wc.sum(axis=1), np.zeros(K, np.int64)):
+            rank = np.empty(K, np.int64)
+            for r, units in enumerate(ptrr_assign(costs, P)):
+                rank[units] = r
+            starts.append((layout_step_cost(Wc, rank, P), rank))
+        cur, rank = starts[0] if starts[0][0] <= starts[1][0] else starts[1]
+        rank = rank.copy()
+        for _ in range(MAX_SWAP_PASSES):
+            swapped = False
+            for a in range(K):
+                for b in range(a + 1, K):
+                    if rank[a] == rank[b]:
+                        continue
+                    rank[a], rank[b] = rank[b], rank[a]
+                    c = layout_step_cost(Wc, rank, P)
+                    if c < cur:
+                        cur, swapped = c, True
+                    else:
+                        rank[a], rank[b] = rank[b], rank[a]
+            if not swapped:
+                break
+        C = cur + tau * P * k
+        if best is None or C < best[0]:
+            best = (C, k, rank.copy(), cur)
+    if best is None:
+        raise ValueError("no chunk count divides the blocks evenly")
+    return best

@@ -575,3 +575,90 @@ def test_fp32_merge_is_exact_to_fp32_rounding():
         assert np.abs(Of - O).max() < 8 * 2.0**-24 * max(1.0, np.abs(O).max())
         assert np.abs(Lf[fin] - L[fin]).max() < 1e-12
     assert ring.round_f32(1 + 2.0**-24) == 1.0 and ring.round_f32(1 + 3 * 2.0**-24) == 1 + 2.0**-22
+
+
+def test_layout_step_cost_by_hand_and_brute_force():
+    # P = 2, one chunk per rank: W = Wc, steps s = 0 (diagonal) and s = 1 (off-diagonal)
+    Wc = np.array([[5, 7], [2, 9]])
+    assert plan.layout_step_cost(Wc, [0, 1], 2) == max(5, 9) + max(7, 2)
+    assert plan.layout_step_cost(Wc, [1, 0], 2) == max(9, 5) + max(2, 7)
+    rng = np.random.default_rng(20)
+    for P in (2, 3, 4):
+        K = 3 * P
+        Wc = rng.integers(0, 1000, (K, K))
+        rank = rng.permutation(np.repeat(np.arange(P), 3))
+        Wr = [[sum(int(Wc[a, b]) for a in range(K) for b in range(K)
+                   if rank[a] == r and rank[b] == j) for j in range(P)] for r in range(P)]
+        want = sum(max(Wr[r][(r - s) % P] for r in range(P)) for s in range(P))
+        assert plan.layout_step_cost(Wc, rank, P) == want
+
+
+def _search_case(seed, nblocks=64, P=4):
+    rng = np.random.default_rng(seed)
+    tr = wl.random_pack(rng, nblocks * 128, max_samples=5)
+    return tr, plan.block_pair_counts(tr, INF), P
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_chunk_search_is_a_local_optimum_below_both_starts(seed):
+    tr, Wb, P = _search_case(seed)
+    assert Wb.sum() == counts.by_brute_force(tr, INF)
+    C, k, rank, cost = plan.chunk_search(Wb, P, tau=1000)
+    K = k * P
+    assert C == cost + 1000 * P * k
+    assert sorted(np.bincount(rank, minlength=P)) == [k] * P
+    cs = Wb.shape[0] // K
+    Wc = Wb.reshape(K, cs, K, cs).sum(axis=(1, 3))
+    assert plan.layout_step_cost(Wc, rank, P) == cost
+    # no single swap between ranks lowers the step cost
+    for a in range(K):
+        for b in range(a + 1, K):
+            if rank[a] != rank[b]:
+                r2 = rank.copy()
+                r2[a], r2[b] = r2[b], r2[a]
+                assert plan.layout_step_cost(Wc, r2, P) >= cost
+    # and it is no worse than either PTRR start
+    for costs in (Wc.sum(axis=1), np.zeros(K)):
+        r0 = np.empty(K, np.int64)
+        for r, units in enumerate(plan.ptrr_assign(costs, P)):
+            r0[units] = r
+        assert cost <= plan.layout_step_cost(Wc, r0, P)
+
+
+def test_chunk_search_range_cost_trades_chunks():
+    tr, Wb, P = _search_case(3)
+    # no per-range cost: the best step cost over all chunk counts; a huge one: one chunk
+    C0, k0, _, cost0 = plan.chunk_search(Wb, P, tau=0)
+    assert C0 == cost0
+    C1, k1, _, _ = plan.chunk_search(Wb, P, tau=10**12)
+    assert k1 == 1
+    # uniform work (one bidirectional sample): every layout costs P * (nb / P)^2 * 128^2
+    samples = [[wl.Span("full", 64 * 128)]]
+    tru = wl.tracks_from_samples(samples)
+    Wu = plan.block_pair_counts(tru, INF)
+    assert (Wu == 128 * 128).all()
+    Cu, ku, _, costu = plan.chunk_search(Wu, 4, tau=0)
+    assert costu == 4 * 16 * 16 * 128 * 128 and ku == 1
+
+
+def test_chunk_search_plan_realises_the_searched_cost():
+    # the plan built from the search's layout has exactly the searched step cost when its
+    # shard work is summed in legal pairs from its own step lists
+    tr, Wb, P = _search_case(4)
+    tau = 5000
+    C, k, rank, cost = plan.chunk_search(Wb, P, tau)
+    pl = plan.make_plan(tr, INF, P, "chunk_search", range_cost=tau)
+    nb, bps = pl.nb, pl.nb // P
+    Wr = np.zeros((P, P), np.int64)
+    for nq in range(nb):
+        for j in range(P):
+            for e in range(pl.step_ptr[nq * P + j], pl.step_ptr[nq * P + j + 1]):
+                Wr[nq // bps, j] += Wb[pl.block_perm[nq], pl.block_perm[pl.step_col[e]]]
+    assert sum(max(Wr[r, (r - s) % P] for r in range(P)) for s in range(P)) == cost
+    # each rank holds k contiguous chunks, ascending
+    cs = nb // (k * P)
+    chunks = pl.block_perm.reshape(-1, cs)
+    assert (np.diff(chunks, axis=1) == 1).all() and (chunks[:, 0] % cs == 0).all()
+    for r in range(P):
+        mine = chunks[r * k:(r + 1) * k, 0] // cs
+        assert (np.diff(mine) > 0).all() and (rank[mine] == r).all()
