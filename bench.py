@@ -145,11 +145,12 @@ def oracle_sample_rate(cfg, tr, budget_s: float, seed: int = 0):
     tokens = 0
     nsamp = 0
     elapsed = 0.0
-    for sid in order:
-        idx = np.flatnonzero(st == sid)
+    small = [sid for sid in order if np.count_nonzero(st == sid) <= 4096]
+    for sid in (small or order[:1]):
+        # whole samples of at most 4096 tokens; a pack without any: the first 4096 tokens of
+        # one sample (its mask restricted to them is the same predicate on those tokens)
+        idx = np.flatnonzero(st == sid)[:4096]
         L = len(idx)
-        if L > 4096:
-            continue
         sub = {k: np.asarray(v)[idx] for k, v in tr.items()}
         sub["pos"] = idx
         q = torch.randn((L, cfg.hq, cfg.d), generator=g).to(torch.bfloat16)
@@ -168,13 +169,30 @@ def oracle_sample_rate(cfg, tr, budget_s: float, seed: int = 0):
     return flops / elapsed / 1e12, elapsed, nsamp, tokens
 
 
+def workload(args):
+    """The configuration and tracks the command line asks for: one of the numbered
+    workloads, optionally a smaller pack of its recipe (--tokens) and another token order
+    (--order, --chunk-tokens, --range-cost)."""
+    import dataclasses
+    import workloads as wl
+    cid = args.config
+    base = wl.CONFIGS[cid] if cid in wl.CONFIGS else wl.EXTRA[cid]
+    cfg = base if args.tokens <= 0 else wl.mini_config(cid, args.tokens, hq=base.hq)
+    if args.order:
+        cfg = dataclasses.replace(cfg, order=args.order, chunk_tokens=args.chunk_tokens,
+                                  range_cost=args.range_cost,
+                                  name=f"{cfg.name}_{args.order}")
+    elif args.range_cost:
+        cfg = dataclasses.replace(cfg, range_cost=args.range_cost)
+    tr = wl.config_tracks(cid) if args.tokens <= 0 else wl.config_tracks(cid, cfg.n)
+    return cfg, tr
+
+
 def run_reference(args, rank, world, dist):
     """The oracle as it stands, timed on the host cores (rank 0 only)."""
-    import workloads as wl
-    cfg = wl.CONFIGS[args.config]
+    cfg, tr = workload(args)
     if rank != 0:
         return
-    tr = wl.config_tracks(args.config)
     for _ in range(args.warmup):
         oracle_sample_rate(cfg, tr, args.ref_budget)
     rates, times = [], []
@@ -214,10 +232,9 @@ def run_marble(args, rank, world, local, dist):
 
     torch.cuda.set_device(local)
     _build.build()
-    cfg = wl.CONFIGS[args.config]
+    cfg, tr = workload(args)
     n, hq, hkv, d, P = cfg.n, cfg.hq, cfg.hkv, cfg.d, cfg.shards
     needed = cfg.needed
-    tr = wl.config_tracks(args.config)
     trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
     stream = torch.cuda.current_stream()
 
@@ -229,7 +246,8 @@ def run_marble(args, rank, world, local, dist):
             pl.close()
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens)
+        pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens,
+                    range_cost=cfg.range_cost)
         torch.cuda.synchronize()
         plan_ms.append(1e3 * (time.perf_counter() - t0))
     stats = pl.stats()
@@ -339,7 +357,7 @@ def run_marble(args, rank, world, local, dist):
             for dst, src in zip(dev_in + dev_tr, hq_pin + htr):
                 dst.copy_(src, non_blocking=True)
             p2 = M.Plan(dev_tr[0], dev_tr[1], dev_tr[2], cfg.window, P, cfg.order,
-                        cfg.chunk_tokens)
+                        cfg.chunk_tokens, range_cost=cfg.range_cost)
             q2, k2, v2, do2 = (p2.permute(t) for t in dev_in)
             M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
             dq.zero_()
@@ -401,6 +419,7 @@ def run_marble(args, rank, world, local, dist):
             "data": "synthetic",
             "config": {"workload": cfg.name, "n_tokens": n, "heads": f"{hq}/{hkv}", "d": d,
                        "shards": P, "order": cfg.order, "window": cfg.window,
+                       "range_cost": cfg.range_cost if cfg.order == "chunk_search" else None,
                        "schedule": "needed-blocks" if needed else "ring r-major P^2 steps",
                        "l2": "inputs larger than L2 (Q/K/V/dO 256 MiB each; state 512 MiB)",
                        "legal_pairs_per_head": pairs, "flops_per_step": flops,
@@ -433,11 +452,10 @@ def run_profile_pass(args):
     import torch
     import context_attention_metadata_gb300 as M
     import workloads as wl
-    cid = args.config
-    cfg = wl.CONFIGS[cid] if args.tokens <= 0 else wl.mini_config(cid, args.tokens, hq=wl.CONFIGS[cid].hq)
-    tr = wl.config_tracks(cid) if args.tokens <= 0 else wl.config_tracks(cid, cfg.n)
+    cfg, tr = workload(args)
     trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
-    pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens)
+    pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens,
+                range_cost=cfg.range_cost)
     n, hq, hkv, d = cfg.n, cfg.hq, cfg.hkv, cfg.d
     q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda")
     qp, kp, vp, dop = (pl.permute(t) for t in (q, k, v, do))
@@ -471,7 +489,12 @@ def main():
     ap.add_argument("--profile-pass", type=int, default=0,
                     help="run this many untimed fwd+bwd passes for a profiler and exit")
     ap.add_argument("--tokens", type=int, default=0,
-                    help="with --profile-pass: a smaller pack of the same recipe")
+                    help="a smaller pack of the same recipe (side measurements, profiling)")
+    ap.add_argument("--order", default="",
+                    help="token order instead of the workload's (side measurements)")
+    ap.add_argument("--chunk-tokens", type=int, default=0, help="with --order ptrr_chunk")
+    ap.add_argument("--range-cost", type=int, default=0,
+                    help="with the chunk_search order: tau, legal pairs per range and step")
     args = ap.parse_args()
     if args.profile_pass > 0:
         run_profile_pass(args)

@@ -28,7 +28,7 @@ STEP_FIRST = 1
 STEP_BF16_MERGE = 2  # standard ring merge in bf16 (the comparison baseline)
 STEP_FP32_MERGE = 4  # merge of fp32 partials by their LSE
 _MERGE = {None: 0, "carried": 0, "bf16": STEP_BF16_MERGE, "fp32": STEP_FP32_MERGE}
-ORDERS = {"contiguous": 0, "ptrr_block": 1, "ptrr_chunk": 2}
+ORDERS = {"contiguous": 0, "ptrr_block": 1, "ptrr_chunk": 2, "chunk_search": 3}
 FIELDS = {
     "perm": (0, "int32"), "block_perm": (1, "int32"), "tracks_perm": (2, "int32"),
     "tile_rowptr": (3, "int64"), "tile_col": (4, "int32"), "tile_tag": (5, "uint8"),
@@ -48,13 +48,15 @@ class _PlanDesc(ctypes.Structure):
     _fields_ = [("n_tokens", ctypes.c_int64), ("sample_id", ctypes.c_void_p),
                 ("seg_id", ctypes.c_void_p), ("noise_id", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("num_shards", ctypes.c_int32),
-                ("order", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32)]
+                ("order", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
+                ("range_cost", ctypes.c_int64)]
 
 
 class _PlanStats(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int64) for name in (
         "n_tokens", "n_blocks", "num_shards", "nnz", "n_full", "n_partial", "legal_pairs",
-        "shard_cost_max", "shard_cost_sum", "step_cost", "needed_total", "needed_remote")]
+        "shard_cost_max", "shard_cost_sum", "step_cost", "needed_total", "needed_remote",
+        "chunks_per_rank", "layout_cost", "layout_step_cost")]
 
 
 class _QKV(ctypes.Structure):
@@ -74,6 +76,8 @@ _SIGS = {
     "marble_plan": ([ctypes.POINTER(_PlanDesc), ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
     "marble_plan_destroy": ([ctypes.c_void_p]),
     "marble_plan_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_PlanStats)]),
+    "marble_chunk_layout_search": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
     "marble_plan_field_bytes": ([ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
     "marble_plan_export": ([ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t,
                             ctypes.c_void_p]),
@@ -162,7 +166,8 @@ class Plan:
     sample/seg/noise: int32 CUDA tensors [N] in original token order (see marble.h)."""
 
     def __init__(self, sample, seg, noise, window: int, num_shards: int,
-                 order: str = "contiguous", chunk_tokens: int = 0, stream=None):
+                 order: str = "contiguous", chunk_tokens: int = 0, stream=None,
+                 range_cost: int = 0):
         import torch
         for t, nm in ((sample, "sample"), (seg, "seg"), (noise, "noise")):
             _need(t, torch.int32, nm, (sample.shape[0],))
@@ -171,7 +176,8 @@ class Plan:
         self.window = int(window)
         self.order = order
         d = _PlanDesc(self.n, sample.data_ptr(), seg.data_ptr(), noise.data_ptr(),
-                      int(window), int(num_shards), ORDERS[order], int(chunk_tokens))
+                      int(window), int(num_shards), ORDERS[order], int(chunk_tokens),
+                      int(range_cost))
         h = ctypes.c_void_p()
         _call("marble_plan", ctypes.byref(d), _stream(stream), ctypes.byref(h))
         self._h = h
@@ -404,6 +410,22 @@ def backward(plan: Plan, q, k, v, o, do, lse, delta, dq_acc, dk_acc, dv_acc,
     attn_bwd_prep(plan, o, do, delta, stream=stream)
     attn_bwd_steps(plan, q, k, v, do, lse, delta, ring_schedule(plan.num_shards, needed),
                    dq_acc, dk_acc, dv_acc, scale=scale, stream=stream)
+
+
+def chunk_layout_search(block_pairs, num_shards: int, range_cost: int = 0):
+    """The chunk-layout search (marble_chunk_layout_search) on a host int64 [nb, nb] matrix
+    of work between blocks.  Returns (k, layout cost C, step cost, rank of every chunk)."""
+    import numpy as np
+    w = np.ascontiguousarray(block_pairs, dtype=np.int64)
+    nb = w.shape[0]
+    if w.shape != (nb, nb):
+        raise ValueError("block_pairs must be square")
+    rank = np.zeros(min(nb, 1024), np.int32)
+    out = np.zeros(3, np.int64)
+    _call("marble_chunk_layout_search", w.ctypes.data, nb, int(num_shards), int(range_cost),
+          rank.ctypes.data, out.ctypes.data)
+    k = int(out[0])
+    return k, int(out[1]), int(out[2]), rank[:k * int(num_shards)].astype(np.int64)
 
 
 def version() -> str:

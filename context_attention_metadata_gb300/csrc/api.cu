@@ -187,8 +187,10 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
   const int64_t nb = d->n_tokens / MARBLE_BLOCK;
   if (nb % d->num_shards)
     return fail(MARBLE_ERR_INVALID_ARG, "number of 128-token blocks must be divisible by num_shards");
-  if (d->order < MARBLE_ORDER_CONTIGUOUS || d->order > MARBLE_ORDER_PTRR_CHUNK)
+  if (d->order < MARBLE_ORDER_CONTIGUOUS || d->order > MARBLE_ORDER_CHUNK_SEARCH)
     return fail(MARBLE_ERR_INVALID_ARG, "unknown order");
+  if (d->order == MARBLE_ORDER_CHUNK_SEARCH && d->range_cost < 0)
+    return fail(MARBLE_ERR_INVALID_ARG, "range_cost must be >= 0");
   if (d->order == MARBLE_ORDER_PTRR_CHUNK) {
     if (d->chunk_tokens <= 0 || d->chunk_tokens % MARBLE_BLOCK || d->n_tokens % d->chunk_tokens ||
         (d->n_tokens / d->chunk_tokens) % d->num_shards)
@@ -207,6 +209,7 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
   p->W = d->window;
   p->order = d->order;
   p->chunk_tokens = d->chunk_tokens;
+  p->range_cost = d->order == MARBLE_ORDER_CHUNK_SEARCH ? d->range_cost : 0;
   p->bps = nb / d->num_shards;
   marble_status_t st = build_plan(d, (cudaStream_t)stream, p);
   if (st != MARBLE_OK) {
@@ -225,6 +228,32 @@ MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
   for (void* q : p->owned) cudaFree(q);
   if (p->ds_scratch) cudaFree(p->ds_scratch);
   delete p;
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_chunk_layout_search(const int64_t* block_pairs, int64_t n_blocks,
+                                                      int32_t num_shards, int64_t range_cost,
+                                                      int32_t* chunk_rank, int64_t* out) {
+  if (!block_pairs || !chunk_rank || !out)
+    return fail(MARBLE_ERR_INVALID_ARG, "block_pairs, chunk_rank and out must be non-null");
+  if (num_shards < 1 || num_shards > 256 || n_blocks < 1 || n_blocks % num_shards)
+    return fail(MARBLE_ERR_INVALID_ARG, "n_blocks must be a positive multiple of num_shards <= 256");
+  if (n_blocks > 65536) return fail(MARBLE_ERR_INVALID_ARG, "n_blocks must be <= 65536");
+  if (range_cost < 0) return fail(MARBLE_ERR_INVALID_ARG, "range_cost must be >= 0");
+  const int Kf = marble::finest_chunks(n_blocks, num_shards);
+  const int64_t cs = n_blocks / Kf;
+  std::vector<int64_t> wf((size_t)Kf * Kf, 0);
+  for (int64_t a = 0; a < n_blocks; ++a)
+    for (int64_t b = 0; b < n_blocks; ++b) {
+      const int64_t v = block_pairs[a * n_blocks + b];
+      if (v < 0) return fail(MARBLE_ERR_INVALID_ARG, "block_pairs must be >= 0");
+      wf[(size_t)(a / cs) * Kf + b / cs] += v;
+    }
+  int k = 0;
+  std::vector<int> rank;
+  marble::chunk_layout_host(wf, Kf, num_shards, range_cost, &k, &rank, &out[1], &out[2]);
+  out[0] = k;
+  for (size_t u = 0; u < rank.size(); ++u) chunk_rank[u] = rank[u];
   return MARBLE_OK;
 }
 
@@ -279,6 +308,9 @@ MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stre
     for (int64_t x = nptr[r]; x < nptr[r + 1]; ++x)
       remote += (needed[x] / p->bps) != r;
   out->needed_remote = remote;
+  out->chunks_per_rank = p->chunks_per_rank;
+  out->layout_cost = p->layout_cost;
+  out->layout_step_cost = p->layout_step_cost;
   return MARBLE_OK;
 }
 

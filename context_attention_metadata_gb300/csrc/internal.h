@@ -25,12 +25,20 @@ struct Summary {
   int pad;
 };
 
+// chunk-layout search (plan.cu): the finest chunk count for nb blocks and P ranks, and the
+// search over the pairs wf [Kf][Kf] between the finest chunks
+int finest_chunks(int64_t nb, int P);
+void chunk_layout_host(const std::vector<int64_t>& wf, int Kf, int P, int64_t tau, int* k,
+                       std::vector<int>* rank, int64_t* cost, int64_t* step);
+
 }  // namespace marble
 
 struct marble_plan {
   int device = 0;
   int64_t n = 0, nb = 0;
   int P = 1, W = 0, order = 0, chunk_tokens = 0;
+  int64_t range_cost = 0;                       // CHUNK_SEARCH: tau
+  int64_t chunks_per_rank = 0, layout_cost = 0, layout_step_cost = 0;  // its result
   int64_t bps = 0;           // blocks per shard
   int64_t nnz = 0, needed_total = 0;
   // device arrays (owned)

@@ -13,9 +13,11 @@
 // outside [first block whose max sample >= this block's min sample, last block whose min
 // sample <= this block's max sample] has a disjoint sample range and is empty by the
 // sample test; classification only visits the band.
+#include <algorithm>
 #include <climits>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "common.cuh"
 #include "internal.h"
@@ -522,6 +524,38 @@ __global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t
   }
 }
 
+// chunk-layout search input: legal pairs between every pair of chunks of cs blocks (original
+// order), full tiles 128 * 128, partial tiles counted pair by pair; one warp per q block
+__global__ void k_chunk_pairs(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
+                              const uint8_t* __restrict__ tag, const int32_t* __restrict__ sample,
+                              const int32_t* __restrict__ seg, const int32_t* __restrict__ noise,
+                              int64_t nb, int W, int cs, int K,
+                              unsigned long long* __restrict__ wc) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
+  for (int64_t qb = warp0; qb < nb; qb += nwarps) {
+    for (int64_t e = row_ptr[qb]; e < row_ptr[qb + 1]; ++e) {
+      const int64_t kb = col[e];
+      unsigned long long c = 0;
+      if (tag[e] == MARBLE_TILE_FULL) {
+        c = lane == 0 ? (unsigned long long)(kBlock * kBlock) : 0ull;
+      } else {
+        for (int qi = lane; qi < kBlock; qi += 32) {
+          const int64_t q = qb * kBlock + qi;
+          const int sq = sample[q], gq = seg[q], zq = noise[q];
+          for (int ki = 0; ki < kBlock; ++ki) {
+            const int64_t k = kb * kBlock + ki;
+            c += mask_legal(sq, gq, zq, (int)q, sample[k], seg[k], noise[k], (int)k, W);
+          }
+        }
+      }
+      for (int o = 16; o; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0 && c) atomicAdd(&wc[(qb / cs) * K + kb / cs], c);
+    }
+  }
+}
+
 inline unsigned grid_for(int64_t items, int per_cta) {
   return (unsigned)((items + per_cta - 1) / per_cta);
 }
@@ -599,6 +633,159 @@ __global__ void __launch_bounds__(1024) k_work_order(const int64_t* __restrict__
   }
 }
 
+// ------------------------------------------------------------------------------------
+// chunk-layout search (host): see MARBLE_ORDER_CHUNK_SEARCH in marble.h
+// ------------------------------------------------------------------------------------
+constexpr int kMaxChunks = 1024;
+constexpr int kMaxSwapPasses = 64;
+
+// sum over steps s of max over ranks r of W[r, (r - s) mod P]
+static int64_t layout_step_cost(const std::vector<int64_t>& Wr, int P) {
+  int64_t c = 0;
+  for (int s = 0; s < P; ++s) {
+    int64_t m = Wr[(size_t)(P - s) % P];  // r = 0
+    for (int r = 1; r < P; ++r) m = std::max(m, Wr[(size_t)r * P + (r - s + P) % P]);
+    c += m;
+  }
+  return c;
+}
+
+// PTRR's dealing over K units: (cost desc, index asc) order, round t of P units to ranks
+// 0..P-1 (t even) or P-1..0 (t odd)
+static void ptrr_deal(const std::vector<int64_t>& cost, int P, std::vector<int>& rank) {
+  const int K = (int)cost.size();
+  std::vector<int> order(K);
+  for (int u = 0; u < K; ++u) order[u] = u;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+  rank.assign(K, 0);
+  for (int i = 0; i < K; ++i) {
+    const int t = i / P, slot = i % P;
+    rank[order[i]] = (t & 1) ? P - 1 - slot : slot;
+  }
+}
+
+struct LayoutChoice {
+  int k = 0;
+  std::vector<int> rank;  // rank of every chunk
+  int64_t C = 0, step = 0;
+};
+
+// search over one chunk count: K = k * P chunks, Wc [K][K] legal pairs between chunks
+static void search_chunks(const std::vector<int64_t>& Wc, int K, int P, std::vector<int>& rank,
+                          int64_t* step) {
+  std::vector<int64_t> Wr((size_t)P * P);
+  auto rank_work = [&](const std::vector<int>& rk) {
+    std::fill(Wr.begin(), Wr.end(), 0);
+    for (int a = 0; a < K; ++a)
+      for (int b = 0; b < K; ++b) Wr[(size_t)rk[a] * P + rk[b]] += Wc[(size_t)a * K + b];
+    return layout_step_cost(Wr, P);
+  };
+  std::vector<int64_t> work(K, 0), zero(K, 0);
+  for (int a = 0; a < K; ++a)
+    for (int b = 0; b < K; ++b) work[a] += Wc[(size_t)a * K + b];
+  std::vector<int> ra, rb;
+  ptrr_deal(work, P, ra);
+  ptrr_deal(zero, P, rb);
+  const int64_t ca = rank_work(ra), cb = rank_work(rb);
+  rank = ca <= cb ? ra : rb;
+  int64_t cur = rank_work(rank);  // leaves Wr for the chosen start
+  // per chunk: its work towards / from every rank
+  std::vector<int64_t> srow((size_t)K * P, 0), scol((size_t)K * P, 0);
+  for (int a = 0; a < K; ++a)
+    for (int b = 0; b < K; ++b) {
+      srow[(size_t)a * P + rank[b]] += Wc[(size_t)a * K + b];
+      scol[(size_t)b * P + rank[a]] += Wc[(size_t)a * K + b];
+    }
+  std::vector<int64_t> W2((size_t)P * P);
+  for (int pass = 0; pass < kMaxSwapPasses; ++pass) {
+    bool swapped = false;
+    for (int a = 0; a < K; ++a)
+      for (int b = a + 1; b < K; ++b) {
+        const int x = rank[a], y = rank[b];
+        if (x == y) continue;
+        // chunk a moves from rank x to y, chunk b from y to x
+        const int64_t waa = Wc[(size_t)a * K + a], wbb = Wc[(size_t)b * K + b];
+        const int64_t wab = Wc[(size_t)a * K + b], wba = Wc[(size_t)b * K + a];
+        W2 = Wr;
+        for (int j = 0; j < P; ++j) {
+          // a's and b's work towards the other chunks of rank j
+          const int64_t ta = srow[(size_t)a * P + j] - (j == x ? waa : 0) - (j == y ? wab : 0);
+          const int64_t tb = srow[(size_t)b * P + j] - (j == x ? wba : 0) - (j == y ? wbb : 0);
+          W2[(size_t)x * P + j] += tb - ta;
+          W2[(size_t)y * P + j] += ta - tb;
+          // the other chunks of rank j towards a and b
+          const int64_t ua = scol[(size_t)a * P + j] - (j == x ? waa : 0) - (j == y ? wba : 0);
+          const int64_t ub = scol[(size_t)b * P + j] - (j == x ? wab : 0) - (j == y ? wbb : 0);
+          W2[(size_t)j * P + x] += ub - ua;
+          W2[(size_t)j * P + y] += ua - ub;
+        }
+        W2[(size_t)x * P + x] += wbb - waa;
+        W2[(size_t)y * P + y] += waa - wbb;
+        W2[(size_t)x * P + y] += wba - wab;
+        W2[(size_t)y * P + x] += wab - wba;
+        const int64_t c = layout_step_cost(W2, P);
+        if (c >= cur) continue;
+        cur = c;
+        swapped = true;
+        Wr = W2;
+        for (int z = 0; z < K; ++z) {
+          const int64_t dz = Wc[(size_t)z * K + b] - Wc[(size_t)z * K + a];
+          srow[(size_t)z * P + x] += dz;
+          srow[(size_t)z * P + y] -= dz;
+          const int64_t ez = Wc[(size_t)b * K + z] - Wc[(size_t)a * K + z];
+          scol[(size_t)z * P + x] += ez;
+          scol[(size_t)z * P + y] -= ez;
+        }
+        rank[a] = y;
+        rank[b] = x;
+      }
+    if (!swapped) break;
+  }
+  *step = cur;
+}
+
+// the layout with the lowest C over 1, 2, 4, ..., 64 chunks per rank; Wf [Kf][Kf] holds
+// the pairs between the finest chunks (Kf = kf * P, kf the largest candidate)
+static LayoutChoice choose_layout(const std::vector<int64_t>& Wf, int Kf, int P, int64_t tau) {
+  LayoutChoice best;
+  const int kf = Kf / P;
+  for (int k = 1; k <= kf; k *= 2) {
+    const int K = k * P, f = kf / k;
+    std::vector<int64_t> Wc((size_t)K * K, 0);
+    for (int a = 0; a < Kf; ++a)
+      for (int b = 0; b < Kf; ++b) Wc[(size_t)(a / f) * K + b / f] += Wf[(size_t)a * Kf + b];
+    std::vector<int> rank;
+    int64_t step = 0;
+    search_chunks(Wc, K, P, rank, &step);
+    const int64_t C = step + tau * P * k;
+    if (best.k == 0 || C < best.C) {
+      best.k = k;
+      best.rank = rank;
+      best.C = C;
+      best.step = step;
+    }
+  }
+  return best;
+}
+
+// the finest chunk count the search tries: k * P chunks with k = 1, 2, 4, ..., 64 dividing
+// the blocks evenly, at most kMaxChunks in all
+int finest_chunks(int64_t nb, int P) {
+  int kf = 1;
+  while (kf * 2 <= 64 && (int64_t)kf * 2 * P <= kMaxChunks && nb % ((int64_t)kf * 2 * P) == 0)
+    kf *= 2;
+  return kf * P;
+}
+
+void chunk_layout_host(const std::vector<int64_t>& wf, int Kf, int P, int64_t tau, int* k,
+                       std::vector<int>* rank, int64_t* cost, int64_t* step) {
+  const LayoutChoice L = choose_layout(wf, Kf, P, tau);
+  *k = L.k;
+  *rank = L.rank;
+  *cost = L.C;
+  *step = L.step;
+}
+
 #define MARBLE_TRY(x)                     \
   do {                                    \
     marble_status_t st_ = (x);            \
@@ -659,7 +846,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(salloc(&cntT, nb * P));
   MARBLE_TRY(salloc(&ucost, units));
   MARBLE_TRY(salloc(&rank_of, units));
-  MARBLE_TRY(salloc(&unit_new, units));
+  MARBLE_TRY(salloc(&unit_new, nb));  // the searched chunk layout has at most nb units
   MARBLE_TRY(salloc(&ncount, P));
 
   MARBLE_CK(cudaMemsetAsync(p->err, 0, 4 * sizeof(unsigned), s));
@@ -704,6 +891,37 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   if (p->order == MARBLE_ORDER_CONTIGUOUS) {
     k_block_perm<<<grid_for(nb, threads), threads, 0, s>>>(nullptr, 1, nb, p->block_perm,
                                                             p->inv_block_perm);
+  } else if (p->order == MARBLE_ORDER_CHUNK_SEARCH) {
+    // legal pairs between the finest chunks (the most chunks per rank the search tries),
+    // then the search on the host
+    const int Kf = finest_chunks(nb, P);
+    const int cs = (int)(nb / Kf);
+    void* wq = nullptr;
+    cudaError_t e = cudaMalloc(&wq, (size_t)Kf * Kf * sizeof(unsigned long long));
+    if (e != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(MARBLE_ERR_OOM, "cudaMalloc of the chunk-pair matrix failed");
+    }
+    scratch.push_back(wq);
+    auto* wc = static_cast<unsigned long long*>(wq);
+    MARBLE_CK(cudaMemsetAsync(wc, 0, (size_t)Kf * Kf * sizeof(unsigned long long), s));
+    k_chunk_pairs<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->row_ptr, p->col, p->tag, d->sample_id,
+                                                          d->seg_id, d->noise_id, nb, W, cs, Kf, wc);
+    MARBLE_CK(cudaGetLastError());
+    std::vector<int64_t> wf((size_t)Kf * Kf);
+    MARBLE_CK(cudaMemcpyAsync(wf.data(), wc, wf.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s));
+    MARBLE_CK(cudaStreamSynchronize(s));
+    const LayoutChoice L = choose_layout(wf, Kf, P, p->range_cost);
+    const int K = L.k * P;
+    std::vector<int32_t> un(K), seen(P, 0);
+    for (int u = 0; u < K; ++u) un[u] = L.rank[u] * L.k + seen[L.rank[u]]++;
+    MARBLE_CK(cudaMemcpyAsync(unit_new, un.data(), K * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    k_block_perm<<<grid_for(nb, threads), threads, 0, s>>>(unit_new, (int)(nb / K), nb,
+                                                            p->block_perm, p->inv_block_perm);
+    MARBLE_CK(cudaStreamSynchronize(s));  // `un` is read before it goes out of scope
+    p->chunks_per_rank = L.k;
+    p->layout_cost = L.C;
+    p->layout_step_cost = L.step;
   } else {
     k_unit_cost<<<grid_for(units, threads), threads, 0, s>>>(cnt, ub, units, ucost);
     k_ptrr_rank<<<grid_for(units, threads), threads, 0, s>>>(ucost, units, P, rank_of);

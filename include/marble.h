@@ -80,8 +80,10 @@ typedef enum {
 typedef enum {
   MARBLE_ORDER_CONTIGUOUS = 0, /* identity order: shard r = contiguous token range */
   MARBLE_ORDER_PTRR_BLOCK = 1, /* PTRR over 128-token blocks (MARBLE s03 "PTRR") */
-  MARBLE_ORDER_PTRR_CHUNK = 2  /* PTRR over contiguous chunks of chunk_tokens tokens
+  MARBLE_ORDER_PTRR_CHUNK = 2, /* PTRR over contiguous chunks of chunk_tokens tokens
                                   (MARBLE s03 "Chunked ring attention") */
+  MARBLE_ORDER_CHUNK_SEARCH = 3 /* contiguous chunks, layout searched for the lowest
+                                   layout cost C (MARBLE s03 "Chunked ring attention") */
 } marble_order_t;
 
 /*
@@ -99,6 +101,17 @@ typedef enum {
  *   1 <= num_shards <= 256 and nb % num_shards == 0;
  *   PTRR_CHUNK: chunk_tokens a positive multiple of 128 dividing n_tokens, and the
  *   number of chunks divisible by num_shards.
+ *   CHUNK_SEARCH: range_cost >= 0, and n_tokens / 128 divisible by num_shards (one chunk
+ *   per rank is always a candidate).  The search (MARBLE s03 "Chunked ring attention"):
+ *   W[r, j] = legal (q, k) pairs between rank r's queries and rank j's keys; a layout of k
+ *   contiguous chunks per rank costs C = sum_s max_r W[r, (r - s) mod P] + range_cost * P * k.
+ *   For k = 1, 2, 4, ..., 64 (equal chunks of whole blocks, at most 1024 chunks in all):
+ *   deal the chunks with PTRR's rule once in the order of their work and once in sequence
+ *   order, keep the start with the lower first term (the work order on a tie), then swap
+ *   chunks between ranks while that strictly lowers it: passes over chunk pairs (a, b),
+ *   a < b ascending, first improvement taken, until a pass makes no swap (64 passes at
+ *   most).  The lowest C wins, the fewer chunks on a tie; each rank keeps its chunks in
+ *   sequence order.  The search runs on the host over pair counts summed on the device.
  * The three track arrays are device int32[n_tokens]; they are read during marble_plan
  * only (the plan keeps its own permuted copy).
  */
@@ -111,6 +124,8 @@ typedef struct {
   int32_t num_shards;
   int32_t order;        /* marble_order_t */
   int32_t chunk_tokens; /* PTRR_CHUNK only */
+  int64_t range_cost;   /* CHUNK_SEARCH only: tau, the fixed cost of one contiguous range in
+                           one ring step, in legal pairs */
 } marble_plan_desc_t;
 
 typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
@@ -145,7 +160,24 @@ typedef struct {
                            chunk-layout cost C without the per-range term) */
   int64_t needed_total; /* sum over q shards of needed kv blocks */
   int64_t needed_remote;/* ... of which lie outside the q shard's own kv shard */
+  int64_t chunks_per_rank; /* CHUNK_SEARCH: k of the chosen layout (0 for other orders) */
+  int64_t layout_cost;  /* CHUNK_SEARCH: its C in legal pairs, range term included */
+  int64_t layout_step_cost; /* CHUNK_SEARCH: its sum_s max_r W[r, (r-s) mod P], in pairs */
 } marble_plan_stats_t;
+
+/*
+ * The chunk-layout search of MARBLE_ORDER_CHUNK_SEARCH on caller-supplied work, on the
+ * host (no device involved): block_pairs is a host int64 [n_blocks][n_blocks] matrix of
+ * legal pairs (or any non-negative work) between q block a and kv block b, n_blocks a
+ * multiple of num_shards and at most 65536.  Writes out[0] = k (chunks per rank), out[1] =
+ * the layout cost C and out[2] = its step cost sum_s max_r W[r, (r-s) mod P], and the rank
+ * of every chunk (k * num_shards entries, chunk c = blocks [c, c + 1) * n_blocks / (k *
+ * num_shards)) to the host array chunk_rank, which must hold min(n_blocks, 1024) entries.
+ * Errors: INVALID_ARG.
+ */
+marble_status_t marble_chunk_layout_search(const int64_t *block_pairs, int64_t n_blocks,
+                                           int32_t num_shards, int64_t range_cost,
+                                           int32_t *chunk_rank, int64_t *out);
 
 /* Plan statistics; counts legal pairs with a kernel over the partial tiles (full tiles
  * contribute 128*128 each).  Synchronises `stream`. */

@@ -16,13 +16,13 @@ def device_tracks(tr):
     return [torch.as_tensor(np.asarray(tr[k], np.int32)).cuda() for k in ("sample", "seg", "noise")]
 
 
-def make_plan(tr, W, P, order="contiguous", chunk_tokens=0):
+def make_plan(tr, W, P, order="contiguous", chunk_tokens=0, range_cost=0):
     s, g, z = device_tracks(tr)
-    return M.Plan(s, g, z, W, P, order, chunk_tokens)
+    return M.Plan(s, g, z, W, P, order, chunk_tokens, range_cost=range_cost)
 
 
 def plan_for(cfg, tr):
-    return make_plan(tr, cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens)
+    return make_plan(tr, cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens, cfg.range_cost)
 
 
 def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried"):

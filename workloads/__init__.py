@@ -149,6 +149,33 @@ def grouped_image_samples(rng: np.random.Generator, n: int) -> List[List[Span]]:
     return _truncate(samples, n)
 
 
+def video_generation_samples(rng: np.random.Generator, n: int,
+                             sample_tokens: Tuple[int, int] = (131072, 1048576)
+                             ) -> List[List[Span]]:
+    """Long-video generation samples of interleaved noise and clean frames (the pack the
+    MARBLE post's chunked ring attention is built for, section 03): a causal text prompt of
+    U[64, 512] tokens, then frames of F ~ U{512, 1024, 2048} tokens (one F per sample), each
+    frame as a noise span (the frame being generated: bidirectional within itself, sees
+    the clean tokens before it, hidden from every later span) followed by the same frame
+    clean (a bidirectional span that later frames see), until the sample holds about
+    U[sample_tokens] tokens.
+    """
+    samples: List[List[Span]] = []
+    total = 0
+    while total < n:
+        target = int(rng.integers(sample_tokens[0], sample_tokens[1] + 1))
+        F = int(rng.choice([512, 1024, 2048]))
+        s = [Span("causal", int(rng.integers(64, 513)))]
+        size = s[0].length
+        while size < target:
+            s.append(Span("noise", F))
+            s.append(Span("full", F))
+            size += 2 * F
+        samples.append(s)
+        total += size
+    return _truncate(samples, n)
+
+
 # --------------------------------------------------------------------------------------
 # configurations
 # --------------------------------------------------------------------------------------
@@ -165,6 +192,7 @@ class Config:
     window: int = WINDOW_INF
     chunk_tokens: int = 0
     needed: bool = False  # run each q shard once over its needed KV blocks
+    range_cost: int = 0   # chunk-layout search: tau, legal pairs per range and step
     bwd: bool = True
     description: str = ""
 
@@ -188,10 +216,17 @@ CONFIGS: Dict[int, Config] = {
                           "interleaved text, 10% generated); P=32 PTRR"),
 }
 
+# workloads beyond the five configurations above: not bench headline cases
+EXTRA: Dict[int, Config] = {
+    6: Config(6, "video_generation_1m", 1048576, 8, 8, 128, 16, "chunk_search",
+              description="N=1048576 long-video generation samples (128K-1M tokens of "
+                          "interleaved noise / clean frames); P=16, searched chunk layout"),
+}
+
 
 def config_samples(cid: int, n: Optional[int] = None) -> List[List[Span]]:
     """Samples of configuration ``cid``; ``n`` shrinks the pack (mini variants)."""
-    cfg = CONFIGS[cid]
+    cfg = CONFIGS[cid] if cid in CONFIGS else EXTRA[cid]
     n = cfg.n if n is None else n
     rng = np.random.default_rng(100 + cid)
     if cid == 1:
@@ -207,6 +242,8 @@ def config_samples(cid: int, n: Optional[int] = None) -> List[List[Span]]:
         return [[Span("causal", gen)]] + packed_mix_samples(rng, n - gen)
     if cid == 5:
         return grouped_image_samples(rng, n)
+    if cid == 6:
+        return video_generation_samples(rng, n, (min(n, 131072), min(n, 1048576)))
     raise KeyError(cid)
 
 
@@ -217,7 +254,7 @@ def config_tracks(cid: int, n: Optional[int] = None) -> Dict[str, np.ndarray]:
 def mini_config(cid: int, n: int = 16384, hq: Optional[int] = None,
                 hkv: Optional[int] = None) -> Config:
     """A small variant of config ``cid`` (same recipe, fewer tokens/heads)."""
-    c = CONFIGS[cid]
+    c = CONFIGS[cid] if cid in CONFIGS else EXTRA[cid]
     hq = hq if hq is not None else min(c.hq, 4)
     hkv = hkv if hkv is not None else (hq if c.hq == c.hkv else max(1, hq // (c.hq // c.hkv)))
     window = c.window if c.window == WINDOW_INF else min(c.window, n // 8)
