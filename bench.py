@@ -28,7 +28,7 @@ import time
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel on
 # the 64K packed workload, from one ncu capture of the kernels as they are now (the capture's
 # command is recorded beside its summary); None where the kernel changed since its capture
-KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 495.7e6, "k_bwd_dq": 284.3e6, "k_attn_fwd": 147.4e6}
+KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 499.2e6, "k_bwd_dq": 284.5e6, "k_attn_fwd": 147.7e6}
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -474,6 +474,83 @@ def run_profile_pass(args):
     print(f"profile pass ok: {cfg.name} n={n} passes={args.profile_pass}", flush=True)
 
 
+def run_emulated_ring(args):
+    """Side measurement for token layouts: every ring step (q shard r, kv shard j) timed on
+    its own on an otherwise idle GPU (one GPU standing for one rank), then the time of a
+    ring of P such GPUs: sum over steps s of the slowest rank's step, forward ring then
+    backward ring.  Prints one JSON line with the plan's step cost in legal pairs beside it
+    (the first term of the layout cost C of the chunked ring)."""
+    import numpy as np
+    import torch
+    import context_attention_metadata_gb300 as M
+    from context_attention_metadata_gb300 import _build
+
+    _build.build()
+    cfg, tr = workload(args)
+    n, hq, hkv, d, P = cfg.n, cfg.hq, cfg.hkv, cfg.d, cfg.shards
+    trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens,
+                range_cost=cfg.range_cost)
+    torch.cuda.synchronize()
+    plan_ms = 1e3 * (time.perf_counter() - t0)
+    stats = pl.stats()
+    import workloads as wl
+    q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda", seed=0)
+    qp, kp, vp, dop = (pl.permute(t) for t in (q, k, v, do))
+    st = M.State(n, hq, d)
+    o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
+    delta = torch.empty_like(lse)
+    dq = torch.zeros((n, hq, d), dtype=torch.float32, device="cuda")
+    dk = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    dv = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    tf = np.full((args.steps, P, P), np.inf)
+    tb = np.full((args.steps, P, P), np.inf)
+    for it in range(args.warmup + args.steps):
+        for r in range(P):
+            for s_ in range(P):
+                j = (r - s_) % P
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                M.attn_step(pl, qp, kp, vp, r, j, st, first=(s_ == 0))
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    tf[it - args.warmup, r, j] = e0.elapsed_time(e1)
+        M.attn_finalize(pl, st, o, lse)
+        M.attn_bwd_prep(pl, o, dop, delta)
+        for r in range(P):
+            for s_ in range(P):
+                j = (r - s_) % P
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                M.attn_bwd_steps(pl, qp, kp, vp, dop, lse, delta, [(r, j, False)], dq, dk, dv)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= args.warmup:
+                    tb[it - args.warmup, r, j] = e0.elapsed_time(e1)
+    pl.check()
+    tf, tb = np.median(tf, axis=0), np.median(tb, axis=0)
+
+    def ring(t):
+        return float(sum(max(t[r, (r - s_) % P] for r in range(P)) for s_ in range(P)))
+
+    line = {"measurement": "emulated ring of P GPUs, one rank per launch",
+            "workload": cfg.name, "n_tokens": n, "heads": f"{hq}/{hkv}", "shards": P,
+            "order": cfg.order, "chunk_tokens": cfg.chunk_tokens, "range_cost": cfg.range_cost,
+            "steps": args.steps, "warmup": args.warmup,
+            "ring_ms": {"fwd": ring(tf), "bwd": ring(tb), "total": ring(tf) + ring(tb)},
+            "serial_ms": {"fwd": float(tf.sum()), "bwd": float(tb.sum())},
+            "plan_ms": plan_ms,
+            "step_cost_pairs": stats["step_cost_pairs"], "step_cost_tiles": stats["step_cost"],
+            "chunks_per_rank": stats["chunks_per_rank"], "layout_cost": stats["layout_cost"],
+            "legal_pairs": stats["legal_pairs"], "nnz": stats["nnz"]}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -495,9 +572,15 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0, help="with --order ptrr_chunk")
     ap.add_argument("--range-cost", type=int, default=0,
                     help="with the chunk_search order: tau, legal pairs per range and step")
+    ap.add_argument("--emulate-ring", action="store_true",
+                    help="side measurement: time every ring step alone, report the ring time "
+                         "of P GPUs (sum over steps of the slowest rank)")
     args = ap.parse_args()
     if args.profile_pass > 0:
         run_profile_pass(args)
+        return
+    if args.emulate_ring:
+        run_emulated_ring(args)
         return
     rank, world, local, dist = _dist()
     if args.impl == "reference":

@@ -56,7 +56,7 @@ class _PlanStats(ctypes.Structure):
     _fields_ = [(name, ctypes.c_int64) for name in (
         "n_tokens", "n_blocks", "num_shards", "nnz", "n_full", "n_partial", "legal_pairs",
         "shard_cost_max", "shard_cost_sum", "step_cost", "needed_total", "needed_remote",
-        "chunks_per_rank", "layout_cost", "layout_step_cost")]
+        "chunks_per_rank", "layout_cost", "layout_step_cost", "step_cost_pairs")]
 
 
 class _QKV(ctypes.Structure):

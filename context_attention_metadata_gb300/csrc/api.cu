@@ -266,7 +266,8 @@ MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stre
   out->n_blocks = p->nb;
   out->num_shards = p->P;
   out->nnz = p->nnz;
-  marble_status_t st = plan_legal_pairs(p, s, &out->legal_pairs, &out->n_full, &out->n_partial);
+  marble_status_t st = plan_legal_pairs(p, s, &out->legal_pairs, &out->n_full, &out->n_partial,
+                                        &out->step_cost_pairs);
   if (st != MARBLE_OK) return st;
   const int64_t np = p->nb * p->P + 1;
   std::vector<int64_t> ptr(np);

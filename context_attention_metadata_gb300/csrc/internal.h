@@ -39,6 +39,7 @@ struct marble_plan {
   int P = 1, W = 0, order = 0, chunk_tokens = 0;
   int64_t range_cost = 0;                       // CHUNK_SEARCH: tau
   int64_t chunks_per_rank = 0, layout_cost = 0, layout_step_cost = 0;  // its result
+  unsigned long long* shard_pairs = nullptr;    // [P*P] statistics: legal pairs per shard pair
   int64_t bps = 0;           // blocks per shard
   int64_t nnz = 0, needed_total = 0;
   // device arrays (owned)
@@ -108,7 +109,7 @@ uint64_t wait_limit_ns();
 // planner (plan.cu)
 marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_plan_t* p);
 marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t* pairs,
-                                 int64_t* n_full, int64_t* n_partial);
+                                 int64_t* n_full, int64_t* n_partial, int64_t* step_pairs);
 
 // elementwise kernels (misc.cu)
 cudaError_t launch_permute(const marble_plan_t* p, const void* src, void* dst, int64_t row_bytes,

@@ -480,7 +480,8 @@ __global__ void k_needed(const int64_t* __restrict__ colT_ptr, int64_t nb, int P
 __global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
                               const uint8_t* __restrict__ tag, const int32_t* __restrict__ inv,
                               const int32_t* __restrict__ tracks, int64_t n, int64_t nb, int W,
-                              unsigned long long* __restrict__ acc) {
+                              int64_t bps, int P, unsigned long long* __restrict__ acc,
+                              unsigned long long* __restrict__ shard_pairs) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
@@ -492,12 +493,19 @@ __global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t
   for (int64_t qb = warp0; qb < nb; qb += nwarps) {
     const int64_t qn = (int64_t)inv[qb] * kBlock;
     for (int64_t e = row_ptr[qb]; e < row_ptr[qb + 1]; ++e) {
+      // W[q shard, kv shard] in legal pairs
+      unsigned long long* wsh = shard_pairs + (inv[qb] / bps) * P + inv[col[e]] / bps;
       if (tag[e] == MARBLE_TILE_FULL) {
-        if (lane == 0) { legal += kBlock * kBlock; ++nfull; }
+        if (lane == 0) {
+          legal += kBlock * kBlock;
+          ++nfull;
+          atomicAdd(wsh, (unsigned long long)(kBlock * kBlock));
+        }
         continue;
       }
       if (lane == 0) ++npart;
       const int64_t kn = (int64_t)inv[col[e]] * kBlock;
+      unsigned long long tile = 0;
       for (int qi = lane; qi < kBlock; qi += 32) {
         const int64_t q = qn + qi;
         const int sq = smp[q], gq = sg[q], zq = nz[q], pq = ps[q];
@@ -511,7 +519,10 @@ __global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t
           c += (causal || span) && keep && smp[k] == sq;
         }
         legal += c;
+        tile += c;
       }
+      for (int o = 16; o; o >>= 1) tile += __shfl_xor_sync(0xffffffffu, tile, o);
+      if (lane == 0 && tile) atomicAdd(wsh, tile);
     }
   }
   for (int o = 16; o; o >>= 1) {
@@ -801,6 +812,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
 
   MARBLE_TRY(dalloc(p, &p->err, 4));
   MARBLE_TRY(dalloc(p, &p->counters, 8));
+  MARBLE_TRY(dalloc(p, &p->shard_pairs, (size_t)P * P));
   MARBLE_TRY(dalloc(p, &p->summ, nb));
   MARBLE_TRY(dalloc(p, &p->band, 2 * nb));
   MARBLE_TRY(dalloc(p, &p->row_ptr, nb + 1));
@@ -988,19 +1000,25 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
 }
 
 marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t* pairs,
-                                 int64_t* n_full, int64_t* n_partial) {
+                                 int64_t* n_full, int64_t* n_partial, int64_t* step_pairs) {
   MARBLE_CK(cudaMemsetAsync(p->counters, 0, 3 * sizeof(unsigned long long), s));
+  MARBLE_CK(cudaMemsetAsync(p->shard_pairs, 0, (size_t)p->P * p->P * sizeof(unsigned long long), s));
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const unsigned ctas = (unsigned)std::min<int64_t>(grid_for(p->nb, kWarpsPerCta), 8 * sms);
   k_legal_pairs<<<ctas, 32 * kWarpsPerCta, 0, s>>>(p->row_ptr, p->col, p->tag,
                                                    p->inv_block_perm, p->tracks, p->n, p->nb,
-                                                   p->W, p->counters);
+                                                   p->W, p->bps, p->P, p->counters,
+                                                   p->shard_pairs);
   MARBLE_CK(cudaGetLastError());
   unsigned long long h[3] = {0, 0, 0};
+  std::vector<int64_t> w((size_t)p->P * p->P);
   MARBLE_CK(cudaMemcpyAsync(h, p->counters, sizeof(h), cudaMemcpyDeviceToHost, s));
+  MARBLE_CK(cudaMemcpyAsync(w.data(), p->shard_pairs, w.size() * sizeof(int64_t),
+                            cudaMemcpyDeviceToHost, s));
   MARBLE_CK(cudaStreamSynchronize(s));
+  *step_pairs = layout_step_cost(w, p->P);
   *pairs = (int64_t)h[0];
   *n_full = (int64_t)h[1];
   *n_partial = (int64_t)h[2];

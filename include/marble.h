@@ -163,6 +163,7 @@ typedef struct {
   int64_t chunks_per_rank; /* CHUNK_SEARCH: k of the chosen layout (0 for other orders) */
   int64_t layout_cost;  /* CHUNK_SEARCH: its C in legal pairs, range term included */
   int64_t layout_step_cost; /* CHUNK_SEARCH: its sum_s max_r W[r, (r-s) mod P], in pairs */
+  int64_t step_cost_pairs;  /* any order: sum_s max_r W[r, (r-s) mod P], W in legal pairs */
 } marble_plan_stats_t;
 
 /*

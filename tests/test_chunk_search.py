@@ -68,6 +68,23 @@ def test_searched_plan_matches_oracle_plan(seed):
     C, k, _, step = oplan.chunk_search(oplan.block_pair_counts(tr, W), P, tau)
     st = pl.stats()
     assert (st["chunks_per_rank"], st["layout_cost"], st["layout_step_cost"]) == (k, C, step)
+    assert st["step_cost_pairs"] == step
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("order", ["contiguous", "ptrr_block", "ptrr_chunk"])
+def test_step_cost_in_pairs_for_every_order(order):
+    from marble_testlib import make_plan
+    rng = np.random.default_rng(90)
+    n, P = 128 * 64, 4
+    tr = wl.random_pack(rng, n, max_samples=5)
+    pl = make_plan(tr, INF, P, order, chunk_tokens=1024)
+    opl = oplan.make_plan(tr, INF, P, order, chunk_tokens=1024)
+    Wb = oplan.block_pair_counts(tr, INF)
+    bps = opl.nb // P
+    rank = np.repeat(np.arange(P), bps)  # new block -> its shard
+    Wc = Wb[np.ix_(opl.block_perm, opl.block_perm)]
+    assert pl.stats()["step_cost_pairs"] == oplan.layout_step_cost(Wc, rank, P)
 
 
 @pytest.mark.gpu

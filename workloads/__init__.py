@@ -219,8 +219,10 @@ CONFIGS: Dict[int, Config] = {
 # workloads beyond the five configurations above: not bench headline cases
 EXTRA: Dict[int, Config] = {
     6: Config(6, "video_generation_1m", 1048576, 8, 8, 128, 16, "chunk_search",
+              range_cost=167800,
               description="N=1048576 long-video generation samples (128K-1M tokens of "
-                          "interleaved noise / clean frames); P=16, searched chunk layout"),
+                          "interleaved noise / clean frames); P=16, searched chunk layout, "
+                          "tau = 167800 legal pairs (fitted to emulated ring times on GB300)"),
 }
 
 
