@@ -109,3 +109,26 @@ def test_attention_on_searched_layout():
     pl = plan_for(cfg, tr)
     dq, dk, dv = run_backward(pl, q, k, v, do)
     _check_dense(tr, cfg.window, q, k, v, do, dq, dk, dv)
+
+
+@pytest.mark.gpu
+def test_full_video_generation_forward_sampled():
+    # the 1M-token long-video generation pack on its searched layout (P = 16, fitted tau):
+    # sampled rows of the output and LSE against the fp64 oracle
+    import torch
+    from marble_testlib import check_o_lse, plan_for, run_forward
+    cfg = wl.EXTRA[6]
+    tr = wl.config_tracks(6)
+    q, k, v = wl.make_qkvdo(cfg.n, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=3)[:3]
+    pl = plan_for(cfg, tr)
+    st = pl.stats()
+    assert st["chunks_per_rank"] >= 1 and st["layout_step_cost"] == st["step_cost_pairs"]
+    O, L, _ = run_forward(pl, q, k, v)
+    assert torch.isfinite(L).all()
+    rng = np.random.default_rng(6)
+    rows = np.sort(rng.choice(cfg.n, 24, replace=False))
+    heads = np.array([0, cfg.hq - 1])
+    qc, kc, vc = (t.cpu() for t in (q, k, v))
+    Oref, Lref = attention.rows_forward(qc, kc, vc, tr, cfg.window, rows, heads=heads)
+    rt, ht = torch.as_tensor(rows).cuda(), torch.as_tensor(heads).cuda()
+    check_o_lse(O[rt][:, ht], L[ht][:, rt], Oref, Lref)
