@@ -349,3 +349,38 @@ def chunk_search(Wb, P, tau):
     if best is None:
         raise ValueError("no chunk count divides the blocks evenly")
     return best
+
+
+# --------------------------------------------------------------------------------------
+# key intervals
+# --------------------------------------------------------------------------------------
+def key_intervals(tr, W):
+    """Per key k (original order): the smallest interval [lo_k, hi_k) of query indices that
+    holds every query allowed to see k, and whether the interval is exact, i.e. every query
+    inside it sees k (MARBLE post, section 03: each key's visible queries form one range,
+    so a partial tile can test lo_k <= pos_q < hi_k).  A key no query sees gets (0, 0),
+    exact.  Queries of other samples never see a key, so each sample is treated alone.
+    Returns lo, hi (int64) and exact (bool)."""
+    sample = np.asarray(tr["sample"])
+    n = len(sample)
+    lo = np.zeros(n, np.int64)
+    hi = np.zeros(n, np.int64)
+    exact = np.ones(n, bool)
+    starts = np.flatnonzero(np.r_[True, sample[1:] != sample[:-1]])
+    ends = np.r_[starts[1:], n]
+    for a, b in zip(starts, ends):
+        idx = np.arange(a, b)
+        Mk = dense_mask(tr, W, idx, idx)          # [query, key] within the sample
+        for j in range(b - a):
+            vis = np.flatnonzero(Mk[:, j])
+            if len(vis) == 0:
+                continue
+            lo[a + j] = a + vis[0]
+            hi[a + j] = a + vis[-1] + 1
+            exact[a + j] = len(vis) == vis[-1] - vis[0] + 1
+    return lo, hi, exact
+
+
+def interval_blocks(exact) -> np.ndarray:
+    """Per 128-token block: True if every key of the block has an exact interval."""
+    return np.asarray(exact).reshape(-1, BLOCK).all(axis=1)

@@ -662,3 +662,60 @@ def test_chunk_search_plan_realises_the_searched_cost():
     for r in range(P):
         mine = chunks[r * k:(r + 1) * k, 0] // cs
         assert (np.diff(mine) > 0).all() and (rank[mine] == r).all()
+
+
+def test_key_intervals_closed_forms():
+    # one sample: causal text of 300, a bidirectional span of 200, a noise span of 100, then
+    # causal text of 424; positions are indices
+    samples = [[wl.Span("causal", 300), wl.Span("full", 200), wl.Span("noise", 100),
+                wl.Span("causal", 424)]]
+    tr = wl.tracks_from_samples(samples)
+    n = 1024
+    W = INF
+    lo, hi, ex = plan.key_intervals(tr, W)
+    assert ex.all()
+    k = np.arange(n)
+    # causal keys: themselves up to the end of the sample, except that the noise span [500, 600)
+    # sees clean keys too, so the range stays [k, n)
+    for kk in (0, 17, 299, 600, 1023):
+        assert (lo[kk], hi[kk]) == (kk, n)
+    # bidirectional span keys: from the span start to the end of the sample
+    for kk in (300, 399, 499):
+        assert (lo[kk], hi[kk]) == (300, n)
+    # noise keys: only the noise span itself
+    for kk in (500, 550, 599):
+        assert (lo[kk], hi[kk]) == (500, 600)
+    # a window of 50: causal keys see [k, k + 50), span keys at least their span
+    lo, hi, ex = plan.key_intervals(tr, 50)
+    assert ex.all() and (lo[10], hi[10]) == (10, 60) and (lo[310], hi[310]) == (300, 500)
+    assert (lo[480], hi[480]) == (300, 530)
+
+
+def test_key_intervals_group_is_not_contiguous():
+    # image group of two spans with text between: a key of the second image is seen by the
+    # first image (same group) but not by the text between them
+    samples = [[wl.Span("causal", 128), wl.Span("group", 128, 0), wl.Span("causal", 128),
+                wl.Span("group", 128, 0), wl.Span("causal", 128)]]
+    tr = wl.tracks_from_samples(samples)
+    lo, hi, ex = plan.key_intervals(tr, INF)
+    assert not ex[384:512].any() and (lo[400], hi[400]) == (128, 640)
+    assert ex[:384].all() and ex[512:].all()
+    assert list(plan.interval_blocks(ex)) == [True, True, True, False, True]
+    # W = 0: a causal key is seen by nobody
+    lo, hi, ex = plan.key_intervals(tr, 0)
+    assert (lo[5], hi[5]) == (0, 0) and ex[5]
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_key_intervals_reproduce_the_mask(seed):
+    # where exact, the interval test equals the mask on every pair
+    rng = np.random.default_rng(70 + seed)
+    n = 512
+    tr = wl.random_pack(rng, n, max_samples=4)
+    W = [INF, 64, 300][seed]
+    lo, hi, ex = plan.key_intervals(tr, W)
+    M = mask.dense_mask(tr, W)
+    q = np.arange(n)[:, None]
+    test = (q >= lo[None, :]) & (q < hi[None, :])
+    assert (test[:, ex] == M[:, ex]).all()
+    assert (M[:, ~ex] & ~test[:, ~ex]).sum() == 0  # the interval always covers the visible set
