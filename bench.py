@@ -247,7 +247,7 @@ def run_marble(args, rank, world, local, dist):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens,
-                    range_cost=cfg.range_cost)
+                    range_cost=cfg.range_cost, key_intervals=not args.no_key_intervals)
         torch.cuda.synchronize()
         plan_ms.append(1e3 * (time.perf_counter() - t0))
     stats = pl.stats()
@@ -357,7 +357,8 @@ def run_marble(args, rank, world, local, dist):
             for dst, src in zip(dev_in + dev_tr, hq_pin + htr):
                 dst.copy_(src, non_blocking=True)
             p2 = M.Plan(dev_tr[0], dev_tr[1], dev_tr[2], cfg.window, P, cfg.order,
-                        cfg.chunk_tokens, range_cost=cfg.range_cost)
+                        cfg.chunk_tokens, range_cost=cfg.range_cost,
+                        key_intervals=not args.no_key_intervals)
             q2, k2, v2, do2 = (p2.permute(t) for t in dev_in)
             M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
             dq.zero_()
@@ -420,6 +421,7 @@ def run_marble(args, rank, world, local, dist):
             "config": {"workload": cfg.name, "n_tokens": n, "heads": f"{hq}/{hkv}", "d": d,
                        "shards": P, "order": cfg.order, "window": cfg.window,
                        "range_cost": cfg.range_cost if cfg.order == "chunk_search" else None,
+                       "key_intervals": not args.no_key_intervals,
                        "schedule": "needed-blocks" if needed else "ring r-major P^2 steps",
                        "l2": "inputs larger than L2 (Q/K/V/dO 256 MiB each; state 512 MiB)",
                        "legal_pairs_per_head": pairs, "flops_per_step": flops,
@@ -572,6 +574,9 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0, help="with --order ptrr_chunk")
     ap.add_argument("--range-cost", type=int, default=0,
                     help="with the chunk_search order: tau, legal pairs per range and step")
+    ap.add_argument("--no-key-intervals", action="store_true",
+                    help="side measurement: partial tiles always evaluate the four-track "
+                         "predicate")
     ap.add_argument("--emulate-ring", action="store_true",
                     help="side measurement: time every ring step alone, report the ring time "
                          "of P GPUs (sum over steps of the slowest rank)")

@@ -35,6 +35,7 @@ FIELDS = {
     "step_ptr": (6, "int64"), "step_col": (7, "int32"), "step_tag": (8, "uint8"),
     "colT_ptr": (9, "int64"), "colT_row": (10, "int32"), "colT_tag": (11, "uint8"),
     "needed_ptr": (12, "int64"), "needed": (13, "int32"),
+    "key_intervals": (14, "int32"), "interval_blocks": (15, "uint8"),
 }
 
 
@@ -49,7 +50,7 @@ class _PlanDesc(ctypes.Structure):
                 ("seg_id", ctypes.c_void_p), ("noise_id", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("num_shards", ctypes.c_int32),
                 ("order", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
-                ("range_cost", ctypes.c_int64)]
+                ("range_cost", ctypes.c_int64), ("no_key_intervals", ctypes.c_int32)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -167,7 +168,7 @@ class Plan:
 
     def __init__(self, sample, seg, noise, window: int, num_shards: int,
                  order: str = "contiguous", chunk_tokens: int = 0, stream=None,
-                 range_cost: int = 0):
+                 range_cost: int = 0, key_intervals: bool = True):
         import torch
         for t, nm in ((sample, "sample"), (seg, "seg"), (noise, "noise")):
             _need(t, torch.int32, nm, (sample.shape[0],))
@@ -177,7 +178,7 @@ class Plan:
         self.order = order
         d = _PlanDesc(self.n, sample.data_ptr(), seg.data_ptr(), noise.data_ptr(),
                       int(window), int(num_shards), ORDERS[order], int(chunk_tokens),
-                      int(range_cost))
+                      int(range_cost), 0 if key_intervals else 1)
         h = ctypes.c_void_p()
         _call("marble_plan", ctypes.byref(d), _stream(stream), ctypes.byref(h))
         self._h = h

@@ -332,6 +332,8 @@ static bool field_info(const marble_plan_t* p, int32_t field, const void** src, 
     case MARBLE_FIELD_COLT_TAG: *src = p->colT_tag; *bytes = p->nnz; return true;
     case MARBLE_FIELD_NEEDED_PTR: *src = p->needed_ptr; *bytes = (P + 1) * 8; return true;
     case MARBLE_FIELD_NEEDED: *src = p->needed; *bytes = p->needed_total * 4; return true;
+    case MARBLE_FIELD_KEY_INTERVALS: *src = p->kiv; *bytes = 2 * n * 4; return true;
+    case MARBLE_FIELD_INTERVAL_BLOCKS: *src = p->iv_block; *bytes = nb; return true;
     default: return false;
   }
 }

@@ -64,6 +64,8 @@ struct BwdParams {
   long long ds_slot0;        // first scratch slot of this step's dS^T tiles
   unsigned* sched;           // ticket counter pair of the launch
   const int32_t* tracks;     // [4][n] plan order
+  const int32_t* kiv;        // [2][n] lo, hi of every key's visible-query interval
+  const uint8_t* iv_block;   // [nb] 1: every key of the block has an exact interval
   const float* lse;          // [hq][n] natural log
   const float* delta;        // [hq][n]
   float* dq;
@@ -666,6 +668,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       const int64_t tk = nk * 128 + row;
       const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
                 pk = p.tracks[3 * n + tk];
+      // every key of the unit's block has an exact visible-query interval: partial tiles test
+      // lo_k <= pos_q < hi_k instead of the four-track predicate
+      const bool ivt = p.iv_block[nk] != 0;
+      const int klo = p.kiv[tk], khi = p.kiv[n + tk];
       for (int it = 0; it < items; ++it, ++g) {
         const int h = kh * p.group + it / L;
         const int64_t e = c0 + it % L;
@@ -682,7 +688,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         }
         mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
         uint32_t lm[2] = {~0u, ~0u};
-        if (partial) {
+        if (partial && ivt) {
+          const int32_t* qpos = p.tracks + 3 * n + (int64_t)p.colT_row[e] * 128 + half * 64;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t2 = 0; t2 < 32; t2 += 4) {
+              const int4 p4 = __ldg(reinterpret_cast<const int4*>(qpos + cc * 32 + t2));
+              bits |= ((p4.x >= klo) & (p4.x < khi) ? 1u : 0u) << t2;
+              bits |= ((p4.y >= klo) & (p4.y < khi) ? 1u : 0u) << (t2 + 1);
+              bits |= ((p4.z >= klo) & (p4.z < khi) ? 1u : 0u) << (t2 + 2);
+              bits |= ((p4.w >= klo) & (p4.w < khi) ? 1u : 0u) << (t2 + 3);
+            }
+            lm[cc] = bits;
+          }
+        } else if (partial) {
           // the half's 64 queries' tracks, read straight from global memory (the same
           // addresses for every lane: broadcast loads), four queries per load
           const int32_t* qt = p.tracks + (int64_t)p.colT_row[e] * 128 + half * 64;
@@ -880,6 +901,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   prm.needed_ptr = pl->needed_ptr;
   prm.needed = pl->needed;
   prm.tracks = pl->tracks;
+  prm.kiv = pl->kiv;
+  prm.iv_block = pl->iv_block;
   prm.lse = lse;
   prm.delta = delta;
   prm.dq = dq;

@@ -104,6 +104,8 @@ struct FwdParams {
   int W;
   int first;
   int lse_merge;   // 0 carried state; 1 merge of bf16 partials (standard ring); 2 of fp32 ones
+  const int32_t* kiv;       // [2][n] lo, hi of every key's visible-query interval
+  const uint8_t* iv_block;  // [nb] 1: every key of the block has an exact interval
   float scale_log2;
 };
 
@@ -419,8 +421,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
           const uint32_t par = (n_partial >> 1) & 1;
           ++n_partial;
           int32_t* kt = ktr + bb * 512;
-          const int64_t t = (int64_t)p.step_col[e0 + j] * 128 + row;
-          if (half == 0) {
+          const int64_t kb = p.step_col[e0 + j];
+          const int64_t t = kb * 128 + row;
+          // every key of the block has an exact visible-query interval: the test is
+          // lo_k <= pos_q < hi_k (two values a key) instead of the four-track predicate
+          const bool ivt = p.iv_block[kb] != 0;
+          if (ivt) {
+            kt[half * 128 + row] = p.kiv[half * n + t];
+          } else if (half == 0) {
             kt[row] = p.tracks[t];
             kt[128 + row] = p.tracks[n + t];
           } else {
@@ -433,11 +441,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
           for (int cc = 0; cc < 2; ++cc) {
             const int kc0 = (2 * half + cc) * 32;
             uint32_t bits = 0;
+            if (ivt) {
 #pragma unroll
-            for (int t2 = 0; t2 < 32; ++t2) {
-              const int kc = kc0 + t2;
-              bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc],
-                                  kt[384 + kc], p.W) ? 1u : 0u) << t2;
+              for (int t2 = 0; t2 < 32; ++t2) {
+                const int kc = kc0 + t2;
+                bits |= ((pq >= kt[kc]) & (pq < kt[128 + kc]) ? 1u : 0u) << t2;
+              }
+            } else {
+#pragma unroll
+              for (int t2 = 0; t2 < 32; ++t2) {
+                const int kc = kc0 + t2;
+                bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc],
+                                    kt[384 + kc], p.W) ? 1u : 0u) << t2;
+              }
             }
             lm[cc] = bits;
           }
@@ -735,6 +751,8 @@ marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
   prm->step_col = pl->step_col;
   prm->step_tag = pl->step_tag;
   prm->tracks = pl->tracks;
+  prm->kiv = pl->kiv;
+  prm->iv_block = pl->iv_block;
   prm->o_acc = st->o_acc;
   prm->m = st->m;
   prm->l = st->l;

@@ -40,6 +40,8 @@ struct marble_plan {
   int64_t range_cost = 0;                       // CHUNK_SEARCH: tau
   int64_t chunks_per_rank = 0, layout_cost = 0, layout_step_cost = 0;  // its result
   unsigned long long* shard_pairs = nullptr;    // [P*P] statistics: legal pairs per shard pair
+  int32_t* kiv = nullptr;       // [2*n] new order: lo, hi of every key's visible query interval
+  uint8_t* iv_block = nullptr;  // [nb] new order: 1 if every key of the block is exact
   int64_t bps = 0;           // blocks per shard
   int64_t nnz = 0, needed_total = 0;
   // device arrays (owned)

@@ -274,6 +274,95 @@ __global__ void k_perm_tracks(const int32_t* __restrict__ block_perm,
 }
 
 // ------------------------------------------------------------------------------------
+// key intervals: per key, the interval [lo, hi) of query indices that see it, and whether
+// every query inside sees it (the fast mask test of partial tiles)
+// ------------------------------------------------------------------------------------
+// first / last index and size of every segment id and noise id below n
+__global__ void k_iv_tables(const int32_t* __restrict__ seg, const int32_t* __restrict__ noise,
+                            int64_t n, int32_t* __restrict__ gfirst, int32_t* __restrict__ glast,
+                            int32_t* __restrict__ gcount, int32_t* __restrict__ zfirst,
+                            int32_t* __restrict__ zlast, int32_t* __restrict__ zcount) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int g = seg[i], z = noise[i];
+  if (g >= 0 && g < n) {
+    atomicMin(&gfirst[g], (int)i);
+    atomicMax(&glast[g], (int)i);
+    atomicAdd(&gcount[g], 1);
+  }
+  if (z >= 0 && z < n) {
+    atomicMin(&zfirst[z], (int)i);
+    atomicMax(&zlast[z], (int)i);
+    atomicAdd(&zcount[z], 1);
+  }
+}
+
+// Per key k of sample run [a, b): the causal queries form [k, min(k + W, b)); a key of a
+// span or group is also seen by the whole segment, and a noise key only by its noise span.
+// With the segment and the noise span each one run inside the sample, the visible set is
+// (causal u segment) n noise span, an interval; otherwise the key is not exact.  iv_orig
+// (per original block, preset to 1) is cleared by any key that is not exact.
+__global__ void k_iv_keys(const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
+                          const int32_t* __restrict__ noise, int64_t n, int W,
+                          const int32_t* __restrict__ gfirst, const int32_t* __restrict__ glast,
+                          const int32_t* __restrict__ gcount, const int32_t* __restrict__ zfirst,
+                          const int32_t* __restrict__ zlast, const int32_t* __restrict__ zcount,
+                          int32_t* __restrict__ lo_out, int32_t* __restrict__ hi_out,
+                          uint8_t* __restrict__ iv_orig) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  const int s = sample[k];
+  int64_t a = 0, b = k;  // a = first index of the sample (sample ids are non-decreasing)
+  while (a < b) {
+    const int64_t m = (a + b) >> 1;
+    if (sample[m] < s) a = m + 1; else b = m;
+  }
+  int64_t lo2 = k + 1, b2 = n;  // b2 = one past the last index of the sample
+  while (lo2 < b2) {
+    const int64_t m = (lo2 + b2) >> 1;
+    if (sample[m] <= s) lo2 = m + 1; else b2 = m;
+  }
+  b = b2;
+  const int64_t c1 = min(b, k + (int64_t)W);
+  int64_t lo = k, hi = c1;  // causal part, empty when W == 0
+  bool ex = true;
+  const int g = seg[k], z = noise[k];
+  if (g >= 0) {
+    if (g < n && gcount[g] == glast[g] - gfirst[g] + 1 && gfirst[g] >= a && glast[g] < b) {
+      lo = hi > lo ? min(lo, (int64_t)gfirst[g]) : (int64_t)gfirst[g];
+      hi = max(hi, (int64_t)glast[g] + 1);
+    } else {
+      ex = false;
+    }
+  }
+  if (z >= 0) {
+    if (z < n && zcount[z] == zlast[z] - zfirst[z] + 1 && zfirst[z] >= a && zlast[z] < b) {
+      lo = max(lo, (int64_t)zfirst[z]);
+      hi = min(hi, (int64_t)zlast[z] + 1);
+    } else {
+      ex = false;
+    }
+  }
+  if (hi <= lo) lo = hi = 0;  // seen by no query
+  lo_out[k] = (int32_t)lo;
+  hi_out[k] = (int32_t)hi;
+  if (!ex) iv_orig[k >> 7] = 0;
+}
+
+// intervals and block flags into the new order
+__global__ void k_perm_iv(const int32_t* __restrict__ perm, const int32_t* __restrict__ block_perm,
+                          const int32_t* __restrict__ lo, const int32_t* __restrict__ hi,
+                          const uint8_t* __restrict__ iv_orig, int64_t n,
+                          int32_t* __restrict__ kiv, uint8_t* __restrict__ iv_block) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  const int64_t o = perm[t];
+  kiv[t] = lo[o];
+  kiv[n + t] = hi[o];
+  if ((t & (kBlock - 1)) == 0) iv_block[t >> 7] = iv_orig[block_perm[t >> 7]];
+}
+
+// ------------------------------------------------------------------------------------
 // a5: per-step lists
 // ------------------------------------------------------------------------------------
 // rows: new q block nq (forward / dQ lists keyed (nq, kv shard j))
@@ -944,6 +1033,36 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   k_perm_tracks<<<grid_for(n, threads), threads, 0, s>>>(p->block_perm, d->sample_id, d->seg_id,
                                                           d->noise_id, n, p->perm, p->tracks);
   MARBLE_CK(cudaGetLastError());
+
+  // key intervals (all blocks flagged 0 when switched off: partial tiles then always
+  // evaluate the four-track predicate)
+  MARBLE_TRY(dalloc(p, &p->kiv, 2 * n));
+  MARBLE_TRY(dalloc(p, &p->iv_block, nb));
+  MARBLE_CK(cudaMemsetAsync(p->kiv, 0, 2 * n * sizeof(int32_t), s));
+  MARBLE_CK(cudaMemsetAsync(p->iv_block, 0, nb, s));
+  if (!d->no_key_intervals) {
+    int32_t *tab = nullptr, *klo = nullptr;
+    MARBLE_TRY(salloc(&tab, 6 * n));
+    MARBLE_TRY(salloc(&klo, 2 * n + (nb + 3) / 4));
+    int32_t *gfirst = tab, *glast = tab + n, *gcount = tab + 2 * n, *zfirst = tab + 3 * n,
+            *zlast = tab + 4 * n, *zcount = tab + 5 * n;
+    uint8_t* iv_orig = reinterpret_cast<uint8_t*>(klo + 2 * n);
+    MARBLE_CK(cudaMemsetAsync(gfirst, 0x7f, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(glast, 0xff, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(gcount, 0, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(zfirst, 0x7f, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(zlast, 0xff, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(zcount, 0, n * sizeof(int32_t), s));
+    MARBLE_CK(cudaMemsetAsync(iv_orig, 1, nb, s));
+    k_iv_tables<<<grid_for(n, threads), threads, 0, s>>>(d->seg_id, d->noise_id, n, gfirst, glast,
+                                                        gcount, zfirst, zlast, zcount);
+    k_iv_keys<<<grid_for(n, threads), threads, 0, s>>>(d->sample_id, d->seg_id, d->noise_id, n, W,
+                                                      gfirst, glast, gcount, zfirst, zlast, zcount,
+                                                      klo, klo + n, iv_orig);
+    k_perm_iv<<<grid_for(n, threads), threads, 0, s>>>(p->perm, p->block_perm, klo, klo + n,
+                                                      iv_orig, n, p->kiv, p->iv_block);
+    MARBLE_CK(cudaGetLastError());
+  }
 
   // a5: forward lists
   const size_t offs_smem = (size_t)kWarpsPerCta * P * sizeof(int64_t);

@@ -126,6 +126,8 @@ typedef struct {
   int32_t chunk_tokens; /* PTRR_CHUNK only */
   int64_t range_cost;   /* CHUNK_SEARCH only: tau, the fixed cost of one contiguous range in
                            one ring step, in legal pairs */
+  int32_t no_key_intervals; /* 1: partial tiles always evaluate the four-track predicate;
+                               0 (default): key-interval test where it is exact */
 } marble_plan_desc_t;
 
 typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
@@ -201,8 +203,12 @@ typedef enum {
   MARBLE_FIELD_COLT_ROW = 10,    /* int32[nnz] new q block, ascending per list */
   MARBLE_FIELD_COLT_TAG = 11,    /* uint8[nnz] */
   MARBLE_FIELD_NEEDED_PTR = 12,  /* int64[P+1] */
-  MARBLE_FIELD_NEEDED = 13       /* int32[needed_total] sorted unique new kv blocks that
+  MARBLE_FIELD_NEEDED = 13,      /* int32[needed_total] sorted unique new kv blocks that
                                     q shard r's rows need (local blocks included) */
+  MARBLE_FIELD_KEY_INTERVALS = 14, /* int32[2][N] new order: lo, hi of every key's
+                                      visible-query interval (original indices) */
+  MARBLE_FIELD_INTERVAL_BLOCKS = 15 /* uint8[nb] new order: 1 if every key of the block
+                                       has an exact interval */
 } marble_field_t;
 
 /* Size in bytes of an exported field (host call, no synchronisation). */
