@@ -413,7 +413,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         const uint32_t b = (uint32_t)(g & 1);
         const bool partial = p.step_tag[e0 + j] == MARBLE_TILE_PARTIAL;
         uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
-        if (partial) {
+        const int64_t kb = partial ? p.step_col[e0 + j] : 0;
+        // every key of the block has an exact visible-query interval: the test is
+        // lo_k <= pos_q < hi_k, with the half's 64 (lo, hi) pairs read straight from global
+        // memory (the same addresses for every lane: broadcast loads)
+        const bool ivt = partial && p.iv_block[kb] != 0;
+        if (ivt) {
+          const int32_t* klo = p.kiv + kb * 128 + half * 64;
+          const int32_t* khi = klo + n;
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t bits = 0;
+#pragma unroll
+            for (int t2 = 0; t2 < 32; t2 += 4) {
+              const int4 l4 = __ldg(reinterpret_cast<const int4*>(klo + cc * 32 + t2));
+              const int4 h4 = __ldg(reinterpret_cast<const int4*>(khi + cc * 32 + t2));
+              bits |= ((pq >= l4.x) & (pq < h4.x) ? 1u : 0u) << t2;
+              bits |= ((pq >= l4.y) & (pq < h4.y) ? 1u : 0u) << (t2 + 1);
+              bits |= ((pq >= l4.z) & (pq < h4.z) ? 1u : 0u) << (t2 + 2);
+              bits |= ((pq >= l4.w) & (pq < h4.w) ? 1u : 0u) << (t2 + 3);
+            }
+            lm[cc] = bits;
+          }
+        } else if (partial) {
           // stage the 128 keys' tracks in one of two buffers (the two halves load two tracks
           // each); every softmax thread arrives before any reads, so a buffer is rewritten
           // only after every thread left its previous use
@@ -421,14 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
           const uint32_t par = (n_partial >> 1) & 1;
           ++n_partial;
           int32_t* kt = ktr + bb * 512;
-          const int64_t kb = p.step_col[e0 + j];
           const int64_t t = kb * 128 + row;
-          // every key of the block has an exact visible-query interval: the test is
-          // lo_k <= pos_q < hi_k (two values a key) instead of the four-track predicate
-          const bool ivt = p.iv_block[kb] != 0;
-          if (ivt) {
-            kt[half * 128 + row] = p.kiv[half * n + t];
-          } else if (half == 0) {
+          if (half == 0) {
             kt[row] = p.tracks[t];
             kt[128 + row] = p.tracks[n + t];
           } else {
@@ -441,19 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
           for (int cc = 0; cc < 2; ++cc) {
             const int kc0 = (2 * half + cc) * 32;
             uint32_t bits = 0;
-            if (ivt) {
 #pragma unroll
-              for (int t2 = 0; t2 < 32; ++t2) {
-                const int kc = kc0 + t2;
-                bits |= ((pq >= kt[kc]) & (pq < kt[128 + kc]) ? 1u : 0u) << t2;
-              }
-            } else {
-#pragma unroll
-              for (int t2 = 0; t2 < 32; ++t2) {
-                const int kc = kc0 + t2;
-                bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc],
-                                    kt[384 + kc], p.W) ? 1u : 0u) << t2;
-              }
+            for (int t2 = 0; t2 < 32; ++t2) {
+              const int kc = kc0 + t2;
+              bits |= (mask_legal(sq, gq, zq, pq, kt[kc], kt[128 + kc], kt[256 + kc],
+                                  kt[384 + kc], p.W) ? 1u : 0u) << t2;
             }
             lm[cc] = bits;
           }
