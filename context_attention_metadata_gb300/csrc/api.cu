@@ -53,20 +53,21 @@ bool once_per_device(int key) {
 // Fork / join of a per-device side stream: work queued on the side stream between fork()
 // and join() runs after everything queued on `s` before fork(), and everything queued on `s`
 // after join() runs after it.
-cudaStream_t side_stream() {
+cudaStream_t side_stream(int idx) {
   static std::mutex mu;
-  static std::map<int, cudaStream_t> streams;
+  static std::map<std::pair<int, int>, cudaStream_t> streams;
+  if (idx < 0 || idx >= kSideStreams) return nullptr;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
-  auto it = streams.find(dev);
+  auto it = streams.find({dev, idx});
   if (it != streams.end()) return it->second;
   cudaStream_t st = nullptr;
   if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
     (void)cudaGetLastError();
     return nullptr;
   }
-  streams[dev] = st;
+  streams[{dev, idx}] = st;
   return st;
 }
 

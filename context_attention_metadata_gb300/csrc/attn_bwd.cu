@@ -966,15 +966,23 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   if (buf_slots > 0 &&
       !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, 2 * buf_slots * 128, 1, 128, 64, 128, sw))
     return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
-  // Step i: the dK/dV kernel (side stream) writes the step's dS^T tiles into half i & 1 of the
-  // scratch, then the dQ GEMM (stream s) reads them; dK/dV of step i+2 waits until the dQ GEMM
-  // of step i has finished with that half.  dK/dV of step i+1 overlaps the dQ GEMM of step i.
-  cudaStream_t s2 = side_stream();
-  if (!s2) s2 = s;
-  if (s2 != s) {
-    cudaError_t e = stream_fork(s, s2);
-    if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
-  }
+  // Step i: the dK/dV kernel (a side stream) writes the step's dS^T tiles into half i & 1 of
+  // the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step i+2 waits until the dQ
+  // GEMM of step i has finished with that half.  dK/dV of kv shard j runs on side stream
+  // j mod 2, so that the launches of one kv shard (which add into the same dK/dV rows) stay
+  // in order while consecutive steps (different kv shards) overlap, and dK/dV of step i+1
+  // overlaps the dQ GEMM of step i.  With every needed block at once, all dK/dV launches
+  // share one side stream.
+  cudaStream_t sk[2] = {side_stream(0), side_stream(1)};
+  const bool needed_mode = n_steps > 0 && kv_shards[0] < 0;
+  if (!sk[0]) sk[0] = sk[1] = s;
+  if (!sk[1] || needed_mode) sk[1] = sk[0];
+  for (int k = 0; k < 2; ++k)
+    if (sk[k] != s && (k == 0 || sk[1] != sk[0])) {
+      cudaError_t e = stream_fork(s, sk[k]);
+      if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+    }
+  const cudaStream_t s2 = sk[0];
   std::vector<cudaEvent_t> ev_k(n_steps, nullptr), ev_q(n_steps, nullptr);
   auto make_event = [](cudaEvent_t* ev) {
     return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
@@ -998,17 +1006,18 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
         pk.nwork = (int)(pl->h_needed_ptr[pk.q_shard + 1] - pl->h_needed_ptr[pk.q_shard]) *
                    qkv->hkv;
       }
-      if (s2 != s && i >= 2) err = cudaStreamWaitEvent(s2, ev_q[i - 2], 0);
+      const cudaStream_t sks = sk[pk.kv_shard >= 0 ? (pk.kv_shard & 1) : 0];
+      if (sks != s && i >= 2) err = cudaStreamWaitEvent(sks, ev_q[i - 2], 0);
       if (pk.nwork > 0 && err == cudaSuccess) {
         pk.sched = sched_slot(pl);
-        const int span = timing_begin(s2);
-        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, s2>>>(pk);
-        timing_end(span, s2, kTimeDkdv, 1);
+        const int span = timing_begin(sks);
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+        timing_end(span, sks, kTimeDkdv, 1);
         ++launches_k;
       }
-      if (s2 != s && err == cudaSuccess) {
+      if (sks != s && err == cudaSuccess) {
         err = make_event(&ev_k[i]);
-        if (err == cudaSuccess) err = cudaEventRecord(ev_k[i], s2);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_k[i], sks);
         if (err == cudaSuccess) err = cudaStreamWaitEvent(s, ev_k[i], 0);
       }
     }
@@ -1031,7 +1040,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       }
     }
   }
-  if (s2 != s && err == cudaSuccess) err = stream_fork(s2, s);
+  for (int k = 0; k < 2 && err == cudaSuccess; ++k)
+    if (sk[k] != s && (k == 0 || sk[1] != sk[0])) err = stream_fork(sk[k], s);
   for (cudaEvent_t ev : ev_k)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : ev_q)

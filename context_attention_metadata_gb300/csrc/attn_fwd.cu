@@ -794,17 +794,21 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  // Steps of different q shards touch disjoint rows of the state: those of odd q shards run on
-  // a side stream, so that consecutive launches' tails overlap.  Steps of one q shard stay in
-  // order on one stream.
-  cudaStream_t s2 = n_steps > 1 ? side_stream() : nullptr;
-  if (!s2) s2 = s;
-  if (s2 != s) {
-    cudaError_t e = stream_fork(s, s2);
-    if (e != cudaSuccess) return cuda_fail(e, "fork of the forward streams");
-  }
-  const int span_s = timing_begin(s), span_s2 = s2 != s ? timing_begin(s2) : -1;
-  int launches_s = 0, launches_s2 = 0;
+  // Steps of different q shards touch disjoint rows of the state: q shard r runs on stream
+  // r mod ns (the caller's stream and up to three side streams), so that the tails of
+  // launches of different shards overlap.  Steps of one q shard stay in order on one stream.
+  cudaStream_t st_of[1 + kSideStreams] = {s};
+  int ns = 1;
+  if (n_steps > 1)
+    for (int k = 0; k < kSideStreams; ++k) {
+      cudaStream_t x = side_stream(k);
+      if (!x) break;
+      cudaError_t e = stream_fork(s, x);
+      if (e != cudaSuccess) return cuda_fail(e, "fork of the forward streams");
+      st_of[ns++] = x;
+    }
+  int span[1 + kSideStreams], launches[1 + kSideStreams] = {0};
+  for (int k = 0; k < ns; ++k) span[k] = timing_begin(st_of[k]);
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;
     prm.q_shard = q_shards[i];
@@ -820,14 +824,13 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     // initialises the units without tiles, spread over the whole grid
     const int want = prm.first ? base.units : prm.nwork;
     const unsigned grid = (unsigned)(want < sms ? want : sms);
-    const bool side = (prm.q_shard & 1) && s2 != s;
-    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), side ? s2 : s>>>(prm);
-    ++(side ? launches_s2 : launches_s);
+    const int k = prm.q_shard % ns;
+    k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), st_of[k]>>>(prm);
+    ++launches[k];
   }
-  timing_end(span_s, s, kTimeFwd, launches_s);
-  timing_end(span_s2, s2, kTimeFwd, launches_s2);
-  if (s2 != s) {
-    cudaError_t e = stream_fork(s2, s);
+  for (int k = 0; k < ns; ++k) timing_end(span[k], st_of[k], kTimeFwd, launches[k]);
+  for (int k = 1; k < ns; ++k) {
+    cudaError_t e = stream_fork(st_of[k], s);
     if (e != cudaSuccess) return cuda_fail(e, "join of the forward streams");
   }
   cudaError_t e = cudaGetLastError();

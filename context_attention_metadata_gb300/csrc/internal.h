@@ -137,7 +137,8 @@ bool once_per_device(int key);
 
 // a second stream of the current device (nullptr if it cannot be created), and an ordering
 // edge from everything queued on `from` so far to everything queued on `to` afterwards
-cudaStream_t side_stream();
+constexpr int kSideStreams = 3;
+cudaStream_t side_stream(int idx = 0);
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);
 
 // per-kernel timing (marble_timing_enable): kinds of kernels, and a span of launches of one
