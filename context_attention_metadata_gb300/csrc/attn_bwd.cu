@@ -44,6 +44,8 @@ constexpr int kThreads = 384;  // producer, MMA, 8 elementwise warps, scheduler,
 constexpr int kWarpSched = 10;
 constexpr int kWarpStore = 11;
 constexpr int kQueue = 4;
+constexpr int kDsBufs = 4;        // steps whose dS^T tiles the scratch holds at once
+constexpr int kDkdvStreams = 4;   // side streams of the dK/dV launches
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdParams {
@@ -934,8 +936,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int P = pl->P;
   prm.step_off = pl->step_off;
   prm.colT_j = pl->colT_j;
-  // scratch for the bf16 dS^T tiles of two steps: the dQ GEMM of step i reads one half while
-  // the dK/dV kernel of step i+1 writes the other
+  // scratch for the bf16 dS^T tiles of kDsBufs steps: the dQ GEMM of step i reads buffer
+  // i mod kDsBufs while the dK/dV kernels of the next steps write the others
   int64_t max_tiles = 0;  // the largest step of this call
   for (int i = 0; i < n_steps; ++i) {
     const int64_t t =
@@ -945,7 +947,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int64_t buf_slots = max_tiles * qkv->hq;
   {
     std::lock_guard<std::mutex> lock(pl->scratch_mu);
-    const size_t need = (size_t)(2 * buf_slots) * 32768;
+    const size_t need = (size_t)(kDsBufs * buf_slots) * 32768;
     if (need > pl->ds_scratch_bytes) {
       if (pl->ds_scratch) {
         cudaDeviceSynchronize();
@@ -964,24 +966,27 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     }
   }
   if (buf_slots > 0 &&
-      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, 2 * buf_slots * 128, 1, 128, 64, 128, sw))
+      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, kDsBufs * buf_slots * 128, 1, 128, 64,
+                     128, sw))
     return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
-  // Step i: the dK/dV kernel (a side stream) writes the step's dS^T tiles into half i & 1 of
-  // the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step i+2 waits until the dQ
-  // GEMM of step i has finished with that half.  dK/dV of kv shard j runs on side stream
-  // j mod 2, so that the launches of one kv shard (which add into the same dK/dV rows) stay
-  // in order while consecutive steps (different kv shards) overlap, and dK/dV of step i+1
-  // overlaps the dQ GEMM of step i.  With every needed block at once, all dK/dV launches
-  // share one side stream.
-  cudaStream_t sk[2] = {side_stream(0), side_stream(1)};
+  // Step i: the dK/dV kernel (a side stream) writes the step's dS^T tiles into buffer
+  // i mod kDsBufs of the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step
+  // i + kDsBufs waits until the dQ GEMM of step i has finished with that buffer.  dK/dV of kv
+  // shard j runs on side stream j mod kDkdvStreams, so that the launches of one kv shard
+  // (which add into the same dK/dV rows) stay in order while consecutive steps (different kv
+  // shards) overlap one another and the dQ GEMMs.  With every needed block at once, all
+  // dK/dV launches share one side stream.
   const bool needed_mode = n_steps > 0 && kv_shards[0] < 0;
-  if (!sk[0]) sk[0] = sk[1] = s;
-  if (!sk[1] || needed_mode) sk[1] = sk[0];
-  for (int k = 0; k < 2; ++k)
-    if (sk[k] != s && (k == 0 || sk[1] != sk[0])) {
-      cudaError_t e = stream_fork(s, sk[k]);
-      if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
-    }
+  cudaStream_t sk[kDkdvStreams];
+  int nsk = 0;
+  for (int k = 0; k < (needed_mode ? 1 : kDkdvStreams); ++k) {
+    cudaStream_t x = side_stream(k);
+    if (!x) break;
+    cudaError_t e = stream_fork(s, x);
+    if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+    sk[nsk++] = x;
+  }
+  if (nsk == 0) sk[nsk++] = s;
   const cudaStream_t s2 = sk[0];
   std::vector<cudaEvent_t> ev_k(n_steps, nullptr), ev_q(n_steps, nullptr);
   auto make_event = [](cudaEvent_t* ev) {
@@ -992,7 +997,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
-    prm.ds_slot0 = (long long)(i & 1) * buf_slots;
+    prm.ds_slot0 = (long long)(i % kDsBufs) * buf_slots;
     // dK/dV: the kv blocks of the kv shard listed for the q shard (longest list first), or
     // the q shard's needed kv blocks
     {
@@ -1006,8 +1011,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
         pk.nwork = (int)(pl->h_needed_ptr[pk.q_shard + 1] - pl->h_needed_ptr[pk.q_shard]) *
                    qkv->hkv;
       }
-      const cudaStream_t sks = sk[pk.kv_shard >= 0 ? (pk.kv_shard & 1) : 0];
-      if (sks != s && i >= 2) err = cudaStreamWaitEvent(sks, ev_q[i - 2], 0);
+      const cudaStream_t sks = sk[pk.kv_shard >= 0 ? pk.kv_shard % nsk : 0];
+      if (sks != s && i >= kDsBufs) err = cudaStreamWaitEvent(sks, ev_q[i - kDsBufs], 0);
       if (pk.nwork > 0 && err == cudaSuccess) {
         pk.sched = sched_slot(pl);
         const int span = timing_begin(sks);
@@ -1040,8 +1045,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       }
     }
   }
-  for (int k = 0; k < 2 && err == cudaSuccess; ++k)
-    if (sk[k] != s && (k == 0 || sk[1] != sk[0])) err = stream_fork(sk[k], s);
+  for (int k = 0; k < nsk && err == cudaSuccess; ++k)
+    if (sk[k] != s) err = stream_fork(sk[k], s);
   for (cudaEvent_t ev : ev_k)
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : ev_q)

@@ -797,17 +797,18 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   // Steps of different q shards touch disjoint rows of the state: q shard r runs on stream
   // r mod ns (the caller's stream and up to three side streams), so that the tails of
   // launches of different shards overlap.  Steps of one q shard stay in order on one stream.
-  cudaStream_t st_of[1 + kSideStreams] = {s};
+  constexpr int kFwdSide = 3;
+  cudaStream_t st_of[1 + kFwdSide] = {s};
   int ns = 1;
   if (n_steps > 1)
-    for (int k = 0; k < kSideStreams; ++k) {
+    for (int k = 0; k < kFwdSide; ++k) {
       cudaStream_t x = side_stream(k);
       if (!x) break;
       cudaError_t e = stream_fork(s, x);
       if (e != cudaSuccess) return cuda_fail(e, "fork of the forward streams");
       st_of[ns++] = x;
     }
-  int span[1 + kSideStreams], launches[1 + kSideStreams] = {0};
+  int span[1 + kFwdSide], launches[1 + kFwdSide] = {0};
   for (int k = 0; k < ns; ++k) span[k] = timing_begin(st_of[k]);
   for (int i = 0; i < n_steps; ++i) {
     FwdParams prm = base;

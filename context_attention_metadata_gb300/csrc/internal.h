@@ -137,7 +137,7 @@ bool once_per_device(int key);
 
 // a second stream of the current device (nullptr if it cannot be created), and an ordering
 // edge from everything queued on `from` so far to everything queued on `to` afterwards
-constexpr int kSideStreams = 3;
+constexpr int kSideStreams = 4;
 cudaStream_t side_stream(int idx = 0);
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);
 
