@@ -33,6 +33,8 @@
 // Masks only on partial tiles.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tma_host.h"
@@ -44,7 +46,8 @@ constexpr int kThreads = 384;  // producer, MMA, 8 elementwise warps, scheduler,
 constexpr int kWarpSched = 10;
 constexpr int kWarpStore = 11;
 constexpr int kQueue = 4;
-constexpr int kDsBufs = 4;        // steps whose dS^T tiles the scratch holds at once
+constexpr int kDsBufs = 4;        // steps whose dS^T tiles the scratch holds at once (at most)
+constexpr size_t kDsScratchCap = size_t(32) << 30;  // fewer buffers (down to 2) above this
 constexpr int kDkdvStreams = 4;   // side streams of the dK/dV launches
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -945,9 +948,12 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     max_tiles = t > max_tiles ? t : max_tiles;
   }
   const int64_t buf_slots = max_tiles * qkv->hq;
+  const int nbuf = (int)std::max<int64_t>(
+      2, std::min<int64_t>(kDsBufs, (int64_t)(kDsScratchCap / ((size_t)std::max<int64_t>(
+                                                                 buf_slots, 1) * 32768))));
   {
     std::lock_guard<std::mutex> lock(pl->scratch_mu);
-    const size_t need = (size_t)(kDsBufs * buf_slots) * 32768;
+    const size_t need = (size_t)(nbuf * buf_slots) * 32768;
     if (need > pl->ds_scratch_bytes) {
       if (pl->ds_scratch) {
         cudaDeviceSynchronize();
@@ -966,12 +972,12 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     }
   }
   if (buf_slots > 0 &&
-      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, kDsBufs * buf_slots * 128, 1, 128, 64,
+      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, nbuf * buf_slots * 128, 1, 128, 64,
                      128, sw))
     return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
   // Step i: the dK/dV kernel (a side stream) writes the step's dS^T tiles into buffer
-  // i mod kDsBufs of the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step
-  // i + kDsBufs waits until the dQ GEMM of step i has finished with that buffer.  dK/dV of kv
+  // i mod nbuf of the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step
+  // i + nbuf waits until the dQ GEMM of step i has finished with that buffer.  dK/dV of kv
   // shard j runs on side stream j mod kDkdvStreams, so that the launches of one kv shard
   // (which add into the same dK/dV rows) stay in order while consecutive steps (different kv
   // shards) overlap one another and the dQ GEMMs.  With every needed block at once, all
@@ -997,7 +1003,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
     prm.q_shard = q_shards[i];
     prm.kv_shard = kv_shards[i];
-    prm.ds_slot0 = (long long)(i % kDsBufs) * buf_slots;
+    prm.ds_slot0 = (long long)(i % nbuf) * buf_slots;
     // dK/dV: the kv blocks of the kv shard listed for the q shard (longest list first), or
     // the q shard's needed kv blocks
     {
@@ -1012,7 +1018,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
                    qkv->hkv;
       }
       const cudaStream_t sks = sk[pk.kv_shard >= 0 ? pk.kv_shard % nsk : 0];
-      if (sks != s && i >= kDsBufs) err = cudaStreamWaitEvent(sks, ev_q[i - kDsBufs], 0);
+      if (sks != s && i >= nbuf) err = cudaStreamWaitEvent(sks, ev_q[i - nbuf], 0);
       if (pk.nwork > 0 && err == cudaSuccess) {
         pk.sched = sched_slot(pl);
         const int span = timing_begin(sks);

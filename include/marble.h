@@ -332,7 +332,14 @@ marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *q
                                 marble_stream_t stream);
 
 /* A list of backward ring steps in one call: step i is marble_attn_bwd(..., q_shards[i],
- * kv_shards[i], ..., flags = 0), in list order on `stream`; host arrays of n_steps entries. */
+ * kv_shards[i], ..., flags = 0), with the same result as issuing them in list order on
+ * `stream`; host arrays of n_steps entries.  Each step runs a dK/dV kernel, which also
+ * writes the step's bf16 dS tiles to a scratch array the plan owns, and a dQ GEMM over those
+ * tiles.  The scratch holds the tiles of up to four steps (two when four would exceed 32 GB)
+ * and grows on demand; backward calls on one plan must therefore be ordered with respect to
+ * each other.  The launches spread over side streams of the device, forked from `stream` at
+ * the start and joined back into it at the end; launches that add into the same dK/dV rows
+ * (one kv shard) stay on one stream, so results do not depend on timing. */
 marble_status_t marble_attn_bwd_steps(const marble_plan_t *plan, const marble_qkv_t *qkv,
                                       const void *d_o, const float *lse, const float *delta,
                                       int32_t n_steps, const int32_t *q_shards,
