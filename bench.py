@@ -28,7 +28,7 @@ import time
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel on
 # the 64K packed workload, from one ncu capture of the kernels as they are now (the capture's
 # command is recorded beside its summary); None where the kernel changed since its capture
-KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 499.2e6, "k_bwd_dq": 284.5e6, "k_attn_fwd": 147.7e6}
+KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 494.7e6, "k_bwd_dq": 283.5e6, "k_attn_fwd": 147.9e6}
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -336,55 +336,132 @@ def run_marble(args, rank, world, local, dist):
             "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
             "kernel_ms": {k_: round(v_[1] / args.steps, 3) for k_, v_ in kern.items()},
             "kernel_tflops": {k_: (v_[0] * args.steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
-                              for k_, v_ in kern.items()}}
+                              for k_, v_ in kern.items()},
+            "note": "per-launch spans inside the timed step, whose launches overlap on several "
+                    "streams: a span includes time spent waiting for SMs"}
+
+    # the same kernels with every launch in list order on one stream (no overlap), warm: the
+    # per-launch durations of the kernels themselves
+    iso_steps = 2
+    M.set_side_streams(0)
+    step()
+    torch.cuda.synchronize()
+    M.timing_read()
+    M.timing_enable(True)
+    for _ in range(iso_steps):
+        step()
+    torch.cuda.synchronize()
+    M.timing_enable(False)
+    kt_iso = M.timing_read()
+    M.set_side_streams(4)
+    pl.check()
+    kern_iso = {
+        "k_attn_fwd": (flops_fwd, kt_iso["fwd_ms"], kt_iso["fwd_launches"]),
+        "k_bwd_dkdv": (0.8 * flops_bwd, kt_iso["dkdv_ms"], kt_iso["dkdv_launches"]),
+        "k_bwd_dq": (0.2 * flops_bwd, kt_iso["dq_ms"], kt_iso["dq_launches"]),
+    }
+    dom_iso = max(kern_iso, key=lambda k_: kern_iso[k_][1])
+    f_i, ms_i, l_i = kern_iso[dom_iso]
+    mpl_i = ms_i / max(l_i, 1)
+    fpl_i = f_i * iso_steps / max(l_i, 1)
+    ach_i = fpl_i / (mpl_i / 1e3) / 1e12
+    tot_i = sum(v_[1] for v_ in kern_iso.values())
+    roof_iso = {"bound": "tensor", "achieved": ach_i, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach_i / peak, "traffic": KERNEL_DRAM_BYTES_PER_LAUNCH.get(dom_iso),
+                "kernel": dom_iso, "launches": l_i, "ms_per_launch": mpl_i,
+                "flops_per_launch": fpl_i,
+                "kernel_ms": {k_: round(v_[1] / iso_steps, 3) for k_, v_ in kern_iso.items()},
+                "kernel_share": {k_: round(v_[1] / tot_i, 3) for k_, v_ in kern_iso.items()},
+                "kernel_tflops": {k_: (v_[0] * iso_steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
+                                  for k_, v_ in kern_iso.items()},
+                "note": "one launch at a time on one stream, warm, after the timed step"}
 
     # end to end through the public API: H2D of the step's inputs from pinned memory,
-    # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results
+    # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results.
+    # Steps are pipelined the way a training loop runs them: the next step's inputs are
+    # copied in on one copy stream while this step computes, and this step's results are
+    # copied out on another while the next step plans and computes (double-buffered inputs
+    # and outputs).  Plans are destroyed after the timed steps (destroying one synchronises the
+    # device).
     e2e = None
     if args.e2e_steps > 0:
         hq_pin = [t.cpu().pin_memory() for t in (q, k, v, do)]
         htr = [t.cpu().pin_memory() for t in trk]
-        out_pin = [torch.empty((n, hq, d), dtype=torch.bfloat16).pin_memory()] + \
-                  [torch.empty(s, dtype=torch.bfloat16).pin_memory()
-                   for s in ((n, hq, d), (n, hkv, d), (n, hkv, d))]
-        dq_b = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
-        dk_b = torch.empty((n, hkv, d), dtype=torch.bfloat16, device="cuda")
-        dv_b = torch.empty((n, hkv, d), dtype=torch.bfloat16, device="cuda")
-        dev_in = [torch.empty_like(t, device="cuda") for t in hq_pin]
-        dev_tr = [torch.empty_like(t, device="cuda") for t in htr]
+        shapes = ((n, hq, d), (n, hq, d), (n, hkv, d), (n, hkv, d))
+        out_pin = [[torch.empty(s_, dtype=torch.bfloat16).pin_memory() for s_ in shapes]
+                   for _ in range(2)]
+        outs = [[torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in shapes]
+                for _ in range(2)]
+        dev_in = [[torch.empty_like(t, device="cuda") for t in hq_pin] for _ in range(2)]
+        dev_tr = [[torch.empty_like(t, device="cuda") for t in htr] for _ in range(2)]
+        g_tmp = [torch.empty((n, hq, d), dtype=torch.float32, device="cuda"),
+                 torch.empty((n, hkv, d), dtype=torch.float32, device="cuda")]
+        cs = torch.cuda.Stream()       # host -> device
+        cs_out = torch.cuda.Stream()   # device -> host (the two directions overlap)
+        comp = torch.cuda.current_stream()
 
-        def e2e_step():
-            for dst, src in zip(dev_in + dev_tr, hq_pin + htr):
-                dst.copy_(src, non_blocking=True)
-            p2 = M.Plan(dev_tr[0], dev_tr[1], dev_tr[2], cfg.window, P, cfg.order,
-                        cfg.chunk_tokens, range_cost=cfg.range_cost,
-                        key_intervals=not args.no_key_intervals)
-            q2, k2, v2, do2 = (p2.permute(t) for t in dev_in)
-            M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
-            dq.zero_()
-            dk.zero_()
-            dv.zero_()
-            M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
-            o_u = p2.permute(o, inverse=True)
-            for g_, b_ in ((dq, dq_b), (dk, dk_b), (dv, dv_b)):
-                M.cast_bf16(p2.permute(g_, inverse=True), b_)
-            for dst, src in zip(out_pin, (o_u, dq_b, dk_b, dv_b)):
-                dst.copy_(src, non_blocking=True)
+        def e2e_run(K):
+            plans = []
+            ev_in, ev_used, ev_out, ev_d2h = ([torch.cuda.Event() for _ in range(2)]
+                                              for _ in range(4))
+
+            def h2d(i):
+                b = i % 2
+                with torch.cuda.stream(cs):
+                    if i >= 2:
+                        cs.wait_event(ev_used[b])   # step i - 2 is done with buffer b
+                    for dst, src in zip(dev_in[b] + dev_tr[b], hq_pin + htr):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[b].record(cs)
+
+            h2d(0)
+            for i in range(K):
+                b = i % 2
+                if i + 1 < K:
+                    h2d(i + 1)
+                comp.wait_event(ev_in[b])
+                p2 = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P, cfg.order,
+                            cfg.chunk_tokens, range_cost=cfg.range_cost,
+                            key_intervals=not args.no_key_intervals)
+                plans.append(p2)
+                q2, k2, v2, do2 = (p2.permute(t) for t in dev_in[b])
+                M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
+                dq.zero_()
+                dk.zero_()
+                dv.zero_()
+                M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
+                ev_used[b].record(comp)
+                if i >= 2:
+                    comp.wait_event(ev_d2h[b])      # step i - 2's results have left buffer b
+                ob = outs[b]
+                p2.permute(o, inverse=True, out=ob[0])
+                for g_, t_, b_ in ((dq, g_tmp[0], ob[1]), (dk, g_tmp[1], ob[2]),
+                                   (dv, g_tmp[1], ob[3])):
+                    p2.permute(g_, inverse=True, out=t_)
+                    M.cast_bf16(t_, b_)
+                ev_out[b].record(comp)
+                with torch.cuda.stream(cs_out):
+                    cs_out.wait_event(ev_out[b])
+                    for dst, src in zip(out_pin[b], ob):
+                        dst.copy_(src, non_blocking=True)
+                    ev_d2h[b].record(cs_out)
             torch.cuda.synchronize()
-            p2.close()
+            for p2 in plans:
+                p2.close()
 
-        e2e_step()
+        e2e_run(1)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            e2e_step()
+        e2e_run(args.e2e_steps)
         e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dist)
-        h2d = sum(t.numel() * t.element_size() for t in hq_pin + htr)
-        d2h = sum(t.numel() * t.element_size() for t in out_pin)
+        h2d_b = sum(t.numel() * t.element_size() for t in hq_pin + htr)
+        d2h_b = sum(t.numel() * t.element_size() for t in out_pin[0])
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
-               "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H"}
+               "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H; "
+               "steps pipelined (copies on a copy stream overlap compute), plan teardown "
+               "after the timed steps"}
 
     # the forward with each merge of the ring steps: the carried fp32 state (the timed step
     # above), the merge of fp32 partials and the standard merge of bf16 partials
@@ -435,6 +512,7 @@ def run_marble(args, rank, world, local, dist):
             "plan_ms": min(plan_ms), "plan_stats": stats,
             "wall_s_timed_region": t_wall,
             "roofline": roof,
+            "roofline_isolated": roof_iso,
             "fwd_merge_variants": merge_variants,
             "cpu_baseline": cpu,
             "e2e": e2e,
@@ -560,7 +638,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="marble", choices=["marble", "reference"])
     ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for cpu_baseline (0 disables)")
     ap.add_argument("--ref-budget", type=float, default=5.0,

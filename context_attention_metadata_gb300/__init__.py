@@ -105,6 +105,7 @@ _SIGS = {
     "marble_cast_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "marble_check": ([ctypes.c_void_p, ctypes.c_void_p]),
     "marble_set_wait_limit_ns": ([ctypes.c_uint64]),
+    "marble_set_side_streams": ([ctypes.c_int32]),
     "marble_debug_wait_timeout": ([ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p]),
     "marble_timing_enable": ([ctypes.c_int]),
     "marble_timing_read": ([ctypes.c_void_p]),
@@ -321,6 +322,12 @@ def cast_bf16(src, dst, stream=None):
 
 def set_wait_limit_ns(ns: int):
     _call("marble_set_wait_limit_ns", int(ns))
+
+
+def set_side_streams(n: int):
+    """Cap the side streams the step-list calls use (0: all launches on the caller's
+    stream, in list order)."""
+    _call("marble_set_side_streams", int(n))
 
 
 def timing_enable(on: bool = True):

@@ -53,10 +53,44 @@ bool once_per_device(int key) {
 // Fork / join of a per-device side stream: work queued on the side stream between fork()
 // and join() runs after everything queued on `s` before fork(), and everything queued on `s`
 // after join() runs after it.
+std::atomic<int> g_side_limit{kSideStreams};
+
+static cudaMemPool_t mem_pool() {
+  static std::mutex mu;
+  static std::map<int, cudaMemPool_t> pools;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = pools.find(dev);
+  if (it != pools.end()) return it->second;
+  cudaMemPoolProps props;
+  memset(&props, 0, sizeof(props));
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool = nullptr;
+  if (cudaMemPoolCreate(&pool, &props) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  uint64_t keep = UINT64_MAX;  // freed blocks stay in the pool
+  cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  pools[dev] = pool;
+  return pool;
+}
+
+cudaError_t dev_alloc(void** p, size_t bytes, cudaStream_t s) {
+  cudaMemPool_t pool = mem_pool();
+  if (!pool) return cudaErrorMemoryAllocation;
+  return cudaMallocFromPoolAsync(p, bytes, pool, s);
+}
+
+cudaError_t dev_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+
 cudaStream_t side_stream(int idx) {
   static std::mutex mu;
   static std::map<std::pair<int, int>, cudaStream_t> streams;
-  if (idx < 0 || idx >= kSideStreams) return nullptr;
+  if (idx < 0 || idx >= kSideStreams || idx >= g_side_limit.load()) return nullptr;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
@@ -226,8 +260,8 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
 MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
   if (!p) return MARBLE_OK;
   cudaDeviceSynchronize();
-  for (void* q : p->owned) cudaFree(q);
-  if (p->ds_scratch) cudaFree(p->ds_scratch);
+  for (void* q : p->owned) dev_free(q, nullptr);
+  if (p->ds_scratch) dev_free(p->ds_scratch, nullptr);
   delete p;
   return MARBLE_OK;
 }
@@ -539,6 +573,12 @@ MARBLE_API marble_status_t marble_check(const marble_plan_t* p, marble_stream_t 
                                           std::to_string(h) + ")");
     return fail(MARBLE_ERR_CUDA, "device error word " + std::to_string(h));
   }
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_set_side_streams(int32_t n) {
+  if (n < 0 || n > kSideStreams) return fail(MARBLE_ERR_INVALID_ARG, "n must be in [0, 4]");
+  g_side_limit.store(n);
   return MARBLE_OK;
 }
 

@@ -955,16 +955,17 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     std::lock_guard<std::mutex> lock(pl->scratch_mu);
     const size_t need = (size_t)(nbuf * buf_slots) * 32768;
     if (need > pl->ds_scratch_bytes) {
+      // earlier calls joined their side streams back into their stream, and calls on one
+      // plan are ordered: freeing in the order of `s` is safe
       if (pl->ds_scratch) {
-        cudaDeviceSynchronize();
-        cudaFree(pl->ds_scratch);
+        dev_free(pl->ds_scratch, s);
         pl->ds_scratch = nullptr;
         pl->ds_scratch_bytes = 0;
       }
       void* q = nullptr;
-      if (cudaMalloc(&q, need) != cudaSuccess) {
+      if (dev_alloc(&q, need, s) != cudaSuccess) {
         (void)cudaGetLastError();
-        return fail(MARBLE_ERR_OOM, "cudaMalloc of the backward dS scratch failed (" +
+        return fail(MARBLE_ERR_OOM, "allocation of the backward dS scratch failed (" +
                                         std::to_string(need) + " bytes)");
       }
       pl->ds_scratch = q;

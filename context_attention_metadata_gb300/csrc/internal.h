@@ -38,6 +38,7 @@ struct marble_plan {
   int64_t n = 0, nb = 0;
   int P = 1, W = 0, order = 0, chunk_tokens = 0;
   int64_t range_cost = 0;                       // CHUNK_SEARCH: tau
+  cudaStream_t build_stream = nullptr;          // the stream marble_plan ran on
   int64_t chunks_per_rank = 0, layout_cost = 0, layout_step_cost = 0;  // its result
   unsigned long long* shard_pairs = nullptr;    // [P*P] statistics: legal pairs per shard pair
   int32_t* kiv = nullptr;       // [2*n] new order: lo, hi of every key's visible query interval
@@ -137,6 +138,13 @@ bool once_per_device(int key);
 
 // a second stream of the current device (nullptr if it cannot be created), and an ordering
 // edge from everything queued on `from` so far to everything queued on `to` afterwards
+// Device memory of plans, planner temporaries and the backward scratch comes from a
+// library-owned memory pool per device, allocated and freed in stream order: no call
+// synchronises the device (cudaFree does), and freed blocks stay in the pool for the next
+// plan.
+cudaError_t dev_alloc(void** p, size_t bytes, cudaStream_t s);
+cudaError_t dev_free(void* p, cudaStream_t s);
+
 constexpr int kSideStreams = 4;
 cudaStream_t side_stream(int idx = 0);
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);

@@ -675,10 +675,10 @@ template <typename T>
 static marble_status_t dalloc(marble_plan_t* p, T** ptr, size_t count) {
   void* q = nullptr;
   const size_t bytes = count * sizeof(T) > 0 ? count * sizeof(T) : 16;
-  cudaError_t e = cudaMalloc(&q, bytes);
+  cudaError_t e = dev_alloc(&q, bytes, p->build_stream);
   if (e != cudaSuccess) {
     (void)cudaGetLastError();
-    return fail(MARBLE_ERR_OOM, "cudaMalloc of plan workspace failed (" +
+    return fail(MARBLE_ERR_OOM, "allocation of plan workspace failed (" +
                                     std::to_string(bytes) + " bytes)");
   }
   p->owned.push_back(q);
@@ -893,6 +893,7 @@ void chunk_layout_host(const std::vector<int64_t>& wf, int Kf, int P, int64_t ta
   } while (0)
 
 marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_plan_t* p) {
+  p->build_stream = s;
   const int64_t n = p->n, nb = p->nb;
   const int P = p->P, W = p->W;
   const int64_t bps = p->bps;
@@ -925,10 +926,10 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   std::vector<void*> scratch;
   auto salloc = [&](int32_t** ptr, size_t count) -> marble_status_t {
     void* q = nullptr;
-    cudaError_t e = cudaMalloc(&q, (count ? count : 1) * sizeof(int32_t));
+    cudaError_t e = dev_alloc(&q, (count ? count : 1) * sizeof(int32_t), s);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
-      return fail(MARBLE_ERR_OOM, "cudaMalloc of planner scratch failed");
+      return fail(MARBLE_ERR_OOM, "allocation of planner scratch failed");
     }
     scratch.push_back(q);
     *ptr = static_cast<int32_t*>(q);
@@ -936,10 +937,11 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   };
   struct Freer {
     std::vector<void*>* v;
+    cudaStream_t s;
     ~Freer() {
-      for (void* q : *v) cudaFree(q);
+      for (void* q : *v) dev_free(q, s);  // in stream order, after the kernels that use it
     }
-  } freer{&scratch};
+  } freer{&scratch, s};
   const int ub = (p->order == MARBLE_ORDER_PTRR_CHUNK) ? p->chunk_tokens / kBlock : 1;
   const int64_t units = nb / ub;
   MARBLE_TRY(salloc(&cnt, nb));
@@ -998,10 +1000,10 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
     const int Kf = finest_chunks(nb, P);
     const int cs = (int)(nb / Kf);
     void* wq = nullptr;
-    cudaError_t e = cudaMalloc(&wq, (size_t)Kf * Kf * sizeof(unsigned long long));
+    cudaError_t e = dev_alloc(&wq, (size_t)Kf * Kf * sizeof(unsigned long long), s);
     if (e != cudaSuccess) {
       (void)cudaGetLastError();
-      return fail(MARBLE_ERR_OOM, "cudaMalloc of the chunk-pair matrix failed");
+      return fail(MARBLE_ERR_OOM, "allocation of the chunk-pair matrix failed");
     }
     scratch.push_back(wq);
     auto* wc = static_cast<unsigned long long*>(wq);

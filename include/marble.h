@@ -363,6 +363,14 @@ marble_status_t marble_check(const marble_plan_t *plan, marble_stream_t stream);
 marble_status_t marble_set_wait_limit_ns(uint64_t ns);
 
 /*
+ * Process-wide cap on the side streams that marble_attn_steps and marble_attn_bwd_steps
+ * spread their launches over (default 4, the most they use; 0 runs every launch in list
+ * order on the caller's stream).  Results do not depend on it.  Errors: INVALID_ARG if n is
+ * outside [0, 4].
+ */
+marble_status_t marble_set_side_streams(int32_t n);
+
+/*
  * Per-kernel device timing, a measurement hook (off by default).  While it is on, every
  * marble_attn_step(s) / marble_attn_bwd(_steps) call records CUDA events, on the stream each
  * kernel runs on, before its first and after its last launch of that kernel, and counts the

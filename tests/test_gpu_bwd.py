@@ -98,3 +98,24 @@ def test_full_configs_backward_sampled(cid):
     c_t = torch.as_tensor(cols).cuda()
     assert rel_fro(dk[c_t][:, :1].cpu().double().numpy(), rk) <= TOL_GRAD_REL
     assert rel_fro(dv[c_t][:, :1].cpu().double().numpy(), rv) <= TOL_GRAD_REL
+
+
+def test_results_do_not_depend_on_stream_overlap():
+    # the step-list calls spread launches over side streams; launches that add into the same
+    # rows stay ordered, so every result is bit-identical with all launches on one stream
+    import context_attention_metadata_gb300 as M
+    from marble_testlib import run_forward
+    cfg = wl.mini_config(2, 8192, hq=2)
+    tr = wl.config_tracks(2, cfg.n)
+    q, k, v, do = wl.make_qkvdo(cfg.n, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=4)
+    pl = plan_for(cfg, tr)
+    out = []
+    try:
+        for n_side in (4, 0):
+            M.set_side_streams(n_side)
+            O, L, _ = run_forward(pl, q, k, v)
+            out.append((O, L) + tuple(run_backward(pl, q, k, v, do)))
+    finally:
+        M.set_side_streams(4)
+    for a, b in zip(*out):
+        assert torch.equal(a, b)
