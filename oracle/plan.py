@@ -384,3 +384,47 @@ def key_intervals(tr, W):
 def interval_blocks(exact) -> np.ndarray:
     """Per 128-token block: True if every key of the block has an exact interval."""
     return np.asarray(exact).reshape(-1, BLOCK).all(axis=1)
+
+
+# --------------------------------------------------------------------------------------
+# vision-group layout
+# --------------------------------------------------------------------------------------
+def vision_group_layout(tr) -> np.ndarray:
+    """The vision-group layout transform (MARBLE post, section 04 "Layout transforms"): in
+    every sample, first every token outside an image group, in order ("all the text first"),
+    then the group's spans, the last span first ("its group spans after in reverse").  An
+    image group is a segment id that forms more than one run of consecutive tokens in the
+    sample; a span is one such run.  Tokens keep their original positions, so the mask is
+    unchanged.  Returns perm: new index -> original index."""
+    sample = np.asarray(tr["sample"])
+    seg = np.asarray(tr["seg"])
+    n = len(sample)
+    out = []
+    starts = np.flatnonzero(np.r_[True, sample[1:] != sample[:-1]])
+    ends = np.r_[starts[1:], n]
+    for a, b in zip(starts, ends):
+        runs = []                      # (start, end, seg) of every run in the sample
+        i = a
+        while i < b:
+            j = i + 1
+            while j < b and seg[j] == seg[i]:
+                j += 1
+            runs.append((i, j, int(seg[i])))
+            i = j
+        nruns = {}
+        for _, _, g in runs:
+            if g >= 0:
+                nruns[g] = nruns.get(g, 0) + 1
+        grouped = [r for r in runs if r[2] >= 0 and nruns[r[2]] > 1]
+        for r in runs:
+            if not (r[2] >= 0 and nruns[r[2]] > 1):
+                out.extend(range(r[0], r[1]))
+        for r in reversed(grouped):
+            out.extend(range(r[0], r[1]))
+    return np.asarray(out, np.int64)
+
+
+def apply_layout(tr, perm):
+    """Tracks of the permuted pack, each token carrying its original position."""
+    sample, seg, noise, pos = tracks_with_pos(tr)
+    return {"sample": sample[perm], "seg": seg[perm], "noise": noise[perm], "pos": pos[perm]}

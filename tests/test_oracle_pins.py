@@ -719,3 +719,32 @@ def test_key_intervals_reproduce_the_mask(seed):
     test = (q >= lo[None, :]) & (q < hi[None, :])
     assert (test[:, ex] == M[:, ex]).all()
     assert (M[:, ~ex] & ~test[:, ~ex]).sum() == 0  # the interval always covers the visible set
+
+
+def test_vision_group_layout_by_hand_and_contiguity():
+    # T0 G1a T1 G1b T2 G2a T3 G2b: text first, then the group spans last first
+    L = 40
+    samples = [[wl.Span("causal", L), wl.Span("group", L, 1), wl.Span("causal", L),
+                wl.Span("group", L, 1), wl.Span("causal", L), wl.Span("group", L, 2),
+                wl.Span("causal", L), wl.Span("group", L, 2)],
+               [wl.Span("causal", 16), wl.Span("full", 24)]]
+    tr = wl.tracks_from_samples(samples)
+    perm = plan.vision_group_layout(tr)
+    T = [np.arange(i * L, (i + 1) * L) for i in range(8)]
+    want = np.concatenate([T[0], T[2], T[4], T[6], T[7], T[5], T[3], T[1],
+                           np.arange(8 * L, 8 * L + 40)])
+    assert np.array_equal(perm, want)
+    trp = plan.apply_layout(tr, perm)
+    n = len(perm)
+    # the mask is the same mask, read in the new order
+    assert np.array_equal(mask.dense_mask(trp, INF), mask.dense_mask(tr, INF)[np.ix_(perm, perm)])
+    # before: keys of later group spans see a broken range; after: every key's is one range
+    _, _, ex0 = plan.key_intervals(tr, INF)
+    _, _, ex1 = plan.key_intervals(trp, INF)
+    assert not ex0.all() and ex1.all()
+
+
+def test_vision_group_layout_is_identity_without_groups():
+    rng = np.random.default_rng(31)
+    tr = wl.tracks_from_samples(wl.packed_mix_samples(rng, 4096))
+    assert np.array_equal(plan.vision_group_layout(tr), np.arange(4096))

@@ -176,6 +176,27 @@ def video_generation_samples(rng: np.random.Generator, n: int,
     return _truncate(samples, n)
 
 
+def video_group_samples(rng: np.random.Generator, n: int) -> List[List[Span]]:
+    """Video question-answer samples whose frames form one image group (the vision-group
+    packs the MARBLE post's layout transform is built for, section 04): a causal prompt of
+    U[64, 512] tokens, then 32..256 frames of F ~ U{64, 128, 192, 256} tokens (one F per
+    sample, all frames one group: joint bidirectional attention) each followed by a causal
+    timestamp of U[4, 16] tokens, then a causal answer of U[64, 1024] tokens.
+    """
+    samples: List[List[Span]] = []
+    total = 0
+    while total < n:
+        F = int(rng.choice([64, 128, 192, 256]))
+        s = [Span("causal", int(rng.integers(64, 513)))]
+        for _ in range(int(rng.integers(32, 257))):
+            s.append(Span("group", F, group=0))
+            s.append(Span("causal", int(rng.integers(4, 17))))
+        s.append(Span("causal", int(rng.integers(64, 1025))))
+        samples.append(s)
+        total += sum(sp.length for sp in s)
+    return _truncate(samples, n)
+
+
 # --------------------------------------------------------------------------------------
 # configurations
 # --------------------------------------------------------------------------------------
@@ -223,6 +244,9 @@ EXTRA: Dict[int, Config] = {
               description="N=1048576 long-video generation samples (128K-1M tokens of "
                           "interleaved noise / clean frames); P=16, searched chunk layout, "
                           "tau = 167800 legal pairs (fitted to emulated ring times on GB300)"),
+    7: Config(7, "video_group_512k", 524288, 8, 8, 128, 16, "ptrr_block",
+              description="N=524288 video question-answer samples, frames of 64-256 tokens in "
+                          "one image group with timestamps between; P=16 PTRR"),
 }
 
 
@@ -246,6 +270,8 @@ def config_samples(cid: int, n: Optional[int] = None) -> List[List[Span]]:
         return grouped_image_samples(rng, n)
     if cid == 6:
         return video_generation_samples(rng, n, (min(n, 131072), min(n, 1048576)))
+    if cid == 7:
+        return video_group_samples(rng, n)
     raise KeyError(cid)
 
 
