@@ -152,7 +152,8 @@ def oracle_sample_rate(cfg, tr, budget_s: float, seed: int = 0):
         idx = np.flatnonzero(st == sid)[:4096]
         L = len(idx)
         sub = {k: np.asarray(v)[idx] for k, v in tr.items()}
-        sub["pos"] = idx
+        if "pos" not in tr:
+            sub["pos"] = idx
         q = torch.randn((L, cfg.hq, cfg.d), generator=g).to(torch.bfloat16)
         k = torch.randn((L, cfg.hkv, cfg.d), generator=g).to(torch.bfloat16)
         v = torch.randn((L, cfg.hkv, cfg.d), generator=g).to(torch.bfloat16)
@@ -185,6 +186,14 @@ def workload(args):
     elif args.range_cost:
         cfg = dataclasses.replace(cfg, range_cost=args.range_cost)
     tr = wl.config_tracks(cid) if args.tokens <= 0 else wl.config_tracks(cid, cfg.n)
+    if args.layout == "vision_groups":
+        # the tokens in the vision-group order, each carrying its original position
+        import numpy as np
+        import context_attention_metadata_gb300 as M
+        perm = M.layout_vision_groups(tr["sample"], tr["seg"]).astype(np.int64)
+        tr = {"sample": tr["sample"][perm], "seg": tr["seg"][perm], "noise": tr["noise"][perm],
+              "pos": perm.astype(np.int32)}
+        cfg = dataclasses.replace(cfg, name=f"{cfg.name}_vision_groups")
     return cfg, tr
 
 
@@ -236,6 +245,7 @@ def run_marble(args, rank, world, local, dist):
     n, hq, hkv, d, P = cfg.n, cfg.hq, cfg.hkv, cfg.d, cfg.shards
     needed = cfg.needed
     trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    pos_t = torch.as_tensor(np.asarray(tr["pos"], np.int32)).cuda() if "pos" in tr else None
     stream = torch.cuda.current_stream()
 
     # plan: built once per pack, timed on its own (best of 3)
@@ -247,7 +257,8 @@ def run_marble(args, rank, world, local, dist):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens,
-                    range_cost=cfg.range_cost, key_intervals=not args.no_key_intervals)
+                    range_cost=cfg.range_cost, key_intervals=not args.no_key_intervals,
+                    pos=pos_t)
         torch.cuda.synchronize()
         plan_ms.append(1e3 * (time.perf_counter() - t0))
     stats = pl.stats()
@@ -386,7 +397,7 @@ def run_marble(args, rank, world, local, dist):
     e2e = None
     if args.e2e_steps > 0:
         hq_pin = [t.cpu().pin_memory() for t in (q, k, v, do)]
-        htr = [t.cpu().pin_memory() for t in trk]
+        htr = [t.cpu().pin_memory() for t in trk + ([pos_t] if pos_t is not None else [])]
         shapes = ((n, hq, d), (n, hq, d), (n, hkv, d), (n, hkv, d))
         out_pin = [[torch.empty(s_, dtype=torch.bfloat16).pin_memory() for s_ in shapes]
                    for _ in range(2)]
@@ -422,7 +433,8 @@ def run_marble(args, rank, world, local, dist):
                 comp.wait_event(ev_in[b])
                 p2 = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P, cfg.order,
                             cfg.chunk_tokens, range_cost=cfg.range_cost,
-                            key_intervals=not args.no_key_intervals)
+                            key_intervals=not args.no_key_intervals,
+                            pos=dev_tr[b][3] if pos_t is not None else None)
                 plans.append(p2)
                 q2, k2, v2, do2 = (p2.permute(t) for t in dev_in[b])
                 M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
@@ -499,6 +511,7 @@ def run_marble(args, rank, world, local, dist):
                        "shards": P, "order": cfg.order, "window": cfg.window,
                        "range_cost": cfg.range_cost if cfg.order == "chunk_search" else None,
                        "key_intervals": not args.no_key_intervals,
+                       "layout": args.layout or "as generated",
                        "schedule": "needed-blocks" if needed else "ring r-major P^2 steps",
                        "l2": "inputs larger than L2 (Q/K/V/dO 256 MiB each; state 512 MiB)",
                        "legal_pairs_per_head": pairs, "flops_per_step": flops,
@@ -534,8 +547,9 @@ def run_profile_pass(args):
     import workloads as wl
     cfg, tr = workload(args)
     trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    pos_t = torch.as_tensor(np.asarray(tr["pos"], np.int32)).cuda() if "pos" in tr else None
     pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens,
-                range_cost=cfg.range_cost)
+                range_cost=cfg.range_cost, pos=pos_t)
     n, hq, hkv, d = cfg.n, cfg.hq, cfg.hkv, cfg.d
     q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda")
     qp, kp, vp, dop = (pl.permute(t) for t in (q, k, v, do))
@@ -569,10 +583,11 @@ def run_emulated_ring(args):
     cfg, tr = workload(args)
     n, hq, hkv, d, P = cfg.n, cfg.hq, cfg.hkv, cfg.d, cfg.shards
     trk = [torch.as_tensor(np.asarray(tr[x], np.int32)).cuda() for x in ("sample", "seg", "noise")]
+    pos_t = torch.as_tensor(np.asarray(tr["pos"], np.int32)).cuda() if "pos" in tr else None
     torch.cuda.synchronize()
     t0 = time.perf_counter()
     pl = M.Plan(trk[0], trk[1], trk[2], cfg.window, P, cfg.order, cfg.chunk_tokens,
-                range_cost=cfg.range_cost)
+                range_cost=cfg.range_cost, pos=pos_t)
     torch.cuda.synchronize()
     plan_ms = 1e3 * (time.perf_counter() - t0)
     stats = pl.stats()
@@ -652,6 +667,8 @@ def main():
     ap.add_argument("--chunk-tokens", type=int, default=0, help="with --order ptrr_chunk")
     ap.add_argument("--range-cost", type=int, default=0,
                     help="with the chunk_search order: tau, legal pairs per range and step")
+    ap.add_argument("--layout", default="", choices=["", "vision_groups"],
+                    help="side measurement: run the workload in another token layout")
     ap.add_argument("--no-key-intervals", action="store_true",
                     help="side measurement: partial tiles always evaluate the four-track "
                          "predicate")

@@ -50,7 +50,8 @@ class _PlanDesc(ctypes.Structure):
                 ("seg_id", ctypes.c_void_p), ("noise_id", ctypes.c_void_p),
                 ("window", ctypes.c_int32), ("num_shards", ctypes.c_int32),
                 ("order", ctypes.c_int32), ("chunk_tokens", ctypes.c_int32),
-                ("range_cost", ctypes.c_int64), ("no_key_intervals", ctypes.c_int32)]
+                ("range_cost", ctypes.c_int64), ("no_key_intervals", ctypes.c_int32),
+                ("pos_id", ctypes.c_void_p)]
 
 
 class _PlanStats(ctypes.Structure):
@@ -77,6 +78,8 @@ _SIGS = {
     "marble_plan": ([ctypes.POINTER(_PlanDesc), ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]),
     "marble_plan_destroy": ([ctypes.c_void_p]),
     "marble_plan_stats": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(_PlanStats)]),
+    "marble_layout_vision_groups": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                     ctypes.c_void_p]),
     "marble_chunk_layout_search": ([ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
                                     ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]),
     "marble_plan_field_bytes": ([ctypes.c_void_p, ctypes.c_int32, ctypes.POINTER(ctypes.c_size_t)]),
@@ -169,17 +172,20 @@ class Plan:
 
     def __init__(self, sample, seg, noise, window: int, num_shards: int,
                  order: str = "contiguous", chunk_tokens: int = 0, stream=None,
-                 range_cost: int = 0, key_intervals: bool = True):
+                 range_cost: int = 0, key_intervals: bool = True, pos=None):
         import torch
         for t, nm in ((sample, "sample"), (seg, "seg"), (noise, "noise")):
             _need(t, torch.int32, nm, (sample.shape[0],))
+        if pos is not None:
+            _need(pos, torch.int32, "pos", (sample.shape[0],))
         self.n = int(sample.shape[0])
         self.num_shards = int(num_shards)
         self.window = int(window)
         self.order = order
         d = _PlanDesc(self.n, sample.data_ptr(), seg.data_ptr(), noise.data_ptr(),
                       int(window), int(num_shards), ORDERS[order], int(chunk_tokens),
-                      int(range_cost), 0 if key_intervals else 1)
+                      int(range_cost), 0 if key_intervals else 1,
+                      pos.data_ptr() if pos is not None else None)
         h = ctypes.c_void_p()
         _call("marble_plan", ctypes.byref(d), _stream(stream), ctypes.byref(h))
         self._h = h
@@ -418,6 +424,20 @@ def backward(plan: Plan, q, k, v, o, do, lse, delta, dq_acc, dk_acc, dv_acc,
     attn_bwd_prep(plan, o, do, delta, stream=stream)
     attn_bwd_steps(plan, q, k, v, do, lse, delta, ring_schedule(plan.num_shards, needed),
                    dq_acc, dk_acc, dv_acc, scale=scale, stream=stream)
+
+
+def layout_vision_groups(sample, seg):
+    """The vision-group layout (marble_layout_vision_groups) of host int32 tracks: returns
+    perm (new index -> index), an int32 numpy array."""
+    import numpy as np
+    s_ = np.ascontiguousarray(sample, dtype=np.int32)
+    g_ = np.ascontiguousarray(seg, dtype=np.int32)
+    if s_.shape != g_.shape or s_.ndim != 1:
+        raise ValueError("sample and seg must be 1-D arrays of one length")
+    perm = np.empty(len(s_), np.int32)
+    _call("marble_layout_vision_groups", s_.ctypes.data, g_.ctypes.data, len(s_),
+          perm.ctypes.data)
+    return perm
 
 
 def chunk_layout_search(block_pairs, num_shards: int, range_cost: int = 0):

@@ -235,6 +235,8 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
   }
   if (!is_device_ptr(d->sample_id) || !is_device_ptr(d->seg_id) || !is_device_ptr(d->noise_id))
     return fail(MARBLE_ERR_INVALID_ARG, "track arrays must be device memory");
+  if (d->pos_id && !is_device_ptr(d->pos_id))
+    return fail(MARBLE_ERR_INVALID_ARG, "pos_id must be device memory");
   marble_plan_t* p = new (std::nothrow) marble_plan_t();
   if (!p) return fail(MARBLE_ERR_OOM, "host allocation failed");
   cudaGetDevice(&p->device);
@@ -289,6 +291,45 @@ MARBLE_API marble_status_t marble_chunk_layout_search(const int64_t* block_pairs
   marble::chunk_layout_host(wf, Kf, num_shards, range_cost, &k, &rank, &out[1], &out[2]);
   out[0] = k;
   for (size_t u = 0; u < rank.size(); ++u) chunk_rank[u] = rank[u];
+  return MARBLE_OK;
+}
+
+MARBLE_API marble_status_t marble_layout_vision_groups(const int32_t* sample, const int32_t* seg,
+                                                       int64_t n, int32_t* perm) {
+  if (!sample || !seg || !perm) return fail(MARBLE_ERR_INVALID_ARG, "arrays must be non-null");
+  if (n < 0 || n >= (int64_t)INT_MAX) return fail(MARBLE_ERR_INVALID_ARG, "bad n");
+  for (int64_t i = 0; i < n; ++i)
+    if ((i > 0 && sample[i] < sample[i - 1]) || sample[i] < 0 || seg[i] < -1)
+      return fail(MARBLE_ERR_INVALID_ARG,
+                  "sample ids must be >= 0 and non-decreasing, seg ids >= -1");
+  int64_t o = 0;
+  std::map<int32_t, int> nruns;
+  std::vector<std::pair<int64_t, int64_t>> runs, grouped;
+  for (int64_t a = 0; a < n;) {
+    int64_t b = a;
+    while (b < n && sample[b] == sample[a]) ++b;  // the sample [a, b)
+    runs.clear();
+    nruns.clear();
+    for (int64_t i = a; i < b;) {
+      int64_t j = i + 1;
+      while (j < b && seg[j] == seg[i]) ++j;
+      runs.push_back({i, j});
+      if (seg[i] >= 0) ++nruns[seg[i]];
+      i = j;
+    }
+    grouped.clear();
+    for (const auto& r : runs) {
+      const int32_t g = seg[r.first];
+      if (g >= 0 && nruns[g] > 1) {
+        grouped.push_back(r);
+      } else {
+        for (int64_t t = r.first; t < r.second; ++t) perm[o++] = (int32_t)t;
+      }
+    }
+    for (auto it = grouped.rbegin(); it != grouped.rend(); ++it)
+      for (int64_t t = it->first; t < it->second; ++t) perm[o++] = (int32_t)t;
+    a = b;
+  }
   return MARBLE_OK;
 }
 

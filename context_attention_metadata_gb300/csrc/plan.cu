@@ -37,19 +37,23 @@ __device__ __forceinline__ unsigned lanemask_lt() {
 // a1 + a2: validation and block summaries (one warp per block, 4 tokens per lane)
 // ------------------------------------------------------------------------------------
 __global__ void k_summaries(const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
-                            const int32_t* __restrict__ noise, int64_t nb,
-                            Summary* __restrict__ out, unsigned* err) {
+                            const int32_t* __restrict__ noise, const int32_t* __restrict__ pos,
+                            int64_t nb, Summary* __restrict__ out, unsigned* err) {
   const int lane = threadIdx.x & 31;
   const int64_t b = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   if (b >= nb) return;
   const int64_t t0 = b * kBlock + lane * 4;
   int slo = INT_MAX, shi = INT_MIN, nlo = INT_MAX, nhi = INT_MIN, glo = INT_MAX, ghi = -1;
+  int plo = INT_MAX, phi = INT_MIN;  // positions: the index unless a position track is given
   unsigned blo = 0, bhi = 0;
   bool any_seg = false, all_seg = true, bad = false;
   int prev = t0 > 0 ? sample[t0 - 1] : INT_MIN;
   for (int i = 0; i < 4; ++i) {
     const int s = sample[t0 + i], g = seg[t0 + i], z = noise[t0 + i];
-    bad |= (s < 0) | (g < -1) | (z < -1) | (s < prev);
+    const int ps = pos ? pos[t0 + i] : (int)(t0 + i);
+    bad |= (s < 0) | (g < -1) | (z < -1) | (s < prev) | (ps < 0);
+    plo = min(plo, ps);
+    phi = max(phi, ps);
     prev = s;
     slo = min(slo, s); shi = max(shi, s);
     nlo = min(nlo, z); nhi = max(nhi, z);
@@ -66,6 +70,7 @@ __global__ void k_summaries(const int32_t* __restrict__ sample, const int32_t* _
   slo = __reduce_min_sync(full, slo); shi = __reduce_max_sync(full, shi);
   nlo = __reduce_min_sync(full, nlo); nhi = __reduce_max_sync(full, nhi);
   glo = __reduce_min_sync(full, glo); ghi = __reduce_max_sync(full, ghi);
+  plo = __reduce_min_sync(full, plo); phi = __reduce_max_sync(full, phi);
   blo = __reduce_or_sync(full, blo); bhi = __reduce_or_sync(full, bhi);
   const bool has = __any_sync(full, any_seg);
   const bool all = __all_sync(full, all_seg);
@@ -73,7 +78,7 @@ __global__ void k_summaries(const int32_t* __restrict__ sample, const int32_t* _
   if (lane == 0) {
     Summary r;
     r.slo = slo; r.shi = shi; r.nlo = nlo; r.nhi = nhi; r.glo = glo; r.ghi = ghi;
-    r.plo = (int)(b * kBlock); r.phi = (int)(b * kBlock + kBlock - 1);
+    r.plo = plo; r.phi = phi;
     r.gbits = ((unsigned long long)bhi << 32) | blo;
     r.flags = (has ? 1 : 0) | (all ? 2 : 0);
     r.pad = 0;
@@ -261,7 +266,8 @@ __global__ void k_block_perm(const int32_t* __restrict__ unit_new, int ub, int64
 
 __global__ void k_perm_tracks(const int32_t* __restrict__ block_perm,
                               const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
-                              const int32_t* __restrict__ noise, int64_t n,
+                              const int32_t* __restrict__ noise, const int32_t* __restrict__ pos,
+                              int64_t n,
                               int32_t* __restrict__ perm, int32_t* __restrict__ tracks) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= n) return;
@@ -270,7 +276,7 @@ __global__ void k_perm_tracks(const int32_t* __restrict__ block_perm,
   tracks[t] = sample[o];
   tracks[n + t] = seg[o];
   tracks[2 * n + t] = noise[o];
-  tracks[3 * n + t] = (int32_t)o;
+  tracks[3 * n + t] = pos ? pos[o] : (int32_t)o;
 }
 
 // ------------------------------------------------------------------------------------
@@ -629,7 +635,7 @@ __global__ void k_legal_pairs(const int64_t* __restrict__ row_ptr, const int32_t
 __global__ void k_chunk_pairs(const int64_t* __restrict__ row_ptr, const int32_t* __restrict__ col,
                               const uint8_t* __restrict__ tag, const int32_t* __restrict__ sample,
                               const int32_t* __restrict__ seg, const int32_t* __restrict__ noise,
-                              int64_t nb, int W, int cs, int K,
+                              const int32_t* __restrict__ pos, int64_t nb, int W, int cs, int K,
                               unsigned long long* __restrict__ wc) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
@@ -643,10 +649,10 @@ __global__ void k_chunk_pairs(const int64_t* __restrict__ row_ptr, const int32_t
       } else {
         for (int qi = lane; qi < kBlock; qi += 32) {
           const int64_t q = qb * kBlock + qi;
-          const int sq = sample[q], gq = seg[q], zq = noise[q];
+          const int sq = sample[q], gq = seg[q], zq = noise[q], pq = pos ? pos[q] : (int)q;
           for (int ki = 0; ki < kBlock; ++ki) {
             const int64_t k = kb * kBlock + ki;
-            c += mask_legal(sq, gq, zq, (int)q, sample[k], seg[k], noise[k], (int)k, W);
+            c += mask_legal(sq, gq, zq, pq, sample[k], seg[k], noise[k], pos ? pos[k] : (int)k, W);
           }
         }
       }
@@ -959,8 +965,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_CK(cudaMemsetAsync(cntT, 0, nb * P * sizeof(int32_t), s));
 
   // a1 + a2
-  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(d->sample_id, d->seg_id, d->noise_id, nb,
-                                                      p->summ, p->err);
+  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(d->sample_id, d->seg_id, d->noise_id,
+                                                      d->pos_id, nb, p->summ, p->err);
   MARBLE_CK(cudaGetLastError());
   unsigned herr = 0;
   MARBLE_CK(cudaMemcpyAsync(&herr, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
@@ -968,7 +974,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   if (herr & kErrBadTracks)
     return fail(MARBLE_ERR_INVALID_ARG,
                 "metadata check failed: sample ids must be >= 0 and non-decreasing, seg and "
-                "noise ids >= -1");
+                "noise ids >= -1, positions >= 0");
 
   // a3
   k_band<<<grid_for(nb, threads), threads, 0, s>>>(p->summ, nb, p->band);
@@ -1009,7 +1015,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
     auto* wc = static_cast<unsigned long long*>(wq);
     MARBLE_CK(cudaMemsetAsync(wc, 0, (size_t)Kf * Kf * sizeof(unsigned long long), s));
     k_chunk_pairs<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->row_ptr, p->col, p->tag, d->sample_id,
-                                                          d->seg_id, d->noise_id, nb, W, cs, Kf, wc);
+                                                          d->seg_id, d->noise_id, d->pos_id, nb, W,
+                                                          cs, Kf, wc);
     MARBLE_CK(cudaGetLastError());
     std::vector<int64_t> wf((size_t)Kf * Kf);
     MARBLE_CK(cudaMemcpyAsync(wf.data(), wc, wf.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s));
@@ -1033,7 +1040,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
                                                             p->inv_block_perm);
   }
   k_perm_tracks<<<grid_for(n, threads), threads, 0, s>>>(p->block_perm, d->sample_id, d->seg_id,
-                                                          d->noise_id, n, p->perm, p->tracks);
+                                                          d->noise_id, d->pos_id, n, p->perm,
+                                                          p->tracks);
   MARBLE_CK(cudaGetLastError());
 
   // key intervals (all blocks flagged 0 when switched off: partial tiles then always
@@ -1042,7 +1050,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->iv_block, nb));
   MARBLE_CK(cudaMemsetAsync(p->kiv, 0, 2 * n * sizeof(int32_t), s));
   MARBLE_CK(cudaMemsetAsync(p->iv_block, 0, nb, s));
-  if (!d->no_key_intervals) {
+  // (the interval rule reads positions as indices: with a position track it stays off)
+  if (!d->no_key_intervals && !d->pos_id) {
     int32_t *tab = nullptr, *klo = nullptr;
     MARBLE_TRY(salloc(&tab, 6 * n));
     MARBLE_TRY(salloc(&klo, 2 * n + (nb + 3) / 4));
@@ -1260,7 +1269,8 @@ extern "C" __attribute__((visibility("default"))) marble_status_t marble_tile_ma
   const int warp_ctas = (int)grid_for(nb, kWarpsPerCta);
   // the validation word accumulates with atomicOr: it must start at zero on every call
   MARBLE_CK(cudaMemsetAsync(err, 0, sizeof(unsigned), s));
-  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(sample_id, seg_id, noise_id, nb, summ, err);
+  k_summaries<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(sample_id, seg_id, noise_id, nullptr, nb,
+                                                      summ, err);
   k_band<<<grid_for(nb, 256), 256, 0, s>>>(summ, nb, band);
   k_tiles_count<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(summ, band, nb, window, cnt);
   k_scan<int32_t><<<1, 1024, 0, s>>>(cnt, nb, row_ptr);

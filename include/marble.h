@@ -128,6 +128,11 @@ typedef struct {
                            one ring step, in legal pairs */
   int32_t no_key_intervals; /* 1: partial tiles always evaluate the four-track predicate;
                                0 (default): key-interval test where it is exact */
+  const int32_t *pos_id;    /* NULL: a token's position is its index.  Otherwise device
+                               int32[n_tokens] >= 0, the original position of every token of
+                               a permuted pack (MARBLE s04 "Layout transforms": tokens carry
+                               their position), read during marble_plan only; the key-interval
+                               test is then off */
 } marble_plan_desc_t;
 
 typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
@@ -181,6 +186,20 @@ typedef struct {
 marble_status_t marble_chunk_layout_search(const int64_t *block_pairs, int64_t n_blocks,
                                            int32_t num_shards, int64_t range_cost,
                                            int32_t *chunk_rank, int64_t *out);
+
+/*
+ * The vision-group layout (MARBLE s04 "Layout transforms"), on the host: for host int32
+ * arrays sample[n] and seg[n] of a pack (same rules as marble_plan_desc_t), writes perm[n],
+ * new index -> index in the given order.  In every sample the tokens outside image groups
+ * come first, in order, then the group spans, the last span first; an image group is a
+ * segment id with more than one run of consecutive tokens in the sample, a span one such
+ * run.  Apply perm to every per-token array (activations and the three tracks) and pass the
+ * tokens' original positions (perm itself, for a pack in position order) as pos_id: the
+ * mask is unchanged, and each key's visible queries form one range in the new order.
+ * Errors: INVALID_ARG.
+ */
+marble_status_t marble_layout_vision_groups(const int32_t *sample, const int32_t *seg, int64_t n,
+                                            int32_t *perm);
 
 /* Plan statistics; counts legal pairs with a kernel over the partial tiles (full tiles
  * contribute 128*128 each).  Synchronises `stream`. */
