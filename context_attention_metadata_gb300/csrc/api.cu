@@ -50,9 +50,7 @@ bool once_per_device(int key) {
   return seen.insert({key, dev}).second;
 }
 
-// Fork / join of a per-device side stream: work queued on the side stream between fork()
-// and join() runs after everything queued on `s` before fork(), and everything queued on `s`
-// after join() runs after it.
+// the most side streams the step-list calls may use (marble_set_side_streams)
 std::atomic<int> g_side_limit{kSideStreams};
 
 static cudaMemPool_t mem_pool() {
@@ -86,6 +84,10 @@ cudaError_t dev_alloc(void** p, size_t bytes, cudaStream_t s) {
 }
 
 cudaError_t dev_free(void* p, cudaStream_t s) { return cudaFreeAsync(p, s); }
+
+// Side streams, created once per device and index: work queued on one between a fork from
+// `s` and the join back into `s` runs after everything queued on `s` before the fork, and
+// everything queued on `s` after the join runs after it.
 
 cudaStream_t side_stream(int idx) {
   static std::mutex mu;

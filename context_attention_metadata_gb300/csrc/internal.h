@@ -136,8 +136,6 @@ marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, co
 // true the first time it is called for (key, current device); used for per-device set-up
 bool once_per_device(int key);
 
-// a second stream of the current device (nullptr if it cannot be created), and an ordering
-// edge from everything queued on `from` so far to everything queued on `to` afterwards
 // Device memory of plans, planner temporaries and the backward scratch comes from a
 // library-owned memory pool per device, allocated and freed in stream order: no call
 // synchronises the device (cudaFree does), and freed blocks stay in the pool for the next
@@ -145,6 +143,9 @@ bool once_per_device(int key);
 cudaError_t dev_alloc(void** p, size_t bytes, cudaStream_t s);
 cudaError_t dev_free(void* p, cudaStream_t s);
 
+// side stream idx of the current device (nullptr if it cannot be created or idx is at or
+// above the cap of marble_set_side_streams), and an ordering edge from everything queued on
+// `from` so far to everything queued on `to` afterwards
 constexpr int kSideStreams = 4;
 cudaStream_t side_stream(int idx = 0);
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to);

@@ -395,9 +395,10 @@ marble_status_t marble_set_side_streams(int32_t n);
  * kernel runs on, before its first and after its last launch of that kernel, and counts the
  * launches.  marble_timing_read synchronises on those events, adds up their spans since the
  * previous read and writes out[0..5] = forward ms, forward launches, dQ-kernel ms, dQ-kernel
- * launches, dK/dV-kernel ms, dK/dV-kernel launches.  The launches of one kernel on one stream
- * run back to back, so a span is the sum of their durations; different kernels may overlap
- * in time (they run on two streams).  Returns MARBLE_ERR_INVALID_ARG if `out` is null.
+ * launches, dK/dV-kernel ms, dK/dV-kernel launches.  Launches on different streams overlap
+ * in time (see marble_set_side_streams), and a launch that waits for SMs held by another
+ * stream's launch has that wait in its span; with the side streams capped at 0 every launch
+ * runs alone and a span is its duration.  Returns MARBLE_ERR_INVALID_ARG if `out` is null.
  */
 marble_status_t marble_timing_enable(int on);
 marble_status_t marble_timing_read(double *out);
