@@ -390,9 +390,9 @@ def run_marble(args, rank, world, local, dist):
     # end to end through the public API: H2D of the step's inputs from pinned memory,
     # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results.
     # Steps are pipelined the way a training loop runs them: the next step's inputs are
-    # copied in on one copy stream while this step computes, and this step's results are
-    # copied out on another while the next step plans and computes (double-buffered inputs
-    # and outputs).  Plans are destroyed after the timed steps (destroying one synchronises the
+    # copied in, and its plan built, on one copy stream while this step computes, and this
+    # step's results are copied out on another while the next step computes (double-buffered
+    # inputs and outputs).  Plans are destroyed after the timed steps (destroying one synchronises the
     # device).
     e2e = None
     if args.e2e_steps > 0:
@@ -412,30 +412,32 @@ def run_marble(args, rank, world, local, dist):
         comp = torch.cuda.current_stream()
 
         def e2e_run(K):
-            plans = []
-            ev_in, ev_used, ev_out, ev_d2h = ([torch.cuda.Event() for _ in range(2)]
-                                              for _ in range(4))
+            plans = [None] * K
+            ev_in, ev_used, ev_out, ev_d2h, ev_plan = ([torch.cuda.Event() for _ in range(2)]
+                                                       for _ in range(5))
 
-            def h2d(i):
+            def h2d_and_plan(i):
+                # inputs in on the copy stream, then the plan on that same stream: the
+                # planner's own synchronisations wait for the copies only, not for the
+                # previous step's compute
                 b = i % 2
                 with torch.cuda.stream(cs):
                     if i >= 2:
                         cs.wait_event(ev_used[b])   # step i - 2 is done with buffer b
                     for dst, src in zip(dev_in[b] + dev_tr[b], hq_pin + htr):
                         dst.copy_(src, non_blocking=True)
-                    ev_in[b].record(cs)
+                plans[i] = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P,
+                                  cfg.order, cfg.chunk_tokens, stream=cs,
+                                  range_cost=cfg.range_cost,
+                                  key_intervals=not args.no_key_intervals,
+                                  pos=dev_tr[b][3] if pos_t is not None else None)
+                ev_plan[b].record(cs)
 
-            h2d(0)
+            h2d_and_plan(0)
             for i in range(K):
                 b = i % 2
-                if i + 1 < K:
-                    h2d(i + 1)
-                comp.wait_event(ev_in[b])
-                p2 = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P, cfg.order,
-                            cfg.chunk_tokens, range_cost=cfg.range_cost,
-                            key_intervals=not args.no_key_intervals,
-                            pos=dev_tr[b][3] if pos_t is not None else None)
-                plans.append(p2)
+                p2 = plans[i]
+                comp.wait_event(ev_plan[b])
                 q2, k2, v2, do2 = (p2.permute(t) for t in dev_in[b])
                 M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
                 dq.zero_()
@@ -457,6 +459,8 @@ def run_marble(args, rank, world, local, dist):
                     for dst, src in zip(out_pin[b], ob):
                         dst.copy_(src, non_blocking=True)
                     ev_d2h[b].record(cs_out)
+                if i + 1 < K:
+                    h2d_and_plan(i + 1)             # while step i computes
             torch.cuda.synchronize()
             for p2 in plans:
                 p2.close()
@@ -472,8 +476,8 @@ def run_marble(args, rank, world, local, dist):
                "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
                "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H; "
-               "steps pipelined (copies on a copy stream overlap compute), plan teardown "
-               "after the timed steps"}
+               "steps pipelined (copies and the next step's plan on copy streams overlap "
+               "compute), plan teardown after the timed steps"}
 
     # the forward with each merge of the ring steps: the carried fp32 state (the timed step
     # above), the merge of fp32 partials and the standard merge of bf16 partials
