@@ -54,3 +54,14 @@ def test_host_side_argument_checks(libm):
     assert libm.marble_plan(ctypes.byref(d), None, ctypes.byref(h)) == M.ERR_INVALID_ARG
     assert b"multiple of 128" in libm.marble_last_error()
     assert b"sm_103a" in libm.marble_version()
+    # process-wide settings and host-only entry points
+    assert libm.marble_set_side_streams(5) == M.ERR_INVALID_ARG
+    assert libm.marble_set_side_streams(-1) == M.ERR_INVALID_ARG
+    assert libm.marble_set_side_streams(4) == M.OK
+    assert libm.marble_layout_vision_groups(None, None, 4, None) == M.ERR_INVALID_ARG
+    assert libm.marble_chunk_layout_search(None, 4, 2, 0, None, None) == M.ERR_INVALID_ARG
+    d = M._PlanDesc(1024, 0, 0, 0, 0, 2, 3, 0, -5)  # chunk search with a negative range cost
+    assert libm.marble_plan(ctypes.byref(d), None, ctypes.byref(h)) == M.ERR_INVALID_ARG
+    assert b"range_cost" in libm.marble_last_error()
+    d = M._PlanDesc(1024, 0, 0, 0, 0, 2, 4, 0)      # unknown order
+    assert libm.marble_plan(ctypes.byref(d), None, ctypes.byref(h)) == M.ERR_INVALID_ARG
