@@ -65,25 +65,6 @@ def ring_forward(q, k, v, mask=None, P=4, step_order=None, scale=None, dtype=np.
     return O.astype(dtype), LSE.astype(dtype)
 
 
-def dense_unmasked_f32(q, k, v):
-    """Single-device float32 softmax attention without a mask (one head), for the
-    worked example of the ring simulation page: subtract the row max, exponentiate,
-    normalise, multiply by V."""
-    q, k, v = (np.asarray(x, np.float32) for x in (q, k, v))
-    s = (q @ k.T) * np.float32(1.0 / np.sqrt(q.shape[1]))
-    s = s - s.max(axis=1, keepdims=True)
-    e = np.exp(s)
-    return (e / e.sum(axis=1, keepdims=True)) @ v
-
-
-def worked_example_inputs():
-    """Inputs of the ring simulation page's worked example: 16 tokens, head dim 8,
-    numpy default_rng(0), Q, K, V drawn in that order as standard normals -> float32."""
-    rng = np.random.default_rng(0)
-    Q, K, V = (rng.normal(size=(16, 8)).astype(np.float32) for _ in range(3))
-    return Q, K, V
-
-
 def round_bf16(x):
     """Round to the nearest bfloat16 (ties to even), returned as float64: the value goes to
     float32 first (a CUDA kernel holds it in fp32), then keeps the top 16 bits of its

@@ -46,14 +46,24 @@ def _rand_qkv(rng, n, hq, hkv, d):
 # --------------------------------------------------------------------------------------
 # ring / online recurrence
 # --------------------------------------------------------------------------------------
+def _worked_example_inputs():
+    """Inputs of the worked example on the ring-attention simulation page (section "The
+    whole algorithm, simulated"): 16 tokens, head dim 8, numpy default_rng(0), with Q, K
+    and V drawn in that order as standard normals and stored as float32."""
+    rng = np.random.default_rng(0)
+    return tuple(rng.normal(size=(16, 8)).astype(np.float32) for _ in range(3))
+
+
 def test_worked_example_ring_equals_full_attention_f32():
     g = _golden_kv("ring_worked_example.txt")
-    Q, K, V = ring.worked_example_inputs()
+    Q, K, V = _worked_example_inputs()
     assert Q.shape == (int(g["tokens"]), int(g["head_dim"]))
     P = int(g["devices"])
     O, _ = ring.ring_forward(Q[:, None, :], K[:, None, :], V[:, None, :], None, P=P,
                              dtype=np.float32)
-    ref = ring.dense_unmasked_f32(Q, K, V)
+    # the oracle's own dense softmax attention, evaluated in float32 like the page's reference
+    ref = attention.forward(Q[:, None, :], K[:, None, :], V[:, None, :],
+                            np.ones((16, 16), bool), dtype=np.float32)[0][:, 0, :]
     diff = float(np.abs(O[:, 0, :] - ref).max())
     page = float(g["max_difference"])
     # same arithmetic in float32: the page's figure is one or two ulp-scale roundings
