@@ -26,9 +26,37 @@ import threading
 import time
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each kernel on
-# the 64K packed workload, from one ncu capture of the kernels as they are now (the capture's
-# command is recorded beside its summary); None where the kernel changed since its capture
-KERNEL_DRAM_BYTES_PER_LAUNCH = {"k_bwd_dkdv": 494.7e6, "k_bwd_dq": 283.5e6, "k_attn_fwd": 147.9e6}
+# the 64K packed workload, from one ncu capture (its command and summary are in profiles/),
+# with the digest of the kernel's source files at the time of the capture: a figure is
+# reported only while the source is unchanged, null otherwise.
+KERNEL_DRAM_BYTES_PER_LAUNCH = {
+    "k_bwd_dkdv": (494.7e6, "profiles/k_bwd_dkdv_packed_multimodal.md", "stale"),
+    "k_bwd_dq": (283.5e6, "profiles/k_bwd_dq_packed_multimodal.md", "stale"),
+    "k_attn_fwd": (147.9e6, "profiles/k_attn_fwd_packed_multimodal.md", "stale"),
+}
+KERNEL_SOURCES = {"k_bwd_dkdv": ("attn_bwd.cu", "common.cuh"),
+                  "k_bwd_dq": ("attn_bwd.cu", "common.cuh"),
+                  "k_attn_fwd": ("attn_fwd.cu", "common.cuh")}
+
+
+def kernel_source_digest(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "context_attention_metadata_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(kernel: str):
+    """(DRAM bytes per launch, source of the figure) if the capture matches the kernel's
+    current source, else (None, why)."""
+    if kernel not in KERNEL_DRAM_BYTES_PER_LAUNCH:
+        return None, "no capture"
+    b, where, digest = KERNEL_DRAM_BYTES_PER_LAUNCH[kernel]
+    if kernel_source_digest(kernel) != digest:
+        return None, f"kernel source changed since the capture in {where}"
+    return b, f"ncu capture in {where} (dram__bytes_read.sum + dram__bytes_write.sum per launch)"
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
@@ -159,14 +187,17 @@ def oracle_sample_rate(cfg, tr, budget_s: float, seed: int = 0):
         v = torch.randn((L, cfg.hkv, cfg.d), generator=g).to(torch.bfloat16)
         do = torch.randn((L, cfg.hq, cfg.d), generator=g).to(torch.bfloat16)
         t0 = time.perf_counter()
-        attention.backward(q, k, v, do, mask.dense_mask(sub, cfg.window))
+        if cfg.bwd:
+            attention.backward(q, k, v, do, mask.dense_mask(sub, cfg.window))
+        else:
+            attention.forward(q, k, v, mask.dense_mask(sub, cfg.window))
         elapsed += time.perf_counter() - t0
         pairs += counts.by_key_classes(sub, cfg.window)
         tokens += L
         nsamp += 1
         if elapsed >= budget_s:
             break
-    flops = 14.0 * cfg.d * pairs * cfg.hq
+    flops = (14.0 if cfg.bwd else 4.0) * cfg.d * pairs * cfg.hq
     return flops / elapsed / 1e12, elapsed, nsamp, tokens
 
 
@@ -211,7 +242,8 @@ def run_reference(args, rank, world, dist):
         rates.append(r)
         times.append(el)
         desc = (f"{ns} whole samples ({tok} tokens) of the {cfg.name} pack, all {cfg.hq} q "
-                f"heads, fp64 dense forward+backward, ~{args.ref_budget:.0f} s per step")
+                f"heads, fp64 dense {'forward+backward' if cfg.bwd else 'forward'}, "
+                f"~{args.ref_budget:.0f} s per step")
     value = statistics.mean(rates)
     cores = os.cpu_count()
     line = {
@@ -263,8 +295,9 @@ def run_marble(args, rank, world, local, dist):
         plan_ms.append(1e3 * (time.perf_counter() - t0))
     stats = pl.stats()
     pairs = stats["legal_pairs"]
+    with_bwd = cfg.bwd
     flops_fwd = 4.0 * d * pairs * hq
-    flops_bwd = 10.0 * d * pairs * hq
+    flops_bwd = 10.0 * d * pairs * hq if with_bwd else 0.0
     flops = flops_fwd + flops_bwd
 
     q, k, v, do = wl.make_qkvdo(n, hq, hkv, d, device="cuda", seed=0)
@@ -286,13 +319,15 @@ def run_marble(args, rank, world, local, dist):
         if marks:
             marks[1].record(stream)
         M.attn_finalize(pl, st, o, lse)
-        M.attn_bwd_prep(pl, o, dop, delta)
-        dq.zero_()
-        dk.zero_()
-        dv.zero_()
+        if with_bwd:
+            M.attn_bwd_prep(pl, o, dop, delta)
+            dq.zero_()
+            dk.zero_()
+            dv.zero_()
         if marks:
             marks[2].record(stream)
-        M.attn_bwd_steps(pl, qp, kp, vp, dop, lse, delta, sched, dq, dk, dv)
+        if with_bwd:
+            M.attn_bwd_steps(pl, qp, kp, vp, dop, lse, delta, sched, dq, dk, dv)
         if marks:
             marks[3].record(stream)
 
@@ -327,32 +362,40 @@ def run_marble(args, rank, world, local, dist):
 
     peak, peak_sus, hbm, peak_kind = _peaks()
     mf, mb = statistics.mean(fwd_ms), statistics.mean(bwd_ms)
-    # roofline of the dominant kernel: its algorithmic FLOPs (forward: S and PV; dK/dV
-    # kernel: S, dP, dV, dK; dQ kernel: dQ -- its S and dP are recomputed, not algorithmic)
-    # over its own summed device time, per launch
-    kern = {
-        "k_attn_fwd": (flops_fwd, ktime["fwd_ms"], ktime["fwd_launches"]),
-        "k_bwd_dkdv": (0.8 * flops_bwd, ktime["dkdv_ms"], ktime["dkdv_launches"]),
-        "k_bwd_dq": (0.2 * flops_bwd, ktime["dq_ms"], ktime["dq_launches"]),
-    }
-    dom_name = max(kern, key=lambda k_: kern[k_][1])
-    f_step, k_ms, k_launches = kern[dom_name]
-    ms_per_launch = k_ms / max(k_launches, 1)
-    flops_per_launch = f_step * args.steps / max(k_launches, 1)
-    ach = flops_per_launch / (ms_per_launch / 1e3) / 1e12
-    roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-            "frac": ach / peak, "traffic": KERNEL_DRAM_BYTES_PER_LAUNCH.get(dom_name),
-            "kernel": dom_name, "launches": k_launches, "ms_per_launch": ms_per_launch,
-            "flops_per_launch": flops_per_launch,
-            "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
-            "kernel_ms": {k_: round(v_[1] / args.steps, 3) for k_, v_ in kern.items()},
-            "kernel_tflops": {k_: (v_[0] * args.steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
-                              for k_, v_ in kern.items()},
-            "note": "per-launch spans inside the timed step, whose launches overlap on several "
-                    "streams: a span includes time spent waiting for SMs"}
 
-    # the same kernels with every launch in list order on one stream (no overlap), warm: the
-    # per-launch durations of the kernels themselves
+    def roofline_of(kt, n_steps, note):
+        """Roofline of the dominant kernel from per-kernel device times: its algorithmic
+        FLOPs (forward: S and PV, 4 d per legal pair and q head; dK/dV kernel: S, dP, dV and
+        dK, 8 d; dQ kernel: dQ, 2 d) over its own summed duration, per launch."""
+        kern = {"k_attn_fwd": (flops_fwd, kt["fwd_ms"], kt["fwd_launches"])}
+        if with_bwd:
+            kern["k_bwd_dkdv"] = (0.8 * flops_bwd, kt["dkdv_ms"], kt["dkdv_launches"])
+            kern["k_bwd_dq"] = (0.2 * flops_bwd, kt["dq_ms"], kt["dq_launches"])
+        dom = max(kern, key=lambda k_: kern[k_][1])
+        f_step, k_ms, k_launches = kern[dom]
+        mpl = k_ms / max(k_launches, 1)
+        fpl = f_step * n_steps / max(k_launches, 1)
+        ach = fpl / (mpl / 1e3) / 1e12
+        tot = sum(v_[1] for v_ in kern.values())
+        traffic, traffic_src = kernel_traffic(dom)
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": traffic, "traffic_source": traffic_src,
+                "kernel": dom, "launches": k_launches, "ms_per_launch": mpl,
+                "flops_per_launch": fpl,
+                "peak_source": f"{peak_kind} bf16 dense burst (MEASURED_PEAKS.json)",
+                "kernel_ms": {k_: round(v_[1] / n_steps, 3) for k_, v_ in kern.items()},
+                "kernel_share": {k_: round(v_[1] / tot, 3) for k_, v_ in kern.items()},
+                "kernel_tflops": {k_: (v_[0] * n_steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
+                                  for k_, v_ in kern.items()},
+                "note": note}
+
+    roof_situ = roofline_of(
+        ktime, args.steps,
+        "per-launch spans inside the timed step, whose launches overlap on several streams: a "
+        "span includes time spent waiting for SMs held by other launches")
+
+    # The dominant kernel's own duration: the same step with every launch in list order on
+    # one stream (no overlap), warm; each kernel's span is then its duration.
     iso_steps = 2
     M.set_side_streams(0)
     step()
@@ -366,39 +409,56 @@ def run_marble(args, rank, world, local, dist):
     kt_iso = M.timing_read()
     M.set_side_streams(4)
     pl.check()
-    kern_iso = {
-        "k_attn_fwd": (flops_fwd, kt_iso["fwd_ms"], kt_iso["fwd_launches"]),
-        "k_bwd_dkdv": (0.8 * flops_bwd, kt_iso["dkdv_ms"], kt_iso["dkdv_launches"]),
-        "k_bwd_dq": (0.2 * flops_bwd, kt_iso["dq_ms"], kt_iso["dq_launches"]),
-    }
-    dom_iso = max(kern_iso, key=lambda k_: kern_iso[k_][1])
-    f_i, ms_i, l_i = kern_iso[dom_iso]
-    mpl_i = ms_i / max(l_i, 1)
-    fpl_i = f_i * iso_steps / max(l_i, 1)
-    ach_i = fpl_i / (mpl_i / 1e3) / 1e12
-    tot_i = sum(v_[1] for v_ in kern_iso.values())
-    roof_iso = {"bound": "tensor", "achieved": ach_i, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach_i / peak, "traffic": KERNEL_DRAM_BYTES_PER_LAUNCH.get(dom_iso),
-                "kernel": dom_iso, "launches": l_i, "ms_per_launch": mpl_i,
-                "flops_per_launch": fpl_i,
-                "kernel_ms": {k_: round(v_[1] / iso_steps, 3) for k_, v_ in kern_iso.items()},
-                "kernel_share": {k_: round(v_[1] / tot_i, 3) for k_, v_ in kern_iso.items()},
-                "kernel_tflops": {k_: (v_[0] * iso_steps / (v_[1] / 1e3) / 1e12 if v_[1] else None)
-                                  for k_, v_ in kern_iso.items()},
-                "note": "one launch at a time on one stream, warm, after the timed step"}
+    roof = roofline_of(kt_iso, iso_steps,
+                       "each launch alone on one stream, warm, after the timed steps: the "
+                       "kernel's own duration (CUDA events on its stream)")
+
+    # HBM-bound helpers, each timed alone (CUDA events, warm, mean of 5), against the measured
+    # copy bandwidth; bytes per call from the algorithmic formulas (reads + writes)
+    def time_call(fn, reps=5):
+        fn()
+        evs = [(ev(), ev()) for _ in range(reps)]
+        for e0, e1 in evs:
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    helpers = {}
+    th = time_call(lambda: M.attn_finalize(pl, st, o, lse))
+    by = n * hq * (6 * d + 12)
+    helpers["finalize"] = {"ms": th, "bytes": by, "gbs": by / th / 1e6}
+    if with_bwd:
+        th = time_call(lambda: M.attn_bwd_prep(pl, o, dop, delta))
+        by = n * hq * (4 * d + 4)
+        helpers["bwd_prep"] = {"ms": th, "bytes": by, "gbs": by / th / 1e6}
+    th = time_call(lambda: pl.permute(q, out=qp))
+    by = 2 * n * hq * d * 2
+    helpers["permute_q"] = {"ms": th, "bytes": by, "gbs": by / th / 1e6}
+    plan_bytes = n * (12 + 4 + 16) + 3 * 5 * stats["nnz"]
+    helpers["plan"] = {"ms": min(plan_ms), "bytes": plan_bytes,
+                       "gbs": plan_bytes / min(plan_ms) / 1e6,
+                       "note": "marble_plan end to end (host wall clock, it synchronises its "
+                               "stream to size its arrays): 12 B of tracks in, perm and "
+                               "permuted tracks out per token, 5 B per non-empty tile in each "
+                               "of three tile lists"}
+    for v_ in helpers.values():
+        v_["frac_of_hbm"] = v_["gbs"] / hbm
+    helpers["hbm_peak_gbs"] = hbm
 
     # end to end through the public API: H2D of the step's inputs from pinned memory,
     # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results.
     # Steps are pipelined the way a training loop runs them: the next step's inputs are
     # copied in, and its plan built, on one copy stream while this step computes, and this
     # step's results are copied out on another while the next step computes (double-buffered
-    # inputs and outputs).  Plans are destroyed after the timed steps (destroying one synchronises the
-    # device).
+    # inputs and outputs).  Each plan is destroyed as soon as its step is queued: the
+    # library frees it in stream order, without synchronising.
     e2e = None
     if args.e2e_steps > 0:
-        hq_pin = [t.cpu().pin_memory() for t in (q, k, v, do)]
+        hq_pin = [t.cpu().pin_memory() for t in ((q, k, v, do) if with_bwd else (q, k, v))]
         htr = [t.cpu().pin_memory() for t in trk + ([pos_t] if pos_t is not None else [])]
-        shapes = ((n, hq, d), (n, hq, d), (n, hkv, d), (n, hkv, d))
+        shapes = ((n, hq, d), (n, hq, d), (n, hkv, d), (n, hkv, d)) if with_bwd else ((n, hq, d),)
         out_pin = [[torch.empty(s_, dtype=torch.bfloat16).pin_memory() for s_ in shapes]
                    for _ in range(2)]
         outs = [[torch.empty(s_, dtype=torch.bfloat16, device="cuda") for s_ in shapes]
@@ -438,32 +498,34 @@ def run_marble(args, rank, world, local, dist):
                 b = i % 2
                 p2 = plans[i]
                 comp.wait_event(ev_plan[b])
-                q2, k2, v2, do2 = (p2.permute(t) for t in dev_in[b])
+                q2, k2, v2, do2 = [p2.permute(t) for t in dev_in[b]] + ([] if with_bwd else [None])
                 M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
-                dq.zero_()
-                dk.zero_()
-                dv.zero_()
-                M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
+                if with_bwd:
+                    dq.zero_()
+                    dk.zero_()
+                    dv.zero_()
+                    M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
                 ev_used[b].record(comp)
                 if i >= 2:
                     comp.wait_event(ev_d2h[b])      # step i - 2's results have left buffer b
                 ob = outs[b]
                 p2.permute(o, inverse=True, out=ob[0])
-                for g_, t_, b_ in ((dq, g_tmp[0], ob[1]), (dk, g_tmp[1], ob[2]),
-                                   (dv, g_tmp[1], ob[3])):
-                    p2.permute(g_, inverse=True, out=t_)
-                    M.cast_bf16(t_, b_)
+                if with_bwd:
+                    for g_, t_, b_ in ((dq, g_tmp[0], ob[1]), (dk, g_tmp[1], ob[2]),
+                                       (dv, g_tmp[1], ob[3])):
+                        p2.permute(g_, inverse=True, out=t_)
+                        M.cast_bf16(t_, b_)
                 ev_out[b].record(comp)
                 with torch.cuda.stream(cs_out):
                     cs_out.wait_event(ev_out[b])
                     for dst, src in zip(out_pin[b], ob):
                         dst.copy_(src, non_blocking=True)
                     ev_d2h[b].record(cs_out)
+                p2.close()                          # stream-ordered: no synchronisation
+                plans[i] = None
                 if i + 1 < K:
                     h2d_and_plan(i + 1)             # while step i computes
             torch.cuda.synchronize()
-            for p2 in plans:
-                p2.close()
 
         e2e_run(1)
         torch.cuda.synchronize()
@@ -475,9 +537,10 @@ def run_marble(args, rank, world, local, dist):
         e2e = {"value": world * flops / e2e_s / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
-               "permute, fwd, finalize, bwd_prep, bwd, inverse permute, bf16 cast, D2H; "
-               "steps pipelined (copies and the next step's plan on copy streams overlap "
-               "compute), plan teardown after the timed steps"}
+               "permute, fwd, finalize, " + ("bwd_prep, bwd, " if with_bwd else "") +
+               "inverse permute, " + ("bf16 cast, " if with_bwd else "") + "D2H, plan "
+               "teardown; steps pipelined (copies and the next step's plan on copy streams "
+               "overlap compute)"}
 
     # the forward with each merge of the ring steps: the carried fp32 state (the timed step
     # above), the merge of fp32 partials and the standard merge of bf16 partials
@@ -525,11 +588,12 @@ def run_marble(args, rank, world, local, dist):
             "phases_ms": {"fwd_steps": mf, "finalize+prep+zero": statistics.mean(mid_ms),
                           "bwd_steps": mb},
             "fwd_tflops": flops_fwd / (mf / 1e3) / 1e12,
-            "bwd_tflops": flops_bwd / (mb / 1e3) / 1e12,
+            "bwd_tflops": flops_bwd / (mb / 1e3) / 1e12 if with_bwd else None,
             "plan_ms": min(plan_ms), "plan_stats": stats,
             "wall_s_timed_region": t_wall,
             "roofline": roof,
-            "roofline_isolated": roof_iso,
+            "roofline_in_situ": roof_situ,
+            "hbm_helpers": helpers,
             "fwd_merge_variants": merge_variants,
             "cpu_baseline": cpu,
             "e2e": e2e,

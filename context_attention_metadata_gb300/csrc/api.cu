@@ -150,6 +150,39 @@ void timing_end(int span, cudaStream_t s, int kind, int launches) {
   t.launches = launches;
 }
 
+void plan_used(const marble_plan_t* p, cudaStream_t s) {
+  std::lock_guard<std::mutex> lock(p->use_mu);
+  cudaEvent_t ev = nullptr;
+  for (auto& u : p->uses)
+    if (u.first == s) ev = u.second;
+  if (!ev) {
+    if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return;
+    }
+    p->uses.push_back({s, ev});
+  }
+  if (cudaEventRecord(ev, s) != cudaSuccess) (void)cudaGetLastError();
+}
+
+// the stream on which plans of the current device are freed (created once per device)
+static cudaStream_t teardown_stream() {
+  static std::mutex mu;
+  static std::map<int, cudaStream_t> streams;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = streams.find(dev);
+  if (it != streams.end()) return it->second;
+  cudaStream_t st = nullptr;
+  if (cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  streams[dev] = st;
+  return st;
+}
+
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
   cudaEvent_t e;
   cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -161,7 +194,7 @@ cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
 }
 
 // true for device or managed memory of the current context
-static bool is_device_ptr(const void* p) {
+bool is_device_ptr(const void* p) {
   if (!p) return false;
   cudaPointerAttributes a;
   cudaError_t e = cudaPointerGetAttributes(&a, p);
@@ -214,6 +247,7 @@ using namespace marble;
 
 MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_stream_t stream,
                                        marble_plan_t** out) {
+  NvtxRange nvtx_("marble_plan");
   if (!d || !out) return fail(MARBLE_ERR_INVALID_ARG, "desc and out must be non-null");
   *out = nullptr;
   if (d->n_tokens <= 0 || d->n_tokens % MARBLE_BLOCK || d->n_tokens >= (int64_t)INT_MAX)
@@ -251,6 +285,7 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
   p->range_cost = d->order == MARBLE_ORDER_CHUNK_SEARCH ? d->range_cost : 0;
   p->bps = nb / d->num_shards;
   marble_status_t st = build_plan(d, (cudaStream_t)stream, p);
+  plan_used(p, (cudaStream_t)stream);  // the planner's kernels, also on failure
   if (st != MARBLE_OK) {
     std::string msg = g_last_error;
     marble_plan_destroy(p);
@@ -262,17 +297,44 @@ MARBLE_API marble_status_t marble_plan(const marble_plan_desc_t* d, marble_strea
 }
 
 MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
+  NvtxRange nvtx_("marble_plan_destroy");
   if (!p) return MARBLE_OK;
-  cudaDeviceSynchronize();
-  for (void* q : p->owned) dev_free(q, nullptr);
-  if (p->ds_scratch) dev_free(p->ds_scratch, nullptr);
+  // Free in stream order, without synchronising anything: a library stream of the plan's
+  // device waits for the last recorded use of the plan on every stream that used it, then
+  // returns the workspace to the memory pool.  The host object goes at once.
+  int prev = 0;
+  cudaError_t err = cudaGetDevice(&prev);
+  if (err == cudaSuccess && prev != p->device) err = cudaSetDevice(p->device);
+  cudaStream_t fs = err == cudaSuccess ? teardown_stream() : nullptr;
+  if (err == cudaSuccess && !fs) err = cudaErrorUnknown;
+  {
+    std::lock_guard<std::mutex> lock(p->use_mu);
+    for (auto& u : p->uses) {
+      if (err == cudaSuccess) err = cudaStreamWaitEvent(fs, u.second, 0);
+      cudaEventDestroy(u.second);  // released once the recorded work completes
+    }
+    p->uses.clear();
+  }
+  if (err == cudaSuccess) {
+    for (void* q : p->owned) {
+      const cudaError_t e = dev_free(q, fs);
+      if (err == cudaSuccess) err = e;
+    }
+    if (p->ds_scratch) {
+      const cudaError_t e = dev_free(p->ds_scratch, fs);
+      if (err == cudaSuccess) err = e;
+    }
+  }
+  if (prev != p->device) cudaSetDevice(prev);
   delete p;
+  if (err != cudaSuccess) return cuda_fail(err, "marble_plan_destroy: stream-ordered free");
   return MARBLE_OK;
 }
 
 MARBLE_API marble_status_t marble_chunk_layout_search(const int64_t* block_pairs, int64_t n_blocks,
                                                       int32_t num_shards, int64_t range_cost,
                                                       int32_t* chunk_rank, int64_t* out) {
+  NvtxRange nvtx_("marble_chunk_layout_search");
   if (!block_pairs || !chunk_rank || !out)
     return fail(MARBLE_ERR_INVALID_ARG, "block_pairs, chunk_rank and out must be non-null");
   if (num_shards < 1 || num_shards > 256 || n_blocks < 1 || n_blocks % num_shards)
@@ -298,6 +360,7 @@ MARBLE_API marble_status_t marble_chunk_layout_search(const int64_t* block_pairs
 
 MARBLE_API marble_status_t marble_layout_vision_groups(const int32_t* sample, const int32_t* seg,
                                                        int64_t n, int32_t* perm) {
+  NvtxRange nvtx_("marble_layout_vision_groups");
   if (!sample || !seg || !perm) return fail(MARBLE_ERR_INVALID_ARG, "arrays must be non-null");
   if (n < 0 || n >= (int64_t)INT_MAX) return fail(MARBLE_ERR_INVALID_ARG, "bad n");
   for (int64_t i = 0; i < n; ++i)
@@ -337,6 +400,7 @@ MARBLE_API marble_status_t marble_layout_vision_groups(const int32_t* sample, co
 
 MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stream_t stream,
                                              marble_plan_stats_t* out) {
+  NvtxRange nvtx_("marble_plan_stats");
   if (!p || !out) return fail(MARBLE_ERR_INVALID_ARG, "plan and out must be non-null");
   cudaStream_t s = (cudaStream_t)stream;
   memset(out, 0, sizeof(*out));
@@ -346,6 +410,7 @@ MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stre
   out->nnz = p->nnz;
   marble_status_t st = plan_legal_pairs(p, s, &out->legal_pairs, &out->n_full, &out->n_partial,
                                         &out->step_cost_pairs);
+  plan_used(p, s);
   if (st != MARBLE_OK) return st;
   const int64_t np = p->nb * p->P + 1;
   std::vector<int64_t> ptr(np);
@@ -426,6 +491,7 @@ MARBLE_API marble_status_t marble_plan_field_bytes(const marble_plan_t* p, int32
 
 MARBLE_API marble_status_t marble_plan_export(const marble_plan_t* p, int32_t field, void* dst,
                                               size_t bytes, marble_stream_t stream) {
+  NvtxRange nvtx_("marble_plan_export");
   const void* src = nullptr;
   size_t want = 0;
   if (!p || (!dst && bytes)) return fail(MARBLE_ERR_INVALID_ARG, "plan and dst must be non-null");
@@ -433,6 +499,7 @@ MARBLE_API marble_status_t marble_plan_export(const marble_plan_t* p, int32_t fi
   if (bytes != want) return fail(MARBLE_ERR_INVALID_ARG, "bytes does not match the field size");
   if (!bytes) return MARBLE_OK;
   cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "marble_plan_export");
   return MARBLE_OK;
 }
@@ -440,6 +507,7 @@ MARBLE_API marble_status_t marble_plan_export(const marble_plan_t* p, int32_t fi
 MARBLE_API marble_status_t marble_permute(const marble_plan_t* p, const void* src, void* dst,
                                           int64_t row_bytes, int32_t inverse,
                                           marble_stream_t stream) {
+  NvtxRange nvtx_("marble_permute");
   if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
   if (row_bytes <= 0 || row_bytes % 4)
     return fail(MARBLE_ERR_INVALID_ARG, "row_bytes must be a positive multiple of 4");
@@ -451,6 +519,7 @@ MARBLE_API marble_status_t marble_permute(const marble_plan_t* p, const void* sr
   const int64_t bytes = p->n * row_bytes;
   if (a < b + bytes && b < a + bytes) return fail(MARBLE_ERR_INVALID_ARG, "src and dst overlap");
   cudaError_t e = launch_permute(p, src, dst, row_bytes, inverse ? 1 : 0, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "marble_permute launch");
   return MARBLE_OK;
 }
@@ -466,6 +535,7 @@ MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble
                                             int32_t q_shard, int32_t kv_shard,
                                             const marble_state_t* state, uint32_t flags,
                                             marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_step");
   if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
   marble_status_t st;
   if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
@@ -474,7 +544,9 @@ MARBLE_API marble_status_t marble_attn_step(const marble_plan_t* p, const marble
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
   if (!step_flags_ok(flags)) return fail(MARBLE_ERR_INVALID_ARG, "unknown or conflicting flags");
-  return run_attn_fwd(p, qkv, 1, &q_shard, &kv_shard, &flags, state, (cudaStream_t)stream);
+  st = run_attn_fwd(p, qkv, 1, &q_shard, &kv_shard, &flags, state, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
 }
 
 static marble_status_t check_step_list(const marble_plan_t* p, int32_t n_steps,
@@ -494,6 +566,7 @@ MARBLE_API marble_status_t marble_attn_steps(const marble_plan_t* p, const marbl
                                              const int32_t* kv_shards, const uint32_t* flags,
                                              const marble_state_t* state,
                                              marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_steps");
   if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
   marble_status_t st;
   if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
@@ -509,7 +582,9 @@ MARBLE_API marble_status_t marble_attn_steps(const marble_plan_t* p, const marbl
   if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
   if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
   if (n_steps == 0) return MARBLE_OK;
-  return run_attn_fwd(p, qkv, n_steps, q_shards, kv_shards, flags, state, (cudaStream_t)stream);
+  st = run_attn_fwd(p, qkv, n_steps, q_shards, kv_shards, flags, state, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
 }
 
 MARBLE_API marble_status_t marble_attn_bwd_steps(const marble_plan_t* p, const marble_qkv_t* qkv,
@@ -519,6 +594,7 @@ MARBLE_API marble_status_t marble_attn_bwd_steps(const marble_plan_t* p, const m
                                                  const int32_t* kv_shards, float* dq_acc,
                                                  float* dk_acc, float* dv_acc,
                                                  marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_bwd_steps");
   if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
   marble_status_t st;
   if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
@@ -530,14 +606,17 @@ MARBLE_API marble_status_t marble_attn_bwd_steps(const marble_plan_t* p, const m
   if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
   if (n_steps == 0) return MARBLE_OK;
-  return run_attn_bwd(p, qkv, d_o, lse, delta, n_steps, q_shards, kv_shards, dq_acc, dk_acc,
-                      dv_acc, (cudaStream_t)stream);
+  st = run_attn_bwd(p, qkv, d_o, lse, delta, n_steps, q_shards, kv_shards, dq_acc, dk_acc,
+                    dv_acc, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
 }
 
 MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
                                                 const marble_state_t* state, int32_t hq,
                                                 int32_t d, void* o_bf16, float* lse,
                                                 marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_finalize");
   if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
   if (d != 64 && d != 128) return fail(MARBLE_ERR_INVALID_ARG, "d must be 64 or 128");
   if (hq < 1) return fail(MARBLE_ERR_INVALID_ARG, "hq must be >= 1");
@@ -549,6 +628,7 @@ MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
   if ((st = check_tensor(lse, "lse")) != MARBLE_OK) return st;
   cudaError_t e = launch_finalize(p, state->o_acc, state->m, state->l, hq, d, o_bf16, lse,
                                   (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "marble_attn_finalize launch");
   return MARBLE_OK;
 }
@@ -556,6 +636,7 @@ MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
 MARBLE_API marble_status_t marble_attn_bwd_prep(const marble_plan_t* p, const void* o,
                                                 const void* d_o, int32_t hq, int32_t d,
                                                 float* delta, marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_bwd_prep");
   if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
   if (d != 64 && d != 128) return fail(MARBLE_ERR_INVALID_ARG, "d must be 64 or 128");
   if (hq < 1) return fail(MARBLE_ERR_INVALID_ARG, "hq must be >= 1");
@@ -564,6 +645,7 @@ MARBLE_API marble_status_t marble_attn_bwd_prep(const marble_plan_t* p, const vo
   if ((st = check_tensor(d_o, "d_o")) != MARBLE_OK) return st;
   if ((st = check_tensor(delta, "delta")) != MARBLE_OK) return st;
   cudaError_t e = launch_bwd_prep(p, o, d_o, hq, d, delta, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "marble_attn_bwd_prep launch");
   return MARBLE_OK;
 }
@@ -574,6 +656,7 @@ MARBLE_API marble_status_t marble_attn_bwd(const marble_plan_t* p, const marble_
                                            int32_t kv_shard, float* dq_acc, float* dk_acc,
                                            float* dv_acc, uint32_t flags,
                                            marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_bwd");
   if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
   marble_status_t st;
   if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
@@ -585,12 +668,15 @@ MARBLE_API marble_status_t marble_attn_bwd(const marble_plan_t* p, const marble_
   if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
   if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
   if (flags != 0) return fail(MARBLE_ERR_INVALID_ARG, "flags must be 0");
-  return run_attn_bwd(p, qkv, d_o, lse, delta, 1, &q_shard, &kv_shard, dq_acc, dk_acc, dv_acc,
-                      (cudaStream_t)stream);
+  st = run_attn_bwd(p, qkv, d_o, lse, delta, 1, &q_shard, &kv_shard, dq_acc, dk_acc, dv_acc,
+                    (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
 }
 
 MARBLE_API marble_status_t marble_cast_bf16(const float* src, void* dst, int64_t n,
                                             marble_stream_t stream) {
+  NvtxRange nvtx_("marble_cast_bf16");
   if (n < 0 || n % 4) return fail(MARBLE_ERR_INVALID_ARG, "n must be a non-negative multiple of 4");
   if (n == 0) return MARBLE_OK;
   marble_status_t st;
@@ -602,6 +688,7 @@ MARBLE_API marble_status_t marble_cast_bf16(const float* src, void* dst, int64_t
 }
 
 MARBLE_API marble_status_t marble_check(const marble_plan_t* p, marble_stream_t stream) {
+  NvtxRange nvtx_("marble_check");
   if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "asynchronous CUDA error");
@@ -668,6 +755,7 @@ MARBLE_API marble_status_t marble_debug_wait_timeout(const marble_plan_t* p, uin
   if (limit_ns == 0 || limit_ns > 10000000000ull)
     return fail(MARBLE_ERR_INVALID_ARG, "limit_ns must be in (0, 10 s]");
   cudaError_t e = launch_debug_wait(p->err, limit_ns, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "marble_debug_wait_timeout launch");
   return MARBLE_OK;
 }

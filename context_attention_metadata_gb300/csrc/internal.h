@@ -9,6 +9,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/marble.h"
 
 namespace marble {
@@ -91,9 +93,22 @@ struct marble_plan {
   unsigned long long* counters = nullptr;  // [8] device scratch for statistics
   std::vector<int64_t> h_needed_ptr;      // host copy of needed_ptr
   std::vector<void*> owned;
+  // the last use of the plan on each stream a call ran on (an event recorded after the
+  // call's work): marble_plan_destroy frees the workspace in stream order after all of them
+  mutable std::mutex use_mu;
+  mutable std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;
 };
 
 namespace marble {
+
+// An NVTX range named after the API call, open for the call's host-side duration, so that
+// a profiler timeline shows which call queued which kernels (no cost without a profiler).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kSchedSlots = 256;
 
@@ -102,6 +117,13 @@ inline unsigned* sched_slot(const marble_plan_t* p) {
   const unsigned i = p->sched_next.fetch_add(1u, std::memory_order_relaxed) % kSchedSlots;
   return p->sched + 2 * i;
 }
+
+// true for device or managed memory of the current context (api.cu)
+bool is_device_ptr(const void* p);
+
+// record that work using plan `p` has been queued on `s` (api.cu); every call that
+// launches work on a plan's memory records it before returning
+void plan_used(const marble_plan_t* p, cudaStream_t s);
 
 // error reporting (api.cu)
 void set_error(const std::string& msg);

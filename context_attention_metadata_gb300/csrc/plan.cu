@@ -1220,6 +1220,8 @@ std::mutex g_scratch_mu;
 void* g_scratch_addr[64] = {};
 
 // Device address of the scratch array on the current device, looked up once per device.
+// The address belongs to the device's primary context: after cudaDeviceReset the module
+// is loaded anew and the cached address no longer applies (documented in marble.h).
 marble_status_t static_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1244,6 +1246,7 @@ extern "C" __attribute__((visibility("default"))) marble_status_t marble_tile_ma
     int32_t window, int64_t* row_ptr, int32_t* col, uint8_t* tag, int64_t capacity,
     marble_stream_t stream) {
   using namespace marble;
+  NvtxRange nvtx_("marble_tile_map_static");
   if (n_tokens <= 0 || n_tokens % kBlock)
     return fail(MARBLE_ERR_INVALID_ARG, "n_tokens must be a positive multiple of 128");
   if (n_tokens > MARBLE_TILE_MAP_STATIC_MAX_TOKENS)
@@ -1255,6 +1258,11 @@ extern "C" __attribute__((visibility("default"))) marble_status_t marble_tile_ma
   if (capacity < 0) return fail(MARBLE_ERR_INVALID_ARG, "capacity must be >= 0");
   if (!sample_id || !seg_id || !noise_id || !row_ptr || (capacity > 0 && (!col || !tag)))
     return fail(MARBLE_ERR_INVALID_ARG, "null pointer");
+  // every pointer goes straight to a kernel: host or foreign memory is refused here
+  if (!is_device_ptr(sample_id) || !is_device_ptr(seg_id) || !is_device_ptr(noise_id) ||
+      !is_device_ptr(row_ptr) || (capacity > 0 && (!is_device_ptr(col) || !is_device_ptr(tag))))
+    return fail(MARBLE_ERR_INVALID_ARG,
+                "sample_id, seg_id, noise_id, row_ptr, col and tag must be device memory");
   void* base = nullptr;
   marble_status_t st = static_scratch(&base);
   if (st != MARBLE_OK) return st;

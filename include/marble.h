@@ -23,8 +23,10 @@
  *     stated otherwise.  Arguments are validated before anything is launched; an invalid
  *     argument returns MARBLE_ERR_INVALID_ARG and launches nothing.
  *   - The caller owns every tensor it passes.  A plan owns only its own device
- *     workspace, allocated by marble_plan and freed by marble_plan_destroy.  No other
- *     call allocates memory.
+ *     workspace: allocated by marble_plan, grown by the backward calls for their scratch
+ *     of bf16 dS tiles, and freed by marble_plan_destroy.  This memory comes from a
+ *     stream-ordered pool the library keeps per device.  No call allocates memory that
+ *     the caller sees.
  *   - No C++ exception crosses this boundary.  marble_last_error() returns a
  *     thread-local, human-readable message for the last failing call on this thread.
  *   - Every wait inside a kernel is bounded in time; a wait that runs out sets an error
@@ -154,7 +156,11 @@ typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
 marble_status_t marble_plan(const marble_plan_desc_t *desc, marble_stream_t stream,
                             marble_plan_t **out);
 
-/* Frees the plan (synchronises the device first).  NULL is accepted. */
+/* Frees the plan without synchronising: the workspace returns to the library's memory
+ * pool in stream order, once the work of every earlier call that used the plan has
+ * completed, on whatever streams those calls ran; the plan handle is invalid as soon as
+ * the call returns.  NULL is accepted.  Errors: CUDA (the plan is freed on the host all
+ * the same). */
 marble_status_t marble_plan_destroy(marble_plan_t *plan);
 
 typedef struct {
@@ -431,10 +437,13 @@ marble_status_t marble_debug_wait_timeout(const marble_plan_t *plan, uint64_t li
  *             non-empty tiles.  If the metadata fails validation, row_ptr[0] is set to -1;
  *   col, tag  device int32[capacity], uint8[capacity]; entries at CSR index >= capacity are
  *             not written (compare row_ptr[nb] with capacity to detect a short buffer).
+ * Every pointer must be device (or managed) memory of the current device; others are
+ * rejected with MARBLE_ERR_INVALID_ARG.
  * Asynchronous on `stream`; host-side argument errors return before any launch.  The first
  * call on a device looks up the device address of the scratch array on that device (a
  * host-side step, done once per device, with that device current); make that first call
- * before any stream capture.  All calls on a device share the one scratch array, so calls
+ * before any stream capture.  The address belongs to the device's context: do not call this
+ * again after cudaDeviceReset in the same process.  All calls on a device share the one scratch array, so calls
  * whose executions overlap on the GPU (different streams, or several host threads) race;
  * serialise them, e.g. on one stream.
  */

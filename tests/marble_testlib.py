@@ -84,3 +84,29 @@ def rel_fro(a, b):
     a = np.asarray(a, np.float64)
     b = np.asarray(b, np.float64)
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def token_shards(pl):
+    """Shard of the plan that every original token lands in (plan order is shard-major)."""
+    perm = pl.export("perm").cpu().numpy().astype(np.int64)
+    inv = np.empty_like(perm)
+    inv[perm] = np.arange(len(perm))
+    return (inv // wl.BLOCK) // pl.blocks_per_shard
+
+
+def spread_tokens(cands, shard, P, count, rng):
+    """About `count` tokens of `cands`, spread as evenly as the candidates allow over the
+    plan's P shards, half of each shard's share at block edges (first or last token of a
+    128-token block) where it has any."""
+    cands = np.unique(np.asarray(cands, np.int64))
+    per = -(-count // P)
+    out = []
+    for r in range(P):
+        c = cands[shard[cands] == r]
+        if len(c) == 0:
+            continue
+        at_edge = (c % wl.BLOCK == 0) | (c % wl.BLOCK == wl.BLOCK - 1)
+        edge = rng.permutation(c[at_edge])[:(per + 1) // 2]
+        rest = rng.permutation(c[~at_edge])[:per - len(edge)]
+        out += list(edge) + list(rest)
+    return np.sort(np.array(out, np.int64))

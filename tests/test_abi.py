@@ -65,3 +65,41 @@ def test_host_side_argument_checks(libm):
     assert b"range_cost" in libm.marble_last_error()
     d = M._PlanDesc(1024, 0, 0, 0, 0, 2, 4, 0)      # unknown order
     assert libm.marble_plan(ctypes.byref(d), None, ctypes.byref(h)) == M.ERR_INVALID_ARG
+
+
+def test_tile_map_static_argument_checks(libm):
+    """marble_tile_map_static refuses bad arguments on the host, before any launch: sizes,
+    the static scratch's limit, the window, the capacity, null pointers, and pointers that
+    are not device memory (host buffers here; no GPU is needed to refuse them)."""
+    import numpy as np
+    import context_attention_metadata_gb300 as M
+    n = 1024
+    trk = [np.zeros(n, np.int32) for _ in range(3)]
+    rp = np.zeros(n // 128 + 1, np.int64)
+    col = np.zeros(64, np.int32)
+    tag = np.zeros(64, np.uint8)
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    f = libm.marble_tile_map_static
+
+    def call(n_=n, w=0, cap=64, c=col, t=tag, tracks=trk, r=rp):
+        return f(n_, *[ptr(x) for x in tracks], w, ptr(r),
+                 ptr(c) if c is not None else None, ptr(t) if t is not None else None, cap,
+                 None)
+
+    cases = [
+        (dict(n_=1000), b"multiple of 128"),
+        (dict(n_=0), b"multiple of 128"),
+        (dict(n_=M.TILE_MAP_STATIC_MAX_TOKENS + 128), b"MAX_TOKENS"),
+        (dict(w=-1), b"window"),
+        (dict(cap=-1), b"capacity"),
+        (dict(c=None), b"null"),
+        (dict(t=None), b"null"),
+        (dict(), b"device memory"),  # host buffers
+    ]
+    for kw, msg in cases:
+        assert call(**kw) == M.ERR_INVALID_ARG, kw
+        assert msg in libm.marble_last_error(), (kw, libm.marble_last_error())
+    # null col / tag are allowed with capacity 0 (only the row pointers are written); the
+    # host track buffers are then what is refused
+    assert call(cap=0, c=None, t=None) == M.ERR_INVALID_ARG
+    assert b"device memory" in libm.marble_last_error()

@@ -6,7 +6,8 @@ import pytest
 import torch
 
 import workloads as wl
-from marble_testlib import TOL_GRAD_REL, make_plan, plan_for, rel_fro, run_backward
+from marble_testlib import (TOL_GRAD_REL, make_plan, plan_for, rel_fro, run_backward,
+                            spread_tokens, token_shards)
 from oracle import attention, mask
 
 pytestmark = pytest.mark.gpu
@@ -68,8 +69,56 @@ def test_mini_configs_backward(cid):
     _check_dense(tr, cfg.window, q, k, v, do, dq, dk, dv)
 
 
+def full_size_samples(cid, tr, shard, P, rng):
+    """Rows for the dQ check and key columns for the dK/dV check at full size, with the kv
+    heads to check: about 256 of each, spread over every shard of the plan and at block
+    edges where the candidates allow.
+
+    The fp64 oracle scores each sampled row against its legal keys and each sampled key
+    against its visible queries, whose own rows it also needs; the candidates are
+    restricted so that this stays within seconds:
+      rows:    whole samples of at most 4096 tokens, the first 1024 tokens of every longer
+               sample (a causal prefix, or the start of an image, sees at most its own span
+               and the tokens before it) -- in the chunked 1M pack this takes rows inside
+               the 512K causal generation;
+      columns: whole samples of at most 1024 tokens and the last 128-token block of every
+               longer sample (seen by the few queries after it) -- the last block of the
+               512K causal generation in the 1M pack; in the grouped-image pack also 32 keys
+               inside the first image of the shortest sample with a group (seen by the
+               whole group), on kv head 0;
+      window:  with the 4096-token window every token has at most 4096 partners, so any
+               row qualifies, and the columns are two clusters of 128 keys around two shard
+               boundaries (keys at the end of a shard are the remote blocks the next shard
+               fetches), checked on every kv head."""
+    st, en = mask.sample_runs(tr)
+    n = len(st)
+    idx = np.arange(n)
+    L = en - st
+    if cid == 3:
+        rows = spread_tokens(idx, shard, P, 256, rng)
+        bps = n // P
+        cols = np.concatenate([np.arange(j * bps - 64, j * bps + 64) for j in (P // 4, 3 * P // 4)])
+        return rows, cols, None
+    rows = spread_tokens(idx[(L <= 4096) | (idx - st < 1024)], shard, P, 256, rng)
+    cand = idx[(L <= 1024) | (en - idx <= 128)]
+    cols = spread_tokens(cand, shard, P, 256, rng)
+    if cid == 5:
+        seg = np.asarray(tr["seg"])
+        grouped = [a for a in np.unique(st) if
+                   len(np.flatnonzero(np.diff(seg[a:en[a]]) != 0)) >= 3 and
+                   np.bincount(seg[a:en[a]][seg[a:en[a]] >= 0]).max(initial=0) > 4096]
+        a = min(grouped, key=lambda a_: en[a_] - a_)
+        first_img = a + int(np.flatnonzero(seg[a:en[a]] >= 0)[0])
+        e = (first_img // 128 + 2) * 128
+        cols = np.union1d(cols, np.arange(e - 16, e + 16))
+        return rows, cols, np.array([0])  # the group's keys are seen by ~15K queries each
+    return rows, cols, np.array([0, -1])
+
+
 @pytest.mark.parametrize("cid", [2, 3, 4, 5])
 def test_full_configs_backward_sampled(cid):
+    """dQ on ~256 rows (every q head) and dK/dV on ~256 key columns over every shard of the
+    plan, against the fp64 oracle's exact gradients of those rows and columns."""
     cfg = wl.CONFIGS[cid]
     tr = wl.config_tracks(cid)
     q, k, v, do = wl.make_qkvdo(cfg.n, cfg.hq, cfg.hkv, cfg.d, device="cuda")
@@ -77,27 +126,17 @@ def test_full_configs_backward_sampled(cid):
     dq, dk, dv = run_backward(pl, q, k, v, do, needed=cfg.needed)
     for g in (dq, dk, dv):
         assert torch.isfinite(g).all()
-    qc, kc, vc, dc = (t.cpu() for t in (q, k, v, do))
     rng = np.random.default_rng(10 + cid)
-    st = np.asarray(tr["sample"])
-    lengths = np.bincount(st)
-    # rows and key columns from samples small enough for the fp64 oracle to finish quickly
-    small = np.flatnonzero(lengths[st] <= 8192)
-    pool = small if len(small) >= 64 else np.arange(cfg.n)
-    rows = np.sort(rng.choice(pool, 48, replace=False))
-    heads = np.array([0, cfg.hq - 1])
-    ref = attention.rows_dq(qc, kc, vc, dc, tr, cfg.window, rows, heads=heads)
-    got = dq[torch.as_tensor(rows).cuda()][:, torch.as_tensor(heads).cuda()].cpu().double().numpy()
+    rows, cols, kvh = full_size_samples(cid, tr, token_shards(pl), cfg.shards, rng)
+    kvh = np.arange(cfg.hkv) if kvh is None else np.unique(kvh % cfg.hkv)
+    qc, kc, vc, dc = (t.cpu() for t in (q, k, v, do))
+    ref = attention.rows_dq(qc, kc, vc, dc, tr, cfg.window, rows)
+    got = dq[torch.as_tensor(rows).cuda()].cpu().double().numpy()
     assert rel_fro(got, ref) <= TOL_GRAD_REL
-    # eight consecutive key columns (their visible-query sets overlap)
-    c0 = int(rng.choice(pool))
-    c0 = min(c0, cfg.n - 8)
-    cols = np.arange(c0, c0 + 8)
-    kvh = np.array([0])
     rk, rv = attention.cols_backward(qc, kc, vc, dc, tr, cfg.window, cols, kv_heads=kvh)
-    c_t = torch.as_tensor(cols).cuda()
-    assert rel_fro(dk[c_t][:, :1].cpu().double().numpy(), rk) <= TOL_GRAD_REL
-    assert rel_fro(dv[c_t][:, :1].cpu().double().numpy(), rv) <= TOL_GRAD_REL
+    c_t, h_t = torch.as_tensor(cols).cuda(), torch.as_tensor(kvh).cuda()
+    assert rel_fro(dk[c_t][:, h_t].cpu().double().numpy(), rk) <= TOL_GRAD_REL
+    assert rel_fro(dv[c_t][:, h_t].cpu().double().numpy(), rv) <= TOL_GRAD_REL
 
 
 def test_results_do_not_depend_on_stream_overlap():

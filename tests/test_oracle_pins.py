@@ -462,11 +462,17 @@ def test_step_lists_partition_the_tile_map(order):
 # --------------------------------------------------------------------------------------
 # sampled-row / sampled-column oracle paths agree with the dense oracle
 # --------------------------------------------------------------------------------------
-def test_sampled_rows_and_columns_equal_dense():
-    rng = np.random.default_rng(21)
+@pytest.mark.parametrize("seed,W,pos", [(21, 120, False), (22, INF, False), (23, 0, False),
+                                        (24, 1, False), (25, 300, True), (26, INF, True)])
+def test_sampled_rows_and_columns_equal_dense(seed, W, pos):
+    # the sampled paths score each token against a superset of its legal partners (window
+    # and span members, or the whole sample with a position track): they must agree with
+    # the dense oracle for every window, including none, W = 0 and W = 1
+    rng = np.random.default_rng(seed)
     n = 900
     tr = wl.random_pack(rng, n, max_samples=4)
-    W = 120
+    if pos:
+        tr = dict(tr, pos=np.arange(n, dtype=np.int32))
     M = mask.dense_mask(tr, W)
     q, k, v = _rand_qkv(rng, n, 4, 2, 8)
     do = rng.standard_normal(q.shape)

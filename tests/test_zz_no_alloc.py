@@ -77,6 +77,28 @@ def test_static_tile_map_short_buffer_and_bad_metadata():
     assert (srp == rp).all() and (scol[:88] == col).all()
 
 
+def test_static_tile_map_allocates_nothing():
+    """After a first call on the device (which loads the kernels and looks up the scratch
+    array's address), repeated calls leave the device's free memory exactly unchanged: the
+    entry point takes no memory from the driver, the library's pool or torch."""
+    tr, W = wl.config_tracks(2), INF
+    s, g, z = device_tracks(tr)
+    nb = s.shape[0] // M.BLOCK
+    row_ptr = torch.empty((nb + 1,), dtype=torch.int64, device="cuda")
+    col = torch.empty((nb * 64,), dtype=torch.int32, device="cuda")
+    tag = torch.empty((nb * 64,), dtype=torch.uint8, device="cuda")
+    M.tile_map_static(s, g, z, W, row_ptr, col, tag)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0 = torch.cuda.memory_reserved()
+    for _ in range(5):
+        M.tile_map_static(s, g, z, W, row_ptr, col, tag)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_reserved() == reserved0
+
+
 def test_static_tile_map_rejects_packs_beyond_its_scratch():
     n = M.TILE_MAP_STATIC_MAX_TOKENS + M.BLOCK
     z = torch.zeros(n, dtype=torch.int32, device="cuda")
