@@ -561,6 +561,56 @@ def run_marble(args, rank, world, local, dist):
                       **{k_: round(v_, 3) for k_, v_ in merge_ms.items()},
                       "tflops": {k_: flops_fwd / (v_ / 1e3) / 1e12 for k_, v_ in merge_ms.items()}}
 
+    # The fused ring beside the per-step path: every forward ring step in one launch with the
+    # state on chip between steps, then one dK/dV launch per kv shard over its ring (dK/dV on
+    # chip across q shards) with the per-step dQ GEMMs; same inputs, same FLOPs, same
+    # finalize and bwd_prep, device-timed over the same number of steps.
+    fused = None
+    if not needed:
+        def fused_step():
+            M.attn_fwd_fused(pl, qp, kp, vp, st)
+            M.attn_finalize(pl, st, o, lse)
+            if with_bwd:
+                M.attn_bwd_prep(pl, o, dop, delta)
+                dq.zero_()
+                dk.zero_()
+                dv.zero_()
+                M.attn_bwd_fused(pl, qp, kp, vp, dop, lse, delta, dq, dk, dv)
+
+        for _ in range(max(3, args.warmup)):
+            fused_step()
+        torch.cuda.synchronize()
+        evs = [(ev(), ev(), ev()) for _ in range(args.steps)]
+        M.timing_read()
+        M.timing_enable(True)
+        for e0, e1, e2 in evs:
+            e0.record(stream)
+            M.attn_fwd_fused(pl, qp, kp, vp, st)
+            e1.record(stream)
+            M.attn_finalize(pl, st, o, lse)
+            if with_bwd:
+                M.attn_bwd_prep(pl, o, dop, delta)
+                dq.zero_()
+                dk.zero_()
+                dv.zero_()
+                M.attn_bwd_fused(pl, qp, kp, vp, dop, lse, delta, dq, dk, dv)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        M.timing_enable(False)
+        kt_f = M.timing_read()
+        pl.check()
+        f_ms = statistics.mean(a.elapsed_time(c) for a, b, c in evs)
+        ff_ms = statistics.mean(a.elapsed_time(b) for a, b, c in evs)
+        f_dev_s = max_over_ranks(f_ms * args.steps / 1e3, dist)
+        fused = {"value": world * flops * args.steps / f_dev_s / 1e12, "unit": UNIT,
+                 "ms_per_step": f_ms, "fwd_ms": ff_ms,
+                 "fwd_tflops": flops_fwd / (ff_ms / 1e3) / 1e12,
+                 "bwd_ms": f_ms - ff_ms,
+                 "launches_per_step": {k_: kt_f[k_ + "_launches"] // args.steps
+                                       for k_ in ("fwd", "dkdv", "dq")},
+                 "what": "marble_attn_fwd_fused + finalize + bwd_prep + marble_attn_bwd_fused "
+                         "(the same ring steps; state and dK/dV on chip between them)"}
+
     cpu = None
     if rank == 0 and args.cpu_budget > 0:
         r, el, ns, tok = oracle_sample_rate(cfg, tr, args.cpu_budget)
@@ -587,6 +637,8 @@ def run_marble(args, rank, world, local, dist):
             "pct_of_sustained_peak": (100.0 * value / world / peak_sus) if peak_sus else None,
             "phases_ms": {"fwd_steps": mf, "finalize+prep+zero": statistics.mean(mid_ms),
                           "bwd_steps": mb},
+            "tile_tflops": (14.0 if with_bwd else 4.0) * d * hq * stats["nnz"] * 128 * 128
+                           / (ms_per_step / 1e3) / 1e12,
             "fwd_tflops": flops_fwd / (mf / 1e3) / 1e12,
             "bwd_tflops": flops_bwd / (mb / 1e3) / 1e12 if with_bwd else None,
             "plan_ms": min(plan_ms), "plan_stats": stats,
@@ -595,6 +647,7 @@ def run_marble(args, rank, world, local, dist):
             "roofline_in_situ": roof_situ,
             "hbm_helpers": helpers,
             "fwd_merge_variants": merge_variants,
+            "fused": fused,
             "cpu_baseline": cpu,
             "e2e": e2e,
             # our kernels in the timed region: attention launches counted by the library,

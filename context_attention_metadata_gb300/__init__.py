@@ -105,6 +105,11 @@ _SIGS = {
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                ctypes.c_void_p]),
+    "marble_attn_fwd_fused": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.POINTER(_State),
+                               ctypes.c_void_p]),
+    "marble_attn_bwd_fused": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "marble_cast_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]),
     "marble_check": ([ctypes.c_void_p, ctypes.c_void_p]),
     "marble_set_wait_limit_ns": ([ctypes.c_uint64]),
@@ -410,20 +415,58 @@ def attn_bwd_steps(plan: Plan, q, k, v, do, lse, delta, schedule, dq_acc, dk_acc
           _ptr(delta), n, qs, ks, _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), _stream(stream))
 
 
+def attn_fwd_fused(plan: Plan, q, k, v, state: State, scale: float = 0.0, stream=None):
+    """Every forward ring step in one launch, the state on chip between steps
+    (marble_attn_fwd_fused)."""
+    c = _qkv(plan, q, k, v, scale)
+    st = state._c()
+    _call("marble_attn_fwd_fused", plan.handle, ctypes.byref(c), ctypes.byref(st),
+          _stream(stream))
+
+
+def attn_bwd_fused(plan: Plan, q, k, v, do, lse, delta, dq_acc, dk_acc, dv_acc,
+                   scale: float = 0.0, stream=None):
+    """Every backward ring step, one dK/dV launch per kv shard over its ring
+    (marble_attn_bwd_fused); accumulators fp32 and caller-zeroed."""
+    import torch
+    c = _qkv(plan, q, k, v, scale)
+    _need(do, torch.bfloat16, "do", q.shape)
+    _need(lse, torch.float32, "lse", (q.shape[1], plan.n))
+    _need(delta, torch.float32, "delta", (q.shape[1], plan.n))
+    _need(dq_acc, torch.float32, "dq_acc", q.shape)
+    _need(dk_acc, torch.float32, "dk_acc", k.shape)
+    _need(dv_acc, torch.float32, "dv_acc", k.shape)
+    _call("marble_attn_bwd_fused", plan.handle, ctypes.byref(c), _ptr(do), _ptr(lse),
+          _ptr(delta), _ptr(dq_acc), _ptr(dk_acc), _ptr(dv_acc), _stream(stream))
+
+
 def forward(plan: Plan, q, k, v, state: State, o, lse, needed: bool = False, scale: float = 0.0,
-            stream=None, merge: str = "carried"):
-    """All forward ring steps (r-major, keeping shard r's state hot in L2) + finalize."""
-    attn_steps(plan, q, k, v, ring_schedule(plan.num_shards, needed), state, scale=scale,
-               stream=stream, merge=merge)
+            stream=None, merge: str = "carried", fused: bool = False):
+    """All forward ring steps (r-major, keeping shard r's state hot in L2) + finalize;
+    ``fused``: the whole ring in one launch (marble_attn_fwd_fused)."""
+    if fused:
+        if needed or merge not in (None, "carried"):
+            raise ValueError("the fused ring carries the fp32 state over the ring steps only")
+        attn_fwd_fused(plan, q, k, v, state, scale=scale, stream=stream)
+    else:
+        attn_steps(plan, q, k, v, ring_schedule(plan.num_shards, needed), state, scale=scale,
+                   stream=stream, merge=merge)
     attn_finalize(plan, state, o, lse, stream=stream)
 
 
 def backward(plan: Plan, q, k, v, o, do, lse, delta, dq_acc, dk_acc, dv_acc,
-             needed: bool = False, scale: float = 0.0, stream=None):
-    """bwd preprocessing + all backward ring steps (accumulators must be zeroed)."""
+             needed: bool = False, scale: float = 0.0, stream=None, fused: bool = False):
+    """bwd preprocessing + all backward ring steps (accumulators must be zeroed);
+    ``fused``: one dK/dV launch per kv shard over its ring (marble_attn_bwd_fused)."""
     attn_bwd_prep(plan, o, do, delta, stream=stream)
-    attn_bwd_steps(plan, q, k, v, do, lse, delta, ring_schedule(plan.num_shards, needed),
-                   dq_acc, dk_acc, dv_acc, scale=scale, stream=stream)
+    if fused:
+        if needed:
+            raise ValueError("the fused ring runs the ring steps, not the needed-block mode")
+        attn_bwd_fused(plan, q, k, v, do, lse, delta, dq_acc, dk_acc, dv_acc, scale=scale,
+                       stream=stream)
+    else:
+        attn_bwd_steps(plan, q, k, v, do, lse, delta, ring_schedule(plan.num_shards, needed),
+                       dq_acc, dk_acc, dv_acc, scale=scale, stream=stream)
 
 
 def layout_vision_groups(sample, seg):

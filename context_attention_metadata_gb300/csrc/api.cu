@@ -612,6 +612,41 @@ MARBLE_API marble_status_t marble_attn_bwd_steps(const marble_plan_t* p, const m
   return st;
 }
 
+MARBLE_API marble_status_t marble_attn_fwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                                 const marble_state_t* state,
+                                                 marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_fwd_fused");
+  if (!p || !state) return fail(MARBLE_ERR_INVALID_ARG, "plan and state must be non-null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->o_acc, "state.o_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->m, "state.m")) != MARBLE_OK) return st;
+  if ((st = check_tensor(state->l, "state.l")) != MARBLE_OK) return st;
+  st = run_attn_fwd_fused(p, qkv, state, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
+}
+
+MARBLE_API marble_status_t marble_attn_bwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                                 const void* d_o, const float* lse,
+                                                 const float* delta, float* dq_acc,
+                                                 float* dk_acc, float* dv_acc,
+                                                 marble_stream_t stream) {
+  NvtxRange nvtx_("marble_attn_bwd_fused");
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  marble_status_t st;
+  if ((st = check_qkv(p, qkv)) != MARBLE_OK) return st;
+  if ((st = check_tensor(d_o, "d_o")) != MARBLE_OK) return st;
+  if ((st = check_tensor(lse, "lse")) != MARBLE_OK) return st;
+  if ((st = check_tensor(delta, "delta")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dq_acc, "dq_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dk_acc, "dk_acc")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dv_acc, "dv_acc")) != MARBLE_OK) return st;
+  st = run_attn_bwd_fused(p, qkv, d_o, lse, delta, dq_acc, dk_acc, dv_acc, (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  return st;
+}
+
 MARBLE_API marble_status_t marble_attn_finalize(const marble_plan_t* p,
                                                 const marble_state_t* state, int32_t hq,
                                                 int32_t d, void* o_bf16, float* lse,

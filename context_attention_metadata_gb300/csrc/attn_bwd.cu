@@ -34,6 +34,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <cstdlib>
 
 #include "common.cuh"
 #include "internal.h"
@@ -50,6 +51,7 @@ constexpr int kDsBufs = 4;        // steps whose dS^T tiles the scratch holds at
 constexpr size_t kDsScratchCap = size_t(32) << 30;  // fewer buffers (down to 2) above this
 constexpr int kDkdvStreams = 4;   // side streams of the dK/dV launches
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxShards = 256;   // the most virtual shards a plan has
 
 struct BwdParams {
   CUtensorMap q_map, k_map, v_map, do_map;
@@ -67,9 +69,16 @@ struct BwdParams {
   const int32_t* step_off;   // [nb][P+1] tiles of the q shard's earlier q blocks in a step
   const int32_t* colT_j;     // [nnz] index of a column-list entry in its q block's row list
   long long ds_slot0;        // first scratch slot of this step's dS^T tiles
+  // fused ring (ring_len > 0, dK/dV kernel only): kv shard kv_shard over ring steps
+  // [ring_s0, ring_s0 + ring_len), i.e. q shards (kv_shard + s) mod P, its dK/dV kept on chip
+  // across them; the dS^T tile of q block nq lands at ds_base[nq / bps] + (its index in the
+  // step's numbering) * hq + head
+  int ring_s0, ring_len;
+  long long ds_base[kMaxShards];
   unsigned* sched;           // ticket counter pair of the launch
   const int32_t* tracks;     // [4][n] plan order
   const int32_t* kiv;        // [2][n] lo, hi of every key's visible-query interval
+  const int32_t* qidx;       // [n] plan order -> index in the given token order (the plan's perm)
   const uint8_t* iv_block;   // [nb] 1: every key of the block has an exact interval
   const float* lse;          // [hq][n] natural log
   const float* delta;        // [hq][n]
@@ -86,13 +95,21 @@ struct BwdParams {
   float scale, sl2;
 };
 
-// queue entry: head, block (plan order), list start and length
+// queue entry: head, block (plan order), list start and length; a dK/dV unit of the fused
+// ring may have its list in two pieces of the column CSR: entries [0, La) at e0 + x, the
+// rest at e1 + (x - La)
 struct Queue {
   int head[kQueue];  // -1: no more work
   int blk[kQueue];
   int T[kQueue];
+  int La[kQueue];
   long long e0[kQueue];
+  long long e1[kQueue];
 };
+
+__device__ __forceinline__ int64_t list_entry(int64_t e0, int64_t e1, int La, int x) {
+  return x < La ? e0 + x : e1 + (x - La);
+}
 
 // ticket -> unit of the dQ kernel: q head h (innermost), q block of the order
 __device__ __forceinline__ void dq_unit(const BwdParams& p, unsigned t, int* h, int* blk,
@@ -113,9 +130,11 @@ __device__ __forceinline__ void dq_unit(const BwdParams& p, unsigned t, int* h, 
 }
 
 // ticket -> unit of the dK/dV kernel: kv head (innermost), kv block of the order (or of the
-// needed list); T = number of listed q blocks (items = T x group)
+// needed list); T = number of listed q blocks (items = T x group).  In the fused ring the
+// list runs over the q shards of the ring range, in ring order: one CSR range, or two when
+// the range wraps past the last shard.
 __device__ __forceinline__ void dkdv_unit(const BwdParams& p, unsigned t, int* kh, int* blk,
-                                          int64_t* c0, int* T) {
+                                          int64_t* c0, int* T, int64_t* c1, int* La) {
   *kh = (int)(t % (unsigned)p.hkv);
   const unsigned i = t / (unsigned)p.hkv;
   int64_t nk;
@@ -124,8 +143,22 @@ __device__ __forceinline__ void dkdv_unit(const BwdParams& p, unsigned t, int* k
   else
     nk = p.needed[p.needed_ptr[p.q_shard] + i];
   *blk = (int)nk;
+  if (p.ring_len > 0) {
+    const int a = (p.kv_shard + p.ring_s0) % p.P, b = a + p.ring_len;
+    *c0 = p.colT_ptr[nk * p.P + a];
+    if (b <= p.P) {
+      *La = *T = (int)(p.colT_ptr[nk * p.P + b] - *c0);
+      *c1 = 0;
+    } else {
+      *La = (int)(p.colT_ptr[nk * p.P + p.P] - *c0);
+      *c1 = p.colT_ptr[nk * p.P];
+      *T = *La + (int)(p.colT_ptr[nk * p.P + (b - p.P)] - *c1);
+    }
+    return;
+  }
   *c0 = p.colT_ptr[nk * p.P + p.q_shard];
-  *T = (int)(p.colT_ptr[nk * p.P + p.q_shard + 1] - *c0);
+  *La = *T = (int)(p.colT_ptr[nk * p.P + p.q_shard + 1] - *c0);
+  *c1 = 0;
 }
 
 // scheduler loop (one lane): post units until the tickets run out, then a terminator.  An
@@ -136,24 +169,28 @@ __device__ void schedule(const BwdParams& p, Queue& queue, uint64_t* ufull, uint
   for (int uc = 0;; ++uc) {
     const int slot = uc % kQueue;
     if (uc >= kQueue && !mbar_wait(&uempty[slot], ((uc / kQueue) - 1) & 1, w)) return;
-    int hd = -1, blk = 0, T = 0;
-    int64_t e0 = 0;
-    while (true) {  // units with an empty list (possible only in the needed-block mode) are skipped
+    int hd = -1, blk = 0, T = 0, La = 0;
+    int64_t e0 = 0, e1 = 0;
+    while (true) {  // units with an empty list (needed-block mode, part of a ring) are skipped
       const unsigned t = atomicAdd(p.sched, 1u);
       if (t >= (unsigned)p.nwork) {
         hd = -1;
         break;
       }
-      if (kDQ)
+      if (kDQ) {
         dq_unit(p, t, &hd, &blk, &e0, &T);
-      else
-        dkdv_unit(p, t, &hd, &blk, &e0, &T);
+        La = T;
+      } else {
+        dkdv_unit(p, t, &hd, &blk, &e0, &T, &e1, &La);
+      }
       if (T > 0) break;
     }
     queue.head[slot] = hd;
     queue.blk[slot] = blk;
     queue.T[slot] = T;
+    queue.La[slot] = La;
     queue.e0[slot] = e0;
+    queue.e1[slot] = e1;
     mbar_arrive(&ufull[slot]);
     if (hd < 0) return;
   }
@@ -463,8 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       const int kh = queue.head[slot];
       if (kh < 0) break;
       const int64_t nk = queue.blk[slot];
-      const int L = queue.T[slot];
-      const int64_t c0 = queue.e0[slot];
+      const int L = queue.T[slot], La = queue.La[slot];
+      const int64_t c0 = queue.e0[slot], c1 = queue.e1[slot];
       const int items = L * p.group;
       // K and V of the unit once the previous unit's last S^T / dP^T have read the slot
       if (uc >= 1 && !wait_all(&bar[K_KVEMPTY], (uc - 1) & 1, w)) break;
@@ -480,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         const int s = g & 1;
         if (g >= 2 && !wait_all(&bar[K_QEMPTY0 + s], ((g >> 1) - 1) & 1, w)) { ok = false; break; }
         const int h = kh * p.group + it / L;
-        const int nqb = p.colT_row[c0 + it % L];
+        const int nqb = p.colT_row[list_entry(c0, c1, La, it % L)];
         if (lane == 0) {
           uint8_t* sQ = sQ0 + s * 2 * kTile;
           uint8_t* sDO = sQ + kTile;
@@ -667,8 +704,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         break;
       }
       const int64_t nk = queue.blk[slot];
-      const int L = queue.T[slot];
-      const int64_t c0 = queue.e0[slot];
+      const int L = queue.T[slot], La = queue.La[slot];
+      const int64_t c0 = queue.e0[slot], c1 = queue.e1[slot];
       const int items = L * p.group;
       const int64_t tk = nk * 128 + row;
       const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
@@ -679,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       const int klo = p.kiv[tk], khi = p.kiv[n + tk];
       for (int it = 0; it < items; ++it, ++g) {
         const int h = kh * p.group + it / L;
-        const int64_t e = c0 + it % L;
+        const int64_t e = list_entry(c0, c1, La, it % L);
         const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
         const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
         // stage this half's per-query LSE (base 2) and delta (threads of rows [0, 64))
@@ -694,7 +731,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
         uint32_t lm[2] = {~0u, ~0u};
         if (partial && ivt) {
-          const int32_t* qpos = p.tracks + 3 * n + (int64_t)p.colT_row[e] * 128 + half * 64;
+          // lo_k <= i_q < hi_k, i_q the query's index in the given token order
+          const int32_t* qpos = p.qidx + (int64_t)p.colT_row[e] * 128 + half * 64;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             uint32_t bits = 0;
@@ -801,7 +839,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
           const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
           int64_t jj = p.colT_j[e];
           if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
-          ds_mail[half] = p.ds_slot0 + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
+          const long long base = p.ring_len > 0 ? p.ds_base[nq / p.bps] : p.ds_slot0;
+          ds_mail[half] = base + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
         }
         fence_proxy_async_smem();
         mbar_arrive(&bar[K_DSSTG0 + half]);
@@ -876,12 +915,12 @@ size_t dkdv_smem() {
   return 6 * (128 * D * 2) + 16384 + 2 * 2 * 128 * 4 + 1024;
 }
 
+// everything of a backward call but the step, its work list and the scratch: encoded once
 template <int D>
-marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
-                             const float* lse, const float* delta, int n_steps,
-                             const int* q_shards, const int* kv_shards, float* dq, float* dk,
-                             float* dv, cudaStream_t s) {
-  BwdParams prm;
+marble_status_t prepare_bwd(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
+                            const float* lse, const float* delta, float* dq, float* dk, float* dv,
+                            BwdParams* out) {
+  BwdParams& prm = *out;
   memset(&prm, 0, sizeof(prm));
   const int64_t n = pl->n;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -907,6 +946,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   prm.needed = pl->needed;
   prm.tracks = pl->tracks;
   prm.kiv = pl->kiv;
+  prm.qidx = pl->perm;
   prm.iv_block = pl->iv_block;
   prm.lse = lse;
   prm.delta = delta;
@@ -924,21 +964,87 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   prm.W = pl->W;
   prm.scale = qkv->scale > 0.f ? qkv->scale : 1.0f / sqrtf((float)D);
   prm.sl2 = prm.scale * kLog2e;
-  const size_t smem_q = DqSmem<D>::bytes(), smem_k = dkdv_smem<D>();
+  prm.step_off = pl->step_off;
+  prm.colT_j = pl->colT_j;
   if (once_per_device(D == 128 ? 3 : 4)) {
-    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_q);
+    cudaError_t e = cudaFuncSetAttribute(k_bwd_dq<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)DqSmem<D>::bytes());
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(k_bwd_dkdv<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)smem_k);
+                               (int)dkdv_smem<D>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
   }
+  return MARBLE_OK;
+}
+
+// The plan-owned scratch for bf16 dS^T tiles: at least `need` bytes, and its tensor map as
+// [slots * 128 rows] x 128 columns with 64 x 128 boxes.
+marble_status_t ds_scratch(const marble_plan_t* pl, size_t slots, cudaStream_t s, BwdParams* prm) {
+  std::lock_guard<std::mutex> lock(pl->scratch_mu);
+  const size_t need = slots * 32768;
+  if (need > pl->ds_scratch_bytes) {
+    // earlier calls joined their side streams back into their stream, and calls on one plan
+    // are ordered: freeing in the order of `s` is safe
+    if (pl->ds_scratch) {
+      dev_free(pl->ds_scratch, s);
+      pl->ds_scratch = nullptr;
+      pl->ds_scratch_bytes = 0;
+    }
+    void* q = nullptr;
+    if (dev_alloc(&q, need, s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return fail(MARBLE_ERR_OOM, "allocation of the backward dS scratch failed (" +
+                                      std::to_string(need) + " bytes)");
+    }
+    pl->ds_scratch = q;
+    pl->ds_scratch_bytes = need;
+  }
+  if (slots > 0 && !make_rows_map(&prm->ds_map, pl->ds_scratch, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                  2, (int64_t)slots * 128, 1, 128, 64, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B))
+    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
+  return MARBLE_OK;
+}
+
+int sm_count() {
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+// dQ GEMM of step (q shard r, kv shard or every needed block), reading dS^T slots from slot0
+template <int D>
+void launch_dq(const marble_plan_t* pl, const BwdParams& prm, int r, int j, long long slot0,
+               int hq, int sms, cudaStream_t s) {
   const int P = pl->P;
-  prm.step_off = pl->step_off;
-  prm.colT_j = pl->colT_j;
+  BwdParams pq = prm;
+  pq.q_shard = r;
+  pq.kv_shard = j;
+  pq.ds_slot0 = slot0;
+  pq.ring_len = 0;
+  const int64_t seg = (int64_t)r * (P + 1) + (j >= 0 ? j : P);
+  pq.order = pl->fwd_order + seg * pl->bps;
+  pq.nwork = pl->h_fwd_nwork[seg] * hq;
+  if (pq.nwork > 0) {
+    pq.sched = sched_slot(pl);
+    const int span = timing_begin(s);
+    k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kGThreads, DqSmem<D>::bytes(), s>>>(pq);
+    timing_end(span, s, kTimeDq, 1);
+  }
+}
+
+template <int D>
+marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
+                             const float* lse, const float* delta, int n_steps,
+                             const int* q_shards, const int* kv_shards, float* dq, float* dk,
+                             float* dv, cudaStream_t s) {
+  BwdParams prm;
+  marble_status_t rc = prepare_bwd<D>(pl, qkv, d_o, lse, delta, dq, dk, dv, &prm);
+  if (rc != MARBLE_OK) return rc;
+  const int smem_k = (int)dkdv_smem<D>();
+  const int sms = sm_count();
+  const int P = pl->P;
   // scratch for the bf16 dS^T tiles of kDsBufs steps: the dQ GEMM of step i reads buffer
   // i mod kDsBufs while the dK/dV kernels of the next steps write the others
   int64_t max_tiles = 0;  // the largest step of this call
@@ -951,31 +1057,8 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int nbuf = (int)std::max<int64_t>(
       2, std::min<int64_t>(kDsBufs, (int64_t)(kDsScratchCap / ((size_t)std::max<int64_t>(
                                                                  buf_slots, 1) * 32768))));
-  {
-    std::lock_guard<std::mutex> lock(pl->scratch_mu);
-    const size_t need = (size_t)(nbuf * buf_slots) * 32768;
-    if (need > pl->ds_scratch_bytes) {
-      // earlier calls joined their side streams back into their stream, and calls on one
-      // plan are ordered: freeing in the order of `s` is safe
-      if (pl->ds_scratch) {
-        dev_free(pl->ds_scratch, s);
-        pl->ds_scratch = nullptr;
-        pl->ds_scratch_bytes = 0;
-      }
-      void* q = nullptr;
-      if (dev_alloc(&q, need, s) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return fail(MARBLE_ERR_OOM, "allocation of the backward dS scratch failed (" +
-                                        std::to_string(need) + " bytes)");
-      }
-      pl->ds_scratch = q;
-      pl->ds_scratch_bytes = need;
-    }
-  }
-  if (buf_slots > 0 &&
-      !make_rows_map(&prm.ds_map, pl->ds_scratch, bf, 2, nbuf * buf_slots * 128, 1, 128, 64,
-                     128, sw))
-    return fail(MARBLE_ERR_CUDA, "cuTensorMapEncodeTiled failed for the dS scratch");
+  rc = ds_scratch(pl, (size_t)(nbuf * buf_slots), s, &prm);
+  if (rc != MARBLE_OK) return rc;
   // Step i: the dK/dV kernel (a side stream) writes the step's dS^T tiles into buffer
   // i mod nbuf of the scratch, then the dQ GEMM (stream s) reads them; dK/dV of step
   // i + nbuf waits until the dQ GEMM of step i has finished with that buffer.  dK/dV of kv
@@ -999,7 +1082,6 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   auto make_event = [](cudaEvent_t* ev) {
     return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
   };
-  int launches_q = 0, launches_k = 0;
   cudaError_t err = cudaSuccess;
   for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
     prm.q_shard = q_shards[i];
@@ -1025,7 +1107,6 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
         const int span = timing_begin(sks);
         k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
         timing_end(span, sks, kTimeDkdv, 1);
-        ++launches_k;
       }
       if (sks != s && err == cudaSuccess) {
         err = make_event(&ev_k[i]);
@@ -1035,17 +1116,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     }
     // dQ GEMM: the q blocks of the q shard with tiles in this step, longest list first
     if (err == cudaSuccess) {
-      BwdParams pq = prm;
-      const int64_t seg = (int64_t)pq.q_shard * (P + 1) + (pq.kv_shard >= 0 ? pq.kv_shard : P);
-      pq.order = pl->fwd_order + seg * pl->bps;
-      pq.nwork = pl->h_fwd_nwork[seg] * qkv->hq;
-      if (pq.nwork > 0) {
-        pq.sched = sched_slot(pl);
-        const int span = timing_begin(s);
-        k_bwd_dq<D><<<(unsigned)(pq.nwork < sms ? pq.nwork : sms), kGThreads, smem_q, s>>>(pq);
-        timing_end(span, s, kTimeDq, 1);
-        ++launches_q;
-      }
+      launch_dq<D>(pl, prm, prm.q_shard, prm.kv_shard, prm.ds_slot0, qkv->hq, sms, s);
       if (s2 != s) {
         err = make_event(&ev_q[i]);
         if (err == cudaSuccess) err = cudaEventRecord(ev_q[i], s);
@@ -1058,15 +1129,128 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
     if (ev) cudaEventDestroy(ev);
   for (cudaEvent_t ev : ev_q)
     if (ev) cudaEventDestroy(ev);
-  (void)launches_q;
-  (void)launches_k;
   if (err != cudaSuccess) return cuda_fail(err, "ordering of the backward streams");
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");
   return MARBLE_OK;
 }
 
+// The fused ring: for every kv shard j, one dK/dV launch over the ring steps of a range
+// (q shards j, j + 1, ... in ring order; the whole ring unless its dS^T tiles exceed the
+// scratch cap), keeping the kv blocks' dK/dV in TMEM across all of them and adding them to
+// dk_acc / dv_acc once per range; then the range's dQ GEMMs, one per step (q shard, j), on
+// the caller's stream.  Ranges of one kv shard run in order on one side stream.
+template <int D>
+marble_status_t launch_fused(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
+                             const float* lse, const float* delta, float* dq, float* dk,
+                             float* dv, cudaStream_t s) {
+  BwdParams prm;
+  marble_status_t rc = prepare_bwd<D>(pl, qkv, d_o, lse, delta, dq, dk, dv, &prm);
+  if (rc != MARBLE_OK) return rc;
+  const int smem_k = (int)dkdv_smem<D>();
+  const int sms = sm_count();
+  const int P = pl->P;
+  const int64_t hq = qkv->hq;
+  // ranges of ring steps: consecutive q shards of one kv shard whose dS^T tiles fit in half
+  // the scratch cap (two ranges in flight); MARBLE_DS_SCRATCH_CAP_MB lowers the cap (tests)
+  struct Range { int j, s0, len; int64_t tiles; };
+  std::vector<Range> ranges;
+  size_t cap = kDsScratchCap;
+  if (const char* env = std::getenv("MARBLE_DS_SCRATCH_CAP_MB")) {
+    const unsigned long long mb = std::strtoull(env, nullptr, 10);
+    if (mb > 0 && (mb << 20) < cap) cap = (size_t)(mb << 20);
+  }
+  const int64_t cap_slots = (int64_t)(cap / 2 / 32768);
+  int64_t buf_slots = 0;
+  for (int j = 0; j < P; ++j) {
+    int s0 = 0;
+    int64_t acc = 0;
+    for (int st = 0; st < P; ++st) {
+      const int r = (j + st) % P;
+      const int64_t t = pl->h_step_tiles[(size_t)r * (P + 1) + j];
+      if (st > s0 && (acc + t) * hq > cap_slots) {
+        ranges.push_back({j, s0, st - s0, acc});
+        buf_slots = std::max(buf_slots, acc * hq);
+        s0 = st;
+        acc = 0;
+      }
+      acc += t;
+    }
+    ranges.push_back({j, s0, P - s0, acc});
+    buf_slots = std::max(buf_slots, acc * hq);
+  }
+  const int nbuf = 2;
+  rc = ds_scratch(pl, (size_t)(nbuf * buf_slots), s, &prm);
+  if (rc != MARBLE_OK) return rc;
+  cudaStream_t sk[kDkdvStreams];
+  int nsk = 0;
+  for (int k = 0; k < kDkdvStreams; ++k) {
+    cudaStream_t x = side_stream(k);
+    if (!x) break;
+    cudaError_t e = stream_fork(s, x);
+    if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+    sk[nsk++] = x;
+  }
+  if (nsk == 0) sk[nsk++] = s;
+  const int nr = (int)ranges.size();
+  std::vector<cudaEvent_t> ev_q(nr, nullptr);
+  cudaError_t err = cudaSuccess;
+  for (int i = 0; i < nr && err == cudaSuccess; ++i) {
+    const Range& g = ranges[i];
+    BwdParams pk = prm;
+    pk.kv_shard = g.j;
+    pk.q_shard = 0;
+    pk.ring_s0 = g.s0;
+    pk.ring_len = g.len;
+    long long base = (long long)(i % nbuf) * buf_slots;
+    for (int st = g.s0; st < g.s0 + g.len; ++st) {
+      const int r = (g.j + st) % P;
+      pk.ds_base[r] = base;
+      base += (long long)pl->h_step_tiles[(size_t)r * (P + 1) + g.j] * hq;
+    }
+    // every kv block of shard j with a tile anywhere in its column (blocks without one in this
+    // range are skipped by the scheduler)
+    const int64_t seg = (int64_t)g.j * (P + 1) + P;
+    pk.order = pl->bwd_order + seg * pl->bps;
+    pk.nwork = pl->h_bwd_nwork[seg] * qkv->hkv;
+    const cudaStream_t sks = sk[g.j % nsk];
+    if (sks != s && i >= nbuf) err = cudaStreamWaitEvent(sks, ev_q[i - nbuf], 0);
+    if (pk.nwork > 0 && err == cudaSuccess) {
+      pk.sched = sched_slot(pl);
+      const int span = timing_begin(sks);
+      k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+      timing_end(span, sks, kTimeDkdv, 1);
+    }
+    if (sks != s && err == cudaSuccess) err = stream_fork(sks, s);
+    for (int st = g.s0; st < g.s0 + g.len && err == cudaSuccess; ++st) {
+      const int r = (g.j + st) % P;
+      launch_dq<D>(pl, prm, r, g.j, pk.ds_base[r], (int)hq, sms, s);
+    }
+    if (err == cudaSuccess && sks != s) {
+      err = cudaEventCreateWithFlags(&ev_q[i], cudaEventDisableTiming);
+      if (err == cudaSuccess) err = cudaEventRecord(ev_q[i], s);
+    }
+  }
+  for (int k = 0; k < nsk && err == cudaSuccess; ++k)
+    if (sk[k] != s) err = stream_fork(sk[k], s);
+  for (cudaEvent_t ev : ev_q)
+    if (ev) cudaEventDestroy(ev);
+  if (err != cudaSuccess) return cuda_fail(err, "ordering of the fused backward streams");
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch of the fused backward kernels");
+  return MARBLE_OK;
+}
+
 }  // namespace
+
+marble_status_t run_attn_bwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                   const void* d_o, const float* lse, const float* delta,
+                                   float* dq, float* dk, float* dv, cudaStream_t s) {
+  if (p->P > kMaxShards) return fail(MARBLE_ERR_UNSUPPORTED, "more than 256 shards");
+  if (qkv->d == 128) return launch_fused<128>(p, qkv, d_o, lse, delta, dq, dk, dv, s);
+  if (qkv->d == 64) return launch_fused<64>(p, qkv, d_o, lse, delta, dq, dk, dv, s);
+  return fail(MARBLE_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+}
 
 marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
                              const float* lse, const float* delta, int n_steps,

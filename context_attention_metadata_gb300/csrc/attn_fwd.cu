@@ -32,6 +32,7 @@
 // Scores are kept in base-2 units (s * scale * log2 e); the stored m is in the same units
 // and always an integer, so that every rescale (lazy, when the max grows past 2^8, within
 // a call; and the merge with the stored state) multiplies by an exact power of two.
+#include <limits.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -105,6 +106,7 @@ struct FwdParams {
   int first;
   int lse_merge;   // 0 carried state; 1 merge of bf16 partials (standard ring); 2 of fp32 ones
   const int32_t* kiv;       // [2][n] lo, hi of every key's visible-query interval
+  const int32_t* qidx;      // [n] plan order -> index in the given token order (the plan's perm)
   const uint8_t* iv_block;  // [nb] 1: every key of the block has an exact interval
   float scale_log2;
 };
@@ -407,6 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
       const int64_t tq = ((int64_t)p.q_shard * p.bps + unit % p.bps) * 128 + row;
       const int sq = p.tracks[tq], gq = p.tracks[n + tq], zq = p.tracks[2 * n + tq],
                 pq = p.tracks[3 * n + tq];
+      const int iq = p.qidx[tq];  // the interval test's coordinate: the query's index
       const uint32_t ob = tO + (uint32_t)(uc & 1) * 128;
       float m_run = -INFINITY, l_h = 0.f;
       for (int j = 0; j < T; ++j, ++g) {
@@ -415,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         uint32_t lm[2] = {~0u, ~0u};  // legal-key bits of this row in this half's 64 columns
         const int64_t kb = partial ? p.step_col[e0 + j] : 0;
         // every key of the block has an exact visible-query interval: the test is
-        // lo_k <= pos_q < hi_k, with the half's 64 (lo, hi) pairs read straight from global
-        // memory (the same addresses for every lane: broadcast loads)
+        // lo_k <= i_q < hi_k (i_q the query's index in the given token order), with the half's
+        // 64 (lo, hi) pairs read straight from global memory (the same addresses for every
+        // lane: broadcast loads)
         const bool ivt = partial && p.iv_block[kb] != 0;
         if (ivt) {
           const int32_t* klo = p.kiv + kb * 128 + half * 64;
@@ -428,10 +432,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
             for (int t2 = 0; t2 < 32; t2 += 4) {
               const int4 l4 = __ldg(reinterpret_cast<const int4*>(klo + cc * 32 + t2));
               const int4 h4 = __ldg(reinterpret_cast<const int4*>(khi + cc * 32 + t2));
-              bits |= ((pq >= l4.x) & (pq < h4.x) ? 1u : 0u) << t2;
-              bits |= ((pq >= l4.y) & (pq < h4.y) ? 1u : 0u) << (t2 + 1);
-              bits |= ((pq >= l4.z) & (pq < h4.z) ? 1u : 0u) << (t2 + 2);
-              bits |= ((pq >= l4.w) & (pq < h4.w) ? 1u : 0u) << (t2 + 3);
+              bits |= ((iq >= l4.x) & (iq < h4.x) ? 1u : 0u) << t2;
+              bits |= ((iq >= l4.y) & (iq < h4.y) ? 1u : 0u) << (t2 + 1);
+              bits |= ((iq >= l4.z) & (iq < h4.z) ? 1u : 0u) << (t2 + 2);
+              bits |= ((iq >= l4.w) & (iq < h4.w) ? 1u : 0u) << (t2 + 3);
             }
             lm[cc] = bits;
           }
@@ -760,6 +764,7 @@ marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
   prm->step_tag = pl->step_tag;
   prm->tracks = pl->tracks;
   prm->kiv = pl->kiv;
+  prm->qidx = pl->perm;
   prm->iv_block = pl->iv_block;
   prm->o_acc = st->o_acc;
   prm->m = st->m;
@@ -839,7 +844,50 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
   return MARBLE_OK;
 }
 
+// The fused forward: one launch over every (q block, q head) of every shard, each row
+// walking its tiles in ring order (kv shard (r - s) mod P at step s, the plan's ring-ordered
+// copy of its lists) with the fp32 state held on chip from the first step to the last; the
+// state is written once, as the FIRST step of the per-step path writes it.
+template <int D>
+marble_status_t launch_fused(const marble_plan_t* pl, const marble_qkv_t* qkv,
+                             const marble_state_t* st, cudaStream_t s) {
+  FwdParams prm;
+  marble_status_t rc = prepare<D>(pl, qkv, st, &prm);
+  if (rc != MARBLE_OK) return rc;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // every block of the pack as one shard of nb blocks, whole rows, ring-ordered lists
+  prm.bps = (int)pl->nb;
+  prm.q_shard = 0;
+  prm.kv_shard = -1;
+  prm.first = 1;
+  prm.lse_merge = 0;
+  prm.step_col = pl->ring_col;
+  prm.step_tag = pl->ring_tag;
+  prm.order = pl->fwd_order_all;
+  prm.units = (int)(pl->nb * qkv->hq);
+  prm.nwork = pl->h_fwd_nwork_all * qkv->hq;
+  prm.sched = sched_slot(pl);
+  const unsigned grid = (unsigned)(prm.units < sms ? prm.units : sms);
+  const int span = timing_begin(s);
+  k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), s>>>(prm);
+  timing_end(span, s, kTimeFwd, 1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch k_attn_fwd (fused)");
+  return MARBLE_OK;
+}
+
 }  // namespace
+
+marble_status_t run_attn_fwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                   const marble_state_t* st, cudaStream_t s) {
+  if ((int64_t)p->nb * qkv->hq > INT_MAX)
+    return fail(MARBLE_ERR_UNSUPPORTED, "too many (block, head) work units");
+  if (qkv->d == 128) return launch_fused<128>(p, qkv, st, s);
+  if (qkv->d == 64) return launch_fused<64>(p, qkv, st, s);
+  return fail(MARBLE_ERR_UNSUPPORTED, "head dim must be 64 or 128");
+}
 
 marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int n_steps,
                              const int* q_shards, const int* kv_shards, const uint32_t* flags,

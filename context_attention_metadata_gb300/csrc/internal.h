@@ -73,6 +73,13 @@ struct marble_plan {
   int32_t* bwd_order = nullptr;      // [P*(P+1)*bps] over colT_ptr (kv blocks)
   int32_t* bwd_nwork = nullptr;      // [P*(P+1)]
   std::vector<int32_t> h_fwd_nwork, h_bwd_nwork;
+  // the fused forward: row lists in ring order (same CSR ranges as step_ptr over all kv
+  // shards) and the work order of every block of the pack, longest row first
+  int32_t* ring_col = nullptr;       // [nnz]
+  uint8_t* ring_tag = nullptr;       // [nnz]
+  int32_t* fwd_order_all = nullptr;  // [nb]
+  int32_t* fwd_nwork_all = nullptr;  // [1]
+  int32_t h_fwd_nwork_all = 0;
   // compact tile numbering of each step (the backward's dS tiles): step_off[nq*(P+1)+opt] is
   // the number of tiles of the q blocks before nq in its q shard, for option opt (kv shard opt,
   // or every kv shard when opt == P); colT_j[e] the index of column-list entry e's kv block in
@@ -150,6 +157,13 @@ cudaError_t launch_debug_wait(unsigned* err, uint64_t limit_ns, cudaStream_t s);
 marble_status_t run_attn_fwd(const marble_plan_t* p, const marble_qkv_t* qkv, int n_steps,
                              const int* q_shards, const int* kv_shards, const uint32_t* flags,
                              const marble_state_t* st, cudaStream_t s);
+// the fused ring (attn_fwd.cu, attn_bwd.cu): every ring step of the pass in one forward
+// launch, and one dK/dV launch per kv shard over its ring
+marble_status_t run_attn_fwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                   const marble_state_t* st, cudaStream_t s);
+marble_status_t run_attn_bwd_fused(const marble_plan_t* p, const marble_qkv_t* qkv,
+                                   const void* d_o, const float* lse, const float* delta,
+                                   float* dq, float* dk, float* dv, cudaStream_t s);
 marble_status_t run_attn_bwd(const marble_plan_t* p, const marble_qkv_t* qkv, const void* d_o,
                              const float* lse, const float* delta, int n_steps,
                              const int* q_shards, const int* kv_shards, float* dq, float* dk,

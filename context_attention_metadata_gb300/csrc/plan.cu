@@ -329,8 +329,7 @@ __global__ void k_iv_keys(const int32_t* __restrict__ sample, const int32_t* __r
     if (sample[m] <= s) lo2 = m + 1; else b2 = m;
   }
   b = b2;
-  const int64_t c1 = min(b, k + (int64_t)W);
-  int64_t lo = k, hi = c1;  // causal part, empty when W == 0
+  int64_t lo = k, hi = min(b, k + (int64_t)W);  // causal part, empty when W == 0
   bool ex = true;
   const int g = seg[k], z = noise[k];
   if (g >= 0) {
@@ -353,6 +352,196 @@ __global__ void k_iv_keys(const int32_t* __restrict__ sample, const int32_t* __r
   lo_out[k] = (int32_t)lo;
   hi_out[k] = (int32_t)hi;
   if (!ex) iv_orig[k >> 7] = 0;
+}
+
+// Key intervals of a pack given with a position track (a permuted pack, MARBLE s04 "Layout
+// transforms"), on globally causal layers.  Key k is seen causally by the queries of its
+// sample at a position >= pos[k]; the layout transform is what makes the visible queries
+// one range of indices.  Here every key gets a hull [lo, hi) that provably holds all of its
+// visible queries, and a warp then checks the predicate on every query of the hull: the key
+// is exact when all of them see it.
+//   causal hull  the smallest and largest index among the sample's tokens at a position
+//                >= pos[k], from suffix minima / maxima over positions (this needs positions
+//                that are a permutation of [0, n) with each sample holding one range of
+//                them: checked, and otherwise no key is exact);
+//   segment      every token of k's segment id lies in [gfirst, glast], cut to the sample;
+//   noise        a noise key is seen only inside [zfirst, zlast].
+// inv[position] = index.
+__global__ void k_pos_inv(const int32_t* __restrict__ pos, int64_t n, int32_t* __restrict__ inv,
+                          unsigned* __restrict__ bad) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int p = pos[i];
+  if (p < 0 || p >= n || atomicCAS(&inv[p], -1, (int)i) != -1) atomicOr(bad, 1u);
+}
+
+__device__ __forceinline__ void sample_run(const int32_t* __restrict__ sample, int64_t n,
+                                           int64_t k, int64_t* a_out, int64_t* b_out) {
+  const int s = sample[k];
+  int64_t a = 0, b = k;
+  while (a < b) {
+    const int64_t m = (a + b) >> 1;
+    if (sample[m] < s) a = m + 1; else b = m;
+  }
+  int64_t lo2 = k + 1, b2 = n;
+  while (lo2 < b2) {
+    const int64_t m = (lo2 + b2) >> 1;
+    if (sample[m] <= s) lo2 = m + 1; else b2 = m;
+  }
+  *a_out = a;
+  *b_out = b2;
+}
+
+// per sample run [a, b) of indices: min and max position, kept at the run's first index
+__global__ void k_pos_runs(const int32_t* __restrict__ sample, const int32_t* __restrict__ pos,
+                           int64_t n, int32_t* __restrict__ rmin, int32_t* __restrict__ rmax) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  int64_t a, b;
+  sample_run(sample, n, k, &a, &b);
+  atomicMin(&rmin[a], pos[k]);
+  atomicMax(&rmax[a], pos[k]);
+}
+
+// the sample id of every position, and a flag if some sample's positions are not one range
+__global__ void k_pos_check(const int32_t* __restrict__ sample, const int32_t* __restrict__ pos,
+                            int64_t n, const int32_t* __restrict__ rmin,
+                            const int32_t* __restrict__ rmax, int32_t* __restrict__ psample,
+                            unsigned* __restrict__ bad) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  int64_t a, b;
+  sample_run(sample, n, k, &a, &b);
+  if (k == a && (int64_t)rmax[a] - rmin[a] + 1 != b - a) atomicOr(bad, 1u);
+  const int p = pos[k];
+  if (p >= 0 && p < n) psample[p] = sample[k];  // out-of-range positions were flagged
+}
+
+// Suffix minimum and maximum of inv[] over positions >= p within the sample of position p,
+// by one CTA walking the positions downward in chunks of 1024 (a segmented scan; a segment
+// is a sample's range of positions).
+__global__ void __launch_bounds__(1024) k_pos_suffix(const int32_t* __restrict__ inv,
+                                                     const int32_t* __restrict__ psample,
+                                                     int64_t n, int32_t* __restrict__ smin,
+                                                     int32_t* __restrict__ smax) {
+  __shared__ int vmin[1024], vmax[1024], head[1024];
+  __shared__ int cmin_c, cmax_c, cs_c;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    cmin_c = INT_MAX;
+    cmax_c = INT_MIN;
+    cs_c = INT_MIN;  // sample of the lowest position of the previous (higher) chunk
+  }
+  __syncthreads();
+  for (int64_t top = n; top > 0; top -= 1024) {
+    // element t of the chunk is position top - 1 - t (walking down)
+    const int64_t p = top - 1 - t;
+    const bool ok = p >= 0;
+    const int sp = ok ? psample[p] : INT_MIN;
+    int mn = ok ? inv[p] : INT_MAX, mx = ok ? inv[p] : INT_MIN;
+    // a segment starts at element t if position p + 1 belongs to another sample; element 0
+    // continues the previous chunk's segment when the sample matches
+    int hd;
+    if (t == 0) {
+      hd = sp != cs_c;
+      if (!hd) {
+        mn = min(mn, cmin_c);
+        mx = max(mx, cmax_c);
+      }
+    } else {
+      hd = ok && psample[p + 1] != sp;
+    }
+    vmin[t] = mn;
+    vmax[t] = mx;
+    head[t] = hd;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+      int a = vmin[t], b = vmax[t], h = head[t];
+      if (t >= off && !h) {
+        a = min(a, vmin[t - off]);
+        b = max(b, vmax[t - off]);
+        h = head[t - off];
+      }
+      __syncthreads();
+      vmin[t] = a;
+      vmax[t] = b;
+      head[t] = h;
+      __syncthreads();
+    }
+    if (ok) {
+      smin[p] = vmin[t];
+      smax[p] = vmax[t];
+    }
+    __syncthreads();
+    if (t == 1023 || p == 0) {
+      cmin_c = vmin[t];
+      cmax_c = vmax[t];
+      cs_c = sp;
+    }
+    __syncthreads();
+  }
+}
+
+// the hull of every key (see above); with invalid positions every key is marked inexact
+__global__ void k_iv_hull_pos(const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
+                              const int32_t* __restrict__ noise, const int32_t* __restrict__ pos,
+                              int64_t n, const int32_t* __restrict__ gfirst,
+                              const int32_t* __restrict__ glast, const int32_t* __restrict__ zfirst,
+                              const int32_t* __restrict__ zlast, const int32_t* __restrict__ smin,
+                              const int32_t* __restrict__ smax, const unsigned* __restrict__ bad,
+                              int32_t* __restrict__ lo_out, int32_t* __restrict__ hi_out,
+                              uint8_t* __restrict__ iv_orig) {
+  const int64_t k = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= n) return;
+  if (*bad) {
+    lo_out[k] = hi_out[k] = 0;
+    iv_orig[k >> 7] = 0;
+    return;
+  }
+  int64_t a, b;
+  sample_run(sample, n, k, &a, &b);
+  const int p = pos[k];
+  int64_t lo = smin[p], hi = (int64_t)smax[p] + 1;  // holds k itself
+  const int g = seg[k], z = noise[k];
+  if (g >= 0) {
+    if (g < n) {
+      lo = min(lo, max(a, (int64_t)gfirst[g]));
+      hi = max(hi, min(b, (int64_t)glast[g] + 1));
+    } else {
+      lo = a;  // no table for this id: the whole sample
+      hi = b;
+    }
+  }
+  if (z >= 0 && z < n) {
+    lo = max(lo, (int64_t)zfirst[z]);
+    hi = min(hi, (int64_t)zlast[z] + 1);
+  }
+  if (hi <= lo) lo = hi = 0;
+  lo_out[k] = (int32_t)lo;
+  hi_out[k] = (int32_t)hi;
+}
+
+// one warp per key: clears the key's block flag unless every query of its hull sees it
+__global__ void k_iv_verify(const int32_t* __restrict__ sample, const int32_t* __restrict__ seg,
+                            const int32_t* __restrict__ noise, const int32_t* __restrict__ pos,
+                            int64_t n, const int32_t* __restrict__ lo_in,
+                            const int32_t* __restrict__ hi_in, uint8_t* __restrict__ iv_orig) {
+  const int lane = threadIdx.x & 31;
+  const int64_t k = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (k >= n) return;
+  const int64_t lo = lo_in[k], hi = hi_in[k];
+  if (hi <= lo || !iv_orig[k >> 7]) return;  // nothing to check, or the block is off already
+  const int sk = sample[k], gk = seg[k], zk = noise[k], pk = pos[k];
+  for (int64_t q0 = lo; q0 < hi; q0 += 32) {
+    const int64_t q = q0 + lane;
+    bool ok = true;
+    if (q < hi)
+      ok = mask_legal(sample[q], seg[q], noise[q], pos[q], sk, gk, zk, pk, MARBLE_WINDOW_INF);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) iv_orig[k >> 7] = 0;
+      return;
+    }
+  }
 }
 
 // intervals and block flags into the new order
@@ -426,6 +615,30 @@ __global__ void k_step_write(const int64_t* __restrict__ row_ptr, const int32_t*
     __syncwarp();
     if (ok && (peers & lanemask_lt()) == 0) offs[j] += __popc(peers);
     __syncwarp();
+  }
+}
+
+// The row lists in ring order, for the fused forward: q block nq of shard r visits kv shard
+// (r - s) mod P at step s (MARBLE s03 ring pairing), so its entries are copied segment by
+// segment, kv shard r first, then r - 1, ..., wrapping round to r + 1.  Same CSR ranges as
+// step_ptr[nq * P] .. step_ptr[nq * P + P]; one warp per q block.
+__global__ void k_ring_write(const int64_t* __restrict__ step_ptr,
+                             const int32_t* __restrict__ step_col,
+                             const uint8_t* __restrict__ step_tag, int64_t nb, int P, int64_t bps,
+                             int32_t* __restrict__ ring_col, uint8_t* __restrict__ ring_tag) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nq = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
+  if (nq >= nb) return;
+  const int r = (int)(nq / bps);
+  int64_t o = step_ptr[nq * P];
+  for (int st = 0; st < P; ++st) {
+    const int j = (r - st + P) % P;
+    const int64_t a = step_ptr[nq * P + j], e = step_ptr[nq * P + j + 1];
+    for (int64_t i = a + lane; i < e; i += 32) {
+      ring_col[o + (i - a)] = step_col[i];
+      ring_tag[o + (i - a)] = step_tag[i];
+    }
+    o += e - a;
   }
 }
 
@@ -698,14 +911,32 @@ static marble_status_t dalloc(marble_plan_t* p, T** ptr, size_t count) {
 // row -- sorted by that count, longest first (counts above 1023 share a bucket).  Equal
 // counts come out in no fixed order: each unit's result does not depend on where or when
 // it runs.
+__device__ void work_order_segment(const int64_t* __restrict__ ptr, int P, int64_t bps, int s,
+                                   int c_lo, int c_hi, int32_t* __restrict__ out,
+                                   int32_t* __restrict__ nwork_out);
+
 __global__ void __launch_bounds__(1024) k_work_order(const int64_t* __restrict__ ptr, int P,
                                                      int64_t bps, int32_t* __restrict__ order,
                                                      int32_t* __restrict__ nwork) {
-  __shared__ int hist[1024];
-  __shared__ int scan[1024];
   const int seg = blockIdx.x;
   const int s = seg / (P + 1), k = seg % (P + 1);
   const int c_lo = k < P ? k : 0, c_hi = k < P ? k + 1 : P;
+  work_order_segment(ptr, P, bps, s, c_lo, c_hi, order + (int64_t)seg * bps, nwork + seg);
+}
+
+// the same order over every block of the pack, by the length of its whole row (every kv
+// shard): the work order of the fused forward (one CTA)
+__global__ void __launch_bounds__(1024) k_work_order_all(const int64_t* __restrict__ ptr, int P,
+                                                         int64_t nb, int32_t* __restrict__ order,
+                                                         int32_t* __restrict__ nwork) {
+  work_order_segment(ptr, P, nb, 0, 0, P, order, nwork);
+}
+
+__device__ void work_order_segment(const int64_t* __restrict__ ptr, int P, int64_t bps, int s,
+                                   int c_lo, int c_hi, int32_t* __restrict__ out,
+                                   int32_t* __restrict__ nwork_out) {
+  __shared__ int hist[1024];
+  __shared__ int scan[1024];
   hist[threadIdx.x] = 0;
   __syncthreads();
   for (int64_t i = threadIdx.x; i < bps; i += blockDim.x) {
@@ -729,9 +960,8 @@ __global__ void __launch_bounds__(1024) k_work_order(const int64_t* __restrict__
   const int start = scan[t] - hist[b];
   __syncthreads();
   hist[b] = start;  // reused as the bucket cursors
-  if (t == 1023) nwork[seg] = scan[1023];
+  if (t == 1023) *nwork_out = scan[1023];
   __syncthreads();
-  int32_t* out = order + (int64_t)seg * bps;
   for (int64_t i = threadIdx.x; i < bps; i += blockDim.x) {
     const int64_t r = (int64_t)s * bps + i;
     const int64_t c = ptr[r * P + c_hi] - ptr[r * P + c_lo];
@@ -1050,11 +1280,14 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->iv_block, nb));
   MARBLE_CK(cudaMemsetAsync(p->kiv, 0, 2 * n * sizeof(int32_t), s));
   MARBLE_CK(cudaMemsetAsync(p->iv_block, 0, nb, s));
-  // (the interval rule reads positions as indices: with a position track it stays off)
-  if (!d->no_key_intervals && !d->pos_id) {
+  // With a position track the causal part of an interval comes from the positions, on
+  // globally causal layers (with a window the causal queries need not form one range)
+  const bool use_pos = d->pos_id != nullptr;
+  if (!d->no_key_intervals && (!use_pos || W == MARBLE_WINDOW_INF)) {
     int32_t *tab = nullptr, *klo = nullptr;
     MARBLE_TRY(salloc(&tab, 6 * n));
     MARBLE_TRY(salloc(&klo, 2 * n + (nb + 3) / 4));
+
     int32_t *gfirst = tab, *glast = tab + n, *gcount = tab + 2 * n, *zfirst = tab + 3 * n,
             *zlast = tab + 4 * n, *zcount = tab + 5 * n;
     uint8_t* iv_orig = reinterpret_cast<uint8_t*>(klo + 2 * n);
@@ -1067,9 +1300,36 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
     MARBLE_CK(cudaMemsetAsync(iv_orig, 1, nb, s));
     k_iv_tables<<<grid_for(n, threads), threads, 0, s>>>(d->seg_id, d->noise_id, n, gfirst, glast,
                                                         gcount, zfirst, zlast, zcount);
-    k_iv_keys<<<grid_for(n, threads), threads, 0, s>>>(d->sample_id, d->seg_id, d->noise_id, n, W,
-                                                      gfirst, glast, gcount, zfirst, zlast, zcount,
-                                                      klo, klo + n, iv_orig);
+    if (!use_pos) {
+      k_iv_keys<<<grid_for(n, threads), threads, 0, s>>>(d->sample_id, d->seg_id, d->noise_id, n,
+                                                        W, gfirst, glast, gcount, zfirst, zlast,
+                                                        zcount, klo, klo + n, iv_orig);
+    } else {
+      int32_t *inv = nullptr, *rmin = nullptr, *rmax = nullptr, *psample = nullptr,
+              *smin = nullptr, *smax = nullptr, *badw = nullptr;
+      MARBLE_TRY(salloc(&inv, n));
+      MARBLE_TRY(salloc(&rmin, n));
+      MARBLE_TRY(salloc(&rmax, n));
+      MARBLE_TRY(salloc(&psample, n));
+      MARBLE_TRY(salloc(&smin, n));
+      MARBLE_TRY(salloc(&smax, n));
+      MARBLE_TRY(salloc(&badw, 1));
+      unsigned* bad = reinterpret_cast<unsigned*>(badw);
+      MARBLE_CK(cudaMemsetAsync(inv, 0xff, n * sizeof(int32_t), s));
+      MARBLE_CK(cudaMemsetAsync(rmin, 0x7f, n * sizeof(int32_t), s));
+      MARBLE_CK(cudaMemsetAsync(rmax, 0x80, n * sizeof(int32_t), s));
+      MARBLE_CK(cudaMemsetAsync(bad, 0, sizeof(unsigned), s));
+      k_pos_inv<<<grid_for(n, threads), threads, 0, s>>>(d->pos_id, n, inv, bad);
+      k_pos_runs<<<grid_for(n, threads), threads, 0, s>>>(d->sample_id, d->pos_id, n, rmin, rmax);
+      k_pos_check<<<grid_for(n, threads), threads, 0, s>>>(d->sample_id, d->pos_id, n, rmin, rmax,
+                                                          psample, bad);
+      k_pos_suffix<<<1, 1024, 0, s>>>(inv, psample, n, smin, smax);
+      k_iv_hull_pos<<<grid_for(n, threads), threads, 0, s>>>(
+          d->sample_id, d->seg_id, d->noise_id, d->pos_id, n, gfirst, glast, zfirst, zlast, smin,
+          smax, bad, klo, klo + n, iv_orig);
+      k_iv_verify<<<grid_for(n, kWarpsPerCta), 32 * kWarpsPerCta, 0, s>>>(
+          d->sample_id, d->seg_id, d->noise_id, d->pos_id, n, klo, klo + n, iv_orig);
+    }
     k_perm_iv<<<grid_for(n, threads), threads, 0, s>>>(p->perm, p->block_perm, klo, klo + n,
                                                       iv_orig, n, p->kiv, p->iv_block);
     MARBLE_CK(cudaGetLastError());
@@ -1116,6 +1376,17 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->fwd_order, p->fwd_nwork);
   k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->colT_ptr, P, bps, p->bwd_order, p->bwd_nwork);
   MARBLE_CK(cudaGetLastError());
+  // the fused forward: row lists in ring order and the order of all blocks
+  MARBLE_TRY(dalloc(p, &p->ring_col, nnz));
+  MARBLE_TRY(dalloc(p, &p->ring_tag, nnz));
+  MARBLE_TRY(dalloc(p, &p->fwd_order_all, nb));
+  MARBLE_TRY(dalloc(p, &p->fwd_nwork_all, 1));
+  k_ring_write<<<warp_ctas, 32 * kWarpsPerCta, 0, s>>>(p->step_ptr, p->step_col, p->step_tag, nb,
+                                                       P, bps, p->ring_col, p->ring_tag);
+  k_work_order_all<<<1, 1024, 0, s>>>(p->step_ptr, P, nb, p->fwd_order_all, p->fwd_nwork_all);
+  MARBLE_CK(cudaGetLastError());
+  MARBLE_CK(cudaMemcpyAsync(&p->h_fwd_nwork_all, p->fwd_nwork_all, sizeof(int32_t),
+                            cudaMemcpyDeviceToHost, s));
   p->h_fwd_nwork.resize((size_t)P * (P + 1));
   p->h_bwd_nwork.resize((size_t)P * (P + 1));
   MARBLE_CK(cudaMemcpyAsync(p->h_fwd_nwork.data(), p->fwd_nwork, P * (P + 1) * sizeof(int32_t),

@@ -129,12 +129,20 @@ typedef struct {
   int64_t range_cost;   /* CHUNK_SEARCH only: tau, the fixed cost of one contiguous range in
                            one ring step, in legal pairs */
   int32_t no_key_intervals; /* 1: partial tiles always evaluate the four-track predicate;
-                               0 (default): key-interval test where it is exact */
+                               0 (default): key-interval test where it is exact.  The test is
+                               lo_k <= i_q < hi_k with i_q the query's index in the order the
+                               tracks are given in (MARBLE s03 "Block classification") */
   const int32_t *pos_id;    /* NULL: a token's position is its index.  Otherwise device
                                int32[n_tokens] >= 0, the original position of every token of
                                a permuted pack (MARBLE s04 "Layout transforms": tokens carry
-                               their position), read during marble_plan only; the key-interval
-                               test is then off */
+                               their position), read during marble_plan only.  On globally
+                               causal layers (window MARBLE_WINDOW_INF) the key intervals are
+                               then computed from the positions: exact for a key when the
+                               queries of its sample at a position >= its own form one range
+                               of indices (the vision-group layout gives this), when the
+                               positions are a permutation of [0, n_tokens) and each sample
+                               holds one range of them.  With a window and a position track
+                               the interval test is off. */
 } marble_plan_desc_t;
 
 typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
@@ -231,7 +239,8 @@ typedef enum {
   MARBLE_FIELD_NEEDED = 13,      /* int32[needed_total] sorted unique new kv blocks that
                                     q shard r's rows need (local blocks included) */
   MARBLE_FIELD_KEY_INTERVALS = 14, /* int32[2][N] new order: lo, hi of every key's
-                                      visible-query interval (original indices) */
+                                      visible-query interval (indices in the order the
+                                      tracks were given in) */
   MARBLE_FIELD_INTERVAL_BLOCKS = 15 /* uint8[nb] new order: 1 if every key of the block
                                        has an exact interval */
 } marble_field_t;
@@ -370,6 +379,36 @@ marble_status_t marble_attn_bwd_steps(const marble_plan_t *plan, const marble_qk
                                       int32_t n_steps, const int32_t *q_shards,
                                       const int32_t *kv_shards, float *dq_acc, float *dk_acc,
                                       float *dv_acc, marble_stream_t stream);
+
+/*
+ * The whole forward ring in one launch (MARBLE s03 "Exact ring attention accumulation" and
+ * "PTRR"; RING "Execution Algorithm"): the same result as marble_attn_steps over every
+ * (q_shard r, kv_shard (r - s) mod P, FIRST at s = 0) for s = 0 .. P-1, up to fp32 rounding.
+ * Every (q block, q head) of every shard visits its tiles in that ring order, step after
+ * step, with its fp32 (O_acc, m, l) held on chip from its first step to its last; the state
+ * is written to `state` once, in the form marble_attn_step leaves it (so marble_attn_finalize
+ * follows as usual), rows with no tile included.  The state never passes through HBM between
+ * steps, and the pass is one persistent launch instead of P^2.  Only the carried fp32 state
+ * (no merge flags).  Errors: as marble_attn_steps.
+ */
+marble_status_t marble_attn_fwd_fused(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                      const marble_state_t *state, marble_stream_t stream);
+
+/*
+ * The whole backward ring (MARBLE s03: each kv shard's fp32 dK/dV accumulator travels with
+ * the shard around the ring while dQ is carried per q shard): the same result as
+ * marble_attn_bwd_steps over every (r, (r - s) mod P), up to fp32 rounding.  For every kv
+ * shard j, one dK/dV launch visits the q shards in ring order (j, j + 1, ..., j - 1) and keeps
+ * the dK/dV of each of its kv blocks in TMEM across all of them, adding it to dk_acc / dv_acc
+ * once; the dQ GEMM of each step (q shard, j) follows.  When the dS tiles of a kv shard's
+ * whole ring would exceed half of the 32 GB scratch cap, its ring is split into consecutive
+ * ranges of steps, each added once.  Accumulators must be zeroed by the caller; scratch and
+ * ordering as marble_attn_bwd_steps.  Errors: as marble_attn_bwd_steps.
+ */
+marble_status_t marble_attn_bwd_fused(const marble_plan_t *plan, const marble_qkv_t *qkv,
+                                      const void *d_o, const float *lse, const float *delta,
+                                      float *dq_acc, float *dk_acc, float *dv_acc,
+                                      marble_stream_t stream);
 
 /* Cast fp32 -> bf16 (round to nearest even) for n elements, e.g. gradient accumulators;
  * n must be a multiple of 4 and both pointers 16-byte aligned. */

@@ -25,7 +25,7 @@ def plan_for(cfg, tr):
     return make_plan(tr, cfg.window, cfg.shards, cfg.order, cfg.chunk_tokens, cfg.range_cost)
 
 
-def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried"):
+def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried", fused=False):
     """q/k/v in ORIGINAL order on the GPU.  Returns (O, LSE, state) with O [N, hq, d]
     and LSE [hq, N] in original order and the raw state in plan order."""
     n, hq, d = q.shape
@@ -34,7 +34,7 @@ def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried"):
     o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
     if schedule is None:
-        M.forward(pl, qp, kp, vp, st, o, lse, needed=needed, merge=merge)
+        M.forward(pl, qp, kp, vp, st, o, lse, needed=needed, merge=merge, fused=fused)
     else:
         for r, j, first in schedule:
             M.attn_step(pl, qp, kp, vp, r, j, st, first=first, merge=merge)
@@ -47,7 +47,7 @@ def run_forward(pl, q, k, v, needed=False, schedule=None, merge="carried"):
     return O, LSE, st
 
 
-def run_backward(pl, q, k, v, do, needed=False):
+def run_backward(pl, q, k, v, do, needed=False, fused=False):
     """Full forward + backward through the C ABI; gradients in original order (fp32)."""
     n, hq, d = q.shape
     hkv = k.shape[1]
@@ -55,12 +55,12 @@ def run_backward(pl, q, k, v, do, needed=False):
     st = M.State(n, hq, d)
     o = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((hq, n), dtype=torch.float32, device="cuda")
-    M.forward(pl, qp, kp, vp, st, o, lse, needed=needed)
+    M.forward(pl, qp, kp, vp, st, o, lse, needed=needed, fused=fused)
     delta = torch.empty((hq, n), dtype=torch.float32, device="cuda")
     dq = torch.zeros((n, hq, d), dtype=torch.float32, device="cuda")
     dk = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
     dv = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
-    M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=needed)
+    M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=needed, fused=fused)
     pl.check()
     return (pl.permute(dq, inverse=True), pl.permute(dk, inverse=True),
             pl.permute(dv, inverse=True))

@@ -86,3 +86,75 @@ def test_attention_with_intervals_equals_predicate(cid):
         out.append((O, L, dq, dk, dv))
     for a, b in zip(*out):
         assert torch.equal(a, b)
+
+
+def _layout_tracks(cid, n):
+    tr = wl.config_tracks(cid, n)
+    perm = oplan.vision_group_layout(tr)
+    return oplan.apply_layout(tr, perm)
+
+
+@pytest.mark.parametrize("cid,n,order", [(7, 16384, "ptrr_block"), (5, 16384, "contiguous"),
+                                         (2, 8192, "ptrr_block")])
+def test_intervals_on_layout_packs(cid, n, order):
+    """Packs in the vision-group layout, every token carrying its original position (MARBLE
+    s04 "Layout transforms"): each flagged block's keys have exactly the oracle's intervals
+    (indices of the given order) and are exact in the oracle; on the video-group pack, whose
+    groups the layout turns into single ranges, almost every block is flagged."""
+    from marble_testlib import device_tracks
+    import context_attention_metadata_gb300 as M
+    trp = _layout_tracks(cid, n)
+    s_, g_, z_ = device_tracks(trp)
+    pos = torch.as_tensor(np.asarray(trp["pos"], np.int32)).cuda()
+    pl = M.Plan(s_, g_, z_, INF, 4, order, pos=pos)
+    lo, hi, ex = oplan.key_intervals(trp, INF)
+    perm = pl.export("perm").cpu().numpy()
+    kiv = pl.export("key_intervals").cpu().numpy().reshape(2, -1)
+    ivb = pl.export("interval_blocks").cpu().numpy().astype(bool)
+    oivb = oplan.interval_blocks(ex)[pl.export("block_perm").cpu().numpy()]
+    assert not (ivb & ~oivb).any()                      # sound
+    flagged = np.repeat(ivb, 128)
+    assert (kiv[0][flagged] == lo[perm][flagged]).all()
+    assert (kiv[1][flagged] == hi[perm][flagged]).all()
+    print(f"flagged {ivb.mean():.3f} of blocks, oracle-exact {oivb.mean():.3f}")
+    if cid == 7:
+        assert ivb.sum() >= 0.9 * oivb.sum()
+    # with a window the position track switches the interval test off
+    plw = M.Plan(s_, g_, z_, 300, 4, order, pos=pos)
+    assert not plw.export("interval_blocks").any().item()
+
+
+def test_intervals_reject_positions_that_are_not_a_permutation():
+    """Duplicate positions (not a permutation of the indices): no block is flagged, the plan
+    still works through the four-track predicate."""
+    from marble_testlib import device_tracks
+    import context_attention_metadata_gb300 as M
+    trp = _layout_tracks(7, 4096)
+    pos = np.asarray(trp["pos"], np.int32).copy()
+    pos[10] = pos[11]
+    s_, g_, z_ = device_tracks(trp)
+    pl = M.Plan(s_, g_, z_, INF, 2, "contiguous", pos=torch.as_tensor(pos).cuda())
+    assert not pl.export("interval_blocks").any().item()
+
+
+@pytest.mark.parametrize("cid", [7, 5])
+def test_attention_on_layout_with_intervals_equals_predicate(cid):
+    """Attention on a layout pack with the interval test is bit-identical to attention with
+    the four-track predicate on every partial tile (forward and backward)."""
+    from marble_testlib import device_tracks, run_backward, run_forward
+    import context_attention_metadata_gb300 as M
+    n = 16384 if cid == 5 else 8192
+    cfg = wl.mini_config(cid, n, hq=2)
+    trp = _layout_tracks(cid, n)
+    q, k, v, do = wl.make_qkvdo(n, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=cid)
+    s_, g_, z_ = device_tracks(trp)
+    pos = torch.as_tensor(np.asarray(trp["pos"], np.int32)).cuda()
+    out = []
+    for iv in (True, False):
+        pl = M.Plan(s_, g_, z_, INF, cfg.shards, "ptrr_block", key_intervals=iv, pos=pos)
+        assert pl.export("interval_blocks").any().item() == iv
+        O, L, _ = run_forward(pl, q, k, v)
+        dq, dk, dv = run_backward(pl, q, k, v, do)
+        out.append((O, L, dq, dk, dv))
+    for a, b in zip(*out):
+        assert torch.equal(a, b)

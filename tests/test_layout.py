@@ -48,7 +48,7 @@ def test_plan_with_positions_matches_oracle(order):
     opl = oplan.make_plan(trp, INF, 4, order, range_cost=20000)
     _compare(pl, opl)
     st = pl.stats()
-    assert not pl.export("interval_blocks").any().item()   # off with a position track
+    assert pl.export("interval_blocks").any().item()   # exact intervals from the positions
     # fewer partial tiles than the same pack in its original order
     s0, g0, z0 = device_tracks(tr)
     st0 = M.Plan(s0, g0, z0, INF, 4, order, 0, range_cost=20000).stats()

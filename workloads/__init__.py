@@ -247,6 +247,9 @@ EXTRA: Dict[int, Config] = {
     7: Config(7, "video_group_512k", 524288, 8, 8, 128, 16, "ptrr_block",
               description="N=524288 video question-answer samples, frames of 64-256 tokens in "
                           "one image group with timestamps between; P=16 PTRR"),
+    8: Config(8, "full_span", 262144, 8, 8, 128, 16, "contiguous",
+              description="one bidirectional sample filling the pack: every tile full (the "
+                          "dense reference for per-tile throughput); P=16 contiguous"),
 }
 
 
@@ -272,6 +275,8 @@ def config_samples(cid: int, n: Optional[int] = None) -> List[List[Span]]:
         return video_generation_samples(rng, n, (min(n, 131072), min(n, 1048576)))
     if cid == 7:
         return video_group_samples(rng, n)
+    if cid == 8:
+        return [[Span("full", n)]]
     raise KeyError(cid)
 
 
