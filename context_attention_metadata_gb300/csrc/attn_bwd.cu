@@ -414,49 +414,91 @@ __global__ void __launch_bounds__(kGThreads, 1) k_bwd_dq(const __grid_constant__
 // ======================================================================================
 // dK / dV (KV-stationary)
 // ======================================================================================
-// Item g (counted over all units of the CTA) and half h (q columns [64h, 64h + 64)):
-//   S^T_h = K Q_h^T and dP^T_h = V dO_h^T (N = 64)  ->  elementwise: P^T_h and dS^T_h (bf16)
-//   over them  ->  dV += P^T_h dO_h and dK += dS^T_h Q_h (K = 64).
-// With dV and dK resident, TMEM holds one S^T / dP^T buffer: S^T_h(g+1) is issued once the
-// MMAs of half h of item g have completed, while the other half's elementwise runs.
+// TMEM: two 128-column score regions R0, R1 and the accumulators dV [256, 384), dK [384, 512).
+// Item g (counted over all units of the CTA) puts S^T(g) = K Q^T in R[g & 1] and
+// dP^T(g) = V dO^T in R[(g + 1) & 1], full width (N = 128 q columns).  The elementwise warps
+// load both into registers and say so (YFREE); the dP^T region is then free, and the MMA
+// thread issues S^T(g + 1) into it while the warps compute.  Each half of the warps writes
+// its bf16 P^T and dS^T into the 64 columns of S^T(g)'s region it has itself read (P^T of q
+// columns [64 h, 64 h + 64) in columns [64 h, 64 h + 32), dS^T in [64 h + 32, 64 h + 64)),
+// so no half waits for the other (PFULL); the MMA thread
+// issues dV += P^T dO and dK += dS^T Q (A from TMEM, K = 128 q), then dP^T(g + 1) into the
+// same region, which the tensor core writes only after the two accumulations have read it
+// (tcgen05.mma instructions of one thread execute in issue order).  Per item: 32 MMA
+// instructions, all N = 128.
+// Each half stages its bf16 dS^T (128 kv rows x 64 q columns) in a shared box of its own, from
+// which a lane of the store warp writes it to the step's scratch tile with a TMA store.
 // The epilogue stages dV, then dK, in the Q/dO stage of the unit's last item (free once the
 // unit's last MMAs are done; the epilogue hands it back to the producer) and adds them to
 // dv_acc / dk_acc with TMA reduce-adds.
 enum {
-  K_KVFULL, K_KVEMPTY, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SFULL0, K_SFULL1, K_PFULL0,
-  K_PFULL1, K_CONS0, K_CONS1, K_ACCFULL, K_ACCFREE, K_STG0, K_STG1, K_STGR0, K_STGR1, K_TRK00,
-  K_TRK01, K_TRK10, K_TRK11, K_DSSTG0, K_DSSTG1, K_DSFREE0, K_DSFREE1, K_UFULL0, K_UEMPTY0 = K_UFULL0 + kQueue,
+  K_KVFULL, K_KVEMPTY, K_QFULL0, K_QFULL1, K_QEMPTY0, K_QEMPTY1, K_SDP, K_YFREE, K_PFULL,
+  K_ACCFULL, K_ACCFREE, K_STG0, K_STG1, K_STGR0, K_STGR1, K_TRK00, K_TRK01, K_TRK10, K_TRK11,
+  K_DSSTG0, K_DSSTG1, K_DSFREE0, K_DSFREE1, K_UFULL0, K_UEMPTY0 = K_UFULL0 + kQueue,
   K_DRAIN = K_UEMPTY0 + kQueue, K_NUM
 };
 
 __host__ __device__ constexpr int dkdv_arrivals(int b) {
-  return (b == K_ACCFREE || (b >= K_UEMPTY0 && b < K_UEMPTY0 + kQueue))
+  return (b == K_ACCFREE || b == K_YFREE || b == K_PFULL ||
+          (b >= K_UEMPTY0 && b < K_UEMPTY0 + kQueue))
              ? 256
-             : ((b == K_PFULL0 || b == K_PFULL1 || b == K_STG0 || b == K_STG1 ||
-                 b == K_DSSTG0 || b == K_DSSTG1 || (b >= K_TRK00 && b <= K_TRK11))
+             : ((b == K_STG0 || b == K_STG1 || b == K_DSSTG0 || b == K_DSSTG1 ||
+                 (b >= K_TRK00 && b <= K_TRK11))
                     ? 128
                     : 1);
 }
 
+// The kernel's shared variables, kept at the end of the dynamic shared memory (the kernel
+// has no static shared memory, so that the 1024-byte-aligned layout fits without slack).
+struct DkdvShared {
+  uint64_t bar[K_NUM];
+  Queue queue;
+  uint32_t tmem_base;
+  int abort_flag;
+  int epi_count;
+  long long ds_mail[2];  // per half: scratch slot of the staged dS^T (-1: no more)
+};
+
+// shared memory of the dK/dV kernel: K, V, two Q/dO stages (6 tiles), one 16 KB dS^T box per
+// half, per-half staging of LSE and delta, then the shared variables
+template <int D>
+struct DkdvSmem {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kDS = 6 * kTile;
+  static constexpr int kStg = kDS + 2 * 16384;
+  static constexpr int kVars = kStg + 2 * 2 * 128 * 4;
+  static constexpr size_t bytes() { return (size_t)kVars + sizeof(DkdvShared); }
+};
+static_assert(DkdvSmem<128>::bytes() <= 232448, "shared memory budget");
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant__ BwdParams p) {
-  constexpr int kTile = 128 * D * 2;
+  using Lay = DkdvSmem<D>;
+  constexpr int kTile = Lay::kTile;
   constexpr int kAtoms = D / 64;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The layout needs a 1024-byte-aligned base (TMA boxes and MMA operands with 128-byte
+  // swizzle) and uses the dynamic shared memory to the last byte, with no room to realign:
+  // a base that is not aligned is reported through the error word, before any barrier, TMEM
+  // or TMA is touched.
+  if ((smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrBadPlanSize);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint8_t* sK = smem;
   uint8_t* sV = smem + kTile;
   uint8_t* sQ0 = smem + 2 * kTile;  // stage s: Q at 2+2s, dO at 3+2s
-  // one 16 KB box of bf16 dS^T (128 kv rows x 64 q columns) that the halves take turns in,
-  // then per half and buffer: lse2[64] | delta[64]
-  uint8_t* sDS = smem + 6 * kTile;
-  float* stg = reinterpret_cast<float*>(smem + 6 * kTile + 16384);
-  __shared__ __align__(8) uint64_t bar[K_NUM];
-  __shared__ Queue queue;
-  __shared__ uint32_t tmem_base;
-  __shared__ int abort_flag;
-  __shared__ int epi_count;
-  __shared__ long long ds_mail[2];  // per half: scratch slot of the staged dS^T (-1: no more)
+  uint8_t* sDS = smem + Lay::kDS;   // half h's dS^T box at sDS + 16384 h
+  // per half and buffer: lse2[64] | delta[64]
+  float* stg = reinterpret_cast<float*>(smem + Lay::kStg);
+  DkdvShared& sv = *reinterpret_cast<DkdvShared*>(smem + Lay::kVars);
+  uint64_t* bar = sv.bar;
+  Queue& queue = sv.queue;
+  uint32_t& tmem_base = sv.tmem_base;
+  int& abort_flag = sv.abort_flag;
+  int& epi_count = sv.epi_count;
+  long long* ds_mail = sv.ds_mail;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long n = p.n;
@@ -474,10 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // S^T fp32 [0,128) and dP^T fp32 [128,256), half h in columns [64h, 64h + 64) of each;
-  // P^T_h / dS^T_h bf16 packed into columns [64h, 64h + 32) of the same region
-  const uint32_t tS = tmem_base;
-  const uint32_t tP = tmem_base + 128;
+  // score regions R0, R1; item g: S^T in R[g & 1], dP^T in R[(g + 1) & 1]
+  const uint32_t tR0 = tmem_base;
   const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
   const uint32_t tdK = tmem_base + 384;   // dK fp32 [384, 384+D)
 
@@ -541,25 +581,34 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdS = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdS = idesc_bf16(128, 128, false, false);
       constexpr uint32_t kIdAcc = idesc_bf16(128, D, false, true);
       const uint32_t aK = smem_u32(sK), aV = smem_u32(sV);
-      // S^T_hh(gg) and dP^T_hh(gg): q rows [64 hh, 64 hh + 64) of stage gg & 1
-      auto issue_s = [&](int gg, int hh) {
-        const uint32_t aQ = smem_u32(sQ0 + (gg & 1) * 2 * kTile) + hh * 8192, aDO = aQ + kTile;
+      // S^T(gg) = K Q^T into R[gg & 1]; dP^T(gg) = V dO^T into R[(gg + 1) & 1]
+      auto issue_scores = [&](int gg, bool dp) {
+        const uint32_t aQ = smem_u32(sQ0 + (gg & 1) * 2 * kTile) + (dp ? kTile : 0);
+        const uint32_t aA = dp ? aV : aK;
+        const uint32_t d = tR0 + (uint32_t)(((gg + (dp ? 1 : 0)) & 1) * 128);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
           const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tS + hh * 64, sdesc_sw128(aK + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024),
-                 kIdS, k > 0);
+          mma_ss(d, sdesc_sw128(aA + off, 16, 1024), sdesc_sw128(aQ + off, 16, 1024), kIdS, k > 0);
         }
+      };
+      // dV += P^T dO, dK += dS^T Q over the 128 q columns, 16 per MMA: the P^T of q columns
+      // [16 kk, 16 kk + 16) sits in columns 64 (kk / 4) + 8 (kk % 4) of R[gg & 1], the dS^T 32
+      // columns further
+      auto issue_acc = [&](int gg, bool first) {
+        const uint32_t aQ = smem_u32(sQ0 + (gg & 1) * 2 * kTile), aDO = aQ + kTile;
+        const uint32_t r = tR0 + (uint32_t)((gg & 1) * 128);
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * 16384 + (k & 3) * 32;
-          mma_ss(tP + hh * 64, sdesc_sw128(aV + off, 16, 1024), sdesc_sw128(aDO + off, 16, 1024),
-                 kIdS, k > 0);
-        }
-        mma_commit(&bar[K_SFULL0 + hh]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tdV, r + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_sw128(aDO + kk * 2048, 16384, 1024),
+                 kIdAcc, (first && kk == 0) ? 0u : 1u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tdK, r + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                 sdesc_sw128(aQ + kk * 2048, 16384, 1024), kIdAcc, (first && kk == 0) ? 0u : 1u);
       };
       int uc = 0, j = 0, g = 0, items = 0;
       bool ok = mbar_wait(&bar[K_UFULL0], 0, w) && queue.head[0] >= 0;
@@ -569,8 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       }
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(0, 1);
+        issue_scores(0, false);
+        issue_scores(0, true);
+        mma_commit(&bar[K_SDP]);
         if (items == 1) mma_commit(&bar[K_KVEMPTY]);  // the unit's last read of K and V
       }
       while (ok) {
@@ -587,55 +637,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             itn = queue.T[slot] * p.group;
           }
         }
-        const uint32_t aQ = smem_u32(sQ0 + (g & 1) * 2 * kTile), aDO = aQ + kTile;
-        for (int hh = 0; hh < 2; ++hh) {
-          if (!mbar_wait(&bar[K_PFULL0 + hh], g & 1, w)) { ok = false; break; }
-          // the unit's first accumulation overwrites dV / dK: the previous unit's must be out
-          if (j == 0 && hh == 0 && uc >= 1 && !mbar_wait(&bar[K_ACCFREE], (uc - 1) & 1, w)) { ok = false; break; }
+        // S^T(g + 1) into dP^T(g)'s region once every elementwise thread holds its scores
+        if (nxt) {
+          if (!mbar_wait(&bar[K_YFREE], g & 1, w)) break;
+          if (newu && !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w)) break;
+          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) break;
           tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tdV, tS + hh * 64 + kk * 8,
-                   sdesc_sw128(aDO + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
-                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ts(tdK, tP + hh * 64 + kk * 8,
-                   sdesc_sw128(aQ + (4 * hh + kk) * 2048, 16384, 1024), kIdAcc,
-                   (j > 0 || hh > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&bar[K_CONS0 + hh]);
-          if (hh == 1) {
-            // the unit's last Q/dO stage is handed back by the epilogue, which stages in it
-            if (j == items - 1)
-              mma_commit(&bar[K_ACCFULL]);
-            else
-              mma_commit(&bar[K_QEMPTY0 + (g & 1)]);
-          }
-          if (nxt && !newu) {
-            // the next item's Q / dO are needed from here on only
-            if (hh == 0 && !mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) {
-              ok = false;
-              break;
-            }
-            // S^T_hh(g+1) / dP^T_hh(g+1) overwrite the P^T / dS^T these MMAs read: MMAs issued
-            // by one thread execute in issue order, so no wait is needed in between
-            tc_fence_after();
-            issue_s(g + 1, hh);
-            if (hh == 1 && j + 2 == items) mma_commit(&bar[K_KVEMPTY]);
-          }
+          issue_scores(g + 1, false);
         }
-        // the next unit's first score MMAs once this unit's accumulators are complete: they
-        // wait for the new unit's K / V and first Q / dO
-        if (ok && nxt && newu) {
-          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w) ||
-              !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w))
-            break;
-          tc_fence_after();
-          issue_s(g + 1, 0);
-          issue_s(g + 1, 1);
-          if (itn == 1) mma_commit(&bar[K_KVEMPTY]);
-        }
-        if (!ok || !nxt) break;
+        // dV / dK of item g once its P^T / dS^T are in TMEM; a unit's first accumulation
+        // overwrites dV / dK, so the previous unit's must have been read out
+        if (!mbar_wait(&bar[K_PFULL], g & 1, w)) break;
+        if (j == 0 && uc >= 1 && !mbar_wait(&bar[K_ACCFREE], (uc - 1) & 1, w)) break;
+        tc_fence_after();
+        issue_acc(g, j == 0);
+        // the unit's last Q/dO stage is handed back by the epilogue, which stages in it
+        if (j == items - 1)
+          mma_commit(&bar[K_ACCFULL]);
+        else
+          mma_commit(&bar[K_QEMPTY0 + (g & 1)]);
+        if (!nxt) break;
+        // dP^T(g + 1) into S^T(g)'s region, after the accumulations that read it
+        issue_scores(g + 1, true);
+        mma_commit(&bar[K_SDP]);
+        if ((newu && itn == 1) || (!newu && j + 2 == items)) mma_commit(&bar[K_KVEMPTY]);
         ++g;
         if (newu) {
           ++uc;
@@ -651,29 +676,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
     __syncwarp();
   } else if (warp == kWarpStore) {
     // ------------------------------------------------------------------ dS^T store
-    // one thread writes the staged dS^T boxes to the scratch in the order the halves use the
-    // box (half 0 of item g, half 1 of item g, half 0 of item g + 1, ...), so that no
-    // elementwise warp waits for a TMA to read shared memory
-    if (lane == 0) {
-      bool more = true;
-      for (int g = 0; more; ++g) {
-        for (int half = 0; half < 2 && more; ++half) {
-          if (!mbar_wait(&bar[K_DSSTG0 + half], (uint32_t)(g & 1), w)) {
-            more = false;
-            break;
-          }
-          const long long slot_ds = ds_mail[half];
-          if (slot_ds < 0) {
-            more = false;
-            break;
-          }
-          tma_store_3d(&p.ds_map, sDS, half * 64, (int)(slot_ds * 128), 0);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(&bar[K_DSFREE0 + half]);
-        }
+    // lane h writes half h's staged dS^T boxes to the scratch, one TMA store per item, and
+    // hands the box back once the TMA has read it, so that no elementwise warp waits for it
+    if (lane < 2) {
+      const int half = lane;
+      for (int g = 0;; ++g) {
+        if (!mbar_wait(&bar[K_DSSTG0 + half], (uint32_t)(g & 1), w)) break;
+        const long long slot_ds = ds_mail[half];
+        if (slot_ds < 0) break;
+        tma_store_3d(&p.ds_map, sDS + half * 16384, half * 64, (int)(slot_ds * 128), 0);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&bar[K_DSFREE0 + half]);
       }
-      // the global writes of every store this thread issued have completed
+      // the global writes of every store this lane issued have completed
       bulk_wait_all();
     }
     __syncwarp();
@@ -693,14 +709,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       if (!wait_all(&bar[K_UFULL0 + slot], (uc / kQueue) & 1, w)) break;
       const int kh = queue.head[slot];
       if (kh < 0) {
-        // no more work: half 0 posts the end of the dS^T stores once its last one is read
-        if (half == 0) {
-          if (row == 0) {
-            if (g >= 1) mbar_wait(&bar[K_DSFREE0], (uint32_t)((g - 1) & 1), w);
-            ds_mail[0] = -1;
-          }
-          mbar_arrive(&bar[K_DSSTG0]);
+        // no more work: each half posts the end of its dS^T stores once its last one is read
+        if (row == 0) {
+          if (g >= 1) mbar_wait(&bar[K_DSFREE0 + half], (uint32_t)((g - 1) & 1), w);
+          ds_mail[half] = -1;
         }
+        mbar_arrive(&bar[K_DSSTG0 + half]);
         break;
       }
       const int64_t nk = queue.blk[slot];
@@ -711,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       const int sk = p.tracks[tk], gk = p.tracks[n + tk], zk = p.tracks[2 * n + tk],
                 pk = p.tracks[3 * n + tk];
       // every key of the unit's block has an exact visible-query interval: partial tiles test
-      // lo_k <= pos_q < hi_k instead of the four-track predicate
+      // lo_k <= i_q < hi_k instead of the four-track predicate
       const bool ivt = p.iv_block[nk] != 0;
       const int klo = p.kiv[tk], khi = p.kiv[n + tk];
       for (int it = 0; it < items; ++it, ++g) {
@@ -769,16 +783,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
           }
         }
         if (!wait_all(&bar[K_TRK00 + half * 2 + b], (g >> 1) & 1, w)) { ok = false; break; }
-        if (!wait_all(&bar[K_SFULL0 + half], g & 1, w)) { ok = false; break; }
-        // S^T of the unit's first item is issued: every role has read the queue entry
+        if (!wait_all(&bar[K_SDP], g & 1, w)) { ok = false; break; }
+        // the scores of the unit's first item are issued: every role has read the queue entry
         if (it == 0) mbar_arrive(&bar[K_UEMPTY0 + slot]);
         tc_fence_after();
+        const uint32_t rS = tR0 + (uint32_t)((g & 1) * 128);        // S^T(g), then P^T / dS^T
+        const uint32_t rP = tR0 + (uint32_t)(((g + 1) & 1) * 128);  // dP^T(g)
         uint32_t vs[2][32], vp[2][32];
-        tmem_ld32(tS + lb + half * 64, vs[0]);
-        tmem_ld32(tS + lb + half * 64 + 32, vs[1]);
-        tmem_ld32(tP + lb + half * 64, vp[0]);
-        tmem_ld32(tP + lb + half * 64 + 32, vp[1]);
+        tmem_ld32(rS + lb + half * 64, vs[0]);
+        tmem_ld32(rS + lb + half * 64 + 32, vs[1]);
+        tmem_ld32(rP + lb + half * 64, vp[0]);
+        tmem_ld32(rP + lb + half * 64 + 32, vp[1]);
         tmem_ld_wait();
+        // this thread holds its scores: once every thread has, dP^T(g)'s region may take
+        // S^T(g + 1); the columns of S^T(g)'s region this half read take its P^T / dS^T
+        tc_fence_before();
+        mbar_arrive(&bar[K_YFREE]);
         uint32_t dsv[32];  // this row's bf16 dS^T pairs over the half's 64 q columns
         // P^T = exp2(s * scale * log2 e - lse2[q]), dS^T = P^T (dP^T - delta[q]); the per-query
         // LSE and delta are read four at a time; full tiles skip the mask
@@ -794,8 +814,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             float pv[4], dv4[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float e = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
-              pv[u] = (partial && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : e;
+              const float ex = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
+              pv[u] = (partial && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : ex;
               dv4[u] = pv[u] * (__uint_as_float(vp[cc][t + u]) - dq4[u]);
             }
             pk16[t >> 1] = pack_bf16(pv[0], pv[1]);
@@ -805,27 +825,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             dsv[cc * 16 + (t >> 1)] = dk16[t >> 1];
             dsv[cc * 16 + (t >> 1) + 1] = dk16[(t >> 1) + 1];
           }
-          tmem_st16(tS + lb + half * 64 + cc * 16, pk16);
-          tmem_st16(tP + lb + half * 64 + cc * 16, dk16);
+          // q column pair c of this half -> P^T column 64 half + c, dS^T column 64 half + 32 + c
+          tmem_st16(rS + lb + half * 64 + cc * 16, pk16);
+          tmem_st16(rS + lb + half * 64 + 32 + cc * 16, dk16);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bar[K_PFULL0 + half]);
-        // ---- this half's bf16 dS^T (its 64 q columns) to the step's scratch tile, for the
-        // dQ GEMM.  The halves take turns in one box (half 0 of item g, half 1 of item g, half
-        // 0 of item g+1, ...); DSFREE_h completes one phase per store of half h once its TMA
-        // has read the box.  Before its store of item g a half waits for its own store of item
-        // g-1 and for the other half's latest store (item g-1 for half 0, item g for half 1);
-        // each of these waits is on the current or the just-completed phase of its barrier.
+        mbar_arrive(&bar[K_PFULL]);
+        // ---- this half's bf16 dS^T (its 64 q columns) to the step's scratch tile, for the dQ
+        // GEMM, through the half's own box: the previous store of this half must have read it
         if (g >= 1 && !wait_all(&bar[K_DSFREE0 + half], (uint32_t)((g - 1) & 1), w)) { ok = false; break; }
-        if (half == 0 ? (g >= 1 && !wait_all(&bar[K_DSFREE1], (uint32_t)((g - 1) & 1), w))
-                      : !wait_all(&bar[K_DSFREE0], (uint32_t)(g & 1), w)) {
-          ok = false;
-          break;
-        }
         fence_proxy_async_smem();
         {
-          uint8_t* r8 = sDS + row * 128;
+          uint8_t* r8 = sDS + half * 16384 + row * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t* src = dsv + 4 * c;
@@ -911,8 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
 
 template <int D>
 size_t dkdv_smem() {
-  // K, V, two Q/dO stages (6 tiles) + the dS^T box + per-half staging of LSE and delta
-  return 6 * (128 * D * 2) + 16384 + 2 * 2 * 128 * 4 + 1024;
+  return DkdvSmem<D>::bytes();
 }
 
 // everything of a backward call but the step, its work list and the scratch: encoded once

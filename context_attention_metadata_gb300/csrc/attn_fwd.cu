@@ -57,7 +57,6 @@ enum {
   B_SFULL0, B_SFULL1,                // S buffer (tile & 1) computed
   B_PFULL0, B_PFULL1,                // P written over S buffer (256 softmax arrivals)
   B_PVDONE,                          // one phase per tile: its PV has completed
-  B_PCONS0, B_PCONS1,                // S buffer (tile & 1): its P consumed by the PV
   B_OFULL0, B_OFULL1,                // O buffer (unit & 1): the unit's last PV completed
   B_OFREE0, B_OFREE1,                // O buffer read out by the epilogue (128 arrivals)
   B_MX0, B_MX1,                      // per-row max exchanged between the two halves
@@ -335,7 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
               mma_ts(tO + ob * 128, tS + b * 128 + (k >> 2) * 64 + (k & 3) * 8,
                      sdesc_sw128(aV + k * 2048, 16384, 1024), kIdO, (cp.j > 0 || k > 0) ? 1u : 0u);
             mma_commit(&bar[B_PVDONE]);
-            mma_commit(&bar[B_PCONS0 + b]);
             mma_commit(&bar[B_VEMPTY0 + s]);
             if (cp.j == cp.T - 1) mma_commit(&bar[B_OFULL0 + ob]);
             advance(cp);
@@ -345,9 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         if (cs.state == 1 && cs.g < cp.g + 2) {
           const int g = cs.g;
           const uint32_t b = (uint32_t)(g & 1), s = ring_slot(g), qb = (uint32_t)(cs.uc & 1);
+          // S(g) overwrites the P of tile g - 2, which PV(g - 2) reads: the PV is issued already
+          // (S runs at most two tiles ahead of the next PV), and tcgen05.mma instructions of one
+          // thread execute in issue order, so no wait for its completion is needed
           const bool ready = (cs.j != 0 || mbar_test(&bar[B_QFULL0 + qb], (cs.uc >> 1) & 1)) &&
-                             mbar_test(&bar[B_KFULL0 + s], ring_parity(g)) &&
-                             (g < 2 || mbar_test(&bar[B_PCONS0 + b], ((g - 2) >> 1) & 1));
+                             mbar_test(&bar[B_KFULL0 + s], ring_parity(g));
           if (ready) {
             tc_fence_after();
             const uint32_t aQ = aQ0 + qb * kTile, aK = aK0 + s * kTile;
