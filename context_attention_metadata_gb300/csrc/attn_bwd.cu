@@ -799,7 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         // S^T(g + 1); the columns of S^T(g)'s region this half read take its P^T / dS^T
         tc_fence_before();
         mbar_arrive(&bar[K_YFREE]);
-        uint32_t dsv[32];  // this row's bf16 dS^T pairs over the half's 64 q columns
+        // the half's dS^T box takes this item's tile once its previous store has read it (long
+        // done, normally): each 32-column chunk goes to the box as soon as it is packed
+        if (g >= 1 && !wait_all(&bar[K_DSFREE0 + half], (uint32_t)((g - 1) & 1), w)) { ok = false; break; }
+        fence_proxy_async_smem();
+        uint8_t* box_row = sDS + half * 16384 + row * 128;
         // P^T = exp2(s * scale * log2 e - lse2[q]), dS^T = P^T (dP^T - delta[q]); the per-query
         // LSE and delta are read four at a time; full tiles skip the mask
 #pragma unroll
@@ -822,9 +826,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             pk16[(t >> 1) + 1] = pack_bf16(pv[2], pv[3]);
             dk16[t >> 1] = pack_bf16(dv4[0], dv4[1]);
             dk16[(t >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
-            dsv[cc * 16 + (t >> 1)] = dk16[t >> 1];
-            dsv[cc * 16 + (t >> 1) + 1] = dk16[(t >> 1) + 1];
           }
+          // q columns [32 cc, 32 cc + 32) of this half: 16-byte chunks 4 cc .. 4 cc + 3 of the
+          // row, 128-byte swizzled as the TMA store reads them
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(box_row + (((4 * cc + c) ^ (row & 7)) << 4)) =
+                make_uint4(dk16[4 * c], dk16[4 * c + 1], dk16[4 * c + 2], dk16[4 * c + 3]);
           // q column pair c of this half -> P^T column 64 half + c, dS^T column 64 half + 32 + c
           tmem_st16(rS + lb + half * 64 + cc * 16, pk16);
           tmem_st16(rS + lb + half * 64 + 32 + cc * 16, dk16);
@@ -832,19 +840,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar[K_PFULL]);
-        // ---- this half's bf16 dS^T (its 64 q columns) to the step's scratch tile, for the dQ
-        // GEMM, through the half's own box: the previous store of this half must have read it
-        if (g >= 1 && !wait_all(&bar[K_DSFREE0 + half], (uint32_t)((g - 1) & 1), w)) { ok = false; break; }
-        fence_proxy_async_smem();
-        {
-          uint8_t* r8 = sDS + half * 16384 + row * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t* src = dsv + 4 * c;
-            *reinterpret_cast<uint4*>(r8 + ((c ^ (row & 7)) << 4)) =
-                make_uint4(src[0], src[1], src[2], src[3]);
-          }
-        }
+        // ---- this half's bf16 dS^T (its 64 q columns, staged in its box above) to the step's
+        // scratch tile for the dQ GEMM
         if (row == 0) {
           // the tile's scratch slot: the step's tiles in row-list order, q heads innermost
           const int64_t nq = p.colT_row[e];
