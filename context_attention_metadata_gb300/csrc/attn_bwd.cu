@@ -745,21 +745,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         mbar_arrive(&bar[K_TRK00 + half * 2 + b]);
         uint32_t lm[2] = {~0u, ~0u};
         if (partial && ivt) {
-          // lo_k <= i_q < hi_k, i_q the query's index in the given token order
-          const int32_t* qpos = p.qidx + (int64_t)p.colT_row[e] * 128 + half * 64;
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t bits = 0;
-#pragma unroll
-            for (int t2 = 0; t2 < 32; t2 += 4) {
-              const int4 p4 = __ldg(reinterpret_cast<const int4*>(qpos + cc * 32 + t2));
-              bits |= ((p4.x >= klo) & (p4.x < khi) ? 1u : 0u) << t2;
-              bits |= ((p4.y >= klo) & (p4.y < khi) ? 1u : 0u) << (t2 + 1);
-              bits |= ((p4.z >= klo) & (p4.z < khi) ? 1u : 0u) << (t2 + 2);
-              bits |= ((p4.w >= klo) & (p4.w < khi) ? 1u : 0u) << (t2 + 3);
-            }
-            lm[cc] = bits;
-          }
+          // lo_k <= i_q < hi_k, i_q the query's index in the given token order.  The plan moves
+          // whole 128-token blocks, so the half's 64 queries have the consecutive indices
+          // i0, i0 + 1, ..., and the legal ones are the columns [lo_k - i0, hi_k - i0) cut to
+          // [0, 64): one range of bits
+          const int64_t i0 = (int64_t)p.qidx[(int64_t)p.colT_row[e] * 128] + half * 64;
+          const int64_t a = min(max((int64_t)klo - i0, (int64_t)0), (int64_t)64);
+          const int64_t c = min(max((int64_t)khi - i0, (int64_t)0), (int64_t)64);
+          const uint64_t below_c = c >= 64 ? ~0ull : ((1ull << c) - 1ull);
+          const uint64_t below_a = a >= 64 ? ~0ull : ((1ull << a) - 1ull);
+          const uint64_t bits = a < c ? (below_c & ~below_a) : 0ull;
+          lm[0] = (uint32_t)bits;
+          lm[1] = (uint32_t)(bits >> 32);
         } else if (partial) {
           // the half's 64 queries' tracks, read straight from global memory (the same
           // addresses for every lane: broadcast loads), four queries per load
