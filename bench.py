@@ -681,9 +681,11 @@ def run_profile_pass(args):
     dq = torch.zeros((n, hq, d), dtype=torch.float32, device="cuda")
     dk = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
     dv = torch.zeros((n, hkv, d), dtype=torch.float32, device="cuda")
+    fused = args.profile_fused and not cfg.needed
     for _ in range(args.profile_pass):
-        M.forward(pl, qp, kp, vp, st, o, lse, needed=cfg.needed)
-        M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=cfg.needed)
+        M.forward(pl, qp, kp, vp, st, o, lse, needed=cfg.needed, fused=fused)
+        M.backward(pl, qp, kp, vp, o, dop, lse, delta, dq, dk, dv, needed=cfg.needed,
+                   fused=fused)
     pl.check()
     torch.cuda.synchronize()
     print(f"profile pass ok: {cfg.name} n={n} passes={args.profile_pass}", flush=True)
@@ -781,6 +783,8 @@ def main():
                     help="seconds of oracle time per reference-arm step")
     ap.add_argument("--profile-pass", type=int, default=0,
                     help="run this many untimed fwd+bwd passes for a profiler and exit")
+    ap.add_argument("--profile-fused", action="store_true",
+                    help="with --profile-pass: the fused ring entry points")
     ap.add_argument("--tokens", type=int, default=0,
                     help="a smaller pack of the same recipe (side measurements, profiling)")
     ap.add_argument("--order", default="",

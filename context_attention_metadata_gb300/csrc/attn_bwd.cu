@@ -18,18 +18,19 @@
 //   k_bwd_dq    Q-stationary units (q block, q head): dQ += dS K, a GEMM over the unit's
 //               dS^T tiles (read MN-major) and K tiles, after the step's dK/dV kernel.
 // Both are persistent (one CTA per SM) and take their units from a ticket counter in the
-// plan's order (longest list first), through a 4-entry queue in shared memory:
-//   warp 10     scheduler: ticket -> unit -> queue
+// plan's order (longest list first), through a 4-entry queue in shared memory.  Warps of the
+// dK/dV kernel (the dQ GEMM's are listed with it below):
 //   warp 0      TMA producer: the unit's stationary tiles into one slot (refilled once the
 //               unit's last score MMAs have read it), the streamed tiles through two stages
 //   warp 1      TMEM allocation and MMA issue
-//   warps 2..9  elementwise, four warps (one thread per TMEM lane) for each 64-column half
-//               of a tile; the halves run as two chains offset in time, so that the tensor
-//               core works on one half while the other half's elementwise stage runs.  At a
-//               unit's end the same warps read the fp32 accumulator out of TMEM (releasing it
-//               for the next unit, whose first MMAs are already under way), stage it in a
-//               shared-memory slot the unit no longer needs and add it to the global
-//               accumulator with TMA fp32 reduce-adds (no load of the accumulator).
+//   warp 2      scheduler: ticket -> unit -> queue
+//   warp 3      dS^T store: the staged dS^T boxes to the scratch, by TMA
+//   warps 4..11 elementwise, four warps (one thread per TMEM lane) for each 64-column half
+//               of a tile, with most of the block's registers (warpgroup 0 gives its share
+//               up).  At a unit's end the same warps read the fp32 accumulators out of TMEM
+//               (releasing them for the next unit, whose first MMAs are already under way),
+//               stage them in a shared-memory slot the unit no longer needs and add them to
+//               the global accumulators with TMA fp32 reduce-adds (no load).
 // Masks only on partial tiles.
 #include <math.h>
 
@@ -43,9 +44,15 @@
 namespace marble {
 namespace {
 
-constexpr int kThreads = 384;  // producer, MMA, 8 elementwise warps, scheduler, dS store
-constexpr int kWarpSched = 10;
-constexpr int kWarpStore = 11;
+constexpr int kThreads = 384;  // producer, MMA, scheduler, dS store, 8 elementwise warps
+constexpr int kWarpSched = 2;
+constexpr int kWarpStore = 3;
+// registers per thread: the launch gives every thread 168 (384 x 168 of the SM's 65,536);
+// warpgroup 0 (producer, MMA, scheduler, store) hands 112 of each of its threads' to the two
+// elementwise warpgroups: 128 x 56 + 256 x 224 = 384 x 168
+constexpr int kRegsCtl = 56;
+constexpr int kRegsElem = 224;
+static_assert(128 * kRegsCtl + 256 * kRegsElem <= kThreads * 168, "register split");
 constexpr int kQueue = 4;
 constexpr int kDsBufs = 4;        // steps whose dS^T tiles the scratch holds at once (at most)
 constexpr size_t kDsScratchCap = size_t(32) << 30;  // fewer buffers (down to 2) above this
@@ -74,6 +81,10 @@ struct BwdParams {
   // across them; the dS^T tile of q block nq lands at ds_base[nq / bps] + (its index in the
   // step's numbering) * hq + head
   int ring_s0, ring_len;
+  // whole rows (whole != 0): the dK/dV kernel stores the dS^T tile of row-list entry e (the
+  // plan's row lists, every kv shard) of a q block of shard r at slot ds_base[r] + e * hq +
+  // head, and the dQ kernel runs one unit per (q block, q head) over the block's whole row
+  int whole;
   long long ds_base[kMaxShards];
   unsigned* sched;           // ticket counter pair of the launch
   const int32_t* tracks;     // [4][n] plan order
@@ -114,9 +125,17 @@ __device__ __forceinline__ int64_t list_entry(int64_t e0, int64_t e1, int La, in
 // ticket -> unit of the dQ kernel: q head h (innermost), q block of the order
 __device__ __forceinline__ void dq_unit(const BwdParams& p, unsigned t, int* h, int* blk,
                                         int64_t* e0, int* T) {
+  int64_t nq, a, b;
+  if (p.whole) {
+    *h = (int)(t % (unsigned)p.hq);
+    nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
+    *blk = (int)nq;
+    *e0 = p.step_ptr[nq * p.P];
+    *T = (int)(p.step_ptr[nq * p.P + p.P] - *e0);
+    return;
+  }
   *h = (int)(t % (unsigned)p.hq);
-  const int64_t nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
-  int64_t a, b;
+  nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
   if (p.kv_shard >= 0) {
     a = p.step_ptr[nq * p.P + p.kv_shard];
     b = p.step_ptr[nq * p.P + p.kv_shard + 1];
@@ -292,13 +311,15 @@ __global__ void __launch_bounds__(kGThreads, 1) k_bwd_dq(const __grid_constant__
       const int T = queue.T[slot];
       const int64_t e0 = queue.e0[slot];
       const int kvh = h / p.group;
-      const int64_t base = p.step_off[nq * (p.P + 1) + opt];
+      // the unit's first dS^T slot: by row-list entry (whole backward) or in the step's order
+      const int64_t sl0 = p.whole ? p.ds_base[nq / p.bps] + e0 * p.hq + h
+                                  : p.ds_slot0 + p.step_off[nq * (p.P + 1) + opt] * p.hq + h;
       for (int j = 0; j < T; ++j, ++g) {
         const int s = g % 3;
         if (g >= 3 && !wait_all(&bar[G_EMPTY0 + s], ((g / 3) - 1) & 1, w)) { ok = false; break; }
         if (lane == 0) {
           const int nk = p.step_col[e0 + j];
-          const int64_t sl = p.ds_slot0 + (base + j) * p.hq + h;
+          const int64_t sl = sl0 + (int64_t)j * p.hq;
           uint8_t* st = smem + s * L::kStage;
           mbar_arrive_expect_tx(&bar[G_FULL0 + s], L::kDs + kTile);
           tma_load_3d(st, &p.ds_map, &bar[G_FULL0 + s], 0, (int)(sl * 128), 0);
@@ -521,6 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
   const uint32_t tdV = tmem_base + 256;   // dV fp32 [256, 256+D)
   const uint32_t tdK = tmem_base + 384;   // dK fp32 [384, 384+D)
 
+  if (warp < 4) {
+  // warpgroup 0: scheduler, producer, MMA issuer, dS^T store, with few registers
+  regs_shrink<kRegsCtl>();
   if (warp == kWarpSched) {
     if (lane == 0) schedule<false>(p, queue, &bar[K_UFULL0], &bar[K_UEMPTY0], w);
     __syncwarp();
@@ -693,11 +717,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
       bulk_wait_all();
     }
     __syncwarp();
+  }
   } else {
     // ------------------------------------------------------------------ elementwise
-    // four warps per half: `half` owns q columns [64 half, 64 half + 64), one kv row a thread
+    // warpgroups 1 and 2, with the registers warpgroup 0 gave up; four warps per half:
+    // `half` owns q columns [64 half, 64 half + 64), one kv row a thread
+    regs_grow<kRegsElem>();
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int half = (warp - 4) >> 2;
     const int row = quarter * 32 + lane;  // kv row of the tile
     const int hr = row & 63;
     const uint32_t lb = (uint32_t)(quarter * 32) << 16;
@@ -733,6 +760,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         const int64_t e = list_entry(c0, c1, La, it % L);
         const int64_t qrow = (int64_t)p.colT_row[e] * 128 + half * 64 + hr;
         const bool partial = p.colT_tag[e] == MARBLE_TILE_PARTIAL;
+        // the tile's dS^T scratch slot (row 0 of the half), looked up now so that the loads
+        // are done by the time the box is full: its row-list entry (whole rows), or the step's
+        // tiles in row-list order; q heads innermost
+        long long slot_ds = 0;
+        if (row == 0) {
+          const int64_t nq = p.colT_row[e];
+          if (p.whole) {
+            slot_ds = p.ds_base[nq / p.bps] +
+                      (p.step_ptr[nq * p.P + nk / p.bps] + p.colT_j[e]) * p.hq + h;
+          } else {
+            const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
+            int64_t jj = p.colT_j[e];
+            if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
+            const long long base = p.ring_len > 0 ? p.ds_base[nq / p.bps] : p.ds_slot0;
+            slot_ds = base + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
+          }
+        }
         // stage this half's per-query LSE (base 2) and delta (threads of rows [0, 64))
         const int b = g & 1;
         float* lse2s = stg + (half * 2 + b) * 128;
@@ -779,6 +823,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             lm[cc] = bits;
           }
         }
+        // a partial tile on which every row of this warp keeps all 64 of its columns needs no
+        // mask
+        const bool masked = partial && __any_sync(0xffffffffu, (lm[0] & lm[1]) != ~0u);
         if (!wait_all(&bar[K_TRK00 + half * 2 + b], (g >> 1) & 1, w)) { ok = false; break; }
         if (!wait_all(&bar[K_SDP], g & 1, w)) { ok = false; break; }
         // the scores of the unit's first item are issued: every role has read the queue entry
@@ -816,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
               const float ex = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
-              pv[u] = (partial && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : ex;
+              pv[u] = (masked && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : ex;
               dv4[u] = pv[u] * (__uint_as_float(vp[cc][t + u]) - dq4[u]);
             }
             pk16[t >> 1] = pack_bf16(pv[0], pv[1]);
@@ -837,17 +884,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar[K_PFULL]);
-        // ---- this half's bf16 dS^T (its 64 q columns, staged in its box above) to the step's
-        // scratch tile for the dQ GEMM
-        if (row == 0) {
-          // the tile's scratch slot: the step's tiles in row-list order, q heads innermost
-          const int64_t nq = p.colT_row[e];
-          const int opt = p.kv_shard >= 0 ? p.kv_shard : p.P;
-          int64_t jj = p.colT_j[e];
-          if (opt == p.P) jj += p.step_ptr[nq * p.P + nk / p.bps] - p.step_ptr[nq * p.P];
-          const long long base = p.ring_len > 0 ? p.ds_base[nq / p.bps] : p.ds_slot0;
-          ds_mail[half] = base + ((int64_t)p.step_off[nq * (p.P + 1) + opt] + jj) * p.hq + h;
-        }
+        // ---- this half's bf16 dS^T (its 64 q columns, staged in its box above) to the tile's
+        // scratch slot for the dQ GEMM
+        if (row == 0) ds_mail[half] = slot_ds;
         fence_proxy_async_smem();
         mbar_arrive(&bar[K_DSSTG0 + half]);
       }
@@ -979,6 +1018,17 @@ marble_status_t prepare_bwd(const marble_plan_t* pl, const marble_qkv_t* qkv, co
                                (int)dkdv_smem<D>());
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bwd)");
   }
+  {
+    // the dK/dV kernel's warpgroups trade registers among themselves: the block must be
+    // launched with at least the registers the two budgets add up to, or the growing
+    // warpgroups would wait for registers that never come (checked on every call)
+    cudaFuncAttributes fa;
+    const cudaError_t e = cudaFuncGetAttributes(&fa, k_bwd_dkdv<D>);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes(k_bwd_dkdv)");
+    if ((long long)fa.numRegs * kThreads < 128LL * kRegsCtl + 256LL * kRegsElem)
+      return fail(MARBLE_ERR_UNSUPPORTED, "dK/dV kernel built with " + std::to_string(fa.numRegs) +
+                                              " registers per thread, fewer than its split needs");
+  }
   return MARBLE_OK;
 }
 
@@ -1039,6 +1089,179 @@ void launch_dq(const marble_plan_t* pl, const BwdParams& prm, int r, int j, long
   }
 }
 
+// The cap on the dS^T scratch: kDsScratchCap, or less when MARBLE_DS_SCRATCH_CAP_MB says so
+// (tests use it to reach the paths that larger packs take).
+size_t scratch_cap() {
+  size_t cap = kDsScratchCap;
+  if (const char* env = std::getenv("MARBLE_DS_SCRATCH_CAP_MB")) {
+    const unsigned long long mb = std::strtoull(env, nullptr, 10);
+    if (mb > 0 && (mb << 20) < cap) cap = (size_t)(mb << 20);
+  }
+  return cap;
+}
+
+// the whole backward's dQ GEMM over whole rows: every (q block, q head) of the pack with tiles
+// (q_shard < 0), or those of one q shard; at most `ctas` CTAs
+template <int D>
+void launch_dq_whole(const marble_plan_t* pl, const BwdParams& prm, int q_shard, int hq,
+                     int ctas, cudaStream_t s) {
+  BwdParams pq = prm;
+  pq.whole = 1;
+  pq.kv_shard = -1;
+  pq.ring_len = 0;
+  if (q_shard < 0) {
+    pq.q_shard = 0;
+    pq.order = pl->fwd_order_all;
+    pq.nwork = pl->h_fwd_nwork_all * hq;
+  } else {
+    const int64_t seg = (int64_t)q_shard * (pl->P + 1) + pl->P;
+    pq.q_shard = q_shard;
+    pq.order = pl->fwd_order + seg * pl->bps;
+    pq.nwork = pl->h_fwd_nwork[seg] * hq;
+  }
+  if (pq.nwork > 0) {
+    pq.sched = sched_slot(pl);
+    const int span = timing_begin(s);
+    k_bwd_dq<D><<<(unsigned)(pq.nwork < ctas ? pq.nwork : ctas), kGThreads, DqSmem<D>::bytes(), s>>>(pq);
+    timing_end(span, s, kTimeDq, 1);
+  }
+}
+
+// The whole backward keeps every tile's dS^T (nnz x hq slots of 32 KB) and runs the dQ GEMM
+// once, after every dK/dV launch: dQ of a q block then accumulates its whole row in TMEM and
+// is added to dq_acc once, instead of once per ring step.  It is taken when the scratch fits
+// the cap.
+size_t whole_slots(const marble_plan_t* pl, int hq) {
+  const size_t slots = (size_t)pl->nnz * (size_t)hq;
+  return slots * 32768 <= scratch_cap() ? slots : 0;
+}
+
+// Whole-row dQ for a full ring list: the dK/dV launch of every step (kv shard j on side
+// stream j mod kDkdvStreams, so that the launches adding into one kv shard's dK/dV rows stay in
+// order) and dQ GEMMs over whole rows (stream s, after the side streams' launches so far).  The
+// dS^T tiles of q shard r sit at ds_base[r] + e * hq + head (e the row-list entry):
+//   nbuf >= P  every q shard has its own place in one array (ds_base = 0), and one dQ GEMM
+//              over every q block follows all dK/dV launches;
+//   otherwise  the list holds each q shard's steps in one run, the k-th q shard of the list
+//              takes buffer k mod nbuf of buf_slots slots, its dQ GEMM follows its last step
+//              (overlapping the dK/dV launches of the steps after it), and its first dK/dV
+//              launch waits until the dQ GEMM of the q shard nbuf runs earlier has read that
+//              buffer.
+template <int D>
+marble_status_t launch_whole(const marble_plan_t* pl, const marble_qkv_t* qkv, BwdParams prm,
+                             int n_steps, const int* q_shards, const int* kv_shards, int nbuf,
+                             int64_t buf_slots, cudaStream_t s) {
+  const int smem_k = (int)dkdv_smem<D>();
+  const int sms = sm_count();
+  const int P = pl->P;
+  const int64_t hq = qkv->hq;
+  const bool all = nbuf >= P;
+  marble_status_t rc = ds_scratch(pl, all ? whole_slots(pl, (int)hq) : (size_t)(nbuf * buf_slots),
+                                  s, &prm);
+  if (rc != MARBLE_OK) return rc;
+  prm.whole = 1;
+  prm.ds_slot0 = 0;
+  // first row-list entry of every q shard
+  std::vector<int64_t> first(P + 1, 0);
+  for (int r = 0; r < P; ++r) first[r + 1] = first[r] + pl->h_step_tiles[(size_t)r * (P + 1) + P];
+  cudaStream_t sk[kDkdvStreams];
+  int nsk = 0;
+  for (int k = 0; k < kDkdvStreams; ++k) {
+    cudaStream_t x = side_stream(k);
+    if (!x) break;
+    cudaError_t e = stream_fork(s, x);
+    if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+    sk[nsk++] = x;
+  }
+  if (nsk == 0) sk[nsk++] = s;
+  const bool overlap = sk[0] != s;
+  std::vector<int> issued(P, 0);
+  std::vector<cudaEvent_t> ev_buf(all ? 0 : nbuf, nullptr);
+  int shards_begun = 0;
+  cudaError_t err = cudaSuccess;
+  for (int i = 0; i < n_steps && err == cudaSuccess; ++i) {
+    const int r = q_shards[i];
+    if (issued[r] == 0 && !all) {
+      // the q shard's buffer: free once the dQ GEMM that last read it is done
+      const int k = shards_begun % nbuf;
+      prm.ds_base[r] = (long long)k * buf_slots - first[r] * hq;
+      if (ev_buf[k] && overlap)
+        for (int x = 0; x < nsk && err == cudaSuccess; ++x)
+          err = cudaStreamWaitEvent(sk[x], ev_buf[k], 0);
+      ++shards_begun;
+    }
+    BwdParams pk = prm;
+    pk.q_shard = r;
+    pk.kv_shard = kv_shards[i];
+    const int64_t seg = (int64_t)pk.kv_shard * (P + 1) + r;
+    pk.order = pl->bwd_order + seg * pl->bps;
+    pk.nwork = pl->h_bwd_nwork[seg] * qkv->hkv;
+    if (pk.nwork > 0 && err == cudaSuccess) {
+      const cudaStream_t sks = sk[pk.kv_shard % nsk];
+      pk.sched = sched_slot(pl);
+      const int span = timing_begin(sks);
+      k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+      timing_end(span, sks, kTimeDkdv, 1);
+    }
+    if (++issued[r] == P && !all && err == cudaSuccess) {
+      for (int k = 0; k < nsk && err == cudaSuccess; ++k)
+        if (sk[k] != s) err = stream_fork(sk[k], s);
+      // held to half the SMs while dK/dV launches follow (enough for the memory bandwidth it
+      // is bound by); the last one has the GPU to itself
+      const int ctas = (overlap && i + 1 < n_steps) ? std::max(1, sms / 2) : sms;
+      if (err == cudaSuccess) launch_dq_whole<D>(pl, prm, r, (int)hq, ctas, s);
+      if (err == cudaSuccess) {
+        const int k = (shards_begun - 1) % nbuf;
+        if (ev_buf[k]) cudaEventDestroy(ev_buf[k]);
+        ev_buf[k] = nullptr;
+        err = cudaEventCreateWithFlags(&ev_buf[k], cudaEventDisableTiming);
+        if (err == cudaSuccess) err = cudaEventRecord(ev_buf[k], s);
+      }
+    }
+  }
+  for (int k = 0; k < nsk && err == cudaSuccess; ++k)
+    if (sk[k] != s) err = stream_fork(sk[k], s);
+  for (cudaEvent_t ev : ev_buf)
+    if (ev) cudaEventDestroy(ev);
+  if (err != cudaSuccess) return cuda_fail(err, "ordering of the backward streams");
+  // every tile of the pack at once: one dQ GEMM over every q block's whole row at the end
+  // (one launch balances the rows of all q shards; q shard by q shard in the gaps between
+  // dK/dV launches measured slower)
+  if (all) launch_dq_whole<D>(pl, prm, -1, (int)hq, sms, s);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "launch of the backward kernels");
+  return MARBLE_OK;
+}
+
+// How a full ring list can run with whole-row dQ (launch_whole): 0 if it cannot; else the
+// number of q-shard buffers (P: the whole pack at once) and, below P, each buffer's slots.
+// Below P the list must hold each q shard's steps in one run.
+int whole_plan(const marble_plan_t* pl, int hq, int n_steps, const int* q_shards,
+               const int* kv_shards, int64_t* buf_slots) {
+  const int P = pl->P;
+  if (n_steps != P * P) return 0;
+  std::vector<uint8_t> seen((size_t)P * P, 0), begun(P, 0);
+  bool runs = true;
+  for (int i = 0; i < n_steps; ++i) {
+    const int r = q_shards[i], j = kv_shards[i];
+    if (j < 0 || seen[(size_t)r * P + j]) return 0;
+    seen[(size_t)r * P + j] = 1;
+    if (i % P == 0) {
+      if (begun[r]) runs = false;
+      begun[r] = 1;
+    } else if (r != q_shards[i - 1]) {
+      runs = false;
+    }
+  }
+  if (whole_slots(pl, hq) > 0) return P;
+  if (!runs) return 0;
+  int64_t mx = 0;
+  for (int r = 0; r < P; ++r) mx = std::max(mx, pl->h_step_tiles[(size_t)r * (P + 1) + P]);
+  *buf_slots = mx * hq;
+  const int64_t nbuf = (int64_t)(scratch_cap() / ((size_t)std::max<int64_t>(*buf_slots, 1) * 32768));
+  return nbuf >= 2 ? (int)std::min<int64_t>(nbuf, P - 1) : 0;
+}
+
 template <int D>
 marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, const void* d_o,
                              const float* lse, const float* delta, int n_steps,
@@ -1050,6 +1273,14 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int smem_k = (int)dkdv_smem<D>();
   const int sms = sm_count();
   const int P = pl->P;
+  // a list that holds every (q shard, kv shard) step of the ring exactly once runs with
+  // whole-row dQ GEMMs when its scratch allows (launch_whole)
+  {
+    int64_t buf_slots = 0;
+    const int nbuf = whole_plan(pl, qkv->hq, n_steps, q_shards, kv_shards, &buf_slots);
+    if (nbuf > 0)
+      return launch_whole<D>(pl, qkv, prm, n_steps, q_shards, kv_shards, nbuf, buf_slots, s);
+  }
   // scratch for the bf16 dS^T tiles of kDsBufs steps: the dQ GEMM of step i reads buffer
   // i mod kDsBufs while the dK/dV kernels of the next steps write the others
   int64_t max_tiles = 0;  // the largest step of this call
@@ -1060,7 +1291,7 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   }
   const int64_t buf_slots = max_tiles * qkv->hq;
   const int nbuf = (int)std::max<int64_t>(
-      2, std::min<int64_t>(kDsBufs, (int64_t)(kDsScratchCap / ((size_t)std::max<int64_t>(
+      2, std::min<int64_t>(kDsBufs, (int64_t)(scratch_cap() / ((size_t)std::max<int64_t>(
                                                                  buf_slots, 1) * 32768))));
   rc = ds_scratch(pl, (size_t)(nbuf * buf_slots), s, &prm);
   if (rc != MARBLE_OK) return rc;
@@ -1156,15 +1387,53 @@ marble_status_t launch_fused(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int sms = sm_count();
   const int P = pl->P;
   const int64_t hq = qkv->hq;
+  if (whole_slots(pl, (int)hq) > 0) {
+    // the whole backward: one dK/dV launch per kv shard over its whole ring, storing every
+    // dS^T tile by its row-list entry, then one dQ GEMM over every q block
+    rc = ds_scratch(pl, whole_slots(pl, (int)hq), s, &prm);
+    if (rc != MARBLE_OK) return rc;
+    prm.whole = 1;
+    cudaStream_t sk[kDkdvStreams];
+    int nsk = 0;
+    for (int k = 0; k < kDkdvStreams; ++k) {
+      cudaStream_t x = side_stream(k);
+      if (!x) break;
+      cudaError_t e = stream_fork(s, x);
+      if (e != cudaSuccess) return cuda_fail(e, "fork of the backward streams");
+      sk[nsk++] = x;
+    }
+    if (nsk == 0) sk[nsk++] = s;
+    for (int j = 0; j < P; ++j) {
+      BwdParams pk = prm;
+      pk.kv_shard = j;
+      pk.q_shard = 0;
+      pk.ring_s0 = 0;
+      pk.ring_len = P;
+      const int64_t seg = (int64_t)j * (P + 1) + P;
+      pk.order = pl->bwd_order + seg * pl->bps;
+      pk.nwork = pl->h_bwd_nwork[seg] * qkv->hkv;
+      if (pk.nwork > 0) {
+        const cudaStream_t sks = sk[j % nsk];
+        pk.sched = sched_slot(pl);
+        const int span = timing_begin(sks);
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+        timing_end(span, sks, kTimeDkdv, 1);
+      }
+    }
+    cudaError_t err = cudaSuccess;
+    for (int k = 0; k < nsk && err == cudaSuccess; ++k)
+      if (sk[k] != s) err = stream_fork(sk[k], s);
+    if (err != cudaSuccess) return cuda_fail(err, "ordering of the fused backward streams");
+    launch_dq_whole<D>(pl, prm, -1, (int)hq, sms, s);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "launch of the fused backward kernels");
+    return MARBLE_OK;
+  }
   // ranges of ring steps: consecutive q shards of one kv shard whose dS^T tiles fit in half
   // the scratch cap (two ranges in flight); MARBLE_DS_SCRATCH_CAP_MB lowers the cap (tests)
   struct Range { int j, s0, len; int64_t tiles; };
   std::vector<Range> ranges;
-  size_t cap = kDsScratchCap;
-  if (const char* env = std::getenv("MARBLE_DS_SCRATCH_CAP_MB")) {
-    const unsigned long long mb = std::strtoull(env, nullptr, 10);
-    if (mb > 0 && (mb << 20) < cap) cap = (size_t)(mb << 20);
-  }
+  const size_t cap = scratch_cap();
   const int64_t cap_slots = (int64_t)(cap / 2 / 32768);
   int64_t buf_slots = 0;
   for (int j = 0; j < P; ++j) {

@@ -105,6 +105,7 @@ struct FwdParams {
   int first;
   int lse_merge;   // 0 carried state; 1 merge of bf16 partials (standard ring); 2 of fp32 ones
   const int32_t* kiv;       // [2][n] lo, hi of every key's visible-query interval
+  const int4* kiv_chunk;    // [nb*4] per 32 keys: min lo, max lo, min hi, max hi
   const int32_t* qidx;      // [n] plan order -> index in the given token order (the plan's perm)
   const uint8_t* iv_block;  // [nb] 1: every key of the block has an exact interval
   float scale_log2;
@@ -423,19 +424,28 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         // lane: broadcast loads)
         const bool ivt = partial && p.iv_block[kb] != 0;
         if (ivt) {
+          // per 32-key chunk, its keys' (min lo, max lo, min hi, max hi) first: a row inside
+          // every interval takes all 32 keys and a row outside all of them none; the keys are
+          // tested one by one only when some row of the warp is neither
           const int32_t* klo = p.kiv + kb * 128 + half * 64;
           const int32_t* khi = klo + n;
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
-            uint32_t bits = 0;
+            const int4 cs = __ldg(p.kiv_chunk + kb * 4 + half * 2 + cc);
+            const bool all = iq >= cs.y && iq < cs.z;
+            const bool none = iq < cs.x || iq >= cs.w;
+            uint32_t bits = all ? ~0u : 0u;
+            if (__any_sync(0xffffffffu, !(all || none))) {
+              bits = 0;
 #pragma unroll
-            for (int t2 = 0; t2 < 32; t2 += 4) {
-              const int4 l4 = __ldg(reinterpret_cast<const int4*>(klo + cc * 32 + t2));
-              const int4 h4 = __ldg(reinterpret_cast<const int4*>(khi + cc * 32 + t2));
-              bits |= ((iq >= l4.x) & (iq < h4.x) ? 1u : 0u) << t2;
-              bits |= ((iq >= l4.y) & (iq < h4.y) ? 1u : 0u) << (t2 + 1);
-              bits |= ((iq >= l4.z) & (iq < h4.z) ? 1u : 0u) << (t2 + 2);
-              bits |= ((iq >= l4.w) & (iq < h4.w) ? 1u : 0u) << (t2 + 3);
+              for (int t2 = 0; t2 < 32; t2 += 4) {
+                const int4 l4 = __ldg(reinterpret_cast<const int4*>(klo + cc * 32 + t2));
+                const int4 h4 = __ldg(reinterpret_cast<const int4*>(khi + cc * 32 + t2));
+                bits |= ((iq >= l4.x) & (iq < h4.x) ? 1u : 0u) << t2;
+                bits |= ((iq >= l4.y) & (iq < h4.y) ? 1u : 0u) << (t2 + 1);
+                bits |= ((iq >= l4.z) & (iq < h4.z) ? 1u : 0u) << (t2 + 2);
+                bits |= ((iq >= l4.w) & (iq < h4.w) ? 1u : 0u) << (t2 + 3);
+              }
             }
             lm[cc] = bits;
           }
@@ -470,6 +480,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
             lm[cc] = bits;
           }
         }
+        // a partial tile on which every row of this warp keeps all 64 of its keys takes the
+        // full-tile path below
+        const bool masked = partial && __any_sync(0xffffffffu, (lm[0] & lm[1]) != ~0u);
         if (!wait_all(&bar[B_SFULL0 + b], (g >> 1) & 1, w)) { ok = false; break; }
         tc_fence_after();
         const uint32_t sb = tS + b * 128;
@@ -477,11 +490,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         tmem_ld32(sb + lb + (2 * half) * 32, v[0]);
         tmem_ld32(sb + lb + (2 * half + 1) * 32, v[1]);
         tmem_ld_wait();
-        // this half's row maximum of the scaled, masked scores; on a partial tile the scaled
-        // scores (-inf where masked) replace v, on a full tile v keeps the raw scores (scaling
-        // by a positive constant commutes with the maximum, and P takes one FMA below)
+        // this half's row maximum of the scaled, masked scores; where a key is masked the
+        // scaled scores (-inf where masked) replace v, otherwise v keeps the raw scores
+        // (scaling by a positive constant commutes with the maximum, and P takes one FMA below)
         float mx = -INFINITY;
-        if (partial) {
+        if (masked) {
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
@@ -534,8 +547,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_attn_fwd(const __grid_constant_
         // P = exp2(s - m_run) as bf16, packed into columns [64 half, 64 half + 32) of the S
         // buffer: inside the fp32 columns this warp has just read
         const float base = (m_run == -INFINITY) ? 0.f : m_run;
-        // v holds scaled scores on a partial tile, raw ones on a full tile
-        const float vs = partial ? 1.f : sl2;
+        // v holds scaled scores where keys were masked, raw ones otherwise
+        const float vs = masked ? 1.f : sl2;
         float rs = 0.f;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -764,6 +777,7 @@ marble_status_t prepare(const marble_plan_t* pl, const marble_qkv_t* qkv,
   prm->step_tag = pl->step_tag;
   prm->tracks = pl->tracks;
   prm->kiv = pl->kiv;
+  prm->kiv_chunk = pl->kiv_chunk;
   prm->qidx = pl->perm;
   prm->iv_block = pl->iv_block;
   prm->o_acc = st->o_acc;

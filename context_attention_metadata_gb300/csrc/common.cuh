@@ -356,6 +356,17 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col, int rows) {
 // ------------------------------------------------------------------------------------
 // small numerics helpers
 // ------------------------------------------------------------------------------------
+// Per-warpgroup register budgets (every warp of the warpgroup executes the same one): the
+// block's registers are moved from warpgroups that need few to warpgroups that need many.
+template <int N>
+__device__ __forceinline__ void regs_shrink() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_grow() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

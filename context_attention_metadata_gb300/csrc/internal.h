@@ -45,6 +45,7 @@ struct marble_plan {
   unsigned long long* shard_pairs = nullptr;    // [P*P] statistics: legal pairs per shard pair
   int32_t* kiv = nullptr;       // [2*n] new order: lo, hi of every key's visible query interval
   uint8_t* iv_block = nullptr;  // [nb] new order: 1 if every key of the block is exact
+  int4* kiv_chunk = nullptr;    // [nb*4] per 32 keys: min lo, max lo, min hi, max hi
   int64_t bps = 0;           // blocks per shard
   int64_t nnz = 0, needed_total = 0;
   // device arrays (owned)

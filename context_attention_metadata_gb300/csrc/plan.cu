@@ -557,6 +557,23 @@ __global__ void k_perm_iv(const int32_t* __restrict__ perm, const int32_t* __res
   if ((t & (kBlock - 1)) == 0) iv_block[t >> 7] = iv_orig[block_perm[t >> 7]];
 }
 
+// per 32-key chunk of the new order: (min lo, max lo, min hi, max hi) of its keys' intervals,
+// one warp per chunk.  A query index i with max lo <= i < min hi lies in every key's interval
+// of the chunk; one with i < min lo or i >= max hi in none.
+__global__ void k_iv_chunks(const int32_t* __restrict__ kiv, int64_t n, int4* __restrict__ out) {
+  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (c * 32 >= n) return;
+  const int64_t t = c * 32 + lane;
+  const int lo = kiv[t], hi = kiv[n + t];
+  int4 r;
+  r.x = __reduce_min_sync(0xffffffffu, lo);
+  r.y = __reduce_max_sync(0xffffffffu, lo);
+  r.z = __reduce_min_sync(0xffffffffu, hi);
+  r.w = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) out[c] = r;
+}
+
 // ------------------------------------------------------------------------------------
 // a5: per-step lists
 // ------------------------------------------------------------------------------------
@@ -1278,6 +1295,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   // evaluate the four-track predicate)
   MARBLE_TRY(dalloc(p, &p->kiv, 2 * n));
   MARBLE_TRY(dalloc(p, &p->iv_block, nb));
+  MARBLE_TRY(dalloc(p, &p->kiv_chunk, nb * 4));
+  MARBLE_CK(cudaMemsetAsync(p->kiv_chunk, 0, nb * 4 * sizeof(int4), s));
   MARBLE_CK(cudaMemsetAsync(p->kiv, 0, 2 * n * sizeof(int32_t), s));
   MARBLE_CK(cudaMemsetAsync(p->iv_block, 0, nb, s));
   // With a position track the causal part of an interval comes from the positions, on
@@ -1332,6 +1351,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
     }
     k_perm_iv<<<grid_for(n, threads), threads, 0, s>>>(p->perm, p->block_perm, klo, klo + n,
                                                       iv_orig, n, p->kiv, p->iv_block);
+    k_iv_chunks<<<grid_for(n, threads), threads, 0, s>>>(p->kiv, n, p->kiv_chunk);
     MARBLE_CK(cudaGetLastError());
   }
 

@@ -368,12 +368,18 @@ marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *q
 /* A list of backward ring steps in one call: step i is marble_attn_bwd(..., q_shards[i],
  * kv_shards[i], ..., flags = 0), with the same result as issuing them in list order on
  * `stream`; host arrays of n_steps entries.  Each step runs a dK/dV kernel, which also
- * writes the step's bf16 dS tiles to a scratch array the plan owns, and a dQ GEMM over those
- * tiles.  The scratch holds the tiles of up to four steps (two when four would exceed 32 GB)
- * and grows on demand; backward calls on one plan must therefore be ordered with respect to
- * each other.  The launches spread over side streams of the device, forked from `stream` at
- * the start and joined back into it at the end; launches that add into the same dK/dV rows
- * (one kv shard) stay on one stream, so results do not depend on timing. */
+ * writes the step's bf16 dS tiles to a scratch array the plan owns, and a dQ GEMM reads them:
+ *   - a list that holds every (q shard, kv shard) pair of the ring exactly once, when the dS
+ *     tiles of the whole pack fit the 32 GB scratch cap (nnz tiles x hq x 32 KB): every
+ *     step's dK/dV kernel, then ONE dQ GEMM over every q block's whole row, so each dQ row
+ *     block is accumulated on chip over all its steps and added to dq_acc once (a q shard's
+ *     dQ is local to it on a real ring, so its GEMM may wait for the ring's end);
+ *   - otherwise a dQ GEMM after each step, the scratch holding the tiles of up to four steps
+ *     (two when four would exceed the cap).
+ * The scratch grows on demand; backward calls on one plan must therefore be ordered with
+ * respect to each other.  The launches spread over side streams of the device, forked from
+ * `stream` at the start and joined back into it at the end; launches that add into the same
+ * dK/dV rows (one kv shard) stay on one stream, so results do not depend on timing. */
 marble_status_t marble_attn_bwd_steps(const marble_plan_t *plan, const marble_qkv_t *qkv,
                                       const void *d_o, const float *lse, const float *delta,
                                       int32_t n_steps, const int32_t *q_shards,
@@ -400,8 +406,10 @@ marble_status_t marble_attn_fwd_fused(const marble_plan_t *plan, const marble_qk
  * marble_attn_bwd_steps over every (r, (r - s) mod P), up to fp32 rounding.  For every kv
  * shard j, one dK/dV launch visits the q shards in ring order (j, j + 1, ..., j - 1) and keeps
  * the dK/dV of each of its kv blocks in TMEM across all of them, adding it to dk_acc / dv_acc
- * once; the dQ GEMM of each step (q shard, j) follows.  When the dS tiles of a kv shard's
- * whole ring would exceed half of the 32 GB scratch cap, its ring is split into consecutive
+ * once.  When the dS tiles of the whole pack fit the 32 GB scratch cap, one dQ GEMM over
+ * every q block's whole row follows all of them (as in marble_attn_bwd_steps).  Otherwise
+ * the dQ GEMM of each step (q shard, j) follows its kv shard's launch, and when the dS tiles
+ * of a kv shard's whole ring would exceed half of the cap, its ring is split into consecutive
  * ranges of steps, each added once.  Accumulators must be zeroed by the caller; scratch and
  * ordering as marble_attn_bwd_steps.  Errors: as marble_attn_bwd_steps.
  */

@@ -154,25 +154,42 @@ def test_fused_backward_equals_oracle_and_steps(cid, n, P):
     _close_to_steps(fused, steps, shuf, one)
 
 
-def test_fused_backward_split_ring_ranges():
-    """With a scratch cap too small for a kv shard's whole ring, the fused backward splits
-    each ring into ranges of consecutive steps (dK/dV added once per range); the gradients
-    are unchanged up to fp32 summation order."""
+def _with_cap(mb, fn):
+    os.environ["MARBLE_DS_SCRATCH_CAP_MB"] = str(mb)
+    try:
+        return fn()
+    finally:
+        del os.environ["MARBLE_DS_SCRATCH_CAP_MB"]
+
+
+def test_backward_scratch_modes():
+    """The backward's three ways of holding the dS^T tiles, reached by lowering the scratch
+    cap: every tile of the pack at once (the default here: one whole-row dQ GEMM per q shard,
+    and for the fused backward one at the end); a few q shards' tiles at a time (whole-row
+    dQ per q shard, buffers taken over in turn); and a few steps' tiles at a time (a dQ GEMM
+    after each step; the fused backward splits each kv shard's ring into ranges).  All agree
+    up to fp32 summation order and each matches the oracle."""
     cfg = wl.mini_config(2, 8192, hq=2)
     tr = wl.config_tracks(2, 8192)
     q, k, v, do = wl.make_qkvdo(8192, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=81)
     pl = make_plan(tr, cfg.window, 8, "ptrr_block")
-    whole = _both_backwards(pl, q, k, v, do)[1]
-    os.environ["MARBLE_DS_SCRATCH_CAP_MB"] = "4"  # 32 tiles per range at 2 heads
-    try:
-        steps, split, shuf, one = _both_backwards(pl, q, k, v, do, calibrate=(tr, cfg.window))
-    finally:
-        del os.environ["MARBLE_DS_SCRATCH_CAP_MB"]
+    st = pl.stats()
+    assert st["shard_cost_max"] * cfg.hq * 32768 * 3 < st["nnz"] * cfg.hq * 32768
+    assert st["shard_cost_max"] * cfg.hq * 32768 * 2 > 4 << 20  # 4 MB: two q shards do not fit
+    steps_whole, fused_whole = _both_backwards(pl, q, k, v, do)
+    # three q shards' tiles fit, the whole pack does not
+    mb = -(-st["shard_cost_max"] * cfg.hq * 32768 * 3 // (1 << 20))
+    steps_shards = _with_cap(mb, lambda: _both_backwards(pl, q, k, v, do))[0]
+    steps, split, shuf, one = _with_cap(4, lambda: _both_backwards(pl, q, k, v, do,
+                                                                   calibrate=(tr, cfg.window)))
     _close_to_steps(split, steps, shuf, one)
-    _close_to_steps(split, whole, shuf, one)
+    _close_to_steps(fused_whole, steps, shuf, one)
+    _close_to_steps(steps_whole, steps, shuf, one)
+    _close_to_steps(steps_shards, steps, shuf, one)
     rq, rk, rv, _, _ = attention.backward(q, k, v, do, mask.dense_mask(tr, cfg.window))
-    for g, ref in zip(split, (rq, rk, rv)):
-        assert rel_fro(g.cpu().double().numpy(), ref) <= TOL_GRAD_REL
+    for got in (split, steps, steps_whole, steps_shards, fused_whole):
+        for g, ref in zip(got, (rq, rk, rv)):
+            assert rel_fro(g.cpu().double().numpy(), ref) <= TOL_GRAD_REL
 
 
 def test_fused_full_size_packed_64k_equals_steps():
