@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -849,38 +850,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         fence_proxy_async_smem();
         uint8_t* box_row = sDS + half * 16384 + row * 128;
         // P^T = exp2(s * scale * log2 e - lse2[q]), dS^T = P^T (dP^T - delta[q]); the per-query
-        // LSE and delta are read four at a time; full tiles skip the mask
+        // LSE and delta are read four at a time.  Two copies of the loop, chosen per warp: with
+        // the mask's select, and without it (full tiles, and partial ones whose rows in this
+        // warp keep every column)
+        auto elementwise = [&](auto with_mask) {
+          constexpr bool kMasked = decltype(with_mask)::value;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t pk16[16], dk16[16];
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t pk16[16], dk16[16];
 #pragma unroll
-          for (int t = 0; t < 32; t += 4) {
-            const int q0 = cc * 32 + t;
-            const float4 l4 = *reinterpret_cast<const float4*>(lse2s + q0);
-            const float4 d4 = *reinterpret_cast<const float4*>(dls + q0);
-            const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq4[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dv4[4];
+            for (int t = 0; t < 32; t += 4) {
+              const int q0 = cc * 32 + t;
+              const float4 l4 = *reinterpret_cast<const float4*>(lse2s + q0);
+              const float4 d4 = *reinterpret_cast<const float4*>(dls + q0);
+              const float lq[4] = {l4.x, l4.y, l4.z, l4.w}, dq4[4] = {d4.x, d4.y, d4.z, d4.w};
+              float pv[4], dv4[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float ex = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
-              pv[u] = (masked && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : ex;
-              dv4[u] = pv[u] * (__uint_as_float(vp[cc][t + u]) - dq4[u]);
+              for (int u = 0; u < 4; ++u) {
+                const float ex = fast_exp2(fmaf(__uint_as_float(vs[cc][t + u]), sl2, -lq[u]));
+                pv[u] = (kMasked && !((lm[cc] >> (t + u)) & 1u)) ? 0.f : ex;
+                dv4[u] = pv[u] * (__uint_as_float(vp[cc][t + u]) - dq4[u]);
+              }
+              pk16[t >> 1] = pack_bf16(pv[0], pv[1]);
+              pk16[(t >> 1) + 1] = pack_bf16(pv[2], pv[3]);
+              dk16[t >> 1] = pack_bf16(dv4[0], dv4[1]);
+              dk16[(t >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
             }
-            pk16[t >> 1] = pack_bf16(pv[0], pv[1]);
-            pk16[(t >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-            dk16[t >> 1] = pack_bf16(dv4[0], dv4[1]);
-            dk16[(t >> 1) + 1] = pack_bf16(dv4[2], dv4[3]);
-          }
-          // q columns [32 cc, 32 cc + 32) of this half: 16-byte chunks 4 cc .. 4 cc + 3 of the
-          // row, 128-byte swizzled as the TMA store reads them
+            // q columns [32 cc, 32 cc + 32) of this half: 16-byte chunks 4 cc .. 4 cc + 3 of the
+            // row, 128-byte swizzled as the TMA store reads them
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(box_row + (((4 * cc + c) ^ (row & 7)) << 4)) =
-                make_uint4(dk16[4 * c], dk16[4 * c + 1], dk16[4 * c + 2], dk16[4 * c + 3]);
-          // q column pair c of this half -> P^T column 64 half + c, dS^T column 64 half + 32 + c
-          tmem_st16(rS + lb + half * 64 + cc * 16, pk16);
-          tmem_st16(rS + lb + half * 64 + 32 + cc * 16, dk16);
-        }
+            for (int c = 0; c < 4; ++c)
+              *reinterpret_cast<uint4*>(box_row + (((4 * cc + c) ^ (row & 7)) << 4)) =
+                  make_uint4(dk16[4 * c], dk16[4 * c + 1], dk16[4 * c + 2], dk16[4 * c + 3]);
+            // q column pair c of this half -> P^T column 64 half + c, dS^T column 64 half + 32 + c
+            tmem_st16(rS + lb + half * 64 + cc * 16, pk16);
+            tmem_st16(rS + lb + half * 64 + 32 + cc * 16, dk16);
+          }
+        };
+        if (masked)
+          elementwise(std::true_type{});
+        else
+          elementwise(std::false_type{});
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bar[K_PFULL]);
