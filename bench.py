@@ -616,7 +616,7 @@ def run_marble(args, rank, world, local, dist):
         r, el, ns, tok = oracle_sample_rate(cfg, tr, args.cpu_budget)
         cpu = {"value": r, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"{ns} whole samples ({tok} tokens) of the pack, all {hq} q heads, "
-                         f"fp64 dense fwd+bwd, {el:.1f} s"}
+                         f"fp64 dense {'fwd+bwd' if with_bwd else 'fwd'}, {el:.1f} s"}
 
     if rank == 0:
         line = {

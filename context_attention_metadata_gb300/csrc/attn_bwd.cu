@@ -36,6 +36,7 @@
 
 #include <algorithm>
 #include <cstdlib>
+#include <cstring>
 #include <type_traits>
 
 #include "common.cuh"
@@ -662,14 +663,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
             itn = queue.T[slot] * p.group;
           }
         }
-        // S^T(g + 1) into dP^T(g)'s region once every elementwise thread holds its scores
-        if (nxt) {
-          if (!mbar_wait(&bar[K_YFREE], g & 1, w)) break;
-          if (newu && !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w)) break;
-          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) break;
+        // S^T(g + 1) into dP^T(g)'s region once every elementwise thread holds its scores;
+        // at a unit's end it waits until item g's accumulations are issued (below), so that
+        // the load of the next unit's K and V does not hold back the unit's last dV / dK
+        auto next_scores = [&]() -> bool {
+          if (!mbar_wait(&bar[K_YFREE], g & 1, w)) return false;
+          if (newu && !mbar_wait(&bar[K_KVFULL], (uc + 1) & 1, w)) return false;
+          if (!mbar_wait(&bar[K_QFULL0 + ((g + 1) & 1)], ((g + 1) >> 1) & 1, w)) return false;
           tc_fence_after();
           issue_scores(g + 1, false);
-        }
+          return true;
+        };
+        if (nxt && !newu && !next_scores()) break;
         // dV / dK of item g once its P^T / dS^T are in TMEM; a unit's first accumulation
         // overwrites dV / dK, so the previous unit's must have been read out
         if (!mbar_wait(&bar[K_PFULL], g & 1, w)) break;
@@ -682,6 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_bwd_dkdv(const __grid_constant_
         else
           mma_commit(&bar[K_QEMPTY0 + (g & 1)]);
         if (!nxt) break;
+        if (newu && !next_scores()) break;
         // dP^T(g + 1) into S^T(g)'s region, after the accumulations that read it
         issue_scores(g + 1, true);
         mma_commit(&bar[K_SDP]);
@@ -1245,7 +1251,27 @@ marble_status_t launch_whole(const marble_plan_t* pl, const marble_qkv_t* qkv, B
 
 // How a full ring list can run with whole-row dQ (launch_whole): 0 if it cannot; else the
 // number of q-shard buffers (P: the whole pack at once) and, below P, each buffer's slots.
-// Below P the list must hold each q shard's steps in one run.
+// Below P the list must hold each q shard's steps in one run.  A dQ GEMM unit is a q block's
+// whole row: when the longest row is more than half a CTA's share of its launch, that one
+// unit would set the launch's length, and the per-step GEMMs (rows cut at kv shards) are
+// taken instead.
+// no q block's whole row longer than half a CTA's share of `tiles` rows' worth of units
+// (MARBLE_WHOLE_ROWS=always skips the test; tests use it to reach these paths on small packs)
+bool rows_balance(int64_t longest, int64_t tiles, int hq) {
+  const char* env = std::getenv("MARBLE_WHOLE_ROWS");
+  if (env && std::strcmp(env, "always") == 0) return true;
+  return 2 * longest * sm_count() <= tiles * (int64_t)hq;
+}
+
+// every tile of the pack at once, with one dQ GEMM over all q blocks
+bool whole_all(const marble_plan_t* pl, int hq) {
+  if (whole_slots(pl, hq) == 0) return false;
+  int64_t longest = 0;
+  for (int r = 0; r < pl->P; ++r)
+    longest = std::max(longest, pl->h_step_max[(size_t)r * (pl->P + 1) + pl->P]);
+  return rows_balance(longest, pl->nnz, hq);
+}
+
 int whole_plan(const marble_plan_t* pl, int hq, int n_steps, const int* q_shards,
                const int* kv_shards, int64_t* buf_slots) {
   const int P = pl->P;
@@ -1263,10 +1289,14 @@ int whole_plan(const marble_plan_t* pl, int hq, int n_steps, const int* q_shards
       runs = false;
     }
   }
-  if (whole_slots(pl, hq) > 0) return P;
+  if (whole_all(pl, hq)) return P;
   if (!runs) return 0;
   int64_t mx = 0;
-  for (int r = 0; r < P; ++r) mx = std::max(mx, pl->h_step_tiles[(size_t)r * (P + 1) + P]);
+  for (int r = 0; r < P; ++r) {
+    const int64_t tiles = pl->h_step_tiles[(size_t)r * (P + 1) + P];
+    if (!rows_balance(pl->h_step_max[(size_t)r * (P + 1) + P], tiles, hq)) return 0;
+    mx = std::max(mx, tiles);
+  }
   *buf_slots = mx * hq;
   const int64_t nbuf = (int64_t)(scratch_cap() / ((size_t)std::max<int64_t>(*buf_slots, 1) * 32768));
   return nbuf >= 2 ? (int)std::min<int64_t>(nbuf, P - 1) : 0;
@@ -1397,7 +1427,7 @@ marble_status_t launch_fused(const marble_plan_t* pl, const marble_qkv_t* qkv, c
   const int sms = sm_count();
   const int P = pl->P;
   const int64_t hq = qkv->hq;
-  if (whole_slots(pl, (int)hq) > 0) {
+  if (whole_all(pl, (int)hq)) {
     // the whole backward: one dK/dV launch per kv shard over its whole ring, storing every
     // dS^T tile by its row-list entry, then one dQ GEMM over every q block
     rc = ds_scratch(pl, whole_slots(pl, (int)hq), s, &prm);

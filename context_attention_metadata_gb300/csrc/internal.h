@@ -87,8 +87,10 @@ struct marble_plan {
   // its q block's list for that kv shard
   int32_t* step_off = nullptr;       // [nb*(P+1)]
   int64_t* step_tiles = nullptr;     // [P*(P+1)] tiles per (q shard, option)
+  int64_t* step_max = nullptr;       // [P*(P+1)] longest q-block list per (q shard, option)
   int32_t* colT_j = nullptr;         // [nnz]
   std::vector<int64_t> h_step_tiles;
+  std::vector<int64_t> h_step_max;        // [P*(P+1)] longest list of a q block in the step
   // backward scratch: bf16 dS^T tiles of two steps (allocated by the first backward call)
   mutable std::mutex scratch_mu;
   mutable void* ds_scratch = nullptr;

@@ -737,14 +737,19 @@ __global__ void k_colT_pos(const int64_t* __restrict__ colT_ptr, const int32_t* 
 // the q blocks of shard r before nq; step_tiles[r * (P+1) + opt] = the step's total.
 __global__ void __launch_bounds__(1024) k_step_off(const int64_t* __restrict__ step_ptr, int P,
                                                    int64_t bps, int32_t* __restrict__ step_off,
-                                                   int64_t* __restrict__ step_tiles) {
+                                                   int64_t* __restrict__ step_tiles,
+                                                   int64_t* __restrict__ step_max) {
   __shared__ int64_t sc[1024];
   __shared__ int64_t carry;
+  __shared__ unsigned long long longest;
   const int seg = blockIdx.x;
   const int r = seg / (P + 1), opt = seg % (P + 1);
   const int c_lo = opt < P ? opt : 0, c_hi = opt < P ? opt + 1 : P;
   const int t = threadIdx.x;
-  if (t == 0) carry = 0;
+  if (t == 0) {
+    carry = 0;
+    longest = 0;
+  }
   __syncthreads();
   for (int64_t i0 = 0; i0 < bps; i0 += 1024) {
     const int64_t i = i0 + t;
@@ -752,6 +757,7 @@ __global__ void __launch_bounds__(1024) k_step_off(const int64_t* __restrict__ s
     if (i < bps) {
       const int64_t nq = (int64_t)r * bps + i;
       len = step_ptr[nq * P + c_hi] - step_ptr[nq * P + c_lo];
+      atomicMax(&longest, (unsigned long long)len);
     }
     sc[t] = len;
     __syncthreads();
@@ -766,7 +772,10 @@ __global__ void __launch_bounds__(1024) k_step_off(const int64_t* __restrict__ s
     if (t == 1023) carry += sc[1023];
     __syncthreads();
   }
-  if (t == 0) step_tiles[seg] = carry;
+  if (t == 0) {
+    step_tiles[seg] = carry;
+    step_max[seg] = (int64_t)longest;
+  }
 }
 
 // needed kv blocks of q shard r = kv blocks with a non-empty (kv block, r) list
@@ -1173,6 +1182,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   MARBLE_TRY(dalloc(p, &p->sched, 2 * kSchedSlots));
   MARBLE_TRY(dalloc(p, &p->step_off, (size_t)nb * (P + 1)));
   MARBLE_TRY(dalloc(p, &p->step_tiles, (size_t)P * (P + 1)));
+  MARBLE_TRY(dalloc(p, &p->step_max, (size_t)P * (P + 1)));
   // scratch: counters of the two-pass compactions and the order builder
   int32_t *cnt = nullptr, *cnt2 = nullptr, *cntT = nullptr, *ucost = nullptr,
           *rank_of = nullptr, *unit_new = nullptr, *ncount = nullptr;
@@ -1390,7 +1400,8 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   // positions of the column-list entries in the row lists, and each step's tile numbering
   k_colT_pos<<<(unsigned)grid_for(nb * P, kWarpsPerCta), 32 * kWarpsPerCta, 0, s>>>(
       p->colT_ptr, p->colT_row, p->step_ptr, p->step_col, p->block_perm, nb, P, bps, p->colT_j);
-  k_step_off<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->step_off, p->step_tiles);
+  k_step_off<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->step_off, p->step_tiles,
+                                          p->step_max);
   MARBLE_CK(cudaGetLastError());
   // work order of the persistent kernels
   k_work_order<<<P * (P + 1), 1024, 0, s>>>(p->step_ptr, P, bps, p->fwd_order, p->fwd_nwork);
@@ -1415,6 +1426,9 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
                             cudaMemcpyDeviceToHost, s));
   p->h_step_tiles.resize((size_t)P * (P + 1));
   MARBLE_CK(cudaMemcpyAsync(p->h_step_tiles.data(), p->step_tiles, P * (P + 1) * sizeof(int64_t),
+                            cudaMemcpyDeviceToHost, s));
+  p->h_step_max.resize((size_t)P * (P + 1));
+  MARBLE_CK(cudaMemcpyAsync(p->h_step_max.data(), p->step_max, P * (P + 1) * sizeof(int64_t),
                             cudaMemcpyDeviceToHost, s));
   MARBLE_CK(cudaStreamSynchronize(s));
   return MARBLE_OK;

@@ -374,8 +374,12 @@ marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *q
  *     step's dK/dV kernel, then ONE dQ GEMM over every q block's whole row, so each dQ row
  *     block is accumulated on chip over all its steps and added to dq_acc once (a q shard's
  *     dQ is local to it on a real ring, so its GEMM may wait for the ring's end);
+ *   - such a list in q-shard runs (r-major), when the tiles of two q shards fit the cap: the
+ *     same whole-row GEMM per q shard after its last step, a few q shards' tiles held at once;
  *   - otherwise a dQ GEMM after each step, the scratch holding the tiles of up to four steps
  *     (two when four would exceed the cap).
+ *   Whole rows are used only while no q block's row is longer than half an SM's share of the
+ *   GEMM's tiles (one such unit would set the launch's length).
  * The scratch grows on demand; backward calls on one plan must therefore be ordered with
  * respect to each other.  The launches spread over side streams of the device, forked from
  * `stream` at the start and joined back into it at the end; launches that add into the same
@@ -406,8 +410,9 @@ marble_status_t marble_attn_fwd_fused(const marble_plan_t *plan, const marble_qk
  * marble_attn_bwd_steps over every (r, (r - s) mod P), up to fp32 rounding.  For every kv
  * shard j, one dK/dV launch visits the q shards in ring order (j, j + 1, ..., j - 1) and keeps
  * the dK/dV of each of its kv blocks in TMEM across all of them, adding it to dk_acc / dv_acc
- * once.  When the dS tiles of the whole pack fit the 32 GB scratch cap, one dQ GEMM over
- * every q block's whole row follows all of them (as in marble_attn_bwd_steps).  Otherwise
+ * once.  When the dS tiles of the whole pack fit the 32 GB scratch cap (and the rows balance,
+ * as in marble_attn_bwd_steps), one dQ GEMM over every q block's whole row follows all of
+ * them.  Otherwise
  * the dQ GEMM of each step (q shard, j) follows its kv shard's launch, and when the dS tiles
  * of a kv shard's whole ring would exceed half of the cap, its ring is split into consecutive
  * ranges of steps, each added once.  Accumulators must be zeroed by the caller; scratch and

@@ -154,18 +154,28 @@ def test_fused_backward_equals_oracle_and_steps(cid, n, P):
     _close_to_steps(fused, steps, shuf, one)
 
 
-def _with_cap(mb, fn):
-    os.environ["MARBLE_DS_SCRATCH_CAP_MB"] = str(mb)
+def _with_env(env, fn):
+    os.environ.update(env)
     try:
         return fn()
     finally:
-        del os.environ["MARBLE_DS_SCRATCH_CAP_MB"]
+        for k in env:
+            del os.environ[k]
+
+
+def _with_cap(mb, fn):
+    return _with_env({"MARBLE_DS_SCRATCH_CAP_MB": str(mb)}, fn)
+
+
+# whole-row dQ GEMMs regardless of row balance (on a small pack one long row would otherwise
+# send the backward to the per-step GEMMs)
+WHOLE = {"MARBLE_WHOLE_ROWS": "always"}
 
 
 def test_backward_scratch_modes():
-    """The backward's three ways of holding the dS^T tiles, reached by lowering the scratch
-    cap: every tile of the pack at once (the default here: one whole-row dQ GEMM per q shard,
-    and for the fused backward one at the end); a few q shards' tiles at a time (whole-row
+    """The backward's three ways of holding the dS^T tiles, reached through the scratch cap
+    (and, on this small pack, MARBLE_WHOLE_ROWS=always): every tile of the pack at once (one
+    whole-row dQ GEMM after every dK/dV launch); a few q shards' tiles at a time (whole-row
     dQ per q shard, buffers taken over in turn); and a few steps' tiles at a time (a dQ GEMM
     after each step; the fused backward splits each kv shard's ring into ranges).  All agree
     up to fp32 summation order and each matches the oracle."""
@@ -176,10 +186,11 @@ def test_backward_scratch_modes():
     st = pl.stats()
     assert st["shard_cost_max"] * cfg.hq * 32768 * 3 < st["nnz"] * cfg.hq * 32768
     assert st["shard_cost_max"] * cfg.hq * 32768 * 2 > 4 << 20  # 4 MB: two q shards do not fit
-    steps_whole, fused_whole = _both_backwards(pl, q, k, v, do)
+    steps_whole, fused_whole = _with_env(WHOLE, lambda: _both_backwards(pl, q, k, v, do))
     # three q shards' tiles fit, the whole pack does not
     mb = -(-st["shard_cost_max"] * cfg.hq * 32768 * 3 // (1 << 20))
-    steps_shards = _with_cap(mb, lambda: _both_backwards(pl, q, k, v, do))[0]
+    steps_shards = _with_env({**WHOLE, "MARBLE_DS_SCRATCH_CAP_MB": str(mb)},
+                             lambda: _both_backwards(pl, q, k, v, do))[0]
     steps, split, shuf, one = _with_cap(4, lambda: _both_backwards(pl, q, k, v, do,
                                                                    calibrate=(tr, cfg.window)))
     _close_to_steps(split, steps, shuf, one)
