@@ -380,6 +380,9 @@ marble_status_t marble_attn_bwd(const marble_plan_t *plan, const marble_qkv_t *q
  *     (two when four would exceed the cap).
  *   Whole rows are used only while no q block's row is longer than half an SM's share of the
  *   GEMM's tiles (one such unit would set the launch's length).
+ * Two environment variables, read on every call, reach the other paths on small packs (tests):
+ * MARBLE_DS_SCRATCH_CAP_MB lowers the 32 GB cap; MARBLE_WHOLE_ROWS=always skips the row test.
+ * Results differ between the paths only in fp32 summation order.
  * The scratch grows on demand; backward calls on one plan must therefore be ordered with
  * respect to each other.  The launches spread over side streams of the device, forked from
  * `stream` at the start and joined back into it at the end; launches that add into the same
