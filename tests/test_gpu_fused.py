@@ -172,16 +172,18 @@ def _with_cap(mb, fn):
 WHOLE = {"MARBLE_WHOLE_ROWS": "always"}
 
 
-def test_backward_scratch_modes():
+@pytest.mark.parametrize("hq,hkv,d", [(2, 2, 128), (4, 2, 64)])
+def test_backward_scratch_modes(hq, hkv, d):
     """The backward's three ways of holding the dS^T tiles, reached through the scratch cap
     (and, on this small pack, MARBLE_WHOLE_ROWS=always): every tile of the pack at once (one
     whole-row dQ GEMM after every dK/dV launch); a few q shards' tiles at a time (whole-row
     dQ per q shard, buffers taken over in turn); and a few steps' tiles at a time (a dQ GEMM
     after each step; the fused backward splits each kv shard's ring into ranges).  All agree
-    up to fp32 summation order and each matches the oracle."""
-    cfg = wl.mini_config(2, 8192, hq=2)
+    up to fp32 summation order and each matches the oracle; with and without grouped kv
+    heads, at both head dims."""
+    cfg = wl.mini_config(2, 8192, hq=hq, hkv=hkv)
     tr = wl.config_tracks(2, 8192)
-    q, k, v, do = wl.make_qkvdo(8192, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=81)
+    q, k, v, do = wl.make_qkvdo(8192, hq, hkv, d, device="cuda", seed=81)
     pl = make_plan(tr, cfg.window, 8, "ptrr_block")
     st = pl.stats()
     assert st["shard_cost_max"] * cfg.hq * 32768 * 3 < st["nnz"] * cfg.hq * 32768
