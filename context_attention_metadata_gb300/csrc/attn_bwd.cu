@@ -1191,6 +1191,9 @@ marble_status_t launch_whole(const marble_plan_t* pl, const marble_qkv_t* qkv, B
   }
   if (nsk == 0) sk[nsk++] = s;
   const bool overlap = sk[0] != s;
+  // with side streams, a dK/dV launch takes at most half the SMs: launches of different kv
+  // shards then share the GPU instead of one waiting for the other's tail
+  const int cap = overlap ? (sms + 1) / 2 : sms;
   std::vector<int> issued(P, 0);
   std::vector<cudaEvent_t> ev_buf(all ? 0 : nbuf, nullptr);
   int shards_begun = 0;
@@ -1216,7 +1219,7 @@ marble_status_t launch_whole(const marble_plan_t* pl, const marble_qkv_t* qkv, B
       const cudaStream_t sks = sk[pk.kv_shard % nsk];
       pk.sched = sched_slot(pl);
       const int span = timing_begin(sks);
-      k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+      k_bwd_dkdv<D><<<(unsigned)(pk.nwork < cap ? pk.nwork : cap), kThreads, smem_k, sks>>>(pk);
       timing_end(span, sks, kTimeDkdv, 1);
     }
     if (++issued[r] == P && !all && err == cudaSuccess) {
@@ -1381,7 +1384,9 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, c
       if (pk.nwork > 0 && err == cudaSuccess) {
         pk.sched = sched_slot(pl);
         const int span = timing_begin(sks);
-        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+        // with several side streams, at most half the SMs (as in launch_whole)
+        const int cap = (sks != s && nsk > 1) ? (sms + 1) / 2 : sms;
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < cap ? pk.nwork : cap), kThreads, smem_k, sks>>>(pk);
         timing_end(span, sks, kTimeDkdv, 1);
       }
       if (sks != s && err == cudaSuccess) {

@@ -843,7 +843,10 @@ marble_status_t launch_steps(const marble_plan_t* pl, const marble_qkv_t* qkv, i
     // persistent: one CTA per SM (each takes all 512 TMEM columns); the FIRST call also
     // initialises the units without tiles, spread over the whole grid
     const int want = prm.first ? base.units : prm.nwork;
-    const unsigned grid = (unsigned)(want < sms ? want : sms);
+    // with side streams, a launch takes at most half the SMs: launches of different q shards
+    // then share the GPU instead of one waiting for the other's tail
+    const int cap = ns > 1 ? (sms + 1) / 2 : sms;
+    const unsigned grid = (unsigned)(want < cap ? want : cap);
     const int k = prm.q_shard % ns;
     k_attn_fwd<D><<<grid, kThreads, Smem<D>::bytes(), st_of[k]>>>(prm);
     ++launches[k];
