@@ -30,8 +30,8 @@ import time
 # with the digest of the kernel's source files at the time of the capture: a figure is
 # reported only while the source is unchanged, null otherwise.
 KERNEL_DRAM_BYTES_PER_LAUNCH = {
-    "k_bwd_dkdv": (467.6e6, "profiles/k_bwd_dkdv_packed_multimodal.md", "26d37dc206239dd9"),
-    "k_bwd_dq": (14775.6e6, "profiles/k_bwd_dq_packed_multimodal.md", "26d37dc206239dd9"),
+    "k_bwd_dkdv": (467.6e6, "profiles/k_bwd_dkdv_packed_multimodal.md", "62eb66bbc3d615f4"),
+    "k_bwd_dq": (14599.0e6, "profiles/k_bwd_dq_packed_multimodal.md", "62eb66bbc3d615f4"),
     "k_attn_fwd": (151.9e6, "profiles/k_attn_fwd_packed_multimodal.md", "5ac2f710191f7577"),
 }
 KERNEL_SOURCES = {"k_bwd_dkdv": ("attn_bwd.cu", "common.cuh"),

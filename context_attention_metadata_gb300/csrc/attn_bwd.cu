@@ -1461,7 +1461,10 @@ marble_status_t launch_fused(const marble_plan_t* pl, const marble_qkv_t* qkv, c
         const cudaStream_t sks = sk[j % nsk];
         pk.sched = sched_slot(pl);
         const int span = timing_begin(sks);
-        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < sms ? pk.nwork : sms), kThreads, smem_k, sks>>>(pk);
+        // with several side streams, at most half the SMs (as in launch_whole; measured a
+        // little faster here, slower in the ranges below, whose dQ GEMMs interleave)
+        const int cap = nsk > 1 ? (sms + 1) / 2 : sms;
+        k_bwd_dkdv<D><<<(unsigned)(pk.nwork < cap ? pk.nwork : cap), kThreads, smem_k, sks>>>(pk);
         timing_end(span, sks, kTimeDkdv, 1);
       }
     }
