@@ -30,8 +30,8 @@ import time
 # with the digest of the kernel's source files at the time of the capture: a figure is
 # reported only while the source is unchanged, null otherwise.
 KERNEL_DRAM_BYTES_PER_LAUNCH = {
-    "k_bwd_dkdv": (467.6e6, "profiles/k_bwd_dkdv_packed_multimodal.md", "62eb66bbc3d615f4"),
-    "k_bwd_dq": (14599.0e6, "profiles/k_bwd_dq_packed_multimodal.md", "62eb66bbc3d615f4"),
+    "k_bwd_dkdv": (467.8e6, "profiles/k_bwd_dkdv_packed_multimodal.md", "371c0b41d71435a5"),
+    "k_bwd_dq": (12860.8e6, "profiles/k_bwd_dq_packed_multimodal.md", "371c0b41d71435a5"),
     "k_attn_fwd": (151.9e6, "profiles/k_attn_fwd_packed_multimodal.md", "5ac2f710191f7577"),
 }
 KERNEL_SOURCES = {"k_bwd_dkdv": ("attn_bwd.cu", "common.cuh"),
@@ -450,10 +450,10 @@ def run_marble(args, rank, world, local, dist):
     # end to end through the public API: H2D of the step's inputs from pinned memory,
     # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results.
     # Steps are pipelined the way a training loop runs them: the next step's inputs are
-    # copied in, and its plan built, on one copy stream while this step computes, and this
-    # step's results are copied out on another while the next step computes (double-buffered
-    # inputs and outputs).  Each plan is destroyed as soon as its step is queued: the
-    # library frees it in stream order, without synchronising.
+    # copied in on one copy stream and its tracks copied and its plan built on another while
+    # this step computes, and this step's results are copied out on a third while the next
+    # step computes (double-buffered inputs and outputs).  Each plan is destroyed as soon as
+    # its step is queued: the library frees it in stream order, without synchronising.
     e2e = None
     if args.e2e_steps > 0:
         hq_pin = [t.cpu().pin_memory() for t in ((q, k, v, do) if with_bwd else (q, k, v))]
@@ -467,7 +467,8 @@ def run_marble(args, rank, world, local, dist):
         dev_tr = [[torch.empty_like(t, device="cuda") for t in htr] for _ in range(2)]
         g_tmp = [torch.empty((n, hq, d), dtype=torch.float32, device="cuda"),
                  torch.empty((n, hkv, d), dtype=torch.float32, device="cuda")]
-        cs = torch.cuda.Stream()       # host -> device
+        cs = torch.cuda.Stream()       # host -> device: tracks, then the plan
+        cs_in = torch.cuda.Stream()    # host -> device: Q, K, V, dO
         cs_out = torch.cuda.Stream()   # device -> host (the two directions overlap)
         comp = torch.cuda.current_stream()
 
@@ -477,14 +478,20 @@ def run_marble(args, rank, world, local, dist):
                                                        for _ in range(5))
 
             def h2d_and_plan(i):
-                # inputs in on the copy stream, then the plan on that same stream: the
-                # planner's own synchronisations wait for the copies only, not for the
-                # previous step's compute
+                # the step's Q/K/V/dO on one copy stream; its tracks, then its plan, on another:
+                # the planner's own synchronisation waits for the small track copy only, not for
+                # the inputs' copy nor for the previous step's compute
                 b = i % 2
+                with torch.cuda.stream(cs_in):
+                    if i >= 2:
+                        cs_in.wait_event(ev_used[b])   # step i - 2 is done with buffer b
+                    for dst, src in zip(dev_in[b], hq_pin):
+                        dst.copy_(src, non_blocking=True)
+                    ev_in[b].record(cs_in)
                 with torch.cuda.stream(cs):
                     if i >= 2:
-                        cs.wait_event(ev_used[b])   # step i - 2 is done with buffer b
-                    for dst, src in zip(dev_in[b] + dev_tr[b], hq_pin + htr):
+                        cs.wait_event(ev_used[b])
+                    for dst, src in zip(dev_tr[b], htr):
                         dst.copy_(src, non_blocking=True)
                 plans[i] = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P,
                                   cfg.order, cfg.chunk_tokens, stream=cs,
@@ -498,6 +505,7 @@ def run_marble(args, rank, world, local, dist):
                 b = i % 2
                 p2 = plans[i]
                 comp.wait_event(ev_plan[b])
+                comp.wait_event(ev_in[b])
                 q2, k2, v2, do2 = [p2.permute(t) for t in dev_in[b]] + ([] if with_bwd else [None])
                 M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
                 if with_bwd:

@@ -83,9 +83,10 @@ struct BwdParams {
   // across them; the dS^T tile of q block nq lands at ds_base[nq / bps] + (its index in the
   // step's numbering) * hq + head
   int ring_s0, ring_len;
-  // whole rows (whole != 0): the dK/dV kernel stores the dS^T tile of row-list entry e (the
-  // plan's row lists, every kv shard) of a q block of shard r at slot ds_base[r] + e * hq +
-  // head, and the dQ kernel runs one unit per (q block, q head) over the block's whole row
+  // whole rows (whole != 0; 2: the dQ GEMM over every q block): the dK/dV kernel stores the
+  // dS^T tile of row-list entry e (the plan's row lists, every kv shard) of a q block of shard
+  // r at slot ds_base[r] + e * hq + head, and the dQ kernel runs one unit per (q block, q head)
+  // over the block's whole row
   int whole;
   long long ds_base[kMaxShards];
   unsigned* sched;           // ticket counter pair of the launch
@@ -129,8 +130,16 @@ __device__ __forceinline__ void dq_unit(const BwdParams& p, unsigned t, int* h, 
                                         int64_t* e0, int* T) {
   int64_t nq, a, b;
   if (p.whole) {
-    *h = (int)(t % (unsigned)p.hq);
-    nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
+    // over every q block of the pack (whole == 2) the q heads go outermost, so that the units
+    // in flight read one head's K from L2; per q shard they go innermost
+    if (p.whole == 2) {
+      const unsigned nbk = (unsigned)(p.nwork / p.hq);
+      *h = (int)(t / nbk);
+      nq = p.order[t % nbk];
+    } else {
+      *h = (int)(t % (unsigned)p.hq);
+      nq = (int64_t)p.q_shard * p.bps + p.order[t / (unsigned)p.hq];
+    }
     *blk = (int)nq;
     *e0 = p.step_ptr[nq * p.P];
     *T = (int)(p.step_ptr[nq * p.P + p.P] - *e0);
@@ -1126,6 +1135,7 @@ void launch_dq_whole(const marble_plan_t* pl, const BwdParams& prm, int q_shard,
   pq.kv_shard = -1;
   pq.ring_len = 0;
   if (q_shard < 0) {
+    pq.whole = 2;
     pq.q_shard = 0;
     pq.order = pl->fwd_order_all;
     pq.nwork = pl->h_fwd_nwork_all * hq;
