@@ -436,6 +436,12 @@ def run_marble(args, rank, world, local, dist):
     th = time_call(lambda: pl.permute(q, out=qp))
     by = 2 * n * hq * d * 2
     helpers["permute_q"] = {"ms": th, "bytes": by, "gbs": by / th / 1e6}
+    if with_bwd:
+        dq_bf = torch.empty((n, hq, d), dtype=torch.bfloat16, device="cuda")
+        th = time_call(lambda: pl.permute_cast_bf16(dq, inverse=True, out=dq_bf))
+        by = n * hq * d * (4 + 2)
+        helpers["permute_cast_dq"] = {"ms": th, "bytes": by, "gbs": by / th / 1e6}
+        del dq_bf
     plan_bytes = n * (12 + 4 + 16) + 3 * 5 * stats["nnz"]
     helpers["plan"] = {"ms": min(plan_ms), "bytes": plan_bytes,
                        "gbs": plan_bytes / min(plan_ms) / 1e6,
@@ -448,12 +454,13 @@ def run_marble(args, rank, world, local, dist):
     helpers["hbm_peak_gbs"] = hbm
 
     # end to end through the public API: H2D of the step's inputs from pinned memory,
-    # plan, permutation, forward, backward, inverse permutation, bf16 cast, D2H results.
-    # Steps are pipelined the way a training loop runs them: the next step's inputs are
-    # copied in on one copy stream and its tracks copied and its plan built on another while
-    # this step computes, and this step's results are copied out on a third while the next
-    # step computes (double-buffered inputs and outputs).  Each plan is destroyed as soon as
-    # its step is queued: the library frees it in stream order, without synchronising.
+    # plan, permutation, forward, backward, inverse permutation (with the bf16 cast of the
+    # gradients), D2H results.  Steps are pipelined the way a training loop runs them: the
+    # next step's inputs are copied in on one copy stream and its tracks copied and its plan
+    # built on another while this step computes, and this step's results are copied out on a
+    # third while the next step computes (double-buffered inputs and outputs; O leaves as
+    # soon as the forward has made it).  Each plan is destroyed as soon as its step is
+    # queued: the library frees it in stream order, without synchronising.
     e2e = None
     if args.e2e_steps > 0:
         hq_pin = [t.cpu().pin_memory() for t in ((q, k, v, do) if with_bwd else (q, k, v))]
@@ -465,8 +472,6 @@ def run_marble(args, rank, world, local, dist):
                 for _ in range(2)]
         dev_in = [[torch.empty_like(t, device="cuda") for t in hq_pin] for _ in range(2)]
         dev_tr = [[torch.empty_like(t, device="cuda") for t in htr] for _ in range(2)]
-        g_tmp = [torch.empty((n, hq, d), dtype=torch.float32, device="cuda"),
-                 torch.empty((n, hkv, d), dtype=torch.float32, device="cuda")]
         cs = torch.cuda.Stream()       # host -> device: tracks, then the plan
         cs_in = torch.cuda.Stream()    # host -> device: Q, K, V, dO
         cs_out = torch.cuda.Stream()   # device -> host (the two directions overlap)
@@ -474,25 +479,28 @@ def run_marble(args, rank, world, local, dist):
 
         def e2e_run(K):
             plans = [None] * K
-            ev_in, ev_used, ev_out, ev_d2h, ev_plan = ([torch.cuda.Event() for _ in range(2)]
-                                                       for _ in range(5))
+            ev_qkv, ev_do, ev_used, ev_o, ev_out, ev_d2h, ev_plan = (
+                [torch.cuda.Event() for _ in range(2)] for _ in range(7))
 
             def h2d_and_plan(i):
-                # the step's Q/K/V/dO on one copy stream; its tracks, then its plan, on another:
-                # the planner's own synchronisation waits for the small track copy only, not for
-                # the inputs' copy nor for the previous step's compute
+                # the step's tracks, then its plan, on one copy stream; its Q/K/V (then dO) on
+                # another.  The tracks go first, so that the planner's own synchronisation
+                # waits for their small copy only, not for the inputs' copy nor for the
+                # previous step's compute.
                 b = i % 2
-                with torch.cuda.stream(cs_in):
-                    if i >= 2:
-                        cs_in.wait_event(ev_used[b])   # step i - 2 is done with buffer b
-                    for dst, src in zip(dev_in[b], hq_pin):
-                        dst.copy_(src, non_blocking=True)
-                    ev_in[b].record(cs_in)
                 with torch.cuda.stream(cs):
                     if i >= 2:
-                        cs.wait_event(ev_used[b])
+                        cs.wait_event(ev_used[b])   # step i - 2 is done with buffer b
                     for dst, src in zip(dev_tr[b], htr):
                         dst.copy_(src, non_blocking=True)
+                with torch.cuda.stream(cs_in):
+                    if i >= 2:
+                        cs_in.wait_event(ev_used[b])
+                    for j, (dst, src) in enumerate(zip(dev_in[b], hq_pin)):
+                        dst.copy_(src, non_blocking=True)
+                        if j == 2:
+                            ev_qkv[b].record(cs_in)  # the forward needs Q, K and V only
+                    ev_do[b].record(cs_in)
                 plans[i] = M.Plan(dev_tr[b][0], dev_tr[b][1], dev_tr[b][2], cfg.window, P,
                                   cfg.order, cfg.chunk_tokens, stream=cs,
                                   range_cost=cfg.range_cost,
@@ -500,42 +508,50 @@ def run_marble(args, rank, world, local, dist):
                                   pos=dev_tr[b][3] if pos_t is not None else None)
                 ev_plan[b].record(cs)
 
+            def d2h(ev_ready, pairs, ev_done=None):
+                with torch.cuda.stream(cs_out):
+                    cs_out.wait_event(ev_ready)
+                    for dst, src in pairs:
+                        dst.copy_(src, non_blocking=True)
+                    if ev_done is not None:
+                        ev_done.record(cs_out)
+
             h2d_and_plan(0)
             for i in range(K):
                 b = i % 2
                 p2 = plans[i]
+                ob = outs[b]
                 comp.wait_event(ev_plan[b])
-                comp.wait_event(ev_in[b])
-                q2, k2, v2, do2 = [p2.permute(t) for t in dev_in[b]] + ([] if with_bwd else [None])
+                comp.wait_event(ev_qkv[b])
+                q2, k2, v2 = [p2.permute(t) for t in dev_in[b][:3]]
                 M.forward(p2, q2, k2, v2, st, o, lse, needed=needed)
+                if i >= 2:
+                    comp.wait_event(ev_d2h[b])      # step i - 2's results have left buffer b
+                p2.permute(o, inverse=True, out=ob[0])
+                ev_o[b].record(comp)
                 if with_bwd:
+                    d2h(ev_o[b], [(out_pin[b][0], ob[0])])   # O leaves while dK/dV run
+                    comp.wait_event(ev_do[b])
+                    do2 = p2.permute(dev_in[b][3])
                     dq.zero_()
                     dk.zero_()
                     dv.zero_()
                     M.backward(p2, q2, k2, v2, o, do2, lse, delta, dq, dk, dv, needed=needed)
                 ev_used[b].record(comp)
-                if i >= 2:
-                    comp.wait_event(ev_d2h[b])      # step i - 2's results have left buffer b
-                ob = outs[b]
-                p2.permute(o, inverse=True, out=ob[0])
                 if with_bwd:
-                    for g_, t_, b_ in ((dq, g_tmp[0], ob[1]), (dk, g_tmp[1], ob[2]),
-                                       (dv, g_tmp[1], ob[3])):
-                        p2.permute(g_, inverse=True, out=t_)
-                        M.cast_bf16(t_, b_)
+                    for g_, b_ in ((dq, ob[1]), (dk, ob[2]), (dv, ob[3])):
+                        p2.permute_cast_bf16(g_, inverse=True, out=b_)
                 ev_out[b].record(comp)
-                with torch.cuda.stream(cs_out):
-                    cs_out.wait_event(ev_out[b])
-                    for dst, src in zip(out_pin[b], ob):
-                        dst.copy_(src, non_blocking=True)
-                    ev_d2h[b].record(cs_out)
+                pairs = list(zip(out_pin[b], ob))
+                d2h(ev_out[b], pairs[1:] if with_bwd else pairs, ev_d2h[b])
                 p2.close()                          # stream-ordered: no synchronisation
                 plans[i] = None
                 if i + 1 < K:
                     h2d_and_plan(i + 1)             # while step i computes
             torch.cuda.synchronize()
 
-        e2e_run(1)
+        # warm-up long enough for the memory pool to hold the plans of the steps in flight
+        e2e_run(max(4, args.warmup))
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_run(args.e2e_steps)
@@ -546,7 +562,8 @@ def run_marble(args, rank, world, local, dist):
                "h2d_bytes_per_step": h2d_b, "d2h_bytes_per_step": d2h_b,
                "ms_per_step": 1e3 * e2e_s, "includes": "H2D inputs+tracks, marble_plan, "
                "permute, fwd, finalize, " + ("bwd_prep, bwd, " if with_bwd else "") +
-               "inverse permute, " + ("bf16 cast, " if with_bwd else "") + "D2H, plan "
+               "inverse permute" + (" (gradients: fused with the bf16 cast)" if with_bwd
+                                    else "") + ", D2H, plan "
                "teardown; steps pipelined (copies and the next step's plan on copy streams "
                "overlap compute)"}
 
@@ -784,7 +801,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="marble", choices=["marble", "reference"])
     ap.add_argument("--config", type=int, default=2)
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for cpu_baseline (0 disables)")
     ap.add_argument("--ref-budget", type=float, default=5.0,

@@ -87,6 +87,8 @@ _SIGS = {
                             ctypes.c_void_p]),
     "marble_permute": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                         ctypes.c_int32, ctypes.c_void_p]),
+    "marble_permute_cast_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                  ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]),
     "marble_attn_step": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_int32, ctypes.c_int32,
                           ctypes.POINTER(_State), ctypes.c_uint32, ctypes.c_void_p]),
     "marble_attn_finalize": ([ctypes.c_void_p, ctypes.POINTER(_State), ctypes.c_int32,
@@ -239,6 +241,18 @@ class Plan:
         row_bytes = src.numel() // self.n * src.element_size()
         _call("marble_permute", self._h, _ptr(src), _ptr(out), row_bytes, 1 if inverse else 0,
               _stream(stream))
+        return out
+
+    def permute_cast_bf16(self, src, inverse: bool = True, out=None, stream=None):
+        """permute() of an fp32 tensor, written as bf16 (round to nearest even)."""
+        import torch
+        _need(src, torch.float32, "src")
+        if src.shape[0] != self.n:
+            raise ValueError("src must have N rows")
+        out = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device) if out is None else out
+        _need(out, torch.bfloat16, "out", src.shape)
+        _call("marble_permute_cast_bf16", self._h, _ptr(src), _ptr(out), src.numel() // self.n,
+              1 if inverse else 0, _stream(stream))
         return out
 
     def check(self, stream=None):

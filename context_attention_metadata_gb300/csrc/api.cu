@@ -524,6 +524,27 @@ MARBLE_API marble_status_t marble_permute(const marble_plan_t* p, const void* sr
   return MARBLE_OK;
 }
 
+MARBLE_API marble_status_t marble_permute_cast_bf16(const marble_plan_t* p, const float* src,
+                                                    void* dst, int64_t row_elems,
+                                                    int32_t inverse, marble_stream_t stream) {
+  NvtxRange nvtx_("marble_permute_cast_bf16");
+  if (!p) return fail(MARBLE_ERR_INVALID_ARG, "plan is null");
+  if (row_elems <= 0 || row_elems % 4)
+    return fail(MARBLE_ERR_INVALID_ARG, "row_elems must be a positive multiple of 4");
+  marble_status_t st;
+  if ((st = check_tensor(src, "src")) != MARBLE_OK) return st;
+  if ((st = check_tensor(dst, "dst")) != MARBLE_OK) return st;
+  const char* a = reinterpret_cast<const char*>(src);
+  const char* b = static_cast<const char*>(dst);
+  if (a < b + p->n * row_elems * 2 && b < a + p->n * row_elems * 4)
+    return fail(MARBLE_ERR_INVALID_ARG, "src and dst overlap");
+  cudaError_t e = launch_permute_cast_bf16(p, src, dst, row_elems, inverse ? 1 : 0,
+                                           (cudaStream_t)stream);
+  plan_used(p, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "marble_permute_cast_bf16 launch");
+  return MARBLE_OK;
+}
+
 constexpr uint32_t kMergeBits = MARBLE_STEP_BF16_MERGE | MARBLE_STEP_FP32_MERGE;
 
 // known bits only, and at most one merge variant

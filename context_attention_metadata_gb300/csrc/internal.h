@@ -149,6 +149,8 @@ marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t
 // elementwise kernels (misc.cu)
 cudaError_t launch_permute(const marble_plan_t* p, const void* src, void* dst, int64_t row_bytes,
                            int inverse, cudaStream_t s);
+cudaError_t launch_permute_cast_bf16(const marble_plan_t* p, const float* src, void* dst,
+                                     int64_t row_elems, int inverse, cudaStream_t s);
 cudaError_t launch_cast_bf16(const float* src, void* dst, int64_t n, cudaStream_t s);
 cudaError_t launch_finalize(const marble_plan_t* p, const float* o_acc, const float* m,
                             const float* l, int hq, int d, void* o, float* lse, cudaStream_t s);

@@ -10,18 +10,41 @@
 namespace marble {
 namespace {
 
-// dst row i <- src row perm[i]  (inverse: dst row perm[i] <- src row i), 16-byte chunks
-__global__ void k_permute16(const int32_t* __restrict__ perm, const uint4* __restrict__ src,
-                            uint4* __restrict__ dst, int64_t n, int64_t chunks, int inverse) {
-  const int64_t total = n * chunks;
-  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < total;
-       x += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = x / chunks, c = x % chunks;
-    const int64_t o = perm[r];
-    if (inverse)
-      dst[o * chunks + c] = src[r * chunks + c];
-    else
-      dst[r * chunks + c] = src[o * chunks + c];
+// dst row i <- src row perm[i]  (inverse: dst row perm[i] <- src row i), rows of `chunks`
+// 16-byte chunks.  A block moves kRows rows at a time, so that each thread has kRows loads in
+// flight before its first store.  CAST: a source chunk is 4 fp32, written as 4 bf16 (round
+// to nearest even) into rows of `chunks` 8-byte chunks.
+constexpr int kRows = 4;
+
+template <bool CAST>
+__global__ void k_permute_rows(const int32_t* __restrict__ perm, const uint4* __restrict__ src,
+                               void* __restrict__ dst, int64_t n, int chunks, int inverse) {
+  for (int64_t r0 = (int64_t)blockIdx.x * kRows; r0 < n; r0 += (int64_t)gridDim.x * kRows) {
+    int64_t from[kRows], to[kRows];
+#pragma unroll
+    for (int j = 0; j < kRows; ++j) {
+      const int64_t r = r0 + j < n ? r0 + j : r0;
+      const int64_t o = perm[r];
+      from[j] = inverse ? r : o;
+      to[j] = inverse ? o : r;
+    }
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      uint4 v[kRows];
+#pragma unroll
+      for (int j = 0; j < kRows; ++j)
+        if (r0 + j < n) v[j] = src[from[j] * chunks + c];
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        if (r0 + j >= n) continue;
+        if constexpr (CAST) {
+          const float4 f = *reinterpret_cast<const float4*>(&v[j]);
+          static_cast<uint2*>(dst)[to[j] * chunks + c] =
+              make_uint2(pack_bf16(f.x, f.y), pack_bf16(f.z, f.w));
+        } else {
+          static_cast<uint4*>(dst)[to[j] * chunks + c] = v[j];
+        }
+      }
+    }
   }
 }
 
@@ -140,18 +163,31 @@ unsigned grid_exact(int64_t items, int threads) {
 
 }  // namespace
 
+// threads per block of k_permute_rows: one 16-byte chunk each, up to 256
+static int row_threads(int64_t chunks) {
+  return chunks >= 256 ? 256 : (int)((chunks + 31) / 32 * 32);
+}
+
 cudaError_t launch_permute(const marble_plan_t* p, const void* src, void* dst, int64_t row_bytes,
                            int inverse, cudaStream_t s) {
   if (row_bytes % 16 == 0) {
     const int64_t chunks = row_bytes / 16;
-    k_permute16<<<grid_of(p->n * chunks, 256), 256, 0, s>>>(
-        p->perm, static_cast<const uint4*>(src), static_cast<uint4*>(dst), p->n, chunks, inverse);
+    k_permute_rows<false><<<grid_of(p->n, kRows), row_threads(chunks), 0, s>>>(
+        p->perm, static_cast<const uint4*>(src), dst, p->n, (int)chunks, inverse);
   } else {
     const int64_t words = row_bytes / 4;
     k_permute4<<<grid_of(p->n * words, 256), 256, 0, s>>>(
         p->perm, static_cast<const uint32_t*>(src), static_cast<uint32_t*>(dst), p->n, words,
         inverse);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_cast_bf16(const marble_plan_t* p, const float* src, void* dst,
+                                     int64_t row_elems, int inverse, cudaStream_t s) {
+  const int64_t chunks = row_elems / 4;
+  k_permute_rows<true><<<grid_of(p->n, kRows), row_threads(chunks), 0, s>>>(
+      p->perm, reinterpret_cast<const uint4*>(src), dst, p->n, (int)chunks, inverse);
   return cudaGetLastError();
 }
 

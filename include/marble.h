@@ -264,6 +264,20 @@ marble_status_t marble_plan_export(const marble_plan_t *plan, int32_t field, voi
 marble_status_t marble_permute(const marble_plan_t *plan, const void *src, void *dst,
                                int64_t row_bytes, int32_t inverse, marble_stream_t stream);
 
+/*
+ * marble_permute fused with the fp32 -> bf16 cast of marble_cast_bf16, for fp32 results
+ * that leave plan order as bf16 (the gradient accumulators): inverse = 1 writes
+ * dst[perm[i]] = bf16(src[i]), inverse = 0 writes dst[i] = bf16(src[perm[i]]), rows of
+ * `row_elems` elements, each rounded to nearest even (MARBLE s04 "Layout transforms").
+ * src: device fp32 [N, row_elems]; dst: device bf16 [N, row_elems]; the two must not
+ * overlap.  row_elems must be a positive multiple of 4 and both pointers 16-byte aligned.
+ * Errors: INVALID_ARG for a null plan, a bad row_elems, a pointer that is not device
+ * memory or not aligned, or overlapping buffers; CUDA if the launch fails.
+ */
+marble_status_t marble_permute_cast_bf16(const marble_plan_t *plan, const float *src,
+                                         void *dst, int64_t row_elems, int32_t inverse,
+                                         marble_stream_t stream);
+
 /* Queries, keys and values in plan order (layouts above). scale <= 0 selects 1/sqrt(d)
  * (LIBRA Eq. 1). */
 typedef struct {

@@ -49,6 +49,8 @@ def test_host_side_argument_checks(libm):
     assert libm.marble_plan_destroy(None) == M.OK
     assert libm.marble_check(None, None) == M.ERR_INVALID_ARG
     assert libm.marble_cast_bf16(None, None, 3, None) == M.ERR_INVALID_ARG
+    assert libm.marble_permute_cast_bf16(None, None, None, 4, 1, None) == M.ERR_INVALID_ARG
+    assert b"plan is null" in libm.marble_last_error()
     d = M._PlanDesc(1000, 0, 0, 0, 0, 1, 0, 0)  # not a multiple of 128
     h = ctypes.c_void_p()
     assert libm.marble_plan(ctypes.byref(d), None, ctypes.byref(h)) == M.ERR_INVALID_ARG
