@@ -486,16 +486,15 @@ def run_marble(args, rank, world, local, dist):
                 # the step's tracks, then its plan, on one copy stream; its Q/K/V (then dO) on
                 # another.  The tracks go first, so that the planner's own synchronisation
                 # waits for their small copy only, not for the inputs' copy nor for the
-                # previous step's compute.
+                # previous step's compute.  marble_plan has read its tracks when it returns,
+                # so their buffer is free again at once.
                 b = i % 2
                 with torch.cuda.stream(cs):
-                    if i >= 2:
-                        cs.wait_event(ev_used[b])   # step i - 2 is done with buffer b
                     for dst, src in zip(dev_tr[b], htr):
                         dst.copy_(src, non_blocking=True)
                 with torch.cuda.stream(cs_in):
                     if i >= 2:
-                        cs_in.wait_event(ev_used[b])
+                        cs_in.wait_event(ev_used[b])   # step i - 2 is done with buffer b
                     for j, (dst, src) in enumerate(zip(dev_in[b], hq_pin)):
                         dst.copy_(src, non_blocking=True)
                         if j == 2:
@@ -550,8 +549,9 @@ def run_marble(args, rank, world, local, dist):
                     h2d_and_plan(i + 1)             # while step i computes
             torch.cuda.synchronize()
 
-        # warm-up long enough for the memory pool to hold the plans of the steps in flight
-        e2e_run(max(4, args.warmup))
+        # warm-up as long as the timed run, so that the memory pool already holds the
+        # workspaces of the plans in flight
+        e2e_run(max(4, args.warmup, args.e2e_steps))
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_run(args.e2e_steps)

@@ -157,8 +157,9 @@ typedef struct marble_plan marble_plan_t; /* opaque; immutable after creation */
  * token order (contiguous or PTRR); permuted tracks; per (q block, kv shard) tile lists
  * for the forward and dQ, per (kv block, q shard) lists for dK/dV, and the needed-KV
  * block index of every q shard.
- * Synchronises `stream` a few times (to size its arrays).  On success *out owns device
- * memory until marble_plan_destroy.  Errors: INVALID_ARG (descriptor or metadata),
+ * Synchronises `stream` a few times (to size its arrays), the last time after its last
+ * kernel: the tracks are read only during the call, and their buffers may be reused as soon
+ * as it returns.  On success *out owns device memory until marble_plan_destroy.  Errors: INVALID_ARG (descriptor or metadata),
  * UNSUPPORTED, OOM, CUDA.
  */
 marble_status_t marble_plan(const marble_plan_desc_t *desc, marble_stream_t stream,
