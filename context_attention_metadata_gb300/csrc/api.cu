@@ -183,6 +183,68 @@ static cudaStream_t teardown_stream() {
   return st;
 }
 
+// cached dS^T scratch buffers per device: at most kScratchKept; a buffer put beyond that
+// goes back to the pool, in stream order after its last use
+namespace {
+constexpr size_t kScratchKept = 2;
+struct CachedScratch {
+  void* ptr;
+  size_t bytes;
+  cudaEvent_t ready;
+};
+std::mutex g_scratch_mu;
+std::map<int, std::vector<CachedScratch>> g_scratch;
+}  // namespace
+
+void scratch_put(int device, void* ptr, size_t bytes, cudaEvent_t ready) {
+  std::vector<CachedScratch> drop;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    auto& v = g_scratch[device];
+    v.push_back({ptr, bytes, ready});
+    while (v.size() > kScratchKept) {
+      drop.push_back(v.front());
+      v.erase(v.begin());
+    }
+  }
+  for (auto& c : drop) {
+    cudaStream_t fs = teardown_stream();
+    if (fs && cudaStreamWaitEvent(fs, c.ready, 0) == cudaSuccess) dev_free(c.ptr, fs);
+    cudaEventDestroy(c.ready);
+  }
+}
+
+void* scratch_take(size_t bytes, cudaStream_t s, size_t* got) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  CachedScratch c{nullptr, 0, nullptr};
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    auto it = g_scratch.find(dev);
+    if (it == g_scratch.end()) return nullptr;
+    auto& v = it->second;
+    for (size_t i = 0; i < v.size(); ++i) {
+      if (v[i].bytes >= bytes) {
+        c = v[i];
+        v.erase(v.begin() + (long)i);
+        break;
+      }
+    }
+  }
+  if (!c.ptr) return nullptr;
+  if (cudaStreamWaitEvent(s, c.ready, 0) != cudaSuccess) {
+    // not usable on this stream: back to the pool after its last use
+    (void)cudaGetLastError();
+    cudaStream_t fs = teardown_stream();
+    if (fs && cudaStreamWaitEvent(fs, c.ready, 0) == cudaSuccess) dev_free(c.ptr, fs);
+    cudaEventDestroy(c.ready);
+    return nullptr;
+  }
+  cudaEventDestroy(c.ready);  // released once the wait above has been satisfied
+  *got = c.bytes;
+  return c.ptr;
+}
+
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
   cudaEvent_t e;
   cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -321,7 +383,17 @@ MARBLE_API marble_status_t marble_plan_destroy(marble_plan_t* p) {
       if (err == cudaSuccess) err = e;
     }
     if (p->ds_scratch) {
-      const cudaError_t e = dev_free(p->ds_scratch, fs);
+      // the dS^T scratch goes to the cache for the next plan's backward, ready once the
+      // teardown stream has passed the plan's last uses
+      cudaEvent_t ready = nullptr;
+      cudaError_t e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventRecord(ready, fs);
+      if (e == cudaSuccess) {
+        scratch_put(p->device, p->ds_scratch, p->ds_scratch_bytes, ready);
+      } else {
+        if (ready) cudaEventDestroy(ready);
+        e = dev_free(p->ds_scratch, fs);
+      }
       if (err == cudaSuccess) err = e;
     }
   }

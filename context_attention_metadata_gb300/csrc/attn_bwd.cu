@@ -1070,14 +1070,15 @@ marble_status_t ds_scratch(const marble_plan_t* pl, size_t slots, cudaStream_t s
       pl->ds_scratch = nullptr;
       pl->ds_scratch_bytes = 0;
     }
-    void* q = nullptr;
-    if (dev_alloc(&q, need, s) != cudaSuccess) {
+    size_t got = need;
+    void* q = scratch_take(need, s, &got);
+    if (!q && dev_alloc(&q, need, s) != cudaSuccess) {
       (void)cudaGetLastError();
       return fail(MARBLE_ERR_OOM, "allocation of the backward dS scratch failed (" +
                                       std::to_string(need) + " bytes)");
     }
     pl->ds_scratch = q;
-    pl->ds_scratch_bytes = need;
+    pl->ds_scratch_bytes = got;
   }
   if (slots > 0 && !make_rows_map(&prm->ds_map, pl->ds_scratch, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                                   2, (int64_t)slots * 128, 1, 128, 64, 128,

@@ -135,6 +135,15 @@ bool is_device_ptr(const void* p);
 // launches work on a plan's memory records it before returning
 void plan_used(const marble_plan_t* p, cudaStream_t s);
 
+// dS^T scratch buffers of destroyed plans, kept per device for the next plans' backward calls
+// (api.cu).  scratch_put hands over a buffer whose last use completes with `ready` (the cache
+// owns the event); scratch_take returns a cached buffer of at least `bytes` bytes (the oldest
+// that fits) after making `s` wait for its `ready`, or nullptr.  A buffer reused this way
+// stays with the stream order of its previous owner, where a new pool allocation on another
+// stream would make the pool map fresh memory while the old buffer's free is still queued.
+void scratch_put(int device, void* ptr, size_t bytes, cudaEvent_t ready);
+void* scratch_take(size_t bytes, cudaStream_t s, size_t* got);
+
 // error reporting (api.cu)
 void set_error(const std::string& msg);
 marble_status_t fail(marble_status_t st, const std::string& msg);

@@ -24,7 +24,8 @@
  *     argument returns MARBLE_ERR_INVALID_ARG and launches nothing.
  *   - The caller owns every tensor it passes.  A plan owns only its own device
  *     workspace: allocated by marble_plan, grown by the backward calls for their scratch
- *     of bf16 dS tiles, and freed by marble_plan_destroy.  This memory comes from a
+ *     of bf16 dS tiles, and freed by marble_plan_destroy (which keeps up to two dS
+ *     scratch buffers per device for later plans).  This memory comes from a
  *     stream-ordered pool the library keeps per device.  No call allocates memory that
  *     the caller sees.
  *   - No C++ exception crosses this boundary.  marble_last_error() returns a
@@ -168,8 +169,11 @@ marble_status_t marble_plan(const marble_plan_desc_t *desc, marble_stream_t stre
 /* Frees the plan without synchronising: the workspace returns to the library's memory
  * pool in stream order, once the work of every earlier call that used the plan has
  * completed, on whatever streams those calls ran; the plan handle is invalid as soon as
- * the call returns.  NULL is accepted.  Errors: CUDA (the plan is freed on the host all
- * the same). */
+ * the call returns.  The backward's dS^T scratch is kept instead for the backward calls of
+ * later plans on the device (at most two such buffers; the stream of the call that takes
+ * one waits for the last use by its previous plan), so that a training loop with one plan
+ * per batch does not have the pool map a new scratch for every batch.  NULL is accepted.
+ * Errors: CUDA (the plan is freed on the host all the same). */
 marble_status_t marble_plan_destroy(marble_plan_t *plan);
 
 typedef struct {
