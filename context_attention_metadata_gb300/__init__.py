@@ -16,6 +16,14 @@ import ctypes
 import os
 from typing import Dict, Optional
 
+# The library queues work on up to five streams of its own (four side streams and a teardown
+# stream) beside the caller's.  With CUDA's default of 8 hardware work queues, streams share
+# queues, and work on one waits behind unrelated work on another: in a training loop the
+# input and output copies then wait for the attention kernels.  More queues are asked for
+# here, before the CUDA context exists, unless the caller chose a value; it has no effect if
+# the process created its CUDA context before importing this module.
+os.environ.setdefault("CUDA_DEVICE_MAX_CONNECTIONS", "32")
+
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_lib", "libmarble.so")
 

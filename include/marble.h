@@ -30,6 +30,12 @@
  *     the caller sees.
  *   - No C++ exception crosses this boundary.  marble_last_error() returns a
  *     thread-local, human-readable message for the last failing call on this thread.
+ *   - The step-list and fused calls spread launches over up to four side streams of the
+ *     library, and plans are freed on a library stream.  With CUDA's default of 8 hardware
+ *     work queues (CUDA_DEVICE_MAX_CONNECTIONS) these share queues with the caller's
+ *     streams, so that a caller's copy can wait behind unrelated attention kernels; set
+ *     CUDA_DEVICE_MAX_CONNECTIONS=32 before the process creates its CUDA context (the
+ *     Python binding does so at import unless the variable is set).
  *   - Every wait inside a kernel is bounded in time; a wait that runs out sets an error
  *     word owned by the plan and the kernel returns.  marble_check() reports it as
  *     MARBLE_ERR_TIMEOUT.  Asynchronous CUDA faults surface as MARBLE_ERR_CUDA.
