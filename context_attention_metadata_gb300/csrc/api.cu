@@ -245,6 +245,65 @@ void* scratch_take(size_t bytes, cudaStream_t s, size_t* got) {
   return c.ptr;
 }
 
+// the calling thread's pinned staging buffer, grown to at least `bytes`
+static void* pinned_stage(size_t bytes, cudaError_t* err) {
+  thread_local void* buf = nullptr;
+  thread_local size_t cap = 0;
+  if (bytes > cap) {
+    size_t want = cap ? cap : 4096;
+    while (want < bytes) want *= 2;
+    void* q = nullptr;
+    const cudaError_t e = cudaHostAlloc(&q, want, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      *err = e;
+      return nullptr;
+    }
+    if (buf) cudaFreeHost(buf);
+    buf = q;
+    cap = want;
+  }
+  *err = cudaSuccess;
+  return buf;
+}
+
+static size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
+
+cudaError_t read_back(cudaStream_t s, std::initializer_list<HostPart> parts) {
+  size_t total = 0;
+  for (const HostPart& h : parts) total += round16(h.bytes);
+  cudaError_t e = cudaSuccess;
+  uint8_t* stage = static_cast<uint8_t*>(pinned_stage(total, &e));
+  if (!stage) return e;
+  size_t off = 0;
+  for (const HostPart& h : parts) {
+    if (h.bytes) {
+      e = cudaMemcpyAsync(stage + off, h.dev, h.bytes, cudaMemcpyDeviceToHost, s);
+      if (e != cudaSuccess) return e;
+    }
+    off += round16(h.bytes);
+  }
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  off = 0;
+  for (const HostPart& h : parts) {
+    if (h.bytes) memcpy(h.host, stage + off, h.bytes);
+    off += round16(h.bytes);
+  }
+  return cudaSuccess;
+}
+
+cudaError_t write_to_device(cudaStream_t s, void* dev, const void* host, size_t bytes) {
+  if (!bytes) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  void* stage = pinned_stage(bytes, &e);
+  if (!stage) return e;
+  // every user of the buffer synchronises its stream before returning: no copy still reads it
+  memcpy(stage, host, bytes);
+  e = cudaMemcpyAsync(dev, stage, bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaStreamSynchronize(s);
+}
+
 cudaError_t stream_fork(cudaStream_t from, cudaStream_t to) {
   cudaEvent_t e;
   cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
@@ -488,12 +547,9 @@ MARBLE_API marble_status_t marble_plan_stats(const marble_plan_t* p, marble_stre
   std::vector<int64_t> ptr(np);
   std::vector<int64_t> nptr(p->P + 1);
   std::vector<int32_t> needed(p->needed_total);
-  cudaError_t e = cudaMemcpyAsync(ptr.data(), p->step_ptr, np * 8, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(nptr.data(), p->needed_ptr, (p->P + 1) * 8, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess && p->needed_total)
-    e = cudaMemcpyAsync(needed.data(), p->needed, p->needed_total * 4, cudaMemcpyDeviceToHost, s);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  const cudaError_t e = read_back(s, {{ptr.data(), p->step_ptr, (size_t)np * 8},
+                                      {nptr.data(), p->needed_ptr, (size_t)(p->P + 1) * 8},
+                                      {needed.data(), p->needed, (size_t)p->needed_total * 4}});
   if (e != cudaSuccess) return cuda_fail(e, "marble_plan_stats copies");
   const int P = p->P;
   std::vector<int64_t> W((size_t)P * P, 0);
@@ -821,7 +877,7 @@ MARBLE_API marble_status_t marble_check(const marble_plan_t* p, marble_stream_t 
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "asynchronous CUDA error");
   unsigned h = 0;
-  e = cudaMemcpy(&h, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+  e = read_back((cudaStream_t)stream, {{&h, p->err, sizeof(unsigned)}});
   if (e != cudaSuccess) return cuda_fail(e, "reading the plan's error word");
   if (h) {
     e = cudaMemset(p->err, 0, sizeof(unsigned));

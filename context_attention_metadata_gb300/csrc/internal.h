@@ -5,6 +5,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <initializer_list>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -134,6 +135,22 @@ bool is_device_ptr(const void* p);
 // record that work using plan `p` has been queued on `s` (api.cu); every call that
 // launches work on a plan's memory records it before returning
 void plan_used(const marble_plan_t* p, cudaStream_t s);
+
+// Small transfers between the device and pageable host memory (the planner's sizes and
+// work counts, the error word, statistics) go through a pinned buffer of the calling thread
+// (api.cu).  A copy to or from pageable memory is carried out by the copy engines on pages
+// the driver has to resolve on the fly, and a training loop's large input and output copies
+// then wait behind it; pinned memory needs no such step.  read_back queues a copy of every
+// part into the buffer on `s`, synchronises `s` and copies the parts out; write_to_device
+// copies `bytes` from `host` into the buffer, queues the copy to `dev` on `s` and
+// synchronises `s`.  The buffer grows as needed and lives as long as the thread.
+struct HostPart {
+  void* host;
+  const void* dev;
+  size_t bytes;
+};
+cudaError_t read_back(cudaStream_t s, std::initializer_list<HostPart> parts);
+cudaError_t write_to_device(cudaStream_t s, void* dev, const void* host, size_t bytes);
 
 // dS^T scratch buffers of destroyed plans, kept per device for the next plans' backward calls
 // (api.cu).  scratch_put hands over a buffer whose last use completes with `ready` (the cache

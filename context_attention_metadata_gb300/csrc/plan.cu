@@ -1226,8 +1226,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
                                                       d->pos_id, nb, p->summ, p->err);
   MARBLE_CK(cudaGetLastError());
   unsigned herr = 0;
-  MARBLE_CK(cudaMemcpyAsync(&herr, p->err, sizeof(unsigned), cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
+  MARBLE_CK(read_back(s, {{&herr, p->err, sizeof(unsigned)}}));
   if (herr & kErrBadTracks)
     return fail(MARBLE_ERR_INVALID_ARG,
                 "metadata check failed: sample ids must be >= 0 and non-decreasing, seg and "
@@ -1239,8 +1238,7 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   k_scan<int32_t><<<1, 1024, 0, s>>>(cnt, nb, p->row_ptr);
   MARBLE_CK(cudaGetLastError());
   int64_t nnz = 0;
-  MARBLE_CK(cudaMemcpyAsync(&nnz, p->row_ptr + nb, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
+  MARBLE_CK(read_back(s, {{&nnz, p->row_ptr + nb, sizeof(int64_t)}}));
   p->nnz = nnz;
   MARBLE_TRY(dalloc(p, &p->col, nnz));
   MARBLE_TRY(dalloc(p, &p->tag, nnz));
@@ -1276,16 +1274,14 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
                                                           cs, Kf, wc);
     MARBLE_CK(cudaGetLastError());
     std::vector<int64_t> wf((size_t)Kf * Kf);
-    MARBLE_CK(cudaMemcpyAsync(wf.data(), wc, wf.size() * sizeof(int64_t), cudaMemcpyDeviceToHost, s));
-    MARBLE_CK(cudaStreamSynchronize(s));
+    MARBLE_CK(read_back(s, {{wf.data(), wc, wf.size() * sizeof(int64_t)}}));
     const LayoutChoice L = choose_layout(wf, Kf, P, p->range_cost);
     const int K = L.k * P;
     std::vector<int32_t> un(K), seen(P, 0);
     for (int u = 0; u < K; ++u) un[u] = L.rank[u] * L.k + seen[L.rank[u]]++;
-    MARBLE_CK(cudaMemcpyAsync(unit_new, un.data(), K * sizeof(int32_t), cudaMemcpyHostToDevice, s));
+    MARBLE_CK(write_to_device(s, unit_new, un.data(), K * sizeof(int32_t)));
     k_block_perm<<<grid_for(nb, threads), threads, 0, s>>>(unit_new, (int)(nb / K), nb,
                                                             p->block_perm, p->inv_block_perm);
-    MARBLE_CK(cudaStreamSynchronize(s));  // `un` is read before it goes out of scope
     p->chunks_per_rank = L.k;
     p->layout_cost = L.C;
     p->layout_step_cost = L.step;
@@ -1386,14 +1382,10 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
   k_needed<false><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, ncount, nullptr, nullptr);
   k_scan<int32_t><<<1, 1024, 0, s>>>(ncount, P, p->needed_ptr);
   MARBLE_CK(cudaGetLastError());
-  int64_t ntot = 0;
-  MARBLE_CK(cudaMemcpyAsync(&ntot, p->needed_ptr + P, sizeof(int64_t), cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
-  p->needed_total = ntot;
   p->h_needed_ptr.resize(P + 1);
-  MARBLE_CK(cudaMemcpyAsync(p->h_needed_ptr.data(), p->needed_ptr, (P + 1) * sizeof(int64_t),
-                            cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
+  MARBLE_CK(read_back(s, {{p->h_needed_ptr.data(), p->needed_ptr, (P + 1) * sizeof(int64_t)}}));
+  const int64_t ntot = p->h_needed_ptr[P];
+  p->needed_total = ntot;
   MARBLE_TRY(dalloc(p, &p->needed, ntot));
   k_needed<true><<<P, 1024, 0, s>>>(p->colT_ptr, nb, P, nullptr, p->needed_ptr, p->needed);
   MARBLE_CK(cudaGetLastError());
@@ -1416,21 +1408,16 @@ marble_status_t build_plan(const marble_plan_desc_t* d, cudaStream_t s, marble_p
                                                        P, bps, p->ring_col, p->ring_tag);
   k_work_order_all<<<1, 1024, 0, s>>>(p->step_ptr, P, nb, p->fwd_order_all, p->fwd_nwork_all);
   MARBLE_CK(cudaGetLastError());
-  MARBLE_CK(cudaMemcpyAsync(&p->h_fwd_nwork_all, p->fwd_nwork_all, sizeof(int32_t),
-                            cudaMemcpyDeviceToHost, s));
   p->h_fwd_nwork.resize((size_t)P * (P + 1));
   p->h_bwd_nwork.resize((size_t)P * (P + 1));
-  MARBLE_CK(cudaMemcpyAsync(p->h_fwd_nwork.data(), p->fwd_nwork, P * (P + 1) * sizeof(int32_t),
-                            cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaMemcpyAsync(p->h_bwd_nwork.data(), p->bwd_nwork, P * (P + 1) * sizeof(int32_t),
-                            cudaMemcpyDeviceToHost, s));
   p->h_step_tiles.resize((size_t)P * (P + 1));
-  MARBLE_CK(cudaMemcpyAsync(p->h_step_tiles.data(), p->step_tiles, P * (P + 1) * sizeof(int64_t),
-                            cudaMemcpyDeviceToHost, s));
   p->h_step_max.resize((size_t)P * (P + 1));
-  MARBLE_CK(cudaMemcpyAsync(p->h_step_max.data(), p->step_max, P * (P + 1) * sizeof(int64_t),
-                            cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
+  const size_t pp = (size_t)P * (P + 1);
+  MARBLE_CK(read_back(s, {{&p->h_fwd_nwork_all, p->fwd_nwork_all, sizeof(int32_t)},
+                          {p->h_fwd_nwork.data(), p->fwd_nwork, pp * sizeof(int32_t)},
+                          {p->h_bwd_nwork.data(), p->bwd_nwork, pp * sizeof(int32_t)},
+                          {p->h_step_tiles.data(), p->step_tiles, pp * sizeof(int64_t)},
+                          {p->h_step_max.data(), p->step_max, pp * sizeof(int64_t)}}));
   return MARBLE_OK;
 }
 
@@ -1449,10 +1436,8 @@ marble_status_t plan_legal_pairs(const marble_plan_t* p, cudaStream_t s, int64_t
   MARBLE_CK(cudaGetLastError());
   unsigned long long h[3] = {0, 0, 0};
   std::vector<int64_t> w((size_t)p->P * p->P);
-  MARBLE_CK(cudaMemcpyAsync(h, p->counters, sizeof(h), cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaMemcpyAsync(w.data(), p->shard_pairs, w.size() * sizeof(int64_t),
-                            cudaMemcpyDeviceToHost, s));
-  MARBLE_CK(cudaStreamSynchronize(s));
+  MARBLE_CK(read_back(s, {{h, p->counters, sizeof(h)},
+                          {w.data(), p->shard_pairs, w.size() * sizeof(int64_t)}}));
   *step_pairs = layout_step_cost(w, p->P);
   *pairs = (int64_t)h[0];
   *n_full = (int64_t)h[1];
