@@ -26,8 +26,10 @@
  *     workspace: allocated by marble_plan, grown by the backward calls for their scratch
  *     of bf16 dS tiles, and freed by marble_plan_destroy (which keeps up to two dS
  *     scratch buffers per device for later plans).  This memory comes from a
- *     stream-ordered pool the library keeps per device.  No call allocates memory that
- *     the caller sees.
+ *     stream-ordered pool the library keeps per device.  The calls that read sizes or
+ *     status back to the host (marble_plan, marble_plan_stats, marble_check) do so through
+ *     a small pinned host buffer the library keeps per calling thread.  No call allocates
+ *     memory that the caller sees.
  *   - No C++ exception crosses this boundary.  marble_last_error() returns a
  *     thread-local, human-readable message for the last failing call on this thread.
  *   - The step-list and fused calls spread launches over up to four side streams of the
