@@ -223,8 +223,9 @@ void* scratch_take(size_t bytes, cudaStream_t s, size_t* got) {
     auto it = g_scratch.find(dev);
     if (it == g_scratch.end()) return nullptr;
     auto& v = it->second;
+    // the oldest buffer that fits without holding more than twice the need
     for (size_t i = 0; i < v.size(); ++i) {
-      if (v[i].bytes >= bytes) {
+      if (v[i].bytes >= bytes && v[i].bytes / 2 <= bytes) {
         c = v[i];
         v.erase(v.begin() + (long)i);
         break;

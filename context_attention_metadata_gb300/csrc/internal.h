@@ -154,8 +154,8 @@ cudaError_t write_to_device(cudaStream_t s, void* dev, const void* host, size_t 
 
 // dS^T scratch buffers of destroyed plans, kept per device for the next plans' backward calls
 // (api.cu).  scratch_put hands over a buffer whose last use completes with `ready` (the cache
-// owns the event); scratch_take returns a cached buffer of at least `bytes` bytes (the oldest
-// that fits) after making `s` wait for its `ready`, or nullptr.  A buffer reused this way
+// owns the event); scratch_take returns a cached buffer of at least `bytes` bytes and at most
+// twice that (the oldest such) after making `s` wait for its `ready`, or nullptr.  A buffer reused this way
 // stays with the stream order of its previous owner, where a new pool allocation on another
 // stream would make the pool map fresh memory while the old buffer's free is still queued.
 void scratch_put(int device, void* ptr, size_t bytes, cudaEvent_t ready);
