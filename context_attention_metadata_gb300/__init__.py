@@ -97,6 +97,7 @@ _SIGS = {
                         ctypes.c_int32, ctypes.c_void_p]),
     "marble_permute_cast_bf16": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                   ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p]),
+    "marble_release_memory": ([]),
     "marble_attn_step": ([ctypes.c_void_p, ctypes.POINTER(_QKV), ctypes.c_int32, ctypes.c_int32,
                           ctypes.POINTER(_State), ctypes.c_uint32, ctypes.c_void_p]),
     "marble_attn_finalize": ([ctypes.c_void_p, ctypes.POINTER(_State), ctypes.c_int32,
@@ -355,6 +356,12 @@ def cast_bf16(src, dst, stream=None):
 
 def set_wait_limit_ns(ns: int):
     _call("marble_set_wait_limit_ns", int(ns))
+
+
+def release_memory():
+    """Give the memory the library keeps for reuse (cached dS scratch of destroyed plans, the
+    pool's unused blocks) back to the current device."""
+    _call("marble_release_memory")
 
 
 def set_side_streams(n: int):

@@ -897,6 +897,33 @@ MARBLE_API marble_status_t marble_set_side_streams(int32_t n) {
   return MARBLE_OK;
 }
 
+MARBLE_API marble_status_t marble_release_memory(void) {
+  NvtxRange nvtx_("marble_release_memory");
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return cuda_fail(err, "marble_release_memory");
+  std::vector<CachedScratch> drop;
+  {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    auto it = g_scratch.find(dev);
+    if (it != g_scratch.end()) drop.swap(it->second);
+  }
+  cudaStream_t fs = teardown_stream();
+  if (!fs) return cuda_fail(cudaErrorUnknown, "marble_release_memory: teardown stream");
+  for (auto& c : drop) {
+    cudaError_t e = cudaStreamWaitEvent(fs, c.ready, 0);
+    if (e == cudaSuccess) e = dev_free(c.ptr, fs);
+    cudaEventDestroy(c.ready);
+    if (err == cudaSuccess) err = e;
+  }
+  const cudaError_t e = cudaStreamSynchronize(fs);
+  if (err == cudaSuccess) err = e;
+  cudaMemPool_t pool = mem_pool();
+  if (err == cudaSuccess && pool) err = cudaMemPoolTrimTo(pool, 0);
+  if (err != cudaSuccess) return cuda_fail(err, "marble_release_memory");
+  return MARBLE_OK;
+}
+
 MARBLE_API marble_status_t marble_set_wait_limit_ns(uint64_t ns) {
   if (ns == 0) return fail(MARBLE_ERR_INVALID_ARG, "limit must be > 0");
   g_wait_limit_ns = ns;

@@ -478,6 +478,16 @@ marble_status_t marble_set_wait_limit_ns(uint64_t ns);
 marble_status_t marble_set_side_streams(int32_t n);
 
 /*
+ * Give back to the device the memory the library keeps for reuse on the current device:
+ * the dS^T scratch buffers that destroyed plans left for later plans, and the unused part
+ * of the library's memory pool (which otherwise keeps freed blocks for later allocations).
+ * Memory of plans that are still alive is not touched.  Waits for the library's teardown
+ * stream, so that every free queued by marble_plan_destroy has happened; queues no work on
+ * any other stream.  Errors: CUDA.
+ */
+marble_status_t marble_release_memory(void);
+
+/*
  * Per-kernel device timing, a measurement hook (off by default).  While it is on, every
  * marble_attn_step(s) / marble_attn_bwd(_steps) call records CUDA events, on the stream each
  * kernel runs on, before its first and after its last launch of that kernel, and counts the

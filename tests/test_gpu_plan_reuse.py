@@ -56,3 +56,23 @@ def test_back_to_back_plans_reuse_the_scratch_in_stream_order():
         for g, g0 in zip(got, ref):
             torch.testing.assert_close(g, g0, rtol=1e-6, atol=1e-6)
     assert free[1] >= free[0], (free, "device memory grew over back-to-back plans")
+
+
+def test_release_memory_gives_back_the_kept_scratch():
+    """marble_release_memory returns the scratch a destroyed plan left for later plans, and
+    the pool's unused blocks, to the device."""
+    cfg = wl.mini_config(2, n=8192, hq=8)
+    tr = wl.config_tracks(2, cfg.n)
+    q, k, v, do = wl.make_qkvdo(cfg.n, cfg.hq, cfg.hkv, cfg.d, device="cuda", seed=6)
+    _step(cfg, tr, q, k, v, do)  # warms torch's own allocator for the same tensors
+    torch.cuda.synchronize()
+    M.release_memory()
+    free0 = torch.cuda.mem_get_info()[0]
+    _step(cfg, tr, q, k, v, do)  # the plan and its scratch come from the pool again
+    torch.cuda.synchronize()
+    free1 = torch.cuda.mem_get_info()[0]
+    assert free1 < free0, (free0, free1)
+    M.release_memory()
+    free2 = torch.cuda.mem_get_info()[0]
+    assert free2 > free1, (free1, free2)
+    assert free2 >= free0 - (64 << 20), (free0, free2)
